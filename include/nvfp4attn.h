@@ -1,0 +1,187 @@
+/*
+ * nvfp4attn.h — C ABI of the GB300 (sm_103a) NVFP4 fake-quantized attention library.
+ *
+ * What the library computes
+ * -------------------------
+ * NVFP4 fake quantization (FastVideo "nvfp4_qad.py", module docstring and
+ * weight_global_sf / nvfp4_gemm; "vsqa-preview-1.3b metadata.json",
+ * attention.precision: group_size 16, NVFP4 E2M1 values, FP8 E4M3FN scales):
+ * every block of 16 contiguous elements gets the scale s = E4M3(amax*gsf/6)
+ * (round to nearest even, saturating at 448), every element the code
+ * E2M1(|x|*gsf/s) on {0,.5,1,1.5,2,3,4,6} (nearest even, saturating at 6), and
+ * the fake-quantized value is sign(x)*code*s/gsf.  gsf is the global scale: 1
+ * ("unit") or 448*6/amax(X) ("static").  Both roundings are decided on IEEE
+ * fp32 values of amax*gsf/6 and |x|*gsf/s, each product and quotient rounded to
+ * nearest even; with unit gsf and bf16 input these decisions are exact.
+ *
+ * Attention training with fake-quantized Q, K, V and P ("attn_qat_train" API
+ * page, source of attn_qat_train(): is_qat, unit global scales for Q/K/V and P,
+ * straight-through backward on the quantized operands, sm_scale default
+ * 1/sqrt(D); "Attn-QAT Training" guide, "Architecture-specific Triton routing":
+ * exact (final) row-max statistics):
+ *   Q~,K~,V~ = fq16 along D;  S = scale*Q~K~^T;  m = rowmax S;  P = exp(S-m);
+ *   l = sum P (unquantized);  P~ = fq16 along keys (blocks from key 0);
+ *   O = P~V~/l;  LSE = m + ln l.
+ *   Backward (straight-through, m constant): A = P/l; dV = (P~/l)^T dO;
+ *   dP = dO V~^T; delta = rowsum(dO*O); dS = A*(dP-delta); dQ = scale*dS K~;
+ *   dK = scale*dS^T Q~.
+ *
+ * Conventions for every call
+ * --------------------------
+ *  - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *    allocates no memory.  Scratch memory ("workspace") is passed by the
+ *    caller; its size comes from the matching *_workspace() query.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream).  A return of NVQ_OK means every argument was valid and every
+ *    kernel was launched.
+ *  - Arguments are validated on the host before anything is launched.  On an
+ *    error nothing is launched and no output is written.
+ *  - Device-side waits are bounded.  A wait that runs out records a code that
+ *    nvq_device_status() returns (NVQ_ERR_TIMEOUT); the kernel then leaves.
+ *  - bf16 = IEEE bfloat16, f32 = IEEE binary32; all layouts are row-major.
+ *  - Pointers must be 16-byte aligned; row strides (ld_*) are in elements.
+ */
+#ifndef NVFP4ATTN_H
+#define NVFP4ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* nvq_stream_t; /* the same type as cudaStream_t */
+
+typedef enum {
+  NVQ_OK = 0,
+  NVQ_ERR_INVALID = 1,     /* null or misaligned pointer, bad size or stride, scale <= 0 or not finite */
+  NVQ_ERR_UNSUPPORTED = 2, /* valid but not supported: D not in {64,128}; causal with Nq != Nkv */
+  NVQ_ERR_WORKSPACE = 3,   /* workspace pointer NULL or smaller than the *_workspace() size */
+  NVQ_ERR_CUDA = 4,        /* a CUDA runtime/driver call or a launch failed */
+  NVQ_ERR_TIMEOUT = 5      /* a bounded device-side wait ran out (see nvq_device_status) */
+} nvq_status;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* nvq_status_string(int status);
+
+/* Library ABI version: (major << 16) | minor. */
+int nvq_version(void);
+
+/*
+ * Synchronizes `stream`, then returns and clears the device error word that
+ * bounded waits set on the current device: NVQ_OK or NVQ_ERR_TIMEOUT (or
+ * NVQ_ERR_CUDA if the synchronization itself failed).
+ */
+nvq_status nvq_device_status(nvq_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* NVFP4 quantizer                                                          */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Static global scale ("nvfp4_qad.py", weight_global_sf):
+ *   *global_sf = fp32(2688 / max(amax(|x|), 1e-12)), amax over the finite bf16
+ *   matrix x [rows, cols] with row stride ld_x (elements).
+ * global_sf: device pointer to one f32 (written; used as scratch while the
+ * amax is reduced).  rows, cols >= 1; ld_x >= cols; ld_x % 8 == 0.
+ */
+nvq_status nvfp4_global_sf(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
+                           float* global_sf, nvq_stream_t stream);
+
+/*
+ * NVFP4 fake quantization of a bf16 matrix (the standalone quantizer).
+ *   x         bf16 [rows, cols], row stride ld_x; cols % 16 == 0, ld_x % 8 == 0
+ *   global_sf device pointer to one f32 static global scale, or NULL for the
+ *             unit scale 1.0
+ *   out       bf16 [rows, cols], row stride ld_out (may alias x when
+ *             ld_out == ld_x): sign(x)*code*s/gsf rounded to bf16 (exact for
+ *             unit gsf)
+ *   scales    uint8 [rows, cols/16], row stride ld_scales (bytes): the E4M3FN
+ *             bit pattern of each block scale s; may be NULL (not written)
+ * Blocks are the 16-element groups [16t, 16t+16) of each row.
+ */
+nvq_status nvfp4_fake_quant(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
+                            const float* global_sf, void* out, int64_t ld_out,
+                            uint8_t* scales, int64_t ld_scales, nvq_stream_t stream);
+
+/*
+ * Same quantizer, packed codes instead of dequantized values.
+ *   codes   uint8 [rows, cols/2], row stride ld_codes (bytes, % 8 == 0): two
+ *           4-bit codes per byte, element 2i in the low nibble; code =
+ *           sign << 3 | m, m the E2M1 magnitude index 0..7 (values
+ *           0,.5,1,1.5,2,3,4,6); the sign of a zero code is the sign bit of x
+ *   scales  as in nvfp4_fake_quant (required here)
+ */
+nvq_status nvfp4_quantize_codes(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
+                                const float* global_sf, uint8_t* codes, int64_t ld_codes,
+                                uint8_t* scales, int64_t ld_scales, nvq_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Attention (AttentionImpl(num_heads, head_size, softmax_scale, causal))   */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Forward.
+ *   q       bf16 [B, Nq, H, D] contiguous ("BLHD", the layout attn_qat_train()
+ *           receives)
+ *   k, v    bf16 [B, Nkv, H, D] contiguous
+ *   D       64 or 128 (else NVQ_ERR_UNSUPPORTED); B, H, Nq, Nkv >= 1
+ *   scale   softmax scale (> 0, finite); callers wanting the default pass
+ *           1/sqrt(D)
+ *   causal  0 or 1; causal needs Nq == Nkv (top-left aligned), else
+ *           NVQ_ERR_UNSUPPORTED
+ *   o       bf16 [B, Nq, H, D] contiguous (written)
+ *   stats   f32 [B, H, 2, Nq] (written): stats[b][h][0][i] = LSE_i (natural
+ *           log), stats[b][h][1][i] = m_i (row max of scale*S).  The backward
+ *           needs m because P~ is not shift invariant.
+ *   ws      device workspace of at least attn_qat_fwd_workspace(...) bytes,
+ *           256-byte aligned; contents on entry do not matter
+ */
+size_t attn_qat_fwd_workspace(int B, int Nq, int Nkv, int H, int D);
+nvq_status attn_qat_fwd(const void* q, const void* k, const void* v,
+                        int B, int Nq, int Nkv, int H, int D, float scale, int causal,
+                        void* o, float* stats, void* ws, size_t ws_bytes, nvq_stream_t stream);
+
+/*
+ * Straight-through backward.
+ *   q, k, v, D, scale, causal  as in the forward (same values)
+ *   o       bf16 [B, Nq, H, D]: the forward output (delta = rowsum(dO*o))
+ *   stats   f32 [B, H, 2, Nq]: the forward's stats
+ *   dout    bf16 [B, Nq, H, D]: dL/dO
+ *   dq      bf16 [B, Nq, H, D]; dk, dv bf16 [B, Nkv, H, D] (written)
+ *   ws      device workspace of at least attn_qat_bwd_workspace(...) bytes,
+ *           256-byte aligned; contents on entry do not matter
+ */
+size_t attn_qat_bwd_workspace(int B, int Nq, int Nkv, int H, int D);
+nvq_status attn_qat_bwd(const void* q, const void* k, const void* v, const void* o,
+                        const float* stats, const void* dout, void* dq, void* dk, void* dv,
+                        int B, int Nq, int Nkv, int H, int D, float scale, int causal,
+                        void* ws, size_t ws_bytes, nvq_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Self-tests of the hardware encodings the kernels rely on (no paper       */
+/* counterpart; used by the GPU tests)                                      */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * One 128 x N x K tcgen05 BF16 MMA through shared-memory descriptors, the same
+ * encodings the attention kernels use.  a: bf16 [128, K] if a_mn == 0 (K-major)
+ * or [K, 128] if a_mn == 1; b: bf16 [N, K] if b_mn == 0 or [K, N] if b_mn == 1;
+ * c: f32 [128, N] = A * B^T (as [128,K] x [K,N]).  N in {64,128}, K in {64,128}.
+ */
+nvq_status nvq_selftest_umma(const void* a, const void* b, float* c, int N, int K,
+                             int a_mn, int b_mn, nvq_stream_t stream);
+
+/*
+ * Launches one block that waits on a barrier nothing arrives on, with a wait
+ * limit of `limit_ns` nanoseconds (1..1e9).  The wait must run out and record
+ * NVQ_ERR_TIMEOUT for nvq_device_status(); nothing hangs.
+ */
+nvq_status nvq_selftest_timeout(int64_t limit_ns, nvq_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4ATTN_H */

@@ -1,0 +1,87 @@
+"""ctypes loader of ``libnvfp4attn.so``: the C ABI of include/nvfp4attn.h, same names.
+
+Loading fails loudly (``NvqLibraryError``) when the library is missing: there is
+no fallback implementation of any entry point.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libnvfp4attn.so")
+
+c_void_p = ctypes.c_void_p
+c_int = ctypes.c_int
+c_int64 = ctypes.c_int64
+c_size_t = ctypes.c_size_t
+c_float = ctypes.c_float
+
+# name -> (restype, argtypes); mirrors include/nvfp4attn.h
+SIGNATURES = {
+    "nvq_status_string": (ctypes.c_char_p, [c_int]),
+    "nvq_version": (c_int, []),
+    "nvq_device_status": (c_int, [c_void_p]),
+    "nvfp4_global_sf": (c_int, [c_void_p, c_int64, c_int64, c_int64, c_void_p, c_void_p]),
+    "nvfp4_fake_quant": (c_int, [c_void_p, c_int64, c_int64, c_int64, c_void_p, c_void_p, c_int64,
+                                 c_void_p, c_int64, c_void_p]),
+    "nvfp4_quantize_codes": (c_int, [c_void_p, c_int64, c_int64, c_int64, c_void_p, c_void_p,
+                                     c_int64, c_void_p, c_int64, c_void_p]),
+    "attn_qat_fwd_workspace": (c_size_t, [c_int, c_int, c_int, c_int, c_int]),
+    "attn_qat_fwd": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int,
+                             c_float, c_int, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
+    "attn_qat_bwd_workspace": (c_size_t, [c_int, c_int, c_int, c_int, c_int]),
+    "attn_qat_bwd": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                             c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_float, c_int,
+                             c_void_p, c_size_t, c_void_p]),
+    "nvq_selftest_umma": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int,
+                                  c_void_p]),
+    "nvq_selftest_timeout": (c_int, [c_int64, c_void_p]),
+}
+
+STATUS = {0: "NVQ_OK", 1: "NVQ_ERR_INVALID", 2: "NVQ_ERR_UNSUPPORTED", 3: "NVQ_ERR_WORKSPACE",
+          4: "NVQ_ERR_CUDA", 5: "NVQ_ERR_TIMEOUT"}
+
+
+class NvqLibraryError(RuntimeError):
+    """libnvfp4attn.so is missing or does not export the C ABI."""
+
+
+class NvqError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} returned {STATUS.get(status, status)}")
+        self.status = status
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """The loaded library (built by ``__graft_entry__.build()``)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(path):
+                raise NvqLibraryError(
+                    f"{path} not found: build it with "
+                    "`python -c 'import __graft_entry__ as g; g.build()'`")
+            lib = ctypes.CDLL(path)
+            for name, (res, args) in SIGNATURES.items():
+                try:
+                    fn = getattr(lib, name)
+                except AttributeError as e:
+                    raise NvqLibraryError(f"{path} does not export {name}") from e
+                fn.restype = res
+                fn.argtypes = args
+            _lib = lib
+        return _lib
+
+
+def call(name: str, *args) -> int:
+    """Call an entry point returning nvq_status; raise NvqError unless NVQ_OK."""
+    st = getattr(load(), name)(*args)
+    if st != 0:
+        raise NvqError(name, st)
+    return st

@@ -1,0 +1,207 @@
+"""PyTorch-facing binding of the C ABI (argument marshalling only).
+
+Every function takes CUDA tensors, checks dtype/layout/device, allocates the
+outputs and the workspace the caller did not pass, and calls the entry point
+of the same name on the current CUDA stream.  All computation happens in the
+library's kernels; there is no CPU or PyTorch fallback.
+
+``AttnQAT`` mirrors the pages' ``AttentionImpl(num_heads, head_size,
+softmax_scale, causal).forward(q, k, v)`` ("attn_qat_train" API page,
+``AttnQatTrainImpl``): q, k, v in [B, L, H, D] layout, dropout rejected,
+softmax_scale None meaning 1/sqrt(D).
+"""
+from __future__ import annotations
+
+import math
+
+import torch
+
+from . import _lib
+
+BF16 = torch.bfloat16
+
+
+def _stream_ptr(t: torch.Tensor):
+    return torch.cuda.current_stream(t.device).cuda_stream
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _check(t: torch.Tensor, name: str, dtype=BF16):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def _check_bnhd(t, name, shape=None):
+    _check(t, name)
+    if t.dim() != 4 or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous [B, N, H, D] tensor")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def _rows_ld(x: torch.Tensor):
+    if x.dim() != 2 or x.stride(1) != 1:
+        raise ValueError("x must be a 2-D tensor with unit column stride")
+    return x.shape[0], x.shape[1], x.stride(0)
+
+
+# ------------------------------------------------------------------ quantizer
+
+def nvfp4_global_sf(x: torch.Tensor, out: torch.Tensor | None = None) -> torch.Tensor:
+    """fp32 scalar tensor 448*6/max(amax(|x|), 1e-12) computed on the device."""
+    _check(x, "x")
+    rows, cols, ld = _rows_ld(x)
+    if out is None:
+        out = torch.empty((), dtype=torch.float32, device=x.device)
+    _lib.call("nvfp4_global_sf", _ptr(x), rows, cols, ld, _ptr(out), _stream_ptr(x))
+    return out
+
+
+def nvfp4_fake_quant(x: torch.Tensor, global_sf: torch.Tensor | None = None,
+                     out: torch.Tensor | None = None, scales: torch.Tensor | None = None,
+                     want_scales: bool = True):
+    """NVFP4 fake quantization of a bf16 [rows, cols] matrix, cols % 16 == 0.
+
+    Returns (out bf16 [rows, cols], scales uint8 [rows, cols/16] E4M3FN bytes or
+    None).  ``global_sf`` is a device fp32 scalar or None (unit scale).
+    """
+    _check(x, "x")
+    rows, cols, ld = _rows_ld(x)
+    if out is None:
+        out = torch.empty((rows, cols), dtype=BF16, device=x.device)
+    _check(out, "out")
+    if scales is None and want_scales:
+        scales = torch.empty((rows, cols // 16), dtype=torch.uint8, device=x.device)
+    if global_sf is not None:
+        _check(global_sf, "global_sf", torch.float32)
+    _lib.call("nvfp4_fake_quant", _ptr(x), rows, cols, ld, _ptr(global_sf), _ptr(out),
+              out.stride(0), _ptr(scales), 0 if scales is None else scales.stride(0),
+              _stream_ptr(x))
+    return out, scales
+
+
+def nvfp4_quantize_codes(x: torch.Tensor, global_sf: torch.Tensor | None = None,
+                         codes: torch.Tensor | None = None, scales: torch.Tensor | None = None):
+    """Packed NVFP4 codes (uint8 [rows, cols/2], element 2i in the low nibble) and
+    E4M3FN scale bytes (uint8 [rows, cols/16])."""
+    _check(x, "x")
+    rows, cols, ld = _rows_ld(x)
+    if codes is None:
+        codes = torch.empty((rows, cols // 2), dtype=torch.uint8, device=x.device)
+    if scales is None:
+        scales = torch.empty((rows, cols // 16), dtype=torch.uint8, device=x.device)
+    if global_sf is not None:
+        _check(global_sf, "global_sf", torch.float32)
+    _lib.call("nvfp4_quantize_codes", _ptr(x), rows, cols, ld, _ptr(global_sf), _ptr(codes),
+              codes.stride(0), _ptr(scales), scales.stride(0), _stream_ptr(x))
+    return codes, scales
+
+
+# ------------------------------------------------------------------ attention
+
+def default_scale(d: int) -> float:
+    """sm_scale default of attn_qat_train(): 1/sqrt(D)."""
+    return 1.0 / math.sqrt(d)
+
+
+def attn_qat_fwd_workspace(b, nq, nkv, h, d) -> int:
+    return int(_lib.load().attn_qat_fwd_workspace(b, nq, nkv, h, d))
+
+
+def attn_qat_bwd_workspace(b, nq, nkv, h, d) -> int:
+    return int(_lib.load().attn_qat_bwd_workspace(b, nq, nkv, h, d))
+
+
+def _workspace(nbytes: int, device, ws: torch.Tensor | None) -> torch.Tensor:
+    if ws is None or ws.numel() * ws.element_size() < nbytes:
+        ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+    return ws
+
+
+def attn_qat_fwd(q, k, v, scale=None, causal=False, o=None, stats=None, workspace=None):
+    """Forward: returns (o bf16 [B, Nq, H, D], stats fp32 [B, H, 2, Nq] = (LSE, m))."""
+    _check_bnhd(q, "q")
+    b, nq, h, d = q.shape
+    nkv = k.shape[1]
+    _check_bnhd(k, "k", (b, nkv, h, d))
+    _check_bnhd(v, "v", (b, nkv, h, d))
+    scale = default_scale(d) if scale is None or (isinstance(scale, float) and math.isnan(scale)) \
+        else float(scale)
+    if o is None:
+        o = torch.empty_like(q)
+    if stats is None:
+        stats = torch.empty((b, h, 2, nq), dtype=torch.float32, device=q.device)
+    ws = _workspace(attn_qat_fwd_workspace(b, nq, nkv, h, d), q.device, workspace)
+    _lib.call("attn_qat_fwd", _ptr(q), _ptr(k), _ptr(v), b, nq, nkv, h, d, scale,
+              int(bool(causal)), _ptr(o), _ptr(stats), _ptr(ws), ws.numel() * ws.element_size(),
+              _stream_ptr(q))
+    return o, stats
+
+
+def attn_qat_bwd(q, k, v, o, stats, do, scale=None, causal=False, dq=None, dk=None, dv=None,
+                 workspace=None):
+    """Straight-through backward: returns (dq, dk, dv), bf16, shaped like q, k, v."""
+    _check_bnhd(q, "q")
+    b, nq, h, d = q.shape
+    nkv = k.shape[1]
+    _check_bnhd(k, "k", (b, nkv, h, d))
+    _check_bnhd(v, "v", (b, nkv, h, d))
+    _check_bnhd(o, "o", q.shape)
+    _check_bnhd(do, "do", q.shape)
+    _check(stats, "stats", torch.float32)
+    scale = default_scale(d) if scale is None else float(scale)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    ws = _workspace(attn_qat_bwd_workspace(b, nq, nkv, h, d), q.device, workspace)
+    _lib.call("attn_qat_bwd", _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(stats), _ptr(do),
+              _ptr(dq), _ptr(dk), _ptr(dv), b, nq, nkv, h, d, scale, int(bool(causal)),
+              _ptr(ws), ws.numel() * ws.element_size(), _stream_ptr(q))
+    return dq, dk, dv
+
+
+def device_status(device=None) -> int:
+    """Synchronize the current stream and return (and clear) the device error word."""
+    s = torch.cuda.current_stream(device).cuda_stream
+    return int(_lib.load().nvq_device_status(s))
+
+
+class AttnQATFunction(torch.autograd.Function):
+    """O = attention with NVFP4 fake-quantized Q, K, V, P; straight-through backward."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, scale, causal):
+        o, stats = attn_qat_fwd(q, k, v, scale, causal)
+        ctx.save_for_backward(q, k, v, o, stats)
+        ctx.scale, ctx.causal = scale, causal
+        return o
+
+    @staticmethod
+    def backward(ctx, do):
+        q, k, v, o, stats = ctx.saved_tensors
+        dq, dk, dv = attn_qat_bwd(q, k, v, o, stats, do.contiguous(), ctx.scale, ctx.causal)
+        return dq, dk, dv, None, None
+
+
+class AttnQAT(torch.nn.Module):
+    """``AttentionImpl(num_heads, head_size, softmax_scale, causal)`` with ``forward(q, k, v)``."""
+
+    def __init__(self, num_heads: int, head_size: int, softmax_scale: float | None = None,
+                 causal: bool = False, dropout_p: float = 0.0):
+        super().__init__()
+        if dropout_p > 0:
+            raise NotImplementedError(
+                f"NVFP4 Attn-QAT attention applies no dropout (got dropout_p={dropout_p})")
+        if head_size not in (64, 128):
+            raise ValueError(f"head_size must be 64 or 128, got {head_size}")
+        self.num_heads, self.head_size = num_heads, head_size
+        self.softmax_scale = default_scale(head_size) if softmax_scale is None else softmax_scale
+        self.causal = causal
+
+    def forward(self, q, k, v):
+        return AttnQATFunction.apply(q, k, v, self.softmax_scale, self.causal)

@@ -1,0 +1,329 @@
+// C ABI of the library (declared in include/nvfp4attn.h): argument validation,
+// workspace carving, TMA descriptor creation and kernel launches.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "nvfp4attn.h"
+#include "nvq_internal.h"
+
+namespace nvq {
+
+// Device error word (see nvq_device_status).  One copy per device that loads
+// the library; kernels receive its address as an argument.
+static __device__ int g_error_word = 0;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+int* g_err_ptr[kMaxDevices] = {};
+
+// Address of this device's error word (looked up once per device, with that
+// device current).
+int* error_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_err_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
+    g_err_ptr[dev] = static_cast<int*>(p);
+  }
+  return g_err_ptr[dev];
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+nvq_status from_cuda(cudaError_t e) { return e == cudaSuccess ? NVQ_OK : NVQ_ERR_CUDA; }
+
+}  // namespace
+
+bool make_bnhd_map(CUtensorMap* map, const void* base, int B, int N, int H, int D, bool f16) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(N),
+                              static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(B)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(H) * D * 2,
+                                 static_cast<cuuint64_t>(D) * 2,
+                                 static_cast<cuuint64_t>(N) * H * D * 2};
+  const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(kTile), 1, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r =
+      fn(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+         const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool make_2d_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows), 1, 1};
+  const cuuint64_t rs = static_cast<cuuint64_t>(cols) * 2;
+  const cuuint64_t strides[3] = {rs, rs * rows, rs * rows};
+  const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(box_rows), 1, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+namespace {
+
+nvq_status check_attn(int B, int Nq, int Nkv, int H, int D, float scale, int causal) {
+  if (B < 1 || Nq < 1 || Nkv < 1 || H < 1) return NVQ_ERR_INVALID;
+  if (!(std::isfinite(scale) && scale > 0.f)) return NVQ_ERR_INVALID;
+  if (causal != 0 && causal != 1) return NVQ_ERR_INVALID;
+  if (D != 64 && D != 128) return NVQ_ERR_UNSUPPORTED;
+  if (causal && Nq != Nkv) return NVQ_ERR_UNSUPPORTED;
+  // grid dimensions y and z are limited to 65535
+  if (B > 65535 || H > 65535) return NVQ_ERR_UNSUPPORTED;
+  return NVQ_OK;
+}
+
+size_t bytes_bnhd(int B, int N, int H, int D, size_t elem) {
+  return static_cast<size_t>(B) * N * H * D * elem;
+}
+
+struct FwdWs {
+  size_t q, k, v, total;
+};
+FwdWs fwd_ws(int B, int Nq, int Nkv, int H, int D) {
+  FwdWs w;
+  w.q = 0;
+  w.k = round_up(w.q + bytes_bnhd(B, Nq, H, D, 2), 256);
+  w.v = round_up(w.k + bytes_bnhd(B, Nkv, H, D, 2), 256);
+  w.total = round_up(w.v + bytes_bnhd(B, Nkv, H, D, 2), 256);
+  return w;
+}
+
+struct BwdWs {
+  size_t q, k, v, dq, delta, total;
+};
+BwdWs bwd_ws(int B, int Nq, int Nkv, int H, int D) {
+  BwdWs w;
+  w.q = 0;
+  w.k = round_up(w.q + bytes_bnhd(B, Nq, H, D, 2), 256);
+  w.v = round_up(w.k + bytes_bnhd(B, Nkv, H, D, 2), 256);
+  w.dq = round_up(w.v + bytes_bnhd(B, Nkv, H, D, 2), 256);
+  w.delta = round_up(w.dq + bytes_bnhd(B, Nq, H, D, 4), 256);
+  w.total = round_up(w.delta + static_cast<size_t>(B) * H * Nq * 4, 256);
+  return w;
+}
+
+nvq_status check_quant(const void* x, int64_t rows, int64_t cols, int64_t ld_x) {
+  if (x == nullptr || !aligned16(x)) return NVQ_ERR_INVALID;
+  if (rows < 1 || cols < 16 || cols % 16 != 0) return NVQ_ERR_INVALID;
+  if (ld_x < cols || ld_x % 8 != 0) return NVQ_ERR_INVALID;
+  return NVQ_OK;
+}
+
+}  // namespace
+}  // namespace nvq
+
+using namespace nvq;
+
+extern "C" {
+
+const char* nvq_status_string(int status) {
+  switch (status) {
+    case NVQ_OK: return "NVQ_OK";
+    case NVQ_ERR_INVALID: return "NVQ_ERR_INVALID";
+    case NVQ_ERR_UNSUPPORTED: return "NVQ_ERR_UNSUPPORTED";
+    case NVQ_ERR_WORKSPACE: return "NVQ_ERR_WORKSPACE";
+    case NVQ_ERR_CUDA: return "NVQ_ERR_CUDA";
+    case NVQ_ERR_TIMEOUT: return "NVQ_ERR_TIMEOUT";
+    default: return "NVQ_ERR_UNKNOWN";
+  }
+}
+
+int nvq_version(void) { return (1 << 16) | 0; }
+
+nvq_status nvq_device_status(nvq_stream_t stream) {
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return NVQ_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_error_word, sizeof(int)) != cudaSuccess) return NVQ_ERR_CUDA;
+  if (v != 0) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_error_word, &zero, sizeof(int)) != cudaSuccess) return NVQ_ERR_CUDA;
+    return NVQ_ERR_TIMEOUT;
+  }
+  return NVQ_OK;
+}
+
+nvq_status nvfp4_global_sf(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
+                           float* global_sf, nvq_stream_t stream) {
+  if (x == nullptr || !aligned16(x) || global_sf == nullptr ||
+      (reinterpret_cast<uintptr_t>(global_sf) & 3u) != 0)
+    return NVQ_ERR_INVALID;
+  if (rows < 1 || cols < 1 || ld_x < cols || ld_x % 8 != 0) return NVQ_ERR_INVALID;
+  return from_cuda(launch_global_sf(x, rows, cols, ld_x, global_sf, stream));
+}
+
+nvq_status nvfp4_fake_quant(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
+                            const float* global_sf, void* out, int64_t ld_out, uint8_t* scales,
+                            int64_t ld_scales, nvq_stream_t stream) {
+  nvq_status st = check_quant(x, rows, cols, ld_x);
+  if (st != NVQ_OK) return st;
+  if (out == nullptr || !aligned16(out) || ld_out < cols || ld_out % 8 != 0)
+    return NVQ_ERR_INVALID;
+  if (out == x && ld_out != ld_x) return NVQ_ERR_INVALID;
+  if (scales != nullptr && ld_scales < cols / 16) return NVQ_ERR_INVALID;
+  if (global_sf != nullptr && (reinterpret_cast<uintptr_t>(global_sf) & 3u) != 0)
+    return NVQ_ERR_INVALID;
+  const int mode = global_sf == nullptr ? kUnitBf16 : kStaticBf16;
+  return from_cuda(launch_fake_quant(x, rows, cols, ld_x, global_sf, mode, out, ld_out, scales,
+                                     ld_scales, nullptr, 0, stream));
+}
+
+nvq_status nvfp4_quantize_codes(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
+                                const float* global_sf, uint8_t* codes, int64_t ld_codes,
+                                uint8_t* scales, int64_t ld_scales, nvq_stream_t stream) {
+  nvq_status st = check_quant(x, rows, cols, ld_x);
+  if (st != NVQ_OK) return st;
+  if (codes == nullptr || !aligned16(codes) || ld_codes < cols / 2 || ld_codes % 8 != 0)
+    return NVQ_ERR_INVALID;
+  if (scales == nullptr || ld_scales < cols / 16) return NVQ_ERR_INVALID;
+  if (global_sf != nullptr && (reinterpret_cast<uintptr_t>(global_sf) & 3u) != 0)
+    return NVQ_ERR_INVALID;
+  const int mode = global_sf == nullptr ? kUnitBf16 : kStaticBf16;
+  return from_cuda(launch_fake_quant(x, rows, cols, ld_x, global_sf, mode, nullptr, 0, scales,
+                                     ld_scales, codes, ld_codes, stream));
+}
+
+size_t attn_qat_fwd_workspace(int B, int Nq, int Nkv, int H, int D) {
+  if (B < 1 || Nq < 1 || Nkv < 1 || H < 1 || D < 1) return 0;
+  return fwd_ws(B, Nq, Nkv, H, D).total;
+}
+
+size_t attn_qat_bwd_workspace(int B, int Nq, int Nkv, int H, int D) {
+  if (B < 1 || Nq < 1 || Nkv < 1 || H < 1 || D < 1) return 0;
+  return bwd_ws(B, Nq, Nkv, H, D).total;
+}
+
+nvq_status attn_qat_fwd(const void* q, const void* k, const void* v, int B, int Nq, int Nkv,
+                        int H, int D, float scale, int causal, void* o, float* stats, void* ws,
+                        size_t ws_bytes, nvq_stream_t stream) {
+  nvq_status st = check_attn(B, Nq, Nkv, H, D, scale, causal);
+  if (st != NVQ_OK) return st;
+  if (!q || !k || !v || !o || !stats || !aligned16(q) || !aligned16(k) || !aligned16(v) ||
+      !aligned16(o) || !aligned16(stats))
+    return NVQ_ERR_INVALID;
+  const FwdWs w = fwd_ws(B, Nq, Nkv, H, D);
+  if (ws == nullptr || ws_bytes < w.total || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
+    return NVQ_ERR_WORKSPACE;
+  int* err = error_word();
+  if (err == nullptr) return NVQ_ERR_CUDA;
+  uint8_t* wb = static_cast<uint8_t*>(ws);
+  void* qt = wb + w.q;
+  void* kt = wb + w.k;
+  void* vt = wb + w.v;
+  CUtensorMap mq, mk, mv;
+  if (!make_bnhd_map(&mq, qt, B, Nq, H, D, false) ||
+      !make_bnhd_map(&mk, kt, B, Nkv, H, D, false) || !make_bnhd_map(&mv, vt, B, Nkv, H, D, true))
+    return NVQ_ERR_CUDA;
+  const int64_t rq = static_cast<int64_t>(B) * Nq * H, rk = static_cast<int64_t>(B) * Nkv * H;
+  cudaError_t e =
+      launch_fake_quant(q, rq, D, D, nullptr, kUnitBf16, qt, D, nullptr, 0, nullptr, 0, stream);
+  if (e == cudaSuccess)
+    e = launch_fake_quant(k, rk, D, D, nullptr, kUnitBf16, kt, D, nullptr, 0, nullptr, 0, stream);
+  if (e == cudaSuccess)
+    e = launch_fake_quant(v, rk, D, D, nullptr, kUnitF16, vt, D, nullptr, 0, nullptr, 0, stream);
+  if (e != cudaSuccess) return NVQ_ERR_CUDA;
+  const AttnShape s{B, Nq, Nkv, H, D, scale, causal};
+  return from_cuda(launch_attn_fwd(s, mq, mk, mv, o, stats, err, stream));
+}
+
+nvq_status attn_qat_bwd(const void* q, const void* k, const void* v, const void* o,
+                        const float* stats, const void* dout, void* dq, void* dk, void* dv, int B,
+                        int Nq, int Nkv, int H, int D, float scale, int causal, void* ws,
+                        size_t ws_bytes, nvq_stream_t stream) {
+  nvq_status st = check_attn(B, Nq, Nkv, H, D, scale, causal);
+  if (st != NVQ_OK) return st;
+  const void* ptrs[] = {q, k, v, o, stats, dout, dq, dk, dv};
+  for (const void* p : ptrs)
+    if (p == nullptr || !aligned16(p)) return NVQ_ERR_INVALID;
+  const BwdWs w = bwd_ws(B, Nq, Nkv, H, D);
+  if (ws == nullptr || ws_bytes < w.total || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
+    return NVQ_ERR_WORKSPACE;
+  int* err = error_word();
+  if (err == nullptr) return NVQ_ERR_CUDA;
+  uint8_t* wb = static_cast<uint8_t*>(ws);
+  void* qt = wb + w.q;
+  void* kt = wb + w.k;
+  void* vt = wb + w.v;
+  float* dq_acc = reinterpret_cast<float*>(wb + w.dq);
+  float* delta = reinterpret_cast<float*>(wb + w.delta);
+  CUtensorMap mq, mk, mv, mdo;
+  if (!make_bnhd_map(&mq, qt, B, Nq, H, D, false) ||
+      !make_bnhd_map(&mk, kt, B, Nkv, H, D, false) ||
+      !make_bnhd_map(&mv, vt, B, Nkv, H, D, false) ||
+      !make_bnhd_map(&mdo, dout, B, Nq, H, D, false))
+    return NVQ_ERR_CUDA;
+  const int64_t rq = static_cast<int64_t>(B) * Nq * H, rk = static_cast<int64_t>(B) * Nkv * H;
+  const AttnShape s{B, Nq, Nkv, H, D, scale, causal};
+  cudaError_t e =
+      launch_fake_quant(q, rq, D, D, nullptr, kUnitBf16, qt, D, nullptr, 0, nullptr, 0, stream);
+  if (e == cudaSuccess)
+    e = launch_fake_quant(k, rk, D, D, nullptr, kUnitBf16, kt, D, nullptr, 0, nullptr, 0, stream);
+  if (e == cudaSuccess)
+    e = launch_fake_quant(v, rk, D, D, nullptr, kUnitBf16, vt, D, nullptr, 0, nullptr, 0, stream);
+  if (e == cudaSuccess) e = launch_bwd_prep(s, o, dout, delta, dq_acc, stream);
+  if (e == cudaSuccess)
+    e = launch_attn_bwd(s, mq, mk, mv, mdo, stats, delta, dq_acc, dk, dv, err, stream);
+  if (e == cudaSuccess) e = launch_dq_convert(s, dq_acc, dq, stream);
+  return from_cuda(e);
+}
+
+nvq_status nvq_selftest_umma(const void* a, const void* b, float* c, int N, int K, int a_mn,
+                             int b_mn, nvq_stream_t stream) {
+  if (!a || !b || !c || !aligned16(a) || !aligned16(b) || !aligned16(c)) return NVQ_ERR_INVALID;
+  if ((N != 64 && N != 128) || (K != 64 && K != 128) || (a_mn != 0 && a_mn != 1) ||
+      (b_mn != 0 && b_mn != 1))
+    return NVQ_ERR_INVALID;
+  int* err = error_word();
+  if (err == nullptr) return NVQ_ERR_CUDA;
+  CUtensorMap ma, mb;
+  const bool ok = (a_mn ? make_2d_map(&ma, a, K, 128, K) : make_2d_map(&ma, a, 128, K, 128)) &&
+                  (b_mn ? make_2d_map(&mb, b, K, N, K) : make_2d_map(&mb, b, N, K, N));
+  if (!ok) return NVQ_ERR_CUDA;
+  return from_cuda(launch_selftest_umma(ma, mb, c, N, K, a_mn, b_mn, err, stream));
+}
+
+nvq_status nvq_selftest_timeout(int64_t limit_ns, nvq_stream_t stream) {
+  if (limit_ns < 1 || limit_ns > 1000000000) return NVQ_ERR_INVALID;
+  int* err = error_word();
+  if (err == nullptr) return NVQ_ERR_CUDA;
+  return from_cuda(launch_selftest_timeout(limit_ns, err, stream));
+}
+
+}  // extern "C"

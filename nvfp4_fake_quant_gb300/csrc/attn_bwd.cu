@@ -1,0 +1,458 @@
+// Attn-QAT straight-through backward on sm_103a.
+//
+// Kernels, in launch order:
+//   bwd_prep    delta_i = sum_d dO_id * O_id (fp32), zeroes the fp32 dQ accumulator
+//   attn_bwd    one CTA per (128-key tile, head, batch); K~ and V~ stay in shared
+//               memory, the dK and dV accumulators in TMEM; the CTA loops over the
+//               128-query tiles:
+//                 S  = Q~ K~^T, dP = dO V~^T              (BF16 UMMA -> TMEM)
+//                 P  = exp(scale*S - m)                    (m from the forward)
+//                 P~ = fq16(P) per 16 keys                 (bit-identical to the forward)
+//                 A  = P / l,   dS = A * (dP - delta)
+//                 P~/l and dS -> shared memory (bf16)
+//                 dV += (P~/l)^T dO, dK += dS^T Q~, dQ_i = dS K~   (BF16 UMMA)
+//                 dQ_i * scale is added to the fp32 accumulator (vector reductions)
+//               then writes dK * scale and dV (bf16).
+//   dq_convert  fp32 dQ accumulator -> bf16
+// ("attn_qat_train" API page, attn_qat_train(): the backward uses the quantized
+// Q, K, V and the quantized P, with straight-through gradients.)
+//
+// Roles (192 threads, one CTA per SM): warps 0-3 elementwise (thread t = query
+// row t of the tile = TMEM lane t for S/dP/dQ, key row t for dK/dV), warp 4 TMA,
+// warp 5 TMEM allocation and UMMA issue.
+// TMEM columns: [0,128) S then dQ, [128,256) dP, [256,256+D) dV, [384,384+D) dK.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "nvq_internal.h"
+#include "nvq_ptx.cuh"
+#include "nvq_quant.cuh"
+
+namespace nvq {
+
+namespace {
+
+constexpr int kThreads = 192;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr uint32_t kAtomBlock = 128u * 128u;
+
+template <int D>
+struct BwdLayout {
+  static constexpr uint32_t kTileBytes = 128u * D * 2u;
+  static constexpr uint32_t kK = 0;
+  static constexpr uint32_t kV = kK + kTileBytes;
+  static constexpr uint32_t kQ = kV + kTileBytes;
+  static constexpr uint32_t kDO = kQ + kTileBytes;
+  static constexpr uint32_t kPT = kDO + kTileBytes;  // P~/l, [128 q][128 keys] bf16
+  static constexpr uint32_t kDS = kPT + 128u * 128u * 2u;
+  static constexpr uint32_t kBars = kDS + 128u * 128u * 2u;
+  static constexpr uint32_t kNumBars = 9;
+  static constexpr uint32_t kTmemSlot = kBars + kNumBars * 8u;
+  static constexpr uint32_t kAbort = kTmemSlot + 4u;
+  static constexpr uint32_t kUsed = kAbort + 4u;
+  static constexpr uint32_t kAlloc =
+      (kUsed + 1024u) > 150u * 1024u ? (kUsed + 1024u) : 150u * 1024u;
+};
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c),
+               "f"(d)
+               : "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
+                    const float* __restrict__ stats, const float* __restrict__ delta,
+                    float* __restrict__ dq_acc, __nv_bfloat16* __restrict__ dk,
+                    __nv_bfloat16* __restrict__ dv, int Nq, int Nkv, int H, float scale,
+                    int causal, int* __restrict__ err) {
+  using L = BwdLayout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023u) &
+                                             ~static_cast<uintptr_t>(1023u));
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int kt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int k0 = kt * kTile;
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBars);
+  uint64_t* kv_full = bars + 0;
+  uint64_t* qdo_full = bars + 1;
+  uint64_t* qdo_empty = bars + 2;
+  uint64_t* s_full = bars + 3;
+  uint64_t* ds_full = bars + 4;
+  uint64_t* mma2_done = bars + 5;
+  uint64_t* dq_free = bars + 6;
+  uint64_t* dkdv_done = bars + 7;
+  uint64_t* mma_drain = bars + 8;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kAbort);
+
+  const int n_q_all = (Nq + kTile - 1) / kTile;
+  const int i_begin = causal ? kt : 0;  // causal requires Nq == Nkv
+  const int n_iter = n_q_all - i_begin;
+
+  if (threadIdx.x == 0) {
+    *abort = 0;
+    mbar_init(kv_full, 1);
+    mbar_init(qdo_full, 1);
+    mbar_init(qdo_empty, 1);
+    mbar_init(s_full, 1);
+    mbar_init(ds_full, 128);
+    mbar_init(mma2_done, 1);
+    mbar_init(dq_free, 128);
+    mbar_init(dkdv_done, 1);
+    mbar_init(mma_drain, 1);
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 4) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tq);
+      tma_prefetch_desc(&tk);
+      tma_prefetch_desc(&tv);
+      tma_prefetch_desc(&tdo);
+      mbar_arrive_expect_tx(kv_full, 2u * L::kTileBytes);
+#pragma unroll
+      for (int blk = 0; blk < D / 64; ++blk) {
+        tma_load_4d(smem + L::kK + blk * kAtomBlock, &tk, blk * 64, k0, h, b, kv_full);
+        tma_load_4d(smem + L::kV + blk * kAtomBlock, &tv, blk * 64, k0, h, b, kv_full);
+      }
+      int last = -1;
+      bool ok = true;
+      for (int it = 0; it < n_iter; ++it) {
+        if (!(ok = mbar_wait(qdo_empty, (it & 1) ^ 1, abort))) break;
+        const int qrow0 = (i_begin + it) * kTile;
+        mbar_arrive_expect_tx(qdo_full, 2u * L::kTileBytes);
+#pragma unroll
+        for (int blk = 0; blk < D / 64; ++blk) {
+          tma_load_4d(smem + L::kQ + blk * kAtomBlock, &tq, blk * 64, qrow0, h, b, qdo_full);
+          tma_load_4d(smem + L::kDO + blk * kAtomBlock, &tdo, blk * 64, qrow0, h, b, qdo_full);
+        }
+        last = it & 1;
+      }
+      if (!ok) {
+        mbar_wait(kv_full, 0, nullptr, 10000000ull);
+        if (last >= 0) mbar_wait(qdo_full, static_cast<uint32_t>(last), nullptr, 10000000ull);
+      }
+    }
+  } else if (warp == 5) {
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_f16(128, 128, 1, 0, 0);  // S, dP
+      constexpr uint32_t idesc_t = idesc_f16(128, D, 1, 1, 1);    // dV, dK (A, B MN-major)
+      constexpr uint32_t idesc_q = idesc_f16(128, D, 1, 0, 1);    // dQ (A K-major, B MN-major)
+      const uint32_t k_addr = smem_u32(smem + L::kK);
+      const uint32_t v_addr = smem_u32(smem + L::kV);
+      const uint32_t q_addr = smem_u32(smem + L::kQ);
+      const uint32_t do_addr = smem_u32(smem + L::kDO);
+      const uint32_t pt_addr = smem_u32(smem + L::kPT);
+      const uint32_t ds_addr = smem_u32(smem + L::kDS);
+      bool ok = mbar_wait(kv_full, 0, abort);
+      for (int it = 0; it < n_iter && ok; ++it) {
+        if (!(ok = mbar_wait(qdo_full, it & 1, abort))) break;
+        if (it > 0 && !(ok = mbar_wait(dq_free, (it - 1) & 1, abort))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kAtomBlock + (kk & 3) * 32;
+          umma_f16_ss(tmem + 0, sdesc_sw128(q_addr + off, 16, 1024),
+                      sdesc_sw128(k_addr + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kAtomBlock + (kk & 3) * 32;
+          umma_f16_ss(tmem + 128, sdesc_sw128(do_addr + off, 16, 1024),
+                      sdesc_sw128(v_addr + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+        }
+        umma_commit(s_full);
+        if (!(ok = mbar_wait(ds_full, it & 1, abort))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {  // contraction over 128 queries, 16 per UMMA
+          const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
+          umma_f16_ss(tmem + 256, sdesc_sw128(pt_addr + kk * 2048, kAtomBlock, 1024),
+                      sdesc_sw128(do_addr + kk * 2048, kAtomBlock, 1024), idesc_t, acc);
+          umma_f16_ss(tmem + 384, sdesc_sw128(ds_addr + kk * 2048, kAtomBlock, 1024),
+                      sdesc_sw128(q_addr + kk * 2048, kAtomBlock, 1024), idesc_t, acc);
+        }
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {  // contraction over 128 keys
+          const uint32_t aoff = (kk >> 2) * kAtomBlock + (kk & 3) * 32;
+          umma_f16_ss(tmem + 0, sdesc_sw128(ds_addr + aoff, 16, 1024),
+                      sdesc_sw128(k_addr + kk * 2048, kAtomBlock, 1024), idesc_q,
+                      kk > 0 ? 1u : 0u);
+        }
+        umma_commit(mma2_done);
+        umma_commit(qdo_empty);
+      }
+      if (ok) umma_commit(dkdv_done);
+      umma_commit(mma_drain);
+      mbar_wait(mma_drain, 0, nullptr, 10000000ull);
+    }
+  } else {
+    const int t = threadIdx.x;
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const float c1 = scale * kLog2e;
+    uint8_t* pt_smem = smem + L::kPT;
+    uint8_t* ds_smem = smem + L::kDS;
+    const float* lse_g = stats + (static_cast<int64_t>(b) * H + h) * 2 * Nq;
+    const float* m_g = lse_g + Nq;
+    const float* delta_g = delta + (static_cast<int64_t>(b) * H + h) * Nq;
+    bool ok = true;
+    uint32_t rs[32], rd[32];
+    for (int it = 0; it < n_iter && ok; ++it) {
+      const int qi = i_begin + it;
+      const int qrow = qi * kTile + t;
+      const bool row_ok = qrow < Nq;
+      const float m = row_ok ? m_g[qrow] : 0.f;
+      const float lse = row_ok ? lse_g[qrow] : 0.f;
+      const float dl = row_ok ? delta_g[qrow] : 0.f;
+      const float mb = m * kLog2e;
+      const float inv_l = ex2((m - lse) * kLog2e);  // 1 / l
+      const bool edge = !row_ok || (k0 + kTile > Nkv) || (causal && qi == kt) ||
+                        (qi * kTile + kTile > Nq);
+      if (!(ok = mbar_wait(s_full, it & 1, abort))) break;
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        tmem_ld32(tmem + lane_base + c * 32, rs);
+        tmem_ld32(tmem + lane_base + 128 + c * 32, rd);
+        tmem_wait_ld();
+        float p[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          float pv = ex2(fmaf(__uint_as_float(rs[i]), c1, -mb));
+          if (edge) {
+            const int key = k0 + c * 32 + i;
+            if (!(row_ok && key < Nkv && (!causal || key <= qrow))) pv = 0.f;
+          }
+          p[i] = pv;
+        }
+        uint32_t ptw[16], dsw[16];
+#pragma unroll
+        for (int hb = 0; hb < 2; ++hb) {
+          uint32_t q8[8];
+          quant16_p(p + 16 * hb, q8);
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const float lo = f16lo_to_f32(q8[u]) * inv_l;
+            const float hi = f16lo_to_f32(q8[u] >> 16) * inv_l;
+            ptw[8 * hb + u] = pack_bf16(lo, hi);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+          const float a0 = p[2 * u] * inv_l, a1 = p[2 * u + 1] * inv_l;
+          const float d0 = a0 * (__uint_as_float(rd[2 * u]) - dl);
+          const float d1 = a1 * (__uint_as_float(rd[2 * u + 1]) - dl);
+          dsw[u] = pack_bf16(d0, d1);
+        }
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          const uint32_t off = sw128_offset(t, c * 32 + ch * 8, 128);
+          *reinterpret_cast<uint4*>(pt_smem + off) =
+              make_uint4(ptw[4 * ch], ptw[4 * ch + 1], ptw[4 * ch + 2], ptw[4 * ch + 3]);
+          *reinterpret_cast<uint4*>(ds_smem + off) =
+              make_uint4(dsw[4 * ch], dsw[4 * ch + 1], dsw[4 * ch + 2], dsw[4 * ch + 3]);
+        }
+      }
+      tc_fence_before();
+      fence_proxy_async_smem();
+      mbar_arrive(ds_full);
+      if (!(ok = mbar_wait(mma2_done, it & 1, abort))) break;
+      tc_fence_after();
+      float* dqrow = dq_acc + ((static_cast<int64_t>(b) * Nq + qrow) * H + h) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        tmem_ld32(tmem + lane_base + c * 32, rs);
+        tmem_wait_ld();
+        if (row_ok) {
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            red_add_v4(dqrow + c * 32 + 4 * u, __uint_as_float(rs[4 * u]) * scale,
+                       __uint_as_float(rs[4 * u + 1]) * scale,
+                       __uint_as_float(rs[4 * u + 2]) * scale,
+                       __uint_as_float(rs[4 * u + 3]) * scale);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(dq_free);
+    }
+    if (ok && n_iter > 0 && (ok = mbar_wait(dkdv_done, 0, abort))) {
+      tc_fence_after();
+      const int key = k0 + t;
+      const int64_t base = ((static_cast<int64_t>(b) * Nkv + key) * H + h) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        tmem_ld32(tmem + lane_base + 256 + c * 32, rs);
+        tmem_ld32(tmem + lane_base + 384 + c * 32, rd);
+        tmem_wait_ld();
+        if (key < Nkv) {
+          uint32_t wv[16], wk[16];
+#pragma unroll
+          for (int u = 0; u < 16; ++u) {
+            wv[u] = pack_bf16(__uint_as_float(rs[2 * u]), __uint_as_float(rs[2 * u + 1]));
+            wk[u] = pack_bf16(__uint_as_float(rd[2 * u]) * scale,
+                              __uint_as_float(rd[2 * u + 1]) * scale);
+          }
+          uint4* pv = reinterpret_cast<uint4*>(dv + base + c * 32);
+          uint4* pk = reinterpret_cast<uint4*>(dk + base + c * 32);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            pv[u] = make_uint4(wv[4 * u], wv[4 * u + 1], wv[4 * u + 2], wv[4 * u + 3]);
+            pk[u] = make_uint4(wk[4 * u], wk[4 * u + 1], wk[4 * u + 2], wk[4 * u + 3]);
+          }
+        }
+      }
+    } else if (ok && n_iter == 0) {
+      // no query attends this key tile: zero gradients
+      const int key = k0 + t;
+      if (key < Nkv) {
+        const int64_t base = ((static_cast<int64_t>(b) * Nkv + key) * H + h) * D;
+        for (int c = 0; c < D; c += 8) {
+          *reinterpret_cast<uint4*>(dv + base + c) = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(dk + base + c) = make_uint4(0, 0, 0, 0);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  report_abort(abort, err);
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// delta[b,h,i] = sum_d dO[b,i,h,d] * O[b,i,h,d]; zero the dQ accumulator row.
+template <int D>
+__global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __restrict__ o,
+                                                       const __nv_bfloat16* __restrict__ dout,
+                                                       float* __restrict__ delta,
+                                                       float* __restrict__ dq_acc, int B, int Nq,
+                                                       int H) {
+  // 8 threads per (b, i, h) row; each takes D/8 consecutive elements.
+  const int64_t rows = static_cast<int64_t>(B) * Nq * H;
+  const int64_t gt = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t row = gt >> 3;
+  const int part = static_cast<int>(gt & 7);
+  float acc = 0.f;
+  if (row < rows) {
+    constexpr int E = D / 8;
+    const int64_t off = row * D + part * E;
+#pragma unroll
+    for (int c = 0; c < E; c += 8) {
+      const uint4 a = *reinterpret_cast<const uint4*>(o + off + c);
+      const uint4 g = *reinterpret_cast<const uint4*>(dout + off + c);
+      const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, gw[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        acc = fmaf(__uint_as_float(aw[u] << 16), __uint_as_float(gw[u] << 16), acc);
+        acc = fmaf(__uint_as_float(aw[u] & 0xFFFF0000u), __uint_as_float(gw[u] & 0xFFFF0000u),
+                   acc);
+      }
+      float4* z = reinterpret_cast<float4*>(dq_acc + off + c);
+      z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+      z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+  acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 1);
+  acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 2);
+  acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 4);
+  if (row < rows && part == 0) {
+    const int64_t hh = row % H;
+    const int64_t bi = row / H;  // b * Nq + i
+    const int64_t i = bi % Nq;
+    const int64_t bb = bi / Nq;
+    delta[(bb * H + hh) * Nq + i] = acc;
+  }
+}
+
+__global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict__ acc,
+                                                         __nv_bfloat16* __restrict__ dq,
+                                                         int64_t n8) {
+  const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
+       i += step) {
+    const float4 a = reinterpret_cast<const float4*>(acc)[2 * i];
+    const float4 c = reinterpret_cast<const float4*>(acc)[2 * i + 1];
+    reinterpret_cast<uint4*>(dq)[i] = make_uint4(pack_bf16(a.x, a.y), pack_bf16(a.z, a.w),
+                                                 pack_bf16(c.x, c.y), pack_bf16(c.z, c.w));
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_prep(const AttnShape& s, const void* o, const void* dout, float* delta,
+                            float* dq_acc, cudaStream_t stream) {
+  const int64_t rows = static_cast<int64_t>(s.B) * s.Nq * s.H;
+  const int64_t threads = rows * 8;
+  const int grid = static_cast<int>((threads + 255) / 256);
+  const auto* op = static_cast<const __nv_bfloat16*>(o);
+  const auto* gp = static_cast<const __nv_bfloat16*>(dout);
+  if (s.D == 128)
+    bwd_prep_kernel<128><<<grid, 256, 0, stream>>>(op, gp, delta, dq_acc, s.B, s.Nq, s.H);
+  else
+    bwd_prep_kernel<64><<<grid, 256, 0, stream>>>(op, gp, delta, dq_acc, s.B, s.Nq, s.H);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attn_bwd(const AttnShape& s, const CUtensorMap& tq, const CUtensorMap& tk,
+                            const CUtensorMap& tv, const CUtensorMap& tdo, const float* stats,
+                            const float* delta, float* dq_acc, void* dk, void* dv, int* err,
+                            cudaStream_t stream) {
+  const dim3 grid((s.Nkv + kTile - 1) / kTile, s.H, s.B);
+  auto* dkp = static_cast<__nv_bfloat16*>(dk);
+  auto* dvp = static_cast<__nv_bfloat16*>(dv);
+  if (s.D == 128) {
+    using L = BwdLayout<128>;
+    cudaError_t e = cudaFuncSetAttribute(attn_bwd_kernel<128>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+    if (e != cudaSuccess) return e;
+    attn_bwd_kernel<128><<<grid, kThreads, L::kAlloc, stream>>>(
+        tq, tk, tv, tdo, stats, delta, dq_acc, dkp, dvp, s.Nq, s.Nkv, s.H, s.scale, s.causal, err);
+  } else {
+    using L = BwdLayout<64>;
+    cudaError_t e = cudaFuncSetAttribute(attn_bwd_kernel<64>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+    if (e != cudaSuccess) return e;
+    attn_bwd_kernel<64><<<grid, kThreads, L::kAlloc, stream>>>(
+        tq, tk, tv, tdo, stats, delta, dq_acc, dkp, dvp, s.Nq, s.Nkv, s.H, s.scale, s.causal, err);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dq_convert(const AttnShape& s, const float* dq_acc, void* dq,
+                              cudaStream_t stream) {
+  const int64_t n8 = static_cast<int64_t>(s.B) * s.Nq * s.H * s.D / 8;
+  int64_t grid = (n8 + 255) / 256;
+  if (grid > 152 * 8) grid = 152 * 8;
+  dq_convert_kernel<<<static_cast<int>(grid), 256, 0, stream>>>(
+      dq_acc, static_cast<__nv_bfloat16*>(dq), n8);
+  return cudaGetLastError();
+}
+
+}  // namespace nvq

@@ -1,0 +1,52 @@
+// Host-side declarations shared by the C-ABI layer (api.cu) and the kernel
+// translation units.  Every launch_* function enqueues kernels on `stream` and
+// returns the launch's cudaError_t; validation happens in api.cu before.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace nvq {
+
+constexpr int kTile = 128;  // query / key rows per attention tile
+
+// Quantizer output modes.
+enum QuantMode : int { kUnitBf16 = 0, kUnitF16 = 1, kStaticBf16 = 2 };
+
+cudaError_t launch_fake_quant(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
+                              const float* gsf, int mode, void* out, int64_t ld_out,
+                              uint8_t* scales, int64_t ld_s, uint8_t* codes, int64_t ld_c,
+                              cudaStream_t stream);
+cudaError_t launch_global_sf(const void* x, int64_t rows, int64_t cols, int64_t ld_x, float* gsf,
+                             cudaStream_t stream);
+
+struct AttnShape {
+  int B, Nq, Nkv, H, D;
+  float scale;
+  int causal;
+};
+
+// Tensor maps over [B, N, H, D] 16-bit tensors, box {64, 128, 1, 1}, 128-byte swizzle.
+bool make_bnhd_map(CUtensorMap* map, const void* base, int B, int N, int H, int D, bool f16);
+
+cudaError_t launch_attn_fwd(const AttnShape& s, const CUtensorMap& tq, const CUtensorMap& tk,
+                            const CUtensorMap& tv, void* o, float* stats, int* err,
+                            cudaStream_t stream);
+cudaError_t launch_bwd_prep(const AttnShape& s, const void* o, const void* dout, float* delta,
+                            float* dq_acc, cudaStream_t stream);
+cudaError_t launch_attn_bwd(const AttnShape& s, const CUtensorMap& tq, const CUtensorMap& tk,
+                            const CUtensorMap& tv, const CUtensorMap& tdo, const float* stats,
+                            const float* delta, float* dq_acc, void* dk, void* dv, int* err,
+                            cudaStream_t stream);
+cudaError_t launch_dq_convert(const AttnShape& s, const float* dq_acc, void* dq,
+                              cudaStream_t stream);
+
+cudaError_t launch_selftest_umma(const CUtensorMap& ta, const CUtensorMap& tb, float* c, int N,
+                                 int K, int a_mn, int b_mn, int* err, cudaStream_t stream);
+cudaError_t launch_selftest_timeout(int64_t limit_ns, int* err, cudaStream_t stream);
+
+// Maps a [rows, cols] 16-bit row-major matrix with a box of {64, box_rows}.
+bool make_2d_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_rows);
+
+}  // namespace nvq

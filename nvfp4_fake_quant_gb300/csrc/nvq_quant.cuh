@@ -1,0 +1,226 @@
+// NVFP4 block quantization device functions (16 elements, E4M3 scale, E2M1 codes).
+//
+// Definition (FastVideo "nvfp4_qad.py", module docstring; "vsqa-preview-1.3b
+// metadata.json", attention.precision): s = E4M3(amax*gsf/6), code =
+// E2M1(|x|*gsf/s), value = sign(x)*code*s/gsf, both roundings to nearest even
+// and saturating.  The two decisions are taken on IEEE fp32 values of
+// amax*gsf/6 and |x|*gsf/s.
+//
+// Three variants:
+//  * quant16_unit   exact for bf16 input and unit gsf, cheap: the scale uses one
+//                   IEEE division per block; each code uses a hardware
+//                   reciprocal and a product whose value is then rounded to
+//                   17 significant bits ("snapped") before the E2M1 conversion.
+//                   Why that equals the exact decision: x (8-bit significand)
+//                   and s (<= 4 bits) make x/s either exactly a tie point t of
+//                   the E2M1 grid (then x == t*s and the approximate quotient,
+//                   within 2^-22 of t, snaps back onto t) or at relative distance
+//                   >= 2^-13 from every tie (x - t*s is a non-zero multiple of
+//                   2^min(ex-7, es-5) while t*s < 2^(es+4)), which neither the
+//                   2^-22 error nor the 2^-17 snap can cross.
+//  * quant16_static IEEE fp32 products and quotients (mul.rn / div.rn) in the
+//                   order of the definition: bit-identical to any IEEE fp32
+//                   evaluation of the same steps.
+//  * quant16_p      the softmax probabilities inside attention (fp32 inputs):
+//                   reciprocal and product without snapping.  The forward and
+//                   the backward run this same code on bit-identical inputs.
+#pragma once
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+namespace nvq {
+
+// RNE(v) to E4M3FN with saturation; v >= 0 finite.  Returns the bit pattern.
+__device__ __forceinline__ uint32_t e4m3_rn_sat(float v) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(v));
+  return r & 0xFFu;
+}
+
+// E4M3FN bit pattern (low byte of `b`) to its value, as a packed f16x2 whose
+// low half holds the value.
+__device__ __forceinline__ uint32_t e4m3_to_f16x2(uint32_t b) {
+  uint32_t h;
+  const uint16_t in = static_cast<uint16_t>(b & 0xFFu);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h) : "h"(in));
+  return h;
+}
+
+__device__ __forceinline__ float f16lo_to_f32(uint32_t h2) {
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xFFFFu)));
+}
+
+// Eight non-negative fp32 values -> eight E2M1 codes (RNE, satfinite), element
+// i in nibble i of the result.
+__device__ __forceinline__ uint32_t e2m1x8(const float (&v)[8]) {
+  uint32_t out;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(out)
+      : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]),
+        "f"(v[7]));
+  return out;
+}
+
+// Eight packed E2M1 codes -> four f16x2 values (element 2j in the low half of h[j]).
+__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t codes, uint32_t (&h)[4]) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+      : "r"(codes));
+}
+
+__device__ __forceinline__ float rcp_approx(float x) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+__device__ __forceinline__ float snap17(float q) {
+  return __uint_as_float((__float_as_uint(q) + 0x40u) & 0xFFFFFF80u);
+}
+
+__device__ __forceinline__ float bf16_bits_to_f32(uint32_t b16) { return __uint_as_float(b16 << 16); }
+
+// Result of quantizing one 16-element block of bf16 values.
+struct Q16 {
+  uint32_t sbyte;      // E4M3FN scale byte
+  uint32_t codes[2];   // 16 four-bit codes with sign (element i in nibble i%8 of codes[i/8])
+  uint32_t out[8];     // 16 dequantized values as bf16x2 or f16x2 (element 2j low half of out[j])
+};
+
+// x: 16 bf16 values packed as 8 u32 (element 2j in the low half of x[j]).
+// OUT_F16: dequantized values as f16 (exact for unit gsf) instead of bf16.
+template <bool OUT_F16>
+__device__ __forceinline__ Q16 quant16_unit(const uint32_t (&x)[8]) {
+  Q16 r;
+  float a[16];
+  uint32_t sgn = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    a[2 * j] = bf16_bits_to_f32(x[j] & 0x7FFFu);
+    a[2 * j + 1] = bf16_bits_to_f32((x[j] >> 16) & 0x7FFFu);
+    sgn |= ((x[j] >> 15) & 1u) << (2 * j);
+    sgn |= ((x[j] >> 31) & 1u) << (2 * j + 1);
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, a[i]);
+  const float t = __fdiv_rn(amax, 6.0f);
+  r.sbyte = e4m3_rn_sat(t);
+  const uint32_t s_h = e4m3_to_f16x2(r.sbyte);
+  const float s = f16lo_to_f32(s_h);
+  const float inv = s > 0.f ? rcp_approx(s) : 0.f;
+  const uint32_t s_h2 = (s_h & 0xFFFFu) | (s_h << 16);
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    float q[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) q[i] = snap17(a[8 * h + i] * inv);
+    const uint32_t c = e2m1x8(q);
+    uint32_t hv[4];
+    e2m1x8_to_f16x2(c, hv);
+    uint32_t signs_nib = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) signs_nib |= ((sgn >> (8 * h + i)) & 1u) << (4 * i + 3);
+    r.codes[h] = c | signs_nib;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const uint32_t m = hmul2(hv[j], s_h2);  // exact: <= 7 significant bits, f16 normal range
+      const uint32_t sg = (((sgn >> (8 * h + 2 * j)) & 1u) << 15) |
+                          (((sgn >> (8 * h + 2 * j + 1)) & 1u) << 31);
+      if (OUT_F16) {
+        r.out[4 * h + j] = m | sg;
+      } else {
+        const float lo = f16lo_to_f32(m), hi = f16lo_to_f32(m >> 16);
+        __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);  // exact
+        r.out[4 * h + j] = *reinterpret_cast<uint32_t*>(&b) | sg;
+      }
+    }
+  }
+  return r;
+}
+
+// Static global scale g (fp32): IEEE products and quotients in the order of the
+// definition.  Output values are bf16 (RNE of the fp32 quotient code*s/g).
+__device__ __forceinline__ Q16 quant16_static(const uint32_t (&x)[8], float g) {
+  Q16 r;
+  float a[16];
+  uint32_t sgn = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    a[2 * j] = bf16_bits_to_f32(x[j] & 0x7FFFu);
+    a[2 * j + 1] = bf16_bits_to_f32((x[j] >> 16) & 0x7FFFu);
+    sgn |= ((x[j] >> 15) & 1u) << (2 * j);
+    sgn |= ((x[j] >> 31) & 1u) << (2 * j + 1);
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, a[i]);
+  const float t = __fdiv_rn(__fmul_rn(amax, g), 6.0f);
+  r.sbyte = e4m3_rn_sat(t);
+  const float s = f16lo_to_f32(e4m3_to_f16x2(r.sbyte));
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    float q[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) q[i] = s > 0.f ? __fdiv_rn(__fmul_rn(a[8 * h + i], g), s) : 0.f;
+    const uint32_t c = e2m1x8(q);
+    uint32_t hv[4];
+    e2m1x8_to_f16x2(c, hv);
+    uint32_t signs_nib = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) signs_nib |= ((sgn >> (8 * h + i)) & 1u) << (4 * i + 3);
+    r.codes[h] = c | signs_nib;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float lo = __fdiv_rn(__fmul_rn(f16lo_to_f32(hv[j]), s), g);
+      const float hi = __fdiv_rn(__fmul_rn(f16lo_to_f32(hv[j] >> 16), s), g);
+      __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+      const uint32_t sg = (((sgn >> (8 * h + 2 * j)) & 1u) << 15) |
+                          (((sgn >> (8 * h + 2 * j + 1)) & 1u) << 31);
+      r.out[4 * h + j] = *reinterpret_cast<uint32_t*>(&b) | sg;
+    }
+  }
+  return r;
+}
+
+// Softmax probabilities (0 <= p <= 1, fp32) of one 16-key block -> P~ as eight
+// f16x2 (exact: code * E4M3 scale).
+__device__ __forceinline__ void quant16_p(const float* p, uint32_t (&out)[8]) {
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, p[i]);
+  const uint32_t sb = e4m3_rn_sat(amax * (1.0f / 6.0f));
+  const uint32_t s_h = e4m3_to_f16x2(sb);
+  const float s = f16lo_to_f32(s_h);
+  const float inv = s > 0.f ? rcp_approx(s) : 0.f;
+  const uint32_t s_h2 = (s_h & 0xFFFFu) | (s_h << 16);
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    float q[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) q[i] = p[8 * h + i] * inv;
+    uint32_t hv[4];
+    e2m1x8_to_f16x2(e2m1x8(q), hv);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) out[4 * h + j] = hmul2(hv[j], s_h2);
+  }
+}
+
+}  // namespace nvq

@@ -1,0 +1,148 @@
+// Standalone NVFP4 quantizer kernels (HBM-bound) and the static global scale.
+//
+// One thread quantizes one 16-element block: two 16-byte loads, one 32-byte
+// output, one scale byte and/or 8 code bytes.  A warp covers 32 consecutive
+// blocks of a row (1 KiB of input), so loads and stores are fully coalesced.
+// The grid is a whole number of waves over the SMs and strides over the
+// blocks.
+#include <cuda_runtime.h>
+
+#include "nvq_internal.h"
+#include "nvq_ptx.cuh"
+#include "nvq_quant.cuh"
+
+namespace nvq {
+
+namespace {
+
+__device__ __forceinline__ uint4 ld_stream(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(256) fake_quant_kernel(
+    const uint16_t* __restrict__ x, int64_t rows, int64_t nbc, int64_t ld_x,
+    const float* __restrict__ gsf, uint16_t* __restrict__ out, int64_t ld_out,
+    uint8_t* __restrict__ scales, int64_t ld_s, uint8_t* __restrict__ codes, int64_t ld_c) {
+  const float g = (MODE == kStaticBf16) ? *gsf : 1.0f;
+  const int64_t total = rows * nbc;
+  const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
+       idx += step) {
+    const int64_t r = idx / nbc;
+    const int64_t cb = idx - r * nbc;
+    const uint16_t* src = x + r * ld_x + cb * 16;
+    const uint4 v0 = ld_stream(src);
+    const uint4 v1 = ld_stream(src + 8);
+    const uint32_t xv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    Q16 q;
+    if constexpr (MODE == kStaticBf16) {
+      q = quant16_static(xv, g);
+    } else {
+      q = quant16_unit<MODE == kUnitF16>(xv);
+    }
+    if (out != nullptr) {
+      uint4* dst = reinterpret_cast<uint4*>(out + r * ld_out + cb * 16);
+      dst[0] = make_uint4(q.out[0], q.out[1], q.out[2], q.out[3]);
+      dst[1] = make_uint4(q.out[4], q.out[5], q.out[6], q.out[7]);
+    }
+    if (scales != nullptr) scales[r * ld_s + cb] = static_cast<uint8_t>(q.sbyte);
+    if (codes != nullptr) {
+      *reinterpret_cast<uint2*>(codes + r * ld_c + cb * 8) = make_uint2(q.codes[0], q.codes[1]);
+    }
+  }
+}
+
+// amax(|x|) as the unsigned bit pattern of a non-negative float (monotone).
+__global__ void __launch_bounds__(256) amax_kernel(const uint16_t* __restrict__ x, int64_t rows,
+                                                   int64_t cols, int64_t ld_x,
+                                                   unsigned int* __restrict__ amax_bits) {
+  const int64_t nvec = cols / 8;  // 16-byte vectors per row (cols % 8 handled below)
+  const int64_t total = rows * nvec;
+  const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  uint32_t m = 0;  // max of |bf16| bit patterns (monotone for non-negative values)
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += step) {
+    const int64_t r = i / nvec, c = i - r * nvec;
+    const uint4 v = ld_stream(x + r * ld_x + c * 8);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      m = max(m, w[j] & 0x7FFFu);
+      m = max(m, (w[j] >> 16) & 0x7FFFu);
+    }
+  }
+  const int64_t tail = cols - nvec * 8;
+  if (tail > 0) {
+    for (int64_t r = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; r < rows;
+         r += step) {
+      for (int64_t c = nvec * 8; c < cols; ++c)
+        m = max(m, static_cast<uint32_t>(x[r * ld_x + c] & 0x7FFFu));
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
+  if ((threadIdx.x & 31) == 0 && m != 0) atomicMax(amax_bits, m << 16);  // bf16 -> f32 bits
+}
+
+__global__ void global_sf_finalize_kernel(float* gsf) {
+  const float amax = __uint_as_float(*reinterpret_cast<unsigned int*>(gsf));
+  *gsf = __fdiv_rn(2688.0f, fmaxf(amax, 1e-12f));
+}
+
+int grid_for(int64_t work, int threads) {
+  int dev = 0, sms = 152;
+  if (cudaGetDevice(&dev) == cudaSuccess)
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t waves = 8;  // 8 x 256-thread blocks resident per SM at most
+  int64_t blocks = (work + threads - 1) / threads;
+  const int64_t cap = static_cast<int64_t>(sms) * waves;
+  if (blocks > cap) blocks = cap;
+  return static_cast<int>(blocks < 1 ? 1 : blocks);
+}
+
+}  // namespace
+
+cudaError_t launch_fake_quant(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
+                              const float* gsf, int mode, void* out, int64_t ld_out,
+                              uint8_t* scales, int64_t ld_s, uint8_t* codes, int64_t ld_c,
+                              cudaStream_t stream) {
+  const int64_t nbc = cols / 16;
+  const int threads = 256;
+  const int grid = grid_for(rows * nbc, threads);
+  const auto* xs = static_cast<const uint16_t*>(x);
+  auto* os = static_cast<uint16_t*>(out);
+  switch (mode) {
+    case kUnitBf16:
+      fake_quant_kernel<kUnitBf16><<<grid, threads, 0, stream>>>(xs, rows, nbc, ld_x, gsf, os,
+                                                                 ld_out, scales, ld_s, codes, ld_c);
+      break;
+    case kUnitF16:
+      fake_quant_kernel<kUnitF16><<<grid, threads, 0, stream>>>(xs, rows, nbc, ld_x, gsf, os,
+                                                                ld_out, scales, ld_s, codes, ld_c);
+      break;
+    default:
+      fake_quant_kernel<kStaticBf16><<<grid, threads, 0, stream>>>(
+          xs, rows, nbc, ld_x, gsf, os, ld_out, scales, ld_s, codes, ld_c);
+      break;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_global_sf(const void* x, int64_t rows, int64_t cols, int64_t ld_x, float* gsf,
+                             cudaStream_t stream) {
+  cudaError_t e = cudaMemsetAsync(gsf, 0, sizeof(float), stream);
+  if (e != cudaSuccess) return e;
+  const int threads = 256;
+  const int grid = grid_for(rows * (cols / 8 > 0 ? cols / 8 : 1), threads);
+  amax_kernel<<<grid, threads, 0, stream>>>(static_cast<const uint16_t*>(x), rows, cols, ld_x,
+                                            reinterpret_cast<unsigned int*>(gsf));
+  global_sf_finalize_kernel<<<1, 1, 0, stream>>>(gsf);
+  return cudaGetLastError();
+}
+
+}  // namespace nvq

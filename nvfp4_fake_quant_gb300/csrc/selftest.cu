@@ -1,0 +1,131 @@
+// Self-tests of the hardware encodings the attention kernels rely on:
+//  * one 128 x N x K tcgen05 kind::f16 BF16 UMMA fed by 128-byte-swizzled TMA
+//    tiles through the same shared-memory and instruction descriptors, for
+//    K-major and MN-major A and B;
+//  * a bounded mbarrier wait that is meant to run out.
+#include <cuda_runtime.h>
+
+#include "nvq_internal.h"
+#include "nvq_ptx.cuh"
+
+namespace nvq {
+
+namespace {
+
+constexpr uint32_t kSmem = 2 * 32768 + 1024 + 64;
+
+// Tile of a row-major [rows, cols] 16-bit matrix as loaded by TMA with a box
+// of {64, rows}: column block j (64 columns) at j * rows * 128 bytes.
+__global__ void __launch_bounds__(128, 1)
+    selftest_umma_kernel(const __grid_constant__ CUtensorMap ta,
+                         const __grid_constant__ CUtensorMap tb, float* __restrict__ c, int N,
+                         int K, int a_mn, int b_mn, int* __restrict__ err) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023u) &
+                                             ~static_cast<uintptr_t>(1023u));
+  uint8_t* sa = smem;
+  uint8_t* sb = smem + 32768;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 65536);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 65536 + 16);
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + 65536 + 20);
+  const int warp = threadIdx.x >> 5;
+  // A is [128, K] (K-major) or [K, 128] (MN-major); B is [N, K] or [K, N].
+  const int a_rows = a_mn ? K : 128, a_cols = a_mn ? 128 : K;
+  const int b_rows = b_mn ? K : N, b_cols = b_mn ? N : K;
+  if (threadIdx.x == 0) {
+    *abort = 0;
+    mbar_init(&bars[0], 1);
+    mbar_init(&bars[1], 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, 128);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  bool ok = true;
+  if (threadIdx.x == 0) {
+    const uint32_t bytes = static_cast<uint32_t>(a_rows * a_cols * 2 + b_rows * b_cols * 2);
+    mbar_arrive_expect_tx(&bars[0], bytes);
+    for (int j = 0; j < a_cols / 64; ++j)
+      tma_load_4d(sa + j * a_rows * 128, &ta, j * 64, 0, 0, 0, &bars[0]);
+    for (int j = 0; j < b_cols / 64; ++j)
+      tma_load_4d(sb + j * b_rows * 128, &tb, j * 64, 0, 0, 0, &bars[0]);
+    ok = mbar_wait(&bars[0], 0, abort);
+    if (ok) {
+      tc_fence_after();
+      const uint32_t idesc = idesc_f16(128, N, 1, a_mn, b_mn);
+      const uint32_t a0 = smem_u32(sa), b0 = smem_u32(sb);
+      for (int kk = 0; kk < K / 16; ++kk) {
+        uint64_t ad, bd;
+        if (a_mn)  // rows = K: 16 rows per step; 64-column M chunks a_rows*128 apart
+          ad = sdesc_sw128(a0 + kk * 2048, static_cast<uint32_t>(a_rows * 128), 1024);
+        else  // rows = M: 32 bytes per K step inside an atom, next atom block a_rows*128 on
+          ad = sdesc_sw128(a0 + (kk >> 2) * (a_rows * 128) + (kk & 3) * 32, 16, 1024);
+        if (b_mn)
+          bd = sdesc_sw128(b0 + kk * 2048, static_cast<uint32_t>(b_rows * 128), 1024);
+        else
+          bd = sdesc_sw128(b0 + (kk >> 2) * (b_rows * 128) + (kk & 3) * 32, 16, 1024);
+        umma_f16_ss(tmem, ad, bd, idesc, kk > 0 ? 1u : 0u);
+      }
+      umma_commit(&bars[1]);
+    }
+  }
+  __syncthreads();
+  if (ok && !*abort && mbar_wait(&bars[1], 0, abort)) {
+    tc_fence_after();
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const int row = threadIdx.x;
+    uint32_t r[32];
+    for (int cc = 0; cc < N / 32; ++cc) {
+      tmem_ld32(tmem + lane_base + cc * 32, r);
+      tmem_wait_ld();
+      for (int i = 0; i < 32; ++i) c[row * N + cc * 32 + i] = __uint_as_float(r[i]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  report_abort(abort, err);
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 128);
+  }
+}
+
+__global__ void selftest_timeout_kernel(int64_t limit_ns, int* __restrict__ err) {
+  __shared__ uint64_t bar;
+  __shared__ int abort;
+  if (threadIdx.x == 0) {
+    abort = 0;
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    // nothing ever arrives on `bar`: the wait must give up after limit_ns
+    mbar_wait(&bar, 0, &abort, static_cast<uint64_t>(limit_ns));
+  }
+  __syncthreads();
+  report_abort(&abort, err);
+}
+
+}  // namespace
+
+cudaError_t launch_selftest_umma(const CUtensorMap& ta, const CUtensorMap& tb, float* c, int N,
+                                 int K, int a_mn, int b_mn, int* err, cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(selftest_umma_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  if (e != cudaSuccess) return e;
+  selftest_umma_kernel<<<1, 128, kSmem, stream>>>(ta, tb, c, N, K, a_mn, b_mn, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_selftest_timeout(int64_t limit_ns, int* err, cudaStream_t stream) {
+  selftest_timeout_kernel<<<1, 32, 0, stream>>>(limit_ns, err);
+  return cudaGetLastError();
+}
+
+}  // namespace nvq

@@ -1,0 +1,136 @@
+"""C-ABI checks that need no GPU: the library builds and loads, exports every
+function include/nvfp4attn.h declares, sizes its workspaces, and rejects bad
+arguments on the host before launching anything (these calls never reach a
+CUDA API, so they are safe without a device)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from nvfp4_fake_quant_gb300 import _lib
+from nvfp4_fake_quant_gb300 import build as nvbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "nvfp4attn.h")
+
+OK, INVALID, UNSUPPORTED, WORKSPACE = 0, 1, 2, 3
+A = 0x100000  # a 256-byte-aligned non-null address that validation never dereferences
+
+
+@pytest.fixture(scope="module")
+def lib():
+    path = nvbuild.build()
+    return _lib.load(path)
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    return sorted(set(re.findall(r"\b([A-Za-z_]\w*)\s*\([^;{()]*\)\s*;", src)))
+
+
+def test_header_declares_the_abi():
+    names = declared_functions()
+    for required in ["nvfp4_fake_quant", "nvfp4_quantize_codes", "nvfp4_global_sf", "attn_qat_fwd",
+                     "attn_qat_bwd", "attn_qat_fwd_workspace", "attn_qat_bwd_workspace",
+                     "nvq_device_status", "nvq_status_string", "nvq_version"]:
+        assert required in names
+    assert set(names) == set(_lib.SIGNATURES), "binding and header disagree"
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    cdll = ctypes.CDLL(nvbuild.LIB)
+    for name in declared_functions():
+        getattr(cdll, name)
+
+
+def test_status_strings_and_version(lib):
+    for code, name in _lib.STATUS.items():
+        assert lib.nvq_status_string(code).decode() == name
+    assert lib.nvq_status_string(99).decode() == "NVQ_ERR_UNKNOWN"
+    assert lib.nvq_version() >> 16 == 1
+
+
+def test_workspace_sizes(lib):
+    b, n, h, d = 1, 25088, 12, 128
+    t = b * n * h * d * 2
+    assert lib.attn_qat_fwd_workspace(b, n, n, h, d) == 3 * t
+    assert lib.attn_qat_bwd_workspace(b, n, n, h, d) == 3 * t + 2 * t + b * h * n * 4
+    assert lib.attn_qat_fwd_workspace(0, n, n, h, d) == 0
+    assert lib.attn_qat_fwd_workspace(1, 3, 5, 1, 64) % 256 == 0
+
+
+def _fwd(lib, q=A, k=A, v=A, B=1, Nq=128, Nkv=128, H=1, D=128, scale=0.125, causal=0, o=A,
+         stats=A, ws=A, ws_bytes=None):
+    if ws_bytes is None:
+        ws_bytes = lib.attn_qat_fwd_workspace(B, Nq, Nkv, H, D) if min(B, Nq, Nkv, H) > 0 else 0
+    return lib.attn_qat_fwd(q, k, v, B, Nq, Nkv, H, D, scale, causal, o, stats, ws, ws_bytes, None)
+
+
+def test_fwd_rejects_bad_arguments(lib):
+    assert _fwd(lib, D=96) == UNSUPPORTED
+    assert _fwd(lib, D=256) == UNSUPPORTED
+    assert _fwd(lib, causal=1, Nq=128, Nkv=256) == UNSUPPORTED
+    assert _fwd(lib, B=0) == INVALID
+    assert _fwd(lib, Nkv=0) == INVALID
+    assert _fwd(lib, scale=0.0) == INVALID
+    assert _fwd(lib, scale=-1.0) == INVALID
+    assert _fwd(lib, scale=float("nan")) == INVALID
+    assert _fwd(lib, scale=float("inf")) == INVALID
+    assert _fwd(lib, causal=2) == INVALID
+    assert _fwd(lib, q=None) == INVALID
+    assert _fwd(lib, stats=None) == INVALID
+    assert _fwd(lib, o=A + 8) == INVALID
+    assert _fwd(lib, ws=None) == WORKSPACE
+    assert _fwd(lib, ws_bytes=1024) == WORKSPACE
+    assert _fwd(lib, ws=A + 16) == WORKSPACE
+
+
+def test_bwd_rejects_bad_arguments(lib):
+    def bwd(dq=A, D=128, Nq=128, Nkv=128, causal=0, ws=A, ws_bytes=None, scale=0.1):
+        if ws_bytes is None:
+            ws_bytes = lib.attn_qat_bwd_workspace(1, Nq, Nkv, 1, D)
+        return lib.attn_qat_bwd(A, A, A, A, A, A, dq, A, A, 1, Nq, Nkv, 1, D, scale, causal, ws,
+                                ws_bytes, None)
+    assert bwd(D=80) == UNSUPPORTED
+    assert bwd(causal=1, Nkv=64) == UNSUPPORTED
+    assert bwd(dq=None) == INVALID
+    assert bwd(dq=A + 2) == INVALID
+    assert bwd(scale=float("nan")) == INVALID
+    assert bwd(ws_bytes=0) == WORKSPACE
+
+
+def test_quantizer_rejects_bad_arguments(lib):
+    def fq(x=A, rows=4, cols=32, ld=32, gsf=None, out=A + 4096, ld_out=32, sc=A, ld_s=2):
+        return lib.nvfp4_fake_quant(x, rows, cols, ld, gsf, out, ld_out, sc, ld_s, None)
+    assert fq(cols=24, ld=24, ld_out=24) == INVALID     # cols % 16
+    assert fq(cols=0) == INVALID
+    assert fq(rows=0) == INVALID
+    assert fq(ld=16) == INVALID                          # ld_x < cols
+    assert fq(ld=36) == INVALID                          # ld_x % 8
+    assert fq(x=None) == INVALID
+    assert fq(x=A + 2) == INVALID
+    assert fq(out=None) == INVALID
+    assert fq(ld_out=40, out=A) == INVALID               # in place needs ld_out == ld_x
+    assert fq(ld_s=1) == INVALID
+    assert fq(gsf=A + 1) == INVALID
+    assert lib.nvfp4_quantize_codes(A, 4, 32, 32, None, A, 12, A, 2, None) == INVALID  # ld%8
+    assert lib.nvfp4_quantize_codes(A, 4, 32, 32, None, A, 16, None, 2, None) == INVALID
+    assert lib.nvfp4_global_sf(A, 4, 32, 32, None, None) == INVALID
+    assert lib.nvfp4_global_sf(A, 0, 32, 32, A, None) == INVALID
+    assert lib.nvq_selftest_timeout(0, None) == INVALID
+    assert lib.nvq_selftest_umma(A, A, A, 96, 64, 0, 0, None) == INVALID
+
+
+def test_python_layer_conventions():
+    from nvfp4_fake_quant_gb300 import api
+    with pytest.raises(NotImplementedError):
+        api.AttnQAT(12, 128, None, False, dropout_p=0.1)
+    with pytest.raises(ValueError):
+        api.AttnQAT(12, 96)
+    assert api.AttnQAT(12, 128).softmax_scale == 1.0 / 128 ** 0.5
+    assert api.default_scale(64) == 0.125
