@@ -1,0 +1,374 @@
+"""Benchmark of the NVFP4 Attn-QAT hot path on GB300.
+
+One step = one Attn-QAT forward + straight-through backward (all kernels of the
+path: Q/K/V quantization, two-pass forward, delta, KV-outer backward, dQ
+conversion) on the Wan2.1-T2V-1.3B self-attention shape B=1, H=12, N=25088,
+D=128 (16x28x56 latent tokens), seeded synthetic bf16 inputs resident in HBM.
+Counted FLOPs: forward 4*B*H*N^2*D, backward 2.5x that.
+
+Prints one JSON line (rank 0).  Multi-GPU runs (torchrun, one process per GPU)
+are independent replicas of the same step: weak scaling, no data-path
+collective; the barrier and the max-over-ranks time use torch.distributed.
+
+--impl reference runs the CPU oracle (float64, the baseline here) on a bounded
+slice of the same workload: query rows [0, R) of one head against all keys.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "Attn-QAT fwd+bwd TFLOPS and % of GB300 BF16 peak at N=25088,H=12,D=128"
+WORKLOAD = ("Wan2.1-1.3B self-attention at 448x896x61 frames: B=1, H=12, N=25088 "
+            "(16x28x56 latent tokens), D=128, non-causal, scale 1/sqrt(128); Q,K per-(token,head) "
+            "unit-RMS N(0,1), V,dO N(0,1) bf16 (seed 2); NVFP4 fake-quant on Q,K,V,P")
+SHAPE = dict(b=1, n=25088, h=12, d=128)
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def flops_fwd(b, nq, nkv, h, d):
+    return 4.0 * b * h * nq * nkv * d
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    parts = [p.strip() for p in line.split(",")]
+                    if len(parts) >= 9:
+                        rows.append(parts)
+        except Exception:
+            pass
+        finally:
+            try:
+                os.unlink(self.path)
+            except Exception:
+                pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        power = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+                "samples": len(rows), "power_w_max": max(power) if power else None}
+
+
+def dist_setup(n_gpus: int):
+    import torch
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        return rank, ws, local, dist
+    return 0, 1, 0, None
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(x: float, dist, dev) -> float:
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def cpu_baseline(rows: int, head: int = 0):
+    """The oracle, as it stands, on query rows [0, rows) of one head (all keys)."""
+    import torch
+
+    from nvfp4_fake_quant_gb300 import workloads
+    from oracle import attention as oa
+    inp = workloads.wan25088()
+    q = inp.q[:, :rows, head:head + 1]
+    k = inp.k[:, :, head:head + 1]
+    v = inp.v[:, :, head:head + 1]
+    do = inp.do[:, :rows, head:head + 1]
+    t0 = time.perf_counter()
+    o, _, _ = oa.attn_fwd(q, k, v, inp.scale)
+    oa.attn_bwd(q, k, v, o, do, inp.scale)
+    dt = time.perf_counter() - t0
+    fl = 3.5 * flops_fwd(1, rows, SHAPE["n"], 1, SHAPE["d"])
+    return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": torch.get_num_threads(),
+            "kind": "oracle", "seconds": dt,
+            "sample": f"query rows 0..{rows - 1} of head {head} against all {SHAPE['n']} keys, "
+                      "fwd+bwd in float64 (counted FLOPs of that slice)"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    rows = args.ref_rows
+    vals = []
+    for _ in range(args.warmup):
+        cpu_baseline(rows)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        vals.append(cpu_baseline(rows))
+    total = time.perf_counter() - t0
+    fl = 3.5 * flops_fwd(1, rows, SHAPE["n"], 1, SHAPE["d"]) * args.steps
+    value = fl / total / 1e12
+    cb = dict(vals[-1])
+    cb["value"] = value
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": total / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "sample": cb["sample"]},
+            "cpu_baseline": cb,
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def time_events(fn, iters, stream):
+    import torch
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(iters):
+        fn()
+    e.record(stream)
+    e.synchronize()
+    return s.elapsed_time(e) / iters
+
+
+def quantizer_bench(peaks, stream, iters=20):
+    """nvfp4_fake_quant on the 4096x4096 workload, L2 defeated by rotating
+    buffer sets whose total exceeds twice the L2 size."""
+    import torch
+
+    from nvfp4_fake_quant_gb300 import api, workloads
+    x = workloads.quant_matrix().cuda()
+    l2 = torch.cuda.get_device_properties(x.device).L2_cache_size
+    per_set = x.numel() * 2 * 2 + x.numel() // 16
+    nsets = max(4, math.ceil(2 * l2 / per_set) + 1)
+    xs = [x.clone() for _ in range(nsets)]
+    outs = [torch.empty_like(x) for _ in range(nsets)]
+    scs = [torch.empty(x.shape[0], x.shape[1] // 16, dtype=torch.uint8, device=x.device)
+           for _ in range(nsets)]
+    gsf = api.nvfp4_global_sf(x)
+    res = {}
+    alg_bytes = x.numel() * 4.0625
+    for name, g in (("unit", None), ("static", gsf)):
+        state = {"i": 0}
+
+        def one():
+            i = state["i"] % nsets
+            state["i"] += 1
+            api.nvfp4_fake_quant(xs[i], g, out=outs[i], scales=scs[i])
+        for _ in range(nsets):
+            one()
+        ms = time_events(one, iters * nsets, stream)
+        gbs = alg_bytes / (ms * 1e-3) / 1e9
+        res[name] = {"us": ms * 1e3, "GB/s": gbs, "frac": gbs / peaks["hbm_gbs"]}
+    res["algorithmic_bytes"] = alg_bytes
+    res["workload"] = ("bf16 4096x4096, N(0,1), 1% entries x50, 2% zero 16-blocks (seed 1); "
+                       f"{nsets} rotating buffer sets to defeat L2")
+    res["peak_GB/s"] = peaks["hbm_gbs"]
+    return res
+
+
+def run_ours(args):
+    import torch
+
+    from nvfp4_fake_quant_gb300 import _lib, api, workloads
+    rank, ws, local, dist = dist_setup(args.gpus)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    _lib.load()
+    peaks, peak_src = load_peaks()
+    b, n, h, d = SHAPE["b"], SHAPE["n"], SHAPE["h"], SHAPE["d"]
+    inp = workloads.wan25088()
+    q, k, v, do = (t.to(dev) for t in (inp.q, inp.k, inp.v, inp.do))
+    stream = torch.cuda.current_stream(dev)
+    o = torch.empty_like(q)
+    stats = torch.empty((b, h, 2, n), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    wsf = torch.empty(api.attn_qat_fwd_workspace(b, n, n, h, d), dtype=torch.uint8, device=dev)
+    wsb = torch.empty(api.attn_qat_bwd_workspace(b, n, n, h, d), dtype=torch.uint8, device=dev)
+
+    def fwd():
+        api.attn_qat_fwd(q, k, v, inp.scale, False, o=o, stats=stats, workspace=wsf)
+
+    def bwd():
+        api.attn_qat_bwd(q, k, v, o, stats, do, inp.scale, False, dq=dq, dk=dk, dv=dv,
+                         workspace=wsb)
+
+    def step():
+        fwd()
+        bwd()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if api.device_status(dev) != 0:
+        raise RuntimeError("a bounded device wait timed out during warm-up")
+
+    # ---- timed region: K steps, barrier + synchronize on both sides
+    barrier(dist)
+    torch.cuda.synchronize(dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(dist)
+    ms = ev0.elapsed_time(ev1) / args.steps
+    ms = max_over_ranks(ms, dist, dev)
+    clocks = clk.summary()
+    f_fwd = flops_fwd(b, n, n, h, d)
+    f_step = 3.5 * f_fwd
+    value = ws * f_step / (ms * 1e-3) / 1e12
+
+    # ---- per-call durations (fwd, bwd) on the launching stream
+    fwd_ms = time_events(fwd, max(2, args.steps), stream)
+    bwd_ms = time_events(bwd, max(2, args.steps), stream)
+    bwd_tflops = 2.5 * f_fwd / (bwd_ms * 1e-3) / 1e12
+    fwd_tflops = f_fwd / (fwd_ms * 1e-3) / 1e12
+    if api.device_status(dev) != 0:
+        raise RuntimeError("a bounded device wait timed out")
+
+    # ---- end to end through the public API with pinned host buffers
+    hq, hk, hv, hdo = (t.pin_memory() for t in (inp.q, inp.k, inp.v, inp.do))
+    hdq, hdk, hdv = (torch.empty_like(t).pin_memory() for t in (inp.q, inp.k, inp.v))
+
+    def e2e_step():
+        q.copy_(hq, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        v.copy_(hv, non_blocking=True)
+        do.copy_(hdo, non_blocking=True)
+        step()
+        hdq.copy_(dq, non_blocking=True)
+        hdk.copy_(dk, non_blocking=True)
+        hdv.copy_(dv, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(dist)
+    e2e_ms = time_events(e2e_step, args.steps, stream)
+    e2e_ms = max_over_ranks(e2e_ms, dist, dev)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
+    d2h = sum(t.numel() * t.element_size() for t in (hdq, hdk, hdv))
+
+    quant = quantizer_bench(peaks, stream) if rank == 0 and not args.skip_quantizer else None
+
+    peak_t = peaks["bf16_tflops"]
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "flops_per_step": f_step,
+                   "flops_counting": "fwd 4*B*H*N^2*D + bwd 2.5x fwd",
+                   "l2": "inputs larger than L2 (q,k,v,dO 77 MB each + workspaces)",
+                   "parallelism": f"replicas x{ws}"},
+        "pct_of_bf16_peak": value / ws / peak_t,
+        "peaks": {"bf16_tflops": peak_t, "hbm_gbs": peaks["hbm_gbs"], "source": peak_src},
+        "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "fwd_tflops": fwd_tflops, "bwd_tflops": bwd_tflops,
+        "roofline": {"kernel": "attn_qat_bwd call (quantize x3, delta, KV-outer backward, dQ convert)",
+                     "bound": "tensor", "achieved": bwd_tflops, "peak": peak_t,
+                     "unit": "TFLOP/s", "frac": bwd_tflops / peak_t, "traffic": None,
+                     "peak_source": f"{peak_src} bf16_tflops (burst)"},
+        "e2e": {"value": ws * f_step / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 10 * args.steps,
+        "clocks": clocks,
+    }
+    if quant is not None:
+        line["quantizer"] = quant
+    if rank == 0 and not args.skip_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.cpu_rows)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-rows", type=int, default=2048)
+    ap.add_argument("--ref-rows", type=int, default=512)
+    ap.add_argument("--skip-cpu-baseline", action="store_true")
+    ap.add_argument("--skip-quantizer", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -232,7 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float inv_l = ex2((m - lse) * kLog2e);  // 1 / l
       const bool edge = !row_ok || (k0 + kTile > Nkv) || (causal && qi == kt) ||
                         (qi * kTile + kTile > Nq);
-      if (!(ok = mbar_wait(s_full, it & 1, abort))) break;
+      if (!(ok = mbar_wait_warp(s_full, it & 1, abort))) break;
       tc_fence_after();
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
@@ -280,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       fence_proxy_async_smem();
       mbar_arrive(ds_full);
-      if (!(ok = mbar_wait(mma2_done, it & 1, abort))) break;
+      if (!(ok = mbar_wait_warp(mma2_done, it & 1, abort))) break;
       tc_fence_after();
       float* dqrow = dq_acc + ((static_cast<int64_t>(b) * Nq + qrow) * H + h) * D;
 #pragma unroll
@@ -299,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(dq_free);
     }
-    if (ok && n_iter > 0 && (ok = mbar_wait(dkdv_done, 0, abort))) {
+    if (ok && n_iter > 0 && (ok = mbar_wait_warp(dkdv_done, 0, abort))) {
       tc_fence_after();
       const int key = k0 + t;
       const int64_t base = ((static_cast<int64_t>(b) * Nkv + key) * H + h) * D;
@@ -342,6 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   report_abort(abort, err);
   if (warp == 5) {
+    __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }

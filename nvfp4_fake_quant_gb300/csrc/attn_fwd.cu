@@ -235,7 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t r[32];
     for (int j = 0; j < n_kv && ok; ++j) {
       const uint32_t sb = sc & 1u;
-      if (!(ok = mbar_wait(&s_full[sb], (sc >> 1) & 1u, abort))) break;
+      if (!(ok = mbar_wait_warp(&s_full[sb], (sc >> 1) & 1u, abort))) break;
       tc_fence_after();
       const bool edge = (j * kTile + kTile > Nkv) || (causal && j == qt);
 #pragma unroll
@@ -262,7 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float l = 0.f;
     for (int j = 0; j < n_kv && ok; ++j) {
       const uint32_t sb = sc & 1u;
-      if (!(ok = mbar_wait(&s_full[sb], (sc >> 1) & 1u, abort))) break;
+      if (!(ok = mbar_wait_warp(&s_full[sb], (sc >> 1) & 1u, abort))) break;
       tc_fence_after();
       const bool edge = (j * kTile + kTile > Nkv) || (causal && j == qt);
       uint32_t pk[64];
@@ -292,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       mbar_arrive(&s_empty[sb]);
       ++sc;
-      if (j > 0 && !(ok = mbar_wait(pv_done, (j - 1) & 1, abort))) break;
+      if (j > 0 && !(ok = mbar_wait_warp(pv_done, (j - 1) & 1, abort))) break;
 #pragma unroll
       for (int ch = 0; ch < 16; ++ch) {
         *reinterpret_cast<uint4*>(p_smem + sw128_offset(t, ch * 8, 128)) =
@@ -301,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       fence_proxy_async_smem();
       mbar_arrive(p_full);
     }
-    if (ok && (ok = mbar_wait(o_full, 0, abort))) {
+    if (ok && (ok = mbar_wait_warp(o_full, 0, abort))) {
       tc_fence_after();
       const float inv_l = 1.0f / l;
       __nv_bfloat16* orow = o + ((static_cast<int64_t>(b) * Nq + qrow) * H + h) * D;
@@ -335,6 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   report_abort(abort, err);
   if (warp == 5) {
+    __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }

@@ -74,6 +74,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// mbar_wait by every lane of a warp with a warp-uniform result, so that the
+// .sync.aligned tcgen05 instructions that follow run on a converged warp even
+// when some lane's wait gave up.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  const bool ok = mbar_wait(bar, parity, abort);
+  return __all_sync(0xFFFFFFFFu, ok);
+}
+
 // Block teardown: report an aborted wait in the device error word.
 __device__ __forceinline__ void report_abort(volatile int* abort, int* err) {
   if (threadIdx.x == 0 && *abort) atomicExch(err, kErrTimeout);

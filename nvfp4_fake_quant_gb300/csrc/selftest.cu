@@ -75,7 +75,9 @@ __global__ void __launch_bounds__(128, 1)
     }
   }
   __syncthreads();
-  if (ok && !*abort && mbar_wait(&bars[1], 0, abort)) {
+  // every warp waits (warp-uniformly) even when the issue failed: *abort ends it
+  const bool done = mbar_wait_warp(&bars[1], 0, abort);
+  if (done && ok && !*abort) {
     tc_fence_after();
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     const int row = threadIdx.x;
@@ -90,6 +92,7 @@ __global__ void __launch_bounds__(128, 1)
   __syncthreads();
   report_abort(abort, err);
   if (warp == 0) {
+    __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, 128);
   }
