@@ -69,7 +69,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -155,8 +155,9 @@ def cpu_baseline(rows: int, head: int = 0):
     fl = 3.5 * flops_fwd(1, rows, SHAPE["n"], 1, SHAPE["d"])
     return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": torch.get_num_threads(),
             "kind": "oracle", "seconds": dt,
-            "sample": f"query rows 0..{rows - 1} of head {head} against all {SHAPE['n']} keys, "
-                      "fwd+bwd in float64 (counted FLOPs of that slice)"}
+            "sample": f"query rows 0..{rows - 1} of head {head} (of 12) against all "
+                      f"{SHAPE['n']} keys, fwd+bwd in float64; value = counted FLOPs of that "
+                      "slice / its time"}
 
 
 def run_reference(args):
@@ -355,10 +356,10 @@ def run_ours(args):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--cpu-rows", type=int, default=2048)
+    ap.add_argument("--cpu-rows", type=int, default=25088)
     ap.add_argument("--ref-rows", type=int, default=512)
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     ap.add_argument("--skip-quantizer", action="store_true")
