@@ -159,6 +159,31 @@ nvq_status attn_qat_bwd(const void* q, const void* k, const void* v, const void*
                         int B, int Nq, int Nkv, int H, int D, float scale, int causal,
                         void* ws, size_t ws_bytes, nvq_stream_t stream);
 
+/*
+ * attn_qat_bwd with no caller-provided workspace and no allocation.  The paper
+ * has no counterpart: this entry point exists for callers that cannot allocate
+ * device memory, e.g. code running inside a host framework that owns all
+ * device memory through its own pool and hands plug-ins no allocator, or code
+ * on a latency-critical path where cudaMalloc/cudaFree would synchronize the
+ * device.  Arguments and results are those of attn_qat_bwd minus ws/ws_bytes.
+ *
+ * Scratch comes from one 32 MiB array inside the library (held by every GPU
+ * that loads the library until the process exits).  A problem whose
+ * attn_qat_bwd_workspace(B, Nq, Nkv, H, D) exceeds 32 MiB is rejected with
+ * NVQ_ERR_WORKSPACE before anything is launched.  The first call on a device
+ * looks up the array's device address (cudaGetSymbolAddress) with that device
+ * current; make that first call before any stream capture.  Every call shares
+ * the one array: calls whose work overlaps on the GPU (other streams, other
+ * host threads) race and corrupt each other's results.  Each call starts by
+ * zeroing the part of the array that must start at zero (the dQ accumulator)
+ * and overwrites the rest, so the previous call's contents do not matter.
+ */
+nvq_status attn_qat_bwd_builtin_scratch(const void* q, const void* k, const void* v,
+                                        const void* o, const float* stats, const void* dout,
+                                        void* dq, void* dk, void* dv, int B, int Nq, int Nkv,
+                                        int H, int D, float scale, int causal,
+                                        nvq_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* Self-tests of the hardware encodings the kernels rely on (no paper       */
 /* counterpart; used by the GPU tests)                                      */

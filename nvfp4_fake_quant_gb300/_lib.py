@@ -35,6 +35,9 @@ SIGNATURES = {
     "attn_qat_bwd": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                              c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_float, c_int,
                              c_void_p, c_size_t, c_void_p]),
+    "attn_qat_bwd_builtin_scratch": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                             c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int,
+                                             c_int, c_int, c_int, c_float, c_int, c_void_p]),
     "nvq_selftest_umma": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int,
                                   c_void_p]),
     "nvq_selftest_timeout": (c_int, [c_int64, c_void_p]),

@@ -1,0 +1,62 @@
+// attn_qat_bwd_builtin_scratch: the straight-through backward with its scratch
+// memory taken from a fixed array that lives inside this library, for callers
+// that cannot allocate device memory themselves.  Typical such callers run
+// inside a host framework that owns every byte of device memory through its
+// own pool and gives plug-in code no allocator, or sit on a latency-critical
+// path where cudaMalloc/cudaFree would synchronize the whole device.
+//
+// The array (kBuiltinScratchBytes) is part of this library's device image:
+// every GPU that loads the library holds it until the process exits.  In host
+// code the array's name is only a host-side stand-in, so its device address is
+// looked up with cudaGetSymbolAddress, once per device, with that device
+// current, on the first call made on that device.
+#include <mutex>
+
+#include <cuda_runtime.h>
+
+#include "nvfp4attn.h"
+
+namespace {
+
+constexpr size_t kBuiltinScratchBytes = size_t(32) << 20;  // 32 MiB
+constexpr int kMaxDevices = 64;
+
+static __device__ __align__(256) unsigned char g_bwd_scratch[kBuiltinScratchBytes];
+
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of g_bwd_scratch on the current device (first call per device
+// performs the lookup).
+nvq_status scratch_address(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return NVQ_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (g_scratch_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_bwd_scratch) != cudaSuccess || p == nullptr)
+      return NVQ_ERR_CUDA;
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return NVQ_OK;
+}
+
+}  // namespace
+
+extern "C" nvq_status attn_qat_bwd_builtin_scratch(const void* q, const void* k, const void* v,
+                                                   const void* o, const float* stats,
+                                                   const void* dout, void* dq, void* dk, void* dv,
+                                                   int B, int Nq, int Nkv, int H, int D,
+                                                   float scale, int causal, nvq_stream_t stream) {
+  const size_t need = attn_qat_bwd_workspace(B, Nq, Nkv, H, D);
+  if (need == 0) return NVQ_ERR_INVALID;
+  if (need > kBuiltinScratchBytes) return NVQ_ERR_WORKSPACE;  // problem too large for the array
+  void* ws = nullptr;
+  const nvq_status st = scratch_address(&ws);
+  if (st != NVQ_OK) return st;
+  // The scratch needs no clearing here: the backward overwrites the quantized
+  // copies and delta, and its first kernel zeroes the fp32 dQ accumulator.
+  return attn_qat_bwd(q, k, v, o, stats, dout, dq, dk, dv, B, Nq, Nkv, H, D, scale, causal, ws,
+                      kBuiltinScratchBytes, stream);
+}
