@@ -32,27 +32,12 @@ namespace nvq {
 
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kElemThreads = 256;  // two elementwise warpgroups
+constexpr int kTmaWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreads = 320;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint32_t kAtomBlock = 128u * 128u;
-
-template <int D>
-struct BwdLayout {
-  static constexpr uint32_t kTileBytes = 128u * D * 2u;
-  static constexpr uint32_t kK = 0;
-  static constexpr uint32_t kV = kK + kTileBytes;
-  static constexpr uint32_t kQ = kV + kTileBytes;
-  static constexpr uint32_t kDO = kQ + kTileBytes;
-  static constexpr uint32_t kPT = kDO + kTileBytes;  // P~/l, [128 q][128 keys] bf16
-  static constexpr uint32_t kDS = kPT + 128u * 128u * 2u;
-  static constexpr uint32_t kBars = kDS + 128u * 128u * 2u;
-  static constexpr uint32_t kNumBars = 9;
-  static constexpr uint32_t kTmemSlot = kBars + kNumBars * 8u;
-  static constexpr uint32_t kAbort = kTmemSlot + 4u;
-  static constexpr uint32_t kUsed = kAbort + 4u;
-  static constexpr uint32_t kAlloc =
-      (kUsed + 1024u) > 150u * 1024u ? (kUsed + 1024u) : 150u * 1024u;
-};
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -70,6 +55,24 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
 }
+
+template <int D>
+struct BwdLayout {
+  static constexpr uint32_t kTileBytes = 128u * D * 2u;
+  static constexpr uint32_t kK = 0;
+  static constexpr uint32_t kV = kK + kTileBytes;
+  static constexpr uint32_t kQ = kV + kTileBytes;        // [2] stages
+  static constexpr uint32_t kDO = kQ + 2u * kTileBytes;  // [2] stages
+  static constexpr uint32_t kPD = kDO + 2u * kTileBytes; // P~/l, then dS: [128 q][128 keys] bf16
+  static constexpr uint32_t kBars = kPD + 128u * 128u * 2u;
+  static constexpr uint32_t kNumBars = 16;
+  static constexpr uint32_t kStats = kBars + kNumBars * 8u;  // unused padding slot
+  static constexpr uint32_t kTmemSlot = kStats + 8u;
+  static constexpr uint32_t kAbort = kTmemSlot + 4u;
+  static constexpr uint32_t kUsed = kAbort + 4u;
+  static constexpr uint32_t kAlloc =
+      (kUsed + 1024u) > 150u * 1024u ? (kUsed + 1024u) : 150u * 1024u;
+};
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -90,14 +93,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBars);
   uint64_t* kv_full = bars + 0;
-  uint64_t* qdo_full = bars + 1;
-  uint64_t* qdo_empty = bars + 2;
-  uint64_t* s_full = bars + 3;
-  uint64_t* ds_full = bars + 4;
-  uint64_t* mma2_done = bars + 5;
-  uint64_t* dq_free = bars + 6;
-  uint64_t* dkdv_done = bars + 7;
-  uint64_t* mma_drain = bars + 8;
+  uint64_t* qdo_full = bars + 1;   // [2]
+  uint64_t* qdo_empty = bars + 3;  // [2]
+  uint64_t* s_full = bars + 5;
+  uint64_t* dp_full = bars + 6;
+  uint64_t* pt_full = bars + 7;
+  uint64_t* pt_free = bars + 8;
+  uint64_t* ds_full = bars + 9;
+  uint64_t* dq_full = bars + 10;
+  uint64_t* dq_free = bars + 11;
+  uint64_t* dkdv_done = bars + 12;
+  uint64_t* mma_drain = bars + 13;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kAbort);
 
@@ -108,17 +114,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     *abort = 0;
     mbar_init(kv_full, 1);
-    mbar_init(qdo_full, 1);
-    mbar_init(qdo_empty, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&qdo_full[s], 1);
+      mbar_init(&qdo_empty[s], 1);
+    }
     mbar_init(s_full, 1);
-    mbar_init(ds_full, 128);
-    mbar_init(mma2_done, 1);
-    mbar_init(dq_free, 128);
+    mbar_init(dp_full, 1);
+    mbar_init(pt_full, kElemThreads);
+    mbar_init(pt_free, 1);
+    mbar_init(ds_full, kElemThreads);
+    mbar_init(dq_full, 1);
+    mbar_init(dq_free, kElemThreads);
     mbar_init(dkdv_done, 1);
     mbar_init(mma_drain, 1);
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
@@ -127,7 +138,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 4) {
+  if (warp == kTmaWarp) {
+    // ------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_desc(&tq);
       tma_prefetch_desc(&tk);
@@ -139,25 +151,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_4d(smem + L::kK + blk * kAtomBlock, &tk, blk * 64, k0, h, b, kv_full);
         tma_load_4d(smem + L::kV + blk * kAtomBlock, &tv, blk * 64, k0, h, b, kv_full);
       }
-      int last = -1;
+      int last[2] = {-1, -1};
       bool ok = true;
       for (int it = 0; it < n_iter; ++it) {
-        if (!(ok = mbar_wait(qdo_empty, (it & 1) ^ 1, abort))) break;
+        const int st = it & 1;
+        if (!(ok = mbar_wait(&qdo_empty[st], ((it >> 1) & 1) ^ 1, abort))) break;
         const int qrow0 = (i_begin + it) * kTile;
-        mbar_arrive_expect_tx(qdo_full, 2u * L::kTileBytes);
+        mbar_arrive_expect_tx(&qdo_full[st], 2u * L::kTileBytes);
 #pragma unroll
         for (int blk = 0; blk < D / 64; ++blk) {
-          tma_load_4d(smem + L::kQ + blk * kAtomBlock, &tq, blk * 64, qrow0, h, b, qdo_full);
-          tma_load_4d(smem + L::kDO + blk * kAtomBlock, &tdo, blk * 64, qrow0, h, b, qdo_full);
+          tma_load_4d(smem + L::kQ + st * L::kTileBytes + blk * kAtomBlock, &tq, blk * 64, qrow0,
+                      h, b, &qdo_full[st]);
+          tma_load_4d(smem + L::kDO + st * L::kTileBytes + blk * kAtomBlock, &tdo, blk * 64,
+                      qrow0, h, b, &qdo_full[st]);
         }
-        last = it & 1;
+        last[st] = (it >> 1) & 1;
       }
       if (!ok) {
         mbar_wait(kv_full, 0, nullptr, 10000000ull);
-        if (last >= 0) mbar_wait(qdo_full, static_cast<uint32_t>(last), nullptr, 10000000ull);
+        for (int s2 = 0; s2 < 2; ++s2)
+          if (last[s2] >= 0)
+            mbar_wait(&qdo_full[s2], static_cast<uint32_t>(last[s2]), nullptr, 10000000ull);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == kMmaWarp) {
+    // ---------------------------------------------------------------- MMA
+    // Issue order per query tile i: dV_i, S_{i+1}, dK_i, dQ_i, dP_{i+1}, so the
+    // elementwise work of one tile overlaps the UMMAs of its neighbours.
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_f16(128, 128, 1, 0, 0);  // S, dP
       constexpr uint32_t idesc_t = idesc_f16(128, D, 1, 1, 1);    // dV, dK (A, B MN-major)
@@ -166,163 +186,234 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t v_addr = smem_u32(smem + L::kV);
       const uint32_t q_addr = smem_u32(smem + L::kQ);
       const uint32_t do_addr = smem_u32(smem + L::kDO);
-      const uint32_t pt_addr = smem_u32(smem + L::kPT);
-      const uint32_t ds_addr = smem_u32(smem + L::kDS);
-      bool ok = mbar_wait(kv_full, 0, abort);
-      for (int it = 0; it < n_iter && ok; ++it) {
-        if (!(ok = mbar_wait(qdo_full, it & 1, abort))) break;
-        if (it > 0 && !(ok = mbar_wait(dq_free, (it - 1) & 1, abort))) break;
-        tc_fence_after();
+      const uint32_t pd_addr = smem_u32(smem + L::kPD);
+      auto issue_s = [&](int st) {  // S = Q~_st K~^T -> TMEM [0,128)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kAtomBlock + (kk & 3) * 32;
-          umma_f16_ss(tmem + 0, sdesc_sw128(q_addr + off, 16, 1024),
+          umma_f16_ss(tmem + 0, sdesc_sw128(q_addr + st * L::kTileBytes + off, 16, 1024),
                       sdesc_sw128(k_addr + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
         }
+        umma_commit(s_full);
+      };
+      auto issue_dp = [&](int st) {  // dP = dO_st V~^T -> TMEM [128,256)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kAtomBlock + (kk & 3) * 32;
-          umma_f16_ss(tmem + 128, sdesc_sw128(do_addr + off, 16, 1024),
+          umma_f16_ss(tmem + 128, sdesc_sw128(do_addr + st * L::kTileBytes + off, 16, 1024),
                       sdesc_sw128(v_addr + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
         }
-        umma_commit(s_full);
-        if (!(ok = mbar_wait(ds_full, it & 1, abort))) break;
+        umma_commit(dp_full);
+      };
+      bool ok = mbar_wait(kv_full, 0, abort) && (n_iter > 0) && mbar_wait(&qdo_full[0], 0, abort);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0);
+        issue_dp(0);
+      }
+      for (int it = 0; it < n_iter && ok; ++it) {
+        const int st = it & 1;
+        const uint32_t ph = static_cast<uint32_t>(it & 1);
+        if (!(ok = mbar_wait(pt_full, ph, abort))) break;
         tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {  // contraction over 128 queries, 16 per UMMA
-          const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
-          umma_f16_ss(tmem + 256, sdesc_sw128(pt_addr + kk * 2048, kAtomBlock, 1024),
-                      sdesc_sw128(do_addr + kk * 2048, kAtomBlock, 1024), idesc_t, acc);
-          umma_f16_ss(tmem + 384, sdesc_sw128(ds_addr + kk * 2048, kAtomBlock, 1024),
-                      sdesc_sw128(q_addr + kk * 2048, kAtomBlock, 1024), idesc_t, acc);
+        for (int kk = 0; kk < 8; ++kk)  // dV += (P~/l)^T dO: contraction over 128 queries
+          umma_f16_ss(tmem + 256, sdesc_sw128(pd_addr + kk * 2048, kAtomBlock, 1024),
+                      sdesc_sw128(do_addr + st * L::kTileBytes + kk * 2048, kAtomBlock, 1024),
+                      idesc_t, (it > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(pt_free);
+        if (it + 1 < n_iter) {
+          if (!(ok = mbar_wait(&qdo_full[st ^ 1], static_cast<uint32_t>(((it + 1) >> 1) & 1), abort)))
+            break;
+          tc_fence_after();
+          issue_s(st ^ 1);
         }
+        if (!(ok = mbar_wait(ds_full, ph, abort))) break;
+        tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {  // contraction over 128 keys
+        for (int kk = 0; kk < 8; ++kk)  // dK += dS^T Q~: contraction over 128 queries
+          umma_f16_ss(tmem + 384, sdesc_sw128(pd_addr + kk * 2048, kAtomBlock, 1024),
+                      sdesc_sw128(q_addr + st * L::kTileBytes + kk * 2048, kAtomBlock, 1024),
+                      idesc_t, (it > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {  // dQ_i = dS K~: contraction over 128 keys
           const uint32_t aoff = (kk >> 2) * kAtomBlock + (kk & 3) * 32;
-          umma_f16_ss(tmem + 0, sdesc_sw128(ds_addr + aoff, 16, 1024),
+          umma_f16_ss(tmem + 128, sdesc_sw128(pd_addr + aoff, 16, 1024),
                       sdesc_sw128(k_addr + kk * 2048, kAtomBlock, 1024), idesc_q,
                       kk > 0 ? 1u : 0u);
         }
-        umma_commit(mma2_done);
-        umma_commit(qdo_empty);
+        umma_commit(dq_full);
+        umma_commit(&qdo_empty[st]);
+        if (it + 1 < n_iter) {
+          if (!(ok = mbar_wait(dq_free, ph, abort))) break;
+          tc_fence_after();
+          issue_dp(st ^ 1);
+        }
       }
-      if (ok) umma_commit(dkdv_done);
+      if (ok && n_iter > 0) umma_commit(dkdv_done);
       umma_commit(mma_drain);
       mbar_wait(mma_drain, 0, nullptr, 10000000ull);
     }
   } else {
-    const int t = threadIdx.x;
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    // --------------------------------------------------------- elementwise
+    // Warpgroup g (0/1) owns keys [64g, 64g+64) of every tile and dQ columns
+    // [g*D/2, (g+1)*D/2); thread t of the group owns query row t (TMEM lane t).
+    const int g = warp >> 2;
+    const int t = threadIdx.x & 127;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const float c1 = scale * kLog2e;
-    uint8_t* pt_smem = smem + L::kPT;
-    uint8_t* ds_smem = smem + L::kDS;
+    uint8_t* pd_smem = smem + L::kPD;
     const float* lse_g = stats + (static_cast<int64_t>(b) * H + h) * 2 * Nq;
     const float* m_g = lse_g + Nq;
     const float* delta_g = delta + (static_cast<int64_t>(b) * H + h) * Nq;
+    constexpr int kDqCols = D / 2;
     bool ok = true;
-    uint32_t rs[32], rd[32];
+    uint32_t r[32];
+    // statistics of this thread's row, prefetched one tile ahead
+    auto load_row = [&](int it, float& m, float& lse, float& dl) {
+      const int qrow = (i_begin + it) * kTile + t;
+      const bool in = it < n_iter && qrow < Nq;
+      m = in ? m_g[qrow] : 0.f;
+      lse = in ? lse_g[qrow] : 0.f;
+      dl = in ? delta_g[qrow] : 0.f;
+    };
+    float nm, nlse, ndl;
+    load_row(0, nm, nlse, ndl);
+    auto read_dq = [&](int it_prev) {  // dQ of tile it_prev: TMEM [128, 128+D) -> fp32 accumulator
+      const int qrow = (i_begin + it_prev) * kTile + t;
+      float* dqrow = dq_acc + ((static_cast<int64_t>(b) * Nq + qrow) * H + h) * D + g * kDqCols;
+#pragma unroll
+      for (int c = 0; c < kDqCols / 32; ++c) {
+        tmem_ld32(tmem + lane_base + 128 + g * kDqCols + c * 32, r);
+        tmem_wait_ld();
+        if (qrow < Nq) {
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            red_add_v4(dqrow + c * 32 + 4 * u, __uint_as_float(r[4 * u]) * scale,
+                       __uint_as_float(r[4 * u + 1]) * scale, __uint_as_float(r[4 * u + 2]) * scale,
+                       __uint_as_float(r[4 * u + 3]) * scale);
+        }
+      }
+    };
     for (int it = 0; it < n_iter && ok; ++it) {
       const int qi = i_begin + it;
       const int qrow = qi * kTile + t;
       const bool row_ok = qrow < Nq;
-      const float m = row_ok ? m_g[qrow] : 0.f;
-      const float lse = row_ok ? lse_g[qrow] : 0.f;
-      const float dl = row_ok ? delta_g[qrow] : 0.f;
-      const float mb = m * kLog2e;
+      const float m = nm, lse = nlse, dl = ndl;
+      load_row(it + 1, nm, nlse, ndl);
+      const float negmb = -m * kLog2e;
+      const uint64_t c12 = pk2(c1, c1), nmb2 = pk2(negmb, negmb);
       const float inv_l = ex2((m - lse) * kLog2e);  // 1 / l
-      const bool edge = !row_ok || (k0 + kTile > Nkv) || (causal && qi == kt) ||
-                        (qi * kTile + kTile > Nq);
-      if (!(ok = mbar_wait_warp(s_full, it & 1, abort))) break;
+      const bool edge = !row_ok || (k0 + kTile > Nkv) || (causal && qi == kt);
+      const uint32_t ph = static_cast<uint32_t>(it & 1);
+      // ---- P part: S -> P, P~/l
+      if (!(ok = mbar_wait_warp(s_full, ph, abort))) break;
       tc_fence_after();
+      float p[64];       // P for this thread's 64 keys
+      uint32_t ptw[32];  // P~ / l as bf16x2
+      const uint64_t il2 = pk2(inv_l, inv_l);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        tmem_ld32(tmem + lane_base + c * 32, rs);
-        tmem_ld32(tmem + lane_base + 128 + c * 32, rd);
+      for (int c = 0; c < 2; ++c) {
+        tmem_ld32(tmem + lane_base + g * 64 + c * 32, r);
         tmem_wait_ld();
-        float p[32];
+        float x[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          float pv = ex2(fmaf(__uint_as_float(rs[i]), c1, -mb));
-          if (edge) {
-            const int key = k0 + c * 32 + i;
-            if (!(row_ok && key < Nkv && (!causal || key <= qrow))) pv = 0.f;
+        for (int i = 0; i < 16; ++i)
+          up2(fma2(pk2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), c12, nmb2),
+              x[2 * i], x[2 * i + 1]);
+        if (edge) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int key = k0 + g * 64 + c * 32 + i;
+            if (!(row_ok && key < Nkv && (!causal || key <= qrow))) x[i] = -INFINITY;
           }
-          p[i] = pv;
         }
-        uint32_t ptw[16], dsw[16];
 #pragma unroll
         for (int hb = 0; hb < 2; ++hb) {
-          uint32_t q8[8];
-          quant16_p(p + 16 * hb, q8);
+          float pp[16];
+          uint32_t pt[8];
+          pquant16(x + 16 * hb, pp, pt);
+#pragma unroll
+          for (int u = 0; u < 16; ++u) p[c * 32 + hb * 16 + u] = pp[u];
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
-            const float lo = f16lo_to_f32(q8[u]) * inv_l;
-            const float hi = f16lo_to_f32(q8[u] >> 16) * inv_l;
-            ptw[8 * hb + u] = pack_bf16(lo, hi);
+            float a0, a1;
+            up2(mul2(pk2(f16lo_to_f32(pt[u]), f16hi_to_f32(pt[u])), il2), a0, a1);
+            ptw[c * 16 + hb * 8 + u] = pack_bf16(a0, a1);
           }
         }
+      }
+      tc_fence_before();
+      // the P~/dS buffer is free once dK and dQ of the previous tile are done
+      if (it > 0 && !(ok = mbar_wait_warp(dq_full, ph ^ 1u, abort))) break;
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch) {
+        const uint32_t off = sw128_offset(t, g * 64 + ch * 8, 128);
+        *reinterpret_cast<uint4*>(pd_smem + off) =
+            make_uint4(ptw[4 * ch], ptw[4 * ch + 1], ptw[4 * ch + 2], ptw[4 * ch + 3]);
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(pt_full);
+      // ---- dQ of the previous tile
+      if (it > 0) {
+        tc_fence_after();
+        read_dq(it - 1);
+        tc_fence_before();
+        mbar_arrive(dq_free);
+      }
+      // ---- dS part: dP -> dS = A * (dP - delta), A = P / l
+      if (!(ok = mbar_wait_warp(dp_full, ph, abort))) break;
+      tc_fence_after();
+      uint32_t dsw[32];
+      const uint64_t ndl2 = pk2(-dl, -dl);
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        tmem_ld32(tmem + lane_base + 128 + g * 64 + c * 32, r);
+        tmem_wait_ld();
 #pragma unroll
         for (int u = 0; u < 16; ++u) {
-          const float a0 = p[2 * u] * inv_l, a1 = p[2 * u + 1] * inv_l;
-          const float d0 = a0 * (__uint_as_float(rd[2 * u]) - dl);
-          const float d1 = a1 * (__uint_as_float(rd[2 * u + 1]) - dl);
-          dsw[u] = pack_bf16(d0, d1);
-        }
-#pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-          const uint32_t off = sw128_offset(t, c * 32 + ch * 8, 128);
-          *reinterpret_cast<uint4*>(pt_smem + off) =
-              make_uint4(ptw[4 * ch], ptw[4 * ch + 1], ptw[4 * ch + 2], ptw[4 * ch + 3]);
-          *reinterpret_cast<uint4*>(ds_smem + off) =
-              make_uint4(dsw[4 * ch], dsw[4 * ch + 1], dsw[4 * ch + 2], dsw[4 * ch + 3]);
+          const uint64_t a2 = mul2(pk2(p[c * 32 + 2 * u], p[c * 32 + 2 * u + 1]), il2);  // A = P / l
+          const uint64_t d2 = add2(pk2(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1])), ndl2);
+          float d0, d1;
+          up2(mul2(a2, d2), d0, d1);
+          dsw[c * 16 + u] = pack_bf16(d0, d1);
         }
       }
       tc_fence_before();
+      if (!(ok = mbar_wait_warp(pt_free, ph, abort))) break;
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch) {
+        const uint32_t off = sw128_offset(t, g * 64 + ch * 8, 128);
+        *reinterpret_cast<uint4*>(pd_smem + off) =
+            make_uint4(dsw[4 * ch], dsw[4 * ch + 1], dsw[4 * ch + 2], dsw[4 * ch + 3]);
+      }
       fence_proxy_async_smem();
       mbar_arrive(ds_full);
-      if (!(ok = mbar_wait_warp(mma2_done, it & 1, abort))) break;
+    }
+    if (ok && n_iter > 0 && (ok = mbar_wait_warp(dq_full, static_cast<uint32_t>((n_iter - 1) & 1), abort))) {
       tc_fence_after();
-      float* dqrow = dq_acc + ((static_cast<int64_t>(b) * Nq + qrow) * H + h) * D;
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        tmem_ld32(tmem + lane_base + c * 32, rs);
-        tmem_wait_ld();
-        if (row_ok) {
-#pragma unroll
-          for (int u = 0; u < 8; ++u)
-            red_add_v4(dqrow + c * 32 + 4 * u, __uint_as_float(rs[4 * u]) * scale,
-                       __uint_as_float(rs[4 * u + 1]) * scale,
-                       __uint_as_float(rs[4 * u + 2]) * scale,
-                       __uint_as_float(rs[4 * u + 3]) * scale);
-        }
-      }
-      tc_fence_before();
-      mbar_arrive(dq_free);
+      read_dq(n_iter - 1);
     }
     if (ok && n_iter > 0 && (ok = mbar_wait_warp(dkdv_done, 0, abort))) {
       tc_fence_after();
+      // group 0 writes dV, group 1 writes dK (scaled); thread t = key row t
       const int key = k0 + t;
       const int64_t base = ((static_cast<int64_t>(b) * Nkv + key) * H + h) * D;
+      __nv_bfloat16* dst = g == 0 ? dv : dk;
+      const float mul = g == 0 ? 1.0f : scale;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
-        tmem_ld32(tmem + lane_base + 256 + c * 32, rs);
-        tmem_ld32(tmem + lane_base + 384 + c * 32, rd);
+        tmem_ld32(tmem + lane_base + (g == 0 ? 256 : 384) + c * 32, r);
         tmem_wait_ld();
         if (key < Nkv) {
-          uint32_t wv[16], wk[16];
+          uint32_t w[16];
 #pragma unroll
-          for (int u = 0; u < 16; ++u) {
-            wv[u] = pack_bf16(__uint_as_float(rs[2 * u]), __uint_as_float(rs[2 * u + 1]));
-            wk[u] = pack_bf16(__uint_as_float(rd[2 * u]) * scale,
-                              __uint_as_float(rd[2 * u + 1]) * scale);
-          }
-          uint4* pv = reinterpret_cast<uint4*>(dv + base + c * 32);
-          uint4* pk = reinterpret_cast<uint4*>(dk + base + c * 32);
+          for (int u = 0; u < 16; ++u)
+            w[u] = pack_bf16(__uint_as_float(r[2 * u]) * mul, __uint_as_float(r[2 * u + 1]) * mul);
+          uint4* pw = reinterpret_cast<uint4*>(dst + base + c * 32);
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            pv[u] = make_uint4(wv[4 * u], wv[4 * u + 1], wv[4 * u + 2], wv[4 * u + 3]);
-            pk[u] = make_uint4(wk[4 * u], wk[4 * u + 1], wk[4 * u + 2], wk[4 * u + 3]);
-          }
+          for (int u = 0; u < 4; ++u)
+            pw[u] = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
         }
       }
     } else if (ok && n_iter == 0) {
@@ -330,10 +421,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int key = k0 + t;
       if (key < Nkv) {
         const int64_t base = ((static_cast<int64_t>(b) * Nkv + key) * H + h) * D;
-        for (int c = 0; c < D; c += 8) {
-          *reinterpret_cast<uint4*>(dv + base + c) = make_uint4(0, 0, 0, 0);
-          *reinterpret_cast<uint4*>(dk + base + c) = make_uint4(0, 0, 0, 0);
-        }
+        __nv_bfloat16* dst = g == 0 ? dv : dk;
+        for (int c = 0; c < D; c += 8)
+          *reinterpret_cast<uint4*>(dst + base + c) = make_uint4(0, 0, 0, 0);
       }
     }
   }
@@ -341,7 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   report_abort(abort, err);
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, 512);

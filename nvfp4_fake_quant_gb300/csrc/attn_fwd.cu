@@ -31,35 +31,39 @@ namespace nvq {
 
 namespace {
 
-constexpr int kThreads = 192;
-constexpr int kStages = 2;
+constexpr int kSoftmaxThreads = 128;  // one warpgroup per query tile
+constexpr int kTmaWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kThreads = 320;
+constexpr int kRing = 3;  // K/V tile ring (K and V tiles interleave in pass 2)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint32_t kAtomBlock = 128u * 128u;  // bytes of one 64-column block of a 128-row tile
 
 template <int D>
 struct FwdLayout {
   static constexpr uint32_t kTileBytes = 128u * D * 2u;
-  static constexpr uint32_t kQ = 0;
-  static constexpr uint32_t kK = kQ + kTileBytes;
-  static constexpr uint32_t kV = kK + kStages * kTileBytes;
-  static constexpr uint32_t kP = kV + kStages * kTileBytes;
-  static constexpr uint32_t kBars = kP + 128u * 128u * 2u;
-  static constexpr uint32_t kNumBars = 17;
+  static constexpr uint32_t kQ = 0;                          // [2] query tiles
+  static constexpr uint32_t kP = kQ + 2u * kTileBytes;       // [2] P~ tiles, 128 x 128 f16
+  static constexpr uint32_t kRingOff = kP + 2u * 128u * 128u * 2u;
+  static constexpr uint32_t kBars = kRingOff + kRing * kTileBytes;
+  static constexpr uint32_t kNumBars = 1 + 2 * kRing + 2 * 4 + 1;
   static constexpr uint32_t kTmemSlot = kBars + kNumBars * 8u;
   static constexpr uint32_t kAbort = kTmemSlot + 4u;
   static constexpr uint32_t kUsed = kAbort + 4u;
-  // >= 1024 slack for aligning the base; at least ~150 KB so that one CTA
-  // (and its 512 TMEM columns) owns an SM.
   static constexpr uint32_t kAlloc =
       (kUsed + 1024u) > 150u * 1024u ? (kUsed + 1024u) : 150u * 1024u;
 };
 
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
 }
 
+// Grid: (ceil(Nq / 256), H, B).  Each CTA owns two 128-query tiles; softmax
+// warpgroup i (warps 4i..4i+3) owns tile i.  TMEM: S_i at [128 i, 128 i + 128),
+// O_i at [256 + 128 i, 256 + 128 i + D).  The UMMA warp ping-pongs the two
+// tiles so that one warpgroup's softmax overlaps the other's UMMAs.
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
@@ -72,45 +76,43 @@ __global__ void __launch_bounds__(kThreads, 1)
                                              ~static_cast<uintptr_t>(1023u));
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  const int q0 = qt * kTile;
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int q0 = blockIdx.x * 2 * kTile;
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBars);
   uint64_t* q_full = bars + 0;
-  uint64_t* k_full = bars + 1;    // [2]
-  uint64_t* k_empty = bars + 3;   // [2]
-  uint64_t* v_full = bars + 5;    // [2]
-  uint64_t* v_empty = bars + 7;   // [2]
-  uint64_t* s_full = bars + 9;    // [2]
-  uint64_t* s_empty = bars + 11;  // [2]
-  uint64_t* p_full = bars + 13;
-  uint64_t* pv_done = bars + 14;
-  uint64_t* o_full = bars + 15;
-  uint64_t* mma_drain = bars + 16;
+  uint64_t* r_full = bars + 1;              // [kRing]
+  uint64_t* r_empty = bars + 1 + kRing;     // [kRing]
+  uint64_t* s_full = bars + 1 + 2 * kRing;  // [2]
+  uint64_t* s_free = s_full + 2;            // [2]
+  uint64_t* p_full = s_full + 4;            // [2]
+  uint64_t* o_full = s_full + 6;            // [2]
+  uint64_t* mma_drain = s_full + 8;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kAbort);
 
   const int n_kv_all = (Nkv + kTile - 1) / kTile;
-  const int n_kv = causal ? min(n_kv_all, qt + 1) : n_kv_all;
+  // causal: the second query tile sees one more key tile than the first; both
+  // run over it (the first tile's part of it is fully masked)
+  const int n_kv = causal ? min(n_kv_all, 2 * static_cast<int>(blockIdx.x) + 2) : n_kv_all;
 
   if (threadIdx.x == 0) {
     *abort = 0;
     mbar_init(q_full, 1);
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&k_full[s], 1);
-      mbar_init(&k_empty[s], 1);
-      mbar_init(&v_full[s], 1);
-      mbar_init(&v_empty[s], 1);
-      mbar_init(&s_full[s], 1);
-      mbar_init(&s_empty[s], 128);
+    for (int s = 0; s < kRing; ++s) {
+      mbar_init(&r_full[s], 1);
+      mbar_init(&r_empty[s], 1);
     }
-    mbar_init(p_full, 128);
-    mbar_init(pv_done, 1);
-    mbar_init(o_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_free[i], kSoftmaxThreads);
+      mbar_init(&p_full[i], kSoftmaxThreads);
+      mbar_init(&o_full[i], 1);
+    }
     mbar_init(mma_drain, 1);
     fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
   }
@@ -119,132 +121,145 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 4) {
+  if (warp == kTmaWarp) {
     // ------------------------------------------------------------ producer
+    // Load order: Q0, Q1; pass 1: K_0..K_{n-1}; pass 2: K_0, V_0, K_1, V_1, ...
     if (lane == 0) {
       tma_prefetch_desc(&tq);
       tma_prefetch_desc(&tk);
       tma_prefetch_desc(&tv);
-      int k_last[2] = {-1, -1}, v_last[2] = {-1, -1};
+      mbar_arrive_expect_tx(q_full, 2u * L::kTileBytes);
+#pragma unroll
+      for (int i = 0; i < 2; ++i)
+#pragma unroll
+        for (int blk = 0; blk < D / 64; ++blk)
+          tma_load_4d(smem + L::kQ + i * L::kTileBytes + blk * kAtomBlock, &tq, blk * 64,
+                      q0 + i * kTile, h, b, q_full);
+      int last[kRing] = {-1, -1, -1};
       bool ok = true;
-      mbar_arrive_expect_tx(q_full, L::kTileBytes);
+      const int total = 3 * n_kv;
+      for (int li = 0; li < total && ok; ++li) {
+        const int slot = li % kRing;
+        const uint32_t use = static_cast<uint32_t>(li / kRing);
+        if (!(ok = mbar_wait(&r_empty[slot], (use & 1u) ^ 1u, abort))) break;
+        const bool is_v = li >= n_kv && ((li - n_kv) & 1);
+        const int j = li < n_kv ? li : (li - n_kv) >> 1;
+        mbar_arrive_expect_tx(&r_full[slot], L::kTileBytes);
 #pragma unroll
-      for (int blk = 0; blk < D / 64; ++blk)
-        tma_load_4d(smem + L::kQ + blk * kAtomBlock, &tq, blk * 64, q0, h, b, q_full);
-      uint32_t kit = 0, vit = 0;
-      for (int pass = 0; pass < 2 && ok; ++pass) {
-        for (int j = 0; j < n_kv && ok; ++j) {
-          const uint32_t st = kit & 1u;
-          if (!(ok = mbar_wait(&k_empty[st], ((kit >> 1) & 1u) ^ 1u, abort))) break;
-          mbar_arrive_expect_tx(&k_full[st], L::kTileBytes);
-#pragma unroll
-          for (int blk = 0; blk < D / 64; ++blk)
-            tma_load_4d(smem + L::kK + st * L::kTileBytes + blk * kAtomBlock, &tk, blk * 64,
-                        j * kTile, h, b, &k_full[st]);
-          k_last[st] = static_cast<int>((kit >> 1) & 1u);
-          ++kit;
-          if (pass == 1) {
-            const uint32_t vs = vit & 1u;
-            if (!(ok = mbar_wait(&v_empty[vs], ((vit >> 1) & 1u) ^ 1u, abort))) break;
-            mbar_arrive_expect_tx(&v_full[vs], L::kTileBytes);
-#pragma unroll
-            for (int blk = 0; blk < D / 64; ++blk)
-              tma_load_4d(smem + L::kV + vs * L::kTileBytes + blk * kAtomBlock, &tv, blk * 64,
-                          j * kTile, h, b, &v_full[vs]);
-            v_last[vs] = static_cast<int>((vit >> 1) & 1u);
-            ++vit;
-          }
-        }
+        for (int blk = 0; blk < D / 64; ++blk)
+          tma_load_4d(smem + L::kRingOff + slot * L::kTileBytes + blk * kAtomBlock,
+                      is_v ? &tv : &tk, blk * 64, j * kTile, h, b, &r_full[slot]);
+        last[slot] = static_cast<int>(use & 1u);
       }
       if (!ok) {
-        // drain copies still in flight before the block leaves
         mbar_wait(q_full, 0, nullptr, 10000000ull);
-        for (int s = 0; s < 2; ++s) {
-          if (k_last[s] >= 0)
-            mbar_wait(&k_full[s], static_cast<uint32_t>(k_last[s]), nullptr, 10000000ull);
-          if (v_last[s] >= 0)
-            mbar_wait(&v_full[s], static_cast<uint32_t>(v_last[s]), nullptr, 10000000ull);
-        }
+        for (int s = 0; s < kRing; ++s)
+          if (last[s] >= 0) mbar_wait(&r_full[s], static_cast<uint32_t>(last[s]), nullptr, 10000000ull);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------------- MMA
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_f16(128, 128, 1, 0, 0);
       constexpr uint32_t idesc_pv = idesc_f16(128, D, 0, 0, 1);
       const uint32_t q_addr = smem_u32(smem + L::kQ);
-      const uint32_t k_addr = smem_u32(smem + L::kK);
-      const uint32_t v_addr = smem_u32(smem + L::kV);
       const uint32_t p_addr = smem_u32(smem + L::kP);
-      uint32_t kit = 0, sc = 0, vit = 0;
-      bool ok = mbar_wait(q_full, 0, abort);
-      auto issue_s = [&]() -> bool {
-        const uint32_t st = kit & 1u;
-        if (!mbar_wait(&k_full[st], (kit >> 1) & 1u, abort)) return false;
-        const uint32_t sb = sc & 1u;
-        if (!mbar_wait(&s_empty[sb], ((sc >> 1) & 1u) ^ 1u, abort)) return false;
-        tc_fence_after();
-        const uint32_t kb = k_addr + st * L::kTileBytes;
+      const uint32_t ring_addr = smem_u32(smem + L::kRingOff);
+      int li = 0;  // ring load index being consumed
+      auto wait_slot = [&](int idx) -> bool {
+        return mbar_wait(&r_full[idx % kRing], static_cast<uint32_t>((idx / kRing) & 1), abort);
+      };
+      auto issue_s = [&](int i, int idx) {  // S_i = Q~_i K~^T, K~ in ring slot of load idx
+        const uint32_t kb = ring_addr + (idx % kRing) * L::kTileBytes;
+        const uint32_t qb = q_addr + i * L::kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kAtomBlock + (kk & 3) * 32;
-          umma_f16_ss(tmem + sb * 128, sdesc_sw128(q_addr + off, 16, 1024),
-                      sdesc_sw128(kb + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+          umma_f16_ss(tmem + i * 128, sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
+                      idesc_s, kk > 0 ? 1u : 0u);
         }
-        umma_commit(&s_full[sb]);
-        umma_commit(&k_empty[st]);
-        ++kit;
-        ++sc;
-        return true;
+        umma_commit(&s_full[i]);
       };
-      if (ok) tc_fence_after();
-      for (int j = 0; j < n_kv && ok; ++j) ok = issue_s();  // pass 1
-      if (ok) ok = issue_s();                                 // pass 2, tile 0
-      for (int j = 0; j < n_kv && ok; ++j) {
-        if (j + 1 < n_kv && !(ok = issue_s())) break;
-        if (!(ok = mbar_wait(p_full, j & 1, abort))) break;
-        const uint32_t vs = vit & 1u;
-        if (!(ok = mbar_wait(&v_full[vs], (vit >> 1) & 1u, abort))) break;
-        tc_fence_after();
-        const uint32_t vb = v_addr + vs * L::kTileBytes;
+      auto issue_pv = [&](int i, int idx, bool acc) {  // O_i += P~_i V~, V~ in slot of load idx
+        const uint32_t vb = ring_addr + (idx % kRing) * L::kTileBytes;
+        const uint32_t pb = p_addr + i * 128u * 128u * 2u;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint32_t aoff = (kk >> 2) * kAtomBlock + (kk & 3) * 32;
-          umma_f16_ss(tmem + 256, sdesc_sw128(p_addr + aoff, 16, 1024),
+          umma_f16_ss(tmem + 256 + i * 128, sdesc_sw128(pb + aoff, 16, 1024),
                       sdesc_sw128(vb + kk * 2048, kAtomBlock, 1024), idesc_pv,
-                      (j > 0 || kk > 0) ? 1u : 0u);
+                      (acc || kk > 0) ? 1u : 0u);
         }
-        umma_commit(pv_done);
-        umma_commit(&v_empty[vs]);
-        ++vit;
+      };
+      bool ok = mbar_wait(q_full, 0, abort);
+      // pass 1: S_0(j), S_1(j) for the row maxima
+      for (int j = 0; j < n_kv && ok; ++j, ++li) {
+        if (!(ok = wait_slot(li))) break;
+        for (int i = 0; i < 2 && ok; ++i) {
+          if (j > 0 && !(ok = mbar_wait(&s_free[i], static_cast<uint32_t>((j - 1) & 1), abort))) break;
+          tc_fence_after();
+          issue_s(i, li);
+        }
+        umma_commit(&r_empty[li % kRing]);
       }
-      if (ok) umma_commit(o_full);
+      // pass 2 prologue: S_0(0), S_1(0)
+      if (ok && (ok = wait_slot(li))) {
+        for (int i = 0; i < 2 && ok; ++i) {
+          if (!(ok = mbar_wait(&s_free[i], static_cast<uint32_t>((n_kv - 1) & 1), abort))) break;
+          tc_fence_after();
+          issue_s(i, li);
+        }
+        umma_commit(&r_empty[li % kRing]);
+        ++li;
+      }
+      for (int j = 0; j < n_kv && ok; ++j) {
+        const int vi = li++;  // V_j
+        const int ki = (j + 1 < n_kv) ? li : -1;  // K_{j+1}
+        if (ki >= 0) ++li;
+        if (!(ok = wait_slot(vi))) break;
+        for (int i = 0; i < 2 && ok; ++i) {
+          if (!(ok = mbar_wait(&p_full[i], static_cast<uint32_t>(j & 1), abort))) break;
+          tc_fence_after();
+          issue_pv(i, vi, j > 0);
+          if (i == 1) umma_commit(&r_empty[vi % kRing]);
+          if (ki >= 0) {
+            if (!(ok = wait_slot(ki))) break;
+            issue_s(i, ki);  // S_i(j+1): S_i was read before p_full_i(j)
+            if (i == 1) umma_commit(&r_empty[ki % kRing]);
+          }
+        }
+      }
+      if (ok) {
+        umma_commit(&o_full[0]);
+        umma_commit(&o_full[1]);
+      }
       umma_commit(mma_drain);
       mbar_wait(mma_drain, 0, nullptr, 10000000ull);
     }
   } else {
     // ------------------------------------------------------------ softmax
-    const int t = threadIdx.x;  // 0..127 == query row in tile == TMEM lane
-    const int qrow = q0 + t;
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const int wg = warp >> 2;              // query tile of this warpgroup
+    const int t = threadIdx.x & 127;       // row in the tile == TMEM lane
+    const int qrow = q0 + wg * kTile + t;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t s_col = static_cast<uint32_t>(wg * 128);
     const float c1 = scale * kLog2e;
-    uint8_t* p_smem = smem + L::kP;
-    uint32_t sc = 0;
+    uint8_t* p_smem = smem + L::kP + wg * 128 * 128 * 2;
     bool ok = true;
     float mraw = -INFINITY;
     uint32_t r[32];
+    const int q_last = q0 + wg * kTile + kTile - 1;  // last query row of this tile
     for (int j = 0; j < n_kv && ok; ++j) {
-      const uint32_t sb = sc & 1u;
-      if (!(ok = mbar_wait_warp(&s_full[sb], (sc >> 1) & 1u, abort))) break;
+      if (!(ok = mbar_wait_warp(&s_full[wg], static_cast<uint32_t>(j & 1), abort))) break;
       tc_fence_after();
-      const bool edge = (j * kTile + kTile > Nkv) || (causal && j == qt);
+      const bool edge = (j * kTile + kTile > Nkv) || (causal && j * kTile + kTile - 1 > q0 + wg * kTile);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        tmem_ld32(tmem + lane_base + sb * 128 + c * 32, r);
+        tmem_ld32(tmem + lane_base + s_col + c * 32, r);
         tmem_wait_ld();
         if (!edge) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) mraw = fmaxf(mraw, __uint_as_float(r[i]));
+          for (int i = 0; i < 32; i += 2) mraw = max3(mraw, __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
         } else {
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
@@ -254,60 +269,63 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       tc_fence_before();
-      mbar_arrive(&s_empty[sb]);
-      ++sc;
+      mbar_arrive(&s_free[wg]);
     }
+    (void)q_last;
     const float m = mraw * scale;
-    const float mb = m * kLog2e;
-    float l = 0.f;
+    const float negmb = -m * kLog2e;
+    const uint64_t c12 = pk2(c1, c1), nmb2 = pk2(negmb, negmb);
+    uint64_t l2 = pk2(0.f, 0.f);
     for (int j = 0; j < n_kv && ok; ++j) {
-      const uint32_t sb = sc & 1u;
-      if (!(ok = mbar_wait_warp(&s_full[sb], (sc >> 1) & 1u, abort))) break;
+      if (!(ok = mbar_wait_warp(&s_full[wg], static_cast<uint32_t>((n_kv + j) & 1), abort))) break;
       tc_fence_after();
-      const bool edge = (j * kTile + kTile > Nkv) || (causal && j == qt);
-      uint32_t pk[64];
+      // S_i(j) complete implies PV_i(j-1) complete (issued earlier): the P~ tile is free
+      const bool edge = (j * kTile + kTile > Nkv) || (causal && j * kTile + kTile - 1 > q0 + wg * kTile);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
-        tmem_ld32(tmem + lane_base + sb * 128 + c * 32, r);
+        tmem_ld32(tmem + lane_base + s_col + c * 32, r);
         tmem_wait_ld();
-        float p[32];
+        float x[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          float pv = ex2(fmaf(__uint_as_float(r[i]), c1, -mb));
-          if (edge) {
+        for (int i = 0; i < 16; ++i)
+          up2(fma2(pk2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), c12, nmb2),
+              x[2 * i], x[2 * i + 1]);
+        if (edge) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
             const int key = j * kTile + c * 32 + i;
-            if (!(key < Nkv && (!causal || key <= qrow))) pv = 0.f;
+            if (!(key < Nkv && (!causal || key <= qrow))) x[i] = -INFINITY;
           }
-          p[i] = pv;
-          l += pv;
         }
-        uint32_t q8[8];
-        quant16_p(p, q8);
 #pragma unroll
-        for (int u = 0; u < 8; ++u) pk[c * 16 + u] = q8[u];
-        quant16_p(p + 16, q8);
+        for (int hb = 0; hb < 2; ++hb) {
+          float pp[16];
+          uint32_t pt[8];
+          pquant16(x + 16 * hb, pp, pt);
 #pragma unroll
-        for (int u = 0; u < 8; ++u) pk[c * 16 + 8 + u] = q8[u];
+          for (int u = 0; u < 8; ++u) l2 = add2(l2, pk2(pp[2 * u], pp[2 * u + 1]));
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const uint32_t off = sw128_offset(t, c * 32 + hb * 16 + u * 8, 128);
+            *reinterpret_cast<uint4*>(p_smem + off) =
+                make_uint4(pt[4 * u], pt[4 * u + 1], pt[4 * u + 2], pt[4 * u + 3]);
+          }
+        }
       }
       tc_fence_before();
-      mbar_arrive(&s_empty[sb]);
-      ++sc;
-      if (j > 0 && !(ok = mbar_wait_warp(pv_done, (j - 1) & 1, abort))) break;
-#pragma unroll
-      for (int ch = 0; ch < 16; ++ch) {
-        *reinterpret_cast<uint4*>(p_smem + sw128_offset(t, ch * 8, 128)) =
-            make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-      }
       fence_proxy_async_smem();
-      mbar_arrive(p_full);
+      mbar_arrive(&p_full[wg]);
     }
-    if (ok && (ok = mbar_wait_warp(o_full, 0, abort))) {
+    float l_lo, l_hi;
+    up2(l2, l_lo, l_hi);
+    const float l = l_lo + l_hi;
+    if (ok && (ok = mbar_wait_warp(&o_full[wg], 0, abort))) {
       tc_fence_after();
       const float inv_l = 1.0f / l;
       __nv_bfloat16* orow = o + ((static_cast<int64_t>(b) * Nq + qrow) * H + h) * D;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
-        tmem_ld32(tmem + lane_base + 256 + c * 32, r);
+        tmem_ld32(tmem + lane_base + 256 + wg * 128 + c * 32, r);
         tmem_wait_ld();
         if (qrow < Nq) {
           uint32_t w[16];
@@ -334,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   report_abort(abort, err);
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -346,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 cudaError_t launch_attn_fwd(const AttnShape& s, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, void* o, float* stats, int* err,
                             cudaStream_t stream) {
-  const dim3 grid((s.Nq + kTile - 1) / kTile, s.H, s.B);
+  const dim3 grid((s.Nq + 2 * kTile - 1) / (2 * kTile), s.H, s.B);
   auto* op = static_cast<__nv_bfloat16*>(o);
   if (s.D == 128) {
     using L = FwdLayout<128>;

@@ -21,7 +21,7 @@
 //  * quant16_static IEEE fp32 products and quotients (mul.rn / div.rn) in the
 //                   order of the definition: bit-identical to any IEEE fp32
 //                   evaluation of the same steps.
-//  * quant16_p      the softmax probabilities inside attention (fp32 inputs):
+//  * pquant16       the softmax probabilities inside attention (fp32 inputs):
 //                   reciprocal and product without snapping.  The forward and
 //                   the backward run this same code on bit-identical inputs.
 #pragma once
@@ -200,26 +200,91 @@ __device__ __forceinline__ Q16 quant16_static(const uint32_t (&x)[8], float g) {
   return r;
 }
 
-// Softmax probabilities (0 <= p <= 1, fp32) of one 16-key block -> P~ as eight
-// f16x2 (exact: code * E4M3 scale).
-__device__ __forceinline__ void quant16_p(const float* p, uint32_t (&out)[8]) {
-  float amax = 0.f;
+}  // namespace nvq
+
+namespace nvq {
+
+// ---------------------------------------------------------------------------
+// Softmax probabilities inside attention (forward and backward run this same
+// code on bit-identical inputs, so P~ is bit-identical between them).
+//
+// Every rounding decision is taken on fp32 values: O is an incoherent sum of
+// P~V~ terms, so even rare decision flips (from an f16 P or an f16 q = P/s)
+// move it by sqrt(flip rate) x one grid step, about 1e-2 with f16 precision.
+// Packed f32x2 arithmetic halves the FP32 instruction count; the E2M1 decode
+// and the product code*s stay in packed halves, where they are exact.
+__device__ __forceinline__ uint64_t pk2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void up2(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ float ex2_f32(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+__device__ __forceinline__ float f16hi_to_f32(uint32_t h2) {
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(h2 >> 16)));
+}
+// E2M1 code (RNE, satfinite) of two fp32 values, decoded to an f16x2 pair.
+__device__ __forceinline__ uint32_t e2m1_pair_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 b;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b, %2, %1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b;\n\t}"
+      : "=r"(r)
+      : "f"(lo), "f"(hi));
+  return r;
+}
+
+// One 16-key block.  x: exponent arguments log2(e)*(scale*S - m) (-inf for
+// masked keys).  Out: p = 2^x (fp32) and P~ = E2M1(p/s)*s as f16x2 pairs,
+// s = E4M3(amax/6).  Returns nothing else; the caller sums p.
+__device__ __forceinline__ void pquant16(const float* x, float (&p)[16], uint32_t (&pt)[8]) {
 #pragma unroll
-  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, p[i]);
-  const uint32_t sb = e4m3_rn_sat(amax * (1.0f / 6.0f));
+  for (int i = 0; i < 16; ++i) p[i] = ex2_f32(x[i]);
+  float a = max3f(p[0], p[1], p[2]);
+  a = max3f(a, p[3], p[4]);
+  a = max3f(a, p[5], p[6]);
+  a = max3f(a, p[7], p[8]);
+  a = max3f(a, p[9], p[10]);
+  a = max3f(a, p[11], p[12]);
+  a = max3f(a, p[13], p[14]);
+  a = fmaxf(a, p[15]);
+  const uint32_t sb = e4m3_rn_sat(a * (1.0f / 6.0f));
   const uint32_t s_h = e4m3_to_f16x2(sb);
+  const uint32_t s_h2 = (s_h & 0xFFFFu) | (s_h << 16);
   const float s = f16lo_to_f32(s_h);
   const float inv = s > 0.f ? rcp_approx(s) : 0.f;
-  const uint32_t s_h2 = (s_h & 0xFFFFu) | (s_h << 16);
+  const uint64_t inv2 = pk2(inv, inv);
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    float q[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) q[i] = p[8 * h + i] * inv;
-    uint32_t hv[4];
-    e2m1x8_to_f16x2(e2m1x8(q), hv);
-#pragma unroll
-    for (int j = 0; j < 4; ++j) out[4 * h + j] = hmul2(hv[j], s_h2);
+  for (int j = 0; j < 8; ++j) {
+    float q0, q1;
+    up2(mul2(pk2(p[2 * j], p[2 * j + 1]), inv2), q0, q1);
+    pt[j] = hmul2(e2m1_pair_f16x2(q0, q1), s_h2);
   }
 }
 
