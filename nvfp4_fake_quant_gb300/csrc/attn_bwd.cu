@@ -17,9 +17,10 @@
 // ("attn_qat_train" API page, attn_qat_train(): the backward uses the quantized
 // Q, K, V and the quantized P, with straight-through gradients.)
 //
-// Roles (192 threads, one CTA per SM): warps 0-3 elementwise (thread t = query
-// row t of the tile = TMEM lane t for S/dP/dQ, key row t for dK/dV), warp 4 TMA,
-// warp 5 TMEM allocation and UMMA issue.
+// Roles (576 threads, one CTA per SM): warps 0-15 elementwise in four
+// warpgroups, each owning 32 keys of the tile (thread t = query row t = TMEM
+// lane t for S/dP/dQ, key row t for dK/dV), warp 16 TMA, warp 17 TMEM
+// allocation and UMMA issue.
 // TMEM columns: [0,128) S then dQ, [128,256) dP, [256,256+D) dV, [384,384+D) dK.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -32,10 +33,10 @@ namespace nvq {
 
 namespace {
 
-constexpr int kElemThreads = 256;  // two elementwise warpgroups
-constexpr int kTmaWarp = 8;
-constexpr int kMmaWarp = 9;
-constexpr int kThreads = 320;
+constexpr int kElemWarps = 16;  // four elementwise warpgroups
+constexpr int kTmaWarp = 16;
+constexpr int kMmaWarp = 17;
+constexpr int kThreads = 576;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint32_t kAtomBlock = 128u * 128u;
 
@@ -49,6 +50,10 @@ __device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, 
   asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c),
                "f"(d)
                : "memory");
+}
+
+__device__ __forceinline__ void red_add_v2(float* p, float a, float b) {
+  asm volatile("red.global.add.v2.f32 [%0], {%1, %2};" ::"l"(p), "f"(a), "f"(b) : "memory");
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -110,6 +115,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_q_all = (Nq + kTile - 1) / kTile;
   const int i_begin = causal ? kt : 0;  // causal requires Nq == Nkv
   const int n_iter = n_q_all - i_begin;
+  // Query tile of iteration `it`.  Each CTA starts at its own offset, so that
+  // CTAs running at the same time add their dQ partials into different rows of
+  // the accumulator instead of contending for the same L2 lines.
+  const int q_rot = n_iter > 0 ? kt % n_iter : 0;
+  auto qtile = [&](int it) -> int {
+    const int k = it + q_rot;
+    return i_begin + (k >= n_iter ? k - n_iter : k);
+  };
 
   if (threadIdx.x == 0) {
     *abort = 0;
@@ -120,11 +133,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(s_full, 1);
     mbar_init(dp_full, 1);
-    mbar_init(pt_full, kElemThreads);
+    mbar_init(pt_full, kElemWarps);
     mbar_init(pt_free, 1);
-    mbar_init(ds_full, kElemThreads);
+    mbar_init(ds_full, kElemWarps);
     mbar_init(dq_full, 1);
-    mbar_init(dq_free, kElemThreads);
+    mbar_init(dq_free, kElemWarps);
     mbar_init(dkdv_done, 1);
     mbar_init(mma_drain, 1);
     fence_mbar_init();
@@ -156,7 +169,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int it = 0; it < n_iter; ++it) {
         const int st = it & 1;
         if (!(ok = mbar_wait(&qdo_empty[st], ((it >> 1) & 1) ^ 1, abort))) break;
-        const int qrow0 = (i_begin + it) * kTile;
+        const int qrow0 = qtile(it) * kTile;
         mbar_arrive_expect_tx(&qdo_full[st], 2u * L::kTileBytes);
 #pragma unroll
         for (int blk = 0; blk < D / 64; ++blk) {
@@ -256,8 +269,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // --------------------------------------------------------- elementwise
-    // Warpgroup g (0/1) owns keys [64g, 64g+64) of every tile and dQ columns
-    // [g*D/2, (g+1)*D/2); thread t of the group owns query row t (TMEM lane t).
+    // Warpgroup g (0..3) owns keys [32g, 32g+32) of every tile and dQ columns
+    // [g*D/4, (g+1)*D/4); thread t of the group owns query row t (TMEM lane t).
+    // dS is stored pre-multiplied by `scale`, so dK and dQ come out scaled.
     const int g = warp >> 2;
     const int t = threadIdx.x & 127;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -266,12 +280,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float* lse_g = stats + (static_cast<int64_t>(b) * H + h) * 2 * Nq;
     const float* m_g = lse_g + Nq;
     const float* delta_g = delta + (static_cast<int64_t>(b) * H + h) * Nq;
-    constexpr int kDqCols = D / 2;
+    constexpr int kDqCols = D / 4;
+    const uint32_t key_col = static_cast<uint32_t>(g * 32);
     bool ok = true;
     uint32_t r[32];
     // statistics of this thread's row, prefetched one tile ahead
     auto load_row = [&](int it, float& m, float& lse, float& dl) {
-      const int qrow = (i_begin + it) * kTile + t;
+      const int qrow = (it < n_iter ? qtile(it) : 0) * kTile + t;
       const bool in = it < n_iter && qrow < Nq;
       m = in ? m_g[qrow] : 0.f;
       lse = in ? lse_g[qrow] : 0.f;
@@ -279,24 +294,43 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     float nm, nlse, ndl;
     load_row(0, nm, nlse, ndl);
-    auto read_dq = [&](int it_prev) {  // dQ of tile it_prev: TMEM [128, 128+D) -> fp32 accumulator
-      const int qrow = (i_begin + it_prev) * kTile + t;
-      float* dqrow = dq_acc + ((static_cast<int64_t>(b) * Nq + qrow) * H + h) * D + g * kDqCols;
+    // dQ of tile it_prev: TMEM [128, 128+D) -> registers (16-lane x 8-column
+    // loads: four neighbouring threads hold 32 contiguous bytes of one row), the
+    // columns are released (dq_free, when `release`), then every (row, 2
+    // columns) pair is added into the fp32 accumulator, so each group of four
+    // threads covers one full 32-byte sector.
+    auto read_dq = [&](int it_prev, bool release) {
+      const int qbase = qtile(it_prev) * kTile + (warp & 3) * 32;
+      constexpr int kReps = kDqCols / 8;
+      uint32_t v[2][kReps][4];
 #pragma unroll
-      for (int c = 0; c < kDqCols / 32; ++c) {
-        tmem_ld32(tmem + lane_base + 128 + g * kDqCols + c * 32, r);
-        tmem_wait_ld();
-        if (qrow < Nq) {
+      for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
-          for (int u = 0; u < 8; ++u)
-            red_add_v4(dqrow + c * 32 + 4 * u, __uint_as_float(r[4 * u]) * scale,
-                       __uint_as_float(r[4 * u + 1]) * scale, __uint_as_float(r[4 * u + 2]) * scale,
-                       __uint_as_float(r[4 * u + 3]) * scale);
+        for (int k = 0; k < kReps; ++k)
+          tmem_ld16x256(tmem + lane_base + (static_cast<uint32_t>(hh * 16) << 16) + 128 +
+                            g * kDqCols + 8 * k,
+                        v[hh][k]);
+      tmem_wait_ld();
+      if (release) {
+        tc_fence_before();
+        mbar_arrive_warp(dq_free);
+      }
+      const int col = g * kDqCols + 2 * (lane & 3);
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int row_a = qbase + hh * 16 + (lane >> 2);
+        const int row_b = row_a + 8;
+        float* pa = dq_acc + ((static_cast<int64_t>(b) * Nq + row_a) * H + h) * D + col;
+        float* pb = dq_acc + ((static_cast<int64_t>(b) * Nq + row_b) * H + h) * D + col;
+#pragma unroll
+        for (int k = 0; k < kReps; ++k) {
+          if (row_a < Nq) red_add_v2(pa + 8 * k, __uint_as_float(v[hh][k][0]), __uint_as_float(v[hh][k][1]));
+          if (row_b < Nq) red_add_v2(pb + 8 * k, __uint_as_float(v[hh][k][2]), __uint_as_float(v[hh][k][3]));
         }
       }
     };
     for (int it = 0; it < n_iter && ok; ++it) {
-      const int qi = i_begin + it;
+      const int qi = qtile(it);
       const int qrow = qi * kTile + t;
       const bool row_ok = qrow < Nq;
       const float m = nm, lse = nlse, dl = ndl;
@@ -309,12 +343,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---- P part: S -> P, P~/l
       if (!(ok = mbar_wait_warp(s_full, ph, abort))) break;
       tc_fence_after();
-      float p[64];       // P for this thread's 64 keys
-      uint32_t ptw[32];  // P~ / l as bf16x2
+      uint32_t ph2[16];  // P as f16x2 pairs (A = P/l feeds no rounding decision)
+      uint32_t ptw[16];  // P~ / l as bf16x2
       const uint64_t il2 = pk2(inv_l, inv_l);
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        tmem_ld32(tmem + lane_base + g * 64 + c * 32, r);
+      {
+        tmem_ld32(tmem + lane_base + key_col, r);
         tmem_wait_ld();
         float x[32];
 #pragma unroll
@@ -324,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (edge) {
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            const int key = k0 + g * 64 + c * 32 + i;
+            const int key = k0 + key_col + i;
             if (!(row_ok && key < Nkv && (!causal || key <= qrow))) x[i] = -INFINITY;
           }
         }
@@ -334,12 +367,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t pt[8];
           pquant16(x + 16 * hb, pp, pt);
 #pragma unroll
-          for (int u = 0; u < 16; ++u) p[c * 32 + hb * 16 + u] = pp[u];
-#pragma unroll
           for (int u = 0; u < 8; ++u) {
+            ph2[hb * 8 + u] = pack_f16x2_rn(pp[2 * u], pp[2 * u + 1]);
             float a0, a1;
             up2(mul2(pk2(f16lo_to_f32(pt[u]), f16hi_to_f32(pt[u])), il2), a0, a1);
-            ptw[c * 16 + hb * 8 + u] = pack_bf16(a0, a1);
+            ptw[hb * 8 + u] = pack_bf16(a0, a1);
           }
         }
       }
@@ -347,70 +379,70 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the P~/dS buffer is free once dK and dQ of the previous tile are done
       if (it > 0 && !(ok = mbar_wait_warp(dq_full, ph ^ 1u, abort))) break;
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        const uint32_t off = sw128_offset(t, g * 64 + ch * 8, 128);
+      for (int ch = 0; ch < 4; ++ch) {
+        const uint32_t off = sw128_offset(t, key_col + ch * 8, 128);
         *reinterpret_cast<uint4*>(pd_smem + off) =
             make_uint4(ptw[4 * ch], ptw[4 * ch + 1], ptw[4 * ch + 2], ptw[4 * ch + 3]);
       }
       fence_proxy_async_smem();
-      mbar_arrive(pt_full);
+      mbar_arrive_warp(pt_full);
       // ---- dQ of the previous tile
       if (it > 0) {
         tc_fence_after();
-        read_dq(it - 1);
-        tc_fence_before();
-        mbar_arrive(dq_free);
+        read_dq(it - 1, true);
       }
-      // ---- dS part: dP -> dS = A * (dP - delta), A = P / l
+      // ---- dS part: dP -> dS = scale * A * (dP - delta), A = P / l
       if (!(ok = mbar_wait_warp(dp_full, ph, abort))) break;
       tc_fence_after();
-      uint32_t dsw[32];
-      const uint64_t ndl2 = pk2(-dl, -dl);
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        tmem_ld32(tmem + lane_base + 128 + g * 64 + c * 32, r);
+      uint32_t dsw[16];
+      {
+        const uint64_t ndl2 = pk2(-dl, -dl);
+        const uint64_t sl2 = pk2(scale * inv_l, scale * inv_l);
+        tmem_ld32(tmem + lane_base + 128 + key_col, r);
         tmem_wait_ld();
 #pragma unroll
         for (int u = 0; u < 16; ++u) {
-          const uint64_t a2 = mul2(pk2(p[c * 32 + 2 * u], p[c * 32 + 2 * u + 1]), il2);  // A = P / l
+          const uint64_t a2 = mul2(pk2(f16lo_to_f32(ph2[u]), f16hi_to_f32(ph2[u])), sl2);
           const uint64_t d2 = add2(pk2(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1])), ndl2);
           float d0, d1;
           up2(mul2(a2, d2), d0, d1);
-          dsw[c * 16 + u] = pack_bf16(d0, d1);
+          dsw[u] = pack_bf16(d0, d1);
         }
       }
       tc_fence_before();
       if (!(ok = mbar_wait_warp(pt_free, ph, abort))) break;
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        const uint32_t off = sw128_offset(t, g * 64 + ch * 8, 128);
+      for (int ch = 0; ch < 4; ++ch) {
+        const uint32_t off = sw128_offset(t, key_col + ch * 8, 128);
         *reinterpret_cast<uint4*>(pd_smem + off) =
             make_uint4(dsw[4 * ch], dsw[4 * ch + 1], dsw[4 * ch + 2], dsw[4 * ch + 3]);
       }
       fence_proxy_async_smem();
-      mbar_arrive(ds_full);
+      mbar_arrive_warp(ds_full);
     }
-    if (ok && n_iter > 0 && (ok = mbar_wait_warp(dq_full, static_cast<uint32_t>((n_iter - 1) & 1), abort))) {
+    if (ok && n_iter > 0 &&
+        (ok = mbar_wait_warp(dq_full, static_cast<uint32_t>((n_iter - 1) & 1), abort))) {
       tc_fence_after();
-      read_dq(n_iter - 1);
+      read_dq(n_iter - 1, false);
     }
     if (ok && n_iter > 0 && (ok = mbar_wait_warp(dkdv_done, 0, abort))) {
       tc_fence_after();
-      // group 0 writes dV, group 1 writes dK (scaled); thread t = key row t
+      // groups 0, 1 write dV; groups 2, 3 write dK (already scaled); each group
+      // D/2 columns; thread t = key row t
       const int key = k0 + t;
       const int64_t base = ((static_cast<int64_t>(b) * Nkv + key) * H + h) * D;
-      __nv_bfloat16* dst = g == 0 ? dv : dk;
-      const float mul = g == 0 ? 1.0f : scale;
+      __nv_bfloat16* dst = (g < 2 ? dv : dk) + base + (g & 1) * (D / 2);
+      const uint32_t col = (g < 2 ? 256u : 384u) + static_cast<uint32_t>((g & 1) * (D / 2));
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        tmem_ld32(tmem + lane_base + (g == 0 ? 256 : 384) + c * 32, r);
+      for (int c = 0; c < D / 64; ++c) {
+        tmem_ld32(tmem + lane_base + col + c * 32, r);
         tmem_wait_ld();
         if (key < Nkv) {
           uint32_t w[16];
 #pragma unroll
           for (int u = 0; u < 16; ++u)
-            w[u] = pack_bf16(__uint_as_float(r[2 * u]) * mul, __uint_as_float(r[2 * u + 1]) * mul);
-          uint4* pw = reinterpret_cast<uint4*>(dst + base + c * 32);
+            w[u] = pack_bf16(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1]));
+          uint4* pw = reinterpret_cast<uint4*>(dst + c * 32);
 #pragma unroll
           for (int u = 0; u < 4; ++u)
             pw[u] = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
@@ -421,9 +453,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int key = k0 + t;
       if (key < Nkv) {
         const int64_t base = ((static_cast<int64_t>(b) * Nkv + key) * H + h) * D;
-        __nv_bfloat16* dst = g == 0 ? dv : dk;
-        for (int c = 0; c < D; c += 8)
-          *reinterpret_cast<uint4*>(dst + base + c) = make_uint4(0, 0, 0, 0);
+        __nv_bfloat16* dst = (g < 2 ? dv : dk) + base + (g & 1) * (D / 2);
+        for (int c = 0; c < D / 2; c += 8)
+          *reinterpret_cast<uint4*>(dst + c) = make_uint4(0, 0, 0, 0);
       }
     }
   }

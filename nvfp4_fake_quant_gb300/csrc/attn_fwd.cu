@@ -14,12 +14,13 @@
 // bits and V~ values have <= 7, so both are exact in f16 and the P~V~ UMMA
 // runs on f16 operands.
 //
-// Roles (192 threads, one CTA per SM):
-//   warps 0-3  softmax: thread t owns query row t = TMEM lane t
-//   warp 4     TMA producer (lane 0)
-//   warp 5     TMEM allocator and UMMA issuer (lane 0)
-// Buffers: Q~ tile; K~ and V~ rings of 2 stages; one P~ tile; TMEM columns
-// [0,128) and [128,256) hold two S tiles, [256, 256+D) the O accumulator.
+// Roles (576 threads, one CTA per SM, two 128-query tiles per CTA):
+//   warps 0-15 softmax, two warpgroups per query tile (64 key columns each);
+//              thread t owns query row t = TMEM lane t
+//   warp 16    TMA producer (lane 0)
+//   warp 17    TMEM allocator and UMMA issuer (lane 0)
+// Buffers: two Q~ tiles, two P~ tiles, a 3-stage K~/V~ ring; TMEM columns
+// [0,256) hold S_0, S_1 and [256,512) the O_0, O_1 accumulators.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -31,10 +32,11 @@ namespace nvq {
 
 namespace {
 
-constexpr int kSoftmaxThreads = 128;  // one warpgroup per query tile
-constexpr int kTmaWarp = 8;
-constexpr int kMmaWarp = 9;
-constexpr int kThreads = 320;
+constexpr int kPairThreads = 256;  // two softmax warpgroups per query tile
+constexpr int kPairWarps = 8;
+constexpr int kTmaWarp = 16;
+constexpr int kMmaWarp = 17;
+constexpr int kThreads = 576;
 constexpr int kRing = 3;  // K/V tile ring (K and V tiles interleave in pass 2)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint32_t kAtomBlock = 128u * 128u;  // bytes of one 64-column block of a 128-row tile
@@ -61,7 +63,7 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
 }
 
 // Grid: (ceil(Nq / 256), H, B).  Each CTA owns two 128-query tiles; softmax
-// warpgroup i (warps 4i..4i+3) owns tile i.  TMEM: S_i at [128 i, 128 i + 128),
+// warpgroups 2i and 2i+1 (warps 8i..8i+7) own tile i, 64 key columns each.  TMEM: S_i at [128 i, 128 i + 128),
 // O_i at [256 + 128 i, 256 + 128 i + D).  The UMMA warp ping-pongs the two
 // tiles so that one warpgroup's softmax overlaps the other's UMMAs.
 template <int D>
@@ -105,8 +107,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], kSoftmaxThreads);
-      mbar_init(&p_full[i], kSoftmaxThreads);
+      mbar_init(&s_free[i], kPairWarps);
+      mbar_init(&p_full[i], kPairWarps);
       mbar_init(&o_full[i], 1);
     }
     mbar_init(mma_drain, 1);
@@ -238,23 +240,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ softmax
-    const int wg = warp >> 2;              // query tile of this warpgroup
+    // Warpgroups 2i and 2i+1 own query tile i; half `hf` of the pair owns key
+    // columns [64 hf, 64 hf + 64) of S_i and O columns [hf D/2, (hf+1) D/2).
+    // Row maxima and sums are combined across the pair through the tile's P~
+    // buffer, which is idle at both points (before pass 2, after the last PV).
+    const int wg = warp >> 2;
+    const int ti = wg >> 1;                // query tile
+    const int hf = wg & 1;                 // half of the key columns
     const int t = threadIdx.x & 127;       // row in the tile == TMEM lane
-    const int qrow = q0 + wg * kTile + t;
+    const int qrow = q0 + ti * kTile + t;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t s_col = static_cast<uint32_t>(wg * 128);
+    const uint32_t s_col = static_cast<uint32_t>(ti * 128 + hf * 64);
     const float c1 = scale * kLog2e;
-    uint8_t* p_smem = smem + L::kP + wg * 128 * 128 * 2;
+    uint8_t* p_smem = smem + L::kP + ti * 128 * 128 * 2;
+    float* xchg = reinterpret_cast<float*>(p_smem);  // [2][128] floats during the exchanges
+    const uint32_t pair_bar = 1u + static_cast<uint32_t>(ti);
     bool ok = true;
     float mraw = -INFINITY;
     uint32_t r[32];
-    const int q_last = q0 + wg * kTile + kTile - 1;  // last query row of this tile
+    const int tile_q0 = q0 + ti * kTile;
     for (int j = 0; j < n_kv && ok; ++j) {
-      if (!(ok = mbar_wait_warp(&s_full[wg], static_cast<uint32_t>(j & 1), abort))) break;
+      if (!(ok = mbar_wait_warp(&s_full[ti], static_cast<uint32_t>(j & 1), abort))) break;
       tc_fence_after();
-      const bool edge = (j * kTile + kTile > Nkv) || (causal && j * kTile + kTile - 1 > q0 + wg * kTile);
+      const bool edge = (j * kTile + kTile > Nkv) || (causal && j * kTile + kTile - 1 > tile_q0);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         tmem_ld32(tmem + lane_base + s_col + c * 32, r);
         tmem_wait_ld();
         if (!edge) {
@@ -263,26 +273,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            const int key = j * kTile + c * 32 + i;
+            const int key = j * kTile + hf * 64 + c * 32 + i;
             if (key < Nkv && (!causal || key <= qrow)) mraw = fmaxf(mraw, __uint_as_float(r[i]));
           }
         }
       }
       tc_fence_before();
-      mbar_arrive(&s_free[wg]);
+      mbar_arrive_warp(&s_free[ti]);
     }
-    (void)q_last;
+    // combine the row maxima of the pair (always reached, also after an abort)
+    xchg[hf * 128 + t] = mraw;
+    named_bar_sync(pair_bar, kPairThreads);
+    mraw = fmaxf(mraw, xchg[(hf ^ 1) * 128 + t]);
+    named_bar_sync(pair_bar, kPairThreads);
     const float m = mraw * scale;
     const float negmb = -m * kLog2e;
     const uint64_t c12 = pk2(c1, c1), nmb2 = pk2(negmb, negmb);
     uint64_t l2 = pk2(0.f, 0.f);
     for (int j = 0; j < n_kv && ok; ++j) {
-      if (!(ok = mbar_wait_warp(&s_full[wg], static_cast<uint32_t>((n_kv + j) & 1), abort))) break;
+      if (!(ok = mbar_wait_warp(&s_full[ti], static_cast<uint32_t>((n_kv + j) & 1), abort))) break;
       tc_fence_after();
       // S_i(j) complete implies PV_i(j-1) complete (issued earlier): the P~ tile is free
-      const bool edge = (j * kTile + kTile > Nkv) || (causal && j * kTile + kTile - 1 > q0 + wg * kTile);
+      const bool edge = (j * kTile + kTile > Nkv) || (causal && j * kTile + kTile - 1 > tile_q0);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         tmem_ld32(tmem + lane_base + s_col + c * 32, r);
         tmem_wait_ld();
         float x[32];
@@ -293,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (edge) {
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            const int key = j * kTile + c * 32 + i;
+            const int key = j * kTile + hf * 64 + c * 32 + i;
             if (!(key < Nkv && (!causal || key <= qrow))) x[i] = -INFINITY;
           }
         }
@@ -306,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int u = 0; u < 8; ++u) l2 = add2(l2, pk2(pp[2 * u], pp[2 * u + 1]));
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
-            const uint32_t off = sw128_offset(t, c * 32 + hb * 16 + u * 8, 128);
+            const uint32_t off = sw128_offset(t, hf * 64 + c * 32 + hb * 16 + u * 8, 128);
             *reinterpret_cast<uint4*>(p_smem + off) =
                 make_uint4(pt[4 * u], pt[4 * u + 1], pt[4 * u + 2], pt[4 * u + 3]);
           }
@@ -314,18 +328,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       fence_proxy_async_smem();
-      mbar_arrive(&p_full[wg]);
+      mbar_arrive_warp(&p_full[ti]);
     }
     float l_lo, l_hi;
     up2(l2, l_lo, l_hi);
-    const float l = l_lo + l_hi;
-    if (ok && (ok = mbar_wait_warp(&o_full[wg], 0, abort))) {
+    float l = l_lo + l_hi;
+    // the last PV of this tile has read P~ once o_full completes
+    const bool have_o = ok && mbar_wait_warp(&o_full[ti], 0, abort);
+    xchg[hf * 128 + t] = l;
+    named_bar_sync(pair_bar, kPairThreads);
+    l += xchg[(hf ^ 1) * 128 + t];
+    if (have_o) {
       tc_fence_after();
       const float inv_l = 1.0f / l;
-      __nv_bfloat16* orow = o + ((static_cast<int64_t>(b) * Nq + qrow) * H + h) * D;
+      __nv_bfloat16* orow = o + ((static_cast<int64_t>(b) * Nq + qrow) * H + h) * D + hf * (D / 2);
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        tmem_ld32(tmem + lane_base + 256 + wg * 128 + c * 32, r);
+      for (int c = 0; c < D / 64; ++c) {
+        tmem_ld32(tmem + lane_base + 256 + ti * 128 + hf * (D / 2) + c * 32, r);
         tmem_wait_ld();
         if (qrow < Nq) {
           uint32_t w[16];
@@ -341,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             dst[u] = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
         }
       }
-      if (qrow < Nq) {
+      if (qrow < Nq && hf == 0) {
         float* st = stats + (static_cast<int64_t>(b) * H + h) * 2 * Nq;
         st[qrow] = m + logf(l);
         st[Nq + qrow] = m;
