@@ -137,6 +137,20 @@ def max_over_ranks(x: float, dist, dev) -> float:
     return float(t.item())
 
 
+def aggregate(ms_local: float, flops_local: float, dist, dev):
+    """Whole-job figures of a replica run: the slowest rank's time and the
+    total work of all ranks (replicas, no data-path collective).
+    Returns (ms, tflops)."""
+    ms = max_over_ranks(ms_local, dist, dev)
+    flops = flops_local
+    if dist is not None:
+        import torch
+        t = torch.tensor([flops_local], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.SUM)
+        flops = float(t.item())
+    return ms, flops / (ms * 1e-3) / 1e12
+
+
 def cpu_baseline(rows: int, head: int = 0):
     """The oracle, as it stands, on query rows [0, rows) of one head (all keys)."""
     import torch
@@ -285,12 +299,10 @@ def run_ours(args):
         ev1.record(stream)
         torch.cuda.synchronize(dev)
     barrier(dist)
-    ms = ev0.elapsed_time(ev1) / args.steps
-    ms = max_over_ranks(ms, dist, dev)
     clocks = clk.summary()
     f_fwd = flops_fwd(b, n, n, h, d)
     f_step = 3.5 * f_fwd
-    value = ws * f_step / (ms * 1e-3) / 1e12
+    ms, value = aggregate(ev0.elapsed_time(ev1) / args.steps, f_step, dist, dev)
 
     # ---- per-call durations (fwd, bwd) on the launching stream
     fwd_ms = time_events(fwd, max(2, args.steps), stream)
@@ -314,13 +326,12 @@ def run_ours(args):
         hdk.copy_(dk, non_blocking=True)
         hdv.copy_(dv, non_blocking=True)
 
-    e2e_ms = float("nan")
+    e2e_ms = e2e_value = float("nan")
     if not args.skip_e2e:
         e2e_step()
         torch.cuda.synchronize(dev)
         barrier(dist)
-        e2e_ms = time_events(e2e_step, args.steps, stream)
-        e2e_ms = max_over_ranks(e2e_ms, dist, dev)
+        e2e_ms, e2e_value = aggregate(time_events(e2e_step, args.steps, stream), f_step, dist, dev)
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hdo))
     d2h = sum(t.numel() * t.element_size() for t in (hdq, hdk, hdv))
 
@@ -344,7 +355,7 @@ def run_ours(args):
                      "bound": "tensor", "achieved": bwd_tflops, "peak": peak_t,
                      "unit": "TFLOP/s", "frac": bwd_tflops / peak_t, "traffic": None,
                      "peak_source": f"{peak_src} bf16_tflops (burst)"},
-        "e2e": {"value": ws * f_step / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": 10 * args.steps,
         "clocks": clocks,
