@@ -382,6 +382,8 @@ def main(argv=None):
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     ap.add_argument("--skip-quantizer", action="store_true")
     ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--quantizer-only", action="store_true",
+                    help="time only the standalone quantizer (profiling of that kernel)")
     ap.add_argument("--n", type=int, default=None,
                     help="override N (profiling of smaller cases; not the headline workload)")
     ap.add_argument("--heads", type=int, default=None, help="override H (profiling only)")
@@ -394,6 +396,14 @@ def main(argv=None):
         SHAPE["h"] = args.heads
     if args.impl == "reference":
         return run_reference(args)
+    if args.quantizer_only:
+        import torch
+        from nvfp4_fake_quant_gb300 import _lib
+        _lib.load()
+        peaks, _ = load_peaks()
+        print(json.dumps({"quantizer": quantizer_bench(peaks, torch.cuda.current_stream(),
+                                                       iters=args.steps)}), flush=True)
+        return 0
     return run_ours(args)
 
 
