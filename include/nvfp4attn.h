@@ -69,6 +69,15 @@ const char* nvq_status_string(int status);
 int nvq_version(void);
 
 /*
+ * What the last NVQ_ERR_CUDA returned on the calling host thread came from:
+ * the failing step and the CUDA error's name and description, e.g.
+ * "attn_bwd_dq: cudaErrorInvalidValue (invalid argument)".  Empty if no call
+ * on this thread has returned NVQ_ERR_CUDA.  The string is thread-local and
+ * owned by the library; it stays valid until this thread's next failing call.
+ */
+const char* nvq_last_error_detail(void);
+
+/*
  * Synchronizes `stream`, then returns and clears the device error word that
  * bounded waits set on the current device: NVQ_OK or NVQ_ERR_TIMEOUT (or
  * NVQ_ERR_CUDA if the synchronization itself failed).
@@ -174,9 +183,9 @@ nvq_status attn_qat_bwd(const void* q, const void* k, const void* v, const void*
  * looks up the array's device address (cudaGetSymbolAddress) with that device
  * current; make that first call before any stream capture.  Every call shares
  * the one array: calls whose work overlaps on the GPU (other streams, other
- * host threads) race and corrupt each other's results.  Each call starts by
- * zeroing the part of the array that must start at zero (the dQ accumulator)
- * and overwrites the rest, so the previous call's contents do not matter.
+ * host threads) race and corrupt each other's results.  The backward writes
+ * every byte of scratch it later reads, so the previous call's contents do
+ * not matter and nothing needs clearing.
  */
 nvq_status attn_qat_bwd_builtin_scratch(const void* q, const void* k, const void* v,
                                         const void* o, const float* stats, const void* dout,

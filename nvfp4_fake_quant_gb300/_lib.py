@@ -22,6 +22,7 @@ c_float = ctypes.c_float
 SIGNATURES = {
     "nvq_status_string": (ctypes.c_char_p, [c_int]),
     "nvq_version": (c_int, []),
+    "nvq_last_error_detail": (ctypes.c_char_p, []),
     "nvq_device_status": (c_int, [c_void_p]),
     "nvfp4_global_sf": (c_int, [c_void_p, c_int64, c_int64, c_int64, c_void_p, c_void_p]),
     "nvfp4_fake_quant": (c_int, [c_void_p, c_int64, c_int64, c_int64, c_void_p, c_void_p, c_int64,
@@ -52,9 +53,11 @@ class NvqLibraryError(RuntimeError):
 
 
 class NvqError(RuntimeError):
-    def __init__(self, fn: str, status: int):
-        super().__init__(f"{fn} returned {STATUS.get(status, status)}")
+    def __init__(self, fn: str, status: int, detail: str = ""):
+        msg = f"{fn} returned {STATUS.get(status, status)}"
+        super().__init__(f"{msg}: {detail}" if detail else msg)
         self.status = status
+        self.detail = detail
 
 
 _lock = threading.Lock()
@@ -84,7 +87,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
 
 def call(name: str, *args) -> int:
     """Call an entry point returning nvq_status; raise NvqError unless NVQ_OK."""
-    st = getattr(load(), name)(*args)
+    lib = load()
+    st = getattr(lib, name)(*args)
     if st != 0:
-        raise NvqError(name, st)
+        detail = lib.nvq_last_error_detail().decode() if st == 4 else ""
+        raise NvqError(name, st, detail)
     return st

@@ -2,6 +2,7 @@
 // workspace carving, TMA descriptor creation and kernel launches.
 #include <cmath>
 #include <cstdint>
+#include <cstdio>
 #include <cstring>
 #include <mutex>
 
@@ -19,19 +20,86 @@ static __device__ int g_error_word = 0;
 
 namespace {
 
+// Description of the last NVQ_ERR_CUDA returned on this host thread.
+thread_local char t_error_detail[256] = "";
+
+}  // namespace
+
+nvq_status fail_cuda(const char* where, cudaError_t e) {
+  std::snprintf(t_error_detail, sizeof(t_error_detail), "%s: %s (%s)", where, cudaGetErrorName(e),
+                cudaGetErrorString(e));
+  return NVQ_ERR_CUDA;
+}
+
+nvq_status fail_driver(const char* where, int cu_result) {
+  std::snprintf(t_error_detail, sizeof(t_error_detail), "%s: CUresult %d", where, cu_result);
+  return NVQ_ERR_CUDA;
+}
+
+namespace {
+
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 int* g_err_ptr[kMaxDevices] = {};
 
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+
+CtxGetCurrentFn ctx_get_current_fn() {
+  static CtxGetCurrentFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(p);
+  });
+  return fn;
+}
+
+// Makes sure a CUDA context is current on the calling host thread.  A thread
+// that has not yet made a CUDA call needing a context (for instance a worker
+// thread of a framework that only ever touched the device through its own
+// CUDA runtime) has none, and driver calls such as cuTensorMapEncodeTiled then
+// fail with CUDA_ERROR_INVALID_CONTEXT.  In that case the primary context of
+// the runtime's current device is made current; a context the caller made
+// current is left alone.
+cudaError_t bind_context(int dev) {
+  CtxGetCurrentFn get = ctx_get_current_fn();
+  if (get == nullptr) return cudaErrorNotSupported;
+  CUcontext ctx = nullptr;
+  if (get(&ctx) != CUDA_SUCCESS) return cudaErrorInitializationError;
+  return ctx != nullptr ? cudaSuccess : cudaSetDevice(dev);
+}
+
 // Address of this device's error word (looked up once per device, with that
-// device current).
+// device current), after making sure a context is current on this thread.
+// On failure records the reason and returns nullptr.
 int* error_word() {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) {
+    fail_cuda("cudaGetDevice", e);
+    return nullptr;
+  }
+  e = bind_context(dev);
+  if (e != cudaSuccess) {
+    fail_cuda("bind the device's context to this thread", e);
+    return nullptr;
+  }
+  if (dev < 0 || dev >= kMaxDevices) {
+    fail_cuda("device ordinal out of range", cudaErrorInvalidDevice);
+    return nullptr;
+  }
   std::lock_guard<std::mutex> lock(g_mu);
   if (g_err_ptr[dev] == nullptr) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
+    e = cudaGetSymbolAddress(&p, g_error_word);
+    if (e != cudaSuccess) {
+      fail_cuda("cudaGetSymbolAddress(error word)", e);
+      return nullptr;
+    }
     g_err_ptr[dev] = static_cast<int*>(p);
   }
   return g_err_ptr[dev];
@@ -60,31 +128,34 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-nvq_status from_cuda(cudaError_t e) { return e == cudaSuccess ? NVQ_OK : NVQ_ERR_CUDA; }
+nvq_status from_cuda(const char* where, cudaError_t e) {
+  return e == cudaSuccess ? NVQ_OK : fail_cuda(where, e);
+}
 
 }  // namespace
 
-bool make_bnhd_map(CUtensorMap* map, const void* base, int B, int N, int H, int D, bool f16) {
+int make_bnhd_map(CUtensorMap* map, const void* base, int B, int N, int H, int D, bool f16,
+                  int box_rows) {
   EncodeTiledFn fn = encode_fn();
-  if (fn == nullptr) return false;
+  if (fn == nullptr) return CUDA_ERROR_NOT_FOUND;
   const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(N),
                               static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(B)};
   const cuuint64_t strides[3] = {static_cast<cuuint64_t>(H) * D * 2,
                                  static_cast<cuuint64_t>(D) * 2,
                                  static_cast<cuuint64_t>(N) * H * D * 2};
-  const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(kTile), 1, 1};
+  const cuuint32_t box[4] = {64, static_cast<cuuint32_t>(box_rows), 1, 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   const CUresult r =
       fn(map, f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
          const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  return static_cast<int>(r);
 }
 
-bool make_2d_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_rows) {
+int make_2d_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_rows) {
   EncodeTiledFn fn = encode_fn();
-  if (fn == nullptr) return false;
+  if (fn == nullptr) return CUDA_ERROR_NOT_FOUND;
   const cuuint64_t dims[4] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows), 1, 1};
   const cuuint64_t rs = static_cast<cuuint64_t>(cols) * 2;
   const cuuint64_t strides[3] = {rs, rs * rows, rs * rows};
@@ -94,7 +165,7 @@ bool make_2d_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  return static_cast<int>(r);
 }
 
 namespace {
@@ -127,15 +198,14 @@ FwdWs fwd_ws(int B, int Nq, int Nkv, int H, int D) {
 }
 
 struct BwdWs {
-  size_t q, k, v, dq, delta, total;
+  size_t q, k, v, delta, total;
 };
 BwdWs bwd_ws(int B, int Nq, int Nkv, int H, int D) {
   BwdWs w;
   w.q = 0;
   w.k = round_up(w.q + bytes_bnhd(B, Nq, H, D, 2), 256);
   w.v = round_up(w.k + bytes_bnhd(B, Nkv, H, D, 2), 256);
-  w.dq = round_up(w.v + bytes_bnhd(B, Nkv, H, D, 2), 256);
-  w.delta = round_up(w.dq + bytes_bnhd(B, Nq, H, D, 4), 256);
+  w.delta = round_up(w.v + bytes_bnhd(B, Nkv, H, D, 2), 256);
   w.total = round_up(w.delta + static_cast<size_t>(B) * H * Nq * 4, 256);
   return w;
 }
@@ -168,13 +238,18 @@ const char* nvq_status_string(int status) {
 
 int nvq_version(void) { return (1 << 16) | 0; }
 
+const char* nvq_last_error_detail(void) { return t_error_detail; }
+
 nvq_status nvq_device_status(nvq_stream_t stream) {
-  if (cudaStreamSynchronize(stream) != cudaSuccess) return NVQ_ERR_CUDA;
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return fail_cuda("cudaStreamSynchronize", e);
   int v = 0;
-  if (cudaMemcpyFromSymbol(&v, g_error_word, sizeof(int)) != cudaSuccess) return NVQ_ERR_CUDA;
+  e = cudaMemcpyFromSymbol(&v, g_error_word, sizeof(int));
+  if (e != cudaSuccess) return fail_cuda("read error word", e);
   if (v != 0) {
     const int zero = 0;
-    if (cudaMemcpyToSymbol(g_error_word, &zero, sizeof(int)) != cudaSuccess) return NVQ_ERR_CUDA;
+    e = cudaMemcpyToSymbol(g_error_word, &zero, sizeof(int));
+    if (e != cudaSuccess) return fail_cuda("clear error word", e);
     return NVQ_ERR_TIMEOUT;
   }
   return NVQ_OK;
@@ -186,7 +261,7 @@ nvq_status nvfp4_global_sf(const void* x, int64_t rows, int64_t cols, int64_t ld
       (reinterpret_cast<uintptr_t>(global_sf) & 3u) != 0)
     return NVQ_ERR_INVALID;
   if (rows < 1 || cols < 1 || ld_x < cols || ld_x % 8 != 0) return NVQ_ERR_INVALID;
-  return from_cuda(launch_global_sf(x, rows, cols, ld_x, global_sf, stream));
+  return from_cuda("global_sf", launch_global_sf(x, rows, cols, ld_x, global_sf, stream));
 }
 
 nvq_status nvfp4_fake_quant(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
@@ -201,8 +276,8 @@ nvq_status nvfp4_fake_quant(const void* x, int64_t rows, int64_t cols, int64_t l
   if (global_sf != nullptr && (reinterpret_cast<uintptr_t>(global_sf) & 3u) != 0)
     return NVQ_ERR_INVALID;
   const int mode = global_sf == nullptr ? kUnitBf16 : kStaticBf16;
-  return from_cuda(launch_fake_quant(x, rows, cols, ld_x, global_sf, mode, out, ld_out, scales,
-                                     ld_scales, nullptr, 0, stream));
+  return from_cuda("fake_quant", launch_fake_quant(x, rows, cols, ld_x, global_sf, mode, out,
+                                                   ld_out, scales, ld_scales, nullptr, 0, stream));
 }
 
 nvq_status nvfp4_quantize_codes(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
@@ -216,8 +291,9 @@ nvq_status nvfp4_quantize_codes(const void* x, int64_t rows, int64_t cols, int64
   if (global_sf != nullptr && (reinterpret_cast<uintptr_t>(global_sf) & 3u) != 0)
     return NVQ_ERR_INVALID;
   const int mode = global_sf == nullptr ? kUnitBf16 : kStaticBf16;
-  return from_cuda(launch_fake_quant(x, rows, cols, ld_x, global_sf, mode, nullptr, 0, scales,
-                                     ld_scales, codes, ld_codes, stream));
+  return from_cuda("quantize_codes", launch_fake_quant(x, rows, cols, ld_x, global_sf, mode,
+                                                       nullptr, 0, scales, ld_scales, codes,
+                                                       ld_codes, stream));
 }
 
 size_t attn_qat_fwd_workspace(int B, int Nq, int Nkv, int H, int D) {
@@ -248,19 +324,24 @@ nvq_status attn_qat_fwd(const void* q, const void* k, const void* v, int B, int 
   void* kt = wb + w.k;
   void* vt = wb + w.v;
   CUtensorMap mq, mk, mv;
-  if (!make_bnhd_map(&mq, qt, B, Nq, H, D, false) ||
-      !make_bnhd_map(&mk, kt, B, Nkv, H, D, false) || !make_bnhd_map(&mv, vt, B, Nkv, H, D, true))
-    return NVQ_ERR_CUDA;
+  int r;
+  if ((r = make_bnhd_map(&mq, qt, B, Nq, H, D, false)) != 0 ||
+      (r = make_bnhd_map(&mk, kt, B, Nkv, H, D, false)) != 0 ||
+      (r = make_bnhd_map(&mv, vt, B, Nkv, H, D, true)) != 0)
+    return fail_driver("cuTensorMapEncodeTiled", r);
   const int64_t rq = static_cast<int64_t>(B) * Nq * H, rk = static_cast<int64_t>(B) * Nkv * H;
-  cudaError_t e =
-      launch_fake_quant(q, rq, D, D, nullptr, kUnitBf16, qt, D, nullptr, 0, nullptr, 0, stream);
-  if (e == cudaSuccess)
-    e = launch_fake_quant(k, rk, D, D, nullptr, kUnitBf16, kt, D, nullptr, 0, nullptr, 0, stream);
-  if (e == cudaSuccess)
-    e = launch_fake_quant(v, rk, D, D, nullptr, kUnitF16, vt, D, nullptr, 0, nullptr, 0, stream);
-  if (e != cudaSuccess) return NVQ_ERR_CUDA;
+  cudaError_t e;
+  if ((e = launch_fake_quant(q, rq, D, D, nullptr, kUnitBf16, qt, D, nullptr, 0, nullptr, 0,
+                             stream)) != cudaSuccess)
+    return fail_cuda("quantize q", e);
+  if ((e = launch_fake_quant(k, rk, D, D, nullptr, kUnitBf16, kt, D, nullptr, 0, nullptr, 0,
+                             stream)) != cudaSuccess)
+    return fail_cuda("quantize k", e);
+  if ((e = launch_fake_quant(v, rk, D, D, nullptr, kUnitF16, vt, D, nullptr, 0, nullptr, 0,
+                             stream)) != cudaSuccess)
+    return fail_cuda("quantize v", e);
   const AttnShape s{B, Nq, Nkv, H, D, scale, causal};
-  return from_cuda(launch_attn_fwd(s, mq, mk, mv, o, stats, err, stream));
+  return from_cuda("attn_fwd", launch_attn_fwd(s, mq, mk, mv, o, stats, err, stream));
 }
 
 nvq_status attn_qat_bwd(const void* q, const void* k, const void* v, const void* o,
@@ -281,27 +362,34 @@ nvq_status attn_qat_bwd(const void* q, const void* k, const void* v, const void*
   void* qt = wb + w.q;
   void* kt = wb + w.k;
   void* vt = wb + w.v;
-  float* dq_acc = reinterpret_cast<float*>(wb + w.dq);
   float* delta = reinterpret_cast<float*>(wb + w.delta);
-  CUtensorMap mq, mk, mv, mdo;
-  if (!make_bnhd_map(&mq, qt, B, Nq, H, D, false) ||
-      !make_bnhd_map(&mk, kt, B, Nkv, H, D, false) ||
-      !make_bnhd_map(&mv, vt, B, Nkv, H, D, false) ||
-      !make_bnhd_map(&mdo, dout, B, Nq, H, D, false))
-    return NVQ_ERR_CUDA;
+  CUtensorMap mq, mk, mv, mdo, mk64, mv64;
+  int r;
+  if ((r = make_bnhd_map(&mq, qt, B, Nq, H, D, false)) != 0 ||
+      (r = make_bnhd_map(&mk, kt, B, Nkv, H, D, false)) != 0 ||
+      (r = make_bnhd_map(&mv, vt, B, Nkv, H, D, false)) != 0 ||
+      (r = make_bnhd_map(&mdo, dout, B, Nq, H, D, false)) != 0 ||
+      (r = make_bnhd_map(&mk64, kt, B, Nkv, H, D, false, 64)) != 0 ||
+      (r = make_bnhd_map(&mv64, vt, B, Nkv, H, D, false, 64)) != 0)
+    return fail_driver("cuTensorMapEncodeTiled", r);
   const int64_t rq = static_cast<int64_t>(B) * Nq * H, rk = static_cast<int64_t>(B) * Nkv * H;
   const AttnShape s{B, Nq, Nkv, H, D, scale, causal};
-  cudaError_t e =
-      launch_fake_quant(q, rq, D, D, nullptr, kUnitBf16, qt, D, nullptr, 0, nullptr, 0, stream);
-  if (e == cudaSuccess)
-    e = launch_fake_quant(k, rk, D, D, nullptr, kUnitBf16, kt, D, nullptr, 0, nullptr, 0, stream);
-  if (e == cudaSuccess)
-    e = launch_fake_quant(v, rk, D, D, nullptr, kUnitBf16, vt, D, nullptr, 0, nullptr, 0, stream);
-  if (e == cudaSuccess) e = launch_bwd_prep(s, o, dout, delta, dq_acc, stream);
-  if (e == cudaSuccess)
-    e = launch_attn_bwd(s, mq, mk, mv, mdo, stats, delta, dq_acc, dk, dv, err, stream);
-  if (e == cudaSuccess) e = launch_dq_convert(s, dq_acc, dq, stream);
-  return from_cuda(e);
+  cudaError_t e;
+  if ((e = launch_fake_quant(q, rq, D, D, nullptr, kUnitBf16, qt, D, nullptr, 0, nullptr, 0,
+                             stream)) != cudaSuccess)
+    return fail_cuda("quantize q", e);
+  if ((e = launch_fake_quant(k, rk, D, D, nullptr, kUnitBf16, kt, D, nullptr, 0, nullptr, 0,
+                             stream)) != cudaSuccess)
+    return fail_cuda("quantize k", e);
+  if ((e = launch_fake_quant(v, rk, D, D, nullptr, kUnitBf16, vt, D, nullptr, 0, nullptr, 0,
+                             stream)) != cudaSuccess)
+    return fail_cuda("quantize v", e);
+  if ((e = launch_bwd_prep(s, o, dout, delta, stream)) != cudaSuccess)
+    return fail_cuda("bwd_prep", e);
+  if ((e = launch_attn_bwd(s, mq, mk, mv, mdo, stats, delta, dk, dv, err, stream)) != cudaSuccess)
+    return fail_cuda("attn_bwd (dK, dV)", e);
+  return from_cuda("attn_bwd_dq", launch_attn_bwd_dq(s, mq, mdo, mk64, mv64, stats, delta, dq,
+                                                     err, stream));
 }
 
 nvq_status nvq_selftest_umma(const void* a, const void* b, float* c, int N, int K, int a_mn,
@@ -313,17 +401,18 @@ nvq_status nvq_selftest_umma(const void* a, const void* b, float* c, int N, int 
   int* err = error_word();
   if (err == nullptr) return NVQ_ERR_CUDA;
   CUtensorMap ma, mb;
-  const bool ok = (a_mn ? make_2d_map(&ma, a, K, 128, K) : make_2d_map(&ma, a, 128, K, 128)) &&
-                  (b_mn ? make_2d_map(&mb, b, K, N, K) : make_2d_map(&mb, b, N, K, N));
-  if (!ok) return NVQ_ERR_CUDA;
-  return from_cuda(launch_selftest_umma(ma, mb, c, N, K, a_mn, b_mn, err, stream));
+  int r;
+  if ((r = a_mn ? make_2d_map(&ma, a, K, 128, K) : make_2d_map(&ma, a, 128, K, 128)) != 0 ||
+      (r = b_mn ? make_2d_map(&mb, b, K, N, K) : make_2d_map(&mb, b, N, K, N)) != 0)
+    return fail_driver("cuTensorMapEncodeTiled", r);
+  return from_cuda("selftest_umma", launch_selftest_umma(ma, mb, c, N, K, a_mn, b_mn, err, stream));
 }
 
 nvq_status nvq_selftest_timeout(int64_t limit_ns, nvq_stream_t stream) {
   if (limit_ns < 1 || limit_ns > 1000000000) return NVQ_ERR_INVALID;
   int* err = error_word();
   if (err == nullptr) return NVQ_ERR_CUDA;
-  return from_cuda(launch_selftest_timeout(limit_ns, err, stream));
+  return from_cuda("selftest_timeout", launch_selftest_timeout(limit_ns, err, stream));
 }
 
 }  // extern "C"

@@ -1,27 +1,30 @@
-// Attn-QAT straight-through backward on sm_103a.
+// Attn-QAT straight-through backward on sm_103a, dK/dV part (key-outer), and
+// the delta pre-pass.
 //
-// Kernels, in launch order:
-//   bwd_prep    delta_i = sum_d dO_id * O_id (fp32), zeroes the fp32 dQ accumulator
+// Kernels, in launch order (attn_bwd_dq.cu adds the dQ kernel after them):
+//   bwd_prep    delta_i = sum_d dO_id * O_id (fp32)
 //   attn_bwd    one CTA per (128-key tile, head, batch); K~ and V~ stay in shared
 //               memory, the dK and dV accumulators in TMEM; the CTA loops over the
 //               128-query tiles:
 //                 S  = Q~ K~^T, dP = dO V~^T              (BF16 UMMA -> TMEM)
 //                 P  = exp(scale*S - m)                    (m from the forward)
 //                 P~ = fq16(P) per 16 keys                 (bit-identical to the forward)
-//                 A  = P / l,   dS = A * (dP - delta)
-//                 P~/l and dS -> shared memory (bf16)
-//                 dV += (P~/l)^T dO, dK += dS^T Q~, dQ_i = dS K~   (BF16 UMMA)
-//                 dQ_i * scale is added to the fp32 accumulator (vector reductions)
-//               then writes dK * scale and dV (bf16).
-//   dq_convert  fp32 dQ accumulator -> bf16
+//                 A  = P / l,   dS = scale * A * (dP - delta)
+//                 P~/l and dS -> shared memory (bf16, one buffer used in turn)
+//                 dV += (P~/l)^T dO, dK += dS^T Q~         (BF16 UMMA)
+//               then writes dK and dV (bf16).
 // ("attn_qat_train" API page, attn_qat_train(): the backward uses the quantized
 // Q, K, V and the quantized P, with straight-through gradients.)
+// dQ is computed by a separate query-outer kernel rather than added into an
+// fp32 accumulator from here: with 128-key tiles those additions would move
+// (N/128) x |dQ| bytes through L2 reductions, which cost more than the extra
+// S and dP UMMAs of the second kernel.
 //
 // Roles (576 threads, one CTA per SM): warps 0-15 elementwise in four
 // warpgroups, each owning 32 keys of the tile (thread t = query row t = TMEM
-// lane t for S/dP/dQ, key row t for dK/dV), warp 16 TMA, warp 17 TMEM
-// allocation and UMMA issue.
-// TMEM columns: [0,128) S then dQ, [128,256) dP, [256,256+D) dV, [384,384+D) dK.
+// lane t for S/dP, key row t for dK/dV), warp 16 TMA, warp 17 TMEM allocation
+// and UMMA issue.
+// TMEM columns: [0,128) S, [128,256) dP, [256,256+D) dV, [384,384+D) dK.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -44,16 +47,6 @@ __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
-}
-
-__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c),
-               "f"(d)
-               : "memory");
-}
-
-__device__ __forceinline__ void red_add_v2(float* p, float a, float b) {
-  asm volatile("red.global.add.v2.f32 [%0], {%1, %2};" ::"l"(p), "f"(a), "f"(b) : "memory");
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -84,7 +77,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                     const float* __restrict__ stats, const float* __restrict__ delta,
-                    float* __restrict__ dq_acc, __nv_bfloat16* __restrict__ dk,
+                    __nv_bfloat16* __restrict__ dk,
                     __nv_bfloat16* __restrict__ dv, int Nq, int Nkv, int H, float scale,
                     int causal, int* __restrict__ err) {
   using L = BwdLayout<D>;
@@ -105,24 +98,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* pt_full = bars + 7;
   uint64_t* pt_free = bars + 8;
   uint64_t* ds_full = bars + 9;
-  uint64_t* dq_full = bars + 10;
-  uint64_t* dq_free = bars + 11;
-  uint64_t* dkdv_done = bars + 12;
-  uint64_t* mma_drain = bars + 13;
+  uint64_t* ds_free = bars + 10;
+  uint64_t* dkdv_done = bars + 11;
+  uint64_t* mma_drain = bars + 12;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kAbort);
 
   const int n_q_all = (Nq + kTile - 1) / kTile;
   const int i_begin = causal ? kt : 0;  // causal requires Nq == Nkv
   const int n_iter = n_q_all - i_begin;
-  // Query tile of iteration `it`.  Each CTA starts at its own offset, so that
-  // CTAs running at the same time add their dQ partials into different rows of
-  // the accumulator instead of contending for the same L2 lines.
-  const int q_rot = n_iter > 0 ? kt % n_iter : 0;
-  auto qtile = [&](int it) -> int {
-    const int k = it + q_rot;
-    return i_begin + (k >= n_iter ? k - n_iter : k);
-  };
+  auto qtile = [&](int it) -> int { return i_begin + it; };
+
 
   if (threadIdx.x == 0) {
     *abort = 0;
@@ -136,8 +122,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(pt_full, kElemWarps);
     mbar_init(pt_free, 1);
     mbar_init(ds_full, kElemWarps);
-    mbar_init(dq_full, 1);
-    mbar_init(dq_free, kElemWarps);
+    mbar_init(ds_free, 1);
     mbar_init(dkdv_done, 1);
     mbar_init(mma_drain, 1);
     fence_mbar_init();
@@ -189,12 +174,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------------- MMA
-    // Issue order per query tile i: dV_i, S_{i+1}, dK_i, dQ_i, dP_{i+1}, so the
+    // Issue order per query tile i: dV_i, S_{i+1}, dK_i, dP_{i+1}, so the
     // elementwise work of one tile overlaps the UMMAs of its neighbours.
     if (lane == 0) {
       constexpr uint32_t idesc_s = idesc_f16(128, 128, 1, 0, 0);  // S, dP
       constexpr uint32_t idesc_t = idesc_f16(128, D, 1, 1, 1);    // dV, dK (A, B MN-major)
-      constexpr uint32_t idesc_q = idesc_f16(128, D, 1, 0, 1);    // dQ (A K-major, B MN-major)
       const uint32_t k_addr = smem_u32(smem + L::kK);
       const uint32_t v_addr = smem_u32(smem + L::kV);
       const uint32_t q_addr = smem_u32(smem + L::kQ);
@@ -239,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!(ok = mbar_wait(&qdo_full[st ^ 1], static_cast<uint32_t>(((it + 1) >> 1) & 1), abort)))
             break;
           tc_fence_after();
-          issue_s(st ^ 1);
+          issue_s(st ^ 1);  // S was read before pt_full_i
         }
         if (!(ok = mbar_wait(ds_full, ph, abort))) break;
         tc_fence_after();
@@ -248,20 +232,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_f16_ss(tmem + 384, sdesc_sw128(pd_addr + kk * 2048, kAtomBlock, 1024),
                       sdesc_sw128(q_addr + st * L::kTileBytes + kk * 2048, kAtomBlock, 1024),
                       idesc_t, (it > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {  // dQ_i = dS K~: contraction over 128 keys
-          const uint32_t aoff = (kk >> 2) * kAtomBlock + (kk & 3) * 32;
-          umma_f16_ss(tmem + 128, sdesc_sw128(pd_addr + aoff, 16, 1024),
-                      sdesc_sw128(k_addr + kk * 2048, kAtomBlock, 1024), idesc_q,
-                      kk > 0 ? 1u : 0u);
-        }
-        umma_commit(dq_full);
+        umma_commit(ds_free);
         umma_commit(&qdo_empty[st]);
-        if (it + 1 < n_iter) {
-          if (!(ok = mbar_wait(dq_free, ph, abort))) break;
-          tc_fence_after();
-          issue_dp(st ^ 1);
-        }
+        if (it + 1 < n_iter) issue_dp(st ^ 1);  // dP was read before ds_full_i
       }
       if (ok && n_iter > 0) umma_commit(dkdv_done);
       umma_commit(mma_drain);
@@ -269,9 +242,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // --------------------------------------------------------- elementwise
-    // Warpgroup g (0..3) owns keys [32g, 32g+32) of every tile and dQ columns
-    // [g*D/4, (g+1)*D/4); thread t of the group owns query row t (TMEM lane t).
-    // dS is stored pre-multiplied by `scale`, so dK and dQ come out scaled.
+    // Warpgroup g (0..3) owns keys [32g, 32g+32) of every tile; thread t of the
+    // group owns query row t (TMEM lane t).  dS is stored pre-multiplied by
+    // `scale`, so dK comes out scaled.
     const int g = warp >> 2;
     const int t = threadIdx.x & 127;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -280,7 +253,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float* lse_g = stats + (static_cast<int64_t>(b) * H + h) * 2 * Nq;
     const float* m_g = lse_g + Nq;
     const float* delta_g = delta + (static_cast<int64_t>(b) * H + h) * Nq;
-    constexpr int kDqCols = D / 4;
     const uint32_t key_col = static_cast<uint32_t>(g * 32);
     bool ok = true;
     uint32_t r[32];
@@ -294,41 +266,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     float nm, nlse, ndl;
     load_row(0, nm, nlse, ndl);
-    // dQ of tile it_prev: TMEM [128, 128+D) -> registers (16-lane x 8-column
-    // loads: four neighbouring threads hold 32 contiguous bytes of one row), the
-    // columns are released (dq_free, when `release`), then every (row, 2
-    // columns) pair is added into the fp32 accumulator, so each group of four
-    // threads covers one full 32-byte sector.
-    auto read_dq = [&](int it_prev, bool release) {
-      const int qbase = qtile(it_prev) * kTile + (warp & 3) * 32;
-      constexpr int kReps = kDqCols / 8;
-      uint32_t v[2][kReps][4];
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-        for (int k = 0; k < kReps; ++k)
-          tmem_ld16x256(tmem + lane_base + (static_cast<uint32_t>(hh * 16) << 16) + 128 +
-                            g * kDqCols + 8 * k,
-                        v[hh][k]);
-      tmem_wait_ld();
-      if (release) {
-        tc_fence_before();
-        mbar_arrive_warp(dq_free);
-      }
-      const int col = g * kDqCols + 2 * (lane & 3);
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int row_a = qbase + hh * 16 + (lane >> 2);
-        const int row_b = row_a + 8;
-        float* pa = dq_acc + ((static_cast<int64_t>(b) * Nq + row_a) * H + h) * D + col;
-        float* pb = dq_acc + ((static_cast<int64_t>(b) * Nq + row_b) * H + h) * D + col;
-#pragma unroll
-        for (int k = 0; k < kReps; ++k) {
-          if (row_a < Nq) red_add_v2(pa + 8 * k, __uint_as_float(v[hh][k][0]), __uint_as_float(v[hh][k][1]));
-          if (row_b < Nq) red_add_v2(pb + 8 * k, __uint_as_float(v[hh][k][2]), __uint_as_float(v[hh][k][3]));
-        }
-      }
-    };
     for (int it = 0; it < n_iter && ok; ++it) {
       const int qi = qtile(it);
       const int qrow = qi * kTile + t;
@@ -376,8 +313,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       tc_fence_before();
-      // the P~/dS buffer is free once dK and dQ of the previous tile are done
-      if (it > 0 && !(ok = mbar_wait_warp(dq_full, ph ^ 1u, abort))) break;
+      // the P~/dS buffer is free once dK of the previous tile is done
+      if (it > 0 && !(ok = mbar_wait_warp(ds_free, ph ^ 1u, abort))) break;
 #pragma unroll
       for (int ch = 0; ch < 4; ++ch) {
         const uint32_t off = sw128_offset(t, key_col + ch * 8, 128);
@@ -386,11 +323,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       fence_proxy_async_smem();
       mbar_arrive_warp(pt_full);
-      // ---- dQ of the previous tile
-      if (it > 0) {
-        tc_fence_after();
-        read_dq(it - 1, true);
-      }
       // ---- dS part: dP -> dS = scale * A * (dP - delta), A = P / l
       if (!(ok = mbar_wait_warp(dp_full, ph, abort))) break;
       tc_fence_after();
@@ -419,11 +351,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       fence_proxy_async_smem();
       mbar_arrive_warp(ds_full);
-    }
-    if (ok && n_iter > 0 &&
-        (ok = mbar_wait_warp(dq_full, static_cast<uint32_t>((n_iter - 1) & 1), abort))) {
-      tc_fence_after();
-      read_dq(n_iter - 1, false);
     }
     if (ok && n_iter > 0 && (ok = mbar_wait_warp(dkdv_done, 0, abort))) {
       tc_fence_after();
@@ -470,12 +397,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// delta[b,h,i] = sum_d dO[b,i,h,d] * O[b,i,h,d]; zero the dQ accumulator row.
+// delta[b,h,i] = sum_d dO[b,i,h,d] * O[b,i,h,d].
 template <int D>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __restrict__ o,
                                                        const __nv_bfloat16* __restrict__ dout,
-                                                       float* __restrict__ delta,
-                                                       float* __restrict__ dq_acc, int B, int Nq,
+                                                       float* __restrict__ delta, int B, int Nq,
                                                        int H) {
   // 8 threads per (b, i, h) row; each takes D/8 consecutive elements.
   const int64_t rows = static_cast<int64_t>(B) * Nq * H;
@@ -497,9 +423,6 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
         acc = fmaf(__uint_as_float(aw[u] & 0xFFFF0000u), __uint_as_float(gw[u] & 0xFFFF0000u),
                    acc);
       }
-      float4* z = reinterpret_cast<float4*>(dq_acc + off + c);
-      z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
-      z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
   }
   acc += __shfl_xor_sync(0xFFFFFFFFu, acc, 1);
@@ -514,38 +437,25 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
   }
 }
 
-__global__ void __launch_bounds__(256) dq_convert_kernel(const float* __restrict__ acc,
-                                                         __nv_bfloat16* __restrict__ dq,
-                                                         int64_t n8) {
-  const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n8;
-       i += step) {
-    const float4 a = reinterpret_cast<const float4*>(acc)[2 * i];
-    const float4 c = reinterpret_cast<const float4*>(acc)[2 * i + 1];
-    reinterpret_cast<uint4*>(dq)[i] = make_uint4(pack_bf16(a.x, a.y), pack_bf16(a.z, a.w),
-                                                 pack_bf16(c.x, c.y), pack_bf16(c.z, c.w));
-  }
-}
-
 }  // namespace
 
 cudaError_t launch_bwd_prep(const AttnShape& s, const void* o, const void* dout, float* delta,
-                            float* dq_acc, cudaStream_t stream) {
+                            cudaStream_t stream) {
   const int64_t rows = static_cast<int64_t>(s.B) * s.Nq * s.H;
   const int64_t threads = rows * 8;
   const int grid = static_cast<int>((threads + 255) / 256);
   const auto* op = static_cast<const __nv_bfloat16*>(o);
   const auto* gp = static_cast<const __nv_bfloat16*>(dout);
   if (s.D == 128)
-    bwd_prep_kernel<128><<<grid, 256, 0, stream>>>(op, gp, delta, dq_acc, s.B, s.Nq, s.H);
+    bwd_prep_kernel<128><<<grid, 256, 0, stream>>>(op, gp, delta, s.B, s.Nq, s.H);
   else
-    bwd_prep_kernel<64><<<grid, 256, 0, stream>>>(op, gp, delta, dq_acc, s.B, s.Nq, s.H);
+    bwd_prep_kernel<64><<<grid, 256, 0, stream>>>(op, gp, delta, s.B, s.Nq, s.H);
   return cudaGetLastError();
 }
 
 cudaError_t launch_attn_bwd(const AttnShape& s, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, const CUtensorMap& tdo, const float* stats,
-                            const float* delta, float* dq_acc, void* dk, void* dv, int* err,
+                            const float* delta, void* dk, void* dv, int* err,
                             cudaStream_t stream) {
   const dim3 grid((s.Nkv + kTile - 1) / kTile, s.H, s.B);
   auto* dkp = static_cast<__nv_bfloat16*>(dk);
@@ -556,25 +466,15 @@ cudaError_t launch_attn_bwd(const AttnShape& s, const CUtensorMap& tq, const CUt
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
     if (e != cudaSuccess) return e;
     attn_bwd_kernel<128><<<grid, kThreads, L::kAlloc, stream>>>(
-        tq, tk, tv, tdo, stats, delta, dq_acc, dkp, dvp, s.Nq, s.Nkv, s.H, s.scale, s.causal, err);
+        tq, tk, tv, tdo, stats, delta, dkp, dvp, s.Nq, s.Nkv, s.H, s.scale, s.causal, err);
   } else {
     using L = BwdLayout<64>;
     cudaError_t e = cudaFuncSetAttribute(attn_bwd_kernel<64>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
     if (e != cudaSuccess) return e;
     attn_bwd_kernel<64><<<grid, kThreads, L::kAlloc, stream>>>(
-        tq, tk, tv, tdo, stats, delta, dq_acc, dkp, dvp, s.Nq, s.Nkv, s.H, s.scale, s.causal, err);
+        tq, tk, tv, tdo, stats, delta, dkp, dvp, s.Nq, s.Nkv, s.H, s.scale, s.causal, err);
   }
-  return cudaGetLastError();
-}
-
-cudaError_t launch_dq_convert(const AttnShape& s, const float* dq_acc, void* dq,
-                              cudaStream_t stream) {
-  const int64_t n8 = static_cast<int64_t>(s.B) * s.Nq * s.H * s.D / 8;
-  int64_t grid = (n8 + 255) / 256;
-  if (grid > 152 * 8) grid = 152 * 8;
-  dq_convert_kernel<<<static_cast<int>(grid), 256, 0, stream>>>(
-      dq_acc, static_cast<__nv_bfloat16*>(dq), n8);
   return cudaGetLastError();
 }
 

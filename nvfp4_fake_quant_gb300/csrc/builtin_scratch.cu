@@ -15,6 +15,7 @@
 #include <cuda_runtime.h>
 
 #include "nvfp4attn.h"
+#include "nvq_internal.h"
 
 namespace {
 
@@ -30,12 +31,15 @@ void* g_scratch_ptr[kMaxDevices] = {};
 // performs the lookup).
 nvq_status scratch_address(void** out) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return NVQ_ERR_CUDA;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return nvq::fail_cuda("cudaGetDevice", e);
+  if (dev < 0 || dev >= kMaxDevices)
+    return nvq::fail_cuda("device ordinal out of range", cudaErrorInvalidDevice);
   std::lock_guard<std::mutex> lock(g_scratch_mu);
   if (g_scratch_ptr[dev] == nullptr) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_bwd_scratch) != cudaSuccess || p == nullptr)
-      return NVQ_ERR_CUDA;
+    e = cudaGetSymbolAddress(&p, g_bwd_scratch);
+    if (e != cudaSuccess) return nvq::fail_cuda("cudaGetSymbolAddress(scratch)", e);
     g_scratch_ptr[dev] = p;
   }
   *out = g_scratch_ptr[dev];
@@ -55,8 +59,8 @@ extern "C" nvq_status attn_qat_bwd_builtin_scratch(const void* q, const void* k,
   void* ws = nullptr;
   const nvq_status st = scratch_address(&ws);
   if (st != NVQ_OK) return st;
-  // The scratch needs no clearing here: the backward overwrites the quantized
-  // copies and delta, and its first kernel zeroes the fp32 dQ accumulator.
+  // The scratch needs no clearing: the backward writes the quantized copies and
+  // delta before reading them.
   return attn_qat_bwd(q, k, v, o, stats, dout, dq, dk, dv, B, Nq, Nkv, H, D, scale, causal, ws,
                       kBuiltinScratchBytes, stream);
 }

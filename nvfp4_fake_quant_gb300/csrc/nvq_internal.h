@@ -7,6 +7,8 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include "nvfp4attn.h"
+
 namespace nvq {
 
 constexpr int kTile = 128;  // query / key rows per attention tile
@@ -27,26 +29,37 @@ struct AttnShape {
   int causal;
 };
 
-// Tensor maps over [B, N, H, D] 16-bit tensors, box {64, 128, 1, 1}, 128-byte swizzle.
-bool make_bnhd_map(CUtensorMap* map, const void* base, int B, int N, int H, int D, bool f16);
+// Record "where: CUDA error" as this host thread's error detail (returned by
+// nvq_last_error_detail) and return NVQ_ERR_CUDA.
+nvq_status fail_cuda(const char* where, cudaError_t e);
+nvq_status fail_driver(const char* where, int cu_result);
+
+// Tensor maps over [B, N, H, D] 16-bit tensors, box {64, box_rows, 1, 1}, 128-byte swizzle.
+// Return the CUresult of cuTensorMapEncodeTiled (0 on success).
+int make_bnhd_map(CUtensorMap* map, const void* base, int B, int N, int H, int D, bool f16,
+                   int box_rows = kTile);
 
 cudaError_t launch_attn_fwd(const AttnShape& s, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, void* o, float* stats, int* err,
                             cudaStream_t stream);
 cudaError_t launch_bwd_prep(const AttnShape& s, const void* o, const void* dout, float* delta,
-                            float* dq_acc, cudaStream_t stream);
+                            cudaStream_t stream);
+// dK, dV (key-outer; Q~, K~, V~, dO maps with 128-row boxes)
 cudaError_t launch_attn_bwd(const AttnShape& s, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, const CUtensorMap& tdo, const float* stats,
-                            const float* delta, float* dq_acc, void* dk, void* dv, int* err,
+                            const float* delta, void* dk, void* dv, int* err,
                             cudaStream_t stream);
-cudaError_t launch_dq_convert(const AttnShape& s, const float* dq_acc, void* dq,
-                              cudaStream_t stream);
+// dQ (query-outer; Q~, dO maps with 128-row boxes, K~, V~ maps with 64-row boxes)
+cudaError_t launch_attn_bwd_dq(const AttnShape& s, const CUtensorMap& tq, const CUtensorMap& tdo,
+                               const CUtensorMap& tk64, const CUtensorMap& tv64,
+                               const float* stats, const float* delta, void* dq, int* err,
+                               cudaStream_t stream);
 
 cudaError_t launch_selftest_umma(const CUtensorMap& ta, const CUtensorMap& tb, float* c, int N,
                                  int K, int a_mn, int b_mn, int* err, cudaStream_t stream);
 cudaError_t launch_selftest_timeout(int64_t limit_ns, int* err, cudaStream_t stream);
 
 // Maps a [rows, cols] 16-bit row-major matrix with a box of {64, box_rows}.
-bool make_2d_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_rows);
+int make_2d_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_rows);
 
 }  // namespace nvq
