@@ -138,108 +138,104 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kTmaWarp) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      tma_prefetch_desc(&tq);
-      tma_prefetch_desc(&tk);
-      tma_prefetch_desc(&tv);
-      tma_prefetch_desc(&tdo);
-      mbar_arrive_expect_tx(kv_full, 2u * L::kTileBytes);
+    tma_prefetch_desc(&tq);
+    tma_prefetch_desc(&tk);
+    tma_prefetch_desc(&tv);
+    tma_prefetch_desc(&tdo);
+    mbar_arrive_expect_tx_w(kv_full, 2u * L::kTileBytes);
+#pragma unroll
+    for (int blk = 0; blk < D / 64; ++blk) {
+      tma_load_4d_w(smem + L::kK + blk * kAtomBlock, &tk, blk * 64, k0, h, b, kv_full);
+      tma_load_4d_w(smem + L::kV + blk * kAtomBlock, &tv, blk * 64, k0, h, b, kv_full);
+    }
+    int last[2] = {-1, -1};
+    bool ok = true;
+    for (int it = 0; it < n_iter; ++it) {
+      const int st = it & 1;
+      if (!(ok = mbar_wait_warp(&qdo_empty[st], ((it >> 1) & 1) ^ 1, abort))) break;
+      const int qrow0 = qtile(it) * kTile;
+      mbar_arrive_expect_tx_w(&qdo_full[st], 2u * L::kTileBytes);
 #pragma unroll
       for (int blk = 0; blk < D / 64; ++blk) {
-        tma_load_4d(smem + L::kK + blk * kAtomBlock, &tk, blk * 64, k0, h, b, kv_full);
-        tma_load_4d(smem + L::kV + blk * kAtomBlock, &tv, blk * 64, k0, h, b, kv_full);
-      }
-      int last[2] = {-1, -1};
-      bool ok = true;
-      for (int it = 0; it < n_iter; ++it) {
-        const int st = it & 1;
-        if (!(ok = mbar_wait(&qdo_empty[st], ((it >> 1) & 1) ^ 1, abort))) break;
-        const int qrow0 = qtile(it) * kTile;
-        mbar_arrive_expect_tx(&qdo_full[st], 2u * L::kTileBytes);
-#pragma unroll
-        for (int blk = 0; blk < D / 64; ++blk) {
-          tma_load_4d(smem + L::kQ + st * L::kTileBytes + blk * kAtomBlock, &tq, blk * 64, qrow0,
+        tma_load_4d_w(smem + L::kQ + st * L::kTileBytes + blk * kAtomBlock, &tq, blk * 64, qrow0,
                       h, b, &qdo_full[st]);
-          tma_load_4d(smem + L::kDO + st * L::kTileBytes + blk * kAtomBlock, &tdo, blk * 64,
+        tma_load_4d_w(smem + L::kDO + st * L::kTileBytes + blk * kAtomBlock, &tdo, blk * 64,
                       qrow0, h, b, &qdo_full[st]);
-        }
-        last[st] = (it >> 1) & 1;
       }
-      if (!ok) {
-        mbar_wait(kv_full, 0, nullptr, 10000000ull);
-        for (int s2 = 0; s2 < 2; ++s2)
-          if (last[s2] >= 0)
-            mbar_wait(&qdo_full[s2], static_cast<uint32_t>(last[s2]), nullptr, 10000000ull);
-      }
+      last[st] = (it >> 1) & 1;
+    }
+    if (!ok) {
+      mbar_wait_warp(kv_full, 0, nullptr, 10000000ull);
+      for (int s2 = 0; s2 < 2; ++s2)
+        if (last[s2] >= 0)
+          mbar_wait_warp(&qdo_full[s2], static_cast<uint32_t>(last[s2]), nullptr, 10000000ull);
     }
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------------- MMA
     // Issue order per query tile i: dV_i, S_{i+1}, dK_i, dP_{i+1}, so the
     // elementwise work of one tile overlaps the UMMAs of its neighbours.
-    if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_f16(128, 128, 1, 0, 0);  // S, dP
-      constexpr uint32_t idesc_t = idesc_f16(128, D, 1, 1, 1);    // dV, dK (A, B MN-major)
-      const uint32_t k_addr = smem_u32(smem + L::kK);
-      const uint32_t v_addr = smem_u32(smem + L::kV);
-      const uint32_t q_addr = smem_u32(smem + L::kQ);
-      const uint32_t do_addr = smem_u32(smem + L::kDO);
-      const uint32_t pd_addr = smem_u32(smem + L::kPD);
-      auto issue_s = [&](int st) {  // S = Q~_st K~^T -> TMEM [0,128)
+    constexpr uint32_t idesc_s = idesc_f16(128, 128, 1, 0, 0);  // S, dP
+    constexpr uint32_t idesc_t = idesc_f16(128, D, 1, 1, 1);    // dV, dK (A, B MN-major)
+    const uint32_t k_addr = smem_u32(smem + L::kK);
+    const uint32_t v_addr = smem_u32(smem + L::kV);
+    const uint32_t q_addr = smem_u32(smem + L::kQ);
+    const uint32_t do_addr = smem_u32(smem + L::kDO);
+    const uint32_t pd_addr = smem_u32(smem + L::kPD);
+    auto issue_s = [&](int st) {  // S = Q~_st K~^T -> TMEM [0,128)
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kAtomBlock + (kk & 3) * 32;
-          umma_f16_ss(tmem + 0, sdesc_sw128(q_addr + st * L::kTileBytes + off, 16, 1024),
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * kAtomBlock + (kk & 3) * 32;
+        umma_f16_ss_w(tmem + 0, sdesc_sw128(q_addr + st * L::kTileBytes + off, 16, 1024),
                       sdesc_sw128(k_addr + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
-        }
-        umma_commit(s_full);
-      };
-      auto issue_dp = [&](int st) {  // dP = dO_st V~^T -> TMEM [128,256)
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kAtomBlock + (kk & 3) * 32;
-          umma_f16_ss(tmem + 128, sdesc_sw128(do_addr + st * L::kTileBytes + off, 16, 1024),
-                      sdesc_sw128(v_addr + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
-        }
-        umma_commit(dp_full);
-      };
-      bool ok = mbar_wait(kv_full, 0, abort) && (n_iter > 0) && mbar_wait(&qdo_full[0], 0, abort);
-      if (ok) {
-        tc_fence_after();
-        issue_s(0);
-        issue_dp(0);
       }
-      for (int it = 0; it < n_iter && ok; ++it) {
-        const int st = it & 1;
-        const uint32_t ph = static_cast<uint32_t>(it & 1);
-        if (!(ok = mbar_wait(pt_full, ph, abort))) break;
-        tc_fence_after();
+      umma_commit_w(s_full);
+    };
+    auto issue_dp = [&](int st) {  // dP = dO_st V~^T -> TMEM [128,256)
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)  // dV += (P~/l)^T dO: contraction over 128 queries
-          umma_f16_ss(tmem + 256, sdesc_sw128(pd_addr + kk * 2048, kAtomBlock, 1024),
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * kAtomBlock + (kk & 3) * 32;
+        umma_f16_ss_w(tmem + 128, sdesc_sw128(do_addr + st * L::kTileBytes + off, 16, 1024),
+                      sdesc_sw128(v_addr + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+      }
+      umma_commit_w(dp_full);
+    };
+    bool ok = mbar_wait_warp(kv_full, 0, abort) && (n_iter > 0) && mbar_wait_warp(&qdo_full[0], 0, abort);
+    if (ok) {
+      tc_fence_after();
+      issue_s(0);
+      issue_dp(0);
+    }
+    for (int it = 0; it < n_iter && ok; ++it) {
+      const int st = it & 1;
+      const uint32_t ph = static_cast<uint32_t>(it & 1);
+      if (!(ok = mbar_wait_warp(pt_full, ph, abort))) break;
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)  // dV += (P~/l)^T dO: contraction over 128 queries
+        umma_f16_ss_w(tmem + 256, sdesc_sw128(pd_addr + kk * 2048, kAtomBlock, 1024),
                       sdesc_sw128(do_addr + st * L::kTileBytes + kk * 2048, kAtomBlock, 1024),
                       idesc_t, (it > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(pt_free);
-        if (it + 1 < n_iter) {
-          if (!(ok = mbar_wait(&qdo_full[st ^ 1], static_cast<uint32_t>(((it + 1) >> 1) & 1), abort)))
-            break;
-          tc_fence_after();
-          issue_s(st ^ 1);  // S was read before pt_full_i
-        }
-        if (!(ok = mbar_wait(ds_full, ph, abort))) break;
+      umma_commit_w(pt_free);
+      if (it + 1 < n_iter) {
+        if (!(ok = mbar_wait_warp(&qdo_full[st ^ 1], static_cast<uint32_t>(((it + 1) >> 1) & 1), abort)))
+          break;
         tc_fence_after();
+        issue_s(st ^ 1);  // S was read before pt_full_i
+      }
+      if (!(ok = mbar_wait_warp(ds_full, ph, abort))) break;
+      tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)  // dK += dS^T Q~: contraction over 128 queries
-          umma_f16_ss(tmem + 384, sdesc_sw128(pd_addr + kk * 2048, kAtomBlock, 1024),
+      for (int kk = 0; kk < 8; ++kk)  // dK += dS^T Q~: contraction over 128 queries
+        umma_f16_ss_w(tmem + 384, sdesc_sw128(pd_addr + kk * 2048, kAtomBlock, 1024),
                       sdesc_sw128(q_addr + st * L::kTileBytes + kk * 2048, kAtomBlock, 1024),
                       idesc_t, (it > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(ds_free);
-        umma_commit(&qdo_empty[st]);
-        if (it + 1 < n_iter) issue_dp(st ^ 1);  // dP was read before ds_full_i
-      }
-      if (ok && n_iter > 0) umma_commit(dkdv_done);
-      umma_commit(mma_drain);
-      mbar_wait(mma_drain, 0, nullptr, 10000000ull);
+      umma_commit_w(ds_free);
+      umma_commit_w(&qdo_empty[st]);
+      if (it + 1 < n_iter) issue_dp(st ^ 1);  // dP was read before ds_full_i
     }
+    if (ok && n_iter > 0) umma_commit_w(dkdv_done);
+    umma_commit_w(mma_drain);
+    mbar_wait_warp(mma_drain, 0, nullptr, 10000000ull);
   } else {
     // --------------------------------------------------------- elementwise
     // Warpgroup g (0..3) owns keys [32g, 32g+32) of every tile; thread t of the

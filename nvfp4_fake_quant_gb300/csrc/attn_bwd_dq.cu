@@ -12,10 +12,14 @@
 //   dQ += dS K~                  (BF16 UMMA, accumulated in TMEM over all keys)
 // and dQ is written once, in bf16: no atomics, no fp32 accumulator in HBM.
 //
-// Roles (576 threads, one CTA per SM): warps 0-15 elementwise in four warpgroups,
-// each owning 16 keys of a step (thread t = query row t = TMEM lane t) and D/4
-// dQ columns at the end; warp 16 TMA; warp 17 TMEM allocation and UMMA issue.
-// TMEM: S at [0,64) and [64,128), dP at [128,192) and [192,256), dQ at [256,256+D).
+// Roles (576 threads, one CTA per SM): warps 0-15 elementwise, in two sets of
+// eight warps that take alternate steps (set s does steps s, s+2, ...), so one
+// set's TMEM loads, exponentials and stores overlap the other set's; within a
+// set, warpgroup gg owns keys [32gg, 32gg+32) of the step (thread t = query row
+// t = TMEM lane t).  At the end every warpgroup writes D/4 dQ columns.  Warp 16
+// issues TMA, warp 17 allocates TMEM and issues the UMMAs.
+// TMEM: S of set s at [64s, 64s+64), dP of set s at [128+64s, 192+64s), dQ at
+// [256, 256+D).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -28,6 +32,7 @@ namespace nvq {
 namespace {
 
 constexpr int kElemWarps = 16;
+constexpr int kSetWarps = 8;  // elementwise warps per set
 constexpr int kTmaWarp = 16;
 constexpr int kMmaWarp = 17;
 constexpr int kThreads = 576;
@@ -47,7 +52,7 @@ struct DqLayout {
   static constexpr uint32_t kDS = kRingOff + kRing * kKVTile;  // [2] x [128 q][64 keys] bf16
   static constexpr uint32_t kDSBytes = 128u * kStep * 2u;
   static constexpr uint32_t kBars = kDS + 2u * kDSBytes;
-  static constexpr uint32_t kNumBars = 1 + 2 * kRing + 2 * 4 + 2;
+  static constexpr uint32_t kNumBars = 1 + 2 * kRing + 2 * 3 + 2;
   static constexpr uint32_t kTmemSlot = kBars + kNumBars * 8u;
   static constexpr uint32_t kAbort = kTmemSlot + 4u;
   static constexpr uint32_t kUsed = kAbort + 4u;
@@ -80,12 +85,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* q_full = bars + 0;
   uint64_t* r_full = bars + 1;              // [kRing]
   uint64_t* r_empty = bars + 1 + kRing;     // [kRing]
-  uint64_t* s_full = bars + 1 + 2 * kRing;  // [2]
-  uint64_t* dp_full = s_full + 2;           // [2]
-  uint64_t* ds_full = s_full + 4;           // [2]
-  uint64_t* ds_free = s_full + 6;           // [2]
-  uint64_t* dq_done = s_full + 8;
-  uint64_t* mma_drain = s_full + 9;
+  uint64_t* sdp_full = bars + 1 + 2 * kRing;  // [2] S and dP of a step are in TMEM
+  uint64_t* ds_full = sdp_full + 2;           // [2] dS of a step is in shared memory
+  uint64_t* ds_free = sdp_full + 4;           // [2] dQ += dS K~ of a step is done
+  uint64_t* dq_done = sdp_full + 6;
+  uint64_t* mma_drain = sdp_full + 7;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kAbort);
 
@@ -100,9 +104,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&r_empty[s], 1);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&s_full[i], 1);
-      mbar_init(&dp_full[i], 1);
-      mbar_init(&ds_full[i], kElemWarps);
+      mbar_init(&sdp_full[i], 1);
+      mbar_init(&ds_full[i], kSetWarps);
       mbar_init(&ds_free[i], 1);
     }
     mbar_init(dq_done, 1);
@@ -121,99 +124,97 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kTmaWarp) {
     // ------------------------------------------------------------ producer
     // Q~, dO once; then K~_0, V~_0, K~_1, V~_1, ... (64-key tiles) through the ring
-    if (lane == 0) {
-      tma_prefetch_desc(&tq);
-      tma_prefetch_desc(&tdo);
-      tma_prefetch_desc(&tk64);
-      tma_prefetch_desc(&tv64);
-      mbar_arrive_expect_tx(q_full, 2u * L::kQTile);
+    tma_prefetch_desc(&tq);
+    tma_prefetch_desc(&tdo);
+    tma_prefetch_desc(&tk64);
+    tma_prefetch_desc(&tv64);
+    mbar_arrive_expect_tx_w(q_full, 2u * L::kQTile);
 #pragma unroll
-      for (int blk = 0; blk < D / 64; ++blk) {
-        tma_load_4d(smem + L::kQ + blk * L::kQBlock, &tq, blk * 64, q0, h, b, q_full);
-        tma_load_4d(smem + L::kDO + blk * L::kQBlock, &tdo, blk * 64, q0, h, b, q_full);
-      }
-      int last[kRing];
-      for (int s = 0; s < kRing; ++s) last[s] = -1;
-      bool ok = true;
-      for (int li = 0; li < 2 * n && ok; ++li) {
-        const int slot = li % kRing;
-        const uint32_t use = static_cast<uint32_t>(li / kRing);
-        if (!(ok = mbar_wait(&r_empty[slot], (use & 1u) ^ 1u, abort))) break;
-        const int j = li >> 1;
-        mbar_arrive_expect_tx(&r_full[slot], L::kKVTile);
+    for (int blk = 0; blk < D / 64; ++blk) {
+      tma_load_4d_w(smem + L::kQ + blk * L::kQBlock, &tq, blk * 64, q0, h, b, q_full);
+      tma_load_4d_w(smem + L::kDO + blk * L::kQBlock, &tdo, blk * 64, q0, h, b, q_full);
+    }
+    int last[kRing];
+    for (int s = 0; s < kRing; ++s) last[s] = -1;
+    bool ok = true;
+    for (int li = 0; li < 2 * n && ok; ++li) {
+      const int slot = li % kRing;
+      const uint32_t use = static_cast<uint32_t>(li / kRing);
+      if (!(ok = mbar_wait_warp(&r_empty[slot], (use & 1u) ^ 1u, abort))) break;
+      const int j = li >> 1;
+      mbar_arrive_expect_tx_w(&r_full[slot], L::kKVTile);
 #pragma unroll
-        for (int blk = 0; blk < D / 64; ++blk)
-          tma_load_4d(smem + L::kRingOff + slot * L::kKVTile + blk * L::kKVBlock,
+      for (int blk = 0; blk < D / 64; ++blk)
+        tma_load_4d_w(smem + L::kRingOff + slot * L::kKVTile + blk * L::kKVBlock,
                       (li & 1) ? &tv64 : &tk64, blk * 64, j * kStep, h, b, &r_full[slot]);
-        last[slot] = static_cast<int>(use & 1u);
-      }
-      if (!ok) {
-        mbar_wait(q_full, 0, nullptr, 10000000ull);
-        for (int s = 0; s < kRing; ++s)
-          if (last[s] >= 0) mbar_wait(&r_full[s], static_cast<uint32_t>(last[s]), nullptr, 10000000ull);
-      }
+      last[slot] = static_cast<int>(use & 1u);
+    }
+    if (!ok) {
+      mbar_wait_warp(q_full, 0, nullptr, 10000000ull);
+      for (int s = 0; s < kRing; ++s)
+        if (last[s] >= 0) mbar_wait_warp(&r_full[s], static_cast<uint32_t>(last[s]), nullptr, 10000000ull);
     }
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------------- MMA
     // Order: S_0, dP_0, S_1, dP_1, then per step j: dQ_j, S_{j+2}, dP_{j+2}.
-    if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_f16(128, kStep, 1, 0, 0);  // S, dP (N = 64 keys)
-      constexpr uint32_t idesc_q = idesc_f16(128, D, 1, 0, 1);      // dQ (A K-major, B MN-major)
-      const uint32_t q_addr = smem_u32(smem + L::kQ);
-      const uint32_t do_addr = smem_u32(smem + L::kDO);
-      const uint32_t ring_addr = smem_u32(smem + L::kRingOff);
-      const uint32_t ds_addr = smem_u32(smem + L::kDS);
-      auto slot_of = [](int li) { return li % kRing; };
-      auto wait_tile = [&](int li) -> bool {
-        return mbar_wait(&r_full[slot_of(li)], static_cast<uint32_t>((li / kRing) & 1), abort);
-      };
-      // S_j (or dP_j) = A (128 x D, K-major) * B^T (B = 64 x D tile, K-major)
-      auto issue_qk = [&](uint32_t a_addr, int li, uint32_t dcol, uint64_t* bar) {
-        const uint32_t bb = ring_addr + slot_of(li) * L::kKVTile;
+    constexpr uint32_t idesc_s = idesc_f16(128, kStep, 1, 0, 0);  // S, dP (N = 64 keys)
+    constexpr uint32_t idesc_q = idesc_f16(128, D, 1, 0, 1);      // dQ (A K-major, B MN-major)
+    const uint32_t q_addr = smem_u32(smem + L::kQ);
+    const uint32_t do_addr = smem_u32(smem + L::kDO);
+    const uint32_t ring_addr = smem_u32(smem + L::kRingOff);
+    const uint32_t ds_addr = smem_u32(smem + L::kDS);
+    auto slot_of = [](int li) { return li % kRing; };
+    auto wait_tile = [&](int li) -> bool {
+      return mbar_wait_warp(&r_full[slot_of(li)], static_cast<uint32_t>((li / kRing) & 1), abort);
+    };
+    // S_j (or dP_j) = A (128 x D, K-major) * B^T (B = 64 x D tile, K-major)
+    auto issue_qk = [&](uint32_t a_addr, int li, uint32_t dcol) {
+      const uint32_t bb = ring_addr + slot_of(li) * L::kKVTile;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          umma_f16_ss(tmem + dcol,
+      for (int kk = 0; kk < D / 16; ++kk) {
+        umma_f16_ss_w(tmem + dcol,
                       sdesc_sw128(a_addr + (kk >> 2) * L::kQBlock + (kk & 3) * 32, 16, 1024),
                       sdesc_sw128(bb + (kk >> 2) * L::kKVBlock + (kk & 3) * 32, 16, 1024), idesc_s,
                       kk > 0 ? 1u : 0u);
-        }
-        umma_commit(bar);
-      };
-      auto issue_step = [&](int j) -> bool {  // S_j and dP_j into buffer j % 2
-        if (!wait_tile(2 * j) || !wait_tile(2 * j + 1)) return false;
-        tc_fence_after();
-        const int bsel = j & 1;
-        issue_qk(q_addr, 2 * j, static_cast<uint32_t>(bsel * kStep), &s_full[bsel]);
-        issue_qk(do_addr, 2 * j + 1, static_cast<uint32_t>(128 + bsel * kStep), &dp_full[bsel]);
-        umma_commit(&r_empty[slot_of(2 * j + 1)]);  // V~_j is no longer needed
-        return true;
-      };
-      bool ok = mbar_wait(q_full, 0, abort);
-      if (ok) ok = issue_step(0);
-      if (ok && n > 1) ok = issue_step(1);
-      for (int j = 0; j < n && ok; ++j) {
-        const int bsel = j & 1;
-        if (!(ok = mbar_wait(&ds_full[bsel], static_cast<uint32_t>((j >> 1) & 1), abort))) break;
-        tc_fence_after();
-        const uint32_t kb = ring_addr + slot_of(2 * j) * L::kKVTile;
-        const uint32_t dsb = ds_addr + bsel * L::kDSBytes;
+      }
+    };
+    auto issue_step = [&](int j) -> bool {  // S_j and dP_j into the buffers of set j % 2
+      if (!wait_tile(2 * j) || !wait_tile(2 * j + 1)) return false;
+      tc_fence_after();
+      const int bsel = j & 1;
+      issue_qk(q_addr, 2 * j, static_cast<uint32_t>(bsel * kStep));
+      issue_qk(do_addr, 2 * j + 1, static_cast<uint32_t>(128 + bsel * kStep));
+      umma_commit_w(&sdp_full[bsel]);
+      umma_commit_w(&r_empty[slot_of(2 * j + 1)]);  // V~_j is no longer needed
+      return true;
+    };
+    bool ok = mbar_wait_warp(q_full, 0, abort);
+    if (ok) ok = issue_step(0);
+    if (ok && n > 1) ok = issue_step(1);
+    for (int j = 0; j < n && ok; ++j) {
+      const int bsel = j & 1;
+      if (!(ok = mbar_wait_warp(&ds_full[bsel], static_cast<uint32_t>((j >> 1) & 1), abort))) break;
+      tc_fence_after();
+      const uint32_t kb = ring_addr + slot_of(2 * j) * L::kKVTile;
+      const uint32_t dsb = ds_addr + bsel * L::kDSBytes;
 #pragma unroll
-        for (int kk = 0; kk < kStep / 16; ++kk)  // dQ += dS K~: contraction over 64 keys
-          umma_f16_ss(tmem + 256, sdesc_sw128(dsb + kk * 32, 16, 1024),
+      for (int kk = 0; kk < kStep / 16; ++kk)  // dQ += dS K~: contraction over 64 keys
+        umma_f16_ss_w(tmem + 256, sdesc_sw128(dsb + kk * 32, 16, 1024),
                       sdesc_sw128(kb + kk * 2048, L::kKVBlock, 1024), idesc_q,
                       (j > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(&ds_free[bsel]);
-        umma_commit(&r_empty[slot_of(2 * j)]);  // K~_j is no longer needed
-        // S/dP buffer bsel was read before ds_full_j: step j+2 may reuse it
-        if (j + 2 < n) ok = issue_step(j + 2);
-      }
-      if (ok) umma_commit(dq_done);
-      umma_commit(mma_drain);
-      mbar_wait(mma_drain, 0, nullptr, 10000000ull);
+      umma_commit_w(&ds_free[bsel]);
+      umma_commit_w(&r_empty[slot_of(2 * j)]);  // K~_j is no longer needed
+      // set bsel read S_j and dP_j before ds_full_j: step j+2 may reuse them
+      if (j + 2 < n) ok = issue_step(j + 2);
     }
+    if (ok) umma_commit_w(dq_done);
+    umma_commit_w(mma_drain);
+    mbar_wait_warp(mma_drain, 0, nullptr, 10000000ull);
   } else {
     // --------------------------------------------------------- elementwise
-    const int g = warp >> 2;                // keys [16g, 16g+16) of each step
+    const int g = warp >> 2;                // warpgroup 0..3
+    const int set = g >> 1;                 // steps set, set + 2, ...
+    const int kc = (g & 1) * 32;            // keys [kc, kc + 32) of each step
     const int t = threadIdx.x & 127;        // query row in the tile == TMEM lane
     const int qrow = q0 + t;
     const bool row_ok = qrow < Nq;
@@ -228,55 +229,45 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t c12 = pk2(c1, c1), nmb2 = pk2(negmb, negmb);
     const uint64_t sl2 = pk2(scale * inv_l, scale * inv_l);  // dS carries the softmax scale
     const uint64_t ndl2 = pk2(-dl, -dl);
-    uint8_t* ds_smem = smem + L::kDS;
+    uint8_t* dsb = smem + L::kDS + set * L::kDSBytes;
+    const uint32_t s_col = static_cast<uint32_t>(set * kStep + kc);
     bool ok = true;
-    uint32_t r[16];
-    for (int j = 0; j < n && ok; ++j) {
-      const int bsel = j & 1;
-      const uint32_t ph = static_cast<uint32_t>((j >> 1) & 1);
-      const int key0 = j * kStep + g * 16;
+    uint32_t rs[32], rd[32];
+    for (int j = set, k = 0; j < n && ok; j += 2, ++k) {
+      const uint32_t ph = static_cast<uint32_t>(k & 1);
+      const int key0 = j * kStep + kc;
       const bool edge = !row_ok || (j * kStep + kStep > Nkv) || (causal && j * kStep + kStep - 1 > q0);
-      // ---- A = scale * P / l for this thread's 16 keys
-      if (!(ok = mbar_wait_warp(&s_full[bsel], ph, abort))) break;
+      if (!(ok = mbar_wait_warp(&sdp_full[set], ph, abort))) break;
       tc_fence_after();
-      tmem_ld16(tmem + lane_base + bsel * kStep + g * 16, r);
+      tmem_ld32(tmem + lane_base + s_col, rs);
+      tmem_ld32(tmem + lane_base + 128 + s_col, rd);
       tmem_wait_ld();
-      float a[16];
+      // dS = (scale / l) * exp(scale*S - m) * (dP - delta), 32 keys
+      uint32_t dsw[16];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
+      for (int i = 0; i < 16; ++i) {
         float x0, x1;
-        up2(fma2(pk2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), c12, nmb2), x0, x1);
+        up2(fma2(pk2(__uint_as_float(rs[2 * i]), __uint_as_float(rs[2 * i + 1])), c12, nmb2), x0, x1);
         if (edge) {
           const int k0 = key0 + 2 * i;
           if (!(row_ok && k0 < Nkv && (!causal || k0 <= qrow))) x0 = -INFINITY;
           if (!(row_ok && k0 + 1 < Nkv && (!causal || k0 + 1 <= qrow))) x1 = -INFINITY;
         }
-        up2(mul2(pk2(ex2_f32(x0), ex2_f32(x1)), sl2), a[2 * i], a[2 * i + 1]);
-      }
-      // ---- dS = A * (dP - delta)
-      if (!(ok = mbar_wait_warp(&dp_full[bsel], ph, abort))) break;
-      tc_fence_after();
-      tmem_ld16(tmem + lane_base + 128 + bsel * kStep + g * 16, r);
-      tmem_wait_ld();
-      uint32_t dsw[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
+        const uint64_t a2 = mul2(pk2(ex2_f32(x0), ex2_f32(x1)), sl2);
         float d0, d1;
-        up2(mul2(pk2(a[2 * u], a[2 * u + 1]),
-                 add2(pk2(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1])), ndl2)),
+        up2(mul2(a2, add2(pk2(__uint_as_float(rd[2 * i]), __uint_as_float(rd[2 * i + 1])), ndl2)),
             d0, d1);
-        dsw[u] = pack_bf16(d0, d1);
+        dsw[i] = pack_bf16(d0, d1);
       }
       tc_fence_before();
-      // dS buffer bsel is free once dQ_{j-2} is done
-      if (j >= 2 && !(ok = mbar_wait_warp(&ds_free[bsel], ph ^ 1u, abort))) break;
-      uint8_t* dsb = ds_smem + bsel * L::kDSBytes;
+      // this set's dS buffer is free once dQ of its previous step (j - 2) is done
+      if (k > 0 && !(ok = mbar_wait_warp(&ds_free[set], ph ^ 1u, abort))) break;
 #pragma unroll
-      for (int ch = 0; ch < 2; ++ch)
-        *reinterpret_cast<uint4*>(dsb + sw128_offset(t, g * 16 + ch * 8, 128)) =
+      for (int ch = 0; ch < 4; ++ch)
+        *reinterpret_cast<uint4*>(dsb + sw128_offset(t, kc + ch * 8, 128)) =
             make_uint4(dsw[4 * ch], dsw[4 * ch + 1], dsw[4 * ch + 2], dsw[4 * ch + 3]);
       fence_proxy_async_smem();
-      mbar_arrive_warp(&ds_full[bsel]);
+      mbar_arrive_warp(&ds_full[set]);
     }
     if (ok && (ok = mbar_wait_warp(dq_done, 0, abort))) {
       tc_fence_after();
@@ -285,6 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t w[kCols / 2];
 #pragma unroll
       for (int c = 0; c < kCols / 16; ++c) {
+        uint32_t r[16];
         tmem_ld16(tmem + lane_base + 256 + g * kCols + c * 16, r);
         tmem_wait_ld();
 #pragma unroll

@@ -126,118 +126,114 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kTmaWarp) {
     // ------------------------------------------------------------ producer
     // Load order: Q0, Q1; pass 1: K_0..K_{n-1}; pass 2: K_0, V_0, K_1, V_1, ...
-    if (lane == 0) {
-      tma_prefetch_desc(&tq);
-      tma_prefetch_desc(&tk);
-      tma_prefetch_desc(&tv);
-      mbar_arrive_expect_tx(q_full, 2u * L::kTileBytes);
+    tma_prefetch_desc(&tq);
+    tma_prefetch_desc(&tk);
+    tma_prefetch_desc(&tv);
+    mbar_arrive_expect_tx_w(q_full, 2u * L::kTileBytes);
 #pragma unroll
-      for (int i = 0; i < 2; ++i)
+    for (int i = 0; i < 2; ++i)
 #pragma unroll
-        for (int blk = 0; blk < D / 64; ++blk)
-          tma_load_4d(smem + L::kQ + i * L::kTileBytes + blk * kAtomBlock, &tq, blk * 64,
+      for (int blk = 0; blk < D / 64; ++blk)
+        tma_load_4d_w(smem + L::kQ + i * L::kTileBytes + blk * kAtomBlock, &tq, blk * 64,
                       q0 + i * kTile, h, b, q_full);
-      int last[kRing] = {-1, -1, -1};
-      bool ok = true;
-      const int total = 3 * n_kv;
-      for (int li = 0; li < total && ok; ++li) {
-        const int slot = li % kRing;
-        const uint32_t use = static_cast<uint32_t>(li / kRing);
-        if (!(ok = mbar_wait(&r_empty[slot], (use & 1u) ^ 1u, abort))) break;
-        const bool is_v = li >= n_kv && ((li - n_kv) & 1);
-        const int j = li < n_kv ? li : (li - n_kv) >> 1;
-        mbar_arrive_expect_tx(&r_full[slot], L::kTileBytes);
+    int last[kRing] = {-1, -1, -1};
+    bool ok = true;
+    const int total = 3 * n_kv;
+    for (int li = 0; li < total && ok; ++li) {
+      const int slot = li % kRing;
+      const uint32_t use = static_cast<uint32_t>(li / kRing);
+      if (!(ok = mbar_wait_warp(&r_empty[slot], (use & 1u) ^ 1u, abort))) break;
+      const bool is_v = li >= n_kv && ((li - n_kv) & 1);
+      const int j = li < n_kv ? li : (li - n_kv) >> 1;
+      mbar_arrive_expect_tx_w(&r_full[slot], L::kTileBytes);
 #pragma unroll
-        for (int blk = 0; blk < D / 64; ++blk)
-          tma_load_4d(smem + L::kRingOff + slot * L::kTileBytes + blk * kAtomBlock,
+      for (int blk = 0; blk < D / 64; ++blk)
+        tma_load_4d_w(smem + L::kRingOff + slot * L::kTileBytes + blk * kAtomBlock,
                       is_v ? &tv : &tk, blk * 64, j * kTile, h, b, &r_full[slot]);
-        last[slot] = static_cast<int>(use & 1u);
-      }
-      if (!ok) {
-        mbar_wait(q_full, 0, nullptr, 10000000ull);
-        for (int s = 0; s < kRing; ++s)
-          if (last[s] >= 0) mbar_wait(&r_full[s], static_cast<uint32_t>(last[s]), nullptr, 10000000ull);
-      }
+      last[slot] = static_cast<int>(use & 1u);
+    }
+    if (!ok) {
+      mbar_wait_warp(q_full, 0, nullptr, 10000000ull);
+      for (int s = 0; s < kRing; ++s)
+        if (last[s] >= 0) mbar_wait_warp(&r_full[s], static_cast<uint32_t>(last[s]), nullptr, 10000000ull);
     }
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------------- MMA
-    if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_f16(128, 128, 1, 0, 0);
-      constexpr uint32_t idesc_pv = idesc_f16(128, D, 0, 0, 1);
-      const uint32_t q_addr = smem_u32(smem + L::kQ);
-      const uint32_t p_addr = smem_u32(smem + L::kP);
-      const uint32_t ring_addr = smem_u32(smem + L::kRingOff);
-      int li = 0;  // ring load index being consumed
-      auto wait_slot = [&](int idx) -> bool {
-        return mbar_wait(&r_full[idx % kRing], static_cast<uint32_t>((idx / kRing) & 1), abort);
-      };
-      auto issue_s = [&](int i, int idx) {  // S_i = Q~_i K~^T, K~ in ring slot of load idx
-        const uint32_t kb = ring_addr + (idx % kRing) * L::kTileBytes;
-        const uint32_t qb = q_addr + i * L::kTileBytes;
+    constexpr uint32_t idesc_s = idesc_f16(128, 128, 1, 0, 0);
+    constexpr uint32_t idesc_pv = idesc_f16(128, D, 0, 0, 1);
+    const uint32_t q_addr = smem_u32(smem + L::kQ);
+    const uint32_t p_addr = smem_u32(smem + L::kP);
+    const uint32_t ring_addr = smem_u32(smem + L::kRingOff);
+    int li = 0;  // ring load index being consumed
+    auto wait_slot = [&](int idx) -> bool {
+      return mbar_wait_warp(&r_full[idx % kRing], static_cast<uint32_t>((idx / kRing) & 1), abort);
+    };
+    auto issue_s = [&](int i, int idx) {  // S_i = Q~_i K~^T, K~ in ring slot of load idx
+      const uint32_t kb = ring_addr + (idx % kRing) * L::kTileBytes;
+      const uint32_t qb = q_addr + i * L::kTileBytes;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kAtomBlock + (kk & 3) * 32;
-          umma_f16_ss(tmem + i * 128, sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * kAtomBlock + (kk & 3) * 32;
+        umma_f16_ss_w(tmem + i * 128, sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
                       idesc_s, kk > 0 ? 1u : 0u);
-        }
-        umma_commit(&s_full[i]);
-      };
-      auto issue_pv = [&](int i, int idx, bool acc) {  // O_i += P~_i V~, V~ in slot of load idx
-        const uint32_t vb = ring_addr + (idx % kRing) * L::kTileBytes;
-        const uint32_t pb = p_addr + i * 128u * 128u * 2u;
+      }
+      umma_commit_w(&s_full[i]);
+    };
+    auto issue_pv = [&](int i, int idx, bool acc) {  // O_i += P~_i V~, V~ in slot of load idx
+      const uint32_t vb = ring_addr + (idx % kRing) * L::kTileBytes;
+      const uint32_t pb = p_addr + i * 128u * 128u * 2u;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t aoff = (kk >> 2) * kAtomBlock + (kk & 3) * 32;
-          umma_f16_ss(tmem + 256 + i * 128, sdesc_sw128(pb + aoff, 16, 1024),
+      for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t aoff = (kk >> 2) * kAtomBlock + (kk & 3) * 32;
+        umma_f16_ss_w(tmem + 256 + i * 128, sdesc_sw128(pb + aoff, 16, 1024),
                       sdesc_sw128(vb + kk * 2048, kAtomBlock, 1024), idesc_pv,
                       (acc || kk > 0) ? 1u : 0u);
-        }
-      };
-      bool ok = mbar_wait(q_full, 0, abort);
-      // pass 1: S_0(j), S_1(j) for the row maxima
-      for (int j = 0; j < n_kv && ok; ++j, ++li) {
-        if (!(ok = wait_slot(li))) break;
-        for (int i = 0; i < 2 && ok; ++i) {
-          if (j > 0 && !(ok = mbar_wait(&s_free[i], static_cast<uint32_t>((j - 1) & 1), abort))) break;
-          tc_fence_after();
-          issue_s(i, li);
-        }
-        umma_commit(&r_empty[li % kRing]);
       }
-      // pass 2 prologue: S_0(0), S_1(0)
-      if (ok && (ok = wait_slot(li))) {
-        for (int i = 0; i < 2 && ok; ++i) {
-          if (!(ok = mbar_wait(&s_free[i], static_cast<uint32_t>((n_kv - 1) & 1), abort))) break;
-          tc_fence_after();
-          issue_s(i, li);
-        }
-        umma_commit(&r_empty[li % kRing]);
-        ++li;
+    };
+    bool ok = mbar_wait_warp(q_full, 0, abort);
+    // pass 1: S_0(j), S_1(j) for the row maxima
+    for (int j = 0; j < n_kv && ok; ++j, ++li) {
+      if (!(ok = wait_slot(li))) break;
+      for (int i = 0; i < 2 && ok; ++i) {
+        if (j > 0 && !(ok = mbar_wait_warp(&s_free[i], static_cast<uint32_t>((j - 1) & 1), abort))) break;
+        tc_fence_after();
+        issue_s(i, li);
       }
-      for (int j = 0; j < n_kv && ok; ++j) {
-        const int vi = li++;  // V_j
-        const int ki = (j + 1 < n_kv) ? li : -1;  // K_{j+1}
-        if (ki >= 0) ++li;
-        if (!(ok = wait_slot(vi))) break;
-        for (int i = 0; i < 2 && ok; ++i) {
-          if (!(ok = mbar_wait(&p_full[i], static_cast<uint32_t>(j & 1), abort))) break;
-          tc_fence_after();
-          issue_pv(i, vi, j > 0);
-          if (i == 1) umma_commit(&r_empty[vi % kRing]);
-          if (ki >= 0) {
-            if (!(ok = wait_slot(ki))) break;
-            issue_s(i, ki);  // S_i(j+1): S_i was read before p_full_i(j)
-            if (i == 1) umma_commit(&r_empty[ki % kRing]);
-          }
-        }
-      }
-      if (ok) {
-        umma_commit(&o_full[0]);
-        umma_commit(&o_full[1]);
-      }
-      umma_commit(mma_drain);
-      mbar_wait(mma_drain, 0, nullptr, 10000000ull);
+      umma_commit_w(&r_empty[li % kRing]);
     }
+    // pass 2 prologue: S_0(0), S_1(0)
+    if (ok && (ok = wait_slot(li))) {
+      for (int i = 0; i < 2 && ok; ++i) {
+        if (!(ok = mbar_wait_warp(&s_free[i], static_cast<uint32_t>((n_kv - 1) & 1), abort))) break;
+        tc_fence_after();
+        issue_s(i, li);
+      }
+      umma_commit_w(&r_empty[li % kRing]);
+      ++li;
+    }
+    for (int j = 0; j < n_kv && ok; ++j) {
+      const int vi = li++;  // V_j
+      const int ki = (j + 1 < n_kv) ? li : -1;  // K_{j+1}
+      if (ki >= 0) ++li;
+      if (!(ok = wait_slot(vi))) break;
+      for (int i = 0; i < 2 && ok; ++i) {
+        if (!(ok = mbar_wait_warp(&p_full[i], static_cast<uint32_t>(j & 1), abort))) break;
+        tc_fence_after();
+        issue_pv(i, vi, j > 0);
+        if (i == 1) umma_commit_w(&r_empty[vi % kRing]);
+        if (ki >= 0) {
+          if (!(ok = wait_slot(ki))) break;
+          issue_s(i, ki);  // S_i(j+1): S_i was read before p_full_i(j)
+          if (i == 1) umma_commit_w(&r_empty[ki % kRing]);
+        }
+      }
+    }
+    if (ok) {
+      umma_commit_w(&o_full[0]);
+      umma_commit_w(&o_full[1]);
+    }
+    umma_commit_w(mma_drain);
+    mbar_wait_warp(mma_drain, 0, nullptr, 10000000ull);
   } else {
     // ------------------------------------------------------------ softmax
     // Warpgroups 2i and 2i+1 own query tile i; half `hf` of the pair owns key
