@@ -201,8 +201,10 @@ nvq_status attn_qat_bwd_builtin_scratch(const void* q, const void* k, const void
 /*
  * One 128 x N x K tcgen05 BF16 MMA through shared-memory descriptors, the same
  * encodings the attention kernels use.  a: bf16 [128, K] if a_mn == 0 (K-major)
- * or [K, 128] if a_mn == 1; b: bf16 [N, K] if b_mn == 0 or [K, N] if b_mn == 1;
- * c: f32 [128, N] = A * B^T (as [128,K] x [K,N]).  N in {64,128}, K in {64,128}.
+ * or [K, 128] if a_mn == 1; a_mn == 2: a is bf16 [128, K] and the MMA reads A
+ * from tensor memory (stored there row by row, two elements per 32-bit column);
+ * b: bf16 [N, K] if b_mn == 0 or [K, N] if b_mn == 1; c: f32 [128, N] = A * B^T
+ * (as [128,K] x [K,N]).  N in {64,128}, K in {64,128}.
  */
 nvq_status nvq_selftest_umma(const void* a, const void* b, float* c, int N, int K,
                              int a_mn, int b_mn, nvq_stream_t stream);

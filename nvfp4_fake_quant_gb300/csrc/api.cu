@@ -363,14 +363,12 @@ nvq_status attn_qat_bwd(const void* q, const void* k, const void* v, const void*
   void* kt = wb + w.k;
   void* vt = wb + w.v;
   float* delta = reinterpret_cast<float*>(wb + w.delta);
-  CUtensorMap mq, mk, mv, mdo, mk64, mv64;
+  CUtensorMap mq, mk, mv, mdo;
   int r;
   if ((r = make_bnhd_map(&mq, qt, B, Nq, H, D, false)) != 0 ||
       (r = make_bnhd_map(&mk, kt, B, Nkv, H, D, false)) != 0 ||
       (r = make_bnhd_map(&mv, vt, B, Nkv, H, D, false)) != 0 ||
-      (r = make_bnhd_map(&mdo, dout, B, Nq, H, D, false)) != 0 ||
-      (r = make_bnhd_map(&mk64, kt, B, Nkv, H, D, false, 64)) != 0 ||
-      (r = make_bnhd_map(&mv64, vt, B, Nkv, H, D, false, 64)) != 0)
+      (r = make_bnhd_map(&mdo, dout, B, Nq, H, D, false)) != 0)
     return fail_driver("cuTensorMapEncodeTiled", r);
   const int64_t rq = static_cast<int64_t>(B) * Nq * H, rk = static_cast<int64_t>(B) * Nkv * H;
   const AttnShape s{B, Nq, Nkv, H, D, scale, causal};
@@ -388,24 +386,25 @@ nvq_status attn_qat_bwd(const void* q, const void* k, const void* v, const void*
     return fail_cuda("bwd_prep", e);
   if ((e = launch_attn_bwd(s, mq, mk, mv, mdo, stats, delta, dk, dv, err, stream)) != cudaSuccess)
     return fail_cuda("attn_bwd (dK, dV)", e);
-  return from_cuda("attn_bwd_dq", launch_attn_bwd_dq(s, mq, mdo, mk64, mv64, stats, delta, dq,
-                                                     err, stream));
+  return from_cuda("attn_bwd_dq",
+                   launch_attn_bwd_dq(s, mq, mdo, mk, mv, stats, delta, dq, err, stream));
 }
 
 nvq_status nvq_selftest_umma(const void* a, const void* b, float* c, int N, int K, int a_mn,
                              int b_mn, nvq_stream_t stream) {
   if (!a || !b || !c || !aligned16(a) || !aligned16(b) || !aligned16(c)) return NVQ_ERR_INVALID;
-  if ((N != 64 && N != 128) || (K != 64 && K != 128) || (a_mn != 0 && a_mn != 1) ||
+  if ((N != 64 && N != 128) || (K != 64 && K != 128) || a_mn < 0 || a_mn > 2 ||
       (b_mn != 0 && b_mn != 1))
     return NVQ_ERR_INVALID;
   int* err = error_word();
   if (err == nullptr) return NVQ_ERR_CUDA;
   CUtensorMap ma, mb;
   int r;
-  if ((r = a_mn ? make_2d_map(&ma, a, K, 128, K) : make_2d_map(&ma, a, 128, K, 128)) != 0 ||
+  if ((r = a_mn == 1 ? make_2d_map(&ma, a, K, 128, K) : make_2d_map(&ma, a, 128, K, 128)) != 0 ||
       (r = b_mn ? make_2d_map(&mb, b, K, N, K) : make_2d_map(&mb, b, N, K, N)) != 0)
     return fail_driver("cuTensorMapEncodeTiled", r);
-  return from_cuda("selftest_umma", launch_selftest_umma(ma, mb, c, N, K, a_mn, b_mn, err, stream));
+  return from_cuda("selftest_umma",
+                   launch_selftest_umma(ma, mb, a, c, N, K, a_mn, b_mn, err, stream));
 }
 
 nvq_status nvq_selftest_timeout(int64_t limit_ns, nvq_stream_t stream) {

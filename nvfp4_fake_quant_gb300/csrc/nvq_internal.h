@@ -49,14 +49,14 @@ cudaError_t launch_attn_bwd(const AttnShape& s, const CUtensorMap& tq, const CUt
                             const CUtensorMap& tv, const CUtensorMap& tdo, const float* stats,
                             const float* delta, void* dk, void* dv, int* err,
                             cudaStream_t stream);
-// dQ (query-outer; Q~, dO maps with 128-row boxes, K~, V~ maps with 64-row boxes)
+// dQ (query-outer; Q~, dO, K~, V~ maps with 128-row boxes)
 cudaError_t launch_attn_bwd_dq(const AttnShape& s, const CUtensorMap& tq, const CUtensorMap& tdo,
-                               const CUtensorMap& tk64, const CUtensorMap& tv64,
-                               const float* stats, const float* delta, void* dq, int* err,
-                               cudaStream_t stream);
+                               const CUtensorMap& tk, const CUtensorMap& tv, const float* stats,
+                               const float* delta, void* dq, int* err, cudaStream_t stream);
 
-cudaError_t launch_selftest_umma(const CUtensorMap& ta, const CUtensorMap& tb, float* c, int N,
-                                 int K, int a_mn, int b_mn, int* err, cudaStream_t stream);
+cudaError_t launch_selftest_umma(const CUtensorMap& ta, const CUtensorMap& tb, const void* a,
+                                 float* c, int N, int K, int a_mn, int b_mn, int* err,
+                                 cudaStream_t stream);
 cudaError_t launch_selftest_timeout(int64_t limit_ns, int* err, cudaStream_t stream);
 
 // Maps a [rows, cols] 16-bit row-major matrix with a box of {64, box_rows}.

@@ -1,7 +1,7 @@
 // Self-tests of the hardware encodings the attention kernels rely on:
 //  * one 128 x N x K tcgen05 kind::f16 BF16 UMMA fed by 128-byte-swizzled TMA
 //    tiles through the same shared-memory and instruction descriptors, for
-//    K-major and MN-major A and B;
+//    K-major and MN-major A and B, and for A stored in TMEM by tcgen05.st;
 //  * a bounded mbarrier wait that is meant to run out.
 #include <cuda_runtime.h>
 
@@ -16,10 +16,14 @@ constexpr uint32_t kSmem = 2 * 32768 + 1024 + 64;
 
 // Tile of a row-major [rows, cols] 16-bit matrix as loaded by TMA with a box
 // of {64, rows}: column block j (64 columns) at j * rows * 128 bytes.
+// a_mn == 2: A is also read straight from global memory (a_glob, row-major
+// [128, K]) and stored into TMEM columns [128, 128 + K/2) by tcgen05.st, two
+// elements per column, and the UMMA takes A from there.
 __global__ void __launch_bounds__(128, 1)
     selftest_umma_kernel(const __grid_constant__ CUtensorMap ta,
-                         const __grid_constant__ CUtensorMap tb, float* __restrict__ c, int N,
-                         int K, int a_mn, int b_mn, int* __restrict__ err) {
+                         const __grid_constant__ CUtensorMap tb, const uint32_t* __restrict__ a_glob,
+                         float* __restrict__ c, int N, int K, int a_mn, int b_mn,
+                         int* __restrict__ err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023u) &
                                              ~static_cast<uintptr_t>(1023u));
@@ -29,8 +33,10 @@ __global__ void __launch_bounds__(128, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 65536 + 16);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + 65536 + 20);
   const int warp = threadIdx.x >> 5;
+  const bool a_tmem = a_mn == 2;
+  const int a_smem_mn = a_tmem ? 0 : a_mn;
   // A is [128, K] (K-major) or [K, 128] (MN-major); B is [N, K] or [K, N].
-  const int a_rows = a_mn ? K : 128, a_cols = a_mn ? 128 : K;
+  const int a_rows = a_smem_mn ? K : 128, a_cols = a_smem_mn ? 128 : K;
   const int b_rows = b_mn ? K : N, b_cols = b_mn ? N : K;
   if (threadIdx.x == 0) {
     *abort = 0;
@@ -39,29 +45,42 @@ __global__ void __launch_bounds__(128, 1)
     fence_mbar_init();
   }
   if (warp == 0) {
-    tmem_alloc(tmem_slot, 128);
+    tmem_alloc(tmem_slot, 256);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+  if (a_tmem) {  // thread t stores row t of A: K/2 columns of packed pairs
+    const uint32_t* row = a_glob + static_cast<size_t>(threadIdx.x) * (K / 2);
+    for (int cc = 0; cc < K / 32; ++cc) {
+      uint32_t r[16];
+      for (int i = 0; i < 16; ++i) r[i] = row[cc * 16 + i];
+      tmem_st16(tmem + lane_base + 128 + cc * 16, r);
+    }
+    tmem_wait_st();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
   bool ok = true;
-  if (threadIdx.x == 0) {
+  if (warp == 0) {  // converged warp: the issue path the attention kernels use
     const uint32_t bytes = static_cast<uint32_t>(a_rows * a_cols * 2 + b_rows * b_cols * 2);
-    mbar_arrive_expect_tx(&bars[0], bytes);
+    mbar_arrive_expect_tx_w(&bars[0], bytes);
     for (int j = 0; j < a_cols / 64; ++j)
-      tma_load_4d(sa + j * a_rows * 128, &ta, j * 64, 0, 0, 0, &bars[0]);
+      tma_load_4d_w(sa + j * a_rows * 128, &ta, j * 64, 0, 0, 0, &bars[0]);
     for (int j = 0; j < b_cols / 64; ++j)
-      tma_load_4d(sb + j * b_rows * 128, &tb, j * 64, 0, 0, 0, &bars[0]);
-    ok = mbar_wait(&bars[0], 0, abort);
+      tma_load_4d_w(sb + j * b_rows * 128, &tb, j * 64, 0, 0, 0, &bars[0]);
+    ok = mbar_wait_warp(&bars[0], 0, abort);
     if (ok) {
       tc_fence_after();
-      const uint32_t idesc = idesc_f16(128, N, 1, a_mn, b_mn);
+      const uint32_t idesc = idesc_f16(128, N, 1, a_smem_mn, b_mn);
       const uint32_t a0 = smem_u32(sa), b0 = smem_u32(sb);
       for (int kk = 0; kk < K / 16; ++kk) {
         uint64_t ad, bd;
-        if (a_mn)  // rows = K: 16 rows per step; 64-column M chunks a_rows*128 apart
+        if (a_smem_mn)  // rows = K: 16 rows per step; 64-column M chunks a_rows*128 apart
           ad = sdesc_sw128(a0 + kk * 2048, static_cast<uint32_t>(a_rows * 128), 1024);
         else  // rows = M: 32 bytes per K step inside an atom, next atom block a_rows*128 on
           ad = sdesc_sw128(a0 + (kk >> 2) * (a_rows * 128) + (kk & 3) * 32, 16, 1024);
@@ -69,17 +88,19 @@ __global__ void __launch_bounds__(128, 1)
           bd = sdesc_sw128(b0 + kk * 2048, static_cast<uint32_t>(b_rows * 128), 1024);
         else
           bd = sdesc_sw128(b0 + (kk >> 2) * (b_rows * 128) + (kk & 3) * 32, 16, 1024);
-        umma_f16_ss(tmem, ad, bd, idesc, kk > 0 ? 1u : 0u);
+        if (a_tmem)
+          umma_f16_ts_w(tmem, tmem + 128 + kk * 8, bd, idesc, kk > 0 ? 1u : 0u);
+        else
+          umma_f16_ss_w(tmem, ad, bd, idesc, kk > 0 ? 1u : 0u);
       }
-      umma_commit(&bars[1]);
+      umma_commit_w(&bars[1]);
     }
   }
   __syncthreads();
   // every warp waits (warp-uniformly) even when the issue failed: *abort ends it
   const bool done = mbar_wait_warp(&bars[1], 0, abort);
-  if (done && ok && !*abort) {
+  if (done && !*abort) {
     tc_fence_after();
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     const int row = threadIdx.x;
     uint32_t r[32];
     for (int cc = 0; cc < N / 32; ++cc) {
@@ -94,7 +115,7 @@ __global__ void __launch_bounds__(128, 1)
   if (warp == 0) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem, 128);
+    tmem_dealloc(tmem, 256);
   }
 }
 
@@ -117,12 +138,14 @@ __global__ void selftest_timeout_kernel(int64_t limit_ns, int* __restrict__ err)
 
 }  // namespace
 
-cudaError_t launch_selftest_umma(const CUtensorMap& ta, const CUtensorMap& tb, float* c, int N,
-                                 int K, int a_mn, int b_mn, int* err, cudaStream_t stream) {
+cudaError_t launch_selftest_umma(const CUtensorMap& ta, const CUtensorMap& tb, const void* a,
+                                 float* c, int N, int K, int a_mn, int b_mn, int* err,
+                                 cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(selftest_umma_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
-  selftest_umma_kernel<<<1, 128, kSmem, stream>>>(ta, tb, c, N, K, a_mn, b_mn, err);
+  selftest_umma_kernel<<<1, 128, kSmem, stream>>>(ta, tb, static_cast<const uint32_t*>(a), c, N, K,
+                                                  a_mn, b_mn, err);
   return cudaGetLastError();
 }
 

@@ -125,6 +125,7 @@ def test_quantizer_rejects_bad_arguments(lib):
     assert lib.nvfp4_global_sf(A, 0, 32, 32, A, None) == INVALID
     assert lib.nvq_selftest_timeout(0, None) == INVALID
     assert lib.nvq_selftest_umma(A, A, A, 96, 64, 0, 0, None) == INVALID
+    assert lib.nvq_selftest_umma(A, A, A, 64, 64, 3, 0, None) == INVALID
 
 
 def test_python_layer_conventions():
