@@ -2,8 +2,8 @@
 //
 //   pass 1: S = Q~ K~^T (tcgen05 BF16 UMMA into TMEM), m = rowmax(scale*S)
 //   pass 2: S again, P = exp(scale*S - m), l += sum P, P~ = fq16(P) per 16 keys
-//           (in registers, one query row per thread), P~ -> shared memory ->
-//           O += P~ V~ (tcgen05 F16 UMMA into TMEM)
+//           (in registers, one query row per thread), P~ -> TMEM (over the S
+//           columns already read) -> O += P~ V~ (tcgen05 F16 UMMA, A from TMEM)
 //   epilogue: O / l -> bf16, LSE = m + ln l, m
 //
 // The second pass exists because P~ is referenced to the final row max m
@@ -17,10 +17,14 @@
 // Roles (576 threads, one CTA per SM, two 128-query tiles per CTA):
 //   warps 0-15 softmax, two warpgroups per query tile (64 key columns each);
 //              thread t owns query row t = TMEM lane t
-//   warp 16    TMA producer (lane 0)
-//   warp 17    TMEM allocator and UMMA issuer (lane 0)
-// Buffers: two Q~ tiles, two P~ tiles, a 3-stage K~/V~ ring; TMEM columns
-// [0,256) hold S_0, S_1 and [256,512) the O_0, O_1 accumulators.
+//   warp 16    TMA producer
+//   warp 17    TMEM allocator and UMMA issuer
+// (both as converged warps, one elected lane issuing).
+// Buffers: two Q~ tiles and a 5-stage K~/V~ ring in shared memory; TMEM columns
+// [0,256) hold S_0, S_1 (and P~_0, P~_1 over them) and [256,512) the O_0, O_1
+// accumulators.  Warpgroup hf of tile i writes the f16 pairs of its 64 keys
+// into the first 32 of its own 64 S columns, which it has already loaded:
+// the 16-key slice kk of P~_i is at column 128 i + 64 (kk / 4) + 8 (kk % 4).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -37,7 +41,7 @@ constexpr int kPairWarps = 8;
 constexpr int kTmaWarp = 16;
 constexpr int kMmaWarp = 17;
 constexpr int kThreads = 576;
-constexpr int kRing = 3;  // K/V tile ring (K and V tiles interleave in pass 2)
+constexpr int kRing = 5;  // K/V tile ring (K and V tiles interleave in pass 2)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint32_t kAtomBlock = 128u * 128u;  // bytes of one 64-column block of a 128-row tile
 
@@ -45,9 +49,9 @@ template <int D>
 struct FwdLayout {
   static constexpr uint32_t kTileBytes = 128u * D * 2u;
   static constexpr uint32_t kQ = 0;                          // [2] query tiles
-  static constexpr uint32_t kP = kQ + 2u * kTileBytes;       // [2] P~ tiles, 128 x 128 f16
-  static constexpr uint32_t kRingOff = kP + 2u * 128u * 128u * 2u;
-  static constexpr uint32_t kBars = kRingOff + kRing * kTileBytes;
+  static constexpr uint32_t kRingOff = kQ + 2u * kTileBytes;
+  static constexpr uint32_t kX = kRingOff + kRing * kTileBytes;  // [2 tiles][128] f32
+  static constexpr uint32_t kBars = kX + 2u * 128u * 4u;
   static constexpr uint32_t kNumBars = 1 + 2 * kRing + 2 * 4 + 1;
   static constexpr uint32_t kTmemSlot = kBars + kNumBars * 8u;
   static constexpr uint32_t kAbort = kTmemSlot + 4u;
@@ -162,7 +166,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t idesc_s = idesc_f16(128, 128, 1, 0, 0);
     constexpr uint32_t idesc_pv = idesc_f16(128, D, 0, 0, 1);
     const uint32_t q_addr = smem_u32(smem + L::kQ);
-    const uint32_t p_addr = smem_u32(smem + L::kP);
     const uint32_t ring_addr = smem_u32(smem + L::kRingOff);
     int li = 0;  // ring load index being consumed
     auto wait_slot = [&](int idx) -> bool {
@@ -179,16 +182,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       umma_commit_w(&s_full[i]);
     };
-    auto issue_pv = [&](int i, int idx, bool acc) {  // O_i += P~_i V~, V~ in slot of load idx
+    // O_i += P~_i V~ with P~_i read from TMEM, V~ in the ring slot of load idx
+    auto issue_pv = [&](int i, int idx, bool acc) {
       const uint32_t vb = ring_addr + (idx % kRing) * L::kTileBytes;
-      const uint32_t pb = p_addr + i * 128u * 128u * 2u;
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint32_t aoff = (kk >> 2) * kAtomBlock + (kk & 3) * 32;
-        umma_f16_ss_w(tmem + 256 + i * 128, sdesc_sw128(pb + aoff, 16, 1024),
+      for (int kk = 0; kk < 8; ++kk)
+        umma_f16_ts_w(tmem + 256 + i * 128, tmem + i * 128 + 64 * (kk >> 2) + 8 * (kk & 3),
                       sdesc_sw128(vb + kk * 2048, kAtomBlock, 1024), idesc_pv,
                       (acc || kk > 0) ? 1u : 0u);
-      }
     };
     bool ok = mbar_wait_warp(q_full, 0, abort);
     // pass 1: S_0(j), S_1(j) for the row maxima
@@ -223,7 +224,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (i == 1) umma_commit_w(&r_empty[vi % kRing]);
         if (ki >= 0) {
           if (!(ok = wait_slot(ki))) break;
-          issue_s(i, ki);  // S_i(j+1): S_i was read before p_full_i(j)
+          // S_i(j+1): S_i was read before p_full_i(j), and the UMMAs run in
+          // issue order, so PV_i(j) reads P~_i before S_i(j+1) overwrites it
+          issue_s(i, ki);
           if (i == 1) umma_commit_w(&r_empty[ki % kRing]);
         }
       }
@@ -238,8 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ softmax
     // Warpgroups 2i and 2i+1 own query tile i; half `hf` of the pair owns key
     // columns [64 hf, 64 hf + 64) of S_i and O columns [hf D/2, (hf+1) D/2).
-    // Row maxima and sums are combined across the pair through the tile's P~
-    // buffer, which is idle at both points (before pass 2, after the last PV).
+    // Row maxima and sums are combined across the pair through shared memory.
     const int wg = warp >> 2;
     const int ti = wg >> 1;                // query tile
     const int hf = wg & 1;                 // half of the key columns
@@ -248,8 +250,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t s_col = static_cast<uint32_t>(ti * 128 + hf * 64);
     const float c1 = scale * kLog2e;
-    uint8_t* p_smem = smem + L::kP + ti * 128 * 128 * 2;
-    float* xchg = reinterpret_cast<float*>(p_smem);  // [2][128] floats during the exchanges
+    // half 1 posts its partial, half 0 combines and posts the result back
+    float* xchg = reinterpret_cast<float*>(smem + L::kX) + ti * 128;
     const uint32_t pair_bar = 1u + static_cast<uint32_t>(ti);
     bool ok = true;
     float mraw = -INFINITY;
@@ -278,10 +280,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive_warp(&s_free[ti]);
     }
     // combine the row maxima of the pair (always reached, also after an abort)
-    xchg[hf * 128 + t] = mraw;
+    if (hf == 1) xchg[t] = mraw;
     named_bar_sync(pair_bar, kPairThreads);
-    mraw = fmaxf(mraw, xchg[(hf ^ 1) * 128 + t]);
+    if (hf == 0) xchg[t] = mraw = fmaxf(mraw, xchg[t]);
     named_bar_sync(pair_bar, kPairThreads);
+    if (hf == 1) mraw = xchg[t];
     const float m = mraw * scale;
     const float negmb = -m * kLog2e;
     const uint64_t c12 = pk2(c1, c1), nmb2 = pk2(negmb, negmb);
@@ -289,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = 0; j < n_kv && ok; ++j) {
       if (!(ok = mbar_wait_warp(&s_full[ti], static_cast<uint32_t>((n_kv + j) & 1), abort))) break;
       tc_fence_after();
-      // S_i(j) complete implies PV_i(j-1) complete (issued earlier): the P~ tile is free
+      // S_i(j) complete implies PV_i(j-1) complete (issued earlier): P~_i(j-1) is consumed
       const bool edge = (j * kTile + kTile > Nkv) || (causal && j * kTile + kTile - 1 > tile_q0);
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
@@ -307,33 +310,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!(key < Nkv && (!causal || key <= qrow))) x[i] = -INFINITY;
           }
         }
+        uint32_t pt[16];  // P~ of these 32 keys as f16 pairs
 #pragma unroll
         for (int hb = 0; hb < 2; ++hb) {
           float pp[16];
-          uint32_t pt[8];
-          pquant16(x + 16 * hb, pp, pt);
+          uint32_t (&ph)[8] = *reinterpret_cast<uint32_t(*)[8]>(pt + 8 * hb);
+          pquant16(x + 16 * hb, pp, ph);
 #pragma unroll
           for (int u = 0; u < 8; ++u) l2 = add2(l2, pk2(pp[2 * u], pp[2 * u + 1]));
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const uint32_t off = sw128_offset(t, hf * 64 + c * 32 + hb * 16 + u * 8, 128);
-            *reinterpret_cast<uint4*>(p_smem + off) =
-                make_uint4(pt[4 * u], pt[4 * u + 1], pt[4 * u + 2], pt[4 * u + 3]);
-          }
         }
+        // keys [64 hf + 32 c, +32) -> columns [64 hf + 16 c, +16) of S_i, already loaded
+        tmem_st16(tmem + lane_base + s_col + c * 16, pt);
       }
+      tmem_wait_st();
       tc_fence_before();
-      fence_proxy_async_smem();
       mbar_arrive_warp(&p_full[ti]);
     }
     float l_lo, l_hi;
     up2(l2, l_lo, l_hi);
     float l = l_lo + l_hi;
-    // the last PV of this tile has read P~ once o_full completes
     const bool have_o = ok && mbar_wait_warp(&o_full[ti], 0, abort);
-    xchg[hf * 128 + t] = l;
+    if (hf == 1) xchg[t] = l;
     named_bar_sync(pair_bar, kPairThreads);
-    l += xchg[(hf ^ 1) * 128 + t];
+    if (hf == 0) xchg[t] = l = l + xchg[t];
+    named_bar_sync(pair_bar, kPairThreads);
+    if (hf == 1) l = xchg[t];
     if (have_o) {
       tc_fence_after();
       const float inv_l = 1.0f / l;
