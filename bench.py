@@ -1,10 +1,14 @@
 """Benchmark of the NVFP4 Attn-QAT hot path on GB300.
 
 One step = one Attn-QAT forward + straight-through backward (all kernels of the
-path: Q/K/V quantization, two-pass forward, delta, KV-outer backward, dQ
-conversion) on the Wan2.1-T2V-1.3B self-attention shape B=1, H=12, N=25088,
-D=128 (16x28x56 latent tokens), seeded synthetic bf16 inputs resident in HBM.
-Counted FLOPs: forward 4*B*H*N^2*D, backward 2.5x that.
+path: Q/K/V quantization, two-pass forward, delta pre-pass, key-outer dK/dV
+kernel, query-outer dQ kernel) on the Wan2.1-T2V-1.3B self-attention shape
+B=1, H=12, N=25088, D=128 (16x28x56 latent tokens), seeded synthetic bf16
+inputs resident in HBM.  Counted FLOPs: forward 4*B*H*N^2*D, backward 2.5x that.
+
+The roofline object describes the kernel with the largest share of the step,
+timed live inside the timed region with CUDA events that the library records
+around each of its launches on the launching stream (nvq_timing_*).
 
 Prints one JSON line (rank 0).  Multi-GPU runs (torchrun, one process per GPU)
 are independent replicas of the same step: weak scaling, no data-path
@@ -39,6 +43,42 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 def flops_fwd(b, nq, nkv, h, d):
     return 4.0 * b * h * nq * nkv * d
+
+
+def kernel_work(kind, b, n, h, d):
+    """Algorithmic work of one launch of a kernel kind: (amount, unit, bound).
+    Attention kernels count the contractions they execute (the forward's row-max
+    pass included); HBM-bound passes count the bytes they must move."""
+    gemm = 2.0 * b * h * n * n * d  # one N x N x D contraction per (batch, head)
+    rows = b * n * h * d * 2.0      # one bf16 [B, N, H, D] tensor
+    table = {
+        "attn_fwd": (3 * gemm, "flop", "tensor"),   # S (pass 1), S (pass 2), P~ V~
+        "bwd_dkdv": (4 * gemm, "flop", "tensor"),   # S, dP, dV, dK
+        "bwd_dq": (3 * gemm, "flop", "tensor"),     # S, dP, dQ
+        "quantize": (2 * rows, "byte", "hbm"),      # one of q, k, v: read + write
+        "bwd_delta": (2 * rows + b * h * n * 4.0, "byte", "hbm"),  # o, dO in, delta out
+    }
+    return table[kind]
+
+
+# DRAM traffic per launch of a kernel (dram__bytes_read.sum + dram__bytes_write.sum)
+# from one ncu capture of this workload, with the SHA-256 of the kernel's source
+# at the time: a changed source reports null.  The capture is summarised under
+# profiles/ (file named in "summary").
+TRAFFIC = {}
+
+
+def traffic_for(kind):
+    t = TRAFFIC.get(kind)
+    if t is None:
+        return None
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, t["source"]), "rb") as f:
+            digest = hashlib.sha256(f.read()).hexdigest()
+    except OSError:
+        return None
+    return t["bytes"] if digest == t["sha256"] else None
 
 
 def load_peaks():
@@ -292,6 +332,7 @@ def run_ours(args):
     barrier(dist)
     torch.cuda.synchronize(dev)
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    api.timing_enable(True)  # per-launch events on the launching stream, for the roofline
     with ClockSampler(dev.index if dev.index is not None else 0) as clk:
         ev0.record(stream)
         for _ in range(args.steps):
@@ -299,6 +340,8 @@ def run_ours(args):
         ev1.record(stream)
         torch.cuda.synchronize(dev)
     barrier(dist)
+    ktimes = api.timing_read()
+    api.timing_enable(False)
     clocks = clk.summary()
     f_fwd = flops_fwd(b, n, n, h, d)
     f_step = 3.5 * f_fwd
@@ -338,6 +381,22 @@ def run_ours(args):
     quant = quantizer_bench(peaks, stream) if rank == 0 and not args.skip_quantizer else None
 
     peak_t = peaks["bf16_tflops"]
+    k_total = sum(ms for _, ms in ktimes.values())
+    kernels = {name: {"launches": cnt, "avg_ms": ms / cnt, "share": ms / k_total}
+               for name, (cnt, ms) in ktimes.items() if cnt}
+    dom = max(kernels, key=lambda name: ktimes[name][1])
+    amount, unit, bound = kernel_work(dom, b, n, h, d)
+    dom_ms = kernels[dom]["avg_ms"]
+    if unit == "flop":
+        achieved, peak, r_unit = amount / (dom_ms * 1e-3) / 1e12, peak_t, "TFLOP/s"
+        p_name = "bf16_tflops (burst)"
+    else:
+        achieved, peak, r_unit = amount / (dom_ms * 1e-3) / 1e9, peaks["hbm_gbs"], "GB/s"
+        p_name = "hbm_gbs"
+    roofline = {"kernel": dom, "bound": bound, "achieved": achieved, "peak": peak,
+                "unit": r_unit, "frac": achieved / peak, "traffic": traffic_for(dom),
+                "algorithmic_per_launch": amount, "launch_ms": dom_ms,
+                "peak_source": f"{peak_src} {p_name}"}
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -351,13 +410,11 @@ def run_ours(args):
         "pct_of_bf16_peak": value / ws / peak_t,
         "peaks": {"bf16_tflops": peak_t, "hbm_gbs": peaks["hbm_gbs"], "source": peak_src},
         "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "fwd_tflops": fwd_tflops, "bwd_tflops": bwd_tflops,
-        "roofline": {"kernel": "attn_qat_bwd call (quantize x3, delta, KV-outer backward, dQ convert)",
-                     "bound": "tensor", "achieved": bwd_tflops, "peak": peak_t,
-                     "unit": "TFLOP/s", "frac": bwd_tflops / peak_t, "traffic": None,
-                     "peak_source": f"{peak_src} bf16_tflops (burst)"},
+        "roofline": roofline,
+        "kernels": kernels,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": 10 * args.steps,
+        "gpu_launches": sum(k["launches"] for k in kernels.values()),
         "clocks": clocks,
     }
     if quant is not None:

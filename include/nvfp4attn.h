@@ -194,6 +194,37 @@ nvq_status attn_qat_bwd_builtin_scratch(const void* q, const void* k, const void
                                         nvq_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
+/* Per-kernel device timing (a profiling aid; no counterpart in the pages)  */
+/* ------------------------------------------------------------------------ */
+
+/* Kernel kinds the library launches. */
+enum {
+  NVQ_KERNEL_QUANTIZE = 0,   /* NVFP4 fake-quant / codes pass (also inside the attention calls) */
+  NVQ_KERNEL_ATTN_FWD = 1,   /* attention forward */
+  NVQ_KERNEL_BWD_DELTA = 2,  /* backward pre-pass delta = rowsum(dO * o) */
+  NVQ_KERNEL_BWD_DKDV = 3,   /* backward, key-outer dK and dV kernel */
+  NVQ_KERNEL_BWD_DQ = 4,     /* backward, query-outer dQ kernel */
+  NVQ_KERNEL_GLOBAL_SF = 5,  /* static global scale (amax reduction and finalize) */
+  NVQ_KERNEL_KINDS = 6
+};
+
+/*
+ * on = 1: from now on, every kernel launch of the library is bracketed by two
+ * CUDA events recorded on the stream it is launched on (process-wide, all
+ * host threads); records taken before are discarded.  on = 0: stop and
+ * discard.  Costs two event records per launch while on.
+ */
+nvq_status nvq_timing_enable(int on);
+
+/*
+ * Number of recorded launches of `kind` (an NVQ_KERNEL_* value) and their
+ * summed device time in milliseconds, since the last nvq_timing_enable(1).
+ * Synchronizes on the recorded events.  NVQ_ERR_INVALID for a bad kind or a
+ * NULL output pointer.
+ */
+nvq_status nvq_timing_read(int kind, int64_t* launches, double* total_ms);
+
+/* ------------------------------------------------------------------------ */
 /* Self-tests of the hardware encodings the kernels rely on (no paper       */
 /* counterpart; used by the GPU tests)                                      */
 /* ------------------------------------------------------------------------ */

@@ -39,6 +39,8 @@ SIGNATURES = {
     "attn_qat_bwd_builtin_scratch": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                              c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int,
                                              c_int, c_int, c_int, c_float, c_int, c_void_p]),
+    "nvq_timing_enable": (c_int, [c_int]),
+    "nvq_timing_read": (c_int, [c_int, c_void_p, c_void_p]),
     "nvq_selftest_umma": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int,
                                   c_void_p]),
     "nvq_selftest_timeout": (c_int, [c_int64, c_void_p]),

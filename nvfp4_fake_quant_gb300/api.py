@@ -165,6 +165,27 @@ def attn_qat_bwd(q, k, v, o, stats, do, scale=None, causal=False, dq=None, dk=No
     return dq, dk, dv
 
 
+# Kernel kinds of nvq_timing_read (include/nvfp4attn.h, NVQ_KERNEL_*)
+KERNEL_KINDS = {"quantize": 0, "attn_fwd": 1, "bwd_delta": 2, "bwd_dkdv": 3, "bwd_dq": 4,
+                "global_sf": 5}
+
+
+def timing_enable(on: bool = True) -> None:
+    """Start (discarding earlier records) or stop per-kernel event timing."""
+    _lib.call("nvq_timing_enable", int(bool(on)))
+
+
+def timing_read() -> dict:
+    """{kind: (launches, total_ms)} for the launches recorded since timing_enable(True)."""
+    import ctypes
+    out = {}
+    for name, kind in KERNEL_KINDS.items():
+        n, ms = ctypes.c_int64(0), ctypes.c_double(0.0)
+        _lib.call("nvq_timing_read", kind, ctypes.addressof(n), ctypes.addressof(ms))
+        out[name] = (int(n.value), float(ms.value))
+    return out
+
+
 def device_status(device=None) -> int:
     """Synchronize the current stream and return (and clear) the device error word."""
     s = torch.cuda.current_stream(device).cuda_stream

@@ -210,6 +210,15 @@ BwdWs bwd_ws(int B, int Nq, int Nkv, int H, int D) {
   return w;
 }
 
+// Fake-quantizes `rows` contiguous rows of D elements (unit global scale) into
+// `out`, as one timed quantizer launch.
+cudaError_t quantize_rows(const void* x, int64_t rows, int D, int mode, void* out,
+                          cudaStream_t stream) {
+  return timed(NVQ_KERNEL_QUANTIZE, stream, [&] {
+    return launch_fake_quant(x, rows, D, D, nullptr, mode, out, D, nullptr, 0, nullptr, 0, stream);
+  });
+}
+
 nvq_status check_quant(const void* x, int64_t rows, int64_t cols, int64_t ld_x) {
   if (x == nullptr || !aligned16(x)) return NVQ_ERR_INVALID;
   if (rows < 1 || cols < 16 || cols % 16 != 0) return NVQ_ERR_INVALID;
@@ -261,7 +270,9 @@ nvq_status nvfp4_global_sf(const void* x, int64_t rows, int64_t cols, int64_t ld
       (reinterpret_cast<uintptr_t>(global_sf) & 3u) != 0)
     return NVQ_ERR_INVALID;
   if (rows < 1 || cols < 1 || ld_x < cols || ld_x % 8 != 0) return NVQ_ERR_INVALID;
-  return from_cuda("global_sf", launch_global_sf(x, rows, cols, ld_x, global_sf, stream));
+  return from_cuda("global_sf", timed(NVQ_KERNEL_GLOBAL_SF, stream, [&] {
+                     return launch_global_sf(x, rows, cols, ld_x, global_sf, stream);
+                   }));
 }
 
 nvq_status nvfp4_fake_quant(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
@@ -276,8 +287,10 @@ nvq_status nvfp4_fake_quant(const void* x, int64_t rows, int64_t cols, int64_t l
   if (global_sf != nullptr && (reinterpret_cast<uintptr_t>(global_sf) & 3u) != 0)
     return NVQ_ERR_INVALID;
   const int mode = global_sf == nullptr ? kUnitBf16 : kStaticBf16;
-  return from_cuda("fake_quant", launch_fake_quant(x, rows, cols, ld_x, global_sf, mode, out,
-                                                   ld_out, scales, ld_scales, nullptr, 0, stream));
+  return from_cuda("fake_quant", timed(NVQ_KERNEL_QUANTIZE, stream, [&] {
+                     return launch_fake_quant(x, rows, cols, ld_x, global_sf, mode, out, ld_out,
+                                              scales, ld_scales, nullptr, 0, stream);
+                   }));
 }
 
 nvq_status nvfp4_quantize_codes(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
@@ -291,9 +304,10 @@ nvq_status nvfp4_quantize_codes(const void* x, int64_t rows, int64_t cols, int64
   if (global_sf != nullptr && (reinterpret_cast<uintptr_t>(global_sf) & 3u) != 0)
     return NVQ_ERR_INVALID;
   const int mode = global_sf == nullptr ? kUnitBf16 : kStaticBf16;
-  return from_cuda("quantize_codes", launch_fake_quant(x, rows, cols, ld_x, global_sf, mode,
-                                                       nullptr, 0, scales, ld_scales, codes,
-                                                       ld_codes, stream));
+  return from_cuda("quantize_codes", timed(NVQ_KERNEL_QUANTIZE, stream, [&] {
+                     return launch_fake_quant(x, rows, cols, ld_x, global_sf, mode, nullptr, 0,
+                                              scales, ld_scales, codes, ld_codes, stream);
+                   }));
 }
 
 size_t attn_qat_fwd_workspace(int B, int Nq, int Nkv, int H, int D) {
@@ -331,17 +345,16 @@ nvq_status attn_qat_fwd(const void* q, const void* k, const void* v, int B, int 
     return fail_driver("cuTensorMapEncodeTiled", r);
   const int64_t rq = static_cast<int64_t>(B) * Nq * H, rk = static_cast<int64_t>(B) * Nkv * H;
   cudaError_t e;
-  if ((e = launch_fake_quant(q, rq, D, D, nullptr, kUnitBf16, qt, D, nullptr, 0, nullptr, 0,
-                             stream)) != cudaSuccess)
+  if ((e = quantize_rows(q, rq, D, kUnitBf16, qt, stream)) != cudaSuccess)
     return fail_cuda("quantize q", e);
-  if ((e = launch_fake_quant(k, rk, D, D, nullptr, kUnitBf16, kt, D, nullptr, 0, nullptr, 0,
-                             stream)) != cudaSuccess)
+  if ((e = quantize_rows(k, rk, D, kUnitBf16, kt, stream)) != cudaSuccess)
     return fail_cuda("quantize k", e);
-  if ((e = launch_fake_quant(v, rk, D, D, nullptr, kUnitF16, vt, D, nullptr, 0, nullptr, 0,
-                             stream)) != cudaSuccess)
+  if ((e = quantize_rows(v, rk, D, kUnitF16, vt, stream)) != cudaSuccess)
     return fail_cuda("quantize v", e);
   const AttnShape s{B, Nq, Nkv, H, D, scale, causal};
-  return from_cuda("attn_fwd", launch_attn_fwd(s, mq, mk, mv, o, stats, err, stream));
+  return from_cuda("attn_fwd", timed(NVQ_KERNEL_ATTN_FWD, stream, [&] {
+                     return launch_attn_fwd(s, mq, mk, mv, o, stats, err, stream);
+                   }));
 }
 
 nvq_status attn_qat_bwd(const void* q, const void* k, const void* v, const void* o,
@@ -373,21 +386,22 @@ nvq_status attn_qat_bwd(const void* q, const void* k, const void* v, const void*
   const int64_t rq = static_cast<int64_t>(B) * Nq * H, rk = static_cast<int64_t>(B) * Nkv * H;
   const AttnShape s{B, Nq, Nkv, H, D, scale, causal};
   cudaError_t e;
-  if ((e = launch_fake_quant(q, rq, D, D, nullptr, kUnitBf16, qt, D, nullptr, 0, nullptr, 0,
-                             stream)) != cudaSuccess)
+  if ((e = quantize_rows(q, rq, D, kUnitBf16, qt, stream)) != cudaSuccess)
     return fail_cuda("quantize q", e);
-  if ((e = launch_fake_quant(k, rk, D, D, nullptr, kUnitBf16, kt, D, nullptr, 0, nullptr, 0,
-                             stream)) != cudaSuccess)
+  if ((e = quantize_rows(k, rk, D, kUnitBf16, kt, stream)) != cudaSuccess)
     return fail_cuda("quantize k", e);
-  if ((e = launch_fake_quant(v, rk, D, D, nullptr, kUnitBf16, vt, D, nullptr, 0, nullptr, 0,
-                             stream)) != cudaSuccess)
+  if ((e = quantize_rows(v, rk, D, kUnitBf16, vt, stream)) != cudaSuccess)
     return fail_cuda("quantize v", e);
-  if ((e = launch_bwd_prep(s, o, dout, delta, stream)) != cudaSuccess)
+  if ((e = timed(NVQ_KERNEL_BWD_DELTA, stream,
+                 [&] { return launch_bwd_prep(s, o, dout, delta, stream); })) != cudaSuccess)
     return fail_cuda("bwd_prep", e);
-  if ((e = launch_attn_bwd(s, mq, mk, mv, mdo, stats, delta, dk, dv, err, stream)) != cudaSuccess)
+  if ((e = timed(NVQ_KERNEL_BWD_DKDV, stream, [&] {
+         return launch_attn_bwd(s, mq, mk, mv, mdo, stats, delta, dk, dv, err, stream);
+       })) != cudaSuccess)
     return fail_cuda("attn_bwd (dK, dV)", e);
-  return from_cuda("attn_bwd_dq",
-                   launch_attn_bwd_dq(s, mq, mdo, mk, mv, stats, delta, dq, err, stream));
+  return from_cuda("attn_bwd_dq", timed(NVQ_KERNEL_BWD_DQ, stream, [&] {
+                     return launch_attn_bwd_dq(s, mq, mdo, mk, mv, stats, delta, dq, err, stream);
+                   }));
 }
 
 nvq_status nvq_selftest_umma(const void* a, const void* b, float* c, int N, int K, int a_mn,

@@ -34,6 +34,29 @@ struct AttnShape {
 nvq_status fail_cuda(const char* where, cudaError_t e);
 nvq_status fail_driver(const char* where, int cu_result);
 
+// While nvq_timing_enable(1) is in force, brackets the launches made during its
+// lifetime with CUDA events on `stream`, filed under `kind` (an NVQ_KERNEL_*
+// value); otherwise does nothing.
+class TimedLaunch {
+ public:
+  TimedLaunch(int kind, cudaStream_t stream);
+  ~TimedLaunch();
+  TimedLaunch(const TimedLaunch&) = delete;
+  TimedLaunch& operator=(const TimedLaunch&) = delete;
+
+ private:
+  int kind_;
+  cudaStream_t stream_;
+  cudaEvent_t start_ = nullptr, stop_ = nullptr;
+};
+
+// Runs `launch` (a callable returning cudaError_t) inside a TimedLaunch.
+template <class F>
+cudaError_t timed(int kind, cudaStream_t stream, F&& launch) {
+  TimedLaunch t(kind, stream);
+  return launch();
+}
+
 // Tensor maps over [B, N, H, D] 16-bit tensors, box {64, box_rows, 1, 1}, 128-byte swizzle.
 // Return the CUresult of cuTensorMapEncodeTiled (0 on success).
 int make_bnhd_map(CUtensorMap* map, const void* base, int B, int N, int H, int D, bool f16,

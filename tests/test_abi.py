@@ -128,6 +128,19 @@ def test_quantizer_rejects_bad_arguments(lib):
     assert lib.nvq_selftest_umma(A, A, A, 64, 64, 3, 0, None) == INVALID
 
 
+def test_timing_hook_arguments(lib):
+    n, ms = ctypes.c_int64(-1), ctypes.c_double(-1.0)
+    pn, pms = ctypes.addressof(n), ctypes.addressof(ms)
+    assert lib.nvq_timing_enable(2) == INVALID
+    assert lib.nvq_timing_read(6, pn, pms) == INVALID
+    assert lib.nvq_timing_read(-1, pn, pms) == INVALID
+    assert lib.nvq_timing_read(0, None, pms) == INVALID
+    assert lib.nvq_timing_enable(1) == OK
+    assert lib.nvq_timing_read(3, pn, pms) == OK  # nothing launched: no CUDA call needed
+    assert (n.value, ms.value) == (0, 0.0)
+    assert lib.nvq_timing_enable(0) == OK
+
+
 def test_python_layer_conventions():
     from nvfp4_fake_quant_gb300 import api
     with pytest.raises(NotImplementedError):

@@ -135,3 +135,28 @@ def test_calls_from_a_thread_without_a_current_context():
     assert torch.equal(o, o_ref) and torch.equal(stats, s_ref)
     for g, r in zip((dq, dk, dv), g_ref):
         assert torch.equal(g, r)
+
+
+def test_kernel_timing_hook_counts_every_launch():
+    """nvq_timing_* files each launch of a forward + backward under its kernel
+    kind, with a positive device time that fits inside the calls' wall time."""
+    import time
+    inp = workloads.attn_inputs(1, 384, 384, 2, 128, seed=23)
+    q, k, v, do = (t.cuda() for t in (inp.q, inp.k, inp.v, inp.do))
+    o, stats = api.attn_qat_fwd(q, k, v, inp.scale)
+    torch.cuda.synchronize()
+    api.timing_enable(True)
+    try:
+        t0 = time.perf_counter()
+        o, stats = api.attn_qat_fwd(q, k, v, inp.scale)
+        api.attn_qat_bwd(q, k, v, o, stats, do, inp.scale)
+        torch.cuda.synchronize()
+        wall_ms = (time.perf_counter() - t0) * 1e3
+        got = api.timing_read()
+    finally:
+        api.timing_enable(False)
+    assert {k: n for k, (n, _) in got.items()} == {
+        "quantize": 6, "attn_fwd": 1, "bwd_delta": 1, "bwd_dkdv": 1, "bwd_dq": 1, "global_sf": 0}
+    assert all(ms > 0 for n, ms in got.values() if n)
+    assert sum(ms for _, ms in got.values()) <= wall_ms
+    assert api.timing_read()["attn_fwd"] == (0, 0.0)  # disabled: records discarded
