@@ -255,7 +255,10 @@ def time_events(fn, iters, stream):
 
 def quantizer_bench(peaks, stream, iters=20):
     """nvfp4_fake_quant on the 4096x4096 workload, L2 defeated by rotating
-    buffer sets whose total exceeds twice the L2 size."""
+    buffer sets whose total exceeds twice the L2 size.  "us" is the time per
+    launch of a CUDA graph holding iters x sets launches back to back (no host
+    gaps; events around the graph replay); "wall_us" the back-to-back rate of
+    the Python calls, which on a host slower than the kernel includes gaps."""
     import torch
 
     from nvfp4_fake_quant_gb300 import api, workloads
@@ -279,9 +282,24 @@ def quantizer_bench(peaks, stream, iters=20):
             api.nvfp4_fake_quant(xs[i], g, out=outs[i], scales=scs[i])
         for _ in range(nsets):
             one()
-        ms = time_events(one, iters * nsets, stream)
-        gbs = alg_bytes / (ms * 1e-3) / 1e9
-        res[name] = {"us": ms * 1e3, "GB/s": gbs, "frac": gbs / peaks["hbm_gbs"]}
+        torch.cuda.synchronize()
+        wall_ms = time_events(one, iters * nsets, stream)
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for _ in range(nsets):
+                one()
+        torch.cuda.current_stream().wait_stream(side)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for _ in range(iters * nsets):
+                one()
+        graph.replay()
+        torch.cuda.synchronize()
+        us = time_events(graph.replay, 3, stream) / (iters * nsets) * 1e3
+        gbs = alg_bytes / (us * 1e-6) / 1e9
+        res[name] = {"us": us, "GB/s": gbs, "frac": gbs / peaks["hbm_gbs"],
+                     "wall_us": wall_ms * 1e3, "launches_per_graph": iters * nsets}
     res["algorithmic_bytes"] = alg_bytes
     res["workload"] = ("bf16 4096x4096, N(0,1), 1% entries x50, 2% zero 16-blocks (seed 1); "
                        f"{nsets} rotating buffer sets to defeat L2")

@@ -7,17 +7,15 @@
 // amax*gsf/6 and |x|*gsf/s.
 //
 // Three variants:
-//  * quant16_unit   exact for bf16 input and unit gsf, cheap: the scale uses one
-//                   IEEE division per block; each code uses a hardware
-//                   reciprocal and a product whose value is then rounded to
-//                   17 significant bits ("snapped") before the E2M1 conversion.
+//  * quant16_unit   exact for bf16 input and unit gsf, cheap: the scale uses a
+//                   product snapped to 17 bits; each code uses a hardware
+//                   reciprocal, a product and one fma residual correction.
 //                   Why that equals the exact decision: x (8-bit significand)
 //                   and s (<= 4 bits) make x/s either exactly a tie point t of
-//                   the E2M1 grid (then x == t*s and the approximate quotient,
-//                   within 2^-22 of t, snaps back onto t) or at relative distance
-//                   >= 2^-13 from every tie (x - t*s is a non-zero multiple of
-//                   2^min(ex-7, es-5) while t*s < 2^(es+4)), which neither the
-//                   2^-22 error nor the 2^-17 snap can cross.
+//                   the E2M1 grid (then x == t*s and the corrected quotient is
+//                   exactly t) or at relative distance >= 2^-13 from every tie
+//                   (x - t*s is a non-zero multiple of 2^min(ex-7, es-5) while
+//                   t*s < 2^(es+4)), which an error of one ulp cannot cross.
 //  * quant16_static IEEE fp32 products and quotients (mul.rn / div.rn) in the
 //                   order of the definition: bit-identical to any IEEE fp32
 //                   evaluation of the same steps.
@@ -100,56 +98,94 @@ __device__ __forceinline__ float bf16_bits_to_f32(uint32_t b16) { return __uint_
 // Result of quantizing one 16-element block of bf16 values.
 struct Q16 {
   uint32_t sbyte;      // E4M3FN scale byte
-  uint32_t codes[2];   // 16 four-bit codes with sign (element i in nibble i%8 of codes[i/8])
+  uint32_t codes[2];   // 16 four-bit codes, signed (element i in nibble i%8 of codes[i/8])
   uint32_t out[8];     // 16 dequantized values as bf16x2 or f16x2 (element 2j low half of out[j])
 };
 
+__device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// max |x| over 16 bf16 values (exact: bf16 maxima of magnitudes), as fp32.
+__device__ __forceinline__ float amax16_bf16(const uint32_t (&x)[8]) {
+  constexpr uint32_t kAbs = 0x7FFF7FFFu;
+  const uint32_t m01 = bmax2(x[0] & kAbs, x[1] & kAbs), m23 = bmax2(x[2] & kAbs, x[3] & kAbs);
+  const uint32_t m45 = bmax2(x[4] & kAbs, x[5] & kAbs), m67 = bmax2(x[6] & kAbs, x[7] & kAbs);
+  uint32_t m = bmax2(bmax2(m01, m23), bmax2(m45, m67));
+  m = bmax2(m, m >> 16);  // low half: max of both halves
+  return __uint_as_float(m << 16);
+}
+
+// The sign bit of every code from the sign bit of its input element, so that a
+// code rounded to zero keeps the sign of x.
+__device__ __forceinline__ void code_signs(const uint32_t (&x)[8], uint32_t (&codes)[2]) {
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    codes[j >> 2] |= (((x[j] >> 12) & 0x8u) | ((x[j] >> 24) & 0x80u)) << (8 * (j & 3));
+}
+
+__device__ __forceinline__ uint64_t qpk2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void qup2(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+
+// x/s for a pair of fp32 values (signed), from inv = rcp.approx(s) and one
+// residual correction: r = x - q0*s is exact (fma), and q0 + r*inv lands on
+// x/s exactly whenever x/s is a short number (a tie of the E2M1 grid), and
+// within an ulp of it otherwise.  s = 0 (inv = 0) gives signed zeros.
+__device__ __forceinline__ uint64_t quot2(uint64_t x2, uint64_t neg_s2, uint64_t inv2) {
+  uint64_t q0, r, q;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(q0) : "l"(x2), "l"(inv2));
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(q0), "l"(neg_s2), "l"(x2));
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(q) : "l"(r), "l"(inv2), "l"(q0));
+  return q;
+}
+
 // x: 16 bf16 values packed as 8 u32 (element 2j in the low half of x[j]).
 // OUT_F16: dequantized values as f16 (exact for unit gsf) instead of bf16.
+// The scale decision: amax*fp32(1/6) is within 2 ulp of amax/6 and snapped to
+// 17 bits.  amax/6 with an 8-bit amax is either a short number (the snap
+// restores it exactly) or at relative distance >= 2^-8 from every E4M3 tie
+// (3 does not divide the significand), so the E4M3 rounding equals that of
+// the IEEE quotient.  Codes: E2M1 of the signed quotient x/s (quot2).
 template <bool OUT_F16>
 __device__ __forceinline__ Q16 quant16_unit(const uint32_t (&x)[8]) {
   Q16 r;
-  float a[16];
-  uint32_t sgn = 0;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    a[2 * j] = bf16_bits_to_f32(x[j] & 0x7FFFu);
-    a[2 * j + 1] = bf16_bits_to_f32((x[j] >> 16) & 0x7FFFu);
-    sgn |= ((x[j] >> 15) & 1u) << (2 * j);
-    sgn |= ((x[j] >> 31) & 1u) << (2 * j + 1);
-  }
-  float amax = 0.f;
-#pragma unroll
-  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, a[i]);
-  const float t = __fdiv_rn(amax, 6.0f);
-  r.sbyte = e4m3_rn_sat(t);
-  const uint32_t s_h = e4m3_to_f16x2(r.sbyte);
+  const float amax = amax16_bf16(x);
+  r.sbyte = e4m3_rn_sat(snap17(amax * (1.0f / 6.0f)));
+  const uint32_t s_h = e4m3_to_f16x2(r.sbyte) & 0xFFFFu;
   const float s = f16lo_to_f32(s_h);
   const float inv = s > 0.f ? rcp_approx(s) : 0.f;
-  const uint32_t s_h2 = (s_h & 0xFFFFu) | (s_h << 16);
+  const uint64_t inv2 = qpk2(inv, inv), neg_s2 = qpk2(-s, -s);
+  const uint32_t s_h2 = s_h | (s_h << 16);
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     float q[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) q[i] = snap17(a[8 * h + i] * inv);
+    for (int jj = 0; jj < 4; ++jj) {
+      const uint32_t w = x[4 * h + jj];
+      qup2(quot2(qpk2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u)), neg_s2, inv2),
+           q[2 * jj], q[2 * jj + 1]);
+    }
     const uint32_t c = e2m1x8(q);
+    r.codes[h] = c;
     uint32_t hv[4];
     e2m1x8_to_f16x2(c, hv);
-    uint32_t signs_nib = 0;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) signs_nib |= ((sgn >> (8 * h + i)) & 1u) << (4 * i + 3);
-    r.codes[h] = c | signs_nib;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const uint32_t m = hmul2(hv[j], s_h2);  // exact: <= 7 significant bits, f16 normal range
-      const uint32_t sg = (((sgn >> (8 * h + 2 * j)) & 1u) << 15) |
-                          (((sgn >> (8 * h + 2 * j + 1)) & 1u) << 31);
+    for (int jj = 0; jj < 4; ++jj) {
+      const uint32_t m = hmul2(hv[jj], s_h2);  // exact: <= 7 significant bits, f16 normal range
+      const uint32_t sg = x[4 * h + jj] & 0x80008000u;  // zeros keep the sign of x
       if (OUT_F16) {
-        r.out[4 * h + j] = m | sg;
+        r.out[4 * h + jj] = m | sg;
       } else {
-        const float lo = f16lo_to_f32(m), hi = f16lo_to_f32(m >> 16);
-        __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);  // exact
-        r.out[4 * h + j] = *reinterpret_cast<uint32_t*>(&b) | sg;
+        __nv_bfloat162 b = __floats2bfloat162_rn(f16lo_to_f32(m), f16lo_to_f32(m >> 16));  // exact
+        r.out[4 * h + jj] = *reinterpret_cast<uint32_t*>(&b) | sg;
       }
     }
   }
@@ -157,21 +193,11 @@ __device__ __forceinline__ Q16 quant16_unit(const uint32_t (&x)[8]) {
 }
 
 // Static global scale g (fp32): IEEE products and quotients in the order of the
-// definition.  Output values are bf16 (RNE of the fp32 quotient code*s/g).
+// definition, on signed values (round to nearest even is symmetric).  Output
+// values are bf16 (RNE of the fp32 quotient code*s/g).
 __device__ __forceinline__ Q16 quant16_static(const uint32_t (&x)[8], float g) {
   Q16 r;
-  float a[16];
-  uint32_t sgn = 0;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    a[2 * j] = bf16_bits_to_f32(x[j] & 0x7FFFu);
-    a[2 * j + 1] = bf16_bits_to_f32((x[j] >> 16) & 0x7FFFu);
-    sgn |= ((x[j] >> 15) & 1u) << (2 * j);
-    sgn |= ((x[j] >> 31) & 1u) << (2 * j + 1);
-  }
-  float amax = 0.f;
-#pragma unroll
-  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, a[i]);
+  const float amax = amax16_bf16(x);
   const float t = __fdiv_rn(__fmul_rn(amax, g), 6.0f);
   r.sbyte = e4m3_rn_sat(t);
   const float s = f16lo_to_f32(e4m3_to_f16x2(r.sbyte));
@@ -179,22 +205,22 @@ __device__ __forceinline__ Q16 quant16_static(const uint32_t (&x)[8], float g) {
   for (int h = 0; h < 2; ++h) {
     float q[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) q[i] = s > 0.f ? __fdiv_rn(__fmul_rn(a[8 * h + i], g), s) : 0.f;
+    for (int jj = 0; jj < 4; ++jj) {
+      const uint32_t w = x[4 * h + jj];
+      const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xFFFF0000u);
+      q[2 * jj] = s > 0.f ? __fdiv_rn(__fmul_rn(lo, g), s) : lo * 0.f;
+      q[2 * jj + 1] = s > 0.f ? __fdiv_rn(__fmul_rn(hi, g), s) : hi * 0.f;
+    }
     const uint32_t c = e2m1x8(q);
+    r.codes[h] = c;
     uint32_t hv[4];
     e2m1x8_to_f16x2(c, hv);
-    uint32_t signs_nib = 0;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) signs_nib |= ((sgn >> (8 * h + i)) & 1u) << (4 * i + 3);
-    r.codes[h] = c | signs_nib;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float lo = __fdiv_rn(__fmul_rn(f16lo_to_f32(hv[j]), s), g);
-      const float hi = __fdiv_rn(__fmul_rn(f16lo_to_f32(hv[j] >> 16), s), g);
+    for (int jj = 0; jj < 4; ++jj) {
+      const float lo = __fdiv_rn(__fmul_rn(f16lo_to_f32(hv[jj]), s), g);
+      const float hi = __fdiv_rn(__fmul_rn(f16lo_to_f32(hv[jj] >> 16), s), g);
       __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
-      const uint32_t sg = (((sgn >> (8 * h + 2 * j)) & 1u) << 15) |
-                          (((sgn >> (8 * h + 2 * j + 1)) & 1u) << 31);
-      r.out[4 * h + j] = *reinterpret_cast<uint32_t*>(&b) | sg;
+      r.out[4 * h + jj] = *reinterpret_cast<uint32_t*>(&b) | (x[4 * h + jj] & 0x80008000u);
     }
   }
   return r;

@@ -3,8 +3,11 @@
 // One thread quantizes one 16-element block: two 16-byte loads, one 32-byte
 // output, one scale byte and/or 8 code bytes.  A warp covers 32 consecutive
 // blocks of a row (1 KiB of input), so loads and stores are fully coalesced.
-// The grid is a whole number of waves over the SMs and strides over the
-// blocks.
+// Contiguous operands take a flat grid-stride loop over the blocks (a whole
+// number of waves over the SMs); strided ones a 2-D grid (blocks of a row along
+// x, rows along y), so no thread divides a 64-bit index.
+#include <algorithm>
+
 #include <cuda_runtime.h>
 
 #include "nvq_internal.h"
@@ -23,37 +26,81 @@ __device__ __forceinline__ uint4 ld_stream(const void* p) {
   return v;
 }
 
+struct Block16 {
+  uint4 lo, hi;
+};
+
+__device__ __forceinline__ Block16 load_block(const uint16_t* __restrict__ src) {
+  return {ld_stream(src), ld_stream(src + 8)};
+}
+
 template <int MODE>
-__global__ void __launch_bounds__(256) fake_quant_kernel(
+__device__ __forceinline__ void quant_block(const Block16& v, const float g,
+                                            uint16_t* __restrict__ out, uint8_t* __restrict__ sc,
+                                            uint8_t* __restrict__ cd) {
+  const uint32_t xv[8] = {v.lo.x, v.lo.y, v.lo.z, v.lo.w, v.hi.x, v.hi.y, v.hi.z, v.hi.w};
+  Q16 q;
+  if constexpr (MODE == kStaticBf16) {
+    q = quant16_static(xv, g);
+  } else {
+    q = quant16_unit<MODE == kUnitF16>(xv);
+  }
+  if (out != nullptr) {
+    uint4* dst = reinterpret_cast<uint4*>(out);
+    dst[0] = make_uint4(q.out[0], q.out[1], q.out[2], q.out[3]);
+    dst[1] = make_uint4(q.out[4], q.out[5], q.out[6], q.out[7]);
+  }
+  if (sc != nullptr) *sc = static_cast<uint8_t>(q.sbyte);
+  if (cd != nullptr) {
+    code_signs(xv, q.codes);
+    *reinterpret_cast<uint2*>(cd) = make_uint2(q.codes[0], q.codes[1]);
+  }
+}
+
+// Contiguous operands (row strides equal to the row lengths): block i of the
+// flattened matrix at element 16 i, scale byte i, code bytes 8 i.  With a unit
+// global scale each thread loads two blocks (one grid stride apart) before
+// quantizing either, to keep more loads in flight; the static-scale mode, bound
+// by its IEEE divisions, takes one at a time.
+template <int MODE>
+__global__ void __launch_bounds__(256) fake_quant_flat_kernel(
+    const uint16_t* __restrict__ x, int64_t nblocks, const float* __restrict__ gsf,
+    uint16_t* __restrict__ out, uint8_t* __restrict__ scales, uint8_t* __restrict__ codes) {
+  constexpr int kUnroll = MODE == kStaticBf16 ? 1 : 2;
+  const float g = (MODE == kStaticBf16) ? *gsf : 1.0f;
+  const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nblocks;
+       i += kUnroll * step) {
+    Block16 v[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u)
+      if (i + u * step < nblocks) v[u] = load_block(x + (i + u * step) * 16);
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int64_t b = i + u * step;
+      if (b < nblocks)
+        quant_block<MODE>(v[u], g, out != nullptr ? out + b * 16 : nullptr,
+                          scales != nullptr ? scales + b : nullptr,
+                          codes != nullptr ? codes + b * 8 : nullptr);
+    }
+  }
+}
+
+// Strided operands: rows over grid y, 16-element blocks of a row over grid x.
+template <int MODE>
+__global__ void __launch_bounds__(256) fake_quant_rows_kernel(
     const uint16_t* __restrict__ x, int64_t rows, int64_t nbc, int64_t ld_x,
     const float* __restrict__ gsf, uint16_t* __restrict__ out, int64_t ld_out,
     uint8_t* __restrict__ scales, int64_t ld_s, uint8_t* __restrict__ codes, int64_t ld_c) {
   const float g = (MODE == kStaticBf16) ? *gsf : 1.0f;
-  const int64_t total = rows * nbc;
-  const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
-       idx += step) {
-    const int64_t r = idx / nbc;
-    const int64_t cb = idx - r * nbc;
-    const uint16_t* src = x + r * ld_x + cb * 16;
-    const uint4 v0 = ld_stream(src);
-    const uint4 v1 = ld_stream(src + 8);
-    const uint32_t xv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-    Q16 q;
-    if constexpr (MODE == kStaticBf16) {
-      q = quant16_static(xv, g);
-    } else {
-      q = quant16_unit<MODE == kUnitF16>(xv);
-    }
-    if (out != nullptr) {
-      uint4* dst = reinterpret_cast<uint4*>(out + r * ld_out + cb * 16);
-      dst[0] = make_uint4(q.out[0], q.out[1], q.out[2], q.out[3]);
-      dst[1] = make_uint4(q.out[4], q.out[5], q.out[6], q.out[7]);
-    }
-    if (scales != nullptr) scales[r * ld_s + cb] = static_cast<uint8_t>(q.sbyte);
-    if (codes != nullptr) {
-      *reinterpret_cast<uint2*>(codes + r * ld_c + cb * 8) = make_uint2(q.codes[0], q.codes[1]);
-    }
+  const int64_t cstep = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t r = blockIdx.y; r < rows; r += gridDim.y) {
+    for (int64_t cb = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; cb < nbc;
+         cb += cstep)
+      quant_block<MODE>(load_block(x + r * ld_x + cb * 16), g,
+                        out != nullptr ? out + r * ld_out + cb * 16 : nullptr,
+                        scales != nullptr ? scales + r * ld_s + cb : nullptr,
+                        codes != nullptr ? codes + r * ld_c + cb * 8 : nullptr);
   }
 }
 
@@ -105,6 +152,26 @@ int grid_for(int64_t work, int threads) {
   return static_cast<int>(blocks < 1 ? 1 : blocks);
 }
 
+// One full wave of `kernel` (resident blocks per SM x SMs), at most enough
+// blocks for `work` threads.  The occupancy query runs once per kernel.
+template <class K>
+int wave_grid(K kernel, int64_t work, int threads) {
+  static int per_sm = 0;
+  if (per_sm == 0) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, 0) != cudaSuccess ||
+        n < 1)
+      n = 1;
+    per_sm = n;
+  }
+  int dev = 0, sms = 152;
+  if (cudaGetDevice(&dev) == cudaSuccess)
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int64_t blocks = std::min<int64_t>((work + threads - 1) / threads,
+                                           static_cast<int64_t>(sms) * per_sm);
+  return static_cast<int>(std::max<int64_t>(blocks, 1));
+}
+
 }  // namespace
 
 cudaError_t launch_fake_quant(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
@@ -113,20 +180,46 @@ cudaError_t launch_fake_quant(const void* x, int64_t rows, int64_t cols, int64_t
                               cudaStream_t stream) {
   const int64_t nbc = cols / 16;
   const int threads = 256;
-  const int grid = grid_for(rows * nbc, threads);
   const auto* xs = static_cast<const uint16_t*>(x);
   auto* os = static_cast<uint16_t*>(out);
+  const bool flat = ld_x == cols && (out == nullptr || ld_out == cols) &&
+                    (scales == nullptr || ld_s == nbc) && (codes == nullptr || ld_c == cols / 2);
+  if (flat) {
+    const int64_t nblocks = rows * nbc;
+    const int64_t work = mode == kStaticBf16 ? nblocks : (nblocks + 1) / 2;  // threads needed
+    switch (mode) {
+      case kUnitBf16:
+        fake_quant_flat_kernel<kUnitBf16>
+            <<<wave_grid(fake_quant_flat_kernel<kUnitBf16>, work, threads), threads, 0, stream>>>(
+                xs, nblocks, gsf, os, scales, codes);
+        break;
+      case kUnitF16:
+        fake_quant_flat_kernel<kUnitF16>
+            <<<wave_grid(fake_quant_flat_kernel<kUnitF16>, work, threads), threads, 0, stream>>>(
+                xs, nblocks, gsf, os, scales, codes);
+        break;
+      default:
+        fake_quant_flat_kernel<kStaticBf16>
+            <<<wave_grid(fake_quant_flat_kernel<kStaticBf16>, work, threads), threads, 0, stream>>>(
+                xs, nblocks, gsf, os, scales, codes);
+        break;
+    }
+    return cudaGetLastError();
+  }
+  const int64_t gx = std::min<int64_t>((nbc + threads - 1) / threads, 64);
+  const int64_t gy = std::max<int64_t>(1, std::min<int64_t>({rows, 65535, grid_for(rows * nbc, threads) / gx + 1}));
+  const dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(gy));
   switch (mode) {
     case kUnitBf16:
-      fake_quant_kernel<kUnitBf16><<<grid, threads, 0, stream>>>(xs, rows, nbc, ld_x, gsf, os,
-                                                                 ld_out, scales, ld_s, codes, ld_c);
+      fake_quant_rows_kernel<kUnitBf16><<<grid, threads, 0, stream>>>(
+          xs, rows, nbc, ld_x, gsf, os, ld_out, scales, ld_s, codes, ld_c);
       break;
     case kUnitF16:
-      fake_quant_kernel<kUnitF16><<<grid, threads, 0, stream>>>(xs, rows, nbc, ld_x, gsf, os,
-                                                                ld_out, scales, ld_s, codes, ld_c);
+      fake_quant_rows_kernel<kUnitF16><<<grid, threads, 0, stream>>>(
+          xs, rows, nbc, ld_x, gsf, os, ld_out, scales, ld_s, codes, ld_c);
       break;
     default:
-      fake_quant_kernel<kStaticBf16><<<grid, threads, 0, stream>>>(
+      fake_quant_rows_kernel<kStaticBf16><<<grid, threads, 0, stream>>>(
           xs, rows, nbc, ld_x, gsf, os, ld_out, scales, ld_s, codes, ld_c);
       break;
   }
