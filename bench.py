@@ -62,23 +62,32 @@ def kernel_work(kind, b, n, h, d):
 
 
 # DRAM traffic per launch of a kernel (dram__bytes_read.sum + dram__bytes_write.sum)
-# from one ncu capture of this workload, with the SHA-256 of the kernel's source
-# at the time: a changed source reports null.  The capture is summarised under
-# profiles/ (file named in "summary").
-TRAFFIC = {}
+# from one single-pass ncu capture at the Wan 25088 shape
+# (profiles/traffic_attn_kernels_wan25088.md), with the SHA-256 of the kernel's
+# sources at the time: a changed source reports null.
+TRAFFIC = {
+    "bwd_dkdv": {"bytes": 437230336, "sources": ['nvfp4_fake_quant_gb300/csrc/attn_bwd.cu', 'nvfp4_fake_quant_gb300/csrc/nvq_ptx.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_quant.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_internal.h'],
+               "sha256": "38695c9806cad52a9b2ec4501805e86ea3812d84d2a789d4cfdc6c77563c076d"},
+    "bwd_dq": {"bytes": 373778176, "sources": ['nvfp4_fake_quant_gb300/csrc/attn_bwd_dq.cu', 'nvfp4_fake_quant_gb300/csrc/nvq_ptx.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_quant.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_internal.h'],
+               "sha256": "43af392edd85ba19e34ce9ca6cabe66cc2500e69f25d1228c7dd0980d8eb7f5e"},
+    "attn_fwd": {"bytes": 296573440, "sources": ['nvfp4_fake_quant_gb300/csrc/attn_fwd.cu', 'nvfp4_fake_quant_gb300/csrc/nvq_ptx.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_quant.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_internal.h'],
+               "sha256": "aa7567deabe820611e4c9d305e6c4a897925eea13153c00cd19d1c39563fc5e3"},
+}
 
 
 def traffic_for(kind):
     t = TRAFFIC.get(kind)
-    if t is None:
+    if t is None or (SHAPE["n"], SHAPE["h"]) != (25088, 12):
         return None
     import hashlib
+    m = hashlib.sha256()
     try:
-        with open(os.path.join(ROOT, t["source"]), "rb") as f:
-            digest = hashlib.sha256(f.read()).hexdigest()
+        for f in t["sources"]:
+            with open(os.path.join(ROOT, f), "rb") as fh:
+                m.update(fh.read())
     except OSError:
         return None
-    return t["bytes"] if digest == t["sha256"] else None
+    return t["bytes"] if m.hexdigest() == t["sha256"] else None
 
 
 def load_peaks():
