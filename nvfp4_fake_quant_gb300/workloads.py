@@ -9,6 +9,8 @@ Workloads (shapes of the Wan2.1-T2V-1.3B attention that the "Attn-QAT
 Training" guide trains; 12 heads of 128 from the "vsqa-preview-1.3b
 metadata.json" architecture, latent grids from its training geometry):
   tiny        B=1, H=2, N=256, D=64, q/k/v/dO iid N(0,1), seed 0, scale 1/8
+  vsa25088    B=1, H=12, N=25088 (16x28x56 latent), D=128, q/k/v/dO iid N(0,1),
+              seed 4 (block-sparse: 196 cubes of 4x4x8, top-20 key cubes each)
   quant       X bf16 [4096, 4096] N(0,1); 1% of entries (uniform, without
               replacement) multiplied by 50; then 2% of the 16-element blocks
               zeroed; seed 1
@@ -86,6 +88,18 @@ def wan25088() -> AttnInputs:
 
 def wan32760() -> AttnInputs:
     return attn_inputs(1, 32760, 32760, 12, 128, seed=3, dist="lognormal_channels")
+
+
+# Latent grid of the block-sparse workload (Wan2.1-1.3B at 448x896x61 frames:
+# 16 x 28 x 56 tokens) and its cube shape (4 x 4 x 8 = 128 tokens per cube).
+VSA_GRID = (16, 28, 56)
+VSA_CUBE = (4, 4, 8)
+
+
+def vsa25088() -> AttnInputs:
+    """Block-sparse workload: B=1, H=12, N=25088, D=128, q/k/v/dO iid N(0,1), seed 4,
+    tokens in raster (t, h, w) order of the VSA_GRID latent."""
+    return attn_inputs(1, 25088, 25088, 12, 128, seed=4)
 
 
 def quant_matrix(rows=4096, cols=4096, seed=1, outlier_frac=0.01, outlier_mul=50.0,

@@ -11,7 +11,10 @@ Modules
                in numpy with an explicit arithmetic precision, plus an exact
                ``fractions.Fraction`` version used to pin it.
 ``attention``  forward and straight-through backward of fake-quantized attention
-               in float64, whole-tensor and sampled (per query row / per key).
+               in float64, whole-tensor and sampled (per query row / per key),
+               dense or block-sparse (a list of key tiles per query tile).
+``vsa``        video sparse attention: cube token order, the top-k formula and
+               the cube-mean score selection of key tiles.
 
 Sources (web pages on the subject; cited by title and section):
   * "nvfp4_qad.py" (FastVideo ``fastvideo/layers/quantization/nvfp4_qad.py``):
@@ -25,7 +28,8 @@ Sources (web pages on the subject; cited by title and section):
     (the exact-m statistics switch).
   * "vsqa-preview-1.3b metadata.json", ``attention.precision`` of the dense
     ATTN_QAT_TRAIN ancestor (group size 16, NVFP4 E2M1 values, FP8 E4M3FN
-    scales, quant_p, quant_v, no two-level P, backward "consistent STE").
+    scales, quant_p, quant_v, no two-level P, backward "consistent STE"), and
+    ``attention`` of the VSA run (cube_shape, selection sparsity and top-k).
 
 Every function is pinned by ``tests/test_oracle_*.py`` (hand-worked examples,
 library routines, brute force, invariants); none is marked "parity unpinned".

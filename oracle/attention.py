@@ -33,6 +33,15 @@ operands), m held constant:
 ``delta_mode="hp"`` takes d from the unquantized-P output P V~ / l instead (the
 "auxiliary output" reading of the metadata's backward description).
 
+Block-sparse variant (``kv_tiles``): the fine attention of the video sparse
+attention recipe in "vsqa-preview-1.3b metadata.json" (``attention.kind`` vsa,
+``cube_shape`` [4, 4, 8], ``precision.fine`` NVFP4 fake-quant): tokens are in
+cube order, a tile is one cube of TILE = 128 tokens, and query tile i attends
+only to the key tiles listed in ``kv_tiles[b, h, i]``.  Every other score is
+-inf, so P = 0 there; tile boundaries are multiples of 16, so each P~ block lies
+wholly inside or wholly outside the selection and the definition above applies
+unchanged.
+
 Query rows are processed in blocks only to bound memory; nothing else is
 reordered.
 """
@@ -45,6 +54,7 @@ import torch
 from .nvfp4 import fq
 
 F64 = torch.float64
+TILE = 128  # tokens per tile of the block-sparse variant (one 4x4x8 cube)
 
 
 def _t(x) -> torch.Tensor:
@@ -60,11 +70,24 @@ def _head(x, b, h):
     return _t(x)[b, :, h, :]
 
 
-def _scores(qt_rows, kt, scale, rows, causal):
+def _allowed(tiles, rows, keys):
+    """[R, C] bool: key ``keys[c]`` lies in a tile listed for the tile of ``rows[r]``."""
+    rows, keys = torch.as_tensor(rows), torch.as_tensor(keys)
+    ok = torch.zeros(int(tiles.shape[0]), int(keys.max()) // TILE + 1, dtype=torch.bool)
+    for i in range(tiles.shape[0]):
+        for t in tiles[i].tolist():
+            if t < ok.shape[1]:
+                ok[i, t] = True
+    return ok[rows // TILE][:, keys // TILE]
+
+
+def _scores(qt_rows, kt, scale, rows, causal, tiles=None, keys=None):
     s = scale * (qt_rows @ kt.T)
+    keys = torch.arange(kt.shape[0]) if keys is None else torch.as_tensor(keys)
     if causal:
-        j = torch.arange(kt.shape[0])
-        s = s.masked_fill(j[None, :] > torch.as_tensor(rows)[:, None], float("-inf"))
+        s = s.masked_fill(keys[None, :] > torch.as_tensor(rows)[:, None], float("-inf"))
+    if tiles is not None:
+        s = s.masked_fill(~_allowed(tiles, rows, keys), float("-inf"))
     return s
 
 
@@ -79,16 +102,18 @@ def _probs(s, quant):
 class HeadProblem:
     """One (b, h) head with its quantized operands, for sampled evaluation."""
 
-    def __init__(self, q, k, v, b, h, scale, causal=False, quant=True):
+    def __init__(self, q, k, v, b, h, scale, causal=False, quant=True, kv_tiles=None):
         self.qt = quantize_rows(_head(q, b, h), quant)
         self.kt = quantize_rows(_head(k, b, h), quant)
         self.vt = quantize_rows(_head(v, b, h), quant)
         self.scale, self.causal, self.quant = float(scale), bool(causal), bool(quant)
+        # this head's [n_query_tiles, topk] selected key tiles, or None (dense)
+        self.tiles = None if kv_tiles is None else torch.as_tensor(kv_tiles)[b, h].long()
 
     def fwd_rows(self, rows):
         """(o [R, D], lse [R], m [R]) for query rows ``rows``."""
         rows = torch.as_tensor(rows, dtype=torch.long)
-        s = _scores(self.qt[rows], self.kt, self.scale, rows, self.causal)
+        s = _scores(self.qt[rows], self.kt, self.scale, rows, self.causal, self.tiles)
         m, _, l, pt = _probs(s, self.quant)
         o = (pt @ self.vt) / l[:, None]
         return o, m + torch.log(l), m
@@ -99,7 +124,7 @@ class HeadProblem:
         ms, ls = [], []
         for r0 in range(0, n, block):
             rows = torch.arange(r0, min(n, r0 + block))
-            s = _scores(self.qt[rows], self.kt, self.scale, rows, self.causal)
+            s = _scores(self.qt[rows], self.kt, self.scale, rows, self.causal, self.tiles)
             m = s.amax(dim=1)
             ms.append(m)
             ls.append(torch.exp(s - m[:, None]).sum(dim=1))
@@ -108,7 +133,7 @@ class HeadProblem:
     def dq_rows(self, rows, o_rows, do_rows, delta_mode="o"):
         """dQ for query rows ``rows``; o_rows/do_rows are those rows of O and dO."""
         rows = torch.as_tensor(rows, dtype=torch.long)
-        s = _scores(self.qt[rows], self.kt, self.scale, rows, self.causal)
+        s = _scores(self.qt[rows], self.kt, self.scale, rows, self.causal, self.tiles)
         m, p, l, pt = _probs(s, self.quant)
         a = p / l[:, None]
         do_rows = _t(do_rows)
@@ -139,9 +164,8 @@ class HeadProblem:
         n = self.qt.shape[0]
         for r0 in range(0, n, block):
             rows = torch.arange(r0, min(n, r0 + block))
-            s = _scores(self.qt[rows], self.kt[keys], self.scale, rows, False)
-            if self.causal:
-                s = s.masked_fill(keys[None, :] > rows[:, None], float("-inf"))
+            s = _scores(self.qt[rows], self.kt[keys], self.scale, rows, self.causal, self.tiles,
+                        keys)
             m, l = m_all[rows], l_all[rows]
             p = torch.exp(s - m[:, None])
             # keys holds whole 16-key blocks in order, so fq along it is blockwise
@@ -150,7 +174,7 @@ class HeadProblem:
             if delta_mode == "o":
                 delta = (do[rows] * o[rows]).sum(dim=1)
             else:
-                sf = _scores(self.qt[rows], self.kt, self.scale, rows, self.causal)
+                sf = _scores(self.qt[rows], self.kt, self.scale, rows, self.causal, self.tiles)
                 pf = torch.exp(sf - m[:, None])
                 delta = (do[rows] * ((pf @ self.vt) / l[:, None])).sum(dim=1)
             dv += (pt / l[:, None]).T @ do[rows]
@@ -160,8 +184,9 @@ class HeadProblem:
         return dk[sel], dv[sel]
 
 
-def attn_fwd(q, k, v, scale=None, causal=False, quant=True, block=512):
-    """Whole-tensor forward: (o [B,Nq,H,D], lse [B,H,Nq], m [B,H,Nq]) in float64."""
+def attn_fwd(q, k, v, scale=None, causal=False, quant=True, block=512, kv_tiles=None):
+    """Whole-tensor forward: (o [B,Nq,H,D], lse [B,H,Nq], m [B,H,Nq]) in float64.
+    ``kv_tiles``: [B, H, Nq/TILE, topk] selected key tiles (block-sparse), or None."""
     q, k, v = _t(q), _t(k), _t(v)
     bsz, nq, nh, d = q.shape
     scale = 1.0 / math.sqrt(d) if scale is None else scale
@@ -170,7 +195,7 @@ def attn_fwd(q, k, v, scale=None, causal=False, quant=True, block=512):
     mm = torch.zeros(bsz, nh, nq, dtype=F64)
     for b in range(bsz):
         for h in range(nh):
-            hp = HeadProblem(q, k, v, b, h, scale, causal, quant)
+            hp = HeadProblem(q, k, v, b, h, scale, causal, quant, kv_tiles)
             for r0 in range(0, nq, block):
                 rows = torch.arange(r0, min(nq, r0 + block))
                 ob, lb, mb = hp.fwd_rows(rows)
@@ -180,8 +205,10 @@ def attn_fwd(q, k, v, scale=None, causal=False, quant=True, block=512):
     return o, lse, mm
 
 
-def attn_bwd(q, k, v, o, do, scale=None, causal=False, quant=True, delta_mode="o", block=512):
-    """Whole-tensor straight-through backward: (dq, dk, dv) in float64."""
+def attn_bwd(q, k, v, o, do, scale=None, causal=False, quant=True, delta_mode="o", block=512,
+             kv_tiles=None):
+    """Whole-tensor straight-through backward: (dq, dk, dv) in float64.
+    ``kv_tiles`` as in attn_fwd."""
     q, k, v, o, do = _t(q), _t(k), _t(v), _t(o), _t(do)
     bsz, nq, nh, d = q.shape
     nkv = k.shape[1]
@@ -191,10 +218,10 @@ def attn_bwd(q, k, v, o, do, scale=None, causal=False, quant=True, delta_mode="o
     dv = torch.zeros_like(v)
     for b in range(bsz):
         for h in range(nh):
-            hp = HeadProblem(q, k, v, b, h, scale, causal, quant)
+            hp = HeadProblem(q, k, v, b, h, scale, causal, quant, kv_tiles)
             for r0 in range(0, nq, block):
                 rows = torch.arange(r0, min(nq, r0 + block))
-                s = _scores(hp.qt[rows], hp.kt, hp.scale, rows, hp.causal)
+                s = _scores(hp.qt[rows], hp.kt, hp.scale, rows, hp.causal, hp.tiles)
                 m, p, l, pt = _probs(s, hp.quant)
                 a = p / l[:, None]
                 do_r = do[b, rows, h]
