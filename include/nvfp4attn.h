@@ -194,6 +194,62 @@ nvq_status attn_qat_bwd_builtin_scratch(const void* q, const void* k, const void
                                         nvq_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
+/* Block-sparse attention (video sparse attention, VSA)                     */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * The fine attention of the VSA recipe ("vsqa-preview-1.3b metadata.json",
+ * attention: kind vsa, cube_shape [4, 4, 8], precision.fine NVFP4 fake-quant,
+ * selection.sparsity 0.9, selection.effective_topk = max(1, min(ceil((1 -
+ * sparsity) * num_blocks), num_blocks))): tokens in cube order, a tile is one
+ * cube of 128 tokens, and query tile i attends only to the key tiles listed in
+ * kv_tiles[b][h][i][0..topk).  Everything else is the dense Attn-QAT above
+ * with the other scores at -inf (P~ blocks are tile-aligned).
+ */
+
+/*
+ * Token rows between the raster order (t, h, w) of a T x Hh x W latent and cube
+ * order (cubes of ct x ch x cw tokens in raster order over the cube grid, tokens
+ * in raster order inside a cube).
+ *   x, out   bf16 [B, T*Hh*W, H, D] contiguous, distinct (not in place), 16-byte
+ *            aligned; H*D % 8 == 0
+ *   to_cubes 1: raster -> cube order; 0: cube -> raster order
+ * T % ct == Hh % ch == W % cw == 0, else NVQ_ERR_INVALID.
+ */
+nvq_status vsa_reorder(const void* x, int B, int T, int Hh, int W, int H, int D, int ct, int ch,
+                       int cw, int to_cubes, void* out, nvq_stream_t stream);
+
+/*
+ * Block selection.  q, k: bf16 [B, N, H, D] in cube order, N % 128 == 0, D in
+ * 1..1024.  For every (b, h) and query tile i, score(i, j) = mean_q(i) . mean_k(j)
+ * (fp32 means over the 128 tokens of a tile, fp32 dot product over D), and
+ * kv_tiles[b][h][i] (int32 [B, H, N/128, topk], written) receives the topk key
+ * tiles of highest score, ties to the lower index, in ascending tile order.
+ * 1 <= topk <= N/128.  ws: at least vsa_select_workspace(...) bytes, 256-byte aligned.
+ */
+size_t vsa_select_workspace(int B, int N, int H, int D);
+nvq_status vsa_select_tiles(const void* q, const void* k, int B, int N, int H, int D, int topk,
+                            int32_t* kv_tiles, void* ws, size_t ws_bytes, nvq_stream_t stream);
+
+/*
+ * Block-sparse forward and straight-through backward.  Arguments as in
+ * attn_qat_fwd / attn_qat_bwd with Nq == Nkv == N, N % 128 == 0, non-causal,
+ * plus kv_tiles (int32 [B, H, N/128, topk], 4-byte aligned; entries distinct
+ * and in [0, N/128) in every list, as vsa_select_tiles writes them) and
+ * 1 <= topk <= N/128.  The forward workspace is attn_qat_fwd_workspace(B, N, N,
+ * H, D); the backward's is attn_qat_bwd_sparse_workspace (it also holds the
+ * lists transposed to per-key-tile form).
+ */
+nvq_status attn_qat_fwd_sparse(const void* q, const void* k, const void* v, int B, int N, int H,
+                               int D, float scale, const int32_t* kv_tiles, int topk, void* o,
+                               float* stats, void* ws, size_t ws_bytes, nvq_stream_t stream);
+size_t attn_qat_bwd_sparse_workspace(int B, int N, int H, int D, int topk);
+nvq_status attn_qat_bwd_sparse(const void* q, const void* k, const void* v, const void* o,
+                               const float* stats, const void* dout, const int32_t* kv_tiles,
+                               int topk, void* dq, void* dk, void* dv, int B, int N, int H, int D,
+                               float scale, void* ws, size_t ws_bytes, nvq_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
 /* Per-kernel device timing (a profiling aid; no counterpart in the pages)  */
 /* ------------------------------------------------------------------------ */
 
@@ -205,7 +261,8 @@ enum {
   NVQ_KERNEL_BWD_DKDV = 3,   /* backward, key-outer dK and dV kernel */
   NVQ_KERNEL_BWD_DQ = 4,     /* backward, query-outer dQ kernel */
   NVQ_KERNEL_GLOBAL_SF = 5,  /* static global scale (amax reduction and finalize) */
-  NVQ_KERNEL_KINDS = 6
+  NVQ_KERNEL_VSA = 6,        /* block-sparse support: token reorder, block selection */
+  NVQ_KERNEL_KINDS = 7
 };
 
 /*

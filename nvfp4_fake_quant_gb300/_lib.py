@@ -39,6 +39,18 @@ SIGNATURES = {
     "attn_qat_bwd_builtin_scratch": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                              c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int,
                                              c_int, c_int, c_int, c_float, c_int, c_void_p]),
+    "vsa_reorder": (c_int, [c_void_p, c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int,
+                            c_int, c_void_p, c_void_p]),
+    "vsa_select_workspace": (c_size_t, [c_int, c_int, c_int, c_int]),
+    "vsa_select_tiles": (c_int, [c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_void_p,
+                                 c_void_p, c_size_t, c_void_p]),
+    "attn_qat_fwd_sparse": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int,
+                                    c_float, c_void_p, c_int, c_void_p, c_void_p, c_void_p,
+                                    c_size_t, c_void_p]),
+    "attn_qat_bwd_sparse_workspace": (c_size_t, [c_int, c_int, c_int, c_int, c_int]),
+    "attn_qat_bwd_sparse": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                    c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_int, c_int,
+                                    c_int, c_int, c_float, c_void_p, c_size_t, c_void_p]),
     "nvq_timing_enable": (c_int, [c_int]),
     "nvq_timing_read": (c_int, [c_int, c_void_p, c_void_p]),
     "nvq_selftest_umma": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int,

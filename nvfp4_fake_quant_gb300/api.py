@@ -167,7 +167,7 @@ def attn_qat_bwd(q, k, v, o, stats, do, scale=None, causal=False, dq=None, dk=No
 
 # Kernel kinds of nvq_timing_read (include/nvfp4attn.h, NVQ_KERNEL_*)
 KERNEL_KINDS = {"quantize": 0, "attn_fwd": 1, "bwd_delta": 2, "bwd_dkdv": 3, "bwd_dq": 4,
-                "global_sf": 5}
+                "global_sf": 5, "vsa": 6}
 
 
 def timing_enable(on: bool = True) -> None:
@@ -184,6 +184,91 @@ def timing_read() -> dict:
         _lib.call("nvq_timing_read", kind, ctypes.addressof(n), ctypes.addressof(ms))
         out[name] = (int(n.value), float(ms.value))
     return out
+
+
+# ------------------------------------------------------- block-sparse (VSA)
+
+VSA_TILE = 128  # tokens per tile: one 4x4x8 cube
+
+
+def _check_tiles(kv_tiles, b, h, n):
+    _check(kv_tiles, "kv_tiles", torch.int32)
+    if kv_tiles.dim() != 4 or tuple(kv_tiles.shape[:3]) != (b, h, n // VSA_TILE) or \
+            not kv_tiles.is_contiguous():
+        raise ValueError(f"kv_tiles must be contiguous int32 [B, H, N/128, topk] = "
+                         f"[{b}, {h}, {n // VSA_TILE}, topk], got {tuple(kv_tiles.shape)}")
+
+
+def vsa_effective_topk(sparsity: float, num_blocks: int) -> int:
+    """max(1, min(ceil((1 - sparsity) * num_blocks), num_blocks)) (the VSA metadata's formula)."""
+    return max(1, min(math.ceil((1.0 - sparsity) * num_blocks), num_blocks))
+
+
+def vsa_reorder(x, grid, cube=(4, 4, 8), to_cubes=True, out=None):
+    """Token rows of bf16 [B, T*Hh*W, H, D] between raster and cube order."""
+    _check(x, "x", torch.bfloat16)
+    b, n, h, d = x.shape
+    t, hh, w = grid
+    if n != t * hh * w:
+        raise ValueError(f"x has {n} tokens, the grid {t}x{hh}x{w}")
+    out = torch.empty_like(x) if out is None else out
+    _lib.call("vsa_reorder", _ptr(x), b, t, hh, w, h, d, cube[0], cube[1], cube[2],
+              int(bool(to_cubes)), _ptr(out), _stream_ptr(x))
+    return out
+
+
+def vsa_select_tiles(q, k, topk, workspace=None):
+    """int32 [B, H, N/128, topk]: per query tile the topk key tiles by cube-mean score."""
+    _check_bnhd(q, "q")
+    _check_bnhd(k, "k", q.shape)
+    b, n, h, d = q.shape
+    out = torch.empty((b, h, n // VSA_TILE, topk), dtype=torch.int32, device=q.device)
+    need = int(_lib.load().vsa_select_workspace(b, n, h, d))
+    ws = _workspace(need, q.device, workspace)
+    _lib.call("vsa_select_tiles", _ptr(q), _ptr(k), b, n, h, d, int(topk), _ptr(out), _ptr(ws),
+              ws.numel() * ws.element_size(), _stream_ptr(q))
+    return out
+
+
+def attn_qat_fwd_sparse(q, k, v, kv_tiles, scale=None, o=None, stats=None, workspace=None):
+    """Block-sparse forward (tokens in cube order): (o, stats)."""
+    _check_bnhd(q, "q")
+    b, n, h, d = q.shape
+    _check_bnhd(k, "k", q.shape)
+    _check_bnhd(v, "v", q.shape)
+    _check_tiles(kv_tiles, b, h, n)
+    topk = kv_tiles.shape[-1]
+    scale = default_scale(d) if scale is None else float(scale)
+    o = torch.empty_like(q) if o is None else o
+    if stats is None:
+        stats = torch.empty((b, h, 2, n), dtype=torch.float32, device=q.device)
+    ws = _workspace(attn_qat_fwd_workspace(b, n, n, h, d), q.device, workspace)
+    _lib.call("attn_qat_fwd_sparse", _ptr(q), _ptr(k), _ptr(v), b, n, h, d, scale, _ptr(kv_tiles),
+              topk, _ptr(o), _ptr(stats), _ptr(ws), ws.numel() * ws.element_size(),
+              _stream_ptr(q))
+    return o, stats
+
+
+def attn_qat_bwd_sparse(q, k, v, o, stats, do, kv_tiles, scale=None, dq=None, dk=None, dv=None,
+                        workspace=None):
+    """Block-sparse straight-through backward: (dq, dk, dv)."""
+    _check_bnhd(q, "q")
+    b, n, h, d = q.shape
+    for t_, name in ((k, "k"), (v, "v"), (o, "o"), (do, "do")):
+        _check_bnhd(t_, name, q.shape)
+    _check(stats, "stats", torch.float32)
+    _check_tiles(kv_tiles, b, h, n)
+    topk = kv_tiles.shape[-1]
+    scale = default_scale(d) if scale is None else float(scale)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    need = int(_lib.load().attn_qat_bwd_sparse_workspace(b, n, h, d, topk))
+    ws = _workspace(need, q.device, workspace)
+    _lib.call("attn_qat_bwd_sparse", _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(stats), _ptr(do),
+              _ptr(kv_tiles), topk, _ptr(dq), _ptr(dk), _ptr(dv), b, n, h, d, scale, _ptr(ws),
+              ws.numel() * ws.element_size(), _stream_ptr(q))
+    return dq, dk, dv
 
 
 def device_status(device=None) -> int:

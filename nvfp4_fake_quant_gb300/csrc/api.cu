@@ -198,15 +198,23 @@ FwdWs fwd_ws(int B, int Nq, int Nkv, int H, int D) {
 }
 
 struct BwdWs {
-  size_t q, k, v, delta, total;
+  size_t q, k, v, delta, q_off, q_list, total;
 };
-BwdWs bwd_ws(int B, int Nq, int Nkv, int H, int D) {
+// topk > 0: block-sparse, with room for the transposed tile lists
+BwdWs bwd_ws(int B, int Nq, int Nkv, int H, int D, int topk = 0) {
   BwdWs w;
   w.q = 0;
   w.k = round_up(w.q + bytes_bnhd(B, Nq, H, D, 2), 256);
   w.v = round_up(w.k + bytes_bnhd(B, Nkv, H, D, 2), 256);
   w.delta = round_up(w.v + bytes_bnhd(B, Nkv, H, D, 2), 256);
-  w.total = round_up(w.delta + static_cast<size_t>(B) * H * Nq * 4, 256);
+  w.q_off = round_up(w.delta + static_cast<size_t>(B) * H * Nq * 4, 256);
+  w.q_list = w.q_off;
+  w.total = w.q_off;
+  if (topk > 0) {
+    const size_t n_qt = (Nq + kTile - 1) / kTile, n_kt = (Nkv + kTile - 1) / kTile;
+    w.q_list = round_up(w.q_off + static_cast<size_t>(B) * H * (n_kt + 1) * 4, 256);
+    w.total = round_up(w.q_list + static_cast<size_t>(B) * H * n_qt * topk * 4, 256);
+  }
   return w;
 }
 
@@ -227,6 +235,102 @@ nvq_status check_quant(const void* x, int64_t rows, int64_t cols, int64_t ld_x) 
 }
 
 }  // namespace
+// Forward; kv_list: NULL (dense) or the block-sparse key-tile lists (validated
+// by the caller).
+nvq_status fwd_impl(const void* q, const void* k, const void* v, int B, int Nq, int Nkv, int H,
+                    int D, float scale, int causal, const int* kv_list, int topk, void* o,
+                    float* stats, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  nvq_status st = check_attn(B, Nq, Nkv, H, D, scale, causal);
+  if (st != NVQ_OK) return st;
+  if (!q || !k || !v || !o || !stats || !aligned16(q) || !aligned16(k) || !aligned16(v) ||
+      !aligned16(o) || !aligned16(stats))
+    return NVQ_ERR_INVALID;
+  const FwdWs w = fwd_ws(B, Nq, Nkv, H, D);
+  if (ws == nullptr || ws_bytes < w.total || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
+    return NVQ_ERR_WORKSPACE;
+  int* err = error_word();
+  if (err == nullptr) return NVQ_ERR_CUDA;
+  uint8_t* wb = static_cast<uint8_t*>(ws);
+  void* qt = wb + w.q;
+  void* kt = wb + w.k;
+  void* vt = wb + w.v;
+  CUtensorMap mq, mk, mv;
+  int r;
+  if ((r = make_bnhd_map(&mq, qt, B, Nq, H, D, false)) != 0 ||
+      (r = make_bnhd_map(&mk, kt, B, Nkv, H, D, false)) != 0 ||
+      (r = make_bnhd_map(&mv, vt, B, Nkv, H, D, true)) != 0)
+    return fail_driver("cuTensorMapEncodeTiled", r);
+  const int64_t rq = static_cast<int64_t>(B) * Nq * H, rk = static_cast<int64_t>(B) * Nkv * H;
+  cudaError_t e;
+  if ((e = quantize_rows(q, rq, D, kUnitBf16, qt, stream)) != cudaSuccess)
+    return fail_cuda("quantize q", e);
+  if ((e = quantize_rows(k, rk, D, kUnitBf16, kt, stream)) != cudaSuccess)
+    return fail_cuda("quantize k", e);
+  if ((e = quantize_rows(v, rk, D, kUnitF16, vt, stream)) != cudaSuccess)
+    return fail_cuda("quantize v", e);
+  const AttnShape s{B, Nq, Nkv, H, D, scale, causal};
+  return from_cuda("attn_fwd", timed(NVQ_KERNEL_ATTN_FWD, stream, [&] {
+                     return launch_attn_fwd(s, mq, mk, mv, o, stats, kv_list, topk, err, stream);
+                   }));
+}
+
+// Straight-through backward; kv_list as in fwd_impl.
+nvq_status bwd_impl(const void* q, const void* k, const void* v, const void* o,
+                    const float* stats, const void* dout, const int* kv_list, int topk, void* dq,
+                    void* dk, void* dv, int B, int Nq, int Nkv, int H, int D, float scale,
+                    int causal, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  nvq_status st = check_attn(B, Nq, Nkv, H, D, scale, causal);
+  if (st != NVQ_OK) return st;
+  const void* ptrs[] = {q, k, v, o, stats, dout, dq, dk, dv};
+  for (const void* p : ptrs)
+    if (p == nullptr || !aligned16(p)) return NVQ_ERR_INVALID;
+  const BwdWs w = bwd_ws(B, Nq, Nkv, H, D, kv_list != nullptr ? topk : 0);
+  if (ws == nullptr || ws_bytes < w.total || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
+    return NVQ_ERR_WORKSPACE;
+  int* err = error_word();
+  if (err == nullptr) return NVQ_ERR_CUDA;
+  uint8_t* wb = static_cast<uint8_t*>(ws);
+  void* qt = wb + w.q;
+  void* kt = wb + w.k;
+  void* vt = wb + w.v;
+  float* delta = reinterpret_cast<float*>(wb + w.delta);
+  int* q_off = kv_list != nullptr ? reinterpret_cast<int*>(wb + w.q_off) : nullptr;
+  int* q_list = kv_list != nullptr ? reinterpret_cast<int*>(wb + w.q_list) : nullptr;
+  const int n_qt = (Nq + kTile - 1) / kTile, n_kt = (Nkv + kTile - 1) / kTile;
+  CUtensorMap mq, mk, mv, mdo;
+  int r;
+  if ((r = make_bnhd_map(&mq, qt, B, Nq, H, D, false)) != 0 ||
+      (r = make_bnhd_map(&mk, kt, B, Nkv, H, D, false)) != 0 ||
+      (r = make_bnhd_map(&mv, vt, B, Nkv, H, D, false)) != 0 ||
+      (r = make_bnhd_map(&mdo, dout, B, Nq, H, D, false)) != 0)
+    return fail_driver("cuTensorMapEncodeTiled", r);
+  const int64_t rq = static_cast<int64_t>(B) * Nq * H, rk = static_cast<int64_t>(B) * Nkv * H;
+  const AttnShape s{B, Nq, Nkv, H, D, scale, causal};
+  cudaError_t e;
+  if ((e = quantize_rows(q, rq, D, kUnitBf16, qt, stream)) != cudaSuccess)
+    return fail_cuda("quantize q", e);
+  if ((e = quantize_rows(k, rk, D, kUnitBf16, kt, stream)) != cudaSuccess)
+    return fail_cuda("quantize k", e);
+  if ((e = quantize_rows(v, rk, D, kUnitBf16, vt, stream)) != cudaSuccess)
+    return fail_cuda("quantize v", e);
+  if ((e = timed(NVQ_KERNEL_BWD_DELTA, stream,
+                 [&] { return launch_bwd_prep(s, o, dout, delta, stream); })) != cudaSuccess)
+    return fail_cuda("bwd_prep", e);
+  if (kv_list != nullptr &&
+      (e = launch_tile_transpose(kv_list, B, H, n_qt, n_kt, topk, q_off, q_list, stream)) !=
+          cudaSuccess)
+    return fail_cuda("tile_transpose", e);
+  if ((e = timed(NVQ_KERNEL_BWD_DKDV, stream, [&] {
+         return launch_attn_bwd(s, mq, mk, mv, mdo, stats, delta, dk, dv, q_off, q_list,
+                                n_qt * topk, err, stream);
+       })) != cudaSuccess)
+    return fail_cuda("attn_bwd (dK, dV)", e);
+  return from_cuda("attn_bwd_dq", timed(NVQ_KERNEL_BWD_DQ, stream, [&] {
+                     return launch_attn_bwd_dq(s, mq, mdo, mk, mv, stats, delta, dq, kv_list, topk,
+                                               err, stream);
+                   }));
+}
+
 }  // namespace nvq
 
 using namespace nvq;
@@ -323,84 +427,85 @@ size_t attn_qat_bwd_workspace(int B, int Nq, int Nkv, int H, int D) {
 nvq_status attn_qat_fwd(const void* q, const void* k, const void* v, int B, int Nq, int Nkv,
                         int H, int D, float scale, int causal, void* o, float* stats, void* ws,
                         size_t ws_bytes, nvq_stream_t stream) {
-  nvq_status st = check_attn(B, Nq, Nkv, H, D, scale, causal);
-  if (st != NVQ_OK) return st;
-  if (!q || !k || !v || !o || !stats || !aligned16(q) || !aligned16(k) || !aligned16(v) ||
-      !aligned16(o) || !aligned16(stats))
-    return NVQ_ERR_INVALID;
-  const FwdWs w = fwd_ws(B, Nq, Nkv, H, D);
-  if (ws == nullptr || ws_bytes < w.total || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
-    return NVQ_ERR_WORKSPACE;
-  int* err = error_word();
-  if (err == nullptr) return NVQ_ERR_CUDA;
-  uint8_t* wb = static_cast<uint8_t*>(ws);
-  void* qt = wb + w.q;
-  void* kt = wb + w.k;
-  void* vt = wb + w.v;
-  CUtensorMap mq, mk, mv;
-  int r;
-  if ((r = make_bnhd_map(&mq, qt, B, Nq, H, D, false)) != 0 ||
-      (r = make_bnhd_map(&mk, kt, B, Nkv, H, D, false)) != 0 ||
-      (r = make_bnhd_map(&mv, vt, B, Nkv, H, D, true)) != 0)
-    return fail_driver("cuTensorMapEncodeTiled", r);
-  const int64_t rq = static_cast<int64_t>(B) * Nq * H, rk = static_cast<int64_t>(B) * Nkv * H;
-  cudaError_t e;
-  if ((e = quantize_rows(q, rq, D, kUnitBf16, qt, stream)) != cudaSuccess)
-    return fail_cuda("quantize q", e);
-  if ((e = quantize_rows(k, rk, D, kUnitBf16, kt, stream)) != cudaSuccess)
-    return fail_cuda("quantize k", e);
-  if ((e = quantize_rows(v, rk, D, kUnitF16, vt, stream)) != cudaSuccess)
-    return fail_cuda("quantize v", e);
-  const AttnShape s{B, Nq, Nkv, H, D, scale, causal};
-  return from_cuda("attn_fwd", timed(NVQ_KERNEL_ATTN_FWD, stream, [&] {
-                     return launch_attn_fwd(s, mq, mk, mv, o, stats, err, stream);
-                   }));
+  return fwd_impl(q, k, v, B, Nq, Nkv, H, D, scale, causal, nullptr, 0, o, stats, ws, ws_bytes,
+                  stream);
 }
 
 nvq_status attn_qat_bwd(const void* q, const void* k, const void* v, const void* o,
                         const float* stats, const void* dout, void* dq, void* dk, void* dv, int B,
                         int Nq, int Nkv, int H, int D, float scale, int causal, void* ws,
                         size_t ws_bytes, nvq_stream_t stream) {
-  nvq_status st = check_attn(B, Nq, Nkv, H, D, scale, causal);
+  return bwd_impl(q, k, v, o, stats, dout, nullptr, 0, dq, dk, dv, B, Nq, Nkv, H, D, scale, causal,
+                  ws, ws_bytes, stream);
+}
+
+// Block-sparse: N % 128 == 0 (whole tiles), 1 <= topk <= N / 128, an int32
+// list [B, H, N/128, topk], non-causal.
+static nvq_status check_sparse(int N, int topk, const int32_t* kv_tiles) {
+  if (N < 1 || N % kTile != 0 || topk < 1 || topk > N / kTile) return NVQ_ERR_INVALID;
+  if (kv_tiles == nullptr || (reinterpret_cast<uintptr_t>(kv_tiles) & 3u) != 0)
+    return NVQ_ERR_INVALID;
+  return NVQ_OK;
+}
+
+size_t attn_qat_bwd_sparse_workspace(int B, int N, int H, int D, int topk) {
+  if (B < 1 || N < 1 || H < 1 || D < 1 || topk < 1) return 0;
+  return bwd_ws(B, N, N, H, D, topk).total;
+}
+
+nvq_status attn_qat_fwd_sparse(const void* q, const void* k, const void* v, int B, int N, int H,
+                               int D, float scale, const int32_t* kv_tiles, int topk, void* o,
+                               float* stats, void* ws, size_t ws_bytes, nvq_stream_t stream) {
+  const nvq_status st = check_sparse(N, topk, kv_tiles);
   if (st != NVQ_OK) return st;
-  const void* ptrs[] = {q, k, v, o, stats, dout, dq, dk, dv};
-  for (const void* p : ptrs)
-    if (p == nullptr || !aligned16(p)) return NVQ_ERR_INVALID;
-  const BwdWs w = bwd_ws(B, Nq, Nkv, H, D);
-  if (ws == nullptr || ws_bytes < w.total || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
+  return fwd_impl(q, k, v, B, N, N, H, D, scale, 0, kv_tiles, topk, o, stats, ws, ws_bytes,
+                  stream);
+}
+
+nvq_status attn_qat_bwd_sparse(const void* q, const void* k, const void* v, const void* o,
+                               const float* stats, const void* dout, const int32_t* kv_tiles,
+                               int topk, void* dq, void* dk, void* dv, int B, int N, int H, int D,
+                               float scale, void* ws, size_t ws_bytes, nvq_stream_t stream) {
+  const nvq_status st = check_sparse(N, topk, kv_tiles);
+  if (st != NVQ_OK) return st;
+  return bwd_impl(q, k, v, o, stats, dout, kv_tiles, topk, dq, dk, dv, B, N, N, H, D, scale, 0, ws,
+                  ws_bytes, stream);
+}
+
+nvq_status vsa_reorder(const void* x, int B, int T, int Hh, int W, int H, int D, int ct, int ch,
+                       int cw, int to_cubes, void* out, nvq_stream_t stream) {
+  if (!x || !out || x == out || !aligned16(x) || !aligned16(out)) return NVQ_ERR_INVALID;
+  if (B < 1 || T < 1 || Hh < 1 || W < 1 || H < 1 || D < 1 || ct < 1 || ch < 1 || cw < 1)
+    return NVQ_ERR_INVALID;
+  if (T % ct || Hh % ch || W % cw || (static_cast<int64_t>(H) * D) % 8 != 0 ||
+      (to_cubes != 0 && to_cubes != 1))
+    return NVQ_ERR_INVALID;
+  return from_cuda("vsa_reorder", timed(NVQ_KERNEL_VSA, stream, [&] {
+                     return launch_vsa_reorder(x, B, T, Hh, W, H, D, ct, ch, cw, to_cubes, out,
+                                               stream);
+                   }));
+}
+
+size_t vsa_select_workspace(int B, int N, int H, int D) {
+  if (B < 1 || N < kTile || N % kTile != 0 || H < 1 || D < 1) return 0;
+  return 2 * round_up(static_cast<size_t>(B) * H * (N / kTile) * D * 4, 256);
+}
+
+nvq_status vsa_select_tiles(const void* q, const void* k, int B, int N, int H, int D, int topk,
+                            int32_t* kv_tiles, void* ws, size_t ws_bytes, nvq_stream_t stream) {
+  if (!q || !k || !kv_tiles || !aligned16(q) || !aligned16(k) ||
+      (reinterpret_cast<uintptr_t>(kv_tiles) & 3u) != 0)
+    return NVQ_ERR_INVALID;
+  if (B < 1 || H < 1 || D < 1 || D > 1024 || N < kTile || N % kTile != 0 || topk < 1 ||
+      topk > N / kTile)
+    return NVQ_ERR_INVALID;
+  const size_t need = vsa_select_workspace(B, N, H, D);
+  if (ws == nullptr || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
     return NVQ_ERR_WORKSPACE;
-  int* err = error_word();
-  if (err == nullptr) return NVQ_ERR_CUDA;
-  uint8_t* wb = static_cast<uint8_t*>(ws);
-  void* qt = wb + w.q;
-  void* kt = wb + w.k;
-  void* vt = wb + w.v;
-  float* delta = reinterpret_cast<float*>(wb + w.delta);
-  CUtensorMap mq, mk, mv, mdo;
-  int r;
-  if ((r = make_bnhd_map(&mq, qt, B, Nq, H, D, false)) != 0 ||
-      (r = make_bnhd_map(&mk, kt, B, Nkv, H, D, false)) != 0 ||
-      (r = make_bnhd_map(&mv, vt, B, Nkv, H, D, false)) != 0 ||
-      (r = make_bnhd_map(&mdo, dout, B, Nq, H, D, false)) != 0)
-    return fail_driver("cuTensorMapEncodeTiled", r);
-  const int64_t rq = static_cast<int64_t>(B) * Nq * H, rk = static_cast<int64_t>(B) * Nkv * H;
-  const AttnShape s{B, Nq, Nkv, H, D, scale, causal};
-  cudaError_t e;
-  if ((e = quantize_rows(q, rq, D, kUnitBf16, qt, stream)) != cudaSuccess)
-    return fail_cuda("quantize q", e);
-  if ((e = quantize_rows(k, rk, D, kUnitBf16, kt, stream)) != cudaSuccess)
-    return fail_cuda("quantize k", e);
-  if ((e = quantize_rows(v, rk, D, kUnitBf16, vt, stream)) != cudaSuccess)
-    return fail_cuda("quantize v", e);
-  if ((e = timed(NVQ_KERNEL_BWD_DELTA, stream,
-                 [&] { return launch_bwd_prep(s, o, dout, delta, stream); })) != cudaSuccess)
-    return fail_cuda("bwd_prep", e);
-  if ((e = timed(NVQ_KERNEL_BWD_DKDV, stream, [&] {
-         return launch_attn_bwd(s, mq, mk, mv, mdo, stats, delta, dk, dv, err, stream);
-       })) != cudaSuccess)
-    return fail_cuda("attn_bwd (dK, dV)", e);
-  return from_cuda("attn_bwd_dq", timed(NVQ_KERNEL_BWD_DQ, stream, [&] {
-                     return launch_attn_bwd_dq(s, mq, mdo, mk, mv, stats, delta, dq, err, stream);
+  float* qm = static_cast<float*>(ws);
+  float* km = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + need / 2);
+  return from_cuda("vsa_select", timed(NVQ_KERNEL_VSA, stream, [&] {
+                     return launch_vsa_select(q, k, B, N, H, D, topk, kv_tiles, qm, km, stream);
                    }));
 }
 

@@ -79,7 +79,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float* __restrict__ stats, const float* __restrict__ delta,
                     __nv_bfloat16* __restrict__ dk,
                     __nv_bfloat16* __restrict__ dv, int Nq, int Nkv, int H, float scale,
-                    int causal, int* __restrict__ err) {
+                    int causal, const int* __restrict__ q_off, const int* __restrict__ q_list,
+                    int q_stride, int* __restrict__ err) {
   using L = BwdLayout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023u) &
@@ -105,9 +106,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kAbort);
 
   const int n_q_all = (Nq + kTile - 1) / kTile;
-  const int i_begin = causal ? kt : 0;  // causal requires Nq == Nkv
-  const int n_iter = n_q_all - i_begin;
-  auto qtile = [&](int it) -> int { return i_begin + it; };
+  // query tiles of this key tile: all (dense; causal from the diagonal on, which
+  // needs Nq == Nkv) or those whose block-sparse list holds it (q_off/q_list,
+  // per (b, h): offsets [n_kt + 1] and query tiles in ascending order)
+  const int i_begin = causal ? kt : 0;
+  const int* qsel = nullptr;
+  int n_iter = n_q_all - i_begin;
+  if (q_off != nullptr) {
+    const int n_kt = (Nkv + kTile - 1) / kTile;
+    const int64_t head = static_cast<int64_t>(b) * H + h;
+    const int* off = q_off + head * (n_kt + 1);
+    qsel = q_list + head * q_stride + off[kt];
+    n_iter = off[kt + 1] - off[kt];
+  }
+  auto qtile = [&](int it) -> int { return qsel != nullptr ? qsel[it] : i_begin + it; };
 
 
   if (threadIdx.x == 0) {
@@ -433,7 +445,58 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
   }
 }
 
+// Block-sparse lists transposed, per (b, h) (grid (H, B)): for each key tile
+// the query tiles whose list holds it, in ascending order: offsets
+// q_off[n_kt + 1] and entries q_list[<= n_qt * topk].  A list that names a key
+// tile twice counts it once.
+__global__ void __launch_bounds__(256) tile_transpose_kernel(const int* __restrict__ kv_list,
+                                                             int H, int n_qt, int n_kt, int topk,
+                                                             int* __restrict__ q_off,
+                                                             int* __restrict__ q_list) {
+  extern __shared__ int start[];  // [n_kt + 1]
+  const int64_t head = static_cast<int64_t>(blockIdx.y) * H + blockIdx.x;
+  const int* lst = kv_list + head * n_qt * topk;
+  auto holds = [&](int i, int kt) {
+    for (int e = 0; e < topk; ++e)
+      if (lst[i * topk + e] == kt) return true;
+    return false;
+  };
+  for (int kt = threadIdx.x; kt < n_kt; kt += blockDim.x) {
+    int c = 0;
+    for (int i = 0; i < n_qt; ++i) c += holds(i, kt) ? 1 : 0;
+    start[kt] = c;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int acc = 0;
+    for (int kt = 0; kt < n_kt; ++kt) {
+      const int c = start[kt];
+      start[kt] = acc;
+      acc += c;
+    }
+    start[n_kt] = acc;
+  }
+  __syncthreads();
+  int* off = q_off + head * (n_kt + 1);
+  for (int kt = threadIdx.x; kt <= n_kt; kt += blockDim.x) off[kt] = start[kt];
+  int* out = q_list + head * n_qt * topk;
+  for (int kt = threadIdx.x; kt < n_kt; kt += blockDim.x) {
+    int pos = start[kt];
+    for (int i = 0; i < n_qt; ++i)
+      if (holds(i, kt)) out[pos++] = i;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_tile_transpose(const int* kv_list, int B, int H, int n_qt, int n_kt, int topk,
+                                  int* q_off, int* q_list, cudaStream_t stream) {
+  const size_t smem = static_cast<size_t>(n_kt + 1) * sizeof(int);
+  if (smem > 48 * 1024) return cudaErrorInvalidValue;
+  tile_transpose_kernel<<<dim3(H, B), 256, smem, stream>>>(kv_list, H, n_qt, n_kt, topk, q_off,
+                                                           q_list);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_bwd_prep(const AttnShape& s, const void* o, const void* dout, float* delta,
                             cudaStream_t stream) {
@@ -451,8 +514,8 @@ cudaError_t launch_bwd_prep(const AttnShape& s, const void* o, const void* dout,
 
 cudaError_t launch_attn_bwd(const AttnShape& s, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, const CUtensorMap& tdo, const float* stats,
-                            const float* delta, void* dk, void* dv, int* err,
-                            cudaStream_t stream) {
+                            const float* delta, void* dk, void* dv, const int* q_off,
+                            const int* q_list, int q_stride, int* err, cudaStream_t stream) {
   const dim3 grid((s.Nkv + kTile - 1) / kTile, s.H, s.B);
   auto* dkp = static_cast<__nv_bfloat16*>(dk);
   auto* dvp = static_cast<__nv_bfloat16*>(dv);
@@ -462,14 +525,16 @@ cudaError_t launch_attn_bwd(const AttnShape& s, const CUtensorMap& tq, const CUt
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
     if (e != cudaSuccess) return e;
     attn_bwd_kernel<128><<<grid, kThreads, L::kAlloc, stream>>>(
-        tq, tk, tv, tdo, stats, delta, dkp, dvp, s.Nq, s.Nkv, s.H, s.scale, s.causal, err);
+        tq, tk, tv, tdo, stats, delta, dkp, dvp, s.Nq, s.Nkv, s.H, s.scale, s.causal, q_off, q_list,
+        q_stride, err);
   } else {
     using L = BwdLayout<64>;
     cudaError_t e = cudaFuncSetAttribute(attn_bwd_kernel<64>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
     if (e != cudaSuccess) return e;
     attn_bwd_kernel<64><<<grid, kThreads, L::kAlloc, stream>>>(
-        tq, tk, tv, tdo, stats, delta, dkp, dvp, s.Nq, s.Nkv, s.H, s.scale, s.causal, err);
+        tq, tk, tv, tdo, stats, delta, dkp, dvp, s.Nq, s.Nkv, s.H, s.scale, s.causal, q_off, q_list,
+        q_stride, err);
   }
   return cudaGetLastError();
 }

@@ -70,7 +70,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                        const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
                        const float* __restrict__ stats, const float* __restrict__ delta,
                        __nv_bfloat16* __restrict__ dq, int Nq, int Nkv, int H, float scale,
-                       int causal, int* __restrict__ err) {
+                       int causal, const int* __restrict__ kv_list, int topk,
+                       int* __restrict__ err) {
   using L = DqLayout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023u) &
@@ -95,7 +96,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kAbort);
 
   const int n_all = (Nkv + kStep - 1) / kStep;
-  const int n = causal ? min(n_all, q0 / kStep + 1) : n_all;  // causal: Nq == Nkv, kStep == kTile
+  // steps: every key tile (dense; causal: Nq == Nkv, kStep == kTile) or the topk
+  // key tiles listed for this query tile (block-sparse)
+  const int n = kv_list != nullptr ? topk : causal ? min(n_all, q0 / kStep + 1) : n_all;
+  const int* list = kv_list == nullptr ? nullptr
+      : kv_list + ((static_cast<int64_t>(b) * H + h) * ((Nq + kTile - 1) / kTile) + qt) * topk;
+  auto key_tile = [&](int j) -> int { return list != nullptr ? list[j] : j; };
 
   if (threadIdx.x == 0) {
     *abort = 0;
@@ -152,14 +158,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int blk = 0; blk < D / 64; ++blk)
         tma_load_4d_w(smem + L::kK + ks * L::kTileBytes + blk * L::kBlock, &tk, blk * 64,
-                      j * kStep, h, b, &k_full[ks]);
+                      key_tile(j) * kStep, h, b, &k_full[ks]);
       last_k[ks] = static_cast<int>(ku & 1u);
       if (!(ok = mbar_wait_warp(&v_empty[vs], (vu & 1u) ^ 1u, abort))) break;
       mbar_arrive_expect_tx_w(&v_full[vs], L::kTileBytes);
 #pragma unroll
       for (int blk = 0; blk < D / 64; ++blk)
         tma_load_4d_w(smem + L::kV + vs * L::kTileBytes + blk * L::kBlock, &tv, blk * 64,
-                      j * kStep, h, b, &v_full[vs]);
+                      key_tile(j) * kStep, h, b, &v_full[vs]);
       last_v[vs] = static_cast<int>(vu & 1u);
     }
     if (!ok) {  // let the loads already issued land before the block exits
@@ -242,8 +248,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t rs[32], rd[32];
     for (int j = 0; j < n && ok; ++j) {
       const int bsel = j & 1;
-      const int key0 = j * kStep + static_cast<int>(kc);
-      const bool edge = !row_ok || (j * kStep + kStep > Nkv) || (causal && j * kStep + kStep - 1 > q0);
+      const int kt = key_tile(j);
+      const int key0 = kt * kStep + static_cast<int>(kc);
+      const bool edge = !row_ok || kt < 0 || (kt * kStep + kStep > Nkv) ||
+                        (causal && kt * kStep + kStep - 1 > q0);
       if (!(ok = mbar_wait_warp(sdp_full, static_cast<uint32_t>(j & 1), abort))) break;
       tc_fence_after();
       tmem_ld32(tmem + lane_base + kColS + kc, rs);
@@ -259,8 +267,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         up2(fma2(pk2(__uint_as_float(rs[2 * i]), __uint_as_float(rs[2 * i + 1])), c12, nmb2), x0, x1);
         if (edge) {
           const int k0 = key0 + 2 * i;
-          if (!(row_ok && k0 < Nkv && (!causal || k0 <= qrow))) x0 = -INFINITY;
-          if (!(row_ok && k0 + 1 < Nkv && (!causal || k0 + 1 <= qrow))) x1 = -INFINITY;
+          if (!(row_ok && k0 >= 0 && k0 < Nkv && (!causal || k0 <= qrow))) x0 = -INFINITY;
+          if (!(row_ok && k0 + 1 >= 0 && k0 + 1 < Nkv && (!causal || k0 + 1 <= qrow))) x1 = -INFINITY;
         }
         const uint64_t a2 = mul2(pk2(ex2_f32(x0), ex2_f32(x1)), sl2);
         float d0, d1;
@@ -313,7 +321,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 cudaError_t launch_attn_bwd_dq(const AttnShape& s, const CUtensorMap& tq, const CUtensorMap& tdo,
                                const CUtensorMap& tk, const CUtensorMap& tv, const float* stats,
-                               const float* delta, void* dq, int* err, cudaStream_t stream) {
+                               const float* delta, void* dq, const int* kv_list, int topk,
+                               int* err, cudaStream_t stream) {
   const dim3 grid((s.Nq + kTile - 1) / kTile, s.H, s.B);
   auto* dqp = static_cast<__nv_bfloat16*>(dq);
   if (s.D == 128) {
@@ -322,14 +331,14 @@ cudaError_t launch_attn_bwd_dq(const AttnShape& s, const CUtensorMap& tq, const 
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
     if (e != cudaSuccess) return e;
     attn_bwd_dq_kernel<128><<<grid, kThreads, L::kAlloc, stream>>>(
-        tq, tdo, tk, tv, stats, delta, dqp, s.Nq, s.Nkv, s.H, s.scale, s.causal, err);
+        tq, tdo, tk, tv, stats, delta, dqp, s.Nq, s.Nkv, s.H, s.scale, s.causal, kv_list, topk, err);
   } else {
     using L = DqLayout<64>;
     cudaError_t e = cudaFuncSetAttribute(attn_bwd_dq_kernel<64>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
     if (e != cudaSuccess) return e;
     attn_bwd_dq_kernel<64><<<grid, kThreads, L::kAlloc, stream>>>(
-        tq, tdo, tk, tv, stats, delta, dqp, s.Nq, s.Nkv, s.H, s.scale, s.causal, err);
+        tq, tdo, tk, tv, stats, delta, dqp, s.Nq, s.Nkv, s.H, s.scale, s.causal, kv_list, topk, err);
   }
   return cudaGetLastError();
 }

@@ -75,7 +75,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tv, __nv_bfloat16* __restrict__ o,
                     float* __restrict__ stats, int Nq, int Nkv, int H, float scale, int causal,
-                    int* __restrict__ err) {
+                    const int* __restrict__ kv_list, int topk, int* __restrict__ err) {
   using L = FwdLayout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023u) &
@@ -99,8 +99,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int n_kv_all = (Nkv + kTile - 1) / kTile;
   // causal: the second query tile sees one more key tile than the first; both
-  // run over it (the first tile's part of it is fully masked)
-  const int n_kv = causal ? min(n_kv_all, 2 * static_cast<int>(blockIdx.x) + 2) : n_kv_all;
+  // run over it (the first tile's part of it is fully masked); block-sparse:
+  // topk listed key tiles per query tile
+  const int n_kv = kv_list != nullptr ? topk
+                 : causal ? min(n_kv_all, 2 * static_cast<int>(blockIdx.x) + 2) : n_kv_all;
 
   if (threadIdx.x == 0) {
     *abort = 0;
@@ -127,9 +129,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  // Block-sparse: query tile i attends to the key tiles list_i[0..topk); a K or V
+  // step then loads one tile per query tile.  Dense: key tile j at step j, one
+  // load shared by both query tiles.
+  const bool sparse = kv_list != nullptr;
+  const int nt = sparse ? 2 : 1;  // loads per K or V step
+  const int n_qt = (Nq + kTile - 1) / kTile;
+  const int* list0 = nullptr;
+  const int* list1 = nullptr;
+  if (sparse) {
+    const int qt0 = 2 * static_cast<int>(blockIdx.x);
+    const int64_t base = (static_cast<int64_t>(b) * H + h) * n_qt;
+    list0 = kv_list + (base + qt0) * topk;
+    list1 = kv_list + (base + min(qt0 + 1, n_qt - 1)) * topk;  // a missing tile's rows are masked
+  }
+  auto key_tile = [&](int i, int j) -> int { return sparse ? (i ? list1[j] : list0[j]) : j; };
+
   if (warp == kTmaWarp) {
     // ------------------------------------------------------------ producer
-    // Load order: Q0, Q1; pass 1: K_0..K_{n-1}; pass 2: K_0, V_0, K_1, V_1, ...
+    // Load order: Q0, Q1; pass 1: K(j) for every step j; pass 2: K(0), then V(j),
+    // K(j+1) for every step j; K(j), V(j) are one load (dense) or one per query
+    // tile (sparse), in tile order.
     tma_prefetch_desc(&tq);
     tma_prefetch_desc(&tk);
     tma_prefetch_desc(&tv);
@@ -140,21 +160,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int blk = 0; blk < D / 64; ++blk)
         tma_load_4d_w(smem + L::kQ + i * L::kTileBytes + blk * kAtomBlock, &tq, blk * 64,
                       q0 + i * kTile, h, b, q_full);
-    int last[kRing] = {-1, -1, -1};
+    int last[kRing];
+    for (int s = 0; s < kRing; ++s) last[s] = -1;
     bool ok = true;
-    const int total = 3 * n_kv;
-    for (int li = 0; li < total && ok; ++li) {
+    int li = 0;
+    auto load = [&](const CUtensorMap* map, int tile) -> bool {
       const int slot = li % kRing;
       const uint32_t use = static_cast<uint32_t>(li / kRing);
-      if (!(ok = mbar_wait_warp(&r_empty[slot], (use & 1u) ^ 1u, abort))) break;
-      const bool is_v = li >= n_kv && ((li - n_kv) & 1);
-      const int j = li < n_kv ? li : (li - n_kv) >> 1;
+      if (!mbar_wait_warp(&r_empty[slot], (use & 1u) ^ 1u, abort)) return false;
       mbar_arrive_expect_tx_w(&r_full[slot], L::kTileBytes);
 #pragma unroll
       for (int blk = 0; blk < D / 64; ++blk)
-        tma_load_4d_w(smem + L::kRingOff + slot * L::kTileBytes + blk * kAtomBlock,
-                      is_v ? &tv : &tk, blk * 64, j * kTile, h, b, &r_full[slot]);
+        tma_load_4d_w(smem + L::kRingOff + slot * L::kTileBytes + blk * kAtomBlock, map, blk * 64,
+                      tile * kTile, h, b, &r_full[slot]);
       last[slot] = static_cast<int>(use & 1u);
+      ++li;
+      return true;
+    };
+    for (int j = 0; j < n_kv && ok; ++j)
+      for (int i = 0; i < nt && ok; ++i) ok = load(&tk, key_tile(i, j));
+    for (int i = 0; i < nt && ok; ++i) ok = load(&tk, key_tile(i, 0));
+    for (int j = 0; j < n_kv && ok; ++j) {
+      for (int i = 0; i < nt && ok; ++i) ok = load(&tv, key_tile(i, j));
+      if (j + 1 < n_kv)
+        for (int i = 0; i < nt && ok; ++i) ok = load(&tk, key_tile(i, j + 1));
     }
     if (!ok) {
       mbar_wait_warp(q_full, 0, nullptr, 10000000ull);
@@ -191,43 +220,49 @@ __global__ void __launch_bounds__(kThreads, 1)
                       sdesc_sw128(vb + kk * 2048, kAtomBlock, 1024), idesc_pv,
                       (acc || kk > 0) ? 1u : 0u);
     };
+    // Load idx of query tile i within a step whose loads start at `base`; a dense
+    // load serves both tiles and is released after tile 1's UMMAs.
+    auto tile_load = [&](int base, int i) { return base + (sparse ? i : 0); };
+    auto release = [&](int base, int i) {
+      if (sparse || i == 1) umma_commit_w(&r_empty[tile_load(base, i) % kRing]);
+    };
     bool ok = mbar_wait_warp(q_full, 0, abort);
     // pass 1: S_0(j), S_1(j) for the row maxima
-    for (int j = 0; j < n_kv && ok; ++j, ++li) {
-      if (!(ok = wait_slot(li))) break;
+    for (int j = 0; j < n_kv && ok; ++j, li += nt) {
       for (int i = 0; i < 2 && ok; ++i) {
+        if ((sparse || i == 0) && !(ok = wait_slot(tile_load(li, i)))) break;
         if (j > 0 && !(ok = mbar_wait_warp(&s_free[i], static_cast<uint32_t>((j - 1) & 1), abort))) break;
         tc_fence_after();
-        issue_s(i, li);
+        issue_s(i, tile_load(li, i));
+        release(li, i);
       }
-      umma_commit_w(&r_empty[li % kRing]);
     }
     // pass 2 prologue: S_0(0), S_1(0)
-    if (ok && (ok = wait_slot(li))) {
-      for (int i = 0; i < 2 && ok; ++i) {
-        if (!(ok = mbar_wait_warp(&s_free[i], static_cast<uint32_t>((n_kv - 1) & 1), abort))) break;
-        tc_fence_after();
-        issue_s(i, li);
-      }
-      umma_commit_w(&r_empty[li % kRing]);
-      ++li;
+    for (int i = 0; i < 2 && ok; ++i) {
+      if ((sparse || i == 0) && !(ok = wait_slot(tile_load(li, i)))) break;
+      if (!(ok = mbar_wait_warp(&s_free[i], static_cast<uint32_t>((n_kv - 1) & 1), abort))) break;
+      tc_fence_after();
+      issue_s(i, tile_load(li, i));
+      release(li, i);
     }
+    li += nt;
     for (int j = 0; j < n_kv && ok; ++j) {
-      const int vi = li++;  // V_j
-      const int ki = (j + 1 < n_kv) ? li : -1;  // K_{j+1}
-      if (ki >= 0) ++li;
-      if (!(ok = wait_slot(vi))) break;
+      const int vbase = li;  // V(j)
+      li += nt;
+      const int kbase = (j + 1 < n_kv) ? li : -1;  // K(j+1)
+      if (kbase >= 0) li += nt;
       for (int i = 0; i < 2 && ok; ++i) {
+        if ((sparse || i == 0) && !(ok = wait_slot(tile_load(vbase, i)))) break;
         if (!(ok = mbar_wait_warp(&p_full[i], static_cast<uint32_t>(j & 1), abort))) break;
         tc_fence_after();
-        issue_pv(i, vi, j > 0);
-        if (i == 1) umma_commit_w(&r_empty[vi % kRing]);
-        if (ki >= 0) {
-          if (!(ok = wait_slot(ki))) break;
+        issue_pv(i, tile_load(vbase, i), j > 0);
+        release(vbase, i);
+        if (kbase >= 0) {
+          if ((sparse || i == 0) && !(ok = wait_slot(tile_load(kbase, i)))) break;
           // S_i(j+1): S_i was read before p_full_i(j), and the UMMAs run in
           // issue order, so PV_i(j) reads P~_i before S_i(j+1) overwrites it
-          issue_s(i, ki);
-          if (i == 1) umma_commit_w(&r_empty[ki % kRing]);
+          issue_s(i, tile_load(kbase, i));
+          release(kbase, i);
         }
       }
     }
@@ -260,7 +295,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int j = 0; j < n_kv && ok; ++j) {
       if (!(ok = mbar_wait_warp(&s_full[ti], static_cast<uint32_t>(j & 1), abort))) break;
       tc_fence_after();
-      const bool edge = (j * kTile + kTile > Nkv) || (causal && j * kTile + kTile - 1 > tile_q0);
+      const int kt = key_tile(ti, j);
+      const bool edge = kt < 0 || (kt * kTile + kTile > Nkv) || (causal && kt * kTile + kTile - 1 > tile_q0);
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         tmem_ld32(tmem + lane_base + s_col + c * 32, r);
@@ -271,8 +307,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            const int key = j * kTile + hf * 64 + c * 32 + i;
-            if (key < Nkv && (!causal || key <= qrow)) mraw = fmaxf(mraw, __uint_as_float(r[i]));
+            const int key = kt * kTile + hf * 64 + c * 32 + i;
+            if (key >= 0 && key < Nkv && (!causal || key <= qrow)) mraw = fmaxf(mraw, __uint_as_float(r[i]));
           }
         }
       }
@@ -293,7 +329,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!(ok = mbar_wait_warp(&s_full[ti], static_cast<uint32_t>((n_kv + j) & 1), abort))) break;
       tc_fence_after();
       // S_i(j) complete implies PV_i(j-1) complete (issued earlier): P~_i(j-1) is consumed
-      const bool edge = (j * kTile + kTile > Nkv) || (causal && j * kTile + kTile - 1 > tile_q0);
+      const int kt = key_tile(ti, j);
+      const bool edge = kt < 0 || (kt * kTile + kTile > Nkv) || (causal && kt * kTile + kTile - 1 > tile_q0);
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         tmem_ld32(tmem + lane_base + s_col + c * 32, r);
@@ -306,8 +343,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (edge) {
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            const int key = j * kTile + hf * 64 + c * 32 + i;
-            if (!(key < Nkv && (!causal || key <= qrow))) x[i] = -INFINITY;
+            const int key = kt * kTile + hf * 64 + c * 32 + i;
+            if (!(key >= 0 && key < Nkv && (!causal || key <= qrow))) x[i] = -INFINITY;
           }
         }
         uint32_t pt[16];  // P~ of these 32 keys as f16 pairs
@@ -378,8 +415,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 cudaError_t launch_attn_fwd(const AttnShape& s, const CUtensorMap& tq, const CUtensorMap& tk,
-                            const CUtensorMap& tv, void* o, float* stats, int* err,
-                            cudaStream_t stream) {
+                            const CUtensorMap& tv, void* o, float* stats, const int* kv_list,
+                            int topk, int* err, cudaStream_t stream) {
   const dim3 grid((s.Nq + 2 * kTile - 1) / (2 * kTile), s.H, s.B);
   auto* op = static_cast<__nv_bfloat16*>(o);
   if (s.D == 128) {
@@ -387,15 +424,15 @@ cudaError_t launch_attn_fwd(const AttnShape& s, const CUtensorMap& tq, const CUt
     cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<128>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
     if (e != cudaSuccess) return e;
-    attn_fwd_kernel<128><<<grid, kThreads, L::kAlloc, stream>>>(tq, tk, tv, op, stats, s.Nq, s.Nkv,
-                                                                 s.H, s.scale, s.causal, err);
+    attn_fwd_kernel<128><<<grid, kThreads, L::kAlloc, stream>>>(
+        tq, tk, tv, op, stats, s.Nq, s.Nkv, s.H, s.scale, s.causal, kv_list, topk, err);
   } else {
     using L = FwdLayout<64>;
     cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<64>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
     if (e != cudaSuccess) return e;
-    attn_fwd_kernel<64><<<grid, kThreads, L::kAlloc, stream>>>(tq, tk, tv, op, stats, s.Nq, s.Nkv,
-                                                                s.H, s.scale, s.causal, err);
+    attn_fwd_kernel<64><<<grid, kThreads, L::kAlloc, stream>>>(
+        tq, tk, tv, op, stats, s.Nq, s.Nkv, s.H, s.scale, s.causal, kv_list, topk, err);
   }
   return cudaGetLastError();
 }

@@ -62,20 +62,34 @@ cudaError_t timed(int kind, cudaStream_t stream, F&& launch) {
 int make_bnhd_map(CUtensorMap* map, const void* base, int B, int N, int H, int D, bool f16,
                    int box_rows = kTile);
 
+// kv_list: NULL (dense) or int32 [B, H, ceil(Nq/128), topk] key tiles per query tile
 cudaError_t launch_attn_fwd(const AttnShape& s, const CUtensorMap& tq, const CUtensorMap& tk,
-                            const CUtensorMap& tv, void* o, float* stats, int* err,
-                            cudaStream_t stream);
+                            const CUtensorMap& tv, void* o, float* stats, const int* kv_list,
+                            int topk, int* err, cudaStream_t stream);
 cudaError_t launch_bwd_prep(const AttnShape& s, const void* o, const void* dout, float* delta,
                             cudaStream_t stream);
-// dK, dV (key-outer; Q~, K~, V~, dO maps with 128-row boxes)
+// dK, dV (key-outer; Q~, K~, V~, dO maps with 128-row boxes).  Block-sparse:
+// q_off/q_list from launch_tile_transpose (q_stride = n_qt * topk), else NULL.
 cudaError_t launch_attn_bwd(const AttnShape& s, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, const CUtensorMap& tdo, const float* stats,
-                            const float* delta, void* dk, void* dv, int* err,
-                            cudaStream_t stream);
+                            const float* delta, void* dk, void* dv, const int* q_off,
+                            const int* q_list, int q_stride, int* err, cudaStream_t stream);
+// Block-sparse lists [B, H, n_qt, topk] transposed to, per (b, h), offsets
+// q_off [n_kt + 1] and ascending query tiles q_list [n_qt * topk].
+cudaError_t launch_tile_transpose(const int* kv_list, int B, int H, int n_qt, int n_kt, int topk,
+                                  int* q_off, int* q_list, cudaStream_t stream);
 // dQ (query-outer; Q~, dO, K~, V~ maps with 128-row boxes)
 cudaError_t launch_attn_bwd_dq(const AttnShape& s, const CUtensorMap& tq, const CUtensorMap& tdo,
                                const CUtensorMap& tk, const CUtensorMap& tv, const float* stats,
-                               const float* delta, void* dq, int* err, cudaStream_t stream);
+                               const float* delta, void* dq, const int* kv_list, int topk,
+                               int* err, cudaStream_t stream);
+
+// Token rows [B, T*Hh*W, H, D] (bf16) between raster and cube order.
+cudaError_t launch_vsa_reorder(const void* x, int B, int T, int Hh, int W, int H, int D, int ct,
+                               int ch, int cw, int to_cubes, void* out, cudaStream_t stream);
+// Top-k key tiles per query tile by cube-mean scores; qm, km: f32 [B, H, N/128, D] scratch.
+cudaError_t launch_vsa_select(const void* q, const void* k, int B, int N, int H, int D, int topk,
+                              int* kv_tiles, float* qm, float* km, cudaStream_t stream);
 
 cudaError_t launch_selftest_umma(const CUtensorMap& ta, const CUtensorMap& tb, const void* a,
                                  float* c, int N, int K, int a_mn, int b_mn, int* err,

@@ -128,11 +128,46 @@ def test_quantizer_rejects_bad_arguments(lib):
     assert lib.nvq_selftest_umma(A, A, A, 64, 64, 3, 0, None) == INVALID
 
 
+def test_block_sparse_and_vsa_calls_reject_bad_arguments(lib):
+    n, h, d = 25088, 12, 128
+    assert lib.vsa_select_workspace(1, n, h, d) == 2 * 12 * 196 * 128 * 4
+    assert lib.vsa_select_workspace(1, n - 8, h, d) == 0
+    dense = lib.attn_qat_bwd_workspace(1, n, n, h, d)
+    offsets = (12 * 197 * 4 + 255) // 256 * 256  # [B, H, n_tiles + 1] int32, 256-byte aligned
+    assert lib.attn_qat_bwd_sparse_workspace(1, n, h, d, 20) == dense + offsets + 12 * 196 * 20 * 4
+    big = 1 << 40
+
+    def reorder(x=A, out=A + 4096, t=8, hh=8, w=16, ct=4, ch=4, cw=8, to_cubes=1):
+        return lib.vsa_reorder(x, 1, t, hh, w, 2, 64, ct, ch, cw, to_cubes, out, None)
+    assert reorder(out=A) == INVALID         # in place
+    assert reorder(x=None) == INVALID
+    assert reorder(t=6) == INVALID           # not a whole number of cubes
+    assert reorder(to_cubes=2) == INVALID
+
+    def select(nn=384, topk=2, ws=A, ws_bytes=big, dd=64):
+        return lib.vsa_select_tiles(A, A, 1, nn, 2, dd, topk, A, ws, ws_bytes, None)
+    assert select(topk=0) == INVALID
+    assert select(topk=4) == INVALID         # more than N / 128
+    assert select(nn=390) == INVALID         # N % 128
+    assert select(dd=2048) == INVALID
+    assert select(ws_bytes=16) == WORKSPACE
+
+    def fwd(nn=384, topk=2, kv=A, dd=128):
+        return lib.attn_qat_fwd_sparse(A, A, A, 1, nn, 2, dd, 0.1, kv, topk, A, A, A, big, None)
+    assert fwd(nn=300) == INVALID
+    assert fwd(topk=4) == INVALID
+    assert fwd(kv=None) == INVALID
+    assert fwd(kv=A + 2) == INVALID
+    assert fwd(dd=96) == UNSUPPORTED
+    assert lib.attn_qat_bwd_sparse(A, A, A, A, A, A, A, 0, A, A, A, 1, 384, 2, 128, 0.1, A, big,
+                                   None) == INVALID  # topk 0
+
+
 def test_timing_hook_arguments(lib):
     n, ms = ctypes.c_int64(-1), ctypes.c_double(-1.0)
     pn, pms = ctypes.addressof(n), ctypes.addressof(ms)
     assert lib.nvq_timing_enable(2) == INVALID
-    assert lib.nvq_timing_read(6, pn, pms) == INVALID
+    assert lib.nvq_timing_read(7, pn, pms) == INVALID
     assert lib.nvq_timing_read(-1, pn, pms) == INVALID
     assert lib.nvq_timing_read(0, None, pms) == INVALID
     assert lib.nvq_timing_enable(1) == OK
