@@ -316,6 +316,58 @@ def quantizer_bench(peaks, stream, iters=20):
     return res
 
 
+def sparse_bench(peaks, stream, steps, warmup):
+    """The block-sparse workload (Wan latent 16x28x56, B=1, H=12, D=128, 196 cubes
+    of 4x4x8 tokens, top-20 key cubes per query cube): one step = raster -> cube
+    order of q, k, v, dO, block selection, sparse forward and backward, cube ->
+    raster order of o, dq, dk, dv.  Counted FLOPs: forward 4*H*N*(20*128)*D,
+    backward 2.5x that."""
+    import torch
+
+    from nvfp4_fake_quant_gb300 import api, workloads
+    inp = workloads.vsa25088()
+    grid = workloads.VSA_GRID
+    b, n, _, h, d = inp.shape
+    topk = api.vsa_effective_topk(0.9, n // api.VSA_TILE)
+    q, k, v, do = (t.cuda() for t in (inp.q, inp.k, inp.v, inp.do))
+    qc, kc, vc, doc = (torch.empty_like(q) for _ in range(4))
+    o_c, dq_c, dk_c, dv_c = (torch.empty_like(q) for _ in range(4))
+    o, dq, dk, dv = (torch.empty_like(q) for _ in range(4))
+    stats = torch.empty((b, h, 2, n), dtype=torch.float32, device=q.device)
+    wsf = torch.empty(api.attn_qat_fwd_workspace(b, n, n, h, d), dtype=torch.uint8, device=q.device)
+    wsb = torch.empty(api.attn_qat_bwd_sparse_workspace(b, n, h, d, topk), dtype=torch.uint8,
+                      device=q.device)
+
+    def step():
+        for src, dst in ((q, qc), (k, kc), (v, vc), (do, doc)):
+            api.vsa_reorder(src, grid, out=dst)
+        tiles = api.vsa_select_tiles(qc, kc, topk)
+        api.attn_qat_fwd_sparse(qc, kc, vc, tiles, inp.scale, o=o_c, stats=stats, workspace=wsf)
+        api.attn_qat_bwd_sparse(qc, kc, vc, o_c, stats, doc, tiles, inp.scale, dq=dq_c, dk=dk_c,
+                                dv=dv_c, workspace=wsb)
+        for src, dst in ((o_c, o), (dq_c, dq), (dk_c, dk), (dv_c, dv)):
+            api.vsa_reorder(src, grid, to_cubes=False, out=dst)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    api.timing_enable(True)
+    ms = time_events(step, steps, stream)
+    kt = api.timing_read()
+    api.timing_enable(False)
+    if api.device_status() != 0:
+        raise RuntimeError("a bounded device wait timed out (block-sparse)")
+    f_fwd = 4.0 * b * h * n * (topk * api.VSA_TILE) * d
+    total = sum(t for _, t in kt.values())
+    return {"workload": "Wan latent 16x28x56 (N=25088), B=1, H=12, D=128, q,k,v,dO N(0,1) "
+                        "(seed 4); 196 cubes of 4x4x8, top-20 key cubes per query cube",
+            "ms_per_step": ms, "TFLOP/s": 3.5 * f_fwd / (ms * 1e-3) / 1e12,
+            "flops_counting": "fwd 4*B*H*N*(topk*128)*D + bwd 2.5x fwd",
+            "pct_of_bf16_peak": 3.5 * f_fwd / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
+            "kernels": {name: {"launches": c, "avg_ms": t / c, "share": t / total}
+                        for name, (c, t) in kt.items() if c}}
+
+
 def run_ours(args):
     import torch
 
@@ -406,6 +458,8 @@ def run_ours(args):
     d2h = sum(t.numel() * t.element_size() for t in (hdq, hdk, hdv))
 
     quant = quantizer_bench(peaks, stream) if rank == 0 and not args.skip_quantizer else None
+    sparse = (sparse_bench(peaks, stream, max(3, args.steps), args.warmup)
+              if rank == 0 and not args.skip_sparse and (n, h) == (25088, 12) else None)
 
     peak_t = peaks["bf16_tflops"]
     k_total = sum(ms for _, ms in ktimes.values())
@@ -446,6 +500,8 @@ def run_ours(args):
     }
     if quant is not None:
         line["quantizer"] = quant
+    if sparse is not None:
+        line["block_sparse"] = sparse
     if rank == 0 and not args.skip_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_rows)
     if rank == 0:
@@ -466,6 +522,8 @@ def main(argv=None):
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     ap.add_argument("--skip-quantizer", action="store_true")
     ap.add_argument("--skip-e2e", action="store_true")
+    ap.add_argument("--skip-sparse", action="store_true",
+                    help="skip the block-sparse (VSA) workload's extra measurement")
     ap.add_argument("--quantizer-only", action="store_true",
                     help="time only the standalone quantizer (profiling of that kernel)")
     ap.add_argument("--n", type=int, default=None,

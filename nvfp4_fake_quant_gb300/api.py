@@ -223,7 +223,7 @@ def vsa_select_tiles(q, k, topk, workspace=None):
     _check_bnhd(k, "k", q.shape)
     b, n, h, d = q.shape
     out = torch.empty((b, h, n // VSA_TILE, topk), dtype=torch.int32, device=q.device)
-    need = int(_lib.load().vsa_select_workspace(b, n, h, d))
+    need = vsa_select_workspace(b, n, h, d)
     ws = _workspace(need, q.device, workspace)
     _lib.call("vsa_select_tiles", _ptr(q), _ptr(k), b, n, h, d, int(topk), _ptr(out), _ptr(ws),
               ws.numel() * ws.element_size(), _stream_ptr(q))
@@ -249,6 +249,14 @@ def attn_qat_fwd_sparse(q, k, v, kv_tiles, scale=None, o=None, stats=None, works
     return o, stats
 
 
+def attn_qat_bwd_sparse_workspace(b, n, h, d, topk) -> int:
+    return int(_lib.load().attn_qat_bwd_sparse_workspace(b, n, h, d, topk))
+
+
+def vsa_select_workspace(b, n, h, d) -> int:
+    return int(_lib.load().vsa_select_workspace(b, n, h, d))
+
+
 def attn_qat_bwd_sparse(q, k, v, o, stats, do, kv_tiles, scale=None, dq=None, dk=None, dv=None,
                         workspace=None):
     """Block-sparse straight-through backward: (dq, dk, dv)."""
@@ -263,7 +271,7 @@ def attn_qat_bwd_sparse(q, k, v, o, stats, do, kv_tiles, scale=None, dq=None, dk
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    need = int(_lib.load().attn_qat_bwd_sparse_workspace(b, n, h, d, topk))
+    need = attn_qat_bwd_sparse_workspace(b, n, h, d, topk)
     ws = _workspace(need, q.device, workspace)
     _lib.call("attn_qat_bwd_sparse", _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(stats), _ptr(do),
               _ptr(kv_tiles), topk, _ptr(dq), _ptr(dk), _ptr(dv), b, n, h, d, scale, _ptr(ws),

@@ -72,7 +72,7 @@ struct BwdLayout {
       (kUsed + 1024u) > 150u * 1024u ? (kUsed + 1024u) : 150u * 1024u;
 };
 
-template <int D>
+template <int D, bool kSparse>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
@@ -112,14 +112,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int i_begin = causal ? kt : 0;
   const int* qsel = nullptr;
   int n_iter = n_q_all - i_begin;
-  if (q_off != nullptr) {
+  if (kSparse) {
     const int n_kt = (Nkv + kTile - 1) / kTile;
     const int64_t head = static_cast<int64_t>(b) * H + h;
     const int* off = q_off + head * (n_kt + 1);
     qsel = q_list + head * q_stride + off[kt];
     n_iter = off[kt + 1] - off[kt];
   }
-  auto qtile = [&](int it) -> int { return qsel != nullptr ? qsel[it] : i_begin + it; };
+  auto qtile = [&](int it) -> int { return kSparse ? qsel[it] : i_begin + it; };
 
 
   if (threadIdx.x == 0) {
@@ -512,31 +512,37 @@ cudaError_t launch_bwd_prep(const AttnShape& s, const void* o, const void* dout,
   return cudaGetLastError();
 }
 
+template <int D, bool kSparse>
+cudaError_t launch_bwd_t(const AttnShape& s, const CUtensorMap& tq, const CUtensorMap& tk,
+                         const CUtensorMap& tv, const CUtensorMap& tdo, const float* stats,
+                         const float* delta, void* dk, void* dv, const int* q_off,
+                         const int* q_list, int q_stride, int* err, cudaStream_t stream) {
+  using L = BwdLayout<D>;
+  const dim3 grid((s.Nkv + kTile - 1) / kTile, s.H, s.B);
+  cudaError_t e = cudaFuncSetAttribute(attn_bwd_kernel<D, kSparse>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+  if (e != cudaSuccess) return e;
+  attn_bwd_kernel<D, kSparse><<<grid, kThreads, L::kAlloc, stream>>>(
+      tq, tk, tv, tdo, stats, delta, static_cast<__nv_bfloat16*>(dk),
+      static_cast<__nv_bfloat16*>(dv), s.Nq, s.Nkv, s.H, s.scale, s.causal, q_off, q_list,
+      q_stride, err);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_attn_bwd(const AttnShape& s, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, const CUtensorMap& tdo, const float* stats,
                             const float* delta, void* dk, void* dv, const int* q_off,
                             const int* q_list, int q_stride, int* err, cudaStream_t stream) {
-  const dim3 grid((s.Nkv + kTile - 1) / kTile, s.H, s.B);
-  auto* dkp = static_cast<__nv_bfloat16*>(dk);
-  auto* dvp = static_cast<__nv_bfloat16*>(dv);
-  if (s.D == 128) {
-    using L = BwdLayout<128>;
-    cudaError_t e = cudaFuncSetAttribute(attn_bwd_kernel<128>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
-    if (e != cudaSuccess) return e;
-    attn_bwd_kernel<128><<<grid, kThreads, L::kAlloc, stream>>>(
-        tq, tk, tv, tdo, stats, delta, dkp, dvp, s.Nq, s.Nkv, s.H, s.scale, s.causal, q_off, q_list,
-        q_stride, err);
-  } else {
-    using L = BwdLayout<64>;
-    cudaError_t e = cudaFuncSetAttribute(attn_bwd_kernel<64>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
-    if (e != cudaSuccess) return e;
-    attn_bwd_kernel<64><<<grid, kThreads, L::kAlloc, stream>>>(
-        tq, tk, tv, tdo, stats, delta, dkp, dvp, s.Nq, s.Nkv, s.H, s.scale, s.causal, q_off, q_list,
-        q_stride, err);
-  }
-  return cudaGetLastError();
+  const bool sp = q_off != nullptr;
+  if (s.D == 128)
+    return sp ? launch_bwd_t<128, true>(s, tq, tk, tv, tdo, stats, delta, dk, dv, q_off, q_list,
+                                        q_stride, err, stream)
+              : launch_bwd_t<128, false>(s, tq, tk, tv, tdo, stats, delta, dk, dv, q_off, q_list,
+                                         q_stride, err, stream);
+  return sp ? launch_bwd_t<64, true>(s, tq, tk, tv, tdo, stats, delta, dk, dv, q_off, q_list,
+                                     q_stride, err, stream)
+            : launch_bwd_t<64, false>(s, tq, tk, tv, tdo, stats, delta, dk, dv, q_off, q_list,
+                                      q_stride, err, stream);
 }
 
 }  // namespace nvq

@@ -64,7 +64,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-template <int D>
+template <int D, bool kSparse>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tdo,
                        const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv,
@@ -98,10 +98,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_all = (Nkv + kStep - 1) / kStep;
   // steps: every key tile (dense; causal: Nq == Nkv, kStep == kTile) or the topk
   // key tiles listed for this query tile (block-sparse)
-  const int n = kv_list != nullptr ? topk : causal ? min(n_all, q0 / kStep + 1) : n_all;
-  const int* list = kv_list == nullptr ? nullptr
+  const int n = kSparse ? topk : causal ? min(n_all, q0 / kStep + 1) : n_all;
+  const int* list = !kSparse ? nullptr
       : kv_list + ((static_cast<int64_t>(b) * H + h) * ((Nq + kTile - 1) / kTile) + qt) * topk;
-  auto key_tile = [&](int j) -> int { return list != nullptr ? list[j] : j; };
+  auto key_tile = [&](int j) -> int { return kSparse ? list[j] : j; };
 
   if (threadIdx.x == 0) {
     *abort = 0;
@@ -319,28 +319,32 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
+template <int D, bool kSparse>
+cudaError_t launch_dq_t(const AttnShape& s, const CUtensorMap& tq, const CUtensorMap& tdo,
+                        const CUtensorMap& tk, const CUtensorMap& tv, const float* stats,
+                        const float* delta, void* dq, const int* kv_list, int topk, int* err,
+                        cudaStream_t stream) {
+  using L = DqLayout<D>;
+  const dim3 grid((s.Nq + kTile - 1) / kTile, s.H, s.B);
+  cudaError_t e = cudaFuncSetAttribute(attn_bwd_dq_kernel<D, kSparse>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+  if (e != cudaSuccess) return e;
+  attn_bwd_dq_kernel<D, kSparse><<<grid, kThreads, L::kAlloc, stream>>>(
+      tq, tdo, tk, tv, stats, delta, static_cast<__nv_bfloat16*>(dq), s.Nq, s.Nkv, s.H, s.scale,
+      s.causal, kv_list, topk, err);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_attn_bwd_dq(const AttnShape& s, const CUtensorMap& tq, const CUtensorMap& tdo,
                                const CUtensorMap& tk, const CUtensorMap& tv, const float* stats,
                                const float* delta, void* dq, const int* kv_list, int topk,
                                int* err, cudaStream_t stream) {
-  const dim3 grid((s.Nq + kTile - 1) / kTile, s.H, s.B);
-  auto* dqp = static_cast<__nv_bfloat16*>(dq);
-  if (s.D == 128) {
-    using L = DqLayout<128>;
-    cudaError_t e = cudaFuncSetAttribute(attn_bwd_dq_kernel<128>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
-    if (e != cudaSuccess) return e;
-    attn_bwd_dq_kernel<128><<<grid, kThreads, L::kAlloc, stream>>>(
-        tq, tdo, tk, tv, stats, delta, dqp, s.Nq, s.Nkv, s.H, s.scale, s.causal, kv_list, topk, err);
-  } else {
-    using L = DqLayout<64>;
-    cudaError_t e = cudaFuncSetAttribute(attn_bwd_dq_kernel<64>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
-    if (e != cudaSuccess) return e;
-    attn_bwd_dq_kernel<64><<<grid, kThreads, L::kAlloc, stream>>>(
-        tq, tdo, tk, tv, stats, delta, dqp, s.Nq, s.Nkv, s.H, s.scale, s.causal, kv_list, topk, err);
-  }
-  return cudaGetLastError();
+  const bool sp = kv_list != nullptr;
+  if (s.D == 128)
+    return sp ? launch_dq_t<128, true>(s, tq, tdo, tk, tv, stats, delta, dq, kv_list, topk, err, stream)
+              : launch_dq_t<128, false>(s, tq, tdo, tk, tv, stats, delta, dq, kv_list, topk, err, stream);
+  return sp ? launch_dq_t<64, true>(s, tq, tdo, tk, tv, stats, delta, dq, kv_list, topk, err, stream)
+            : launch_dq_t<64, false>(s, tq, tdo, tk, tv, stats, delta, dq, kv_list, topk, err, stream);
 }
 
 }  // namespace nvq

@@ -70,7 +70,7 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
 // warpgroups 2i and 2i+1 (warps 8i..8i+7) own tile i, 64 key columns each.  TMEM: S_i at [128 i, 128 i + 128),
 // O_i at [256 + 128 i, 256 + 128 i + D).  The UMMA warp ping-pongs the two
 // tiles so that one warpgroup's softmax overlaps the other's UMMAs.
-template <int D>
+template <int D, bool kSparse>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tv, __nv_bfloat16* __restrict__ o,
@@ -101,7 +101,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // causal: the second query tile sees one more key tile than the first; both
   // run over it (the first tile's part of it is fully masked); block-sparse:
   // topk listed key tiles per query tile
-  const int n_kv = kv_list != nullptr ? topk
+  const int n_kv = kSparse ? topk
                  : causal ? min(n_kv_all, 2 * static_cast<int>(blockIdx.x) + 2) : n_kv_all;
 
   if (threadIdx.x == 0) {
@@ -132,7 +132,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Block-sparse: query tile i attends to the key tiles list_i[0..topk); a K or V
   // step then loads one tile per query tile.  Dense: key tile j at step j, one
   // load shared by both query tiles.
-  const bool sparse = kv_list != nullptr;
+  constexpr bool sparse = kSparse;
   const int nt = sparse ? 2 : 1;  // loads per K or V step
   const int n_qt = (Nq + kTile - 1) / kTile;
   const int* list0 = nullptr;
@@ -414,27 +414,30 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
+template <int D, bool kSparse>
+cudaError_t launch_fwd_t(const AttnShape& s, const CUtensorMap& tq, const CUtensorMap& tk,
+                         const CUtensorMap& tv, void* o, float* stats, const int* kv_list,
+                         int topk, int* err, cudaStream_t stream) {
+  using L = FwdLayout<D>;
+  const dim3 grid((s.Nq + 2 * kTile - 1) / (2 * kTile), s.H, s.B);
+  cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D, kSparse>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+  if (e != cudaSuccess) return e;
+  attn_fwd_kernel<D, kSparse><<<grid, kThreads, L::kAlloc, stream>>>(
+      tq, tk, tv, static_cast<__nv_bfloat16*>(o), stats, s.Nq, s.Nkv, s.H, s.scale, s.causal,
+      kv_list, topk, err);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_attn_fwd(const AttnShape& s, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, void* o, float* stats, const int* kv_list,
                             int topk, int* err, cudaStream_t stream) {
-  const dim3 grid((s.Nq + 2 * kTile - 1) / (2 * kTile), s.H, s.B);
-  auto* op = static_cast<__nv_bfloat16*>(o);
-  if (s.D == 128) {
-    using L = FwdLayout<128>;
-    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<128>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
-    if (e != cudaSuccess) return e;
-    attn_fwd_kernel<128><<<grid, kThreads, L::kAlloc, stream>>>(
-        tq, tk, tv, op, stats, s.Nq, s.Nkv, s.H, s.scale, s.causal, kv_list, topk, err);
-  } else {
-    using L = FwdLayout<64>;
-    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<64>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
-    if (e != cudaSuccess) return e;
-    attn_fwd_kernel<64><<<grid, kThreads, L::kAlloc, stream>>>(
-        tq, tk, tv, op, stats, s.Nq, s.Nkv, s.H, s.scale, s.causal, kv_list, topk, err);
-  }
-  return cudaGetLastError();
+  const bool sp = kv_list != nullptr;
+  if (s.D == 128)
+    return sp ? launch_fwd_t<128, true>(s, tq, tk, tv, o, stats, kv_list, topk, err, stream)
+              : launch_fwd_t<128, false>(s, tq, tk, tv, o, stats, kv_list, topk, err, stream);
+  return sp ? launch_fwd_t<64, true>(s, tq, tk, tv, o, stats, kv_list, topk, err, stream)
+            : launch_fwd_t<64, false>(s, tq, tk, tv, o, stats, kv_list, topk, err, stream);
 }
 
 }  // namespace nvq
