@@ -368,6 +368,46 @@ def sparse_bench(peaks, stream, steps, warmup):
                         for name, (c, t) in kt.items() if c}}
 
 
+def hp_bench(peaks, stream, steps, inp, q, k, v, do, wsf, wsb):
+    """The Wan step with the auxiliary high-precision output: forward with O_hp =
+    P V~ / l next to O, backward with delta from O_hp.  Same counted FLOPs as the
+    headline step (the extra P V~ product is not counted)."""
+    import torch
+
+    from nvfp4_fake_quant_gb300 import api
+    b, n, h, d = q.shape
+    o, o_hp = torch.empty_like(q), torch.empty_like(q)
+    stats = torch.empty((b, h, 2, n), dtype=torch.float32, device=q.device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+    def fwd():
+        api.attn_qat_fwd_hp(q, k, v, inp.scale, False, o=o, o_hp=o_hp, stats=stats, workspace=wsf)
+
+    def step():
+        fwd()
+        api.attn_qat_bwd(q, k, v, o_hp, stats, do, inp.scale, False, dq=dq, dk=dk, dv=dv,
+                         workspace=wsb)
+
+    step()
+    torch.cuda.synchronize()
+    api.timing_enable(True)
+    ms = time_events(step, steps, stream)
+    kt = api.timing_read()
+    api.timing_enable(False)
+    fwd_ms = time_events(fwd, steps, stream)
+    if api.device_status() != 0:
+        raise RuntimeError("a bounded device wait timed out (auxiliary output)")
+    f_fwd = flops_fwd(b, n, n, h, d)
+    total = sum(t for _, t in kt.values())
+    return {"ms_per_step": ms, "TFLOP/s": 3.5 * f_fwd / (ms * 1e-3) / 1e12,
+            "pct_of_bf16_peak": 3.5 * f_fwd / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
+            "fwd_ms": fwd_ms, "fwd_tflops_executed": 2.0 * f_fwd / (fwd_ms * 1e-3) / 1e12,
+            "flops_counting": "as the headline step; executed forward work is S twice and "
+                              "two P V~ products (4 * 2*N^2*D per head)",
+            "kernels": {name: {"launches": c, "avg_ms": t / c, "share": t / total}
+                        for name, (c, t) in kt.items() if c}}
+
+
 def run_ours(args):
     import torch
 
@@ -460,6 +500,8 @@ def run_ours(args):
     quant = quantizer_bench(peaks, stream) if rank == 0 and not args.skip_quantizer else None
     sparse = (sparse_bench(peaks, stream, max(3, args.steps), args.warmup)
               if rank == 0 and not args.skip_sparse and (n, h) == (25088, 12) else None)
+    hp = (hp_bench(peaks, stream, max(3, args.steps), inp, q, k, v, do, wsf, wsb)
+          if rank == 0 and not args.skip_hp else None)
 
     peak_t = peaks["bf16_tflops"]
     k_total = sum(ms for _, ms in ktimes.values())
@@ -502,6 +544,8 @@ def run_ours(args):
         line["quantizer"] = quant
     if sparse is not None:
         line["block_sparse"] = sparse
+    if hp is not None:
+        line["aux_output"] = hp
     if rank == 0 and not args.skip_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_rows)
     if rank == 0:
@@ -524,6 +568,8 @@ def main(argv=None):
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-sparse", action="store_true",
                     help="skip the block-sparse (VSA) workload's extra measurement")
+    ap.add_argument("--skip-hp", action="store_true",
+                    help="skip the measurement of the step with the auxiliary output")
     ap.add_argument("--quantizer-only", action="store_true",
                     help="time only the standalone quantizer (profiling of that kernel)")
     ap.add_argument("--n", type=int, default=None,

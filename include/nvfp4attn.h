@@ -153,9 +153,28 @@ nvq_status attn_qat_fwd(const void* q, const void* k, const void* v,
                         void* o, float* stats, void* ws, size_t ws_bytes, nvq_stream_t stream);
 
 /*
+ * Forward with the auxiliary high-precision output ("Attn-QAT Training" guide,
+ * attn_qat_train(): use_high_prec_o; the metadata's backward: straight-through
+ * with an auxiliary output).  Arguments and results as in attn_qat_fwd, plus
+ *   o_hp    bf16 [B, Nq, H, D] contiguous, 16-byte aligned (written):
+ *           O_hp = P V~ / l, the output with the softmax probabilities left
+ *           unquantized (P = exp(scale*S - m) rounded to f16 for the tensor
+ *           core product; V~ and l as for o).
+ * o and stats are the same values attn_qat_fwd writes.  Passing o_hp as the
+ * `o` argument of attn_qat_bwd takes the backward's delta from O_hp.  The
+ * workspace is attn_qat_fwd_workspace(...).
+ */
+nvq_status attn_qat_fwd_hp(const void* q, const void* k, const void* v,
+                           int B, int Nq, int Nkv, int H, int D, float scale, int causal,
+                           void* o, void* o_hp, float* stats, void* ws, size_t ws_bytes,
+                           nvq_stream_t stream);
+
+/*
  * Straight-through backward.
  *   q, k, v, D, scale, causal  as in the forward (same values)
- *   o       bf16 [B, Nq, H, D]: the forward output (delta = rowsum(dO*o))
+ *   o       bf16 [B, Nq, H, D]: the forward output (delta = rowsum(dO*o)); it is
+ *           read for delta only, so passing attn_qat_fwd_hp's o_hp takes delta
+ *           from the high-precision output instead
  *   stats   f32 [B, H, 2, Nq]: the forward's stats
  *   dout    bf16 [B, Nq, H, D]: dL/dO
  *   dq      bf16 [B, Nq, H, D]; dk, dv bf16 [B, Nkv, H, D] (written)

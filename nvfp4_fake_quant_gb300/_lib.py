@@ -32,6 +32,9 @@ SIGNATURES = {
     "attn_qat_fwd_workspace": (c_size_t, [c_int, c_int, c_int, c_int, c_int]),
     "attn_qat_fwd": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int,
                              c_float, c_int, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
+    "attn_qat_fwd_hp": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int,
+                                c_float, c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_size_t,
+                                c_void_p]),
     "attn_qat_bwd_workspace": (c_size_t, [c_int, c_int, c_int, c_int, c_int]),
     "attn_qat_bwd": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                              c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_float, c_int,

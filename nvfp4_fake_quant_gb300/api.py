@@ -123,8 +123,7 @@ def _workspace(nbytes: int, device, ws: torch.Tensor | None) -> torch.Tensor:
     return ws
 
 
-def attn_qat_fwd(q, k, v, scale=None, causal=False, o=None, stats=None, workspace=None):
-    """Forward: returns (o bf16 [B, Nq, H, D], stats fp32 [B, H, 2, Nq] = (LSE, m))."""
+def _fwd_args(q, k, v, scale, o, stats, workspace):
     _check_bnhd(q, "q")
     b, nq, h, d = q.shape
     nkv = k.shape[1]
@@ -137,10 +136,31 @@ def attn_qat_fwd(q, k, v, scale=None, causal=False, o=None, stats=None, workspac
     if stats is None:
         stats = torch.empty((b, h, 2, nq), dtype=torch.float32, device=q.device)
     ws = _workspace(attn_qat_fwd_workspace(b, nq, nkv, h, d), q.device, workspace)
-    _lib.call("attn_qat_fwd", _ptr(q), _ptr(k), _ptr(v), b, nq, nkv, h, d, scale,
+    return (b, nq, nkv, h, d), scale, o, stats, ws
+
+
+def attn_qat_fwd(q, k, v, scale=None, causal=False, o=None, stats=None, workspace=None):
+    """Forward: returns (o bf16 [B, Nq, H, D], stats fp32 [B, H, 2, Nq] = (LSE, m))."""
+    dims, scale, o, stats, ws = _fwd_args(q, k, v, scale, o, stats, workspace)
+    _lib.call("attn_qat_fwd", _ptr(q), _ptr(k), _ptr(v), *dims, scale,
               int(bool(causal)), _ptr(o), _ptr(stats), _ptr(ws), ws.numel() * ws.element_size(),
               _stream_ptr(q))
     return o, stats
+
+
+def attn_qat_fwd_hp(q, k, v, scale=None, causal=False, o=None, o_hp=None, stats=None,
+                    workspace=None):
+    """Forward with the auxiliary high-precision output: returns (o, o_hp, stats),
+    o_hp = P V~ / l with P unquantized (bf16 [B, Nq, H, D]); o and stats as in
+    attn_qat_fwd.  Passing o_hp as ``o`` to attn_qat_bwd takes delta from it."""
+    dims, scale, o, stats, ws = _fwd_args(q, k, v, scale, o, stats, workspace)
+    if o_hp is None:
+        o_hp = torch.empty_like(q)
+    _check_bnhd(o_hp, "o_hp", q.shape)
+    _lib.call("attn_qat_fwd_hp", _ptr(q), _ptr(k), _ptr(v), *dims, scale,
+              int(bool(causal)), _ptr(o), _ptr(o_hp), _ptr(stats), _ptr(ws),
+              ws.numel() * ws.element_size(), _stream_ptr(q))
+    return o, o_hp, stats
 
 
 def attn_qat_bwd(q, k, v, o, stats, do, scale=None, causal=False, dq=None, dk=None, dv=None,
@@ -285,29 +305,42 @@ def device_status(device=None) -> int:
     return int(_lib.load().nvq_device_status(s))
 
 
+DELTA_MODES = ("o", "hp")
+
+
 class AttnQATFunction(torch.autograd.Function):
-    """O = attention with NVFP4 fake-quantized Q, K, V, P; straight-through backward."""
+    """O = attention with NVFP4 fake-quantized Q, K, V, P; straight-through backward.
+    ``delta_mode`` "o": the backward's delta = rowsum(dO * O); "hp": from the
+    auxiliary high-precision output P V~ / l, which the forward then also computes."""
 
     @staticmethod
-    def forward(ctx, q, k, v, scale, causal):
-        o, stats = attn_qat_fwd(q, k, v, scale, causal)
-        ctx.save_for_backward(q, k, v, o, stats)
+    def forward(ctx, q, k, v, scale, causal, delta_mode="o"):
+        if delta_mode == "hp":
+            o, o_d, stats = attn_qat_fwd_hp(q, k, v, scale, causal)
+        elif delta_mode == "o":
+            o, stats = attn_qat_fwd(q, k, v, scale, causal)
+            o_d = o
+        else:
+            raise ValueError(f"delta_mode must be one of {DELTA_MODES}, got {delta_mode!r}")
+        ctx.save_for_backward(q, k, v, o_d, stats)
         ctx.scale, ctx.causal = scale, causal
         return o
 
     @staticmethod
     def backward(ctx, do):
-        q, k, v, o, stats = ctx.saved_tensors
-        dq, dk, dv = attn_qat_bwd(q, k, v, o, stats, do.contiguous(), ctx.scale, ctx.causal)
-        return dq, dk, dv, None, None
+        q, k, v, o_d, stats = ctx.saved_tensors
+        dq, dk, dv = attn_qat_bwd(q, k, v, o_d, stats, do.contiguous(), ctx.scale, ctx.causal)
+        return dq, dk, dv, None, None, None
 
 
 class AttnQAT(torch.nn.Module):
     """``AttentionImpl(num_heads, head_size, softmax_scale, causal)`` with ``forward(q, k, v)``."""
 
     def __init__(self, num_heads: int, head_size: int, softmax_scale: float | None = None,
-                 causal: bool = False, dropout_p: float = 0.0):
+                 causal: bool = False, dropout_p: float = 0.0, delta_mode: str = "o"):
         super().__init__()
+        if delta_mode not in DELTA_MODES:
+            raise ValueError(f"delta_mode must be one of {DELTA_MODES}, got {delta_mode!r}")
         if dropout_p > 0:
             raise NotImplementedError(
                 f"NVFP4 Attn-QAT attention applies no dropout (got dropout_p={dropout_p})")
@@ -316,6 +349,7 @@ class AttnQAT(torch.nn.Module):
         self.num_heads, self.head_size = num_heads, head_size
         self.softmax_scale = default_scale(head_size) if softmax_scale is None else softmax_scale
         self.causal = causal
+        self.delta_mode = delta_mode
 
     def forward(self, q, k, v):
-        return AttnQATFunction.apply(q, k, v, self.softmax_scale, self.causal)
+        return AttnQATFunction.apply(q, k, v, self.softmax_scale, self.causal, self.delta_mode)

@@ -236,14 +236,15 @@ nvq_status check_quant(const void* x, int64_t rows, int64_t cols, int64_t ld_x) 
 
 }  // namespace
 // Forward; kv_list: NULL (dense) or the block-sparse key-tile lists (validated
-// by the caller).
+// by the caller); o_hp: NULL or the auxiliary high-precision output (not with
+// kv_list).
 nvq_status fwd_impl(const void* q, const void* k, const void* v, int B, int Nq, int Nkv, int H,
                     int D, float scale, int causal, const int* kv_list, int topk, void* o,
-                    float* stats, void* ws, size_t ws_bytes, cudaStream_t stream) {
+                    void* o_hp, float* stats, void* ws, size_t ws_bytes, cudaStream_t stream) {
   nvq_status st = check_attn(B, Nq, Nkv, H, D, scale, causal);
   if (st != NVQ_OK) return st;
   if (!q || !k || !v || !o || !stats || !aligned16(q) || !aligned16(k) || !aligned16(v) ||
-      !aligned16(o) || !aligned16(stats))
+      !aligned16(o) || !aligned16(stats) || (o_hp != nullptr && !aligned16(o_hp)))
     return NVQ_ERR_INVALID;
   const FwdWs w = fwd_ws(B, Nq, Nkv, H, D);
   if (ws == nullptr || ws_bytes < w.total || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
@@ -270,7 +271,7 @@ nvq_status fwd_impl(const void* q, const void* k, const void* v, int B, int Nq, 
     return fail_cuda("quantize v", e);
   const AttnShape s{B, Nq, Nkv, H, D, scale, causal};
   return from_cuda("attn_fwd", timed(NVQ_KERNEL_ATTN_FWD, stream, [&] {
-                     return launch_attn_fwd(s, mq, mk, mv, o, stats, kv_list, topk, err, stream);
+                     return launch_attn_fwd(s, mq, mk, mv, o, o_hp, stats, kv_list, topk, err, stream);
                    }));
 }
 
@@ -427,8 +428,16 @@ size_t attn_qat_bwd_workspace(int B, int Nq, int Nkv, int H, int D) {
 nvq_status attn_qat_fwd(const void* q, const void* k, const void* v, int B, int Nq, int Nkv,
                         int H, int D, float scale, int causal, void* o, float* stats, void* ws,
                         size_t ws_bytes, nvq_stream_t stream) {
-  return fwd_impl(q, k, v, B, Nq, Nkv, H, D, scale, causal, nullptr, 0, o, stats, ws, ws_bytes,
-                  stream);
+  return fwd_impl(q, k, v, B, Nq, Nkv, H, D, scale, causal, nullptr, 0, o, nullptr, stats, ws,
+                  ws_bytes, stream);
+}
+
+nvq_status attn_qat_fwd_hp(const void* q, const void* k, const void* v, int B, int Nq, int Nkv,
+                           int H, int D, float scale, int causal, void* o, void* o_hp,
+                           float* stats, void* ws, size_t ws_bytes, nvq_stream_t stream) {
+  if (o_hp == nullptr) return NVQ_ERR_INVALID;
+  return fwd_impl(q, k, v, B, Nq, Nkv, H, D, scale, causal, nullptr, 0, o, o_hp, stats, ws,
+                  ws_bytes, stream);
 }
 
 nvq_status attn_qat_bwd(const void* q, const void* k, const void* v, const void* o,
@@ -458,8 +467,8 @@ nvq_status attn_qat_fwd_sparse(const void* q, const void* k, const void* v, int 
                                float* stats, void* ws, size_t ws_bytes, nvq_stream_t stream) {
   const nvq_status st = check_sparse(N, topk, kv_tiles);
   if (st != NVQ_OK) return st;
-  return fwd_impl(q, k, v, B, N, N, H, D, scale, 0, kv_tiles, topk, o, stats, ws, ws_bytes,
-                  stream);
+  return fwd_impl(q, k, v, B, N, N, H, D, scale, 0, kv_tiles, topk, o, nullptr, stats, ws,
+                  ws_bytes, stream);
 }
 
 nvq_status attn_qat_bwd_sparse(const void* q, const void* k, const void* v, const void* o,

@@ -25,6 +25,20 @@
 // accumulators.  Warpgroup hf of tile i writes the f16 pairs of its 64 keys
 // into the first 32 of its own 64 S columns, which it has already loaded:
 // the 16-key slice kk of P~_i is at column 128 i + 64 (kk / 4) + 8 (kk % 4).
+//
+// Modes (template kMode):
+//   kDense   every key tile, one K/V load per step shared by the two query tiles;
+//   kSparse  block-sparse: query tile i runs over its own listed key tiles, one
+//            load per query tile per step;
+//   kAux     the auxiliary high-precision output O_hp = P V~ / l next to O (the
+//            "auxiliary output" of the Attn-QAT backward, "use_high_prec_o"):
+//            one query tile per CTA, and the two softmax pairs take the even
+//            and the odd key tiles of it (key tile 2 j + i at step j for pair
+//            i).  Row maxima and sums are combined over all four warpgroups.
+//            TMEM: S_0, S_1 as above; O at [256, 256 + D), O_hp at
+//            [256 + D, 256 + 2 D).  Each warpgroup writes, per 32 keys c of its
+//            64, P~ into columns [32 c, 32 c + 16) and P (f16) into
+//            [32 c + 16, 32 c + 32) of its S columns (both already loaded).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -44,6 +58,7 @@ constexpr int kThreads = 576;
 constexpr int kRing = 5;  // K/V tile ring (K and V tiles interleave in pass 2)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint32_t kAtomBlock = 128u * 128u;  // bytes of one 64-column block of a 128-row tile
+constexpr int kDense = 0, kSparse = 1, kAux = 2;  // forward modes
 
 template <int D>
 struct FwdLayout {
@@ -70,12 +85,16 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
 // warpgroups 2i and 2i+1 (warps 8i..8i+7) own tile i, 64 key columns each.  TMEM: S_i at [128 i, 128 i + 128),
 // O_i at [256 + 128 i, 256 + 128 i + D).  The UMMA warp ping-pongs the two
 // tiles so that one warpgroup's softmax overlaps the other's UMMAs.
-template <int D, bool kSparse>
+template <int D, int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                     const __grid_constant__ CUtensorMap tv, __nv_bfloat16* __restrict__ o,
-                    float* __restrict__ stats, int Nq, int Nkv, int H, float scale, int causal,
-                    const int* __restrict__ kv_list, int topk, int* __restrict__ err) {
+                    __nv_bfloat16* __restrict__ o_hp, float* __restrict__ stats, int Nq, int Nkv,
+                    int H, float scale, int causal, const int* __restrict__ kv_list, int topk,
+                    int* __restrict__ err) {
+  constexpr bool sparse = kMode == kSparse;
+  constexpr bool aux = kMode == kAux;
+  constexpr int kQTiles = aux ? 1 : 2;  // query tiles per CTA
   using L = FwdLayout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023u) &
@@ -83,7 +102,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int h = blockIdx.y, b = blockIdx.z;
-  const int q0 = blockIdx.x * 2 * kTile;
+  const int q0 = blockIdx.x * kQTiles * kTile;
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBars);
   uint64_t* q_full = bars + 0;
@@ -100,9 +119,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_kv_all = (Nkv + kTile - 1) / kTile;
   // causal: the second query tile sees one more key tile than the first; both
   // run over it (the first tile's part of it is fully masked); block-sparse:
-  // topk listed key tiles per query tile
-  const int n_kv = kSparse ? topk
-                 : causal ? min(n_kv_all, 2 * static_cast<int>(blockIdx.x) + 2) : n_kv_all;
+  // topk listed key tiles per query tile; auxiliary output: two key tiles per
+  // step (a missing odd one is fully masked)
+  int n_kv;
+  if (sparse) {
+    n_kv = topk;
+  } else if (aux) {
+    const int nk = causal ? min(n_kv_all, static_cast<int>(blockIdx.x) + 1) : n_kv_all;
+    n_kv = (nk + 1) / 2;
+  } else {
+    n_kv = causal ? min(n_kv_all, 2 * static_cast<int>(blockIdx.x) + 2) : n_kv_all;
+  }
 
   if (threadIdx.x == 0) {
     *abort = 0;
@@ -131,9 +158,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // Block-sparse: query tile i attends to the key tiles list_i[0..topk); a K or V
   // step then loads one tile per query tile.  Dense: key tile j at step j, one
-  // load shared by both query tiles.
-  constexpr bool sparse = kSparse;
-  const int nt = sparse ? 2 : 1;  // loads per K or V step
+  // load shared by both query tiles.  Auxiliary output: key tile 2 j + i for
+  // pair i, one load per pair.
+  constexpr bool per_pair = sparse || aux;  // one K or V load per pair and step
+  constexpr int nt = per_pair ? 2 : 1;      // loads per K or V step
   const int n_qt = (Nq + kTile - 1) / kTile;
   const int* list0 = nullptr;
   const int* list1 = nullptr;
@@ -143,7 +171,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     list0 = kv_list + (base + qt0) * topk;
     list1 = kv_list + (base + min(qt0 + 1, n_qt - 1)) * topk;  // a missing tile's rows are masked
   }
-  auto key_tile = [&](int i, int j) -> int { return sparse ? (i ? list1[j] : list0[j]) : j; };
+  auto key_tile = [&](int i, int j) -> int {
+    return sparse ? (i ? list1[j] : list0[j]) : aux ? 2 * j + i : j;
+  };
 
   if (warp == kTmaWarp) {
     // ------------------------------------------------------------ producer
@@ -153,9 +183,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tq);
     tma_prefetch_desc(&tk);
     tma_prefetch_desc(&tv);
-    mbar_arrive_expect_tx_w(q_full, 2u * L::kTileBytes);
+    mbar_arrive_expect_tx_w(q_full, static_cast<uint32_t>(kQTiles) * L::kTileBytes);
 #pragma unroll
-    for (int i = 0; i < 2; ++i)
+    for (int i = 0; i < kQTiles; ++i)
 #pragma unroll
       for (int blk = 0; blk < D / 64; ++blk)
         tma_load_4d_w(smem + L::kQ + i * L::kTileBytes + blk * kAtomBlock, &tq, blk * 64,
@@ -202,7 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     auto issue_s = [&](int i, int idx) {  // S_i = Q~_i K~^T, K~ in ring slot of load idx
       const uint32_t kb = ring_addr + (idx % kRing) * L::kTileBytes;
-      const uint32_t qb = q_addr + i * L::kTileBytes;
+      const uint32_t qb = q_addr + (aux ? 0 : i) * L::kTileBytes;
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = (kk >> 2) * kAtomBlock + (kk & 3) * 32;
@@ -211,26 +241,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       umma_commit_w(&s_full[i]);
     };
-    // O_i += P~_i V~ with P~_i read from TMEM, V~ in the ring slot of load idx
+    // O_i += P~_i V~ with P~_i read from TMEM, V~ in the ring slot of load idx;
+    // auxiliary output: O += P~_i V~ and O_hp += P_i V~ (one O for both pairs)
     auto issue_pv = [&](int i, int idx, bool acc) {
       const uint32_t vb = ring_addr + (idx % kRing) * L::kTileBytes;
+      if constexpr (aux) {
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk)
-        umma_f16_ts_w(tmem + 256 + i * 128, tmem + i * 128 + 64 * (kk >> 2) + 8 * (kk & 3),
-                      sdesc_sw128(vb + kk * 2048, kAtomBlock, 1024), idesc_pv,
-                      (acc || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t col = i * 128 + 64 * (kk >> 2) + 32 * ((kk >> 1) & 1) + 8 * (kk & 1);
+          umma_f16_ts_w(tmem + 256, tmem + col, sdesc_sw128(vb + kk * 2048, kAtomBlock, 1024),
+                        idesc_pv, (acc || kk > 0) ? 1u : 0u);
+          umma_f16_ts_w(tmem + 256 + D, tmem + col + 16,
+                        sdesc_sw128(vb + kk * 2048, kAtomBlock, 1024), idesc_pv,
+                        (acc || kk > 0) ? 1u : 0u);
+        }
+      } else {
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma_f16_ts_w(tmem + 256 + i * 128, tmem + i * 128 + 64 * (kk >> 2) + 8 * (kk & 3),
+                        sdesc_sw128(vb + kk * 2048, kAtomBlock, 1024), idesc_pv,
+                        (acc || kk > 0) ? 1u : 0u);
+      }
     };
     // Load idx of query tile i within a step whose loads start at `base`; a dense
     // load serves both tiles and is released after tile 1's UMMAs.
-    auto tile_load = [&](int base, int i) { return base + (sparse ? i : 0); };
+    auto tile_load = [&](int base, int i) { return base + (per_pair ? i : 0); };
     auto release = [&](int base, int i) {
-      if (sparse || i == 1) umma_commit_w(&r_empty[tile_load(base, i) % kRing]);
+      if (per_pair || i == 1) umma_commit_w(&r_empty[tile_load(base, i) % kRing]);
     };
     bool ok = mbar_wait_warp(q_full, 0, abort);
     // pass 1: S_0(j), S_1(j) for the row maxima
     for (int j = 0; j < n_kv && ok; ++j, li += nt) {
       for (int i = 0; i < 2 && ok; ++i) {
-        if ((sparse || i == 0) && !(ok = wait_slot(tile_load(li, i)))) break;
+        if ((per_pair || i == 0) && !(ok = wait_slot(tile_load(li, i)))) break;
         if (j > 0 && !(ok = mbar_wait_warp(&s_free[i], static_cast<uint32_t>((j - 1) & 1), abort))) break;
         tc_fence_after();
         issue_s(i, tile_load(li, i));
@@ -239,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // pass 2 prologue: S_0(0), S_1(0)
     for (int i = 0; i < 2 && ok; ++i) {
-      if ((sparse || i == 0) && !(ok = wait_slot(tile_load(li, i)))) break;
+      if ((per_pair || i == 0) && !(ok = wait_slot(tile_load(li, i)))) break;
       if (!(ok = mbar_wait_warp(&s_free[i], static_cast<uint32_t>((n_kv - 1) & 1), abort))) break;
       tc_fence_after();
       issue_s(i, tile_load(li, i));
@@ -252,13 +295,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int kbase = (j + 1 < n_kv) ? li : -1;  // K(j+1)
       if (kbase >= 0) li += nt;
       for (int i = 0; i < 2 && ok; ++i) {
-        if ((sparse || i == 0) && !(ok = wait_slot(tile_load(vbase, i)))) break;
+        if ((per_pair || i == 0) && !(ok = wait_slot(tile_load(vbase, i)))) break;
         if (!(ok = mbar_wait_warp(&p_full[i], static_cast<uint32_t>(j & 1), abort))) break;
         tc_fence_after();
-        issue_pv(i, tile_load(vbase, i), j > 0);
+        issue_pv(i, tile_load(vbase, i), j > 0 || (aux && i > 0));
         release(vbase, i);
         if (kbase >= 0) {
-          if ((sparse || i == 0) && !(ok = wait_slot(tile_load(kbase, i)))) break;
+          if ((per_pair || i == 0) && !(ok = wait_slot(tile_load(kbase, i)))) break;
           // S_i(j+1): S_i was read before p_full_i(j), and the UMMAs run in
           // issue order, so PV_i(j) reads P~_i before S_i(j+1) overwrites it
           issue_s(i, tile_load(kbase, i));
@@ -281,7 +324,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ti = wg >> 1;                // query tile
     const int hf = wg & 1;                 // half of the key columns
     const int t = threadIdx.x & 127;       // row in the tile == TMEM lane
-    const int qrow = q0 + ti * kTile + t;
+    const int tile_q0 = q0 + (aux ? 0 : ti * kTile);
+    const int qrow = tile_q0 + t;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t s_col = static_cast<uint32_t>(ti * 128 + hf * 64);
     const float c1 = scale * kLog2e;
@@ -291,7 +335,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     float mraw = -INFINITY;
     uint32_t r[32];
-    const int tile_q0 = q0 + ti * kTile;
     for (int j = 0; j < n_kv && ok; ++j) {
       if (!(ok = mbar_wait_warp(&s_full[ti], static_cast<uint32_t>(j & 1), abort))) break;
       tc_fence_after();
@@ -321,6 +364,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (hf == 0) xchg[t] = mraw = fmaxf(mraw, xchg[t]);
     named_bar_sync(pair_bar, kPairThreads);
     if (hf == 1) mraw = xchg[t];
+    if constexpr (aux) {  // both pairs hold the same rows: combine their maxima
+      const float* xall = reinterpret_cast<const float*>(smem + L::kX);
+      named_bar_sync(3, 2 * kPairThreads);
+      mraw = fmaxf(xall[t], xall[128 + t]);
+      named_bar_sync(3, 2 * kPairThreads);  // read before the sums reuse the area
+    }
     const float m = mraw * scale;
     const float negmb = -m * kLog2e;
     const uint64_t c12 = pk2(c1, c1), nmb2 = pk2(negmb, negmb);
@@ -355,9 +404,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           pquant16(x + 16 * hb, pp, ph);
 #pragma unroll
           for (int u = 0; u < 8; ++u) l2 = add2(l2, pk2(pp[2 * u], pp[2 * u + 1]));
+          if constexpr (aux) {
+            // P itself as f16 pairs: keys [64 hf + 32 c + 16 hb, +16) -> columns
+            // [64 hf + 32 c + 16 + 8 hb, +8), inside the 32 columns just loaded
+            uint32_t pr[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              __half2 h2 = __floats2half2_rn(pp[2 * u], pp[2 * u + 1]);
+              pr[u] = *reinterpret_cast<uint32_t*>(&h2);
+            }
+            tmem_st8(tmem + lane_base + s_col + c * 32 + 16 + 8 * hb, pr);
+          }
         }
-        // keys [64 hf + 32 c, +32) -> columns [64 hf + 16 c, +16) of S_i, already loaded
-        tmem_st16(tmem + lane_base + s_col + c * 16, pt);
+        if constexpr (aux) {
+          // keys [64 hf + 32 c, +32): P~ -> columns [64 hf + 32 c, +16)
+          tmem_st16(tmem + lane_base + s_col + c * 32, pt);
+        } else {
+          // keys [64 hf + 32 c, +32) -> columns [64 hf + 16 c, +16) of S_i, already loaded
+          tmem_st16(tmem + lane_base + s_col + c * 16, pt);
+        }
       }
       tmem_wait_st();
       tc_fence_before();
@@ -372,13 +437,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (hf == 0) xchg[t] = l = l + xchg[t];
     named_bar_sync(pair_bar, kPairThreads);
     if (hf == 1) l = xchg[t];
+    if constexpr (aux) {
+      const float* xall = reinterpret_cast<const float*>(smem + L::kX);
+      named_bar_sync(3, 2 * kPairThreads);
+      l = xall[t] + xall[128 + t];
+    }
     if (have_o) {
       tc_fence_after();
       const float inv_l = 1.0f / l;
-      __nv_bfloat16* orow = o + ((static_cast<int64_t>(b) * Nq + qrow) * H + h) * D + hf * (D / 2);
+      // auxiliary output: pair 0 writes O, pair 1 O_hp
+      __nv_bfloat16* obase = (aux && ti == 1) ? o_hp : o;
+      __nv_bfloat16* orow = obase + ((static_cast<int64_t>(b) * Nq + qrow) * H + h) * D + hf * (D / 2);
+      const uint32_t o_col = 256u + static_cast<uint32_t>(ti * (aux ? D : 128) + hf * (D / 2));
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) {
-        tmem_ld32(tmem + lane_base + 256 + ti * 128 + hf * (D / 2) + c * 32, r);
+        tmem_ld32(tmem + lane_base + o_col + c * 32, r);
         tmem_wait_ld();
         if (qrow < Nq) {
           uint32_t w[16];
@@ -394,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             dst[u] = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
         }
       }
-      if (qrow < Nq && hf == 0) {
+      if (qrow < Nq && hf == 0 && (!aux || ti == 0)) {
         float* st = stats + (static_cast<int64_t>(b) * H + h) * 2 * Nq;
         st[qrow] = m + logf(l);
         st[Nq + qrow] = m;
@@ -414,30 +487,39 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-template <int D, bool kSparse>
+template <int D, int kMode>
 cudaError_t launch_fwd_t(const AttnShape& s, const CUtensorMap& tq, const CUtensorMap& tk,
-                         const CUtensorMap& tv, void* o, float* stats, const int* kv_list,
-                         int topk, int* err, cudaStream_t stream) {
+                         const CUtensorMap& tv, void* o, void* o_hp, float* stats,
+                         const int* kv_list, int topk, int* err, cudaStream_t stream) {
   using L = FwdLayout<D>;
-  const dim3 grid((s.Nq + 2 * kTile - 1) / (2 * kTile), s.H, s.B);
-  cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D, kSparse>,
+  const int q_per_cta = (kMode == kAux ? 1 : 2) * kTile;
+  const dim3 grid((s.Nq + q_per_cta - 1) / q_per_cta, s.H, s.B);
+  cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D, kMode>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
-  attn_fwd_kernel<D, kSparse><<<grid, kThreads, L::kAlloc, stream>>>(
-      tq, tk, tv, static_cast<__nv_bfloat16*>(o), stats, s.Nq, s.Nkv, s.H, s.scale, s.causal,
-      kv_list, topk, err);
+  attn_fwd_kernel<D, kMode><<<grid, kThreads, L::kAlloc, stream>>>(
+      tq, tk, tv, static_cast<__nv_bfloat16*>(o), static_cast<__nv_bfloat16*>(o_hp), stats, s.Nq,
+      s.Nkv, s.H, s.scale, s.causal, kv_list, topk, err);
   return cudaGetLastError();
 }
 
+template <int D>
+cudaError_t launch_fwd_d(const AttnShape& s, const CUtensorMap& tq, const CUtensorMap& tk,
+                         const CUtensorMap& tv, void* o, void* o_hp, float* stats,
+                         const int* kv_list, int topk, int* err, cudaStream_t stream) {
+  if (kv_list != nullptr)
+    return launch_fwd_t<D, kSparse>(s, tq, tk, tv, o, o_hp, stats, kv_list, topk, err, stream);
+  if (o_hp != nullptr)
+    return launch_fwd_t<D, kAux>(s, tq, tk, tv, o, o_hp, stats, kv_list, topk, err, stream);
+  return launch_fwd_t<D, kDense>(s, tq, tk, tv, o, o_hp, stats, kv_list, topk, err, stream);
+}
+
 cudaError_t launch_attn_fwd(const AttnShape& s, const CUtensorMap& tq, const CUtensorMap& tk,
-                            const CUtensorMap& tv, void* o, float* stats, const int* kv_list,
-                            int topk, int* err, cudaStream_t stream) {
-  const bool sp = kv_list != nullptr;
-  if (s.D == 128)
-    return sp ? launch_fwd_t<128, true>(s, tq, tk, tv, o, stats, kv_list, topk, err, stream)
-              : launch_fwd_t<128, false>(s, tq, tk, tv, o, stats, kv_list, topk, err, stream);
-  return sp ? launch_fwd_t<64, true>(s, tq, tk, tv, o, stats, kv_list, topk, err, stream)
-            : launch_fwd_t<64, false>(s, tq, tk, tv, o, stats, kv_list, topk, err, stream);
+                            const CUtensorMap& tv, void* o, void* o_hp, float* stats,
+                            const int* kv_list, int topk, int* err, cudaStream_t stream) {
+  if (kv_list != nullptr && o_hp != nullptr) return cudaErrorInvalidValue;
+  return s.D == 128 ? launch_fwd_d<128>(s, tq, tk, tv, o, o_hp, stats, kv_list, topk, err, stream)
+                    : launch_fwd_d<64>(s, tq, tk, tv, o, o_hp, stats, kv_list, topk, err, stream);
 }
 
 }  // namespace nvq

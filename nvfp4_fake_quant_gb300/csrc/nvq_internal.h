@@ -62,10 +62,11 @@ cudaError_t timed(int kind, cudaStream_t stream, F&& launch) {
 int make_bnhd_map(CUtensorMap* map, const void* base, int B, int N, int H, int D, bool f16,
                    int box_rows = kTile);
 
-// kv_list: NULL (dense) or int32 [B, H, ceil(Nq/128), topk] key tiles per query tile
+// kv_list: NULL (dense) or int32 [B, H, ceil(Nq/128), topk] key tiles per query tile;
+// o_hp: NULL or the auxiliary output P V~ / l (bf16, layout of o); not both
 cudaError_t launch_attn_fwd(const AttnShape& s, const CUtensorMap& tq, const CUtensorMap& tk,
-                            const CUtensorMap& tv, void* o, float* stats, const int* kv_list,
-                            int topk, int* err, cudaStream_t stream);
+                            const CUtensorMap& tv, void* o, void* o_hp, float* stats,
+                            const int* kv_list, int topk, int* err, cudaStream_t stream);
 cudaError_t launch_bwd_prep(const AttnShape& s, const void* o, const void* dout, float* delta,
                             cudaStream_t stream);
 // dK, dV (key-outer; Q~, K~, V~, dO maps with 128-row boxes).  Block-sparse:

@@ -118,6 +118,13 @@ class HeadProblem:
         o = (pt @ self.vt) / l[:, None]
         return o, m + torch.log(l), m
 
+    def o_hp_rows(self, rows):
+        """The auxiliary high-precision output P V~ / l (P unquantized) for ``rows``."""
+        rows = torch.as_tensor(rows, dtype=torch.long)
+        s = _scores(self.qt[rows], self.kt, self.scale, rows, self.causal, self.tiles)
+        _, p, l, _ = _probs(s, self.quant)
+        return (p @ self.vt) / l[:, None]
+
     def row_stats(self, block=512):
         """(m, l) for every query row."""
         n = self.qt.shape[0]
@@ -203,6 +210,22 @@ def attn_fwd(q, k, v, scale=None, causal=False, quant=True, block=512, kv_tiles=
                 lse[b, h, rows] = lb
                 mm[b, h, rows] = mb
     return o, lse, mm
+
+
+def attn_fwd_hp(q, k, v, scale=None, causal=False, quant=True, block=512):
+    """Whole-tensor auxiliary high-precision output P V~ / l [B, Nq, H, D] (float64):
+    the forward's output with P left unquantized (Q~, K~, V~ and l as in attn_fwd)."""
+    q, k, v = _t(q), _t(k), _t(v)
+    bsz, nq, nh, d = q.shape
+    scale = 1.0 / math.sqrt(d) if scale is None else scale
+    o_hp = torch.zeros(bsz, nq, nh, d, dtype=F64)
+    for b in range(bsz):
+        for h in range(nh):
+            hp = HeadProblem(q, k, v, b, h, scale, causal, quant)
+            for r0 in range(0, nq, block):
+                rows = torch.arange(r0, min(nq, r0 + block))
+                o_hp[b, rows, h] = hp.o_hp_rows(rows)
+    return o_hp
 
 
 def attn_bwd(q, k, v, o, do, scale=None, causal=False, quant=True, delta_mode="o", block=512,

@@ -91,6 +91,19 @@ def test_fwd_rejects_bad_arguments(lib):
     assert _fwd(lib, ws=A + 16) == WORKSPACE
 
 
+def test_fwd_hp_rejects_bad_arguments(lib):
+    def fwd_hp(o_hp=A + 4096, D=128, causal=0, Nkv=128, ws_bytes=None):
+        if ws_bytes is None:
+            ws_bytes = lib.attn_qat_fwd_workspace(1, 128, Nkv, 1, D)
+        return lib.attn_qat_fwd_hp(A, A, A, 1, 128, Nkv, 1, D, 0.1, causal, A, o_hp, A, A,
+                                   ws_bytes, None)
+    assert fwd_hp(o_hp=None) == INVALID
+    assert fwd_hp(o_hp=A + 8) == INVALID
+    assert fwd_hp(D=96) == UNSUPPORTED
+    assert fwd_hp(causal=1, Nkv=256) == UNSUPPORTED
+    assert fwd_hp(ws_bytes=16) == WORKSPACE
+
+
 def test_bwd_rejects_bad_arguments(lib):
     def bwd(dq=A, D=128, Nq=128, Nkv=128, causal=0, ws=A, ws_bytes=None, scale=0.1):
         if ws_bytes is None:

@@ -193,3 +193,36 @@ def test_delta_modes_differ_only_through_delta():
     hp = at.HeadProblem(q, k, v, 0, 0, 0.3)
     assert torch.allclose(hp.dq_rows([3, 9], o[0, [3, 9], 0], do[0, [3, 9], 0], "hp"),
                           b[0][0, [3, 9], 0], rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_aux_output_is_plain_attention_on_the_quantized_operands(causal):
+    """P V~ / l with P unquantized is softmax attention over (Q~, K~, V~): PyTorch's
+    scaled_dot_product_attention on the pinned quantizer's outputs."""
+    q, k, v, _ = _inputs(2, 40, 40, 2, 32, seed=9)
+    scale = 0.2
+    o_hp = at.attn_fwd_hp(q, k, v, scale, causal)
+    qt, kt, vt = (nv.fq(x, 1.0, torch.float32, axis=-1) for x in (q, k, v))
+    ref = _sdpa(qt, kt, vt, scale, causal)
+    assert torch.allclose(o_hp, ref, rtol=0, atol=1e-12)
+    # it differs from the output, whose P is quantized
+    o, _, _ = at.attn_fwd(q, k, v, scale, causal)
+    assert not torch.allclose(o, o_hp, rtol=0, atol=1e-6)
+
+
+def test_aux_output_equals_the_output_with_quantizers_off():
+    q, k, v, _ = _inputs(1, 33, 21, 2, 16, seed=10)
+    o, _, _ = at.attn_fwd(q, k, v, 0.4, quant=False)
+    assert torch.allclose(at.attn_fwd_hp(q, k, v, 0.4, quant=False), o, rtol=0, atol=1e-13)
+
+
+def test_hp_delta_is_delta_from_the_aux_output():
+    """delta_mode 'hp' equals delta_mode 'o' handed the auxiliary output as O: the
+    backward reads O for delta only."""
+    q, k, v, do = _inputs(1, 24, 24, 2, 16, seed=11)
+    o_hp = at.attn_fwd_hp(q, k, v, 0.3)
+    o, _, _ = at.attn_fwd(q, k, v, 0.3)
+    a = at.attn_bwd(q, k, v, o, do, 0.3, delta_mode="hp")
+    b = at.attn_bwd(q, k, v, o_hp, do, 0.3, delta_mode="o")
+    for x, y in zip(a, b):
+        assert torch.allclose(x, y, rtol=0, atol=1e-12)
