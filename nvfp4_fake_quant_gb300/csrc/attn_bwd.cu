@@ -289,8 +289,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!(ok = mbar_wait_warp(s_full, ph, abort))) break;
       tc_fence_after();
       uint32_t ph2[16];  // P as f16x2 pairs (A = P/l feeds no rounding decision)
-      uint32_t ptw[16];  // P~ / l as bf16x2
-      const uint64_t il2 = pk2(inv_l, inv_l);
       {
         tmem_ld32(tmem + lane_base + key_col, r);
         tmem_wait_ld();
@@ -306,31 +304,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!(row_ok && key < Nkv && (!causal || key <= qrow))) x[i] = -INFINITY;
           }
         }
+        float pp0[16], pp1[16];
+        uint32_t ptw0[8], ptw1[8];  // P~ / l as bf16x2
+        pquant16_scaled_bf16(x, inv_l, pp0, ptw0);
+        pquant16_scaled_bf16(x + 16, inv_l, pp1, ptw1);
+        tc_fence_before();
+        // the P~/dS buffer is free once dK of the previous tile is done
+        if (it > 0 && !(ok = mbar_wait_warp(ds_free, ph ^ 1u, abort))) break;
 #pragma unroll
-        for (int hb = 0; hb < 2; ++hb) {
-          float pp[16];
-          uint32_t pt[8];
-          pquant16(x + 16 * hb, pp, pt);
+        for (int ch = 0; ch < 4; ++ch) {
+          const uint32_t* w = ch < 2 ? ptw0 + 4 * ch : ptw1 + 4 * (ch - 2);
+          const uint32_t off = sw128_offset(t, key_col + ch * 8, 128);
+          *reinterpret_cast<uint4*>(pd_smem + off) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        fence_proxy_async_smem();
+        mbar_arrive_warp(pt_full);
+        // P for dS, packed after the P~/l hand-off
 #pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            ph2[hb * 8 + u] = pack_f16x2_rn(pp[2 * u], pp[2 * u + 1]);
-            float a0, a1;
-            up2(mul2(pk2(f16lo_to_f32(pt[u]), f16hi_to_f32(pt[u])), il2), a0, a1);
-            ptw[hb * 8 + u] = pack_bf16(a0, a1);
-          }
+        for (int u = 0; u < 8; ++u) {
+          ph2[u] = pack_f16x2_rn(pp0[2 * u], pp0[2 * u + 1]);
+          ph2[8 + u] = pack_f16x2_rn(pp1[2 * u], pp1[2 * u + 1]);
         }
       }
-      tc_fence_before();
-      // the P~/dS buffer is free once dK of the previous tile is done
-      if (it > 0 && !(ok = mbar_wait_warp(ds_free, ph ^ 1u, abort))) break;
-#pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        const uint32_t off = sw128_offset(t, key_col + ch * 8, 128);
-        *reinterpret_cast<uint4*>(pd_smem + off) =
-            make_uint4(ptw[4 * ch], ptw[4 * ch + 1], ptw[4 * ch + 2], ptw[4 * ch + 3]);
-      }
-      fence_proxy_async_smem();
-      mbar_arrive_warp(pt_full);
       // ---- dS part: dP -> dS = scale * A * (dP - delta), A = P / l
       if (!(ok = mbar_wait_warp(dp_full, ph, abort))) break;
       tc_fence_after();

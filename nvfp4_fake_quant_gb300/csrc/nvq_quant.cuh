@@ -319,4 +319,69 @@ __device__ __forceinline__ void pquant16(const float* x, float (&p)[16], uint32_
   }
 }
 
+__device__ __forceinline__ uint32_t prmt_b32(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
+}
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+__device__ __forceinline__ uint32_t bf16x2_splat(float v) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %1;" : "=r"(r) : "f"(v));
+  return r;
+}
+
+// Eight non-negative E2M1 codes (element i in nibble i, the 3-bit magnitude
+// index in its low bits) decoded to bf16 by byte lookup and multiplied by the
+// bf16x2 factor f2: four bf16x2 pairs, element 2j in the low half of out[j].
+// The bf16 patterns of the magnitudes 0, .5, 1, 1.5, 2, 3, 4, 6 have high
+// bytes 00 3F 3F 3F 40 40 40 40 and low bytes 00 00 80 C0 00 40 80 C0; prmt
+// looks up four codes per instruction (one code nibble selects one byte).
+__device__ __forceinline__ void e2m1x8_bf16_mul(uint32_t codes, uint32_t f2, uint32_t* out) {
+  constexpr uint32_t kLo0 = 0xC0800000u, kLo1 = 0xC0804000u;
+  constexpr uint32_t kHi0 = 0x3F3F3F00u, kHi1 = 0x40404040u;
+#pragma unroll
+  for (int hv = 0; hv < 2; ++hv) {
+    const uint32_t sel = codes >> (16 * hv);  // four code nibbles in the low 16 bits
+    const uint32_t lo = prmt_b32(kLo0, kLo1, sel), hi = prmt_b32(kHi0, kHi1, sel);
+    out[2 * hv] = mul_bf16x2(prmt_b32(lo, hi, 0x5140u), f2);      // elements 0, 1
+    out[2 * hv + 1] = mul_bf16x2(prmt_b32(lo, hi, 0x7362u), f2);  // elements 2, 3
+  }
+}
+
+// The backward's P~ / l for one 16-key block.  The quantization decisions are
+// pquant16's (p = 2^x, s = E4M3(amax/6), codes = E2M1(p * rcp(s))), so the
+// codes and scale equal the forward's bit for bit; the codes are then decoded
+// to bf16 and multiplied by bf16(s * inv_l).  Also returns p (fp32).
+__device__ __forceinline__ void pquant16_scaled_bf16(const float* x, float inv_l, float (&p)[16],
+                                                     uint32_t (&out)[8]) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) p[i] = ex2_f32(x[i]);
+  float a = max3f(p[0], p[1], p[2]);
+  a = max3f(a, p[3], p[4]);
+  a = max3f(a, p[5], p[6]);
+  a = max3f(a, p[7], p[8]);
+  a = max3f(a, p[9], p[10]);
+  a = max3f(a, p[11], p[12]);
+  a = max3f(a, p[13], p[14]);
+  a = fmaxf(a, p[15]);
+  const uint32_t sb = e4m3_rn_sat(a * (1.0f / 6.0f));
+  const float s = f16lo_to_f32(e4m3_to_f16x2(sb));
+  const float inv = s > 0.f ? rcp_approx(s) : 0.f;
+  const uint64_t inv2 = pk2(inv, inv);
+  float q0[8], q1[8];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    up2(mul2(pk2(p[2 * j], p[2 * j + 1]), inv2), q0[2 * j], q0[2 * j + 1]);
+    up2(mul2(pk2(p[8 + 2 * j], p[8 + 2 * j + 1]), inv2), q1[2 * j], q1[2 * j + 1]);
+  }
+  const uint32_t f2 = bf16x2_splat(s * inv_l);
+  e2m1x8_bf16_mul(e2m1x8(q0), f2, out);
+  e2m1x8_bf16_mul(e2m1x8(q1), f2, out + 4);
+}
+
 }  // namespace nvq
