@@ -269,6 +269,63 @@ nvq_status attn_qat_bwd_sparse(const void* q, const void* k, const void* v, cons
                                float scale, void* ws, size_t ws_bytes, nvq_stream_t stream);
 
 /* ------------------------------------------------------------------------ */
+/* NVFP4 linear ("nvfp4_qad.py": nvfp4_gemm and _NVFP4STE)                   */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * Bytes of the E4M3 scales of a [rows, cols] operand in the 128x4 tiled layout
+ * that block-scaled FP4 GEMMs read (cols % 16 == 0): rows padded to 128, the
+ * cols/16 blocks to 4; 512-byte tiles of 128 rows x 4 blocks, ordered by row
+ * tile then block tile; inside a tile the scale of (r, c) is at byte
+ * (r % 32) * 16 + (r / 32 % 4) * 4 + c % 4.  0 for invalid sizes.
+ */
+size_t nvfp4_tiled_scale_bytes(int64_t rows, int64_t cols);
+
+/*
+ * NVFP4 quantization for the FP4 GEMM: the decisions of nvfp4_fake_quant
+ * (global_sf: device fp32 scalar or NULL = 1.0), written as
+ *   codes   uint8 [rows, cols/2] row-major, two 4-bit codes per byte, element
+ *           2i in the low nibble (sign << 3 | E2M1 magnitude index)
+ *   scales  nvfp4_tiled_scale_bytes(rows, cols) bytes in the tiled layout,
+ *           padding entries zero
+ * x bf16 [rows, cols] with row stride ld_x (elements, % 8 == 0); pointers
+ * 16-byte aligned.  NVQ_ERR_INVALID on bad arguments.
+ */
+nvq_status nvfp4_quantize_tiled(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
+                                const float* global_sf, uint8_t* codes, uint8_t* scales,
+                                nvq_stream_t stream);
+
+/*
+ * Forward of the NVFP4 linear: out = x~ w~^T (+ bias), x bf16 [M, K], w bf16
+ * [N, K], bias bf16 [N] or NULL, out bf16 [M, N], all contiguous and 16-byte
+ * aligned.  Both operands are quantized (nvfp4_quantize_tiled) under their
+ * global scales; x_global_sf / w_global_sf are device fp32 scalars, or NULL for
+ * 448*6/amax of the operand itself (nvfp4_global_sf).  The FP4 block-scaled GEMM
+ * (cuBLASLt) runs with alpha = 1 / (gsf_w * gsf_x) and fp32 accumulation, so
+ * out is the product of the dequantized operands, rounded to bf16.
+ * K % 64 == 0 and N % 16 == 0, else NVQ_ERR_UNSUPPORTED (also when cuBLASLt
+ * offers no algorithm for the shape).  ws: nvfp4_linear_workspace(M, N, K)
+ * bytes, 256-byte aligned (codes, scales, global scales, GEMM workspace).
+ */
+size_t nvfp4_linear_workspace(int64_t M, int64_t N, int64_t K);
+nvq_status nvfp4_linear_fwd(const void* x, const void* w, const void* bias, int64_t M, int64_t N,
+                            int64_t K, const float* x_global_sf, const float* w_global_sf,
+                            void* out, void* ws, size_t ws_bytes, nvq_stream_t stream);
+
+/*
+ * Straight-through backward of the NVFP4 linear: the full-precision linear
+ * gradients grad_x = grad_out w (bf16 [M, K]), grad_w = grad_out^T x (bf16
+ * [N, K]), grad_b = column sums of grad_out (bf16 [N]); each output may be NULL
+ * (not computed).  BF16 GEMMs with fp32 accumulation (cuBLASLt); the bias sums
+ * are fp32.  Sizes and alignment as in the forward; ws:
+ * nvfp4_linear_bwd_workspace(M, N, K) bytes, 256-byte aligned.
+ */
+size_t nvfp4_linear_bwd_workspace(int64_t M, int64_t N, int64_t K);
+nvq_status nvfp4_linear_bwd(const void* grad_out, const void* x, const void* w, int64_t M,
+                            int64_t N, int64_t K, void* grad_x, void* grad_w, void* grad_b,
+                            void* ws, size_t ws_bytes, nvq_stream_t stream);
+
+/* ------------------------------------------------------------------------ */
 /* Per-kernel device timing (a profiling aid; no counterpart in the pages)  */
 /* ------------------------------------------------------------------------ */
 
@@ -281,7 +338,8 @@ enum {
   NVQ_KERNEL_BWD_DQ = 4,     /* backward, query-outer dQ kernel */
   NVQ_KERNEL_GLOBAL_SF = 5,  /* static global scale (amax reduction and finalize) */
   NVQ_KERNEL_VSA = 6,        /* block-sparse support: token reorder, block selection */
-  NVQ_KERNEL_KINDS = 7
+  NVQ_KERNEL_LINEAR = 7,     /* NVFP4 linear: the cuBLASLt GEMMs and the bias gradient */
+  NVQ_KERNEL_KINDS = 8
 };
 
 /*

@@ -42,6 +42,15 @@ SIGNATURES = {
     "attn_qat_bwd_builtin_scratch": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                              c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int,
                                              c_int, c_int, c_int, c_float, c_int, c_void_p]),
+    "nvfp4_tiled_scale_bytes": (c_size_t, [c_int64, c_int64]),
+    "nvfp4_quantize_tiled": (c_int, [c_void_p, c_int64, c_int64, c_int64, c_void_p, c_void_p,
+                                     c_void_p, c_void_p]),
+    "nvfp4_linear_workspace": (c_size_t, [c_int64, c_int64, c_int64]),
+    "nvfp4_linear_fwd": (c_int, [c_void_p, c_void_p, c_void_p, c_int64, c_int64, c_int64,
+                                 c_void_p, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
+    "nvfp4_linear_bwd_workspace": (c_size_t, [c_int64, c_int64, c_int64]),
+    "nvfp4_linear_bwd": (c_int, [c_void_p, c_void_p, c_void_p, c_int64, c_int64, c_int64,
+                                 c_void_p, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
     "vsa_reorder": (c_int, [c_void_p, c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int, c_int,
                             c_int, c_void_p, c_void_p]),
     "vsa_select_workspace": (c_size_t, [c_int, c_int, c_int, c_int]),

@@ -187,7 +187,7 @@ def attn_qat_bwd(q, k, v, o, stats, do, scale=None, causal=False, dq=None, dk=No
 
 # Kernel kinds of nvq_timing_read (include/nvfp4attn.h, NVQ_KERNEL_*)
 KERNEL_KINDS = {"quantize": 0, "attn_fwd": 1, "bwd_delta": 2, "bwd_dkdv": 3, "bwd_dq": 4,
-                "global_sf": 5, "vsa": 6}
+                "global_sf": 5, "vsa": 6, "linear": 7}
 
 
 def timing_enable(on: bool = True) -> None:

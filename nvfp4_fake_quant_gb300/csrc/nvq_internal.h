@@ -20,6 +20,13 @@ cudaError_t launch_fake_quant(const void* x, int64_t rows, int64_t cols, int64_t
                               const float* gsf, int mode, void* out, int64_t ld_out,
                               uint8_t* scales, int64_t ld_s, uint8_t* codes, int64_t ld_c,
                               cudaStream_t stream);
+// Packed E2M1 codes (row-major, cols/2 bytes a row) and E4M3 scales in the 128x4
+// tiled layout of block-scaled FP4 GEMMs (tiled_scale_bytes(rows, cols) bytes,
+// padding zeroed); gsf NULL = unit global scale.
+size_t tiled_scale_bytes(int64_t rows, int64_t cols);
+cudaError_t launch_quant_tiled(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
+                               const float* gsf, uint8_t* codes, uint8_t* scales,
+                               cudaStream_t stream);
 cudaError_t launch_global_sf(const void* x, int64_t rows, int64_t cols, int64_t ld_x, float* gsf,
                              cudaStream_t stream);
 

@@ -104,6 +104,31 @@ __global__ void __launch_bounds__(256) fake_quant_rows_kernel(
   }
 }
 
+// Byte offset of the scale of (row r, 16-element block cb) in the 128x4 tiled
+// layout of block-scaled FP4 GEMMs: 512-byte tiles of 128 rows x 4 blocks,
+// tiles ordered by row tile, then block tile (n_bt tiles per row tile); inside
+// a tile, row r sits at (r % 32) * 16 + (r / 32 % 4) * 4 and block cb at cb % 4.
+__device__ __forceinline__ int64_t tiled_scale_offset(int64_t r, int64_t cb, int64_t n_bt) {
+  return ((r >> 7) * n_bt + (cb >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (cb & 3);
+}
+
+// Packed codes (row-major, cols/2 bytes per row) and scales in the tiled layout;
+// rows over grid y, blocks of a row over grid x.
+template <int MODE>
+__global__ void __launch_bounds__(256) quant_tiled_kernel(
+    const uint16_t* __restrict__ x, int64_t rows, int64_t nbc, int64_t ld_x,
+    const float* __restrict__ gsf, uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+  const float g = (MODE == kStaticBf16) ? *gsf : 1.0f;
+  const int64_t cstep = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int64_t n_bt = (nbc + 3) / 4;
+  for (int64_t r = blockIdx.y; r < rows; r += gridDim.y) {
+    for (int64_t cb = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; cb < nbc;
+         cb += cstep)
+      quant_block<MODE>(load_block(x + r * ld_x + cb * 16), g, nullptr,
+                        scales + tiled_scale_offset(r, cb, n_bt), codes + r * (nbc * 8) + cb * 8);
+  }
+}
+
 // amax(|x|) as the unsigned bit pattern of a non-negative float (monotone).
 __global__ void __launch_bounds__(256) amax_kernel(const uint16_t* __restrict__ x, int64_t rows,
                                                    int64_t cols, int64_t ld_x,
@@ -223,6 +248,33 @@ cudaError_t launch_fake_quant(const void* x, int64_t rows, int64_t cols, int64_t
           xs, rows, nbc, ld_x, gsf, os, ld_out, scales, ld_s, codes, ld_c);
       break;
   }
+  return cudaGetLastError();
+}
+
+size_t tiled_scale_bytes(int64_t rows, int64_t cols) {
+  const int64_t nbc = cols / 16;
+  return static_cast<size_t>((rows + 127) / 128 * 128) * static_cast<size_t>((nbc + 3) / 4 * 4);
+}
+
+cudaError_t launch_quant_tiled(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
+                               const float* gsf, uint8_t* codes, uint8_t* scales,
+                               cudaStream_t stream) {
+  const int64_t nbc = cols / 16;
+  // padding rows of the last row tile and padding blocks of the last block tile
+  // hold zero scales
+  if (rows % 128 != 0 || nbc % 4 != 0) {
+    const cudaError_t e = cudaMemsetAsync(scales, 0, tiled_scale_bytes(rows, cols), stream);
+    if (e != cudaSuccess) return e;
+  }
+  const int threads = 256;
+  const int64_t gx = std::min<int64_t>((nbc + threads - 1) / threads, 64);
+  const int64_t gy = std::max<int64_t>(1, std::min<int64_t>({rows, 65535, grid_for(rows * nbc, threads) / gx + 1}));
+  const dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(gy));
+  const auto* xs = static_cast<const uint16_t*>(x);
+  if (gsf != nullptr)
+    quant_tiled_kernel<kStaticBf16><<<grid, threads, 0, stream>>>(xs, rows, nbc, ld_x, gsf, codes, scales);
+  else
+    quant_tiled_kernel<kUnitBf16><<<grid, threads, 0, stream>>>(xs, rows, nbc, ld_x, gsf, codes, scales);
   return cudaGetLastError();
 }
 

@@ -180,7 +180,7 @@ def test_timing_hook_arguments(lib):
     n, ms = ctypes.c_int64(-1), ctypes.c_double(-1.0)
     pn, pms = ctypes.addressof(n), ctypes.addressof(ms)
     assert lib.nvq_timing_enable(2) == INVALID
-    assert lib.nvq_timing_read(7, pn, pms) == INVALID
+    assert lib.nvq_timing_read(8, pn, pms) == INVALID
     assert lib.nvq_timing_read(-1, pn, pms) == INVALID
     assert lib.nvq_timing_read(0, None, pms) == INVALID
     assert lib.nvq_timing_enable(1) == OK

@@ -157,7 +157,7 @@ def test_kernel_timing_hook_counts_every_launch():
         api.timing_enable(False)
     assert {k: n for k, (n, _) in got.items()} == {
         "quantize": 6, "attn_fwd": 1, "bwd_delta": 1, "bwd_dkdv": 1, "bwd_dq": 1, "global_sf": 0,
-        "vsa": 0}
+        "vsa": 0, "linear": 0}
     assert all(ms > 0 for n, ms in got.values() if n)
     assert sum(ms for _, ms in got.values()) <= wall_ms
     assert api.timing_read()["attn_fwd"] == (0, 0.0)  # disabled: records discarded
