@@ -15,6 +15,8 @@ Modules
                dense or block-sparse (a list of key tiles per query tile).
 ``vsa``        video sparse attention: cube token order, the top-k formula and
                the cube-mean score selection of key tiles.
+``linear``     the NVFP4 linear: quantized forward with the FP4 GEMM's global-scale
+               alpha, straight-through backward, the 128 x 4 tiled scale layout.
 
 Sources (web pages on the subject; cited by title and section):
   * "nvfp4_qad.py" (FastVideo ``fastvideo/layers/quantization/nvfp4_qad.py``):
