@@ -408,6 +408,66 @@ def hp_bench(peaks, stream, steps, inp, q, k, v, do, wsf, wsb):
                         for name, (c, t) in kt.items() if c}}
 
 
+def linear_bench(peaks, stream, steps):
+    """The NVFP4 linear on the Wan FFN up-projection (x [25088, 1536], w [8960, 1536],
+    bias): forward = global scales of x and w, tiled quantization of both, FP4
+    block-scaled GEMM with bias; backward = grad_x, grad_w (BF16 GEMMs) and the bias
+    gradient.  The FP4 GEMM is measured against 6x the measured BF16 peak (the
+    nominal FP4:BF16 dense ratio 13.5:2.25)."""
+    import torch
+
+    from nvfp4_fake_quant_gb300 import api, workloads
+    inp = workloads.wan_ffn_up()
+    x, w, b, g = (t.cuda() for t in (inp.x, inp.w, inp.bias, inp.grad))
+    m, k = x.shape
+    n = w.shape[0]
+    out = torch.empty((m, n), dtype=torch.bfloat16, device=x.device)
+    wsf = torch.empty(api._lib.load().nvfp4_linear_workspace(m, n, k), dtype=torch.uint8,
+                      device=x.device)
+    wsb = torch.empty(api._lib.load().nvfp4_linear_bwd_workspace(m, n, k), dtype=torch.uint8,
+                      device=x.device)
+
+    def fwd():
+        api.nvfp4_linear_fwd(x, w, b, out=out, workspace=wsf)
+
+    def bwd():
+        api.nvfp4_linear_bwd(g, x, w, workspace=wsb)
+
+    for _ in range(3):
+        fwd()
+        bwd()
+    torch.cuda.synchronize()
+    api.timing_enable(True)
+    fwd_ms = time_events(fwd, steps, stream)
+    kt_f = api.timing_read()
+    api.timing_enable(False)
+    api.timing_enable(True)
+    bwd_ms = time_events(bwd, steps, stream)
+    kt_b = api.timing_read()
+    api.timing_enable(False)
+    if api.device_status() != 0:
+        raise RuntimeError("device error (linear)")
+    flops = 2.0 * m * n * k
+    fp4_peak = 6.0 * peaks["bf16_tflops"]
+    gemm_f = kt_f["linear"][1] / kt_f["linear"][0]
+    quant_f = kt_f["quantize"][1] / max(1, kt_f["quantize"][0])
+    gemm_b = kt_b["linear"][1] / steps
+    return {"workload": "Wan FFN up-projection: x [25088, 1536], w [8960, 1536], bias; "
+                        "N(0,1) inputs, w N(0, 1/1536) (seed 6)",
+            "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
+            "fwd_tflops": flops / (fwd_ms * 1e-3) / 1e12,
+            "bwd_tflops": 2 * flops / (bwd_ms * 1e-3) / 1e12,
+            "fp4_gemm_ms": gemm_f, "fp4_gemm_tflops": flops / (gemm_f * 1e-3) / 1e12,
+            "fp4_gemm_frac_of_fp4_peak": flops / (gemm_f * 1e-3) / 1e12 / fp4_peak,
+            "fp4_peak_tflops": fp4_peak, "fp4_peak_source": "6 x measured bf16 (nominal ratio)",
+            "quantize_ms_per_launch": quant_f,
+            "bwd_gemm_tflops": 2 * flops / (gemm_b * 1e-3) / 1e12,
+            "kernels_fwd": {name: {"launches": c / steps, "avg_ms": t / c}
+                            for name, (c, t) in kt_f.items() if c},
+            "kernels_bwd": {name: {"launches": c / steps, "avg_ms": t / c}
+                            for name, (c, t) in kt_b.items() if c}}
+
+
 def run_ours(args):
     import torch
 
@@ -502,6 +562,8 @@ def run_ours(args):
               if rank == 0 and not args.skip_sparse and (n, h) == (25088, 12) else None)
     hp = (hp_bench(peaks, stream, max(3, args.steps), inp, q, k, v, do, wsf, wsb)
           if rank == 0 and not args.skip_hp else None)
+    lin = linear_bench(peaks, stream, max(3, args.steps)) \
+        if rank == 0 and not args.skip_linear else None
 
     peak_t = peaks["bf16_tflops"]
     k_total = sum(ms for _, ms in ktimes.values())
@@ -546,6 +608,8 @@ def run_ours(args):
         line["block_sparse"] = sparse
     if hp is not None:
         line["aux_output"] = hp
+    if lin is not None:
+        line["nvfp4_linear"] = lin
     if rank == 0 and not args.skip_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_rows)
     if rank == 0:
@@ -568,6 +632,8 @@ def main(argv=None):
     ap.add_argument("--skip-e2e", action="store_true")
     ap.add_argument("--skip-sparse", action="store_true",
                     help="skip the block-sparse (VSA) workload's extra measurement")
+    ap.add_argument("--skip-linear", action="store_true",
+                    help="skip the NVFP4 linear (Wan FFN up-projection) measurement")
     ap.add_argument("--skip-hp", action="store_true",
                     help="skip the measurement of the step with the auxiliary output")
     ap.add_argument("--quantizer-only", action="store_true",

@@ -185,6 +185,117 @@ def attn_qat_bwd(q, k, v, o, stats, do, scale=None, causal=False, dq=None, dk=No
     return dq, dk, dv
 
 
+# ------------------------------------------------------------------ NVFP4 linear
+def nvfp4_tiled_scale_bytes(rows: int, cols: int) -> int:
+    return int(_lib.load().nvfp4_tiled_scale_bytes(rows, cols))
+
+
+def nvfp4_quantize_tiled(x: torch.Tensor, global_sf: torch.Tensor | None = None,
+                         codes: torch.Tensor | None = None, scales: torch.Tensor | None = None):
+    """Packed E2M1 codes (uint8 [rows, cols/2]) and E4M3 scales in the 128x4 tiled
+    layout of block-scaled FP4 GEMMs (uint8, nvfp4_tiled_scale_bytes) of a bf16
+    matrix x [rows, cols]."""
+    _check(x, "x")
+    rows, cols, ld = _rows_ld(x)
+    if codes is None:
+        codes = torch.empty((rows, cols // 2), dtype=torch.uint8, device=x.device)
+    if scales is None:
+        scales = torch.empty(nvfp4_tiled_scale_bytes(rows, cols), dtype=torch.uint8,
+                             device=x.device)
+    _lib.call("nvfp4_quantize_tiled", _ptr(x), rows, cols, ld, _opt_ptr(global_sf),
+              _ptr(codes), _ptr(scales), _stream_ptr(x))
+    return codes, scales
+
+
+def _opt_ptr(t):
+    if t is None:
+        return None
+    _check(t, "global_sf", torch.float32)
+    return _ptr(t)
+
+
+def _linear_dims(x, w):
+    _check(x, "x")
+    _check(w, "w")
+    if x.dim() != 2 or w.dim() != 2 or x.shape[1] != w.shape[1]:
+        raise ValueError(f"x [M, K] and w [N, K] expected, got {tuple(x.shape)}, {tuple(w.shape)}")
+    if not (x.is_contiguous() and w.is_contiguous()):
+        raise ValueError("x and w must be contiguous")
+    return x.shape[0], w.shape[0], x.shape[1]
+
+
+def nvfp4_linear_fwd(x, w, bias=None, x_global_sf=None, w_global_sf=None, out=None,
+                     workspace=None):
+    """out [M, N] bf16 = x~ w~^T (+ bias): both operands NVFP4-quantized under
+    their global scales (None: 448*6/amax of the operand), FP4 block-scaled GEMM."""
+    m, n, k = _linear_dims(x, w)
+    if bias is not None:
+        _check(bias, "bias")
+    if out is None:
+        out = torch.empty((m, n), dtype=BF16, device=x.device)
+    ws = _workspace(int(_lib.load().nvfp4_linear_workspace(m, n, k)), x.device, workspace)
+    _lib.call("nvfp4_linear_fwd", _ptr(x), _ptr(w), None if bias is None else _ptr(bias), m, n, k,
+              _opt_ptr(x_global_sf), _opt_ptr(w_global_sf), _ptr(out), _ptr(ws),
+              ws.numel() * ws.element_size(), _stream_ptr(x))
+    return out
+
+
+def nvfp4_linear_bwd(grad, x, w, need_bias=True, workspace=None):
+    """Straight-through gradients (grad_x [M, K], grad_w [N, K], grad_b [N] or None), bf16."""
+    m, n, k = _linear_dims(x, w)
+    _check(grad, "grad")
+    if tuple(grad.shape) != (m, n) or not grad.is_contiguous():
+        raise ValueError("grad must be a contiguous [M, N] tensor")
+    gx = torch.empty_like(x)
+    gw = torch.empty_like(w)
+    gb = torch.empty((n,), dtype=BF16, device=x.device) if need_bias else None
+    ws = _workspace(int(_lib.load().nvfp4_linear_bwd_workspace(m, n, k)), x.device, workspace)
+    _lib.call("nvfp4_linear_bwd", _ptr(grad), _ptr(x), _ptr(w), m, n, k, _ptr(gx), _ptr(gw),
+              None if gb is None else _ptr(gb), _ptr(ws), ws.numel() * ws.element_size(),
+              _stream_ptr(x))
+    return gx, gw, gb
+
+
+class NVFP4LinearFunction(torch.autograd.Function):
+    """Forward: the NVFP4 linear (both operands quantized, FP4 GEMM); backward: the
+    full-precision linear gradients (straight-through)."""
+
+    @staticmethod
+    def forward(ctx, x, w, bias, x_global_sf):
+        shape = x.shape
+        x2 = x.reshape(-1, shape[-1]).contiguous()
+        out = nvfp4_linear_fwd(x2, w.contiguous(), bias, x_global_sf)
+        ctx.save_for_backward(x2, w)
+        ctx.has_bias, ctx.shape = bias is not None, shape
+        return out.view(*shape[:-1], w.shape[0])
+
+    @staticmethod
+    def backward(ctx, grad):
+        x2, w = ctx.saved_tensors
+        g2 = grad.reshape(-1, grad.shape[-1]).contiguous()
+        gx, gw, gb = nvfp4_linear_bwd(g2, x2, w.contiguous(), ctx.has_bias)
+        return gx.view(ctx.shape), gw, gb, None
+
+
+class NVFP4Linear(torch.nn.Module):
+    """A bf16 linear layer whose forward runs as the NVFP4 GEMM (weight quantized
+    under 448*6/amax(w) at every call, input under ``input_global_sf`` or its own
+    amax) and whose backward is straight-through."""
+
+    def __init__(self, in_features: int, out_features: int, bias: bool = True,
+                 input_global_sf: torch.Tensor | None = None, device=None):
+        super().__init__()
+        self.weight = torch.nn.Parameter(torch.empty(out_features, in_features, dtype=BF16,
+                                                     device=device))
+        self.bias = torch.nn.Parameter(torch.zeros(out_features, dtype=BF16, device=device)) \
+            if bias else None
+        self.input_global_sf = input_global_sf
+        torch.nn.init.normal_(self.weight, std=in_features ** -0.5)
+
+    def forward(self, x):
+        return NVFP4LinearFunction.apply(x, self.weight, self.bias, self.input_global_sf)
+
+
 # Kernel kinds of nvq_timing_read (include/nvfp4attn.h, NVQ_KERNEL_*)
 KERNEL_KINDS = {"quantize": 0, "attn_fwd": 1, "bwd_delta": 2, "bwd_dkdv": 3, "bwd_dq": 4,
                 "global_sf": 5, "vsa": 6, "linear": 7}

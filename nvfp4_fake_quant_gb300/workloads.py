@@ -17,6 +17,10 @@ metadata.json" architecture, latent grids from its training geometry):
   wan25088    B=1, H=12, D=128, N=25088 (16x28x56 latent tokens); Q, K N(0,1)
               with every (token, head) row scaled to unit RMS over D; V, dO
               N(0,1); seed 2
+  wan_ffn_up  the NVFP4 linear on the Wan FFN up-projection: x [25088, 1536]
+              (the 16x28x56 latent tokens, hidden 12 x 128) N(0,1), w [8960, 1536]
+              N(0, 1/1536), bias [8960] N(0, 0.01), grad [25088, 8960] N(0,1);
+              seed 6 (ffn_dim 8960 from the metadata's architecture)
   wan32760    B=1, H=12, D=128, N=32760 (21x30x52); Q, K N(0,1) times a
               per-(head, channel) factor exp(N(0,1)) (one set for Q, one for
               K); V, dO N(0,1); seed 3
@@ -122,3 +126,27 @@ def quant_matrix(rows=4096, cols=4096, seed=1, outlier_frac=0.01, outlier_mul=50
 def random_matrix(rows, cols, seed, scale=1.0) -> torch.Tensor:
     """Plain N(0, scale^2) bf16 matrix (parity cases of other sizes)."""
     return (_randn(_gen(seed), rows, cols) * scale).to(BF16)
+
+
+WAN_HIDDEN, WAN_FFN = 1536, 8960
+
+
+@dataclass
+class LinearInputs:
+    x: torch.Tensor      # bf16 [M, K]
+    w: torch.Tensor      # bf16 [N, K]
+    bias: torch.Tensor   # bf16 [N]
+    grad: torch.Tensor   # bf16 [M, N]
+
+
+def linear_inputs(m, n, k, seed) -> LinearInputs:
+    g = _gen(seed)
+    x = _randn(g, m, k).to(BF16)
+    w = (_randn(g, n, k) * k ** -0.5).to(BF16)
+    bias = (_randn(g, n) * 0.1).to(BF16)
+    grad = _randn(g, m, n).to(BF16)
+    return LinearInputs(x, w, bias, grad)
+
+
+def wan_ffn_up() -> LinearInputs:
+    return linear_inputs(25088, WAN_FFN, WAN_HIDDEN, seed=6)
