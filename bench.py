@@ -410,7 +410,8 @@ def hp_bench(peaks, stream, steps, inp, q, k, v, do, wsf, wsb):
 
 def linear_bench(peaks, stream, steps):
     """The NVFP4 linear on the Wan FFN up-projection (x [25088, 1536], w [8960, 1536],
-    bias): forward = global scales of x and w, tiled quantization of both, FP4
+    bias): forward = the weight's global scale, tiled quantization of x (under its
+    calibrated global scale) and w, FP4
     block-scaled GEMM with bias; backward = grad_x, grad_w (BF16 GEMMs) and the bias
     gradient.  The FP4 GEMM is measured against 6x the measured BF16 peak (the
     nominal FP4:BF16 dense ratio 13.5:2.25)."""
@@ -427,8 +428,12 @@ def linear_bench(peaks, stream, steps):
     wsb = torch.empty(api._lib.load().nvfp4_linear_bwd_workspace(m, n, k), dtype=torch.uint8,
                       device=x.device)
 
+    # the input's global scale is a calibrated constant (computed once, as the
+    # reference's input_global_sf); the weight's is taken from w at every call
+    x_sf = api.nvfp4_global_sf(x)
+
     def fwd():
-        api.nvfp4_linear_fwd(x, w, b, out=out, workspace=wsf)
+        api.nvfp4_linear_fwd(x, w, b, x_global_sf=x_sf, out=out, workspace=wsf)
 
     def bwd():
         api.nvfp4_linear_bwd(g, x, w, workspace=wsb)

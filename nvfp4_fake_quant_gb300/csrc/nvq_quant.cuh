@@ -18,7 +18,9 @@
 //                   t*s < 2^(es+4)), which an error of one ulp cannot cross.
 //  * quant16_static IEEE fp32 products and quotients (mul.rn / div.rn) in the
 //                   order of the definition: bit-identical to any IEEE fp32
-//                   evaluation of the same steps.
+//                   evaluation of the same steps.  quant16_static_fast takes
+//                   the same decisions through reciprocals, with a check that
+//                   sends the rare doubtful block back to quant16_static.
 //  * pquant16       the softmax probabilities inside attention (fp32 inputs):
 //                   reciprocal and product without snapping.  The forward and
 //                   the backward run this same code on bit-identical inputs.
@@ -382,6 +384,68 @@ __device__ __forceinline__ void pquant16_scaled_bf16(const float* x, float inv_l
   const uint32_t f2 = bf16x2_splat(s * inv_l);
   e2m1x8_bf16_mul(e2m1x8(q0), f2, out);
   e2m1x8_bf16_mul(e2m1x8(q1), f2, out + 4);
+}
+
+// Static global scale, fast form.  The same decisions as quant16_static, taken
+// on products with reciprocals instead of IEEE quotients wherever that cannot
+// change them: a product q = RN(x*g) * rcp(s) is within 2^-22 (relative) of the
+// IEEE quotient, so when q * (1 - 2^-20) and q * (1 + 2^-20) get the same E2M1
+// code (the code is monotone in its argument), the IEEE quotient, which lies
+// between them, gets that code too.  Likewise each output value o =
+// (code * s) * RN(1/g) is checked through the bf16 roundings of o * (1 -+ 2^-21).
+// A block where any check fails is redone by quant16_static.  inv_g = RN(1/g).
+// The IEEE path as a call of its own, so that its registers stay out of the
+// fast path's allocation.
+static __device__ __noinline__ Q16 quant16_static_cold(const uint32_t (&x)[8], float g) {
+  return quant16_static(x, g);
+}
+
+template <bool OUT>
+__device__ __forceinline__ Q16 quant16_static_fast(const uint32_t (&x)[8], float g, float inv_g) {
+  Q16 r;
+  const float amax = amax16_bf16(x);
+  const float t = __fdiv_rn(__fmul_rn(amax, g), 6.0f);
+  r.sbyte = e4m3_rn_sat(t);
+  const float s = f16lo_to_f32(e4m3_to_f16x2(r.sbyte));
+  const float inv = s > 0.f ? rcp_approx(s) : 0.f;
+  const uint64_t g2 = pk2(g, g), inv2 = pk2(inv, inv);
+  const uint64_t dn2 = pk2(1.0f - 0x1p-20f, 1.0f - 0x1p-20f);
+  const uint64_t up2f = pk2(1.0f + 0x1p-20f, 1.0f + 0x1p-20f);
+  bool ok = true;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    float ql[8], qh[8];
+#pragma unroll
+    for (int jj = 0; jj < 4; ++jj) {
+      const uint32_t w = x[4 * h + jj];
+      const uint64_t q2 = mul2(mul2(pk2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u)), g2), inv2);
+      up2(mul2(q2, dn2), ql[2 * jj], ql[2 * jj + 1]);
+      up2(mul2(q2, up2f), qh[2 * jj], qh[2 * jj + 1]);
+    }
+    const uint32_t c = e2m1x8(ql);
+    ok = ok && c == e2m1x8(qh);
+    r.codes[h] = c;
+    if constexpr (OUT) {
+      uint32_t hv[4];
+      e2m1x8_to_f16x2(c, hv);
+      const uint64_t s2 = pk2(s, s), ig2 = pk2(inv_g, inv_g);
+      const uint64_t dn21 = pk2(1.0f - 0x1p-21f, 1.0f - 0x1p-21f);
+      const uint64_t up21 = pk2(1.0f + 0x1p-21f, 1.0f + 0x1p-21f);
+#pragma unroll
+      for (int jj = 0; jj < 4; ++jj) {
+        const uint64_t o2 = mul2(mul2(pk2(f16lo_to_f32(hv[jj]), f16lo_to_f32(hv[jj] >> 16)), s2), ig2);
+        float a0, a1, b0, b1;
+        up2(mul2(o2, dn21), a0, a1);
+        up2(mul2(o2, up21), b0, b1);
+        __nv_bfloat162 ba = __floats2bfloat162_rn(a0, a1), bb = __floats2bfloat162_rn(b0, b1);
+        const uint32_t wa = *reinterpret_cast<uint32_t*>(&ba), wb = *reinterpret_cast<uint32_t*>(&bb);
+        ok = ok && wa == wb;
+        r.out[4 * h + jj] = wa | (x[4 * h + jj] & 0x80008000u);
+      }
+    }
+  }
+  if (!ok) r = quant16_static_cold(x, g);
+  return r;
 }
 
 }  // namespace nvq

@@ -41,7 +41,9 @@ __device__ __forceinline__ void quant_block(const Block16& v, const float g,
   const uint32_t xv[8] = {v.lo.x, v.lo.y, v.lo.z, v.lo.w, v.hi.x, v.hi.y, v.hi.z, v.hi.w};
   Q16 q;
   if constexpr (MODE == kStaticBf16) {
-    q = quant16_static(xv, g);
+    const float inv_g = __frcp_rn(g);
+    q = out != nullptr ? quant16_static_fast<true>(xv, g, inv_g)
+                       : quant16_static_fast<false>(xv, g, inv_g);
   } else {
     q = quant16_unit<MODE == kUnitF16>(xv);
   }
@@ -112,21 +114,70 @@ __device__ __forceinline__ int64_t tiled_scale_offset(int64_t r, int64_t cb, int
   return ((r >> 7) * n_bt + (cb >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (cb & 3);
 }
 
-// Packed codes (row-major, cols/2 bytes per row) and scales in the tiled layout;
-// rows over grid y, blocks of a row over grid x.
+// Packed codes (row-major, cols/2 bytes per row) and scales in the tiled layout.
+// A flat grid-stride loop over the rows*nbc blocks (32-bit index arithmetic
+// when the count fits), each thread loading two blocks before quantizing.
 template <int MODE>
 __global__ void __launch_bounds__(256) quant_tiled_kernel(
     const uint16_t* __restrict__ x, int64_t rows, int64_t nbc, int64_t ld_x,
     const float* __restrict__ gsf, uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
   const float g = (MODE == kStaticBf16) ? *gsf : 1.0f;
-  const int64_t cstep = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int64_t total = rows * nbc;
+  const bool narrow = total <= 0xFFFFFFFFll;
+  const uint32_t nbc32 = static_cast<uint32_t>(nbc);
+  const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
   const int64_t n_bt = (nbc + 3) / 4;
-  for (int64_t r = blockIdx.y; r < rows; r += gridDim.y) {
-    for (int64_t cb = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; cb < nbc;
-         cb += cstep)
-      quant_block<MODE>(load_block(x + r * ld_x + cb * 16), g, nullptr,
-                        scales + tiled_scale_offset(r, cb, n_bt), codes + r * (nbc * 8) + cb * 8);
+  auto split = [&](int64_t i, int64_t& r, int64_t& cb) {
+    if (narrow) {
+      const uint32_t q = static_cast<uint32_t>(i) / nbc32;
+      r = q;
+      cb = static_cast<int64_t>(static_cast<uint32_t>(i) - q * nbc32);
+    } else {
+      r = i / nbc;
+      cb = i - r * nbc;
+    }
+  };
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += 2 * step) {
+    int64_t r0, c0, r1 = 0, c1 = 0;
+    split(i, r0, c0);
+    const bool two = i + step < total;
+    if (two) split(i + step, r1, c1);
+    const Block16 v0 = load_block(x + r0 * ld_x + c0 * 16);
+    Block16 v1;
+    if (two) v1 = load_block(x + r1 * ld_x + c1 * 16);
+    quant_block<MODE>(v0, g, nullptr, scales + tiled_scale_offset(r0, c0, n_bt), codes + i * 8);
+    if (two)
+      quant_block<MODE>(v1, g, nullptr, scales + tiled_scale_offset(r1, c1, n_bt),
+                        codes + (i + step) * 8);
   }
+}
+
+// amax(|x|) of a contiguous operand as a flat array of 16-byte vectors, four
+// loads in flight per thread.
+__global__ void __launch_bounds__(256) amax_flat_kernel(const uint4* __restrict__ x, int64_t nvec,
+                                                        unsigned int* __restrict__ amax_bits) {
+  const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  uint32_t m = 0;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nvec;
+       i += 4 * step) {
+    uint4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      v[u] = i + u * step < nvec ? ld_stream(x + i + u * step) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        m = max(m, w[j] & 0x7FFFu);
+        m = max(m, (w[j] >> 16) & 0x7FFFu);
+      }
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, off));
+  if ((threadIdx.x & 31) == 0 && m != 0) atomicMax(amax_bits, m << 16);  // bf16 -> f32 bits
 }
 
 // amax(|x|) as the unsigned bit pattern of a non-negative float (monotone).
@@ -177,14 +228,15 @@ int grid_for(int64_t work, int threads) {
   return static_cast<int>(blocks < 1 ? 1 : blocks);
 }
 
-// One full wave of `kernel` (resident blocks per SM x SMs), at most enough
-// blocks for `work` threads.  The occupancy query runs once per kernel.
-template <class K>
-int wave_grid(K kernel, int64_t work, int threads) {
+// One full wave of `Kernel` (resident blocks per SM x SMs), at most enough
+// blocks for `work` threads.  The occupancy query runs once per kernel (one
+// template instance per kernel).
+template <auto Kernel>
+int wave_grid(int64_t work, int threads) {
   static int per_sm = 0;
   if (per_sm == 0) {
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, 0) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, Kernel, threads, 0) != cudaSuccess ||
         n < 1)
       n = 1;
     per_sm = n;
@@ -215,17 +267,17 @@ cudaError_t launch_fake_quant(const void* x, int64_t rows, int64_t cols, int64_t
     switch (mode) {
       case kUnitBf16:
         fake_quant_flat_kernel<kUnitBf16>
-            <<<wave_grid(fake_quant_flat_kernel<kUnitBf16>, work, threads), threads, 0, stream>>>(
+            <<<wave_grid<fake_quant_flat_kernel<kUnitBf16>>(work, threads), threads, 0, stream>>>(
                 xs, nblocks, gsf, os, scales, codes);
         break;
       case kUnitF16:
         fake_quant_flat_kernel<kUnitF16>
-            <<<wave_grid(fake_quant_flat_kernel<kUnitF16>, work, threads), threads, 0, stream>>>(
+            <<<wave_grid<fake_quant_flat_kernel<kUnitF16>>(work, threads), threads, 0, stream>>>(
                 xs, nblocks, gsf, os, scales, codes);
         break;
       default:
         fake_quant_flat_kernel<kStaticBf16>
-            <<<wave_grid(fake_quant_flat_kernel<kStaticBf16>, work, threads), threads, 0, stream>>>(
+            <<<wave_grid<fake_quant_flat_kernel<kStaticBf16>>(work, threads), threads, 0, stream>>>(
                 xs, nblocks, gsf, os, scales, codes);
         break;
     }
@@ -267,14 +319,16 @@ cudaError_t launch_quant_tiled(const void* x, int64_t rows, int64_t cols, int64_
     if (e != cudaSuccess) return e;
   }
   const int threads = 256;
-  const int64_t gx = std::min<int64_t>((nbc + threads - 1) / threads, 64);
-  const int64_t gy = std::max<int64_t>(1, std::min<int64_t>({rows, 65535, grid_for(rows * nbc, threads) / gx + 1}));
-  const dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(gy));
+  const int64_t work = (rows * nbc + 1) / 2;  // two blocks per thread and pass
   const auto* xs = static_cast<const uint16_t*>(x);
   if (gsf != nullptr)
-    quant_tiled_kernel<kStaticBf16><<<grid, threads, 0, stream>>>(xs, rows, nbc, ld_x, gsf, codes, scales);
+    quant_tiled_kernel<kStaticBf16>
+        <<<wave_grid<quant_tiled_kernel<kStaticBf16>>(work, threads), threads, 0, stream>>>(
+            xs, rows, nbc, ld_x, gsf, codes, scales);
   else
-    quant_tiled_kernel<kUnitBf16><<<grid, threads, 0, stream>>>(xs, rows, nbc, ld_x, gsf, codes, scales);
+    quant_tiled_kernel<kUnitBf16>
+        <<<wave_grid<quant_tiled_kernel<kUnitBf16>>(work, threads), threads, 0, stream>>>(
+            xs, rows, nbc, ld_x, gsf, codes, scales);
   return cudaGetLastError();
 }
 
@@ -283,9 +337,15 @@ cudaError_t launch_global_sf(const void* x, int64_t rows, int64_t cols, int64_t 
   cudaError_t e = cudaMemsetAsync(gsf, 0, sizeof(float), stream);
   if (e != cudaSuccess) return e;
   const int threads = 256;
-  const int grid = grid_for(rows * (cols / 8 > 0 ? cols / 8 : 1), threads);
-  amax_kernel<<<grid, threads, 0, stream>>>(static_cast<const uint16_t*>(x), rows, cols, ld_x,
-                                            reinterpret_cast<unsigned int*>(gsf));
+  if (ld_x == cols && cols % 8 == 0) {
+    const int64_t nvec = rows * cols / 8;
+    amax_flat_kernel<<<wave_grid<amax_flat_kernel>((nvec + 3) / 4, threads), threads, 0, stream>>>(
+        static_cast<const uint4*>(x), nvec, reinterpret_cast<unsigned int*>(gsf));
+  } else {
+    const int grid = grid_for(rows * (cols / 8 > 0 ? cols / 8 : 1), threads);
+    amax_kernel<<<grid, threads, 0, stream>>>(static_cast<const uint16_t*>(x), rows, cols, ld_x,
+                                              reinterpret_cast<unsigned int*>(gsf));
+  }
   global_sf_finalize_kernel<<<1, 1, 0, stream>>>(gsf);
   return cudaGetLastError();
 }
