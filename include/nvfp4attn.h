@@ -375,6 +375,23 @@ nvq_status nvq_selftest_umma(const void* a, const void* b, float* c, int N, int 
                              int a_mn, int b_mn, nvq_stream_t stream);
 
 /*
+ * One 128 x N x K block-scaled FP4 MMA (tcgen05 kind::mxf4nvf4, K = 64 * nmma):
+ * a: E2M1 codes [128, K/2] bytes, b: [N, K/2] bytes, two codes a byte (the even
+ * element in the low nibble), loaded by TMA with the (K/2)-byte swizzle.  Each
+ * row has one E4M3 scale per 16 elements.  The scales reach tensor memory in one
+ * of two ways: mode 0 stores sf_img (u32 [2][128][32], A then B: 32 columns per
+ * lane) into TMEM columns [256, 320) by tcgen05.st; mode 1 copies sf_src (bytes
+ * [2][nmma][512], A then B, one 512-byte block of 32 rows x 16 bytes per MMA)
+ * to columns 256 + 4 kk (A) and 288 + 4 kk (B) by tcgen05.cp, replicated to the
+ * four lane quadrants.  MMA kk reads its scales at columns 256 + kk * sf_stride
+ * and 288 + kk * sf_stride.  c: f32 [128, N]; dump: u32 [128][64], TMEM columns
+ * [256, 320) after the MMAs.  N in {64, 128}, nmma in {1, 2}, sf_stride 0..4.
+ */
+nvq_status nvq_selftest_fp4(const void* a, const void* b, const uint32_t* sf_img,
+                            const uint8_t* sf_src, float* c, uint32_t* dump, int N, int nmma,
+                            int sf_stride, int mode, nvq_stream_t stream);
+
+/*
  * Launches one block that waits on a barrier nothing arrives on, with a wait
  * limit of `limit_ns` nanoseconds (1..1e9).  The wait must run out and record
  * NVQ_ERR_TIMEOUT for nvq_device_status(); nothing hangs.

@@ -68,6 +68,8 @@ SIGNATURES = {
     "nvq_selftest_umma": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int,
                                   c_void_p]),
     "nvq_selftest_timeout": (c_int, [c_int64, c_void_p]),
+    "nvq_selftest_fp4": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                                 c_int, c_int, c_int, c_int, c_void_p]),
 }
 
 STATUS = {0: "NVQ_OK", 1: "NVQ_ERR_INVALID", 2: "NVQ_ERR_UNSUPPORTED", 3: "NVQ_ERR_WORKSPACE",

@@ -153,6 +153,23 @@ int make_bnhd_map(CUtensorMap* map, const void* base, int B, int N, int H, int D
   return static_cast<int>(r);
 }
 
+int make_bnhd_u8_map(CUtensorMap* map, const void* base, int B, int N, int H, int D) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return CUDA_ERROR_NOT_FOUND;
+  const cuuint64_t rb = static_cast<cuuint64_t>(D) / 2;
+  const cuuint64_t dims[4] = {rb, static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(H),
+                              static_cast<cuuint64_t>(B)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(H) * rb, rb,
+                                 static_cast<cuuint64_t>(N) * H * rb};
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(rb), static_cast<cuuint32_t>(kTile), 1, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        D == 128 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return static_cast<int>(r);
+}
+
 int make_2d_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return CUDA_ERROR_NOT_FOUND;
@@ -165,6 +182,25 @@ int make_2d_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, 
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return static_cast<int>(r);
+}
+
+int make_u8_map(CUtensorMap* map, const void* base, int64_t rows, int row_bytes, int64_t ld,
+                int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return CUDA_ERROR_NOT_FOUND;
+  if (row_bytes != 32 && row_bytes != 64) return CUDA_ERROR_INVALID_VALUE;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(rows),
+                              1, 1};
+  const cuuint64_t rs = static_cast<cuuint64_t>(ld);
+  const cuuint64_t strides[3] = {rs, rs * rows, rs * rows};
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(row_bytes), static_cast<cuuint32_t>(box_rows),
+                             1, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        row_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return static_cast<int>(r);
 }
 
@@ -185,15 +221,26 @@ size_t bytes_bnhd(int B, int N, int H, int D, size_t elem) {
   return static_cast<size_t>(B) * N * H * D * elem;
 }
 
+// Forward workspace.  BF16 operands (block-sparse and auxiliary-output forms):
+// Q~, K~ (bf16) and V~ (f16) at q, k, v.  FP4 operands (the dense form): the
+// packed codes of Q~ and K~ at qc, kc, their scale blocks at qs, ks, V~ (f16)
+// at v4.  total covers both layouts.
 struct FwdWs {
-  size_t q, k, v, total;
+  size_t q, k, v, qc, kc, qs, ks, v4, total;
 };
 FwdWs fwd_ws(int B, int Nq, int Nkv, int H, int D) {
   FwdWs w;
   w.q = 0;
   w.k = round_up(w.q + bytes_bnhd(B, Nq, H, D, 2), 256);
   w.v = round_up(w.k + bytes_bnhd(B, Nkv, H, D, 2), 256);
-  w.total = round_up(w.v + bytes_bnhd(B, Nkv, H, D, 2), 256);
+  const size_t bf16_total = round_up(w.v + bytes_bnhd(B, Nkv, H, D, 2), 256);
+  w.qc = 0;
+  w.kc = round_up(w.qc + bytes_bnhd(B, Nq, H, D, 1) / 2, 256);
+  w.qs = round_up(w.kc + bytes_bnhd(B, Nkv, H, D, 1) / 2, 256);
+  w.ks = round_up(w.qs + attn_fp4_scale_bytes(B, Nq, H, D), 256);
+  w.v4 = round_up(w.ks + attn_fp4_scale_bytes(B, Nkv, H, D), 256);
+  const size_t fp4_total = round_up(w.v4 + bytes_bnhd(B, Nkv, H, D, 2), 256);
+  w.total = bf16_total > fp4_total ? bf16_total : fp4_total;
   return w;
 }
 
@@ -252,26 +299,53 @@ nvq_status fwd_impl(const void* q, const void* k, const void* v, int B, int Nq, 
   int* err = error_word();
   if (err == nullptr) return NVQ_ERR_CUDA;
   uint8_t* wb = static_cast<uint8_t*>(ws);
+  const int64_t rq = static_cast<int64_t>(B) * Nq * H, rk = static_cast<int64_t>(B) * Nkv * H;
+  const AttnShape s{B, Nq, Nkv, H, D, scale, causal};
+  CUtensorMap mq, mk, mv;
+  int r;
+  cudaError_t e;
+  if (kv_list == nullptr && o_hp == nullptr) {
+    // dense: S on FP4 UMMAs, Q~ and K~ as codes + scale blocks
+    uint8_t* qc = wb + w.qc;
+    uint8_t* kc = wb + w.kc;
+    uint8_t* qs = wb + w.qs;
+    uint8_t* ks = wb + w.ks;
+    void* vt = wb + w.v4;
+    if ((r = make_bnhd_u8_map(&mq, qc, B, Nq, H, D)) != 0 ||
+        (r = make_bnhd_u8_map(&mk, kc, B, Nkv, H, D)) != 0 ||
+        (r = make_bnhd_map(&mv, vt, B, Nkv, H, D, true)) != 0)
+      return fail_driver("cuTensorMapEncodeTiled", r);
+    if ((e = timed(NVQ_KERNEL_QUANTIZE, stream, [&] {
+           return launch_quant_attn_fp4(q, B, Nq, H, D, qc, qs, stream);
+         })) != cudaSuccess)
+      return fail_cuda("quantize q (fp4)", e);
+    if ((e = timed(NVQ_KERNEL_QUANTIZE, stream, [&] {
+           return launch_quant_attn_fp4(k, B, Nkv, H, D, kc, ks, stream);
+         })) != cudaSuccess)
+      return fail_cuda("quantize k (fp4)", e);
+    if ((e = quantize_rows(v, rk, D, kUnitF16, vt, stream)) != cudaSuccess)
+      return fail_cuda("quantize v", e);
+    return from_cuda("attn_fwd", timed(NVQ_KERNEL_ATTN_FWD, stream, [&] {
+                       return launch_attn_fwd(s, mq, mk, mv, o, nullptr, stats, nullptr, 0, qs, ks,
+                                              err, stream);
+                     }));
+  }
   void* qt = wb + w.q;
   void* kt = wb + w.k;
   void* vt = wb + w.v;
-  CUtensorMap mq, mk, mv;
-  int r;
   if ((r = make_bnhd_map(&mq, qt, B, Nq, H, D, false)) != 0 ||
       (r = make_bnhd_map(&mk, kt, B, Nkv, H, D, false)) != 0 ||
       (r = make_bnhd_map(&mv, vt, B, Nkv, H, D, true)) != 0)
     return fail_driver("cuTensorMapEncodeTiled", r);
-  const int64_t rq = static_cast<int64_t>(B) * Nq * H, rk = static_cast<int64_t>(B) * Nkv * H;
-  cudaError_t e;
   if ((e = quantize_rows(q, rq, D, kUnitBf16, qt, stream)) != cudaSuccess)
     return fail_cuda("quantize q", e);
   if ((e = quantize_rows(k, rk, D, kUnitBf16, kt, stream)) != cudaSuccess)
     return fail_cuda("quantize k", e);
   if ((e = quantize_rows(v, rk, D, kUnitF16, vt, stream)) != cudaSuccess)
     return fail_cuda("quantize v", e);
-  const AttnShape s{B, Nq, Nkv, H, D, scale, causal};
   return from_cuda("attn_fwd", timed(NVQ_KERNEL_ATTN_FWD, stream, [&] {
-                     return launch_attn_fwd(s, mq, mk, mv, o, o_hp, stats, kv_list, topk, err, stream);
+                     return launch_attn_fwd(s, mq, mk, mv, o, o_hp, stats, kv_list, topk, nullptr,
+                                            nullptr, err, stream);
                    }));
 }
 
@@ -533,6 +607,26 @@ nvq_status nvq_selftest_umma(const void* a, const void* b, float* c, int N, int 
     return fail_driver("cuTensorMapEncodeTiled", r);
   return from_cuda("selftest_umma",
                    launch_selftest_umma(ma, mb, a, c, N, K, a_mn, b_mn, err, stream));
+}
+
+nvq_status nvq_selftest_fp4(const void* a, const void* b, const uint32_t* sf_img,
+                            const uint8_t* sf_src, float* c, uint32_t* dump, int N, int nmma,
+                            int sf_stride, int mode, nvq_stream_t stream) {
+  if (!a || !b || !c || !dump || !aligned16(a) || !aligned16(b) || !aligned16(c) ||
+      !aligned16(dump))
+    return NVQ_ERR_INVALID;
+  if ((N != 64 && N != 128) || (nmma != 1 && nmma != 2) || sf_stride < 0 || sf_stride > 4 ||
+      (mode != 0 && mode != 1) || (mode == 0 && !sf_img) || (mode == 1 && !sf_src))
+    return NVQ_ERR_INVALID;
+  int* err = error_word();
+  if (err == nullptr) return NVQ_ERR_CUDA;
+  CUtensorMap ma, mb;
+  int r;
+  if ((r = make_u8_map(&ma, a, 128, 32 * nmma, 32 * nmma, 128)) != 0 ||
+      (r = make_u8_map(&mb, b, N, 32 * nmma, 32 * nmma, N)) != 0)
+    return fail_driver("cuTensorMapEncodeTiled", r);
+  return from_cuda("selftest_fp4", launch_selftest_fp4(ma, mb, sf_img, sf_src, c, dump, N, nmma,
+                                                       sf_stride, mode, err, stream));
 }
 
 nvq_status nvq_selftest_timeout(int64_t limit_ns, nvq_stream_t stream) {

@@ -27,6 +27,12 @@ size_t tiled_scale_bytes(int64_t rows, int64_t cols);
 cudaError_t launch_quant_tiled(const void* x, int64_t rows, int64_t cols, int64_t ld_x,
                                const float* gsf, uint8_t* codes, uint8_t* scales,
                                cudaStream_t stream);
+// Q or K of attention for the FP4 UMMA: packed E2M1 codes [B, N, H, D/2] and
+// E4M3 scales in per-(b, h, 128-token tile, 64-element group) 512-byte blocks in
+// the UMMA's tensor-memory scale layout (attn_fp4_scale_bytes(B, N, H, D)).
+size_t attn_fp4_scale_bytes(int B, int N, int H, int D);
+cudaError_t launch_quant_attn_fp4(const void* x, int B, int N, int H, int D, uint8_t* codes,
+                                  uint8_t* scales, cudaStream_t stream);
 cudaError_t launch_global_sf(const void* x, int64_t rows, int64_t cols, int64_t ld_x, float* gsf,
                              cudaStream_t stream);
 
@@ -64,16 +70,23 @@ cudaError_t timed(int kind, cudaStream_t stream, F&& launch) {
   return launch();
 }
 
+// Tensor map over packed E2M1 codes [B, N, H, D/2] (bytes), box {D/2, 128, 1, 1},
+// with the (D/2)-byte swizzle; D in {64, 128}.
+int make_bnhd_u8_map(CUtensorMap* map, const void* base, int B, int N, int H, int D);
 // Tensor maps over [B, N, H, D] 16-bit tensors, box {64, box_rows, 1, 1}, 128-byte swizzle.
 // Return the CUresult of cuTensorMapEncodeTiled (0 on success).
 int make_bnhd_map(CUtensorMap* map, const void* base, int B, int N, int H, int D, bool f16,
                    int box_rows = kTile);
 
 // kv_list: NULL (dense) or int32 [B, H, ceil(Nq/128), topk] key tiles per query tile;
-// o_hp: NULL or the auxiliary output P V~ / l (bf16, layout of o); not both
+// o_hp: NULL or the auxiliary output P V~ / l (bf16, layout of o); q_sc, k_sc:
+// NULL, or the FP4 scale blocks of Q~ and K~ (launch_quant_attn_fp4), in which
+// case tq and tk map their packed codes (make_bnhd_u8_map) and S runs on FP4
+// UMMAs.  At most one of the three.
 cudaError_t launch_attn_fwd(const AttnShape& s, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, void* o, void* o_hp, float* stats,
-                            const int* kv_list, int topk, int* err, cudaStream_t stream);
+                            const int* kv_list, int topk, const uint8_t* q_sc,
+                            const uint8_t* k_sc, int* err, cudaStream_t stream);
 cudaError_t launch_bwd_prep(const AttnShape& s, const void* o, const void* dout, float* delta,
                             cudaStream_t stream);
 // dK, dV (key-outer; Q~, K~, V~, dO maps with 128-row boxes).  Block-sparse:
@@ -103,8 +116,15 @@ cudaError_t launch_selftest_umma(const CUtensorMap& ta, const CUtensorMap& tb, c
                                  float* c, int N, int K, int a_mn, int b_mn, int* err,
                                  cudaStream_t stream);
 cudaError_t launch_selftest_timeout(int64_t limit_ns, int* err, cudaStream_t stream);
+cudaError_t launch_selftest_fp4(const CUtensorMap& ta, const CUtensorMap& tb, const uint32_t* sf_img,
+                                const uint8_t* sf_src, float* c, uint32_t* dump, int N, int nmma,
+                                int sf_stride, int mode, int* err, cudaStream_t stream);
 
 // Maps a [rows, cols] 16-bit row-major matrix with a box of {64, box_rows}.
 int make_2d_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_rows);
+// Maps a [rows, row_bytes] byte matrix (row stride ld bytes) with a box of
+// {row_bytes, box_rows} and the row_bytes-wide swizzle (row_bytes in {32, 64}).
+int make_u8_map(CUtensorMap* map, const void* base, int64_t rows, int row_bytes, int64_t ld,
+                int box_rows);
 
 }  // namespace nvq

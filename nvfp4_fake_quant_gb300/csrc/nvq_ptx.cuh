@@ -126,6 +126,19 @@ __device__ __forceinline__ void tma_load_4d_w(void* smem_dst, const CUtensorMap*
       : "memory");
 }
 
+// Contiguous copy of `bytes` (a multiple of 16; both addresses 16-byte aligned)
+// from global to shared memory, completing on `bar` (tx bytes).  Warp-collective.
+__device__ __forceinline__ void bulk_load_w(void* smem_dst, const void* src, uint32_t bytes,
+                                            uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      "\n\t}" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // 4-D tiled load (coordinates innermost first) completing on `bar` (tx bytes).
 __device__ __forceinline__ void tma_load_4d(void* smem_dst, const CUtensorMap* map, int c0, int c1,
                                             int c2, int c3, uint64_t* bar) {
@@ -310,6 +323,63 @@ __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, int ab_bf16, int 
          | (static_cast<uint32_t>(b_mn) << 16)      // B major
          | (static_cast<uint32_t>(N >> 3) << 17)    // N / 8
          | (static_cast<uint32_t>(M >> 4) << 24);   // M / 16
+}
+
+// Shared-memory descriptor with an explicit layout type (bits 61-63):
+// 0 = no swizzle (8-row x 16-byte core matrices), 2 = 128-byte, 4 = 64-byte,
+// 6 = 32-byte swizzle.  For a K-major operand whose rows are `w` bytes wide and
+// stored with the w-byte swizzle (as a TMA load with that swizzle and a box
+// `w` bytes wide writes them), SBO = 8 * w and LBO is unused.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo,
+                                          uint32_t layout) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(layout & 7u) << 61;
+  return d;
+}
+
+// Instruction descriptor of a block-scaled kind::mxf4nvf4 UMMA: A and B E2M1
+// (format code 1), K-major, f32 accumulation, one unsigned E4M3 scale per 16
+// K-elements (scale type bit 23 = 0), K = 64 per instruction (bit 31 = 0),
+// scale-factor data ids 0.  M = 128, N % 8 == 0, N <= 256.
+__host__ __device__ constexpr uint32_t idesc_mxf4nvf4(int M, int N) {
+  return (1u << 7)                                 // A format: E2M1
+         | (1u << 10)                              // B format: E2M1
+         | (static_cast<uint32_t>(N >> 3) << 17)   // N / 8
+         | (static_cast<uint32_t>(M >> 4) << 24);  // M / 16
+}
+
+// D[tmem] (+)= (A * sA) (B * sB)^T, E2M1 A and B in shared memory (K-major,
+// two codes a byte, the even element in the low nibble), one E4M3 scale per
+// 16 K-elements of each row read from TMEM at sfa_tmem / sfb_tmem.  K = 64.
+__device__ __forceinline__ void umma_fp4_ss_w(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                              uint32_t idesc, uint32_t sfa_tmem,
+                                              uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, "
+      "[%4], [%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Copy 32 rows x 16 bytes (512 contiguous bytes of shared memory, row r at
+// 16 r) into TMEM columns [col, col + 4) of lanes r, r + 32, r + 64, r + 96
+// (the same rows in each of the four lane quadrants).  Ordered before the
+// tcgen05.mma instructions the same thread issues after it.
+__device__ __forceinline__ void tmem_cp_32x128_x4_w(uint32_t taddr, uint32_t saddr) {
+  const uint64_t d = sdesc(saddr, 128, 128, 0);
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;\n\t}" ::"r"(taddr),
+      "l"(d)
+      : "memory");
 }
 
 // Byte offset of element (row, col) of a 16-bit matrix stored as 128-byte

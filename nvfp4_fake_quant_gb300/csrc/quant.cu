@@ -106,6 +106,55 @@ __global__ void __launch_bounds__(256) fake_quant_rows_kernel(
   }
 }
 
+// Q or K of attention for the block-scaled FP4 UMMA.  x: bf16 [B, N, H, D]
+// (contiguous); codes: [B, N, H, D/2] bytes, two E2M1 codes a byte (the even
+// element in the low nibble, the sign bit of x on zero codes); scales: for each
+// (b, h), 128-token tile t and 64 elements kk of D, one 512-byte block at
+// (((b H + h) n_tiles + t) (D/64) + kk) * 512 holding the E4M3 scale of token r
+// of the tile, 16-element block j of the 64, at byte (r % 32) * 16 + (r / 32) * 4
+// + j -- the tensor-memory layout of the UMMA's scale operand, so that one
+// copy per block moves it there.  Tokens of the last tile beyond N get scale 0.
+// Blocks i < nblocks are the input's 16-element blocks in memory order (two
+// per thread in flight); the npad indices after them zero the padding scales.
+__global__ void __launch_bounds__(256) quant_attn_fp4_kernel(
+    const uint16_t* __restrict__ x, uint32_t nblocks, uint32_t npad, uint32_t N, uint32_t H,
+    uint32_t lg_nbd, uint32_t n_tiles, uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
+  const uint32_t nbd = 1u << lg_nbd;  // 16-element blocks per row (D / 16)
+  const uint32_t nkk = nbd >> 2;      // 64-element groups per row
+  const uint32_t step = gridDim.x * blockDim.x;
+  auto scale_at = [&](uint32_t bh, uint32_t n, uint32_t cb) -> uint8_t* {
+    return scales + ((static_cast<int64_t>(bh) * n_tiles + (n >> 7)) * nkk + (cb >> 2)) * 512 +
+           (n & 31u) * 16 + ((n >> 5) & 3u) * 4 + (cb & 3u);
+  };
+  for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < nblocks; i += 2 * step) {
+    Block16 v[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u)
+      if (i + u * step < nblocks) v[u] = load_block(x + static_cast<int64_t>(i + u * step) * 16);
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const uint32_t blk = i + u * step;
+      if (blk >= nblocks) continue;
+      const uint32_t xv[8] = {v[u].lo.x, v[u].lo.y, v[u].lo.z, v[u].lo.w,
+                              v[u].hi.x, v[u].hi.y, v[u].hi.z, v[u].hi.w};
+      Q16 q = quant16_unit<false>(xv);
+      code_signs(xv, q.codes);
+      *reinterpret_cast<uint2*>(codes + static_cast<int64_t>(blk) * 8) =
+          make_uint2(q.codes[0], q.codes[1]);
+      const uint32_t row = blk >> lg_nbd, cb = blk & (nbd - 1u);
+      const uint32_t bn = row / H, h = row - bn * H;
+      const uint32_t b = bn / N, n = bn - b * N;
+      *scale_at(b * H + h, n, cb) = static_cast<uint8_t>(q.sbyte);
+    }
+  }
+  const uint32_t pad_rows = n_tiles * 128u - N;
+  for (uint32_t j = blockIdx.x * blockDim.x + threadIdx.x; j < npad; j += step) {
+    const uint32_t cb = j & (nbd - 1u), t = j >> lg_nbd;
+    const uint32_t bh = t / pad_rows, n = N + (t - bh * pad_rows);
+    *scale_at(bh, n, cb) = 0;
+  }
+}
+
 // Byte offset of the scale of (row r, 16-element block cb) in the 128x4 tiled
 // layout of block-scaled FP4 GEMMs: 512-byte tiles of 128 rows x 4 blocks,
 // tiles ordered by row tile, then block tile (n_bt tiles per row tile); inside
@@ -329,6 +378,27 @@ cudaError_t launch_quant_tiled(const void* x, int64_t rows, int64_t cols, int64_
     quant_tiled_kernel<kUnitBf16>
         <<<wave_grid<quant_tiled_kernel<kUnitBf16>>(work, threads), threads, 0, stream>>>(
             xs, rows, nbc, ld_x, gsf, codes, scales);
+  return cudaGetLastError();
+}
+
+size_t attn_fp4_scale_bytes(int B, int N, int H, int D) {
+  const size_t n_tiles = (static_cast<size_t>(N) + 127) / 128;
+  return static_cast<size_t>(B) * H * n_tiles * (D / 64) * 512;
+}
+
+cudaError_t launch_quant_attn_fp4(const void* x, int B, int N, int H, int D, uint8_t* codes,
+                                  uint8_t* scales, cudaStream_t stream) {
+  const int64_t nblocks = static_cast<int64_t>(B) * N * H * (D / 16);
+  const int64_t n_tiles = (N + 127) / 128;
+  const int64_t npad = static_cast<int64_t>(B) * H * (n_tiles * 128 - N) * (D / 16);
+  if ((D != 64 && D != 128) || nblocks >= (int64_t{1} << 31) || npad >= (int64_t{1} << 31))
+    return cudaErrorInvalidValue;
+  const int threads = 256;
+  const int64_t work = std::max<int64_t>((nblocks + 1) / 2, npad);
+  quant_attn_fp4_kernel<<<wave_grid<quant_attn_fp4_kernel>(work, threads), threads, 0, stream>>>(
+      static_cast<const uint16_t*>(x), static_cast<uint32_t>(nblocks), static_cast<uint32_t>(npad),
+      static_cast<uint32_t>(N), static_cast<uint32_t>(H), D == 128 ? 3u : 2u,
+      static_cast<uint32_t>(n_tiles), codes, scales);
   return cudaGetLastError();
 }
 

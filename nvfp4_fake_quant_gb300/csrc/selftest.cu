@@ -2,6 +2,9 @@
 //  * one 128 x N x K tcgen05 kind::f16 BF16 UMMA fed by 128-byte-swizzled TMA
 //    tiles through the same shared-memory and instruction descriptors, for
 //    K-major and MN-major A and B, and for A stored in TMEM by tcgen05.st;
+//  * one 128 x N x (64 or 128) block-scaled kind::mxf4nvf4 UMMA (E2M1 operands
+//    from 32- or 64-byte-swizzled TMA tiles, E4M3 scales in TMEM written either
+//    by tcgen05.st from a given TMEM image or by tcgen05.cp from shared memory);
 //  * a bounded mbarrier wait that is meant to run out.
 #include <cuda_runtime.h>
 
@@ -119,6 +122,120 @@ __global__ void __launch_bounds__(128, 1)
   }
 }
 
+// FP4 probe.  A: E2M1 codes [128, kb] bytes (kb = 32 * nmma, K = 64 * nmma),
+// B: [N, kb]; both K-major, loaded by TMA with the kb-byte swizzle.  TMEM:
+// D at columns [0, N), A scales at [256, 288), B scales at [288, 320).
+//   mode 0: sf_img (u32 [2][128][32]: A then B, lane-major) is stored into those
+//           columns by tcgen05.st;
+//   mode 1: sf_src (bytes [2][nmma][512]) is copied into shared memory and from
+//           there by tcgen05.cp (32x128b, warpx4): A block kk to column
+//           256 + 4 kk, B block kk to 288 + 4 kk.
+// UMMA kk reads its scales at column 256 + kk * sf_stride (A), 288 + kk *
+// sf_stride (B).  Outputs: c [128, N] f32 and dump (u32 [128][64]): TMEM columns
+// [256, 320) after the UMMAs.
+constexpr uint32_t kFp4Smem = 1024 + 8192 + 8192 + 2048 + 4096 + 256;
+
+__global__ void __launch_bounds__(128, 1)
+    selftest_fp4_kernel(const __grid_constant__ CUtensorMap ta,
+                        const __grid_constant__ CUtensorMap tb, const uint32_t* __restrict__ sf_img,
+                        const uint8_t* __restrict__ sf_src, float* __restrict__ c,
+                        uint32_t* __restrict__ dump, int N, int nmma, int sf_stride, int mode,
+                        int* __restrict__ err) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023u) &
+                                             ~static_cast<uintptr_t>(1023u));
+  uint8_t* sa = smem;
+  uint8_t* sb = smem + 8192;
+  uint8_t* sfs = smem + 16384;  // cp source, followed by 4 KB of slack
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 16384 + 2048 + 4096);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3);
+  volatile int* abort = reinterpret_cast<volatile int*>(bars + 4);
+  const int warp = threadIdx.x >> 5;
+  const int kb = 32 * nmma;
+  if (threadIdx.x == 0) {
+    *abort = 0;
+    for (int i = 0; i < 3; ++i) mbar_init(&bars[i], 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+  if (mode == 0) {
+    const int lane_row = threadIdx.x;  // TMEM lane of this thread
+#pragma unroll
+    for (int m = 0; m < 2; ++m) {
+      const uint32_t* img = sf_img + (static_cast<size_t>(m) * 128 + lane_row) * 32;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t r[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) r[i] = img[h * 16 + i];
+        tmem_st16(tmem + lane_base + 256 + 32 * m + 16 * h, r);
+      }
+    }
+    tmem_wait_st();
+  } else {
+    for (int i = threadIdx.x; i < 2 * nmma * 512; i += 128) sfs[i] = sf_src[i];
+    for (int i = threadIdx.x; i < 4096; i += 128) sfs[2048 + i] = 0;
+    fence_proxy_async_smem();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) {
+    mbar_arrive_expect_tx_w(&bars[0], static_cast<uint32_t>((128 + N) * kb));
+    tma_load_4d_w(sa, &ta, 0, 0, 0, 0, &bars[0]);
+    tma_load_4d_w(sb, &tb, 0, 0, 0, 0, &bars[0]);
+    if (mbar_wait_warp(&bars[0], 0, abort)) {
+      tc_fence_after();
+      const uint32_t layout = kb == 64 ? 4u : 6u;  // 64- or 32-byte swizzle
+      const uint32_t idesc = idesc_mxf4nvf4(128, N);
+      if (mode == 1) {
+        for (int kk = 0; kk < nmma; ++kk) {
+          tmem_cp_32x128_x4_w(tmem + 256 + 4 * kk, smem_u32(sfs + kk * 512));
+          tmem_cp_32x128_x4_w(tmem + 288 + 4 * kk, smem_u32(sfs + (nmma + kk) * 512));
+        }
+      }
+      for (int kk = 0; kk < nmma; ++kk)
+        umma_fp4_ss_w(tmem, sdesc(smem_u32(sa) + 32 * kk, 16, 8 * kb, layout),
+                      sdesc(smem_u32(sb) + 32 * kk, 16, 8 * kb, layout), idesc,
+                      tmem + 256 + kk * sf_stride, tmem + 288 + kk * sf_stride, kk > 0 ? 1u : 0u);
+      umma_commit_w(&bars[2]);
+    }
+  }
+  __syncthreads();
+  const bool done = mbar_wait_warp(&bars[2], 0, abort);
+  if (done && !*abort) {
+    tc_fence_after();
+    const int row = threadIdx.x;
+    uint32_t r[32];
+    for (int cc = 0; cc < N / 32; ++cc) {
+      tmem_ld32(tmem + lane_base + cc * 32, r);
+      tmem_wait_ld();
+      for (int i = 0; i < 32; ++i) c[row * N + cc * 32 + i] = __uint_as_float(r[i]);
+    }
+    for (int cc = 0; cc < 2; ++cc) {
+      tmem_ld32(tmem + lane_base + 256 + cc * 32, r);
+      tmem_wait_ld();
+      for (int i = 0; i < 32; ++i) dump[row * 64 + cc * 32 + i] = r[i];
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  report_abort(abort, err);
+  if (warp == 0) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
 __global__ void selftest_timeout_kernel(int64_t limit_ns, int* __restrict__ err) {
   __shared__ uint64_t bar;
   __shared__ int abort;
@@ -146,6 +263,17 @@ cudaError_t launch_selftest_umma(const CUtensorMap& ta, const CUtensorMap& tb, c
   if (e != cudaSuccess) return e;
   selftest_umma_kernel<<<1, 128, kSmem, stream>>>(ta, tb, static_cast<const uint32_t*>(a), c, N, K,
                                                   a_mn, b_mn, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_selftest_fp4(const CUtensorMap& ta, const CUtensorMap& tb, const uint32_t* sf_img,
+                                const uint8_t* sf_src, float* c, uint32_t* dump, int N, int nmma,
+                                int sf_stride, int mode, int* err, cudaStream_t stream) {
+  cudaError_t e = cudaFuncSetAttribute(selftest_fp4_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kFp4Smem);
+  if (e != cudaSuccess) return e;
+  selftest_fp4_kernel<<<1, 128, kFp4Smem, stream>>>(ta, tb, sf_img, sf_src, c, dump, N, nmma,
+                                                     sf_stride, mode, err);
   return cudaGetLastError();
 }
 

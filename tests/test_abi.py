@@ -139,6 +139,11 @@ def test_quantizer_rejects_bad_arguments(lib):
     assert lib.nvq_selftest_timeout(0, None) == INVALID
     assert lib.nvq_selftest_umma(A, A, A, 96, 64, 0, 0, None) == INVALID
     assert lib.nvq_selftest_umma(A, A, A, 64, 64, 3, 0, None) == INVALID
+    assert lib.nvq_selftest_fp4(A, A, A, None, A, A, 96, 1, 4, 0, None) == INVALID
+    assert lib.nvq_selftest_fp4(A, A, A, None, A, A, 128, 3, 4, 0, None) == INVALID
+    assert lib.nvq_selftest_fp4(A, A, None, None, A, A, 128, 2, 4, 0, None) == INVALID
+    assert lib.nvq_selftest_fp4(A, A, None, None, A, A, 128, 2, 4, 1, None) == INVALID
+    assert lib.nvq_selftest_fp4(A, A, A, None, A, A, 128, 2, 5, 0, None) == INVALID
 
 
 def test_block_sparse_and_vsa_calls_reject_bad_arguments(lib):
