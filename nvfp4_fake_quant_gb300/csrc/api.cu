@@ -326,8 +326,7 @@ nvq_status fwd_impl(const void* q, const void* k, const void* v, int B, int Nq, 
     if ((e = quantize_rows(v, rk, D, kUnitF16, vt, stream)) != cudaSuccess)
       return fail_cuda("quantize v", e);
     return from_cuda("attn_fwd", timed(NVQ_KERNEL_ATTN_FWD, stream, [&] {
-                       return launch_attn_fwd(s, mq, mk, mv, o, nullptr, stats, nullptr, 0, qs, ks,
-                                              err, stream);
+                       return launch_attn_fwd_fp4(s, mq, mk, mv, qs, ks, o, stats, err, stream);
                      }));
   }
   void* qt = wb + w.q;
@@ -344,8 +343,8 @@ nvq_status fwd_impl(const void* q, const void* k, const void* v, int B, int Nq, 
   if ((e = quantize_rows(v, rk, D, kUnitF16, vt, stream)) != cudaSuccess)
     return fail_cuda("quantize v", e);
   return from_cuda("attn_fwd", timed(NVQ_KERNEL_ATTN_FWD, stream, [&] {
-                     return launch_attn_fwd(s, mq, mk, mv, o, o_hp, stats, kv_list, topk, nullptr,
-                                            nullptr, err, stream);
+                     return launch_attn_fwd(s, mq, mk, mv, o, o_hp, stats, kv_list, topk, err,
+                                            stream);
                    }));
 }
 

@@ -30,16 +30,6 @@
 //   kDense   every key tile, one K/V load per step shared by the two query tiles;
 //   kSparse  block-sparse: query tile i runs over its own listed key tiles, one
 //            load per query tile per step;
-//   kFp4     S = Q~ K~^T on block-scaled FP4 UMMAs (tcgen05 kind::mxf4nvf4):
-//            Q~ and K~ arrive as packed E2M1 codes with their E4M3 block scales,
-//            and the UMMA applies the scales, so S is the same sum of exact
-//            products as with BF16 operands.  One query tile per CTA, the two
-//            softmax pairs on the even and the odd key tiles as in kAux (the
-//            scale operands need TMEM columns the two-tile layout has no room
-//            for).  TMEM: S_0, S_1 at [0, 256), O at [256, 256 + D), the Q~
-//            scales at [384 + 4 kk) and pair i's K~ scales at [392 + 8 i + 4 kk)
-//            for the 64-element groups kk of D, copied from shared memory by
-//            tcgen05.cp just before the UMMAs that read them;
 //   kAux     the auxiliary high-precision output O_hp = P V~ / l next to O (the
 //            "auxiliary output" of the Attn-QAT backward, "use_high_prec_o"):
 //            one query tile per CTA, and the two softmax pairs take the even
@@ -68,7 +58,7 @@ constexpr int kThreads = 576;
 constexpr int kRing = 5;  // K/V tile ring (K and V tiles interleave in pass 2)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint32_t kAtomBlock = 128u * 128u;  // bytes of one 64-column block of a 128-row tile
-constexpr int kDense = 0, kSparse = 1, kAux = 2, kFp4 = 3;  // forward modes
+constexpr int kDense = 0, kSparse = 1, kAux = 2;  // forward modes
 
 template <int D>
 struct FwdLayout {
@@ -101,16 +91,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const __grid_constant__ CUtensorMap tv, __nv_bfloat16* __restrict__ o,
                     __nv_bfloat16* __restrict__ o_hp, float* __restrict__ stats, int Nq, int Nkv,
                     int H, float scale, int causal, const int* __restrict__ kv_list, int topk,
-                    const uint8_t* __restrict__ q_sc, const uint8_t* __restrict__ k_sc,
                     int* __restrict__ err) {
   constexpr bool sparse = kMode == kSparse;
   constexpr bool aux = kMode == kAux;
-  constexpr bool fp4 = kMode == kFp4;
-  constexpr bool one_tile = aux || fp4;
-  constexpr int kQTiles = one_tile ? 1 : 2;  // query tiles per CTA
-  // FP4 operands: codes of a 128-row tile, then its scale blocks (D/64 x 512 B)
-  constexpr uint32_t kCodeBytes = 128u * D / 2, kScBytes = (D / 64) * 512u;
-  constexpr uint32_t kScA = 384, kScB = 392;  // TMEM columns of the scale operands
+  constexpr int kQTiles = aux ? 1 : 2;  // query tiles per CTA
   using L = FwdLayout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023u) &
@@ -140,7 +124,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   int n_kv;
   if (sparse) {
     n_kv = topk;
-  } else if (one_tile) {
+  } else if (aux) {
     const int nk = causal ? min(n_kv_all, static_cast<int>(blockIdx.x) + 1) : n_kv_all;
     n_kv = (nk + 1) / 2;
   } else {
@@ -176,7 +160,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // step then loads one tile per query tile.  Dense: key tile j at step j, one
   // load shared by both query tiles.  Auxiliary output: key tile 2 j + i for
   // pair i, one load per pair.
-  constexpr bool per_pair = sparse || one_tile;  // one K or V load per pair and step
+  constexpr bool per_pair = sparse || aux;  // one K or V load per pair and step
   constexpr int nt = per_pair ? 2 : 1;      // loads per K or V step
   const int n_qt = (Nq + kTile - 1) / kTile;
   const int* list0 = nullptr;
@@ -188,7 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     list1 = kv_list + (base + min(qt0 + 1, n_qt - 1)) * topk;  // a missing tile's rows are masked
   }
   auto key_tile = [&](int i, int j) -> int {
-    return sparse ? (i ? list1[j] : list0[j]) : one_tile ? 2 * j + i : j;
+    return sparse ? (i ? list1[j] : list0[j]) : aux ? 2 * j + i : j;
   };
 
   if (warp == kTmaWarp) {
@@ -199,21 +183,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tq);
     tma_prefetch_desc(&tk);
     tma_prefetch_desc(&tv);
-    const int64_t bh = static_cast<int64_t>(b) * H + h;
-    if constexpr (fp4) {
-      mbar_arrive_expect_tx_w(q_full, kCodeBytes + kScBytes);
-      tma_load_4d_w(smem + L::kQ, &tq, 0, q0, h, b, q_full);
-      bulk_load_w(smem + L::kQ + kCodeBytes, q_sc + (bh * n_qt + blockIdx.x) * kScBytes, kScBytes,
-                  q_full);
-    } else {
-      mbar_arrive_expect_tx_w(q_full, static_cast<uint32_t>(kQTiles) * L::kTileBytes);
+    mbar_arrive_expect_tx_w(q_full, static_cast<uint32_t>(kQTiles) * L::kTileBytes);
 #pragma unroll
-      for (int i = 0; i < kQTiles; ++i)
+    for (int i = 0; i < kQTiles; ++i)
 #pragma unroll
-        for (int blk = 0; blk < D / 64; ++blk)
-          tma_load_4d_w(smem + L::kQ + i * L::kTileBytes + blk * kAtomBlock, &tq, blk * 64,
-                        q0 + i * kTile, h, b, q_full);
-    }
+      for (int blk = 0; blk < D / 64; ++blk)
+        tma_load_4d_w(smem + L::kQ + i * L::kTileBytes + blk * kAtomBlock, &tq, blk * 64,
+                      q0 + i * kTile, h, b, q_full);
     int last[kRing];
     for (int s = 0; s < kRing; ++s) last[s] = -1;
     bool ok = true;
@@ -222,20 +198,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int slot = li % kRing;
       const uint32_t use = static_cast<uint32_t>(li / kRing);
       if (!mbar_wait_warp(&r_empty[slot], (use & 1u) ^ 1u, abort)) return false;
-      uint8_t* dst = smem + L::kRingOff + slot * L::kTileBytes;
-      if (fp4 && map == &tk) {
-        // codes (a missing odd tile reads as zeros) and scale blocks (clamped
-        // to the last tile: any finite scale times zero codes)
-        mbar_arrive_expect_tx_w(&r_full[slot], kCodeBytes + kScBytes);
-        tma_load_4d_w(dst, map, 0, tile * kTile, h, b, &r_full[slot]);
-        bulk_load_w(dst + kCodeBytes, k_sc + (bh * n_kv_all + min(tile, n_kv_all - 1)) * kScBytes,
-                    kScBytes, &r_full[slot]);
-      } else {
-        mbar_arrive_expect_tx_w(&r_full[slot], L::kTileBytes);
+      mbar_arrive_expect_tx_w(&r_full[slot], L::kTileBytes);
 #pragma unroll
-        for (int blk = 0; blk < D / 64; ++blk)
-          tma_load_4d_w(dst + blk * kAtomBlock, map, blk * 64, tile * kTile, h, b, &r_full[slot]);
-      }
+      for (int blk = 0; blk < D / 64; ++blk)
+        tma_load_4d_w(smem + L::kRingOff + slot * L::kTileBytes + blk * kAtomBlock, map, blk * 64,
+                      tile * kTile, h, b, &r_full[slot]);
       last[slot] = static_cast<int>(use & 1u);
       ++li;
       return true;
@@ -255,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------------- MMA
-    constexpr uint32_t idesc_s = fp4 ? idesc_mxf4nvf4(128, 128) : idesc_f16(128, 128, 1, 0, 0);
+    constexpr uint32_t idesc_s = idesc_f16(128, 128, 1, 0, 0);
     constexpr uint32_t idesc_pv = idesc_f16(128, D, 0, 0, 1);
     const uint32_t q_addr = smem_u32(smem + L::kQ);
     const uint32_t ring_addr = smem_u32(smem + L::kRingOff);
@@ -265,27 +232,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     auto issue_s = [&](int i, int idx) {  // S_i = Q~_i K~^T, K~ in ring slot of load idx
       const uint32_t kb = ring_addr + (idx % kRing) * L::kTileBytes;
-      if constexpr (fp4) {
-        // E2M1 rows of D/2 bytes with the (D/2)-byte swizzle; 64 elements (32
-        // bytes) per UMMA.  Pair i's previous S_i UMMAs, the last readers of its
-        // K~ scale columns, completed before the softmax released S_i.
-        constexpr uint32_t lay = D == 128 ? 4u : 6u, sbo = 8u * (D / 2);
+      const uint32_t qb = q_addr + (aux ? 0 : i) * L::kTileBytes;
 #pragma unroll
-        for (int kk = 0; kk < D / 64; ++kk)
-          tmem_cp_32x128_x4_w(tmem + kScB + 8 * i + 4 * kk, kb + kCodeBytes + kk * 512);
-#pragma unroll
-        for (int kk = 0; kk < D / 64; ++kk)
-          umma_fp4_ss_w(tmem + i * 128, sdesc(q_addr + 32 * kk, 16, sbo, lay),
-                        sdesc(kb + 32 * kk, 16, sbo, lay), idesc_s, tmem + kScA + 4 * kk,
-                        tmem + kScB + 8 * i + 4 * kk, kk > 0 ? 1u : 0u);
-      } else {
-        const uint32_t qb = q_addr + (aux ? 0 : i) * L::kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kAtomBlock + (kk & 3) * 32;
-          umma_f16_ss_w(tmem + i * 128, sdesc_sw128(qb + off, 16, 1024),
-                        sdesc_sw128(kb + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
-        }
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * kAtomBlock + (kk & 3) * 32;
+        umma_f16_ss_w(tmem + i * 128, sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
+                      idesc_s, kk > 0 ? 1u : 0u);
       }
       umma_commit_w(&s_full[i]);
     };
@@ -304,10 +256,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         (acc || kk > 0) ? 1u : 0u);
         }
       } else {
-        const uint32_t o_acc = 256u + (fp4 ? 0u : static_cast<uint32_t>(i) * 128u);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_f16_ts_w(tmem + o_acc, tmem + i * 128 + 64 * (kk >> 2) + 8 * (kk & 3),
+          umma_f16_ts_w(tmem + 256 + i * 128, tmem + i * 128 + 64 * (kk >> 2) + 8 * (kk & 3),
                         sdesc_sw128(vb + kk * 2048, kAtomBlock, 1024), idesc_pv,
                         (acc || kk > 0) ? 1u : 0u);
       }
@@ -319,14 +270,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (per_pair || i == 1) umma_commit_w(&r_empty[tile_load(base, i) % kRing]);
     };
     bool ok = mbar_wait_warp(q_full, 0, abort);
-    if constexpr (fp4) {  // the Q~ scales stay in TMEM for the whole kernel
-      if (ok) {
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < D / 64; ++kk)
-          tmem_cp_32x128_x4_w(tmem + kScA + 4 * kk, q_addr + kCodeBytes + kk * 512);
-      }
-    }
     // pass 1: S_0(j), S_1(j) for the row maxima
     for (int j = 0; j < n_kv && ok; ++j, li += nt) {
       for (int i = 0; i < 2 && ok; ++i) {
@@ -355,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if ((per_pair || i == 0) && !(ok = wait_slot(tile_load(vbase, i)))) break;
         if (!(ok = mbar_wait_warp(&p_full[i], static_cast<uint32_t>(j & 1), abort))) break;
         tc_fence_after();
-        issue_pv(i, tile_load(vbase, i), j > 0 || (one_tile && i > 0));
+        issue_pv(i, tile_load(vbase, i), j > 0 || (aux && i > 0));
         release(vbase, i);
         if (kbase >= 0) {
           if ((per_pair || i == 0) && !(ok = wait_slot(tile_load(kbase, i)))) break;
@@ -381,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ti = wg >> 1;                // query tile
     const int hf = wg & 1;                 // half of the key columns
     const int t = threadIdx.x & 127;       // row in the tile == TMEM lane
-    const int tile_q0 = q0 + (one_tile ? 0 : ti * kTile);
+    const int tile_q0 = q0 + (aux ? 0 : ti * kTile);
     const int qrow = tile_q0 + t;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t s_col = static_cast<uint32_t>(ti * 128 + hf * 64);
@@ -421,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (hf == 0) xchg[t] = mraw = fmaxf(mraw, xchg[t]);
     named_bar_sync(pair_bar, kPairThreads);
     if (hf == 1) mraw = xchg[t];
-    if constexpr (one_tile) {  // both pairs hold the same rows: combine their maxima
+    if constexpr (aux) {  // both pairs hold the same rows: combine their maxima
       const float* xall = reinterpret_cast<const float*>(smem + L::kX);
       named_bar_sync(3, 2 * kPairThreads);
       mraw = fmaxf(xall[t], xall[128 + t]);
@@ -494,12 +437,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (hf == 0) xchg[t] = l = l + xchg[t];
     named_bar_sync(pair_bar, kPairThreads);
     if (hf == 1) l = xchg[t];
-    if constexpr (one_tile) {
+    if constexpr (aux) {
       const float* xall = reinterpret_cast<const float*>(smem + L::kX);
       named_bar_sync(3, 2 * kPairThreads);
       l = xall[t] + xall[128 + t];
     }
-    if (have_o && !(fp4 && ti == 1)) {  // FP4: pair 0 writes the one O
+    if (have_o) {
       tc_fence_after();
       const float inv_l = 1.0f / l;
       // auxiliary output: pair 0 writes O, pair 1 O_hp
@@ -524,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             dst[u] = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
         }
       }
-      if (qrow < Nq && hf == 0 && (!one_tile || ti == 0)) {
+      if (qrow < Nq && hf == 0 && (!aux || ti == 0)) {
         float* st = stats + (static_cast<int64_t>(b) * H + h) * 2 * Nq;
         st[qrow] = m + logf(l);
         st[Nq + qrow] = m;
@@ -547,49 +490,36 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D, int kMode>
 cudaError_t launch_fwd_t(const AttnShape& s, const CUtensorMap& tq, const CUtensorMap& tk,
                          const CUtensorMap& tv, void* o, void* o_hp, float* stats,
-                         const int* kv_list, int topk, const uint8_t* q_sc, const uint8_t* k_sc,
-                         int* err, cudaStream_t stream) {
+                         const int* kv_list, int topk, int* err, cudaStream_t stream) {
   using L = FwdLayout<D>;
-  const int q_per_cta = (kMode == kAux || kMode == kFp4 ? 1 : 2) * kTile;
+  const int q_per_cta = (kMode == kAux ? 1 : 2) * kTile;
   const dim3 grid((s.Nq + q_per_cta - 1) / q_per_cta, s.H, s.B);
   cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D, kMode>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
   attn_fwd_kernel<D, kMode><<<grid, kThreads, L::kAlloc, stream>>>(
       tq, tk, tv, static_cast<__nv_bfloat16*>(o), static_cast<__nv_bfloat16*>(o_hp), stats, s.Nq,
-      s.Nkv, s.H, s.scale, s.causal, kv_list, topk, q_sc, k_sc, err);
+      s.Nkv, s.H, s.scale, s.causal, kv_list, topk, err);
   return cudaGetLastError();
 }
 
 template <int D>
 cudaError_t launch_fwd_d(const AttnShape& s, const CUtensorMap& tq, const CUtensorMap& tk,
                          const CUtensorMap& tv, void* o, void* o_hp, float* stats,
-                         const int* kv_list, int topk, const uint8_t* q_sc, const uint8_t* k_sc,
-                         int* err, cudaStream_t stream) {
+                         const int* kv_list, int topk, int* err, cudaStream_t stream) {
   if (kv_list != nullptr)
-    return launch_fwd_t<D, kSparse>(s, tq, tk, tv, o, o_hp, stats, kv_list, topk, q_sc, k_sc, err,
-                                    stream);
+    return launch_fwd_t<D, kSparse>(s, tq, tk, tv, o, o_hp, stats, kv_list, topk, err, stream);
   if (o_hp != nullptr)
-    return launch_fwd_t<D, kAux>(s, tq, tk, tv, o, o_hp, stats, kv_list, topk, q_sc, k_sc, err,
-                                 stream);
-  if (q_sc != nullptr)
-    return launch_fwd_t<D, kFp4>(s, tq, tk, tv, o, o_hp, stats, kv_list, topk, q_sc, k_sc, err,
-                                 stream);
-  return launch_fwd_t<D, kDense>(s, tq, tk, tv, o, o_hp, stats, kv_list, topk, q_sc, k_sc, err,
-                                 stream);
+    return launch_fwd_t<D, kAux>(s, tq, tk, tv, o, o_hp, stats, kv_list, topk, err, stream);
+  return launch_fwd_t<D, kDense>(s, tq, tk, tv, o, o_hp, stats, kv_list, topk, err, stream);
 }
 
 cudaError_t launch_attn_fwd(const AttnShape& s, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, void* o, void* o_hp, float* stats,
-                            const int* kv_list, int topk, const uint8_t* q_sc,
-                            const uint8_t* k_sc, int* err, cudaStream_t stream) {
-  if ((kv_list != nullptr) + (o_hp != nullptr) + (q_sc != nullptr) > 1 ||
-      (q_sc != nullptr) != (k_sc != nullptr))
-    return cudaErrorInvalidValue;
-  return s.D == 128 ? launch_fwd_d<128>(s, tq, tk, tv, o, o_hp, stats, kv_list, topk, q_sc, k_sc,
-                                        err, stream)
-                    : launch_fwd_d<64>(s, tq, tk, tv, o, o_hp, stats, kv_list, topk, q_sc, k_sc,
-                                       err, stream);
+                            const int* kv_list, int topk, int* err, cudaStream_t stream) {
+  if (kv_list != nullptr && o_hp != nullptr) return cudaErrorInvalidValue;
+  return s.D == 128 ? launch_fwd_d<128>(s, tq, tk, tv, o, o_hp, stats, kv_list, topk, err, stream)
+                    : launch_fwd_d<64>(s, tq, tk, tv, o, o_hp, stats, kv_list, topk, err, stream);
 }
 
 }  // namespace nvq

@@ -1,0 +1,466 @@
+// Attn-QAT forward with S = Q~ K~^T on block-scaled FP4 UMMAs (sm_103a).
+//
+// The same two passes as the BF16 forward ("Attn-QAT Training" guide,
+// "Architecture-specific Triton routing": statistics against the final row
+// max), computing the same values:
+//   pass 1: S = Q~ K~^T, m = rowmax(scale*S)
+//   pass 2: S again, P = exp(scale*S - m), l += sum P, P~ = fq16(P) per 16 keys,
+//           O += P~ V~ (F16 UMMA, P~ read from TMEM)
+//   epilogue: O / l -> bf16, LSE = m + ln l, m.
+// Q~ and K~ arrive as packed E2M1 codes with their E4M3 scales per 16 elements
+// of D (the quantizer's outputs); the kind::mxf4nvf4 UMMA multiplies the codes
+// and applies both scales, so each S element is the sum of the same exact
+// products code_q*s_q*code_k*s_k that a BF16 UMMA on Q~, K~ would add up.
+//
+// One 128-query tile per CTA; the four softmax warpgroups share every 128-key
+// tile, warpgroup w owning keys [32 w, 32 w + 32) of it.  S tiles live in TMEM
+// buffers of 128 columns: three in pass 1 (columns [0, 384); O is not live
+// yet), two in pass 2 (columns [0, 256), tile j in buffer j % 2), so the UMMAs
+// of the next tiles run while the softmax works on the current one.  P~ of a
+// tile is written over the first 16 of each warpgroup's 32 columns, which it
+// has already loaded, and P~V~ reads it from there.
+//
+// Every tcgen05 instruction and every mbarrier wait costs the issuing warp tens
+// of cycles, more in total than the tensor work of the small FP4 UMMAs, so the
+// UMMAs come from two warps: the S warp (the even pass-1 tiles and every
+// pass-2 S, with their scale copies) and the PV warp (the odd pass-1 tiles,
+// then P~V~).  Before the S warp overwrites a pass-2 buffer
+// it waits for the PV warp's commit of the P~V~ that read the buffer.
+//
+// TMEM: S buffers, O at [256, 256 + D) (pass 2), the Q~ scale operand at
+// [384 + 4 kk), the K~ scale operand of tile counter g at [392 + 8 (g % 3) +
+// 4 kk) (kk: 64-element group of D).  Three copies rotate: before the copy for
+// tile g the S warp has waited on a barrier that implies the UMMAs of tile
+// g - 3 completed (a released pass-1 buffer, or the P~V~ of pass-2 tile j,
+// which follows the softmax of tile j - 1), so a copy never overwrites scales
+// an UMMA in flight may still read.
+//
+// Roles (608 threads, one CTA per SM): warps 0-15 softmax, warp 16 TMA
+// producer, warp 17 TMEM allocator and S issuer, warp 18 P~V~ issuer
+// (converged warps, one elected lane issuing).  Shared memory: Q~ codes and
+// scales, a ring of K~ tiles (codes + scales), a ring of V~ tiles (f16).
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "nvq_internal.h"
+#include "nvq_ptx.cuh"
+#include "nvq_quant.cuh"
+
+namespace nvq {
+
+namespace {
+
+constexpr int kThreads = 608;
+constexpr int kSoftmaxWarps = 16;
+constexpr int kTmaWarp = 16;
+constexpr int kSWarp = 17;
+constexpr int kPvWarp = 18;
+constexpr int kKRing = 6;
+constexpr int kVRing = 4;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr uint32_t kScA = 384, kScB = 392;  // TMEM columns of the scale operands
+
+template <int D>
+struct Fp4Layout {
+  static constexpr uint32_t kCodeBytes = 128u * D / 2;   // codes of a 128-row tile
+  static constexpr uint32_t kScBytes = (D / 64) * 512u;  // its scale blocks
+  static constexpr uint32_t kKSlot = (kCodeBytes + kScBytes + 1023u) / 1024u * 1024u;
+  static constexpr uint32_t kVSlot = 128u * D * 2u;
+  static constexpr uint32_t kQ = 0;
+  static constexpr uint32_t kKRingOff = kKSlot;  // the Q~ tile takes one K~ slot's room
+  static constexpr uint32_t kVRingOff = kKRingOff + kKRing * kKSlot;
+  static constexpr uint32_t kX = kVRingOff + kVRing * kVSlot;  // [4 warpgroups][128] f32
+  static constexpr uint32_t kBars = kX + 4u * 128u * 4u;
+  // q_full, k_full/k_empty, v_full/v_empty, s1_full[3], s1_free[3], s_full[2],
+  // p_full[2], pv_done[2], o_full, drain x2, q_sc_ready
+  static constexpr uint32_t kNumBars = 1 + 2 * kKRing + 2 * kVRing + 12 + 4;
+  static constexpr uint32_t kTmemSlot = kBars + kNumBars * 8u;
+  static constexpr uint32_t kAbort = kTmemSlot + 4u;
+  static constexpr uint32_t kAlloc = kAbort + 4u + 1024u;
+};
+
+// Grid: (ceil(Nq / 128), H, B).
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_fp4_kernel(const __grid_constant__ CUtensorMap tq,
+                        const __grid_constant__ CUtensorMap tk,
+                        const __grid_constant__ CUtensorMap tv, const uint8_t* __restrict__ q_sc,
+                        const uint8_t* __restrict__ k_sc, __nv_bfloat16* __restrict__ o,
+                        float* __restrict__ stats, int Nq, int Nkv, int H, float scale,
+                        int causal, int* __restrict__ err) {
+  using L = Fp4Layout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023u) &
+                                             ~static_cast<uintptr_t>(1023u));
+  const int warp = threadIdx.x >> 5;
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int qt = blockIdx.x;
+  const int q0 = qt * kTile;
+  const int64_t bh = static_cast<int64_t>(b) * H + h;
+
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBars);
+  uint64_t* q_full = bars;
+  uint64_t* k_full = bars + 1;           // [kKRing]
+  uint64_t* k_empty = k_full + kKRing;   // [kKRing]
+  uint64_t* v_full = k_empty + kKRing;   // [kVRing]
+  uint64_t* v_empty = v_full + kVRing;   // [kVRing]
+  uint64_t* s1_full = v_empty + kVRing;  // pass 1 [3]
+  uint64_t* s1_free = s1_full + 3;       // pass 1 [3]
+  uint64_t* s_full = s1_free + 3;        // pass 2 [2]
+  uint64_t* p_full = s_full + 2;         // pass 2 [2]
+  uint64_t* pv_done = p_full + 2;        // pass 2 [2]
+  uint64_t* o_full = pv_done + 2;
+  uint64_t* drain = o_full + 1;          // [2]: S warp, PV warp
+  uint64_t* q_sc_ready = drain + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kAbort);
+
+  const int n_kt = (Nkv + kTile - 1) / kTile;
+  const int n_qt = (Nq + kTile - 1) / kTile;
+  // key tiles this query tile sees (causal: up to its diagonal tile)
+  const int nk = causal ? min(n_kt, qt + 1) : n_kt;
+
+  if (threadIdx.x == 0) {
+    *abort = 0;
+    mbar_init(q_full, 1);
+    for (int s = 0; s < kKRing; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+    }
+    for (int s = 0; s < kVRing; ++s) {
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
+    }
+    for (int i = 0; i < 3; ++i) {
+      mbar_init(&s1_full[i], 1);
+      mbar_init(&s1_free[i], kSoftmaxWarps);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&p_full[i], kSoftmaxWarps);
+      mbar_init(&pv_done[i], 1);
+      mbar_init(&drain[i], 1);
+    }
+    mbar_init(o_full, 1);
+    mbar_init(q_sc_ready, 1);
+    fence_mbar_init();
+  }
+  if (warp == kSWarp) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  // S into TMEM column `col` = Q~ K~^T for K~ load `kl` (loads are numbered in
+  // the producer's order), tile counter g (which scale copy), completion on
+  // `bar`; the K~ slot is released after the UMMAs.  Issued by a converged warp.
+  constexpr uint32_t idesc_s = idesc_mxf4nvf4(128, 128);
+  constexpr uint32_t lay = D == 128 ? 4u : 6u;  // (D/2)-byte swizzle of the code rows
+  constexpr uint32_t sbo = 8u * (D / 2);
+  const uint32_t q_addr = smem_u32(smem + L::kQ);
+  const uint32_t k_ring = smem_u32(smem + L::kKRingOff);
+  auto issue_s = [&](uint32_t col, int kl, int g, uint64_t* bar) -> bool {
+    const int slot = kl % kKRing;
+    if (!mbar_wait_warp(&k_full[slot], static_cast<uint32_t>((kl / kKRing) & 1), abort))
+      return false;
+    tc_fence_after();
+    const uint32_t kb = k_ring + slot * L::kKSlot;
+    const uint32_t sc = kScB + 8u * static_cast<uint32_t>(g % 3);
+#pragma unroll
+    for (int kk = 0; kk < D / 64; ++kk)
+      tmem_cp_32x128_x4_w(tmem + sc + 4 * kk, kb + L::kCodeBytes + kk * 512);
+#pragma unroll
+    for (int kk = 0; kk < D / 64; ++kk)
+      umma_fp4_ss_w(tmem + col, sdesc(q_addr + 32 * kk, 16, sbo, lay),
+                    sdesc(kb + 32 * kk, 16, sbo, lay), idesc_s, tmem + kScA + 4 * kk,
+                    tmem + sc + 4 * kk, kk > 0 ? 1u : 0u);
+    umma_commit_w(bar);
+    umma_commit_w(&k_empty[slot]);
+    return true;
+  };
+  // Pass 1, tile j (load j) into buffer j % 3 once the softmax has loaded tile
+  // j - 3 from there (which also means tile j - 3's UMMAs, the last readers of
+  // the scale copy j reuses, completed).  The S warp takes the even tiles, the
+  // P~V~ warp (idle until pass 2) the odd ones.
+  auto pass1 = [&](int first) -> bool {
+    bool ok = true;
+    for (int j = first; j < nk && ok; j += 2) {
+      const int buf = j % 3;
+      if (j >= 3 &&
+          !(ok = mbar_wait_warp(&s1_free[buf], static_cast<uint32_t>((j / 3 - 1) & 1), abort)))
+        break;
+      ok = issue_s(128u * buf, j, j, &s1_full[buf]);
+    }
+    return ok;
+  };
+
+  if (warp == kTmaWarp) {
+    // ------------------------------------------------------------ producer
+    // Q~; pass 1: K(j) for every tile j; pass 2: K(0), K(1), then per tile
+    // V(j) and K(j + 2) (the order the two UMMA warps first use them in).
+    tma_prefetch_desc(&tq);
+    tma_prefetch_desc(&tk);
+    tma_prefetch_desc(&tv);
+    mbar_arrive_expect_tx_w(q_full, L::kCodeBytes + L::kScBytes);
+    tma_load_4d_w(smem + L::kQ, &tq, 0, q0, h, b, q_full);
+    bulk_load_w(smem + L::kQ + L::kCodeBytes, q_sc + (bh * n_qt + qt) * L::kScBytes, L::kScBytes,
+                q_full);
+    int k_last[kKRing], v_last[kVRing];
+    for (int s = 0; s < kKRing; ++s) k_last[s] = -1;
+    for (int s = 0; s < kVRing; ++s) v_last[s] = -1;
+    int kli = 0, vli = 0;
+    bool ok = true;
+    auto load_k = [&](int tile) -> bool {
+      const int slot = kli % kKRing;
+      const uint32_t use = static_cast<uint32_t>(kli / kKRing);
+      if (!mbar_wait_warp(&k_empty[slot], (use & 1u) ^ 1u, abort)) return false;
+      uint8_t* dst = smem + L::kKRingOff + slot * L::kKSlot;
+      mbar_arrive_expect_tx_w(&k_full[slot], L::kCodeBytes + L::kScBytes);
+      tma_load_4d_w(dst, &tk, 0, tile * kTile, h, b, &k_full[slot]);
+      bulk_load_w(dst + L::kCodeBytes, k_sc + (bh * n_kt + tile) * L::kScBytes, L::kScBytes,
+                  &k_full[slot]);
+      k_last[slot] = static_cast<int>(use & 1u);
+      ++kli;
+      return true;
+    };
+    auto load_v = [&](int tile) -> bool {
+      const int slot = vli % kVRing;
+      const uint32_t use = static_cast<uint32_t>(vli / kVRing);
+      if (!mbar_wait_warp(&v_empty[slot], (use & 1u) ^ 1u, abort)) return false;
+      uint8_t* dst = smem + L::kVRingOff + slot * L::kVSlot;
+      mbar_arrive_expect_tx_w(&v_full[slot], L::kVSlot);
+#pragma unroll
+      for (int blk = 0; blk < D / 64; ++blk)
+        tma_load_4d_w(dst + blk * (128u * 128u), &tv, blk * 64, tile * kTile, h, b, &v_full[slot]);
+      v_last[slot] = static_cast<int>(use & 1u);
+      ++vli;
+      return true;
+    };
+    for (int j = 0; j < nk && ok; ++j) ok = load_k(j);
+    for (int j = 0; j < 2 && j < nk && ok; ++j) ok = load_k(j);
+    for (int j = 0; j < nk && ok; ++j) {
+      ok = load_v(j);
+      if (ok && j + 2 < nk) ok = load_k(j + 2);
+    }
+    if (!ok) {  // let the copies in flight land before the block exits
+      mbar_wait_warp(q_full, 0, nullptr, 10000000ull);
+      for (int s = 0; s < kKRing; ++s)
+        if (k_last[s] >= 0)
+          mbar_wait_warp(&k_full[s], static_cast<uint32_t>(k_last[s]), nullptr, 10000000ull);
+      for (int s = 0; s < kVRing; ++s)
+        if (v_last[s] >= 0)
+          mbar_wait_warp(&v_full[s], static_cast<uint32_t>(v_last[s]), nullptr, 10000000ull);
+    }
+  } else if (warp == kSWarp) {
+    // ------------------------------------------------------------ S issuer
+    bool ok = mbar_wait_warp(q_full, 0, abort);
+    if (ok) {  // the Q~ scales stay in TMEM for the whole kernel
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < D / 64; ++kk)
+        tmem_cp_32x128_x4_w(tmem + kScA + 4 * kk, q_addr + L::kCodeBytes + kk * 512);
+      // the P~V~ warp issues S UMMAs that read them: signal the copy's completion
+      umma_commit_w(q_sc_ready);
+    }
+    if (ok) ok = pass1(0);
+    // every pass-1 buffer released (pass 2 reuses the columns)
+    for (int buf = 0; buf < 3 && ok; ++buf) {
+      const int uses = (nk - buf + 2) / 3;  // tiles j < nk with j % 3 == buf
+      if (uses > 0)
+        ok = mbar_wait_warp(&s1_free[buf], static_cast<uint32_t>((uses - 1) & 1), abort);
+    }
+    // Pass 2 (tile counter g = nk + j): tiles 0 and 1 at once, then tile j + 2
+    // into buffer j % 2 once the P~V~ of tile j, the last reader of its P~, is done.
+    for (int j = 0; j < 2 && j < nk && ok; ++j) ok = issue_s(128u * j, nk + j, nk + j, &s_full[j]);
+    for (int j = 0; j + 2 < nk && ok; ++j) {
+      const int buf = j & 1;
+      if (!(ok = mbar_wait_warp(&pv_done[buf], static_cast<uint32_t>((j >> 1) & 1), abort))) break;
+      ok = issue_s(128u * buf, nk + j + 2, nk + j + 2, &s_full[buf]);
+    }
+    umma_commit_w(&drain[0]);
+    mbar_wait_warp(&drain[0], 0, nullptr, 10000000ull);
+  } else if (warp == kPvWarp) {
+    // ------------------------------------------------------------ P~V~ issuer
+    constexpr uint32_t idesc_pv = idesc_f16(128, D, 0, 0, 1);
+    const uint32_t v_ring = smem_u32(smem + L::kVRingOff);
+    // the Q~ scale copy (S warp) precedes the odd pass-1 tiles' UMMAs
+    bool ok = mbar_wait_warp(q_sc_ready, 0, abort);
+    if (ok) {
+      tc_fence_after();
+      ok = pass1(1);
+    }
+    for (int j = 0; j < nk && ok; ++j) {
+      const int buf = j & 1, slot = j % kVRing;
+      if (!(ok = mbar_wait_warp(&v_full[slot], static_cast<uint32_t>((j / kVRing) & 1), abort))) break;
+      if (!(ok = mbar_wait_warp(&p_full[buf], static_cast<uint32_t>((j >> 1) & 1), abort))) break;
+      tc_fence_after();
+      const uint32_t vb = v_ring + slot * L::kVSlot;
+      // keys [16 kk, 16 kk + 16): warpgroup kk / 2, its P~ columns 8 (kk % 2)
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        umma_f16_ts_w(tmem + 256, tmem + 128 * buf + 32 * (kk >> 1) + 8 * (kk & 1),
+                      sdesc_sw128(vb + kk * 2048, 128u * 128u, 1024), idesc_pv,
+                      (j > 0 || kk > 0) ? 1u : 0u);
+      umma_commit_w(&pv_done[buf]);
+      umma_commit_w(&v_empty[slot]);
+    }
+    if (ok) umma_commit_w(o_full);
+    umma_commit_w(&drain[1]);
+    mbar_wait_warp(&drain[1], 0, nullptr, 10000000ull);
+  } else if (warp < kSoftmaxWarps) {
+    // ------------------------------------------------------------ softmax
+    const int wg = warp >> 2;            // keys [32 wg, 32 wg + 32) of every tile
+    const int t = threadIdx.x & 127;     // query row in the tile == TMEM lane
+    const int qrow = q0 + t;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const float c1 = scale * kLog2e;
+    float* xchg = reinterpret_cast<float*>(smem + L::kX);  // [4][128]
+    auto key0 = [&](int j) { return j * kTile + 32 * wg; };
+    auto is_edge = [&](int k0) { return k0 + 32 > Nkv || (causal && k0 + 31 > q0); };
+    bool ok = true;
+    float mraw = -INFINITY;
+    uint32_t r[32];
+    for (int j = 0; j < nk && ok; ++j) {
+      const int buf = j % 3;
+      if (!(ok = mbar_wait_warp(&s1_full[buf], static_cast<uint32_t>((j / 3) & 1), abort))) break;
+      tc_fence_after();
+      tmem_ld32(tmem + lane_base + 128 * buf + 32 * wg, r);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive_warp(&s1_free[buf]);
+      const int k0 = key0(j);
+      if (!is_edge(k0)) {
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) mraw = max3f(mraw, __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int key = k0 + i;
+          if (key < Nkv && (!causal || key <= qrow)) mraw = fmaxf(mraw, __uint_as_float(r[i]));
+        }
+      }
+    }
+    // row maximum over the four warpgroups (always reached, also after an abort)
+    xchg[wg * 128 + t] = mraw;
+    named_bar_sync(1, 512);
+    mraw = fmaxf(fmaxf(xchg[t], xchg[128 + t]), fmaxf(xchg[256 + t], xchg[384 + t]));
+    named_bar_sync(1, 512);  // read before the sums reuse the area
+    const float m = mraw * scale;
+    const float negmb = -m * kLog2e;
+    const uint64_t c12 = pk2(c1, c1), nmb2 = pk2(negmb, negmb);
+    uint64_t l2 = pk2(0.f, 0.f);
+    for (int j = 0; j < nk && ok; ++j) {
+      const int buf = j & 1;
+      if (!(ok = mbar_wait_warp(&s_full[buf], static_cast<uint32_t>((j >> 1) & 1), abort))) break;
+      tc_fence_after();
+      const uint32_t col = 128u * buf + 32u * wg;
+      tmem_ld32(tmem + lane_base + col, r);
+      tmem_wait_ld();
+      float x[32];
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        up2(fma2(pk2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), c12, nmb2),
+            x[2 * i], x[2 * i + 1]);
+      const int k0 = key0(j);
+      if (is_edge(k0)) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int key = k0 + i;
+          if (!(key < Nkv && (!causal || key <= qrow))) x[i] = -INFINITY;
+        }
+      }
+      uint32_t pt[16];  // P~ of these 32 keys as f16 pairs
+#pragma unroll
+      for (int hb = 0; hb < 2; ++hb) {
+        float pp[16];
+        uint32_t (&ph)[8] = *reinterpret_cast<uint32_t(*)[8]>(pt + 8 * hb);
+        pquant16(x + 16 * hb, pp, ph);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) l2 = add2(l2, pk2(pp[2 * u], pp[2 * u + 1]));
+      }
+      tmem_st16(tmem + lane_base + col, pt);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive_warp(&p_full[buf]);
+    }
+    float l_lo, l_hi;
+    up2(l2, l_lo, l_hi);
+    float l = l_lo + l_hi;
+    const bool have_o = ok && mbar_wait_warp(o_full, 0, abort);
+    xchg[wg * 128 + t] = l;
+    named_bar_sync(1, 512);
+    l = (xchg[t] + xchg[128 + t]) + (xchg[256 + t] + xchg[384 + t]);
+    if (have_o) {
+      tc_fence_after();
+      const float inv_l = 1.0f / l;
+      // warpgroup wg writes O columns [wg D/4, (wg + 1) D/4)
+      constexpr int kCols = D / 4;
+      const uint32_t o_col = 256u + static_cast<uint32_t>(wg * kCols);
+      uint32_t w[kCols / 2];
+      if constexpr (kCols == 32) {
+        tmem_ld32(tmem + lane_base + o_col, r);
+      } else {
+        uint32_t (&r16)[16] = *reinterpret_cast<uint32_t(*)[16]>(r);
+        tmem_ld16(tmem + lane_base + o_col, r16);
+      }
+      tmem_wait_ld();
+      if (qrow < Nq) {
+#pragma unroll
+        for (int i = 0; i < kCols / 2; ++i) {
+          __nv_bfloat162 v2 = __floats2bfloat162_rn(__uint_as_float(r[2 * i]) * inv_l,
+                                                    __uint_as_float(r[2 * i + 1]) * inv_l);
+          w[i] = *reinterpret_cast<uint32_t*>(&v2);
+        }
+        __nv_bfloat16* orow = o + ((static_cast<int64_t>(b) * Nq + qrow) * H + h) * D + wg * kCols;
+        uint4* dst = reinterpret_cast<uint4*>(orow);
+#pragma unroll
+        for (int u = 0; u < kCols / 8; ++u)
+          dst[u] = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+        if (wg == 0) {
+          float* st = stats + bh * 2 * Nq;
+          st[qrow] = m + logf(l);
+          st[Nq + qrow] = m;
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  report_abort(abort, err);
+  if (warp == kSWarp) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D>
+cudaError_t launch_fp4_d(const AttnShape& s, const CUtensorMap& tq, const CUtensorMap& tk,
+                         const CUtensorMap& tv, const uint8_t* q_sc, const uint8_t* k_sc, void* o,
+                         float* stats, int* err, cudaStream_t stream) {
+  using L = Fp4Layout<D>;
+  static_assert(L::kAlloc <= 227u * 1024u, "shared memory");
+  const dim3 grid((s.Nq + kTile - 1) / kTile, s.H, s.B);
+  cudaError_t e = cudaFuncSetAttribute(attn_fwd_fp4_kernel<D>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
+  if (e != cudaSuccess) return e;
+  attn_fwd_fp4_kernel<D><<<grid, kThreads, L::kAlloc, stream>>>(
+      tq, tk, tv, q_sc, k_sc, static_cast<__nv_bfloat16*>(o), stats, s.Nq, s.Nkv, s.H, s.scale,
+      s.causal, err);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attn_fwd_fp4(const AttnShape& s, const CUtensorMap& tq, const CUtensorMap& tk,
+                                const CUtensorMap& tv, const uint8_t* q_sc, const uint8_t* k_sc,
+                                void* o, float* stats, int* err, cudaStream_t stream) {
+  return s.D == 128 ? launch_fp4_d<128>(s, tq, tk, tv, q_sc, k_sc, o, stats, err, stream)
+                    : launch_fp4_d<64>(s, tq, tk, tv, q_sc, k_sc, o, stats, err, stream);
+}
+
+}  // namespace nvq

@@ -79,14 +79,16 @@ int make_bnhd_map(CUtensorMap* map, const void* base, int B, int N, int H, int D
                    int box_rows = kTile);
 
 // kv_list: NULL (dense) or int32 [B, H, ceil(Nq/128), topk] key tiles per query tile;
-// o_hp: NULL or the auxiliary output P V~ / l (bf16, layout of o); q_sc, k_sc:
-// NULL, or the FP4 scale blocks of Q~ and K~ (launch_quant_attn_fp4), in which
-// case tq and tk map their packed codes (make_bnhd_u8_map) and S runs on FP4
-// UMMAs.  At most one of the three.
+// o_hp: NULL or the auxiliary output P V~ / l (bf16, layout of o); not both
 cudaError_t launch_attn_fwd(const AttnShape& s, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, void* o, void* o_hp, float* stats,
-                            const int* kv_list, int topk, const uint8_t* q_sc,
-                            const uint8_t* k_sc, int* err, cudaStream_t stream);
+                            const int* kv_list, int topk, int* err, cudaStream_t stream);
+// Dense forward with S on FP4 UMMAs: tq, tk map the packed codes of Q~ and K~
+// (make_bnhd_u8_map), q_sc, k_sc their scale blocks (launch_quant_attn_fp4),
+// tv the f16 V~ (make_bnhd_map).
+cudaError_t launch_attn_fwd_fp4(const AttnShape& s, const CUtensorMap& tq, const CUtensorMap& tk,
+                                const CUtensorMap& tv, const uint8_t* q_sc, const uint8_t* k_sc,
+                                void* o, float* stats, int* err, cudaStream_t stream);
 cudaError_t launch_bwd_prep(const AttnShape& s, const void* o, const void* dout, float* delta,
                             cudaStream_t stream);
 // dK, dV (key-outer; Q~, K~, V~, dO maps with 128-row boxes).  Block-sparse:
