@@ -288,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---- P part: S -> P, P~/l
       if (!(ok = mbar_wait_warp(s_full, ph, abort))) break;
       tc_fence_after();
-      uint32_t ph2[16];  // P as f16x2 pairs (A = P/l feeds no rounding decision)
+      float pp0[16], pp1[16];  // P (fp32) of this thread's 32 keys, for dS
       {
         tmem_ld32(tmem + lane_base + key_col, r);
         tmem_wait_ld();
@@ -304,7 +304,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!(row_ok && key < Nkv && (!causal || key <= qrow))) x[i] = -INFINITY;
           }
         }
-        float pp0[16], pp1[16];
         uint32_t ptw0[8], ptw1[8];  // P~ / l as bf16x2
         pquant16_scaled_bf16(x, inv_l, pp0, ptw0);
         pquant16_scaled_bf16(x + 16, inv_l, pp1, ptw1);
@@ -319,29 +318,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         fence_proxy_async_smem();
         mbar_arrive_warp(pt_full);
-        // P for dS, packed after the P~/l hand-off
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          ph2[u] = pack_f16x2_rn(pp0[2 * u], pp0[2 * u + 1]);
-          ph2[8 + u] = pack_f16x2_rn(pp1[2 * u], pp1[2 * u + 1]);
-        }
       }
       // ---- dS part: dP -> dS = scale * A * (dP - delta), A = P / l
       if (!(ok = mbar_wait_warp(dp_full, ph, abort))) break;
       tc_fence_after();
       uint32_t dsw[16];
       {
+        // dP in two halves of 16 keys (P stays in fp32 registers meanwhile)
         const uint64_t ndl2 = pk2(-dl, -dl);
         const uint64_t sl2 = pk2(scale * inv_l, scale * inv_l);
-        tmem_ld32(tmem + lane_base + 128 + key_col, r);
-        tmem_wait_ld();
 #pragma unroll
-        for (int u = 0; u < 16; ++u) {
-          const uint64_t a2 = mul2(pk2(f16lo_to_f32(ph2[u]), f16hi_to_f32(ph2[u])), sl2);
-          const uint64_t d2 = add2(pk2(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1])), ndl2);
-          float d0, d1;
-          up2(mul2(a2, d2), d0, d1);
-          dsw[u] = pack_bf16(d0, d1);
+        for (int hv = 0; hv < 2; ++hv) {
+          uint32_t (&r16)[16] = *reinterpret_cast<uint32_t(*)[16]>(r);
+          const float* pp = hv ? pp1 : pp0;
+          tmem_ld16(tmem + lane_base + 128 + key_col + 16 * hv, r16);
+          tmem_wait_ld();
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const uint64_t a2 = mul2(pk2(pp[2 * u], pp[2 * u + 1]), sl2);
+            const uint64_t d2 = add2(pk2(__uint_as_float(r16[2 * u]), __uint_as_float(r16[2 * u + 1])), ndl2);
+            float d0, d1;
+            up2(mul2(a2, d2), d0, d1);
+            dsw[8 * hv + u] = pack_bf16(d0, d1);
+          }
         }
       }
       tc_fence_before();
