@@ -244,10 +244,12 @@ FwdWs fwd_ws(int B, int Nq, int Nkv, int H, int D) {
   return w;
 }
 
+// Backward workspace: Q~, K~, V~ (bf16) and delta; block-sparse (topk > 0):
+// the transposed tile lists; dense: the packed codes and scale blocks of Q~
+// and K~ for the FP4 S of the dQ kernel.
 struct BwdWs {
-  size_t q, k, v, delta, q_off, q_list, total;
+  size_t q, k, v, delta, q_off, q_list, qc, kc, qs, ks, total;
 };
-// topk > 0: block-sparse, with room for the transposed tile lists
 BwdWs bwd_ws(int B, int Nq, int Nkv, int H, int D, int topk = 0) {
   BwdWs w;
   w.q = 0;
@@ -256,7 +258,15 @@ BwdWs bwd_ws(int B, int Nq, int Nkv, int H, int D, int topk = 0) {
   w.delta = round_up(w.v + bytes_bnhd(B, Nkv, H, D, 2), 256);
   w.q_off = round_up(w.delta + static_cast<size_t>(B) * H * Nq * 4, 256);
   w.q_list = w.q_off;
+  w.qc = w.kc = w.qs = w.ks = w.q_off;
   w.total = w.q_off;
+  if (topk <= 0) {
+    w.qc = w.q_off;
+    w.kc = round_up(w.qc + bytes_bnhd(B, Nq, H, D, 1) / 2, 256);
+    w.qs = round_up(w.kc + bytes_bnhd(B, Nkv, H, D, 1) / 2, 256);
+    w.ks = round_up(w.qs + attn_fp4_scale_bytes(B, Nq, H, D), 256);
+    w.total = round_up(w.ks + attn_fp4_scale_bytes(B, Nkv, H, D), 256);
+  }
   if (topk > 0) {
     const size_t n_qt = (Nq + kTile - 1) / kTile, n_kt = (Nkv + kTile - 1) / kTile;
     w.q_list = round_up(w.q_off + static_cast<size_t>(B) * H * (n_kt + 1) * 4, 256);
@@ -399,6 +409,29 @@ nvq_status bwd_impl(const void* q, const void* k, const void* v, const void* o,
                                 n_qt * topk, err, stream);
        })) != cudaSuccess)
     return fail_cuda("attn_bwd (dK, dV)", e);
+  if (kv_list == nullptr) {
+    // dense: dQ with S on FP4 UMMAs over the codes and scale blocks of Q~, K~
+    uint8_t* qc = wb + w.qc;
+    uint8_t* kc = wb + w.kc;
+    uint8_t* qs = wb + w.qs;
+    uint8_t* ks = wb + w.ks;
+    CUtensorMap mq4, mk4;
+    if ((r = make_bnhd_u8_map(&mq4, qc, B, Nq, H, D)) != 0 ||
+        (r = make_bnhd_u8_map(&mk4, kc, B, Nkv, H, D)) != 0)
+      return fail_driver("cuTensorMapEncodeTiled", r);
+    if ((e = timed(NVQ_KERNEL_QUANTIZE, stream, [&] {
+           return launch_quant_attn_fp4(q, B, Nq, H, D, qc, qs, stream);
+         })) != cudaSuccess)
+      return fail_cuda("quantize q (fp4)", e);
+    if ((e = timed(NVQ_KERNEL_QUANTIZE, stream, [&] {
+           return launch_quant_attn_fp4(k, B, Nkv, H, D, kc, ks, stream);
+         })) != cudaSuccess)
+      return fail_cuda("quantize k (fp4)", e);
+    return from_cuda("attn_bwd_dq", timed(NVQ_KERNEL_BWD_DQ, stream, [&] {
+                       return launch_attn_bwd_dq_fp4(s, mq4, mdo, mk4, mk, mv, qs, ks, stats,
+                                                     delta, dq, err, stream);
+                     }));
+  }
   return from_cuda("attn_bwd_dq", timed(NVQ_KERNEL_BWD_DQ, stream, [&] {
                      return launch_attn_bwd_dq(s, mq, mdo, mk, mv, stats, delta, dq, kv_list, topk,
                                                err, stream);

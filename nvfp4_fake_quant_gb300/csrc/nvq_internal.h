@@ -107,6 +107,15 @@ cudaError_t launch_attn_bwd_dq(const AttnShape& s, const CUtensorMap& tq, const 
                                const float* delta, void* dq, const int* kv_list, int topk,
                                int* err, cudaStream_t stream);
 
+// dQ with S on FP4 UMMAs (dense): tq4, tk4 map the packed codes of Q~ and K~
+// (make_bnhd_u8_map), q_sc, k_sc their scale blocks; tdo, tk, tv the bf16 dO,
+// K~, V~ (128-row boxes).
+cudaError_t launch_attn_bwd_dq_fp4(const AttnShape& s, const CUtensorMap& tq4,
+                                   const CUtensorMap& tdo, const CUtensorMap& tk4,
+                                   const CUtensorMap& tk, const CUtensorMap& tv,
+                                   const uint8_t* q_sc, const uint8_t* k_sc, const float* stats,
+                                   const float* delta, void* dq, int* err, cudaStream_t stream);
+
 // Token rows [B, T*Hh*W, H, D] (bf16) between raster and cube order.
 cudaError_t launch_vsa_reorder(const void* x, int B, int T, int Hh, int W, int H, int D, int ct,
                                int ch, int cw, int to_cubes, void* out, cudaStream_t stream);

@@ -60,7 +60,11 @@ def test_workspace_sizes(lib):
     b, n, h, d = 1, 25088, 12, 128
     t = b * n * h * d * 2
     assert lib.attn_qat_fwd_workspace(b, n, n, h, d) == 3 * t
-    assert lib.attn_qat_bwd_workspace(b, n, n, h, d) == 3 * t + b * h * n * 4
+    # Q~, K~, V~ (bf16), delta, then the E2M1 codes (D/2 bytes a row) and the
+    # 512-byte scale blocks (one per 128 rows and 64 elements of D) of Q~ and K~
+    codes = b * n * h * d // 2
+    scales = b * h * ((n + 127) // 128) * (d // 64) * 512
+    assert lib.attn_qat_bwd_workspace(b, n, n, h, d) == 3 * t + b * h * n * 4 + 2 * codes + 2 * scales
     assert lib.attn_qat_fwd_workspace(0, n, n, h, d) == 0
     assert lib.attn_qat_fwd_workspace(1, 3, 5, 1, 64) % 256 == 0
 
@@ -150,9 +154,10 @@ def test_block_sparse_and_vsa_calls_reject_bad_arguments(lib):
     n, h, d = 25088, 12, 128
     assert lib.vsa_select_workspace(1, n, h, d) == 2 * 12 * 196 * 128 * 4
     assert lib.vsa_select_workspace(1, n - 8, h, d) == 0
-    dense = lib.attn_qat_bwd_workspace(1, n, n, h, d)
+    # Q~, K~, V~ (bf16) and delta as in the dense backward (without its FP4 operands)
+    common = 3 * n * h * d * 2 + h * n * 4
     offsets = (12 * 197 * 4 + 255) // 256 * 256  # [B, H, n_tiles + 1] int32, 256-byte aligned
-    assert lib.attn_qat_bwd_sparse_workspace(1, n, h, d, 20) == dense + offsets + 12 * 196 * 20 * 4
+    assert lib.attn_qat_bwd_sparse_workspace(1, n, h, d, 20) == common + offsets + 12 * 196 * 20 * 4
     big = 1 << 40
 
     def reorder(x=A, out=A + 4096, t=8, hh=8, w=16, ct=4, ch=4, cw=8, to_cubes=1):

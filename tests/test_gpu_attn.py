@@ -156,7 +156,7 @@ def test_kernel_timing_hook_counts_every_launch():
     finally:
         api.timing_enable(False)
     assert {k: n for k, (n, _) in got.items()} == {
-        "quantize": 6, "attn_fwd": 1, "bwd_delta": 1, "bwd_dkdv": 1, "bwd_dq": 1, "global_sf": 0,
+        "quantize": 8, "attn_fwd": 1, "bwd_delta": 1, "bwd_dkdv": 1, "bwd_dq": 1, "global_sf": 0,
         "vsa": 0, "linear": 0}
     assert all(ms > 0 for n, ms in got.values() if n)
     assert sum(ms for _, ms in got.values()) <= wall_ms
