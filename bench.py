@@ -52,9 +52,9 @@ def kernel_work(kind, b, n, h, d):
     gemm = 2.0 * b * h * n * n * d  # one N x N x D contraction per (batch, head)
     rows = b * n * h * d * 2.0      # one bf16 [B, N, H, D] tensor
     table = {
-        "attn_fwd": (3 * gemm, "flop", "tensor"),   # S (pass 1), S (pass 2), P~ V~
+        "attn_fwd": (3 * gemm, "flop", "tensor"),   # S (pass 1), S (pass 2) on FP4 UMMAs, P~ V~
         "bwd_dkdv": (4 * gemm, "flop", "tensor"),   # S, dP, dV, dK
-        "bwd_dq": (3 * gemm, "flop", "tensor"),     # S, dP, dQ
+        "bwd_dq": (3 * gemm, "flop", "tensor"),     # S (FP4 UMMAs), dP, dQ
         "quantize": (2 * rows, "byte", "hbm"),      # one of q, k, v: read + write
         "bwd_delta": (2 * rows + b * h * n * 4.0, "byte", "hbm"),  # o, dO in, delta out
     }
@@ -66,12 +66,12 @@ def kernel_work(kind, b, n, h, d):
 # (profiles/traffic_attn_kernels_wan25088.md), with the SHA-256 of the kernel's
 # sources at the time: a changed source reports null.
 TRAFFIC = {
-    "bwd_dkdv": {"bytes": 437230336, "sources": ['nvfp4_fake_quant_gb300/csrc/attn_bwd.cu', 'nvfp4_fake_quant_gb300/csrc/nvq_ptx.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_quant.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_internal.h'],
-               "sha256": "38695c9806cad52a9b2ec4501805e86ea3812d84d2a789d4cfdc6c77563c076d"},
-    "bwd_dq": {"bytes": 373778176, "sources": ['nvfp4_fake_quant_gb300/csrc/attn_bwd_dq.cu', 'nvfp4_fake_quant_gb300/csrc/nvq_ptx.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_quant.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_internal.h'],
-               "sha256": "43af392edd85ba19e34ce9ca6cabe66cc2500e69f25d1228c7dd0980d8eb7f5e"},
-    "attn_fwd": {"bytes": 296573440, "sources": ['nvfp4_fake_quant_gb300/csrc/attn_fwd.cu', 'nvfp4_fake_quant_gb300/csrc/nvq_ptx.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_quant.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_internal.h'],
-               "sha256": "aa7567deabe820611e4c9d305e6c4a897925eea13153c00cd19d1c39563fc5e3"},
+    "bwd_dkdv": {"bytes": 437740544, "sources": ['nvfp4_fake_quant_gb300/csrc/attn_bwd.cu', 'nvfp4_fake_quant_gb300/csrc/nvq_ptx.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_quant.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_internal.h'],
+                "sha256": "c3d35646ea1284d62a9e1bfa7558b5aad1cff2ba87185988cb0519c5ec0cf1c5"},
+    "bwd_dq": {"bytes": 347812352, "sources": ['nvfp4_fake_quant_gb300/csrc/attn_bwd_dq_fp4.cu', 'nvfp4_fake_quant_gb300/csrc/nvq_ptx.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_quant.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_internal.h'],
+              "sha256": "e6e2ce98180633aa19fd38476566b05743407f45b6ffdae1bc5781a4e83f04dc"},
+    "attn_fwd": {"bytes": 173137408, "sources": ['nvfp4_fake_quant_gb300/csrc/attn_fwd_fp4.cu', 'nvfp4_fake_quant_gb300/csrc/nvq_ptx.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_quant.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_internal.h'],
+                "sha256": "93d0e2c52e05a445da8a3ad9ee3f950e69827a2f4feeb514997a7a872bf363ba"},
 }
 
 
