@@ -28,12 +28,15 @@
 // it waits for the PV warp's commit of the P~V~ that read the buffer.
 //
 // TMEM: S buffers, O at [256, 256 + D) (pass 2), the Q~ scale operand at
-// [384 + 4 kk), the K~ scale operand of tile counter g at [392 + 8 (g % 3) +
-// 4 kk) (kk: 64-element group of D).  Three copies rotate: before the copy for
-// tile g the S warp has waited on a barrier that implies the UMMAs of tile
-// g - 3 completed (a released pass-1 buffer, or the P~V~ of pass-2 tile j,
-// which follows the softmax of tile j - 1), so a copy never overwrites scales
-// an UMMA in flight may still read.
+// [384 + 4 kk), the K~ scale operand of tile counter g at [392 + 8 (g % 6) +
+// 4 kk) (kk: 64-element group of D).  The issuing warp copies a tile's scales
+// before it waits for the tile's S buffer, so the copy is off the path from
+// "buffer released" to "UMMA running".  Six copies rotate: when a warp copies
+// the scales of tile g it has already waited on a barrier implying that the
+// UMMAs of tile g - 6 completed (pass 1: the release of tile g - 5, which the
+// softmax arrives on after loading tile g - 6; pass 2: the P~V~ of the tile
+// before, which follows the softmax of tile g - 4), so a copy never overwrites
+// scales an UMMA in flight may still read.
 //
 // Roles (608 threads, one CTA per SM): warps 0-15 softmax, warp 16 TMA
 // producer, warp 17 TMEM allocator and S issuer, warp 18 P~V~ issuer
@@ -162,16 +165,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t sbo = 8u * (D / 2);
   const uint32_t q_addr = smem_u32(smem + L::kQ);
   const uint32_t k_ring = smem_u32(smem + L::kKRingOff);
-  auto issue_s = [&](uint32_t col, int kl, int g, uint64_t* bar) -> bool {
+  // prep_s: wait for the K~ tile of load kl and copy its scales for tile counter g
+  auto prep_s = [&](int kl, int g) -> bool {
     const int slot = kl % kKRing;
     if (!mbar_wait_warp(&k_full[slot], static_cast<uint32_t>((kl / kKRing) & 1), abort))
       return false;
     tc_fence_after();
     const uint32_t kb = k_ring + slot * L::kKSlot;
-    const uint32_t sc = kScB + 8u * static_cast<uint32_t>(g % 3);
+    const uint32_t sc = kScB + 8u * static_cast<uint32_t>(g % 6);
 #pragma unroll
     for (int kk = 0; kk < D / 64; ++kk)
       tmem_cp_32x128_x4_w(tmem + sc + 4 * kk, kb + L::kCodeBytes + kk * 512);
+    return true;
+  };
+  // fire_s: the UMMAs of a prepared tile (after its S buffer is free)
+  auto fire_s = [&](uint32_t col, int kl, int g, uint64_t* bar) {
+    const int slot = kl % kKRing;
+    const uint32_t kb = k_ring + slot * L::kKSlot;
+    const uint32_t sc = kScB + 8u * static_cast<uint32_t>(g % 6);
 #pragma unroll
     for (int kk = 0; kk < D / 64; ++kk)
       umma_fp4_ss_w(tmem + col, sdesc(q_addr + 32 * kk, 16, sbo, lay),
@@ -179,20 +190,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem + sc + 4 * kk, kk > 0 ? 1u : 0u);
     umma_commit_w(bar);
     umma_commit_w(&k_empty[slot]);
-    return true;
   };
   // Pass 1, tile j (load j) into buffer j % 3 once the softmax has loaded tile
-  // j - 3 from there (which also means tile j - 3's UMMAs, the last readers of
-  // the scale copy j reuses, completed).  The S warp takes the even tiles, the
-  // P~V~ warp (idle until pass 2) the odd ones.
+  // j - 3 from there.  The S warp takes the even tiles, the P~V~ warp (idle
+  // until pass 2) the odd ones.
   auto pass1 = [&](int first) -> bool {
     bool ok = true;
     for (int j = first; j < nk && ok; j += 2) {
       const int buf = j % 3;
+      if (!(ok = prep_s(j, j))) break;
       if (j >= 3 &&
           !(ok = mbar_wait_warp(&s1_free[buf], static_cast<uint32_t>((j / 3 - 1) & 1), abort)))
         break;
-      ok = issue_s(128u * buf, j, j, &s1_full[buf]);
+      tc_fence_after();
+      fire_s(128u * buf, j, j, &s1_full[buf]);
     }
     return ok;
   };
@@ -274,11 +285,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // Pass 2 (tile counter g = nk + j): tiles 0 and 1 at once, then tile j + 2
     // into buffer j % 2 once the P~V~ of tile j, the last reader of its P~, is done.
-    for (int j = 0; j < 2 && j < nk && ok; ++j) ok = issue_s(128u * j, nk + j, nk + j, &s_full[j]);
+    for (int j = 0; j < 2 && j < nk && ok; ++j) {
+      if (!(ok = prep_s(nk + j, nk + j))) break;
+      fire_s(128u * j, nk + j, nk + j, &s_full[j]);
+    }
     for (int j = 0; j + 2 < nk && ok; ++j) {
       const int buf = j & 1;
+      if (!(ok = prep_s(nk + j + 2, nk + j + 2))) break;
       if (!(ok = mbar_wait_warp(&pv_done[buf], static_cast<uint32_t>((j >> 1) & 1), abort))) break;
-      ok = issue_s(128u * buf, nk + j + 2, nk + j + 2, &s_full[buf]);
+      tc_fence_after();
+      fire_s(128u * buf, nk + j + 2, nk + j + 2, &s_full[buf]);
     }
     umma_commit_w(&drain[0]);
     mbar_wait_warp(&drain[0], 0, nullptr, 10000000ull);
