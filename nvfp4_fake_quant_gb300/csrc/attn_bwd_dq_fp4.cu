@@ -32,8 +32,8 @@
 // TMEM: S [0,128), dP [128,256), dQ [256,256+D), dS [384,448), the Q~ scale
 // operand at [448 + 4 kk), the K~ scale operand of step j at [456 + 8 (j % 2)
 // + 4 kk) (kk: 64-element group of D).  The copy for step j overwrites the
-// scales of step j - 2, whose UMMAs completed before the barrier the UMMA warp
-// waited on last (the release of S_{j-1}, committed after S_{j-1}).
+// scales of step j - 2, whose UMMAs completed before the release of S_{j-2},
+// which the issuing warp waited on before S_{j-1}.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -230,19 +230,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t do_addr = smem_u32(smem + L::kDO);
     const uint32_t k4_addr = smem_u32(smem + L::kK4);
     const uint32_t v_addr = smem_u32(smem + L::kV);
-    // S_j and dP_j, once their tiles are in and every warp has loaded S_{j-1}, dP_{j-1}
+    // S_j and dP_j, once their tiles are in and every warp has loaded S_{j-1},
+    // dP_{j-1}.  The K~ scales are copied before that last wait, off the path
+    // from the release to the UMMAs (their columns were last read by S_{j-2},
+    // complete since this warp saw S_{j-2} and dP_{j-2} released).
     auto issue_step = [&](int j) -> bool {
       const int k4s = j % kK4Slots, vs = j % kVSlots;
-      if (!mbar_wait_warp(&k4_full[k4s], static_cast<uint32_t>((j / kK4Slots) & 1), abort) ||
-          !mbar_wait_warp(&v_full[vs], static_cast<uint32_t>((j / kVSlots) & 1), abort))
+      if (!mbar_wait_warp(&k4_full[k4s], static_cast<uint32_t>((j / kK4Slots) & 1), abort))
         return false;
-      if (j > 0 && !mbar_wait_warp(sdp_free, static_cast<uint32_t>((j - 1) & 1), abort)) return false;
       tc_fence_after();
       const uint32_t kb = k4_addr + k4s * L::kC4;
       const uint32_t sc = kScB + 8u * static_cast<uint32_t>(j & 1);
 #pragma unroll
       for (int kk = 0; kk < D / 64; ++kk)
         tmem_cp_32x128_x4_w(tmem + sc + 4 * kk, kb + L::kCodeBytes + kk * 512);
+      if (!mbar_wait_warp(&v_full[vs], static_cast<uint32_t>((j / kVSlots) & 1), abort))
+        return false;
+      if (j > 0 && !mbar_wait_warp(sdp_free, static_cast<uint32_t>((j - 1) & 1), abort)) return false;
+      tc_fence_after();
 #pragma unroll
       for (int kk = 0; kk < D / 64; ++kk)
         umma_fp4_ss_w(tmem + kColS, sdesc(q_addr + 32 * kk, 16, sbo, lay),
