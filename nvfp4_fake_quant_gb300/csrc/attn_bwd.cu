@@ -274,6 +274,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     float nm, nlse, ndl;
     load_row(0, nm, nlse, ndl);
+    // The dS stores of tile i are fenced and announced (ds_full) early in tile
+    // i+1, after S_{i+1} has been loaded, so the stores drain while the warp
+    // works instead of stalling it in the fence.
+    bool ds_pending = false;
     for (int it = 0; it < n_iter && ok; ++it) {
       const int qi = qtile(it);
       const int qrow = qi * kTile + t;
@@ -304,6 +308,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!(row_ok && key < Nkv && (!causal || key <= qrow))) x[i] = -INFINITY;
           }
         }
+        if (ds_pending) {  // dS of the previous tile -> dK
+          tc_fence_before();
+          fence_proxy_async_smem();
+          mbar_arrive_warp(ds_full);
+          ds_pending = false;
+        }
         uint32_t ptw0[8], ptw1[8];  // P~ / l as bf16x2
         pquant16_scaled_bf16(x, inv_l, pp0, ptw0);
         pquant16_scaled_bf16(x + 16, inv_l, pp1, ptw1);
@@ -316,29 +326,32 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t off = sw128_offset(t, key_col + ch * 8, 128);
           *reinterpret_cast<uint4*>(pd_smem + off) = make_uint4(w[0], w[1], w[2], w[3]);
         }
-        fence_proxy_async_smem();
-        mbar_arrive_warp(pt_full);
       }
       // ---- dS part: dP -> dS = scale * A * (dP - delta), A = P / l
+      // The first dP load is issued before the P~ stores are fenced, so its
+      // latency overlaps their drain.
       if (!(ok = mbar_wait_warp(dp_full, ph, abort))) break;
       tc_fence_after();
       uint32_t dsw[16];
+      uint32_t (&r16)[16] = *reinterpret_cast<uint32_t(*)[16]>(r);
+      tmem_ld16(tmem + lane_base + 128 + key_col, r16);
+      fence_proxy_async_smem();
+      mbar_arrive_warp(pt_full);
       {
-        // dP in two halves of 16 keys (P stays in fp32 registers meanwhile)
-        const uint64_t ndl2 = pk2(-dl, -dl);
-        const uint64_t sl2 = pk2(scale * inv_l, scale * inv_l);
+        // dP in two halves of 16 keys (P stays in fp32 registers meanwhile);
+        // dS = P * (sl * dP - sl * delta) with sl = scale / l
+        const float sl = scale * inv_l;
+        const uint64_t sl2 = pk2(sl, sl), nsd2 = pk2(-sl * dl, -sl * dl);
 #pragma unroll
         for (int hv = 0; hv < 2; ++hv) {
-          uint32_t (&r16)[16] = *reinterpret_cast<uint32_t(*)[16]>(r);
           const float* pp = hv ? pp1 : pp0;
-          tmem_ld16(tmem + lane_base + 128 + key_col + 16 * hv, r16);
+          if (hv) tmem_ld16(tmem + lane_base + 128 + key_col + 16, r16);
           tmem_wait_ld();
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
-            const uint64_t a2 = mul2(pk2(pp[2 * u], pp[2 * u + 1]), sl2);
-            const uint64_t d2 = add2(pk2(__uint_as_float(r16[2 * u]), __uint_as_float(r16[2 * u + 1])), ndl2);
+            const uint64_t t2 = fma2(pk2(__uint_as_float(r16[2 * u]), __uint_as_float(r16[2 * u + 1])), sl2, nsd2);
             float d0, d1;
-            up2(mul2(a2, d2), d0, d1);
+            up2(mul2(pk2(pp[2 * u], pp[2 * u + 1]), t2), d0, d1);
             dsw[8 * hv + u] = pack_bf16(d0, d1);
           }
         }
@@ -351,6 +364,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         *reinterpret_cast<uint4*>(pd_smem + off) =
             make_uint4(dsw[4 * ch], dsw[4 * ch + 1], dsw[4 * ch + 2], dsw[4 * ch + 3]);
       }
+      ds_pending = true;
+    }
+    if (ok && ds_pending) {
+      tc_fence_before();
       fence_proxy_async_smem();
       mbar_arrive_warp(ds_full);
     }

@@ -12,13 +12,16 @@
 // and applies both scales, so each S element is the sum of the same exact
 // products code_q*s_q*code_k*s_k that a BF16 UMMA on Q~, K~ would add up.
 //
-// One 128-query tile per CTA; the four softmax warpgroups share every 128-key
-// tile, warpgroup w owning keys [32 w, 32 w + 32) of it.  S tiles live in TMEM
-// buffers of 128 columns: three in pass 1 (columns [0, 384); O is not live
-// yet), two in pass 2 (columns [0, 256), tile j in buffer j % 2), so the UMMAs
-// of the next tiles run while the softmax works on the current one.  P~ of a
-// tile is written over the first 16 of each warpgroup's 32 columns, which it
-// has already loaded, and P~V~ reads it from there.
+// One 128-query tile per CTA.  S tiles live in TMEM buffers of 128 columns:
+// three in pass 1 (columns [0, 384); O is not live yet, tile j in buffer
+// j % 3), two in pass 2 (columns [0, 256), tile j in buffer j % 2), so the
+// UMMAs of the next tiles run while the softmax works on the current one.  In
+// pass 1 warpgroup w takes the whole tiles j = w (mod 4): four tiles are read
+// at once, and each tile costs one wait and one release per warp of one
+// warpgroup instead of all sixteen warps.  In pass 2 the four warpgroups share
+// every tile, warpgroup w owning keys [32 w, 32 w + 32) of it; P~ of a tile is
+// written over the first 16 of each warpgroup's 32 columns, which it has
+// already loaded, and P~V~ reads it from there.
 //
 // Every tcgen05 instruction and every mbarrier wait costs the issuing warp tens
 // of cycles, more in total than the tensor work of the small FP4 UMMAs, so the
@@ -28,15 +31,23 @@
 // it waits for the PV warp's commit of the P~V~ that read the buffer.
 //
 // TMEM: S buffers, O at [256, 256 + D) (pass 2), the Q~ scale operand at
-// [384 + 4 kk), the K~ scale operand of tile counter g at [392 + 8 (g % 6) +
+// [384 + 4 kk), the K~ scale operand of tile counter g at [392 + 8 (g % 12) +
 // 4 kk) (kk: 64-element group of D).  The issuing warp copies a tile's scales
 // before it waits for the tile's S buffer, so the copy is off the path from
-// "buffer released" to "UMMA running".  Six copies rotate: when a warp copies
-// the scales of tile g it has already waited on a barrier implying that the
-// UMMAs of tile g - 6 completed (pass 1: the release of tile g - 5, which the
-// softmax arrives on after loading tile g - 6; pass 2: the P~V~ of the tile
-// before, which follows the softmax of tile g - 4), so a copy never overwrites
-// scales an UMMA in flight may still read.
+// "buffer released" to "UMMA running".  Twelve copies rotate, and a copy never
+// overwrites scales an UMMA in flight may still read.  Pass 1: the warp
+// copying the scales of tile g fired tile g - 4 after the release of tile
+// g - 7, whose S the other warp fired after the release of tile g - 10, a
+// tile of this warp fired after its tile g - 12; so tile g - 12, the region's
+// last reader, has completed.  Pass 2: the S warp has waited for the P~V~ of
+// the tile before, which follows the softmax of tile g - 4, and pass 2 starts
+// after every pass-1 tile has been read.
+//
+// Pass-1 barriers are indexed so that every barrier is waited on by one role
+// in phase order (an mbarrier parity wait cannot tell a phase from the one two
+// ahead): s1_full[j % 12] (waited by warpgroup j % 4 only), s1_free[j % 6]
+// (waited by the issuer of tile j + 3 only), and one pass1_done barrier the
+// softmax warps arrive on after their last pass-1 tile.
 //
 // Roles (608 threads, one CTA per SM): warps 0-15 softmax, warp 16 TMA
 // producer, warp 17 TMEM allocator and S issuer, warp 18 P~V~ issuer
@@ -62,6 +73,7 @@ constexpr int kKRing = 6;
 constexpr int kVRing = 4;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint32_t kScA = 384, kScB = 392;  // TMEM columns of the scale operands
+constexpr int kScRegions = 12;               // K~ scale copies at kScB + 8 r, up to 488
 
 template <int D>
 struct Fp4Layout {
@@ -74,9 +86,9 @@ struct Fp4Layout {
   static constexpr uint32_t kVRingOff = kKRingOff + kKRing * kKSlot;
   static constexpr uint32_t kX = kVRingOff + kVRing * kVSlot;  // [4 warpgroups][128] f32
   static constexpr uint32_t kBars = kX + 4u * 128u * 4u;
-  // q_full, k_full/k_empty, v_full/v_empty, s1_full[3], s1_free[3], s_full[2],
-  // p_full[2], pv_done[2], o_full, drain x2, q_sc_ready
-  static constexpr uint32_t kNumBars = 1 + 2 * kKRing + 2 * kVRing + 12 + 4;
+  // q_full, k_full/k_empty, v_full/v_empty, s1_full[12], s1_free[6], pass1_done,
+  // s_full[2], p_full[2], pv_done[2], o_full, drain x2, q_sc_ready
+  static constexpr uint32_t kNumBars = 1 + 2 * kKRing + 2 * kVRing + 12 + 6 + 1 + 6 + 4;
   static constexpr uint32_t kTmemSlot = kBars + kNumBars * 8u;
   static constexpr uint32_t kAbort = kTmemSlot + 4u;
   static constexpr uint32_t kAlloc = kAbort + 4u + 1024u;
@@ -107,9 +119,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* k_empty = k_full + kKRing;   // [kKRing]
   uint64_t* v_full = k_empty + kKRing;   // [kVRing]
   uint64_t* v_empty = v_full + kVRing;   // [kVRing]
-  uint64_t* s1_full = v_empty + kVRing;  // pass 1 [3]
-  uint64_t* s1_free = s1_full + 3;       // pass 1 [3]
-  uint64_t* s_full = s1_free + 3;        // pass 2 [2]
+  uint64_t* s1_full = v_empty + kVRing;  // pass 1 [12]: tile j -> j % 12
+  uint64_t* s1_free = s1_full + 12;      // pass 1 [6]: tile j -> j % 6
+  uint64_t* pass1_done = s1_free + 6;
+  uint64_t* s_full = pass1_done + 1;     // pass 2 [2]
   uint64_t* p_full = s_full + 2;         // pass 2 [2]
   uint64_t* pv_done = p_full + 2;        // pass 2 [2]
   uint64_t* o_full = pv_done + 2;
@@ -134,10 +147,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&v_full[s], 1);
       mbar_init(&v_empty[s], 1);
     }
-    for (int i = 0; i < 3; ++i) {
-      mbar_init(&s1_full[i], 1);
-      mbar_init(&s1_free[i], kSoftmaxWarps);
-    }
+    for (int i = 0; i < 12; ++i) mbar_init(&s1_full[i], 1);
+    for (int i = 0; i < 6; ++i) mbar_init(&s1_free[i], kSoftmaxWarps / 4);
+    mbar_init(pass1_done, kSoftmaxWarps);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], kSoftmaxWarps);
@@ -172,24 +184,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       return false;
     tc_fence_after();
     const uint32_t kb = k_ring + slot * L::kKSlot;
-    const uint32_t sc = kScB + 8u * static_cast<uint32_t>(g % 6);
+    const uint32_t sc = kScB + 8u * static_cast<uint32_t>(g % kScRegions);
 #pragma unroll
     for (int kk = 0; kk < D / 64; ++kk)
       tmem_cp_32x128_x4_w(tmem + sc + 4 * kk, kb + L::kCodeBytes + kk * 512);
     return true;
   };
-  // fire_s: the UMMAs of a prepared tile (after its S buffer is free)
+  // fire_s: the UMMAs of a prepared tile (after its S buffer is free); the K~
+  // slot is released by a commit here in pass 2, by the softmax in pass 1
   auto fire_s = [&](uint32_t col, int kl, int g, uint64_t* bar) {
     const int slot = kl % kKRing;
     const uint32_t kb = k_ring + slot * L::kKSlot;
-    const uint32_t sc = kScB + 8u * static_cast<uint32_t>(g % 6);
+    const uint32_t sc = kScB + 8u * static_cast<uint32_t>(g % kScRegions);
 #pragma unroll
     for (int kk = 0; kk < D / 64; ++kk)
       umma_fp4_ss_w(tmem + col, sdesc(q_addr + 32 * kk, 16, sbo, lay),
                     sdesc(kb + 32 * kk, 16, sbo, lay), idesc_s, tmem + kScA + 4 * kk,
                     tmem + sc + 4 * kk, kk > 0 ? 1u : 0u);
     umma_commit_w(bar);
-    umma_commit_w(&k_empty[slot]);
+    if (g >= nk) umma_commit_w(&k_empty[slot]);
   };
   // Pass 1, tile j (load j) into buffer j % 3 once the softmax has loaded tile
   // j - 3 from there.  The S warp takes the even tiles, the P~V~ warp (idle
@@ -197,13 +210,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto pass1 = [&](int first) -> bool {
     bool ok = true;
     for (int j = first; j < nk && ok; j += 2) {
-      const int buf = j % 3;
       if (!(ok = prep_s(j, j))) break;
-      if (j >= 3 &&
-          !(ok = mbar_wait_warp(&s1_free[buf], static_cast<uint32_t>((j / 3 - 1) & 1), abort)))
+      if (j >= 3 && !(ok = mbar_wait_warp(&s1_free[(j - 3) % 6],
+                                          static_cast<uint32_t>(((j - 3) / 6) & 1), abort)))
         break;
       tc_fence_after();
-      fire_s(128u * buf, j, j, &s1_full[buf]);
+      fire_s(128u * (j % 3), j, j, &s1_full[j % 12]);
     }
     return ok;
   };
@@ -277,12 +289,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       umma_commit_w(q_sc_ready);
     }
     if (ok) ok = pass1(0);
-    // every pass-1 buffer released (pass 2 reuses the columns)
-    for (int buf = 0; buf < 3 && ok; ++buf) {
-      const int uses = (nk - buf + 2) / 3;  // tiles j < nk with j % 3 == buf
-      if (uses > 0)
-        ok = mbar_wait_warp(&s1_free[buf], static_cast<uint32_t>((uses - 1) & 1), abort);
-    }
+    // every pass-1 tile loaded by the softmax (pass 2 reuses the columns)
+    if (ok) ok = mbar_wait_warp(pass1_done, 0, abort);
     // Pass 2 (tile counter g = nk + j): tiles 0 and 1 at once, then tile j + 2
     // into buffer j % 2 once the P~V~ of tile j, the last reader of its P~, is done.
     for (int j = 0; j < 2 && j < nk && ok; ++j) {
@@ -339,25 +347,48 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     float mraw = -INFINITY;
     uint32_t r[32];
-    for (int j = 0; j < nk && ok; ++j) {
-      const int buf = j % 3;
-      if (!(ok = mbar_wait_warp(&s1_full[buf], static_cast<uint32_t>((j / 3) & 1), abort))) break;
-      tc_fence_after();
-      tmem_ld32(tmem + lane_base + 128 * buf + 32 * wg, r);
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive_warp(&s1_free[buf]);
-      const int k0 = key0(j);
-      if (!is_edge(k0)) {
+    {
+      // pass 1: warpgroup wg, tiles j = wg (mod 4), all 128 keys of each
+      uint32_t r2[32];
+      for (int j = wg; j < nk && ok; j += 4) {
+        if (!(ok = mbar_wait_warp(&s1_full[j % 12], static_cast<uint32_t>((j / 12) & 1), abort)))
+          break;
+        tc_fence_after();
+        if ((warp & 3) == 0) mbar_arrive_warp(&k_empty[j % kKRing]);  // S_j read its K~ slot
+        const uint32_t col = 128u * static_cast<uint32_t>(j % 3);
+        const int k0 = j * kTile;
+        const bool edge = k0 + kTile > Nkv || (causal && k0 + kTile - 1 > q0);
+        float mx[4] = {mraw, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) mraw = max3f(mraw, __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
-      } else {
+        for (int hf = 0; hf < 2; ++hf) {
+          tmem_ld32(tmem + lane_base + col + 64 * hf, r);
+          tmem_ld32(tmem + lane_base + col + 64 * hf + 32, r2);
+          tmem_wait_ld();
+          if (hf == 1) {
+            tc_fence_before();
+            mbar_arrive_warp(&s1_free[j % 6]);
+          }
+          if (!edge) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int key = k0 + i;
-          if (key < Nkv && (!causal || key <= qrow)) mraw = fmaxf(mraw, __uint_as_float(r[i]));
+            for (int i = 0; i < 16; i += 2) {
+              mx[0] = max3f(mx[0], __uint_as_float(r[i]), __uint_as_float(r[i + 1]));
+              mx[1] = max3f(mx[1], __uint_as_float(r[16 + i]), __uint_as_float(r[17 + i]));
+              mx[2] = max3f(mx[2], __uint_as_float(r2[i]), __uint_as_float(r2[i + 1]));
+              mx[3] = max3f(mx[3], __uint_as_float(r2[16 + i]), __uint_as_float(r2[17 + i]));
+            }
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              const int key = k0 + 64 * hf + i, key2 = key + 32;
+              if (key < Nkv && (!causal || key <= qrow)) mx[i & 1] = fmaxf(mx[i & 1], __uint_as_float(r[i]));
+              if (key2 < Nkv && (!causal || key2 <= qrow))
+                mx[2 + (i & 1)] = fmaxf(mx[2 + (i & 1)], __uint_as_float(r2[i]));
+            }
+          }
         }
+        mraw = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
       }
+      mbar_arrive_warp(pass1_done);
     }
     // row maximum over the four warpgroups (always reached, also after an abort)
     xchg[wg * 128 + t] = mraw;
