@@ -34,14 +34,14 @@ __device__ __forceinline__ Block16 load_block(const uint16_t* __restrict__ src) 
   return {ld_stream(src), ld_stream(src + 8)};
 }
 
+// g: the global scale (1 for the unit modes), inv_g = RN(1/g).
 template <int MODE>
-__device__ __forceinline__ void quant_block(const Block16& v, const float g,
+__device__ __forceinline__ void quant_block(const Block16& v, const float g, const float inv_g,
                                             uint16_t* __restrict__ out, uint8_t* __restrict__ sc,
                                             uint8_t* __restrict__ cd) {
   const uint32_t xv[8] = {v.lo.x, v.lo.y, v.lo.z, v.lo.w, v.hi.x, v.hi.y, v.hi.z, v.hi.w};
   Q16 q;
   if constexpr (MODE == kStaticBf16) {
-    const float inv_g = __frcp_rn(g);
     q = out != nullptr ? quant16_static_fast<true>(xv, g, inv_g)
                        : quant16_static_fast<false>(xv, g, inv_g);
   } else {
@@ -60,16 +60,16 @@ __device__ __forceinline__ void quant_block(const Block16& v, const float g,
 }
 
 // Contiguous operands (row strides equal to the row lengths): block i of the
-// flattened matrix at element 16 i, scale byte i, code bytes 8 i.  With a unit
-// global scale each thread loads two blocks (one grid stride apart) before
-// quantizing either, to keep more loads in flight; the static-scale mode, bound
-// by its IEEE divisions, takes one at a time.
+// flattened matrix at element 16 i, scale byte i, code bytes 8 i.  Each thread
+// loads two blocks (one grid stride apart) before quantizing either, to keep
+// more loads in flight.
 template <int MODE>
 __global__ void __launch_bounds__(256) fake_quant_flat_kernel(
     const uint16_t* __restrict__ x, int64_t nblocks, const float* __restrict__ gsf,
     uint16_t* __restrict__ out, uint8_t* __restrict__ scales, uint8_t* __restrict__ codes) {
-  constexpr int kUnroll = MODE == kStaticBf16 ? 1 : 2;
+  constexpr int kUnroll = 2;
   const float g = (MODE == kStaticBf16) ? *gsf : 1.0f;
+  const float inv_g = (MODE == kStaticBf16) ? __frcp_rn(g) : 1.0f;
   const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nblocks;
        i += kUnroll * step) {
@@ -81,7 +81,7 @@ __global__ void __launch_bounds__(256) fake_quant_flat_kernel(
     for (int u = 0; u < kUnroll; ++u) {
       const int64_t b = i + u * step;
       if (b < nblocks)
-        quant_block<MODE>(v[u], g, out != nullptr ? out + b * 16 : nullptr,
+        quant_block<MODE>(v[u], g, inv_g, out != nullptr ? out + b * 16 : nullptr,
                           scales != nullptr ? scales + b : nullptr,
                           codes != nullptr ? codes + b * 8 : nullptr);
     }
@@ -95,11 +95,12 @@ __global__ void __launch_bounds__(256) fake_quant_rows_kernel(
     const float* __restrict__ gsf, uint16_t* __restrict__ out, int64_t ld_out,
     uint8_t* __restrict__ scales, int64_t ld_s, uint8_t* __restrict__ codes, int64_t ld_c) {
   const float g = (MODE == kStaticBf16) ? *gsf : 1.0f;
+  const float inv_g = (MODE == kStaticBf16) ? __frcp_rn(g) : 1.0f;
   const int64_t cstep = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t r = blockIdx.y; r < rows; r += gridDim.y) {
     for (int64_t cb = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; cb < nbc;
          cb += cstep)
-      quant_block<MODE>(load_block(x + r * ld_x + cb * 16), g,
+      quant_block<MODE>(load_block(x + r * ld_x + cb * 16), g, inv_g,
                         out != nullptr ? out + r * ld_out + cb * 16 : nullptr,
                         scales != nullptr ? scales + r * ld_s + cb : nullptr,
                         codes != nullptr ? codes + r * ld_c + cb * 8 : nullptr);
@@ -171,6 +172,7 @@ __global__ void __launch_bounds__(256) quant_tiled_kernel(
     const uint16_t* __restrict__ x, int64_t rows, int64_t nbc, int64_t ld_x,
     const float* __restrict__ gsf, uint8_t* __restrict__ codes, uint8_t* __restrict__ scales) {
   const float g = (MODE == kStaticBf16) ? *gsf : 1.0f;
+  const float inv_g = (MODE == kStaticBf16) ? __frcp_rn(g) : 1.0f;
   const int64_t total = rows * nbc;
   const bool narrow = total <= 0xFFFFFFFFll;
   const uint32_t nbc32 = static_cast<uint32_t>(nbc);
@@ -195,9 +197,9 @@ __global__ void __launch_bounds__(256) quant_tiled_kernel(
     const Block16 v0 = load_block(x + r0 * ld_x + c0 * 16);
     Block16 v1;
     if (two) v1 = load_block(x + r1 * ld_x + c1 * 16);
-    quant_block<MODE>(v0, g, nullptr, scales + tiled_scale_offset(r0, c0, n_bt), codes + i * 8);
+    quant_block<MODE>(v0, g, inv_g, nullptr, scales + tiled_scale_offset(r0, c0, n_bt), codes + i * 8);
     if (two)
-      quant_block<MODE>(v1, g, nullptr, scales + tiled_scale_offset(r1, c1, n_bt),
+      quant_block<MODE>(v1, g, inv_g, nullptr, scales + tiled_scale_offset(r1, c1, n_bt),
                         codes + (i + step) * 8);
   }
 }
