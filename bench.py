@@ -66,12 +66,12 @@ def kernel_work(kind, b, n, h, d):
 # (profiles/traffic_attn_kernels_wan25088.md), with the SHA-256 of the kernel's
 # sources at the time: a changed source reports null.
 TRAFFIC = {
-    "bwd_dkdv": {"bytes": 436753920, "sources": ['nvfp4_fake_quant_gb300/csrc/attn_bwd.cu', 'nvfp4_fake_quant_gb300/csrc/nvq_ptx.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_quant.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_internal.h'],
-                "sha256": "c3d35646ea1284d62a9e1bfa7558b5aad1cff2ba87185988cb0519c5ec0cf1c5"},
-    "bwd_dq": {"bytes": 349573376, "sources": ['nvfp4_fake_quant_gb300/csrc/attn_bwd_dq_fp4.cu', 'nvfp4_fake_quant_gb300/csrc/nvq_ptx.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_quant.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_internal.h'],
+    "bwd_dkdv": {"bytes": 438025216, "sources": ['nvfp4_fake_quant_gb300/csrc/attn_bwd.cu', 'nvfp4_fake_quant_gb300/csrc/nvq_ptx.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_quant.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_internal.h'],
+                "sha256": "1431edf994ce6a7d0efac8368a7a7bf878ffee66f4a7f6362533f69bd2aec503"},
+    "bwd_dq": {"bytes": 349380096, "sources": ['nvfp4_fake_quant_gb300/csrc/attn_bwd_dq_fp4.cu', 'nvfp4_fake_quant_gb300/csrc/nvq_ptx.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_quant.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_internal.h'],
               "sha256": "d7fd7c48c93e7bebafde9f6ab23c4619b605324012303a62c80cf0f956bc2985"},
-    "attn_fwd": {"bytes": 173750528, "sources": ['nvfp4_fake_quant_gb300/csrc/attn_fwd_fp4.cu', 'nvfp4_fake_quant_gb300/csrc/nvq_ptx.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_quant.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_internal.h'],
-                "sha256": "e7288749faf93025b8940c3b6268efdca8209c7c74034f2abda2a340a2f05603"},
+    "attn_fwd": {"bytes": 173014016, "sources": ['nvfp4_fake_quant_gb300/csrc/attn_fwd_fp4.cu', 'nvfp4_fake_quant_gb300/csrc/nvq_ptx.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_quant.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_internal.h'],
+                "sha256": "bf49592a0d9ad1f143c984e5f9a8399f3bb3fb4852e02b8dafdd42d11c0781f1"},
 }
 
 
