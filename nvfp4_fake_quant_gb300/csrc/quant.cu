@@ -61,13 +61,14 @@ __device__ __forceinline__ void quant_block(const Block16& v, const float g, con
 
 // Contiguous operands (row strides equal to the row lengths): block i of the
 // flattened matrix at element 16 i, scale byte i, code bytes 8 i.  Each thread
-// loads two blocks (one grid stride apart) before quantizing either, to keep
-// more loads in flight.
+// loads several blocks (a grid stride apart) before quantizing any, to keep
+// more loads in flight: four with a unit scale, two with a static one (whose
+// longer arithmetic needs the registers).
 template <int MODE>
 __global__ void __launch_bounds__(256) fake_quant_flat_kernel(
     const uint16_t* __restrict__ x, int64_t nblocks, const float* __restrict__ gsf,
     uint16_t* __restrict__ out, uint8_t* __restrict__ scales, uint8_t* __restrict__ codes) {
-  constexpr int kUnroll = 2;
+  constexpr int kUnroll = MODE == kStaticBf16 ? 2 : 4;
   const float g = (MODE == kStaticBf16) ? *gsf : 1.0f;
   const float inv_g = (MODE == kStaticBf16) ? __frcp_rn(g) : 1.0f;
   const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -115,7 +116,7 @@ __global__ void __launch_bounds__(256) fake_quant_rows_kernel(
 // of the tile, 16-element block j of the 64, at byte (r % 32) * 16 + (r / 32) * 4
 // + j -- the tensor-memory layout of the UMMA's scale operand, so that one
 // copy per block moves it there.  Tokens of the last tile beyond N get scale 0.
-// Blocks i < nblocks are the input's 16-element blocks in memory order (two
+// Blocks i < nblocks are the input's 16-element blocks in memory order (four
 // per thread in flight); the npad indices after them zero the padding scales.
 __global__ void __launch_bounds__(256) quant_attn_fp4_kernel(
     const uint16_t* __restrict__ x, uint32_t nblocks, uint32_t npad, uint32_t N, uint32_t H,
@@ -127,13 +128,14 @@ __global__ void __launch_bounds__(256) quant_attn_fp4_kernel(
     return scales + ((static_cast<int64_t>(bh) * n_tiles + (n >> 7)) * nkk + (cb >> 2)) * 512 +
            (n & 31u) * 16 + ((n >> 5) & 3u) * 4 + (cb & 3u);
   };
-  for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < nblocks; i += 2 * step) {
-    Block16 v[2];
+  constexpr uint32_t kUnroll = 4;
+  for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < nblocks; i += kUnroll * step) {
+    Block16 v[kUnroll];
 #pragma unroll
-    for (int u = 0; u < 2; ++u)
+    for (uint32_t u = 0; u < kUnroll; ++u)
       if (i + u * step < nblocks) v[u] = load_block(x + static_cast<int64_t>(i + u * step) * 16);
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
+    for (uint32_t u = 0; u < kUnroll; ++u) {
       const uint32_t blk = i + u * step;
       if (blk >= nblocks) continue;
       const uint32_t xv[8] = {v[u].lo.x, v[u].lo.y, v[u].lo.z, v[u].lo.w,
@@ -314,7 +316,8 @@ cudaError_t launch_fake_quant(const void* x, int64_t rows, int64_t cols, int64_t
                     (scales == nullptr || ld_s == nbc) && (codes == nullptr || ld_c == cols / 2);
   if (flat) {
     const int64_t nblocks = rows * nbc;
-    const int64_t work = mode == kStaticBf16 ? nblocks : (nblocks + 1) / 2;  // threads needed
+    const int64_t per_thread = mode == kStaticBf16 ? 2 : 4;  // blocks in flight per thread
+    const int64_t work = (nblocks + per_thread - 1) / per_thread;  // threads needed
     switch (mode) {
       case kUnitBf16:
         fake_quant_flat_kernel<kUnitBf16>
@@ -396,7 +399,7 @@ cudaError_t launch_quant_attn_fp4(const void* x, int B, int N, int H, int D, uin
   if ((D != 64 && D != 128) || nblocks >= (int64_t{1} << 31) || npad >= (int64_t{1} << 31))
     return cudaErrorInvalidValue;
   const int threads = 256;
-  const int64_t work = std::max<int64_t>((nblocks + 1) / 2, npad);
+  const int64_t work = std::max<int64_t>((nblocks + 3) / 4, npad);
   quant_attn_fp4_kernel<<<wave_grid<quant_attn_fp4_kernel>(work, threads), threads, 0, stream>>>(
       static_cast<const uint16_t*>(x), static_cast<uint32_t>(nblocks), static_cast<uint32_t>(npad),
       static_cast<uint32_t>(N), static_cast<uint32_t>(H), D == 128 ? 3u : 2u,
