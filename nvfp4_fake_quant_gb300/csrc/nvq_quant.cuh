@@ -386,61 +386,84 @@ __device__ __forceinline__ void pquant16_scaled_bf16(const float* x, float inv_l
   e2m1x8_bf16_mul(e2m1x8(q1), f2, out + 4);
 }
 
-// Static global scale, fast form.  The same decisions as quant16_static, taken
-// on products with reciprocals instead of IEEE quotients wherever that cannot
-// change them: a product q = RN(x*g) * rcp(s) is within 2^-22 (relative) of the
-// IEEE quotient, so when q * (1 - 2^-20) and q * (1 + 2^-20) get the same E2M1
-// code (the code is monotone in its argument), the IEEE quotient, which lies
-// between them, gets that code too.  Likewise each output value o =
-// (code * s) * RN(1/g) is checked through the bf16 roundings of o * (1 -+ 2^-21).
-// A block where any check fails is redone by quant16_static.  inv_g = RN(1/g).
-// The IEEE path as a call of its own, so that its registers stay out of the
-// fast path's allocation.
+// Static global scale, fast form.  The same decisions as quant16_static, without
+// per-element IEEE divisions.  Codes: y = RN(x*g) and the correctly rounded
+// quotient RN(y / s) from the correctly rounded reciprocal v = RN(1/s) by one
+// FMA correction: q0 = RN(y v) is within an ulp of y / s, the remainder
+// y - q0 s is then exact in one FMA, and RN(q0 + (y - q0 s) v) = RN(y / s)
+// (Markstein's theorem on division by FMA; y / s is far from the fp32
+// underflow range wherever the E2M1 code is not 0).
+// Output values: a code magnitude is 2^k * b with b in {1, 1.5}, and code * s
+// is exact, so RN(code * s / g) = 2^k * RN(b * s / g) and its bf16 rounding is
+// 2^k times that of RN(b * s / g) (no fp32 or bf16 range limit is near: checked).
+// So each block needs two values, bf16(RN(s / g)) and bf16(RN(1.5 s / g)), the
+// quotients again by one FMA correction of a product with inv_g = RN(1/g); the
+// eight possible outputs are then looked up per code.  A block outside that
+// range is redone by quant16_static.  The IEEE path as a call of its own, so that its registers
+// stay out of the fast path's allocation.
 static __device__ __noinline__ Q16 quant16_static_cold(const uint32_t (&x)[8], float g) {
   return quant16_static(x, g);
+}
+
+// bf16 bits of RN(v) (low 16 bits).
+__device__ __forceinline__ uint32_t bf16_bits(float v) {
+  uint16_t r;
+  asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(r) : "f"(v));
+  return r;
 }
 
 template <bool OUT>
 __device__ __forceinline__ Q16 quant16_static_fast(const uint32_t (&x)[8], float g, float inv_g) {
   Q16 r;
   const float amax = amax16_bf16(x);
-  const float t = __fdiv_rn(__fmul_rn(amax, g), 6.0f);
+  // t = RN(RN(amax g) / 6), by the same FMA correction with RN(1/6)
+  const float a = __fmul_rn(amax, g), t0 = __fmul_rn(a, 1.0f / 6.0f);
+  const float t = __fmaf_rn(__fmaf_rn(-t0, 6.0f, a), 1.0f / 6.0f, t0);
   r.sbyte = e4m3_rn_sat(t);
   const float s = f16lo_to_f32(e4m3_to_f16x2(r.sbyte));
-  const float inv = s > 0.f ? rcp_approx(s) : 0.f;
-  const uint64_t g2 = pk2(g, g), inv2 = pk2(inv, inv);
-  const uint64_t dn2 = pk2(1.0f - 0x1p-20f, 1.0f - 0x1p-20f);
-  const uint64_t up2f = pk2(1.0f + 0x1p-20f, 1.0f + 0x1p-20f);
+  const float inv = s > 0.f ? __frcp_rn(s) : 0.f;
+  const uint64_t g2 = pk2(g, g), inv2 = pk2(inv, inv), ns2 = pk2(-s, -s);
   bool ok = true;
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
-    float ql[8], qh[8];
+    float q[8];
 #pragma unroll
     for (int jj = 0; jj < 4; ++jj) {
       const uint32_t w = x[4 * h + jj];
-      const uint64_t q2 = mul2(mul2(pk2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u)), g2), inv2);
-      up2(mul2(q2, dn2), ql[2 * jj], ql[2 * jj + 1]);
-      up2(mul2(q2, up2f), qh[2 * jj], qh[2 * jj + 1]);
+      const uint64_t y2 = mul2(pk2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u)), g2);
+      const uint64_t q0 = mul2(y2, inv2);
+      up2(fma2(fma2(q0, ns2, y2), inv2, q0), q[2 * jj], q[2 * jj + 1]);
     }
-    const uint32_t c = e2m1x8(ql);
-    ok = ok && c == e2m1x8(qh);
-    r.codes[h] = c;
-    if constexpr (OUT) {
-      uint32_t hv[4];
-      e2m1x8_to_f16x2(c, hv);
-      const uint64_t s2 = pk2(s, s), ig2 = pk2(inv_g, inv_g);
-      const uint64_t dn21 = pk2(1.0f - 0x1p-21f, 1.0f - 0x1p-21f);
-      const uint64_t up21 = pk2(1.0f + 0x1p-21f, 1.0f + 0x1p-21f);
+    r.codes[h] = e2m1x8(q);
+  }
+  if constexpr (OUT) {
+    // f1 = RN(s / g), f15 = RN(1.5 s / g)
+    const uint64_t n2 = pk2(s, 1.5f * s), ig2 = pk2(inv_g, inv_g);
+    const uint64_t p0 = mul2(n2, ig2);
+    float f1, f15;
+    up2(fma2(fma2(p0, pk2(-g, -g), n2), ig2, p0), f1, f15);
+    const uint32_t v2 = bf16_bits(f1), v3 = bf16_bits(f15);
+    // 2^k scaling must stay exact: f1 / 2 and 4 f15 inside the normal range
+    ok = s == 0.f || (f1 >= 0x1p-120f && f15 <= 0x1p124f);
+    // bf16 bits of the eight magnitudes {0, .5, 1, 1.5, 2, 3, 4, 6} * s / g:
+    // index 2, 3 are v2, v3; +-0x80 per factor of two in the exponent field
+    const uint32_t nz = s > 0.f ? 0xFFFFFFFFu : 0u;
+    const uint32_t w01 = ((v2 - 0x80u) << 16) & nz;                     // 0, v2 / 2
+    const uint32_t w23 = (v2 | (v3 << 16)) & nz;                        // v2, v3
+    const uint32_t w45 = ((v2 + 0x80u) | ((v3 + 0x80u) << 16)) & nz;    // 2 v2, 2 v3
+    const uint32_t w67 = ((v2 + 0x100u) | ((v3 + 0x100u) << 16)) & nz;  // 4 v2, 4 v3
+    // byte tables: low bytes of entries 0-3 / 4-7, high bytes of entries 0-3 / 4-7
+    const uint32_t lo03 = prmt_b32(w01, w23, 0x6420u), hi03 = prmt_b32(w01, w23, 0x7531u);
+    const uint32_t lo47 = prmt_b32(w45, w67, 0x6420u), hi47 = prmt_b32(w45, w67, 0x7531u);
 #pragma unroll
-      for (int jj = 0; jj < 4; ++jj) {
-        const uint64_t o2 = mul2(mul2(pk2(f16lo_to_f32(hv[jj]), f16lo_to_f32(hv[jj] >> 16)), s2), ig2);
-        float a0, a1, b0, b1;
-        up2(mul2(o2, dn21), a0, a1);
-        up2(mul2(o2, up21), b0, b1);
-        __nv_bfloat162 ba = __floats2bfloat162_rn(a0, a1), bb = __floats2bfloat162_rn(b0, b1);
-        const uint32_t wa = *reinterpret_cast<uint32_t*>(&ba), wb = *reinterpret_cast<uint32_t*>(&bb);
-        ok = ok && wa == wb;
-        r.out[4 * h + jj] = wa | (x[4 * h + jj] & 0x80008000u);
+    for (int h = 0; h < 2; ++h) {
+#pragma unroll
+      for (int hv = 0; hv < 2; ++hv) {
+        const uint32_t sel = (r.codes[h] >> (16 * hv)) & 0x7777u;  // four code magnitudes
+        const uint32_t lo = prmt_b32(lo03, lo47, sel), hi = prmt_b32(hi03, hi47, sel);
+        const int j = 4 * h + 2 * hv;
+        r.out[j] = prmt_b32(lo, hi, 0x5140u) | (x[j] & 0x80008000u);          // elements 0, 1
+        r.out[j + 1] = prmt_b32(lo, hi, 0x7362u) | (x[j + 1] & 0x80008000u);  // elements 2, 3
       }
     }
   }
