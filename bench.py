@@ -66,12 +66,12 @@ def kernel_work(kind, b, n, h, d):
 # (profiles/traffic_attn_kernels_wan25088.md), with the SHA-256 of the kernel's
 # sources at the time: a changed source reports null.
 TRAFFIC = {
-    "bwd_dkdv": {"bytes": 438025216, "sources": ['nvfp4_fake_quant_gb300/csrc/attn_bwd.cu', 'nvfp4_fake_quant_gb300/csrc/nvq_ptx.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_quant.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_internal.h'],
-                "sha256": "1431edf994ce6a7d0efac8368a7a7bf878ffee66f4a7f6362533f69bd2aec503"},
-    "bwd_dq": {"bytes": 349380096, "sources": ['nvfp4_fake_quant_gb300/csrc/attn_bwd_dq_fp4.cu', 'nvfp4_fake_quant_gb300/csrc/nvq_ptx.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_quant.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_internal.h'],
-              "sha256": "d7fd7c48c93e7bebafde9f6ab23c4619b605324012303a62c80cf0f956bc2985"},
-    "attn_fwd": {"bytes": 173014016, "sources": ['nvfp4_fake_quant_gb300/csrc/attn_fwd_fp4.cu', 'nvfp4_fake_quant_gb300/csrc/nvq_ptx.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_quant.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_internal.h'],
-                "sha256": "bf49592a0d9ad1f143c984e5f9a8399f3bb3fb4852e02b8dafdd42d11c0781f1"},
+    "bwd_dkdv": {"bytes": 438211328, "sources": ['nvfp4_fake_quant_gb300/csrc/attn_bwd.cu', 'nvfp4_fake_quant_gb300/csrc/nvq_ptx.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_quant.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_internal.h'],
+                "sha256": "57759ce2781839ef1f8bc3ec368cc7d7356a3537c74f06a10ef30bd3966b1d2f"},
+    "bwd_dq": {"bytes": 349384192, "sources": ['nvfp4_fake_quant_gb300/csrc/attn_bwd_dq_fp4.cu', 'nvfp4_fake_quant_gb300/csrc/nvq_ptx.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_quant.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_internal.h'],
+              "sha256": "56ab1398bd0a7f2737929f54fa5ff96ac42938517f3c920195c706c837117015"},
+    "attn_fwd": {"bytes": 173561600, "sources": ['nvfp4_fake_quant_gb300/csrc/attn_fwd_fp4.cu', 'nvfp4_fake_quant_gb300/csrc/nvq_ptx.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_quant.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_internal.h'],
+                "sha256": "fb18999c10e95b8648ce4430d923d1b122a549356adc85f4b4fcc8949414ddd7"},
 }
 
 

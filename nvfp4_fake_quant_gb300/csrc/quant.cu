@@ -116,7 +116,7 @@ __global__ void __launch_bounds__(256) fake_quant_rows_kernel(
 // of the tile, 16-element block j of the 64, at byte (r % 32) * 16 + (r / 32) * 4
 // + j -- the tensor-memory layout of the UMMA's scale operand, so that one
 // copy per block moves it there.  Tokens of the last tile beyond N get scale 0.
-// Blocks i < nblocks are the input's 16-element blocks in memory order (four
+// Blocks i < nblocks are the input's 16-element blocks in memory order (two
 // per thread in flight); the npad indices after them zero the padding scales.
 __global__ void __launch_bounds__(256) quant_attn_fp4_kernel(
     const uint16_t* __restrict__ x, uint32_t nblocks, uint32_t npad, uint32_t N, uint32_t H,
@@ -128,7 +128,7 @@ __global__ void __launch_bounds__(256) quant_attn_fp4_kernel(
     return scales + ((static_cast<int64_t>(bh) * n_tiles + (n >> 7)) * nkk + (cb >> 2)) * 512 +
            (n & 31u) * 16 + ((n >> 5) & 3u) * 4 + (cb & 3u);
   };
-  constexpr uint32_t kUnroll = 4;
+  constexpr uint32_t kUnroll = 2;
   for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < nblocks; i += kUnroll * step) {
     Block16 v[kUnroll];
 #pragma unroll
@@ -399,7 +399,7 @@ cudaError_t launch_quant_attn_fp4(const void* x, int B, int N, int H, int D, uin
   if ((D != 64 && D != 128) || nblocks >= (int64_t{1} << 31) || npad >= (int64_t{1} << 31))
     return cudaErrorInvalidValue;
   const int threads = 256;
-  const int64_t work = std::max<int64_t>((nblocks + 3) / 4, npad);
+  const int64_t work = std::max<int64_t>((nblocks + 1) / 2, npad);
   quant_attn_fp4_kernel<<<wave_grid<quant_attn_fp4_kernel>(work, threads), threads, 0, stream>>>(
       static_cast<const uint16_t*>(x), static_cast<uint32_t>(nblocks), static_cast<uint32_t>(npad),
       static_cast<uint32_t>(N), static_cast<uint32_t>(H), D == 128 ? 3u : 2u,
