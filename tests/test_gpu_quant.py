@@ -43,7 +43,12 @@ def test_quantizer_workload_unit_and_static():
 
 @pytest.mark.parametrize("rows,cols,ld,seed,spread", [(37, 80, 96, 1, 1.0), (1, 16, 16, 2, 1e-3),
                                                       (513, 208, 208, 3, 300.0),
-                                                      (64, 4096, 4104, 4, 1.0)])
+                                                      (64, 4096, 4104, 4, 1.0),
+                                                      # static scale near the fp32 range ends:
+                                                      # outputs 6*448/gsf above 2^124 take the
+                                                      # IEEE path; a clamped amax (1e-12) gives
+                                                      # gsf = 2.688e15
+                                                      (256, 64, 64, 5, 3e37), (128, 128, 128, 6, 1e-14)])
 def test_quantizer_shapes_and_strides(rows, cols, ld, seed, spread):
     x = workloads.random_matrix(rows, cols, seed, spread)
     _check_matrix(x, ld=ld)
