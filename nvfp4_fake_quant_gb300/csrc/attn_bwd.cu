@@ -1,14 +1,18 @@
 // Attn-QAT straight-through backward on sm_103a, dK/dV part (key-outer), and
 // the delta pre-pass.
 //
-// Kernels, in launch order (attn_bwd_dq.cu adds the dQ kernel after them):
+// Kernels, in launch order (the dQ kernel follows them: attn_bwd_dq_fp4.cu for
+// the dense form, attn_bwd_dq.cu for the block-sparse one):
 //   bwd_prep    delta_i = sum_d dO_id * O_id (fp32)
 //   attn_bwd    one CTA per (128-key tile, head, batch); K~ and V~ stay in shared
 //               memory, the dK and dV accumulators in TMEM; the CTA loops over the
 //               128-query tiles:
 //                 S  = Q~ K~^T, dP = dO V~^T              (BF16 UMMA -> TMEM)
 //                 P  = exp(scale*S - m)                    (m from the forward)
-//                 P~ = fq16(P) per 16 keys                 (bit-identical to the forward)
+//                 P~ = fq16(P) per 16 keys                 (the forward's code; S here
+//                                                           from BF16 UMMAs, the forward's
+//                                                           from FP4 ones: equal up to the
+//                                                           fp32 summation order)
 //                 A  = P / l,   dS = scale * A * (dP - delta)
 //                 P~/l and dS -> shared memory (bf16, one buffer used in turn)
 //                 dV += (P~/l)^T dO, dK += dS^T Q~         (BF16 UMMA)

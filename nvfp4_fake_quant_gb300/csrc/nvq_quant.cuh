@@ -18,12 +18,15 @@
 //                   t*s < 2^(es+4)), which an error of one ulp cannot cross.
 //  * quant16_static IEEE fp32 products and quotients (mul.rn / div.rn) in the
 //                   order of the definition: bit-identical to any IEEE fp32
-//                   evaluation of the same steps.  quant16_static_fast takes
-//                   the same decisions through reciprocals, with a check that
-//                   sends the rare doubtful block back to quant16_static.
+//                   evaluation of the same steps.  quant16_static_fast gets
+//                   the same quotients from correctly rounded reciprocals and
+//                   one FMA correction each (Markstein), and sends a block
+//                   whose outputs leave the normal fp32 range to quant16_static.
 //  * pquant16       the softmax probabilities inside attention (fp32 inputs):
 //                   reciprocal and product without snapping.  The forward and
-//                   the backward run this same code on bit-identical inputs.
+//                   the backward run this same code on S values that agree up
+//                   to the summation order of their UMMAs (FP4 in the forward,
+//                   BF16 in the dK/dV kernel).
 #pragma once
 #include <cstdint>
 #include <cuda_bf16.h>
@@ -234,7 +237,7 @@ namespace nvq {
 
 // ---------------------------------------------------------------------------
 // Softmax probabilities inside attention (forward and backward run this same
-// code on bit-identical inputs, so P~ is bit-identical between them).
+// code, so P~ agrees between them up to the S values they are given).
 //
 // Every rounding decision is taken on fp32 values: O is an incoherent sum of
 // P~V~ terms, so even rare decision flips (from an f16 P or an f16 q = P/s)
