@@ -67,11 +67,11 @@ def kernel_work(kind, b, n, h, d):
 # sources at the time: a changed source reports null.
 TRAFFIC = {
     "bwd_dkdv": {"bytes": 438211328, "sources": ['nvfp4_fake_quant_gb300/csrc/attn_bwd.cu', 'nvfp4_fake_quant_gb300/csrc/nvq_ptx.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_quant.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_internal.h'],
-                "sha256": "57759ce2781839ef1f8bc3ec368cc7d7356a3537c74f06a10ef30bd3966b1d2f"},
+                "sha256": "95d08232d8587acee389ac54085e11ce6605ea0b2bf77599790c2560387a4e4d"},
     "bwd_dq": {"bytes": 349384192, "sources": ['nvfp4_fake_quant_gb300/csrc/attn_bwd_dq_fp4.cu', 'nvfp4_fake_quant_gb300/csrc/nvq_ptx.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_quant.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_internal.h'],
-              "sha256": "56ab1398bd0a7f2737929f54fa5ff96ac42938517f3c920195c706c837117015"},
+              "sha256": "3447a0a67411471bcd5e58de7c648a5a526f62a6a57cd70719b4a2c2b0dba18a"},
     "attn_fwd": {"bytes": 173561600, "sources": ['nvfp4_fake_quant_gb300/csrc/attn_fwd_fp4.cu', 'nvfp4_fake_quant_gb300/csrc/nvq_ptx.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_quant.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_internal.h'],
-                "sha256": "fb18999c10e95b8648ce4430d923d1b122a549356adc85f4b4fcc8949414ddd7"},
+                "sha256": "0cf5c08b6bfc2f6b9924154fa09661487798f10e7f4dca65e944540d2fd51a20"},
 }
 
 
