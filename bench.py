@@ -352,16 +352,33 @@ def sparse_bench(peaks, stream, steps, warmup):
         step()
     torch.cuda.synchronize()
     api.timing_enable(True)
-    ms = time_events(step, steps, stream)
+    ms_eager = time_events(step, steps, stream)
     kt = api.timing_read()
     api.timing_enable(False)
     if api.device_status() != 0:
         raise RuntimeError("a bounded device wait timed out (block-sparse)")
+    # The step's kernels are short (the reorders ~20 us each), so issuing them
+    # one call at a time leaves the GPU waiting for the host; a training loop
+    # would replay the step as one CUDA graph.  Same calls, same buffers.
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        step()
+    stream.wait_stream(side)
+    with torch.cuda.graph(graph):
+        step()
+    graph.replay()
+    torch.cuda.synchronize()
+    ms = time_events(graph.replay, steps, stream)
+    if api.device_status() != 0:
+        raise RuntimeError("a bounded device wait timed out (block-sparse, graph)")
     f_fwd = 4.0 * b * h * n * (topk * api.VSA_TILE) * d
     total = sum(t for _, t in kt.values())
     return {"workload": "Wan latent 16x28x56 (N=25088), B=1, H=12, D=128, q,k,v,dO N(0,1) "
                         "(seed 4); 196 cubes of 4x4x8, top-20 key cubes per query cube",
-            "ms_per_step": ms, "TFLOP/s": 3.5 * f_fwd / (ms * 1e-3) / 1e12,
+            "ms_per_step": ms, "launch": "one CUDA graph per step (the calls captured once)",
+            "ms_per_step_eager": ms_eager, "TFLOP/s": 3.5 * f_fwd / (ms * 1e-3) / 1e12,
             "flops_counting": "fwd 4*B*H*N*(topk*128)*D + bwd 2.5x fwd",
             "pct_of_bf16_peak": 3.5 * f_fwd / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
             "kernels": {name: {"launches": c, "avg_ms": t / c, "share": t / total}
