@@ -1,4 +1,7 @@
-// Attn-QAT straight-through backward, dQ part (query-outer).
+// Attn-QAT straight-through backward, dQ part (query-outer), with S on BF16
+// UMMAs: the block-sparse form (the dense form runs attn_bwd_dq_fp4_kernel; the
+// kernel template keeps the dense structure the block-sparse one specialises,
+// but only the block-sparse instances are built).
 //
 //   dQ = scale * dS K~,   dS = A * (dP - delta),   A = P / l = exp(scale*S - m) / l,
 //   dP = dO V~^T,         S = Q~ K~^T
@@ -339,12 +342,11 @@ cudaError_t launch_attn_bwd_dq(const AttnShape& s, const CUtensorMap& tq, const 
                                const CUtensorMap& tk, const CUtensorMap& tv, const float* stats,
                                const float* delta, void* dq, const int* kv_list, int topk,
                                int* err, cudaStream_t stream) {
-  const bool sp = kv_list != nullptr;
+  // block-sparse only: the dense form runs attn_bwd_dq_fp4_kernel
+  if (kv_list == nullptr) return cudaErrorInvalidValue;
   if (s.D == 128)
-    return sp ? launch_dq_t<128, true>(s, tq, tdo, tk, tv, stats, delta, dq, kv_list, topk, err, stream)
-              : launch_dq_t<128, false>(s, tq, tdo, tk, tv, stats, delta, dq, kv_list, topk, err, stream);
-  return sp ? launch_dq_t<64, true>(s, tq, tdo, tk, tv, stats, delta, dq, kv_list, topk, err, stream)
-            : launch_dq_t<64, false>(s, tq, tdo, tk, tv, stats, delta, dq, kv_list, topk, err, stream);
+    return launch_dq_t<128, true>(s, tq, tdo, tk, tv, stats, delta, dq, kv_list, topk, err, stream);
+  return launch_dq_t<64, true>(s, tq, tdo, tk, tv, stats, delta, dq, kv_list, topk, err, stream);
 }
 
 }  // namespace nvq

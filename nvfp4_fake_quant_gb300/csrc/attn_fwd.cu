@@ -26,8 +26,10 @@
 // into the first 32 of its own 64 S columns, which it has already loaded:
 // the 16-key slice kk of P~_i is at column 128 i + 64 (kk / 4) + 8 (kk % 4).
 //
-// Modes (template kMode):
-//   kDense   every key tile, one K/V load per step shared by the two query tiles;
+// Modes (template kMode; the dense form runs attn_fwd_fp4_kernel, so only the
+// block-sparse and auxiliary-output modes are instantiated):
+//   kDense   every key tile, one K/V load per step shared by the two query tiles
+//            (the structure the other two modes specialise);
 //   kSparse  block-sparse: query tile i runs over its own listed key tiles, one
 //            load per query tile per step;
 //   kAux     the auxiliary high-precision output O_hp = P V~ / l next to O (the
@@ -511,13 +513,13 @@ cudaError_t launch_fwd_d(const AttnShape& s, const CUtensorMap& tq, const CUtens
     return launch_fwd_t<D, kSparse>(s, tq, tk, tv, o, o_hp, stats, kv_list, topk, err, stream);
   if (o_hp != nullptr)
     return launch_fwd_t<D, kAux>(s, tq, tk, tv, o, o_hp, stats, kv_list, topk, err, stream);
-  return launch_fwd_t<D, kDense>(s, tq, tk, tv, o, o_hp, stats, kv_list, topk, err, stream);
+  return cudaErrorInvalidValue;  // dense: attn_fwd_fp4_kernel
 }
 
 cudaError_t launch_attn_fwd(const AttnShape& s, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, void* o, void* o_hp, float* stats,
                             const int* kv_list, int topk, int* err, cudaStream_t stream) {
-  if (kv_list != nullptr && o_hp != nullptr) return cudaErrorInvalidValue;
+  if ((kv_list != nullptr) == (o_hp != nullptr)) return cudaErrorInvalidValue;
   return s.D == 128 ? launch_fwd_d<128>(s, tq, tk, tv, o, o_hp, stats, kv_list, topk, err, stream)
                     : launch_fwd_d<64>(s, tq, tk, tv, o, o_hp, stats, kv_list, topk, err, stream);
 }

@@ -78,8 +78,9 @@ int make_bnhd_u8_map(CUtensorMap* map, const void* base, int B, int N, int H, in
 int make_bnhd_map(CUtensorMap* map, const void* base, int B, int N, int H, int D, bool f16,
                    int box_rows = kTile);
 
-// kv_list: NULL (dense) or int32 [B, H, ceil(Nq/128), topk] key tiles per query tile;
-// o_hp: NULL or the auxiliary output P V~ / l (bf16, layout of o); not both
+// BF16-S forward, block-sparse or auxiliary-output form (exactly one of them):
+// kv_list: int32 [B, H, ceil(Nq/128), topk] key tiles per query tile, or o_hp: the
+// auxiliary output P V~ / l (bf16, layout of o).  The dense form is launch_attn_fwd_fp4.
 cudaError_t launch_attn_fwd(const AttnShape& s, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, void* o, void* o_hp, float* stats,
                             const int* kv_list, int topk, int* err, cudaStream_t stream);
@@ -101,7 +102,8 @@ cudaError_t launch_attn_bwd(const AttnShape& s, const CUtensorMap& tq, const CUt
 // q_off [n_kt + 1] and ascending query tiles q_list [n_qt * topk].
 cudaError_t launch_tile_transpose(const int* kv_list, int B, int H, int n_qt, int n_kt, int topk,
                                   int* q_off, int* q_list, cudaStream_t stream);
-// dQ (query-outer; Q~, dO, K~, V~ maps with 128-row boxes)
+// block-sparse dQ with BF16 S (query-outer; Q~, dO, K~, V~ maps with 128-row boxes;
+// kv_list required: the dense form is launch_attn_bwd_dq_fp4)
 cudaError_t launch_attn_bwd_dq(const AttnShape& s, const CUtensorMap& tq, const CUtensorMap& tdo,
                                const CUtensorMap& tk, const CUtensorMap& tv, const float* stats,
                                const float* delta, void* dq, const int* kv_list, int topk,
