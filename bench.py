@@ -67,11 +67,11 @@ def kernel_work(kind, b, n, h, d):
 # sources at the time: a changed source reports null.
 TRAFFIC = {
     "bwd_dkdv": {"bytes": 438211328, "sources": ['nvfp4_fake_quant_gb300/csrc/attn_bwd.cu', 'nvfp4_fake_quant_gb300/csrc/nvq_ptx.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_quant.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_internal.h'],
-                "sha256": "95d08232d8587acee389ac54085e11ce6605ea0b2bf77599790c2560387a4e4d"},
+                "sha256": "06550a8286468dea84648e0c7c58a21bd1e2ff7f8e40811b2aea9ad0bdff9e69"},
     "bwd_dq": {"bytes": 349384192, "sources": ['nvfp4_fake_quant_gb300/csrc/attn_bwd_dq_fp4.cu', 'nvfp4_fake_quant_gb300/csrc/nvq_ptx.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_quant.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_internal.h'],
-              "sha256": "3447a0a67411471bcd5e58de7c648a5a526f62a6a57cd70719b4a2c2b0dba18a"},
+              "sha256": "2eb21eafec8d8aabd689c67267e2cc75d9ab696f466947f0ae6e580c28dbe858"},
     "attn_fwd": {"bytes": 173561600, "sources": ['nvfp4_fake_quant_gb300/csrc/attn_fwd_fp4.cu', 'nvfp4_fake_quant_gb300/csrc/nvq_ptx.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_quant.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_internal.h'],
-                "sha256": "0cf5c08b6bfc2f6b9924154fa09661487798f10e7f4dca65e944540d2fd51a20"},
+                "sha256": "80e409674a3707b9119daa067d7c2cf661bedd636bedd4fdc0bb5d9641552e1e"},
 }
 
 
