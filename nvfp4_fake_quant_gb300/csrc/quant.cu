@@ -167,8 +167,10 @@ __device__ __forceinline__ int64_t tiled_scale_offset(int64_t r, int64_t cb, int
 }
 
 // Packed codes (row-major, cols/2 bytes per row) and scales in the tiled layout.
-// A flat grid-stride loop over the rows*nbc blocks (32-bit index arithmetic
-// when the count fits), each thread loading two blocks before quantizing.
+// A flat grid-stride loop over the rows*nbc blocks, each thread loading two
+// blocks before quantizing.  A block's (row, block column) is split off its
+// flat index once per thread and then advanced by the grid stride's own
+// (rows, columns) with one carry, with no division per block.
 template <int MODE>
 __global__ void __launch_bounds__(256) quant_tiled_kernel(
     const uint16_t* __restrict__ x, int64_t rows, int64_t nbc, int64_t ld_x,
@@ -176,26 +178,23 @@ __global__ void __launch_bounds__(256) quant_tiled_kernel(
   const float g = (MODE == kStaticBf16) ? *gsf : 1.0f;
   const float inv_g = (MODE == kStaticBf16) ? __frcp_rn(g) : 1.0f;
   const int64_t total = rows * nbc;
-  const bool narrow = total <= 0xFFFFFFFFll;
-  const uint32_t nbc32 = static_cast<uint32_t>(nbc);
   const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
   const int64_t n_bt = (nbc + 3) / 4;
-  auto split = [&](int64_t i, int64_t& r, int64_t& cb) {
-    if (narrow) {
-      const uint32_t q = static_cast<uint32_t>(i) / nbc32;
-      r = q;
-      cb = static_cast<int64_t>(static_cast<uint32_t>(i) - q * nbc32);
-    } else {
-      r = i / nbc;
-      cb = i - r * nbc;
+  const int64_t i0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  int64_t r0 = i0 / nbc, c0 = i0 - r0 * nbc;         // block i
+  const int64_t dr = step / nbc, dc = step - dr * nbc;  // the grid stride
+  auto advance = [&](int64_t& r, int64_t& c) {
+    r += dr;
+    c += dc;
+    if (c >= nbc) {
+      c -= nbc;
+      ++r;
     }
   };
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
-       i += 2 * step) {
-    int64_t r0, c0, r1 = 0, c1 = 0;
-    split(i, r0, c0);
+  for (int64_t i = i0; i < total; i += 2 * step) {
+    int64_t r1 = r0, c1 = c0;
+    advance(r1, c1);  // block i + step
     const bool two = i + step < total;
-    if (two) split(i + step, r1, c1);
     const Block16 v0 = load_block(x + r0 * ld_x + c0 * 16);
     Block16 v1;
     if (two) v1 = load_block(x + r1 * ld_x + c1 * 16);
@@ -203,6 +202,9 @@ __global__ void __launch_bounds__(256) quant_tiled_kernel(
     if (two)
       quant_block<MODE>(v1, g, inv_g, nullptr, scales + tiled_scale_offset(r1, c1, n_bt),
                         codes + (i + step) * 8);
+    r0 = r1;
+    c0 = c1;
+    advance(r0, c0);  // block i + 2 step
   }
 }
 
