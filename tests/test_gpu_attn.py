@@ -35,6 +35,10 @@ CASES = [
     ("single", 1, 1, 1, 1, 64, False, 15, "normal", None),
     ("unit_rms", 1, 640, 640, 2, 128, False, 16, "unit_rms", None),
     ("lognormal_channels", 1, 520, 520, 2, 128, False, 17, "lognormal_channels", None),
+    # 13 key tiles (ragged last): pass-1 tiles unevenly over the four warpgroups,
+    # barrier and scale-copy indices past their first wrap
+    ("thirteen_tiles", 1, 1650, 1650, 1, 128, False, 18, "unit_rms", None),
+    ("thirteen_tiles_causal", 1, 1650, 1650, 1, 64, True, 19, "normal", None),
 ]
 
 
