@@ -313,8 +313,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float negmb = -m * kLog2e;
     const float inv_l = ex2_f32((m - lse) * kLog2e);  // 1 / l
     const uint64_t c12 = pk2(c1, c1), nmb2 = pk2(negmb, negmb);
-    const uint64_t sl2 = pk2(scale * inv_l, scale * inv_l);  // dS carries the softmax scale
-    const uint64_t ndl2 = pk2(-dl, -dl);
+    // dS = P * (sl dP - sl delta), sl = scale / l (dS carries the softmax scale)
+    const float sl = scale * inv_l;
+    const uint64_t sl2 = pk2(sl, sl), nsd2 = pk2(-sl * dl, -sl * dl);
     const uint32_t kc = static_cast<uint32_t>(g * 32);
     bool ok = true;
     uint32_t rs[32], rd[32];
@@ -330,7 +331,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive_warp(sdp_free);  // S_{j+1} and dP_{j+1} may overwrite them now
-      // dS = (scale / l) * exp(scale*S - m) * (dP - delta), 32 keys
+      // dS = (scale / l) * exp(scale*S - m) * (dP - delta), 32 keys, as
+      // P * fma(dP, sl, -sl * delta)
       uint32_t dsw[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
@@ -341,10 +343,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!(row_ok && k0 < Nkv && (!causal || k0 <= qrow))) x0 = -INFINITY;
           if (!(row_ok && k0 + 1 < Nkv && (!causal || k0 + 1 <= qrow))) x1 = -INFINITY;
         }
-        const uint64_t a2 = mul2(pk2(ex2_f32(x0), ex2_f32(x1)), sl2);
+        const uint64_t t2 = fma2(pk2(__uint_as_float(rd[2 * i]), __uint_as_float(rd[2 * i + 1])), sl2, nsd2);
         float d0, d1;
-        up2(mul2(a2, add2(pk2(__uint_as_float(rd[2 * i]), __uint_as_float(rd[2 * i + 1])), ndl2)),
-            d0, d1);
+        up2(mul2(pk2(ex2_f32(x0), ex2_f32(x1)), t2), d0, d1);
         dsw[i] = pack_bf16(d0, d1);
       }
       // the dS buffer is free once dQ += dS_{j-1} K~_{j-1} is done
