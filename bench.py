@@ -66,11 +66,11 @@ def kernel_work(kind, b, n, h, d):
 # (profiles/traffic_attn_kernels_wan25088.md), with the SHA-256 of the kernel's
 # sources at the time: a changed source reports null.
 TRAFFIC = {
-    "bwd_dkdv": {"bytes": 438211328, "sources": ['nvfp4_fake_quant_gb300/csrc/attn_bwd.cu', 'nvfp4_fake_quant_gb300/csrc/nvq_ptx.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_quant.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_internal.h'],
+    "bwd_dkdv": {"bytes": 439465472, "sources": ['nvfp4_fake_quant_gb300/csrc/attn_bwd.cu', 'nvfp4_fake_quant_gb300/csrc/nvq_ptx.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_quant.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_internal.h'],
                 "sha256": "06550a8286468dea84648e0c7c58a21bd1e2ff7f8e40811b2aea9ad0bdff9e69"},
-    "bwd_dq": {"bytes": 349384192, "sources": ['nvfp4_fake_quant_gb300/csrc/attn_bwd_dq_fp4.cu', 'nvfp4_fake_quant_gb300/csrc/nvq_ptx.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_quant.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_internal.h'],
-              "sha256": "2eb21eafec8d8aabd689c67267e2cc75d9ab696f466947f0ae6e580c28dbe858"},
-    "attn_fwd": {"bytes": 173561600, "sources": ['nvfp4_fake_quant_gb300/csrc/attn_fwd_fp4.cu', 'nvfp4_fake_quant_gb300/csrc/nvq_ptx.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_quant.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_internal.h'],
+    "bwd_dq": {"bytes": 350589952, "sources": ['nvfp4_fake_quant_gb300/csrc/attn_bwd_dq_fp4.cu', 'nvfp4_fake_quant_gb300/csrc/nvq_ptx.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_quant.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_internal.h'],
+              "sha256": "becd6cbc983ebb8d4bcbcf51586a160b801c48db4ae6bd534f1b55c7ae8144c1"},
+    "attn_fwd": {"bytes": 173405440, "sources": ['nvfp4_fake_quant_gb300/csrc/attn_fwd_fp4.cu', 'nvfp4_fake_quant_gb300/csrc/nvq_ptx.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_quant.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_internal.h'],
                 "sha256": "80e409674a3707b9119daa067d7c2cf661bedd636bedd4fdc0bb5d9641552e1e"},
 }
 
