@@ -200,10 +200,47 @@ def aggregate(ms_local: float, flops_local: float, dist, dev):
     return ms, flops / (ms * 1e-3) / 1e12
 
 
-def cpu_baseline(rows: int, head: int = 0):
-    """The oracle, as it stands, on query rows [0, rows) of one head (all keys)."""
-    import torch
+def host_info():
+    """The host the oracle runs on: usable cores, CPU model, torch's CPU threads."""
+    import platform
 
+    import torch
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    if not model:
+        try:
+            with open("/proc/cpuinfo") as f:
+                for line in f:
+                    if line.lower().startswith("model name"):
+                        model = line.split(":", 1)[1].strip()
+                        break
+        except Exception:
+            pass
+    return {"cores": len(os.sched_getaffinity(0)), "cpu_model": model or platform.machine(),
+            "torch_threads": torch.get_num_threads(), "arch": platform.machine()}
+
+
+# The oracle's sample of the headline workload, the same in both arms: query
+# rows [0, CPU_ROWS) of head 0 against all 25088 keys, forward + backward.
+CPU_ROWS = 4096
+
+
+def _timed(fn, repeats):
+    t0 = time.perf_counter()
+    for _ in range(repeats):
+        fn()
+    return (time.perf_counter() - t0) / repeats
+
+
+def cpu_baseline(rows: int = CPU_ROWS, head: int = 0, repeats: int = 1):
+    """The oracle, as it stands, on query rows [0, rows) of one head (all keys)."""
     from nvfp4_fake_quant_gb300 import workloads
     from oracle import attention as oa
     inp = workloads.wan25088()
@@ -211,23 +248,105 @@ def cpu_baseline(rows: int, head: int = 0):
     k = inp.k[:, :, head:head + 1]
     v = inp.v[:, :, head:head + 1]
     do = inp.do[:, :rows, head:head + 1]
-    t0 = time.perf_counter()
-    o, _, _ = oa.attn_fwd(q, k, v, inp.scale)
-    oa.attn_bwd(q, k, v, o, do, inp.scale)
-    dt = time.perf_counter() - t0
+
+    def one():
+        o, _, _ = oa.attn_fwd(q, k, v, inp.scale)
+        oa.attn_bwd(q, k, v, o, do, inp.scale)
+    dt = _timed(one, repeats)
     fl = 3.5 * flops_fwd(1, rows, SHAPE["n"], 1, SHAPE["d"])
-    return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": torch.get_num_threads(),
-            "kind": "oracle", "seconds": dt,
+    return {"value": fl / dt / 1e12, "unit": "TFLOP/s", **host_info(), "kind": "oracle",
+            "seconds": dt * repeats, "repeats": repeats,
             "sample": f"query rows 0..{rows - 1} of head {head} (of 12) against all "
                       f"{SHAPE['n']} keys, fwd+bwd in float64; value = counted FLOPs of that "
                       "slice / its time"}
+
+
+def cpu_quantizer():
+    """The oracle's quantizer over the whole 4096x4096 workload (unit and static
+    global scale), in GB/s of the same algorithmic bytes as the GPU figure."""
+    from nvfp4_fake_quant_gb300 import workloads
+    from oracle import nvfp4 as onv
+    x = workloads.quant_matrix()
+    g = onv.global_sf(x)
+    out = {}
+    for name, gsf in (("unit_gsf", 1.0), ("static_gsf", g)):
+        dt = _timed(lambda: onv.quantizer_outputs(x, gsf), 1)
+        out[name] = {"value": x.numel() * 4.0625 / dt / 1e9, "seconds": dt}
+    return {**out, "unit": "GB/s", **host_info(), "kind": "oracle",
+            "sample": "the whole 4096x4096 matrix, codes + scales + dequantized bf16"}
+
+
+def cpu_sparse(rows: int = 2048, head: int = 0):
+    """The oracle's block selection and block-sparse fwd+bwd on query rows
+    [0, rows) (whole cubes) of one head of the block-sparse workload."""
+    from nvfp4_fake_quant_gb300 import api, workloads
+    from oracle import attention as oa
+    from oracle import vsa as ov
+    inp = workloads.vsa25088()
+    t, hh, w = workloads.VSA_GRID
+    b, n, _, _, d = inp.shape
+    topk = api.vsa_effective_topk(0.9, n // 128)
+    sl = slice(head, head + 1)
+    qc, kc, vc, doc = (ov.to_cubes(x[:, :, sl], t, hh, w) for x in (inp.q, inp.k, inp.v, inp.do))
+
+    def one():
+        tiles = ov.select_tiles(qc, kc, topk)[:, :, :rows // 128]
+        o, _, _ = oa.attn_fwd(qc[:, :rows], kc, vc, inp.scale, kv_tiles=tiles)
+        oa.attn_bwd(qc[:, :rows], kc, vc, o, doc[:, :rows], inp.scale, kv_tiles=tiles)
+    dt = _timed(one, 1)
+    fl = 3.5 * 4.0 * rows * topk * 128 * d
+    return {"value": fl / dt / 1e12, "unit": "TFLOP/s", **host_info(), "kind": "oracle",
+            "seconds": dt,
+            "sample": f"head {head}: cube order, selection of all query cubes, fine attention "
+                      f"fwd+bwd of query cubes 0..{rows // 128 - 1} (float64); value = counted "
+                      "sparse FLOPs of that slice / its time"}
+
+
+def cpu_hp(rows: int = CPU_ROWS, head: int = 0):
+    """The oracle's auxiliary-output forward and the backward with delta from it,
+    on the headline sample."""
+    from nvfp4_fake_quant_gb300 import workloads
+    from oracle import attention as oa
+    inp = workloads.wan25088()
+    q = inp.q[:, :rows, head:head + 1]
+    k, v = inp.k[:, :, head:head + 1], inp.v[:, :, head:head + 1]
+    do = inp.do[:, :rows, head:head + 1]
+
+    def one():
+        o, _, _ = oa.attn_fwd(q, k, v, inp.scale)
+        oa.attn_fwd_hp(q, k, v, inp.scale)
+        oa.attn_bwd(q, k, v, o, do, inp.scale, delta_mode="hp")
+    dt = _timed(one, 1)
+    fl = 3.5 * flops_fwd(1, rows, SHAPE["n"], 1, SHAPE["d"])
+    return {"value": fl / dt / 1e12, "unit": "TFLOP/s", **host_info(), "kind": "oracle",
+            "seconds": dt,
+            "sample": f"query rows 0..{rows - 1} of head {head} against all keys: forward, "
+                      "auxiliary output and backward with delta from it (float64)"}
+
+
+def cpu_linear(rows: int = 2048):
+    """The oracle's NVFP4 linear forward and backward on rows [0, rows) of x."""
+    from nvfp4_fake_quant_gb300 import workloads
+    from oracle import linear as ol
+    inp = workloads.wan_ffn_up()
+    x, g = inp.x[:rows], inp.grad[:rows]
+
+    def one():
+        ol.linear_fwd(x, inp.w, inp.bias)
+        ol.linear_bwd(g, x, inp.w)
+    dt = _timed(one, 1)
+    fl = 6.0 * rows * inp.w.shape[0] * inp.w.shape[1]
+    return {"value": fl / dt / 1e12, "unit": "TFLOP/s", **host_info(), "kind": "oracle",
+            "seconds": dt,
+            "sample": f"rows 0..{rows - 1} of x: quantized forward (weight quantized whole) and "
+                      "the three straight-through gradients (float64); value = 6*rows*N*K / time"}
 
 
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
-    rows = args.ref_rows
+    rows = CPU_ROWS
     vals = []
     for _ in range(args.warmup):
         cpu_baseline(rows)
@@ -646,7 +765,10 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "vs_baseline": None, "dtype": "fp4+bf16", "data": "synthetic",
+        "precision": ("Q~/K~/V~/P~ NVFP4 (E2M1 codes, E4M3 scale per 16, unit global scale); "
+                      "S on block-scaled FP4 UMMAs (exact products), P~V~ on F16 UMMAs, backward "
+                      "contractions on BF16 UMMAs; fp32 accumulation; bf16 outputs"),
         "config": {"workload": WORKLOAD if (n, h) == (25088, 12) else
                    f"profiling case B=1, H={h}, N={n}, D=128 (Wan recipe, seed 2)",
                    "flops_per_step": f_step,
@@ -666,16 +788,49 @@ def run_ours(args):
         "gpu_launches": sum(k["launches"] for k in kernels.values()),
         "clocks": clocks,
     }
+    cpu = rank == 0 and not args.skip_cpu_baseline
     if quant is not None:
+        if cpu:
+            quant["cpu_baseline"] = cpu_quantizer()
         line["quantizer"] = quant
     if sparse is not None:
+        if cpu:
+            sparse["cpu_baseline"] = cpu_sparse()
         line["block_sparse"] = sparse
     if hp is not None:
+        if cpu:
+            hp["cpu_baseline"] = cpu_hp()
         line["aux_output"] = hp
     if lin is not None:
+        if cpu:
+            lin["cpu_baseline"] = cpu_linear()
         line["nvfp4_linear"] = lin
-    if rank == 0 and not args.skip_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(args.cpu_rows)
+    if cpu:
+        line["cpu_baseline"] = cpu_baseline(CPU_ROWS, repeats=args.cpu_repeats)
+    # compact figures of every report, last on the line (read from its tail)
+    summ = {"step_ms": ms, "pct_of_bf16_peak": line["pct_of_bf16_peak"],
+            "roofline_frac": roofline["frac"], "e2e_ms": e2e_ms}
+    if quant is not None:
+        summ["quantizer_frac"] = {m: quant[m]["frac"] for m in ("unit", "static")}
+        if "cpu_baseline" in quant:
+            summ["quantizer_cpu_GB/s"] = {m: quant["cpu_baseline"][m + "_gsf"]["value"]
+                                          for m in ("unit", "static")}
+    for key, rep in (("block_sparse", sparse), ("aux_output", hp)):
+        if rep is not None:
+            summ[key] = {"ms_per_step": rep["ms_per_step"], "TFLOP/s": rep["TFLOP/s"],
+                         "pct_of_bf16_peak": rep["pct_of_bf16_peak"]}
+            if "cpu_baseline" in rep:
+                summ[key]["cpu_TFLOP/s"] = rep["cpu_baseline"]["value"]
+    if lin is not None:
+        summ["nvfp4_linear"] = {"fwd_ms": lin["fwd_ms"], "bwd_ms": lin["bwd_ms"],
+                                "fp4_gemm_tflops": lin["fp4_gemm_tflops"],
+                                "bwd_gemm_tflops": lin["bwd_gemm_tflops"]}
+        if "cpu_baseline" in lin:
+            summ["nvfp4_linear"]["cpu_TFLOP/s"] = lin["cpu_baseline"]["value"]
+    if "cpu_baseline" in line:
+        summ["cpu_TFLOP/s"] = line["cpu_baseline"]["value"]
+        summ["cpu_cores"] = line["cpu_baseline"]["cores"]
+    line["summary"] = summ
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist is not None:
@@ -689,8 +844,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--cpu-rows", type=int, default=25088)
-    ap.add_argument("--ref-rows", type=int, default=512)
+    ap.add_argument("--cpu-repeats", type=int, default=4,
+                    help="repeats of the oracle's sample in the cpu_baseline object")
     ap.add_argument("--skip-cpu-baseline", action="store_true")
     ap.add_argument("--skip-quantizer", action="store_true")
     ap.add_argument("--skip-e2e", action="store_true")

@@ -148,6 +148,37 @@ nvq_status nvfp4_quantize_codes(const void* x, int64_t rows, int64_t cols, int64
  *           256-byte aligned; contents on entry do not matter
  */
 size_t attn_qat_fwd_workspace(int B, int Nq, int Nkv, int H, int D);
+
+/*
+ * Where a call keeps the quantized operands in its workspace: byte offsets from
+ * the workspace base (each 256-byte aligned) of
+ *   q_codes, k_codes   the E2M1 codes of Q~ and K~: uint8 [B, N, H, D/2], two a
+ *                      byte (element 2i in the low nibble; sign << 3 | E2M1
+ *                      magnitude index, the sign of x on zero codes)
+ *   q_scales, k_scales their E4M3 block scales as 512-byte scale blocks: for
+ *                      batch b, head h, 128-token tile t and 64-element group g
+ *                      of D, the block at ((((b * H + h) * ceil(N / 128) + t) *
+ *                      (D / 64)) + g) * 512 holds the scale of token r of the
+ *                      tile and 16-element block j of the group at byte
+ *                      (r % 32) * 16 + (r / 32) * 4 + j; tokens t * 128 + r >= N
+ *                      have scale byte 0.  (The layout in which the block-scaled
+ *                      tensor-core MMA reads its scale operand.)
+ *   v_f16              V~ as f16 [B, Nkv, H, D]
+ *   q_bf16, k_bf16, v_bf16  Q~, K~, V~ as bf16 [B, N, H, D]
+ *   delta              f32 [B, H, Nq]: rowsum(dO * o) (backward only)
+ *   total              the workspace size (*_workspace())
+ * A region the workspace does not have is SIZE_MAX.  After attn_qat_fwd the
+ * forward workspace holds q_codes, k_codes, q_scales, k_scales and v_f16
+ * (attn_qat_fwd_hp and attn_qat_fwd_sparse: q_bf16, k_bf16, v_f16); after
+ * attn_qat_bwd the backward workspace holds every region it has.  Other bytes
+ * are unspecified.  NVQ_ERR_INVALID for sizes the calls reject or a NULL out.
+ */
+typedef struct {
+  size_t q_codes, k_codes, q_scales, k_scales, v_f16, q_bf16, k_bf16, v_bf16, delta, total;
+} nvq_attn_layout;
+nvq_status attn_qat_fwd_layout(int B, int Nq, int Nkv, int H, int D, nvq_attn_layout* out);
+nvq_status attn_qat_bwd_layout(int B, int Nq, int Nkv, int H, int D, nvq_attn_layout* out);
+
 nvq_status attn_qat_fwd(const void* q, const void* k, const void* v,
                         int B, int Nq, int Nkv, int H, int D, float scale, int causal,
                         void* o, float* stats, void* ws, size_t ws_bytes, nvq_stream_t stream);
@@ -196,11 +227,14 @@ nvq_status attn_qat_bwd(const void* q, const void* k, const void* v, const void*
  * device.  Arguments and results are those of attn_qat_bwd minus ws/ws_bytes.
  *
  * Scratch comes from one 32 MiB array inside the library (held by every GPU
- * that loads the library until the process exits).  A problem whose
+ * that loads the library until the process exits).  The arguments are checked
+ * as attn_qat_bwd checks them (same status codes); then a problem whose
  * attn_qat_bwd_workspace(B, Nq, Nkv, H, D) exceeds 32 MiB is rejected with
- * NVQ_ERR_WORKSPACE before anything is launched.  The first call on a device
- * looks up the array's device address (cudaGetSymbolAddress) with that device
- * current; make that first call before any stream capture.  Every call shares
+ * NVQ_ERR_WORKSPACE.  Either way nothing is launched.  The first call on a
+ * device looks up the array's device address (cudaGetSymbolAddress) with that
+ * device current, and looks it up again when the thread's current context for
+ * the device has changed (a device reset reloads the module elsewhere); make
+ * that first call before any stream capture.  Every call shares
  * the one array: calls whose work overlaps on the GPU (other streams, other
  * host threads) race and corrupt each other's results.  The backward writes
  * every byte of scratch it later reads, so the previous call's contents do

@@ -30,6 +30,8 @@ SIGNATURES = {
     "nvfp4_quantize_codes": (c_int, [c_void_p, c_int64, c_int64, c_int64, c_void_p, c_void_p,
                                      c_int64, c_void_p, c_int64, c_void_p]),
     "attn_qat_fwd_workspace": (c_size_t, [c_int, c_int, c_int, c_int, c_int]),
+    "attn_qat_fwd_layout": (c_int, [c_int, c_int, c_int, c_int, c_int, c_void_p]),
+    "attn_qat_bwd_layout": (c_int, [c_int, c_int, c_int, c_int, c_int, c_void_p]),
     "attn_qat_fwd": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int,
                              c_float, c_int, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
     "attn_qat_fwd_hp": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int,
@@ -71,6 +73,14 @@ SIGNATURES = {
     "nvq_selftest_fp4": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                  c_int, c_int, c_int, c_int, c_void_p]),
 }
+
+
+class AttnLayout(ctypes.Structure):
+    """nvq_attn_layout: byte offsets of the regions of an attention workspace."""
+    _fields_ = [(name, c_size_t) for name in (
+        "q_codes", "k_codes", "q_scales", "k_scales", "v_f16", "q_bf16", "k_bf16", "v_bf16",
+        "delta", "total")]
+
 
 STATUS = {0: "NVQ_OK", 1: "NVQ_ERR_INVALID", 2: "NVQ_ERR_UNSUPPORTED", 3: "NVQ_ERR_WORKSPACE",
           4: "NVQ_ERR_CUDA", 5: "NVQ_ERR_TIMEOUT"}

@@ -109,12 +109,32 @@ def default_scale(d: int) -> float:
     return 1.0 / math.sqrt(d)
 
 
+def _scale(scale, d: int) -> float:
+    """The softmax scale to pass: None or NaN mean the default 1/sqrt(D)."""
+    if scale is None or math.isnan(float(scale)):
+        return default_scale(d)
+    return float(scale)
+
+
 def attn_qat_fwd_workspace(b, nq, nkv, h, d) -> int:
     return int(_lib.load().attn_qat_fwd_workspace(b, nq, nkv, h, d))
 
 
 def attn_qat_bwd_workspace(b, nq, nkv, h, d) -> int:
     return int(_lib.load().attn_qat_bwd_workspace(b, nq, nkv, h, d))
+
+
+NO_REGION = 2 ** 64 - 1  # SIZE_MAX: the workspace has no such region
+
+
+def attn_qat_layout(b, nq, nkv, h, d, which: str = "fwd") -> dict:
+    """Byte offsets of the regions of the forward ("fwd") or backward ("bwd")
+    workspace (nvq_attn_layout); absent regions are left out."""
+    import ctypes
+    lay = _lib.AttnLayout()
+    _lib.call(f"attn_qat_{which}_layout", b, nq, nkv, h, d, ctypes.addressof(lay))
+    return {name: getattr(lay, name) for name, _ in lay._fields_
+            if getattr(lay, name) != NO_REGION}
 
 
 def _workspace(nbytes: int, device, ws: torch.Tensor | None) -> torch.Tensor:
@@ -129,8 +149,7 @@ def _fwd_args(q, k, v, scale, o, stats, workspace):
     nkv = k.shape[1]
     _check_bnhd(k, "k", (b, nkv, h, d))
     _check_bnhd(v, "v", (b, nkv, h, d))
-    scale = default_scale(d) if scale is None or (isinstance(scale, float) and math.isnan(scale)) \
-        else float(scale)
+    scale = _scale(scale, d)
     if o is None:
         o = torch.empty_like(q)
     if stats is None:
@@ -174,7 +193,7 @@ def attn_qat_bwd(q, k, v, o, stats, do, scale=None, causal=False, dq=None, dk=No
     _check_bnhd(o, "o", q.shape)
     _check_bnhd(do, "do", q.shape)
     _check(stats, "stats", torch.float32)
-    scale = default_scale(d) if scale is None else float(scale)
+    scale = _scale(scale, d)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
@@ -369,7 +388,7 @@ def attn_qat_fwd_sparse(q, k, v, kv_tiles, scale=None, o=None, stats=None, works
     _check_bnhd(v, "v", q.shape)
     _check_tiles(kv_tiles, b, h, n)
     topk = kv_tiles.shape[-1]
-    scale = default_scale(d) if scale is None else float(scale)
+    scale = _scale(scale, d)
     o = torch.empty_like(q) if o is None else o
     if stats is None:
         stats = torch.empty((b, h, 2, n), dtype=torch.float32, device=q.device)
@@ -398,7 +417,7 @@ def attn_qat_bwd_sparse(q, k, v, o, stats, do, kv_tiles, scale=None, dq=None, dk
     _check(stats, "stats", torch.float32)
     _check_tiles(kv_tiles, b, h, n)
     topk = kv_tiles.shape[-1]
-    scale = default_scale(d) if scale is None else float(scale)
+    scale = _scale(scale, d)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
@@ -445,7 +464,15 @@ class AttnQATFunction(torch.autograd.Function):
 
 
 class AttnQAT(torch.nn.Module):
-    """``AttentionImpl(num_heads, head_size, softmax_scale, causal)`` with ``forward(q, k, v)``."""
+    """``AttentionImpl(num_heads, head_size, softmax_scale, causal)`` with ``forward(q, k, v)``.
+
+    ``delta_mode`` chooses where the backward's delta comes from.  The default
+    "o" takes it from the returned output O (the exact straight-through
+    derivative of the forward, the reading the parity tests use).  This differs
+    from the pages: ``attn_qat_train()`` ("attn_qat_train" API page) hard-codes
+    ``use_high_prec_o = True``, i.e. delta from the auxiliary high-precision
+    output P V~ / l, which ``delta_mode="hp"`` selects.
+    """
 
     def __init__(self, num_heads: int, head_size: int, softmax_scale: float | None = None,
                  causal: bool = False, dropout_p: float = 0.0, delta_mode: str = "o"):

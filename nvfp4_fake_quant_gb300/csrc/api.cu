@@ -41,6 +41,7 @@ namespace {
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 int* g_err_ptr[kMaxDevices] = {};
+CUcontext g_err_ctx[kMaxDevices] = {};
 
 using CtxGetCurrentFn = CUresult (*)(CUcontext*);
 
@@ -73,17 +74,27 @@ cudaError_t bind_context(int dev) {
   return ctx != nullptr ? cudaSuccess : cudaSetDevice(dev);
 }
 
-// Address of this device's error word (looked up once per device, with that
-// device current), after making sure a context is current on this thread.
-// On failure records the reason and returns nullptr.
+}  // namespace
+
+cudaError_t current_device_context(int* dev, CUcontext* ctx) {
+  cudaError_t e = cudaGetDevice(dev);
+  if (e != cudaSuccess) return e;
+  e = bind_context(*dev);
+  if (e != cudaSuccess) return e;
+  *ctx = nullptr;
+  return ctx_get_current_fn()(ctx) == CUDA_SUCCESS ? cudaSuccess : cudaErrorInitializationError;
+}
+
+namespace {
+
+// Address of this device's error word, after making sure a context is current
+// on this thread.  Looked up with cudaGetSymbolAddress once per device and
+// context (a module reloaded into a new context after a device reset lives at
+// a new address).  On failure records the reason and returns nullptr.
 int* error_word() {
   int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) {
-    fail_cuda("cudaGetDevice", e);
-    return nullptr;
-  }
-  e = bind_context(dev);
+  CUcontext ctx = nullptr;
+  cudaError_t e = current_device_context(&dev, &ctx);
   if (e != cudaSuccess) {
     fail_cuda("bind the device's context to this thread", e);
     return nullptr;
@@ -93,7 +104,7 @@ int* error_word() {
     return nullptr;
   }
   std::lock_guard<std::mutex> lock(g_mu);
-  if (g_err_ptr[dev] == nullptr) {
+  if (g_err_ptr[dev] == nullptr || g_err_ctx[dev] != ctx) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_error_word);
     if (e != cudaSuccess) {
@@ -101,6 +112,7 @@ int* error_word() {
       return nullptr;
     }
     g_err_ptr[dev] = static_cast<int*>(p);
+    g_err_ctx[dev] = ctx;
   }
   return g_err_ptr[dev];
 }
@@ -221,26 +233,23 @@ size_t bytes_bnhd(int B, int N, int H, int D, size_t elem) {
   return static_cast<size_t>(B) * N * H * D * elem;
 }
 
-// Forward workspace.  BF16 operands (block-sparse and auxiliary-output forms):
-// Q~, K~ (bf16) and V~ (f16) at q, k, v.  FP4 operands (the dense form): the
-// packed codes of Q~ and K~ at qc, kc, their scale blocks at qs, ks, V~ (f16)
-// at v4.  total covers both layouts.
+// Forward workspace: every region at its own offset (nvq_attn_layout).  The
+// dense form writes the packed codes of Q~ and K~ (qc, kc), their scale blocks
+// (qs, ks) and V~ as f16 (v16); the block-sparse and auxiliary-output forms,
+// whose S runs on BF16 UMMAs, write Q~ and K~ as bf16 (qb, kb) and V~ as f16.
 struct FwdWs {
-  size_t q, k, v, qc, kc, qs, ks, v4, total;
+  size_t qc, kc, qs, ks, v16, qb, kb, total;
 };
 FwdWs fwd_ws(int B, int Nq, int Nkv, int H, int D) {
   FwdWs w;
-  w.q = 0;
-  w.k = round_up(w.q + bytes_bnhd(B, Nq, H, D, 2), 256);
-  w.v = round_up(w.k + bytes_bnhd(B, Nkv, H, D, 2), 256);
-  const size_t bf16_total = round_up(w.v + bytes_bnhd(B, Nkv, H, D, 2), 256);
   w.qc = 0;
   w.kc = round_up(w.qc + bytes_bnhd(B, Nq, H, D, 1) / 2, 256);
   w.qs = round_up(w.kc + bytes_bnhd(B, Nkv, H, D, 1) / 2, 256);
   w.ks = round_up(w.qs + attn_fp4_scale_bytes(B, Nq, H, D), 256);
-  w.v4 = round_up(w.ks + attn_fp4_scale_bytes(B, Nkv, H, D), 256);
-  const size_t fp4_total = round_up(w.v4 + bytes_bnhd(B, Nkv, H, D, 2), 256);
-  w.total = bf16_total > fp4_total ? bf16_total : fp4_total;
+  w.v16 = round_up(w.ks + attn_fp4_scale_bytes(B, Nkv, H, D), 256);
+  w.qb = round_up(w.v16 + bytes_bnhd(B, Nkv, H, D, 2), 256);
+  w.kb = round_up(w.qb + bytes_bnhd(B, Nq, H, D, 2), 256);
+  w.total = round_up(w.kb + bytes_bnhd(B, Nkv, H, D, 2), 256);
   return w;
 }
 
@@ -320,7 +329,7 @@ nvq_status fwd_impl(const void* q, const void* k, const void* v, int B, int Nq, 
     uint8_t* kc = wb + w.kc;
     uint8_t* qs = wb + w.qs;
     uint8_t* ks = wb + w.ks;
-    void* vt = wb + w.v4;
+    void* vt = wb + w.v16;
     if ((r = make_bnhd_u8_map(&mq, qc, B, Nq, H, D)) != 0 ||
         (r = make_bnhd_u8_map(&mk, kc, B, Nkv, H, D)) != 0 ||
         (r = make_bnhd_map(&mv, vt, B, Nkv, H, D, true)) != 0)
@@ -339,9 +348,9 @@ nvq_status fwd_impl(const void* q, const void* k, const void* v, int B, int Nq, 
                        return launch_attn_fwd_fp4(s, mq, mk, mv, qs, ks, o, stats, err, stream);
                      }));
   }
-  void* qt = wb + w.q;
-  void* kt = wb + w.k;
-  void* vt = wb + w.v;
+  void* qt = wb + w.qb;
+  void* kt = wb + w.kb;
+  void* vt = wb + w.v16;
   if ((r = make_bnhd_map(&mq, qt, B, Nq, H, D, false)) != 0 ||
       (r = make_bnhd_map(&mk, kt, B, Nkv, H, D, false)) != 0 ||
       (r = make_bnhd_map(&mv, vt, B, Nkv, H, D, true)) != 0)
@@ -358,16 +367,26 @@ nvq_status fwd_impl(const void* q, const void* k, const void* v, int B, int Nq, 
                    }));
 }
 
-// Straight-through backward; kv_list as in fwd_impl.
-nvq_status bwd_impl(const void* q, const void* k, const void* v, const void* o,
-                    const float* stats, const void* dout, const int* kv_list, int topk, void* dq,
-                    void* dk, void* dv, int B, int Nq, int Nkv, int H, int D, float scale,
-                    int causal, void* ws, size_t ws_bytes, cudaStream_t stream) {
+nvq_status check_bwd_args(const void* q, const void* k, const void* v, const void* o,
+                          const float* stats, const void* dout, const void* dq, const void* dk,
+                          const void* dv, int B, int Nq, int Nkv, int H, int D, float scale,
+                          int causal) {
   nvq_status st = check_attn(B, Nq, Nkv, H, D, scale, causal);
   if (st != NVQ_OK) return st;
   const void* ptrs[] = {q, k, v, o, stats, dout, dq, dk, dv};
   for (const void* p : ptrs)
     if (p == nullptr || !aligned16(p)) return NVQ_ERR_INVALID;
+  return NVQ_OK;
+}
+
+// Straight-through backward; kv_list as in fwd_impl.
+nvq_status bwd_impl(const void* q, const void* k, const void* v, const void* o,
+                    const float* stats, const void* dout, const int* kv_list, int topk, void* dq,
+                    void* dk, void* dv, int B, int Nq, int Nkv, int H, int D, float scale,
+                    int causal, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  nvq_status st = check_bwd_args(q, k, v, o, stats, dout, dq, dk, dv, B, Nq, Nkv, H, D, scale,
+                                 causal);
+  if (st != NVQ_OK) return st;
   const BwdWs w = bwd_ws(B, Nq, Nkv, H, D, kv_list != nullptr ? topk : 0);
   if (ws == nullptr || ws_bytes < w.total || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
     return NVQ_ERR_WORKSPACE;
@@ -529,6 +548,22 @@ size_t attn_qat_fwd_workspace(int B, int Nq, int Nkv, int H, int D) {
 size_t attn_qat_bwd_workspace(int B, int Nq, int Nkv, int H, int D) {
   if (B < 1 || Nq < 1 || Nkv < 1 || H < 1 || D < 1) return 0;
   return bwd_ws(B, Nq, Nkv, H, D).total;
+}
+
+nvq_status attn_qat_fwd_layout(int B, int Nq, int Nkv, int H, int D, nvq_attn_layout* out) {
+  if (out == nullptr || B < 1 || Nq < 1 || Nkv < 1 || H < 1 || (D != 64 && D != 128))
+    return NVQ_ERR_INVALID;
+  const FwdWs w = fwd_ws(B, Nq, Nkv, H, D);
+  *out = nvq_attn_layout{w.qc, w.kc, w.qs, w.ks, w.v16, w.qb, w.kb, SIZE_MAX, SIZE_MAX, w.total};
+  return NVQ_OK;
+}
+
+nvq_status attn_qat_bwd_layout(int B, int Nq, int Nkv, int H, int D, nvq_attn_layout* out) {
+  if (out == nullptr || B < 1 || Nq < 1 || Nkv < 1 || H < 1 || (D != 64 && D != 128))
+    return NVQ_ERR_INVALID;
+  const BwdWs w = bwd_ws(B, Nq, Nkv, H, D);
+  *out = nvq_attn_layout{w.qc, w.kc, w.qs, w.ks, SIZE_MAX, w.q, w.k, w.v, w.delta, w.total};
+  return NVQ_OK;
 }
 
 nvq_status attn_qat_fwd(const void* q, const void* k, const void* v, int B, int Nq, int Nkv,

@@ -47,6 +47,17 @@ struct AttnShape {
 nvq_status fail_cuda(const char* where, cudaError_t e);
 nvq_status fail_driver(const char* where, int cu_result);
 
+// The current device and the context current on this thread; a thread with no
+// current context first gets the device's primary context made current.
+cudaError_t current_device_context(int* dev, CUcontext* ctx);
+
+// The host-side argument checks of attn_qat_bwd (sizes, scale, causal flag,
+// null and misaligned pointers), in the order that call applies them.
+nvq_status check_bwd_args(const void* q, const void* k, const void* v, const void* o,
+                          const float* stats, const void* dout, const void* dq, const void* dk,
+                          const void* dv, int B, int Nq, int Nkv, int H, int D, float scale,
+                          int causal);
+
 // While nvq_timing_enable(1) is in force, brackets the launches made during its
 // lifetime with CUDA events on `stream`, filed under `kind` (an NVQ_KERNEL_*
 // value); otherwise does nothing.

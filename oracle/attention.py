@@ -51,7 +51,7 @@ import math
 
 import torch
 
-from .nvfp4 import fq
+from .nvfp4 import fake_quant, fq
 
 F64 = torch.float64
 TILE = 128  # tokens per tile of the block-sparse variant (one 4x4x8 cube)
@@ -117,6 +117,17 @@ class HeadProblem:
         m, _, l, pt = _probs(s, self.quant)
         o = (pt @ self.vt) / l[:, None]
         return o, m + torch.log(l), m
+
+    def probs_rows(self, rows):
+        """(m, l, P, P~, scale bytes) of query rows ``rows``: the forward's row
+        maxima, unquantized row sums, probabilities P = exp(S - m), their
+        fake-quantized P~, and the E4M3 bytes of P~'s block scales, uint8
+        [R, ceil(Nkv / 16)] (None without quantization)."""
+        rows = torch.as_tensor(rows, dtype=torch.long)
+        s = _scores(self.qt[rows], self.kt, self.scale, rows, self.causal, self.tiles)
+        m, p, l, pt = _probs(s, self.quant)
+        sb = fake_quant(p, 1.0, torch.float64, axis=1)[1] if self.quant else None
+        return m, l, p, pt, sb
 
     def o_hp_rows(self, rows):
         """The auxiliary high-precision output P V~ / l (P unquantized) for ``rows``."""

@@ -59,14 +59,46 @@ def test_status_strings_and_version(lib):
 def test_workspace_sizes(lib):
     b, n, h, d = 1, 25088, 12, 128
     t = b * n * h * d * 2
-    assert lib.attn_qat_fwd_workspace(b, n, n, h, d) == 3 * t
     # Q~, K~, V~ (bf16), delta, then the E2M1 codes (D/2 bytes a row) and the
     # 512-byte scale blocks (one per 128 rows and 64 elements of D) of Q~ and K~
     codes = b * n * h * d // 2
     scales = b * h * ((n + 127) // 128) * (d // 64) * 512
+    # forward: codes and scale blocks of Q~, K~, V~ in f16, Q~ and K~ in bf16
+    assert lib.attn_qat_fwd_workspace(b, n, n, h, d) == 2 * codes + 2 * scales + 3 * t
     assert lib.attn_qat_bwd_workspace(b, n, n, h, d) == 3 * t + b * h * n * 4 + 2 * codes + 2 * scales
     assert lib.attn_qat_fwd_workspace(0, n, n, h, d) == 0
     assert lib.attn_qat_fwd_workspace(1, 3, 5, 1, 64) % 256 == 0
+
+
+def test_workspace_layouts(lib):
+    """The regions attn_qat_*_layout reports are 256-byte aligned, disjoint, of
+    the documented sizes, and inside the workspace the size query returns."""
+    from nvfp4_fake_quant_gb300 import api
+    for (b, nq, nkv, h, d) in [(1, 25088, 25088, 12, 128), (2, 300, 333, 3, 64), (1, 1, 1, 1, 128)]:
+        nt = lambda n: (n + 127) // 128
+        size = {"q_codes": b * nq * h * d // 2, "k_codes": b * nkv * h * d // 2,
+                "q_scales": b * h * nt(nq) * (d // 64) * 512,
+                "k_scales": b * h * nt(nkv) * (d // 64) * 512,
+                "v_f16": b * nkv * h * d * 2, "q_bf16": b * nq * h * d * 2,
+                "k_bf16": b * nkv * h * d * 2, "v_bf16": b * nkv * h * d * 2,
+                "delta": b * h * nq * 4}
+        for which, query in (("fwd", lib.attn_qat_fwd_workspace),
+                             ("bwd", lib.attn_qat_bwd_workspace)):
+            lay = api.attn_qat_layout(b, nq, nkv, h, d, which)
+            assert lay["total"] == query(b, nq, nkv, h, d)
+            spans = sorted((off, off + size[name]) for name, off in lay.items() if name != "total")
+            assert all(off % 256 == 0 for off, _ in spans)
+            assert all(e0 <= s1 for (_, e0), (s1, _) in zip(spans, spans[1:]))
+            assert spans[-1][1] <= lay["total"]
+        assert set(api.attn_qat_layout(b, nq, nkv, h, d, "fwd")) == \
+            {"q_codes", "k_codes", "q_scales", "k_scales", "v_f16", "q_bf16", "k_bf16", "total"}
+        assert set(api.attn_qat_layout(b, nq, nkv, h, d, "bwd")) == \
+            {"q_codes", "k_codes", "q_scales", "k_scales", "q_bf16", "k_bf16", "v_bf16", "delta",
+             "total"}
+    lay = _lib.AttnLayout()
+    assert lib.attn_qat_fwd_layout(1, 128, 128, 1, 96, ctypes.addressof(lay)) == INVALID
+    assert lib.attn_qat_bwd_layout(0, 128, 128, 1, 64, ctypes.addressof(lay)) == INVALID
+    assert lib.attn_qat_fwd_layout(1, 128, 128, 1, 64, None) == INVALID
 
 
 def _fwd(lib, q=A, k=A, v=A, B=1, Nq=128, Nkv=128, H=1, D=128, scale=0.125, causal=0, o=A,
