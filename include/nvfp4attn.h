@@ -334,12 +334,13 @@ nvq_status nvfp4_quantize_tiled(const void* x, int64_t rows, int64_t cols, int64
  * [N, K], bias bf16 [N] or NULL, out bf16 [M, N], all contiguous and 16-byte
  * aligned.  Both operands are quantized (nvfp4_quantize_tiled) under their
  * global scales; x_global_sf / w_global_sf are device fp32 scalars, or NULL for
- * 448*6/amax of the operand itself (nvfp4_global_sf).  The FP4 block-scaled GEMM
- * (cuBLASLt) runs with alpha = 1 / (gsf_w * gsf_x) and fp32 accumulation, so
- * out is the product of the dequantized operands, rounded to bf16.
- * K % 64 == 0 and N % 16 == 0, else NVQ_ERR_UNSUPPORTED (also when cuBLASLt
- * offers no algorithm for the shape).  ws: nvfp4_linear_workspace(M, N, K)
- * bytes, 256-byte aligned (codes, scales, global scales, GEMM workspace).
+ * 448*6/amax of the operand itself (nvfp4_global_sf).  The library's FP4
+ * block-scaled GEMM (tcgen05 kind::mxf4nvf4 MMAs, fp32 accumulation in TMEM)
+ * applies alpha = 1 / (gsf_w * gsf_x) and the bias in its epilogue, so out is
+ * the product of the dequantized operands plus bias, rounded to bf16.
+ * K % 64 == 0 and N % 16 == 0, else NVQ_ERR_UNSUPPORTED.  ws:
+ * nvfp4_linear_workspace(M, N, K) bytes, 256-byte aligned (codes, scales,
+ * global scales, alpha).
  */
 size_t nvfp4_linear_workspace(int64_t M, int64_t N, int64_t K);
 nvq_status nvfp4_linear_fwd(const void* x, const void* w, const void* bias, int64_t M, int64_t N,
@@ -350,8 +351,8 @@ nvq_status nvfp4_linear_fwd(const void* x, const void* w, const void* bias, int6
  * Straight-through backward of the NVFP4 linear: the full-precision linear
  * gradients grad_x = grad_out w (bf16 [M, K]), grad_w = grad_out^T x (bf16
  * [N, K]), grad_b = column sums of grad_out (bf16 [N]); each output may be NULL
- * (not computed).  BF16 GEMMs with fp32 accumulation (cuBLASLt); the bias sums
- * are fp32.  Sizes and alignment as in the forward; ws:
+ * (not computed).  The two GEMMs run as one launch of the library's BF16
+ * tcgen05 GEMM (fp32 accumulation); the bias sums are fp32.  Sizes and alignment as in the forward; ws:
  * nvfp4_linear_bwd_workspace(M, N, K) bytes, 256-byte aligned.
  */
 size_t nvfp4_linear_bwd_workspace(int64_t M, int64_t N, int64_t K);
@@ -372,7 +373,7 @@ enum {
   NVQ_KERNEL_BWD_DQ = 4,     /* backward, query-outer dQ kernel */
   NVQ_KERNEL_GLOBAL_SF = 5,  /* static global scale (amax reduction and finalize) */
   NVQ_KERNEL_VSA = 6,        /* block-sparse support: token reorder, block selection */
-  NVQ_KERNEL_LINEAR = 7,     /* NVFP4 linear: the cuBLASLt GEMMs and the bias gradient */
+  NVQ_KERNEL_LINEAR = 7,     /* NVFP4 linear: the FP4 and BF16 GEMMs and the bias gradient */
   NVQ_KERNEL_KINDS = 8
 };
 
@@ -411,7 +412,8 @@ nvq_status nvq_selftest_umma(const void* a, const void* b, float* c, int N, int 
 /*
  * One 128 x N x K block-scaled FP4 MMA (tcgen05 kind::mxf4nvf4, K = 64 * nmma):
  * a: E2M1 codes [128, K/2] bytes, b: [N, K/2] bytes, two codes a byte (the even
- * element in the low nibble), loaded by TMA with the (K/2)-byte swizzle.  Each
+ * element in the low nibble), loaded by TMA with the (K/2)-byte swizzle (32, 64
+ * or 128 bytes).  Each
  * row has one E4M3 scale per 16 elements.  The scales reach tensor memory in one
  * of two ways: mode 0 stores sf_img (u32 [2][128][32], A then B: 32 columns per
  * lane) into TMEM columns [256, 320) by tcgen05.st; mode 1 copies sf_src (bytes
@@ -419,7 +421,7 @@ nvq_status nvq_selftest_umma(const void* a, const void* b, float* c, int N, int 
  * to columns 256 + 4 kk (A) and 288 + 4 kk (B) by tcgen05.cp, replicated to the
  * four lane quadrants.  MMA kk reads its scales at columns 256 + kk * sf_stride
  * and 288 + kk * sf_stride.  c: f32 [128, N]; dump: u32 [128][64], TMEM columns
- * [256, 320) after the MMAs.  N in {64, 128}, nmma in {1, 2}, sf_stride 0..4.
+ * [256, 320) after the MMAs.  N in {64, 128}, nmma in {1, 2, 4}, sf_stride 0..4.
  */
 nvq_status nvq_selftest_fp4(const void* a, const void* b, const uint32_t* sf_img,
                             const uint8_t* sf_src, float* c, uint32_t* dump, int N, int nmma,

@@ -75,10 +75,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
             list(ex.map(run, jobs))
     if jobs or not os.path.exists(LIB) or \
             any(os.path.getmtime(o) > os.path.getmtime(LIB) for o in objs):
-        # cuBLASLt (the NVFP4 linear's GEMMs) from the toolkit that builds the library
-        cuda_lib = os.path.join(os.path.dirname(os.path.dirname(os.path.realpath(cc))), "lib64")
-        run([cc, *ARCH, "-shared", "-o", LIB + ".tmp", *objs, "-cudart", "static",
-             "-L", cuda_lib, "-lcublasLt", "-Xlinker", "-rpath," + cuda_lib])
+        run([cc, *ARCH, "-shared", "-o", LIB + ".tmp", *objs, "-cudart", "static"])
         os.replace(LIB + ".tmp", LIB)
     return LIB
 

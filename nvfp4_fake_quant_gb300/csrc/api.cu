@@ -182,6 +182,24 @@ int make_bnhd_u8_map(CUtensorMap* map, const void* base, int B, int N, int H, in
   return static_cast<int>(r);
 }
 
+int* device_error_word() { return error_word(); }
+
+int make_codes_map(CUtensorMap* map, const void* base, int64_t rows, int64_t row_bytes) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return CUDA_ERROR_NOT_FOUND;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(rows),
+                              1, 1};
+  const cuuint64_t rs = static_cast<cuuint64_t>(row_bytes);
+  const cuuint64_t strides[3] = {rs, rs * rows, rs * rows};
+  const cuuint32_t box[4] = {128, 128, 1, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return static_cast<int>(r);
+}
+
 int make_2d_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return CUDA_ERROR_NOT_FOUND;
@@ -201,7 +219,7 @@ int make_u8_map(CUtensorMap* map, const void* base, int64_t rows, int row_bytes,
                 int box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return CUDA_ERROR_NOT_FOUND;
-  if (row_bytes != 32 && row_bytes != 64) return CUDA_ERROR_INVALID_VALUE;
+  if (row_bytes != 32 && row_bytes != 64 && row_bytes != 128) return CUDA_ERROR_INVALID_VALUE;
   const cuuint64_t dims[4] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(rows),
                               1, 1};
   const cuuint64_t rs = static_cast<cuuint64_t>(ld);
@@ -211,7 +229,9 @@ int make_u8_map(CUtensorMap* map, const void* base, int64_t rows, int row_bytes,
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        row_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B,
+                        row_bytes == 128  ? CU_TENSOR_MAP_SWIZZLE_128B
+                        : row_bytes == 64 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                          : CU_TENSOR_MAP_SWIZZLE_32B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return static_cast<int>(r);
 }
@@ -682,7 +702,8 @@ nvq_status nvq_selftest_fp4(const void* a, const void* b, const uint32_t* sf_img
   if (!a || !b || !c || !dump || !aligned16(a) || !aligned16(b) || !aligned16(c) ||
       !aligned16(dump))
     return NVQ_ERR_INVALID;
-  if ((N != 64 && N != 128) || (nmma != 1 && nmma != 2) || sf_stride < 0 || sf_stride > 4 ||
+  if ((N != 64 && N != 128) || (nmma != 1 && nmma != 2 && nmma != 4) || sf_stride < 0 ||
+      sf_stride > 4 ||
       (mode != 0 && mode != 1) || (mode == 0 && !sf_img) || (mode == 1 && !sf_src))
     return NVQ_ERR_INVALID;
   int* err = error_word();

@@ -144,10 +144,35 @@ cudaError_t launch_selftest_fp4(const CUtensorMap& ta, const CUtensorMap& tb, co
                                 const uint8_t* sf_src, float* c, uint32_t* dump, int N, int nmma,
                                 int sf_stride, int mode, int* err, cudaStream_t stream);
 
+// Address of the current device's error word (see nvq_device_status), or
+// nullptr with the failure recorded.
+int* device_error_word();
+// Maps packed E2M1 codes [rows, row_bytes] (contiguous) with a box of 128 bytes
+// x 128 rows and the 128-byte swizzle.
+int make_codes_map(CUtensorMap* map, const void* base, int64_t rows, int64_t row_bytes);
+
+// The NVFP4 linear's GEMMs (gemm.cu).
+// out [M, N] bf16 = alpha * (x codes . x scales)(w codes . w scales)^T + bias:
+// tx, tw from make_codes_map over [M, K/2] and [N, K/2]; sx, sw the tiled scales;
+// alpha a device scalar; bias bf16 [N] or nullptr.  K % 64 == 0, N % 8 == 0.
+cudaError_t launch_gemm_fp4(const CUtensorMap& tx, const CUtensorMap& tw, const uint8_t* sx,
+                            const uint8_t* sw, const float* alpha, const void* bias, int64_t M,
+                            int64_t N, int64_t K, void* out, int* err, cudaStream_t stream);
+// Two BF16 problems D_i [M_i, N_i] = A_i B_i^T (contraction K_i) in one
+// persistent launch, problem 0's tiles first.  An operand that is K-major
+// (a_mn / b_mn == 0) is mapped as [rows, K] with a box of {64, 128} (A) or
+// {64, 256} (B); an MN-major one as [K, rows] with a box of {64, 64}
+// (make_2d_map).  out_i == nullptr skips problem i.  N_i % 8 == 0.
+cudaError_t launch_gemm_bf16_pair(const CUtensorMap& ta0, const CUtensorMap& tb0, int a_mn0,
+                                  int b_mn0, int64_t M0, int64_t N0, int64_t K0, void* out0,
+                                  const CUtensorMap& ta1, const CUtensorMap& tb1, int a_mn1,
+                                  int b_mn1, int64_t M1, int64_t N1, int64_t K1, void* out1,
+                                  int* err, cudaStream_t stream);
+
 // Maps a [rows, cols] 16-bit row-major matrix with a box of {64, box_rows}.
 int make_2d_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_rows);
 // Maps a [rows, row_bytes] byte matrix (row stride ld bytes) with a box of
-// {row_bytes, box_rows} and the row_bytes-wide swizzle (row_bytes in {32, 64}).
+// {row_bytes, box_rows} and the row_bytes-wide swizzle (row_bytes in {32, 64, 128}).
 int make_u8_map(CUtensorMap* map, const void* base, int64_t rows, int row_bytes, int64_t ld,
                 int box_rows);
 

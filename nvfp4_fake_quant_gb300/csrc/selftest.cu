@@ -122,8 +122,9 @@ __global__ void __launch_bounds__(128, 1)
   }
 }
 
-// FP4 probe.  A: E2M1 codes [128, kb] bytes (kb = 32 * nmma, K = 64 * nmma),
-// B: [N, kb]; both K-major, loaded by TMA with the kb-byte swizzle.  TMEM:
+// FP4 probe.  A: E2M1 codes [128, kb] bytes (kb = 32 * nmma, K = 64 * nmma,
+// nmma in {1, 2, 4}), B: [N, kb]; both K-major, loaded by TMA with the kb-byte
+// swizzle.  TMEM:
 // D at columns [0, N), A scales at [256, 288), B scales at [288, 320).
 //   mode 0: sf_img (u32 [2][128][32]: A then B, lane-major) is stored into those
 //           columns by tcgen05.st;
@@ -133,7 +134,7 @@ __global__ void __launch_bounds__(128, 1)
 // UMMA kk reads its scales at column 256 + kk * sf_stride (A), 288 + kk *
 // sf_stride (B).  Outputs: c [128, N] f32 and dump (u32 [128][64]): TMEM columns
 // [256, 320) after the UMMAs.
-constexpr uint32_t kFp4Smem = 1024 + 8192 + 8192 + 2048 + 4096 + 256;
+constexpr uint32_t kFp4Smem = 1024 + 16384 + 16384 + 4096 + 4096 + 256;
 
 __global__ void __launch_bounds__(128, 1)
     selftest_fp4_kernel(const __grid_constant__ CUtensorMap ta,
@@ -145,9 +146,9 @@ __global__ void __launch_bounds__(128, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023u) &
                                              ~static_cast<uintptr_t>(1023u));
   uint8_t* sa = smem;
-  uint8_t* sb = smem + 8192;
-  uint8_t* sfs = smem + 16384;  // cp source, followed by 4 KB of slack
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 16384 + 2048 + 4096);
+  uint8_t* sb = smem + 16384;
+  uint8_t* sfs = smem + 32768;  // cp source (4 KB), followed by 4 KB of slack
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 32768 + 4096 + 4096);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 3);
   volatile int* abort = reinterpret_cast<volatile int*>(bars + 4);
   const int warp = threadIdx.x >> 5;
@@ -182,7 +183,7 @@ __global__ void __launch_bounds__(128, 1)
     tmem_wait_st();
   } else {
     for (int i = threadIdx.x; i < 2 * nmma * 512; i += 128) sfs[i] = sf_src[i];
-    for (int i = threadIdx.x; i < 4096; i += 128) sfs[2048 + i] = 0;
+    for (int i = threadIdx.x; i < 4096; i += 128) sfs[4096 + i] = 0;
     fence_proxy_async_smem();
   }
   tc_fence_before();
@@ -194,7 +195,8 @@ __global__ void __launch_bounds__(128, 1)
     tma_load_4d_w(sb, &tb, 0, 0, 0, 0, &bars[0]);
     if (mbar_wait_warp(&bars[0], 0, abort)) {
       tc_fence_after();
-      const uint32_t layout = kb == 64 ? 4u : 6u;  // 64- or 32-byte swizzle
+      // 128-, 64- or 32-byte swizzle
+      const uint32_t layout = kb == 128 ? 2u : kb == 64 ? 4u : 6u;
       const uint32_t idesc = idesc_mxf4nvf4(128, N);
       if (mode == 1) {
         for (int kk = 0; kk < nmma; ++kk) {

@@ -39,8 +39,12 @@ def test_tiled_quantizer_is_bit_exact(rows, cols, static):
     assert torch.equal(scales.cpu(), ref_scales)  # includes the zero padding
 
 
+# (2048, 1536, 512): 192 output tiles of 128 x 128, more than one per CTA, so both
+# TMEM accumulators and the persistent loop are used; K = 320 and 192 end on a
+# partial stage of the 256-element pipeline; N = 96 is a partial tile.
 @pytest.mark.parametrize("m,n,k,bias", [(256, 256, 320, True), (200, 512, 128, False),
-                                        (64, 96, 1536, True), (1000, 128, 64, True)])
+                                        (64, 96, 1536, True), (1000, 128, 64, True),
+                                        (2048, 1536, 512, True), (300, 640, 192, False)])
 def test_forward_parity(m, n, k, bias):
     inp = workloads.linear_inputs(m, n, k, seed=60 + m)
     b = inp.bias if bias else None
@@ -64,7 +68,9 @@ def test_forward_with_given_global_scales():
     assert rel_l2(out, ref) <= FWD_RTOL
 
 
-@pytest.mark.parametrize("m,n,k", [(256, 256, 320), (200, 512, 128)])
+# (2048, 1024, 2560): 240 output tiles of 128 x 256 over both gradients in one
+# launch, more than one per CTA; (256, 256, 320): K = 320 is a partial 256-wide tile
+@pytest.mark.parametrize("m,n,k", [(256, 256, 320), (200, 512, 128), (2048, 1024, 2560)])
 def test_backward_parity(m, n, k):
     inp = workloads.linear_inputs(m, n, k, seed=80 + m)
     gx, gw, gb = api.nvfp4_linear_bwd(inp.grad.cuda(), inp.x.cuda(), inp.w.cuda())

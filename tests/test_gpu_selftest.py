@@ -107,7 +107,7 @@ def _run_fp4(a, b, img, src, n, nmma, stride, mode):
 
 
 @pytest.mark.parametrize("n,nmma,mode", [(128, 2, 0), (128, 2, 1), (64, 1, 0), (64, 2, 1),
-                                         (128, 1, 1)])
+                                         (128, 1, 1), (128, 4, 0), (128, 4, 1), (64, 4, 1)])
 def test_fp4_block_scaled_umma(n, nmma, mode):
     k = 64 * nmma
     a, b, sa, sb = _fp4_operands(7 + n + nmma + mode, 128, n, k)
