@@ -184,14 +184,15 @@ int make_bnhd_u8_map(CUtensorMap* map, const void* base, int B, int N, int H, in
 
 int* device_error_word() { return error_word(); }
 
-int make_codes_map(CUtensorMap* map, const void* base, int64_t rows, int64_t row_bytes) {
+int make_codes_map(CUtensorMap* map, const void* base, int64_t rows, int64_t row_bytes,
+                   int box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (fn == nullptr) return CUDA_ERROR_NOT_FOUND;
   const cuuint64_t dims[4] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(rows),
                               1, 1};
   const cuuint64_t rs = static_cast<cuuint64_t>(row_bytes);
   const cuuint64_t strides[3] = {rs, rs * rows, rs * rows};
-  const cuuint32_t box[4] = {128, 128, 1, 1};
+  const cuuint32_t box[4] = {128, static_cast<cuuint32_t>(box_rows), 1, 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims,
                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,

@@ -433,6 +433,265 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ---------------------------------------------------- FP4, x resident, W multicast
+// The same product for K <= kXresMaxK, with far less operand traffic: a cluster
+// of kRc CTAs takes kRc consecutive 128-row tiles of x (one each) and sweeps a
+// chunk of W's 128-row tiles together.  Each CTA keeps its x codes in shared
+// memory and its x scales in TMEM for the whole chunk; each W stage (256
+// K-elements of 128 rows) is loaded once for the cluster, every CTA fetching a
+// 32-row slice and one 512-byte scale block and multicasting them to all four.
+// A stage is refilled only when all four CTAs have released it (their MMA
+// commits arrive on every CTA's "empty" barrier).  x is reloaded box by box
+// (256 K-elements): the chunk's last tile releases box b when its stage b is
+// done, so the next chunk's x arrives under the current tile's MMAs.  Output
+// tiles leave through shared memory by TMA stores (full 128-byte lines).
+#ifndef NVQ_XRES_CLUSTER
+#define NVQ_XRES_CLUSTER 4
+#endif
+constexpr int kRc = NVQ_XRES_CLUSTER;       // CTAs per cluster (1, 2 or 4)
+constexpr int kXresMaxK = 1536;             // x codes (6 boxes of 16 KB) resident
+constexpr int kXresBoxes = kXresMaxK / 256;
+constexpr int kXresStages = 4;
+constexpr uint32_t kXresStage = 16384 + 2048;              // W codes + 4 scale blocks
+constexpr uint32_t kXresA = 0;                             // x codes, box b at b * 16 KB
+constexpr uint32_t kXresAS = kXresBoxes * 16384;           // x scales, step j at j * 512
+constexpr uint32_t kXresB = kXresAS + kXresBoxes * 2048;   // W stages
+constexpr uint32_t kXresO = kXresB + kXresStages * kXresStage;  // output staging
+constexpr uint32_t kXresBars = kXresO + kEpiWarps * 2 * 4096;
+constexpr uint32_t kXresNumBars = 2 * kXresStages + 2 * kXresBoxes + 4 + 1;
+constexpr uint32_t kXresSlot = kXresBars + kXresNumBars * 8;
+constexpr uint32_t kXresAbort = kXresSlot + 4;
+constexpr uint32_t kXresSmem = kXresAbort + 4 + 1024;
+// TMEM: accumulators [0, 256), x scales of step j at 256 + 4 j, W scales of
+// stage s, step j at kXresBCol + 4 (4 s + j).
+constexpr uint32_t kXresBCol = 256 + 4 * 4 * kXresBoxes;
+static_assert(kXresBCol + 4 * 4 * kXresStages <= 512, "TMEM columns");
+
+struct XresProblem {
+  int M, N, m_tiles, n_tiles, k_steps;
+  int n_chunks, chunk_tiles, units;   // unit = (group of kRc x tiles, chunk of W tiles)
+  const uint8_t* sx;
+  const uint8_t* sw;
+  const float* alpha;
+  const __nv_bfloat16* bias;
+  __nv_bfloat16* out;   // [M, N]: written through tout
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_fp4_xres_kernel(const __grid_constant__ CUtensorMap tx,
+                         const __grid_constant__ CUtensorMap tw32,
+                         const __grid_constant__ CUtensorMap tout, const XresProblem p,
+                         int* __restrict__ err) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023u) &
+                                             ~static_cast<uintptr_t>(1023u));
+  const int warp = threadIdx.x >> 5;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kXresBars);
+  uint64_t* full = bars;                          // [kXresStages] W stage landed (all slices)
+  uint64_t* empty = full + kXresStages;           // [kXresStages] released by all kRc CTAs
+  uint64_t* a_full = empty + kXresStages;         // [kXresBoxes] x box landed
+  uint64_t* a_empty = a_full + kXresBoxes;        // [kXresBoxes] x box no longer read
+  uint64_t* acc_full = a_empty + kXresBoxes;      // [2]
+  uint64_t* acc_empty = acc_full + 2;             // [2]
+  uint64_t* drain = acc_full + 4;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kXresSlot);
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + kXresAbort);
+  const int rank = static_cast<int>(cluster_ctarank());
+  const int cid = static_cast<int>(cluster_id_x()), ncl = static_cast<int>(cluster_count_x());
+  const int k_stages = (p.k_steps + 3) / 4;
+  constexpr uint16_t kAll = (1u << kRc) - 1u;
+
+  if (threadIdx.x == 0) {
+    *abort = 0;
+    for (int s = 0; s < kXresStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kRc);
+    }
+    for (int b = 0; b < kXresBoxes; ++b) {
+      mbar_init(&a_full[b], 1);
+      mbar_init(&a_empty[b], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&acc_full[a], 1);
+      mbar_init(&acc_empty[a], kEpiWarps);
+    }
+    mbar_init(drain, 1);
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  cluster_sync_all();  // every CTA's barriers exist before any multicast arrives
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == kTmaWarp) {
+    // ------------------------------------------------------------ producer
+    tma_prefetch_desc(&tx);
+    tma_prefetch_desc(&tw32);
+    uint32_t it = 0, ucount = 0;
+    int issued[kXresStages];
+    for (int s = 0; s < kXresStages; ++s) issued[s] = -1;
+    bool ok = true;
+    for (int u = cid; u < p.units && ok; u += ncl, ++ucount) {
+      const int mt = (u / p.n_chunks) * kRc + rank;
+      const int nt0 = (u % p.n_chunks) * p.chunk_tiles;
+      const int nt1 = min(nt0 + p.chunk_tiles, p.n_tiles);
+      const bool x_ok = mt < p.m_tiles;  // past the last x tile: zero codes, no scales
+      for (int nt = nt0; nt < nt1 && ok; ++nt) {
+        for (int st = 0; st < k_stages; ++st, ++it) {
+          const int ns = min(4, p.k_steps - 4 * st);
+          if (nt == nt0) {  // this chunk's x box st, once the previous chunk is done with it
+            if (!(ok = mbar_wait_warp(&a_empty[st], par(ucount) ^ 1u, abort))) break;
+            mbar_arrive_expect_tx_w(&a_full[st], 16384u + (x_ok ? ns * 512u : 0u));
+            tma_load_4d_w(smem + kXresA + st * 16384, &tx, st * 128, mt * 128, 0, 0, &a_full[st]);
+            if (x_ok)
+              bulk_load_w(smem + kXresAS + st * 2048,
+                          p.sx + (static_cast<int64_t>(mt) * p.k_steps + 4 * st) * 512, ns * 512,
+                          &a_full[st]);
+          }
+          const int s = static_cast<int>(it % kXresStages);
+          if (!(ok = mbar_wait_warp(&empty[s], par(it / kXresStages) ^ 1u, abort))) break;
+          uint8_t* stage = smem + kXresB + s * kXresStage;
+          mbar_arrive_expect_tx_w(&full[s], 16384u + ns * 512u);
+          for (int q = rank; q < 4; q += kRc)  // 32-row slices q of the W tile
+            tma_load_4d_mc_w(stage + q * 4096, &tw32, st * 128, nt * 128 + q * 32, 0, 0, &full[s],
+                             kAll);
+          for (int j = rank; j < ns; j += kRc)  // scale blocks of K-steps j
+            bulk_load_mc_w(stage + 16384 + j * 512,
+                           p.sw + (static_cast<int64_t>(nt) * p.k_steps + 4 * st + j) * 512, 512,
+                           &full[s], kAll);
+          issued[s] = static_cast<int>(par(it / kXresStages));
+        }
+      }
+    }
+    if (!ok) {  // let the copies already issued land before the block leaves
+      for (int s = 0; s < kXresStages; ++s)
+        if (issued[s] >= 0)
+          mbar_wait_warp(&full[s], static_cast<uint32_t>(issued[s]), nullptr, 10000000ull);
+    }
+  } else if (warp == kMmaWarp) {
+    // ----------------------------------------------------------------- MMA
+    constexpr uint32_t idesc = idesc_mxf4nvf4(128, 128);
+    uint32_t it = 0, tcount = 0, ucount = 0;
+    bool ok = true;
+    const uint32_t a_addr = smem_u32(smem + kXresA), as_addr = smem_u32(smem + kXresAS);
+    for (int u = cid; u < p.units && ok; u += ncl, ++ucount) {
+      const int nt0 = (u % p.n_chunks) * p.chunk_tiles;
+      const int nt1 = min(nt0 + p.chunk_tiles, p.n_tiles);
+      for (int nt = nt0; nt < nt1 && ok; ++nt, ++tcount) {
+        const uint32_t acc = tcount & 1u;
+        if (!(ok = mbar_wait_warp(&acc_empty[acc], par(tcount >> 1) ^ 1u, abort))) break;
+        tc_fence_after();
+        const uint32_t d = tmem + acc * 128;
+        for (int st = 0; st < k_stages; ++st, ++it) {
+          const int ns = min(4, p.k_steps - 4 * st);
+          if (nt == nt0) {  // x box st of this chunk: its scales go to TMEM
+            if (!(ok = mbar_wait_warp(&a_full[st], par(ucount), abort))) break;
+            tc_fence_after();
+            for (int j = 0; j < ns; ++j)
+              tmem_cp_32x128_x4_w(tmem + 256 + 4 * (4 * st + j), as_addr + st * 2048 + j * 512);
+          }
+          const int s = static_cast<int>(it % kXresStages);
+          if (!(ok = mbar_wait_warp(&full[s], par(it / kXresStages), abort))) break;
+          tc_fence_after();
+          const uint32_t b = smem_u32(smem + kXresB + s * kXresStage);
+          for (int j = 0; j < ns; ++j) {
+            const uint32_t bcol = tmem + kXresBCol + 4 * (4 * s + j);
+            tmem_cp_32x128_x4_w(bcol, b + 16384 + j * 512);
+            umma_fp4_ss_w(d, sdesc_sw128(a_addr + st * 16384 + 32 * j, 16, 1024),
+                          sdesc_sw128(b + 32 * j, 16, 1024), idesc, tmem + 256 + 4 * (4 * st + j),
+                          bcol, (st > 0 || j > 0) ? 1u : 0u);
+          }
+          umma_commit_mc_w(&empty[s], kAll);  // this CTA is done with stage s
+          if (nt == nt1 - 1) umma_commit_w(&a_empty[st]);  // and, last tile, with x box st
+        }
+        if (ok) umma_commit_w(&acc_full[acc]);
+      }
+    }
+    umma_commit_w(drain);
+    mbar_wait_warp(drain, 0, nullptr, 10000000ull);
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const uint32_t wq = static_cast<uint32_t>(warp & 3);
+    const uint32_t lane = threadIdx.x & 31;
+    const uint32_t lane_base = (wq * 32) << 16;
+    uint8_t* stage_out = smem + kXresO + (warp - 2) * 8192;
+    const float alpha = *p.alpha;
+    uint32_t tcount = 0, sc = 0;
+    bool ok = true;
+    for (int u = cid; u < p.units && ok; u += ncl) {
+      const int mt = (u / p.n_chunks) * kRc + rank;
+      const int nt0 = (u % p.n_chunks) * p.chunk_tiles;
+      const int nt1 = min(nt0 + p.chunk_tiles, p.n_tiles);
+      for (int nt = nt0; nt < nt1 && ok; ++nt, ++tcount) {
+        const uint32_t acc = tcount & 1u;
+        if (!(ok = mbar_wait_warp(&acc_full[acc], par(tcount >> 1), abort))) break;
+        tc_fence_after();
+#pragma unroll 1
+        for (int h = 0; h < 2; ++h, ++sc) {
+          uint32_t v[64];
+          tmem_ld32(tmem + lane_base + acc * 128 + h * 64, *reinterpret_cast<uint32_t(*)[32]>(v));
+          tmem_ld32(tmem + lane_base + acc * 128 + h * 64 + 32,
+                    *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+          tmem_wait_ld();
+          if (h == 1) {
+            tc_fence_before();
+            mbar_arrive_warp(&acc_empty[acc]);  // the MMA may reuse the accumulator
+          }
+          const int c0 = nt * 128 + h * 64;
+          uint32_t w[32];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            float bv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            if (p.bias != nullptr && c0 + 8 * q < p.N) {
+              const uint4 braw = __ldg(reinterpret_cast<const uint4*>(p.bias + c0 + 8 * q));
+              const uint32_t bw[4] = {braw.x, braw.y, braw.z, braw.w};
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                bv[2 * i] = __uint_as_float(bw[i] << 16);
+                bv[2 * i + 1] = __uint_as_float(bw[i] & 0xFFFF0000u);
+              }
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              w[4 * q + i] = pack2_bf16(fmaf(alpha, __uint_as_float(v[8 * q + 2 * i]), bv[2 * i]),
+                                        fmaf(alpha, __uint_as_float(v[8 * q + 2 * i + 1]), bv[2 * i + 1]));
+          }
+          uint8_t* buf = stage_out + (sc & 1u) * 4096;
+          if (lane == 0) bulk_wait_group_read<1>();  // the store from this buffer has read it
+          __syncwarp();
+          // row `lane`, 16-byte chunk q at chunk position q ^ (lane % 8): the
+          // 128-byte swizzle the output tensor map uses (conflict-free writes)
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            *reinterpret_cast<uint4*>(buf + lane * 128 + ((q ^ (lane & 7)) << 4)) =
+                make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_4d(&tout, buf, c0, mt * 128 + static_cast<int>(wq) * 32, 0, 0);
+            bulk_commit_group();
+          }
+        }
+      }
+    }
+    if (lane == 0) bulk_wait_group<0>();  // every store has completed
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();  // no CTA leaves while a peer may still write into it
+  report_abort(abort, err);
+  if (warp == kMmaWarp) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
 int sm_count() {
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -471,6 +730,63 @@ cudaError_t launch_gemm_bf16_pair(const CUtensorMap& ta0, const CUtensorMap& tb0
   if (e != cudaSuccess) return e;
   const int grid = total < sm_count() ? total : sm_count();
   gemm_bf16_kernel<<<grid, kThreads, kBf16Smem, stream>>>(ta0, tb0, ta1, tb1, p0, p1, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gemm_fp4_xres(const CUtensorMap& tx, const CUtensorMap& tw32,
+                                 const CUtensorMap& tout, const uint8_t* sx, const uint8_t* sw,
+                                 const float* alpha, const void* bias, int64_t M, int64_t N,
+                                 int64_t K, void* out, int* err, cudaStream_t stream) {
+  XresProblem p{};
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.M = static_cast<int>(M);
+  p.N = static_cast<int>(N);
+  p.m_tiles = static_cast<int>((M + 127) / 128);
+  p.n_tiles = static_cast<int>((N + 127) / 128);
+  p.k_steps = static_cast<int>(K / 64);
+  p.sx = sx;
+  p.sw = sw;
+  p.alpha = alpha;
+  p.bias = static_cast<const __nv_bfloat16*>(bias);
+  cudaError_t e = cudaFuncSetAttribute(gemm_fp4_xres_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kXresSmem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kRc;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kXresSmem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(sm_count() / kRc * kRc));
+  int clusters = 0;
+  e = cudaOccupancyMaxActiveClusters(&clusters, gemm_fp4_xres_kernel, &cfg);
+  if (e != cudaSuccess) return e;
+  if (clusters < 1) return cudaErrorInvalidConfiguration;
+  // chunks of W tiles per x group: the fewest rounds of (tiles + one x load)
+  const int groups = (p.m_tiles + kRc - 1) / kRc;
+  int best_nc = 1;
+  int64_t best = -1;
+  for (int nc = 1; nc <= p.n_tiles; ++nc) {
+    const int chunk = (p.n_tiles + nc - 1) / nc;
+    const int64_t rounds = (static_cast<int64_t>(groups) * nc + clusters - 1) / clusters;
+    const int64_t cost = rounds * (chunk + 1);
+    if (best < 0 || cost < best) {
+      best = cost;
+      best_nc = nc;
+    }
+  }
+  p.chunk_tiles = (p.n_tiles + best_nc - 1) / best_nc;
+  p.n_chunks = (p.n_tiles + p.chunk_tiles - 1) / p.chunk_tiles;
+  p.units = groups * p.n_chunks;
+  const int used = p.units < clusters ? p.units : clusters;
+  cfg.gridDim = dim3(static_cast<unsigned>(used * kRc));
+  e = cudaLaunchKernelEx(&cfg, gemm_fp4_xres_kernel, tx, tw32, tout, p, err);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -165,8 +165,20 @@ nvq_status nvfp4_linear_fwd(const void* x, const void* w, const void* bias, int6
   if (err == nullptr) return NVQ_ERR_CUDA;
   CUtensorMap tx, tw;
   int r;
-  if ((r = nvq::make_codes_map(&tx, wb + L.cx, M, K / 2)) != 0 ||
-      (r = nvq::make_codes_map(&tw, wb + L.cw, N, K / 2)) != 0)
+  if ((r = nvq::make_codes_map(&tx, wb + L.cx, M, K / 2)) != 0)
+    return nvq::fail_driver("cuTensorMapEncodeTiled", r);
+  if (K <= nvq::kGemmFp4XresMaxK) {
+    // x resident per CTA, W shared across a cluster by multicast, TMA stores
+    CUtensorMap tout;
+    if ((r = nvq::make_codes_map(&tw, wb + L.cw, N, K / 2, 32)) != 0 ||
+        (r = nvq::make_2d_map(&tout, out, M, N, 32)) != 0)
+      return nvq::fail_driver("cuTensorMapEncodeTiled", r);
+    return cuda_st("fp4 gemm", nvq::timed(NVQ_KERNEL_LINEAR, stream, [&] {
+                     return nvq::launch_gemm_fp4_xres(tx, tw, tout, wb + L.sx, wb + L.sw, ab, bias,
+                                                      M, N, K, out, err, stream);
+                   }));
+  }
+  if ((r = nvq::make_codes_map(&tw, wb + L.cw, N, K / 2)) != 0)
     return nvq::fail_driver("cuTensorMapEncodeTiled", r);
   return cuda_st("fp4 gemm", nvq::timed(NVQ_KERNEL_LINEAR, stream, [&] {
                    return nvq::launch_gemm_fp4(tx, tw, wb + L.sx, wb + L.sw, ab, bias, M, N, K, out,

@@ -148,8 +148,9 @@ cudaError_t launch_selftest_fp4(const CUtensorMap& ta, const CUtensorMap& tb, co
 // nullptr with the failure recorded.
 int* device_error_word();
 // Maps packed E2M1 codes [rows, row_bytes] (contiguous) with a box of 128 bytes
-// x 128 rows and the 128-byte swizzle.
-int make_codes_map(CUtensorMap* map, const void* base, int64_t rows, int64_t row_bytes);
+// x box_rows rows and the 128-byte swizzle.
+int make_codes_map(CUtensorMap* map, const void* base, int64_t rows, int64_t row_bytes,
+                   int box_rows = 128);
 
 // The NVFP4 linear's GEMMs (gemm.cu).
 // out [M, N] bf16 = alpha * (x codes . x scales)(w codes . w scales)^T + bias:
@@ -158,6 +159,15 @@ int make_codes_map(CUtensorMap* map, const void* base, int64_t rows, int64_t row
 cudaError_t launch_gemm_fp4(const CUtensorMap& tx, const CUtensorMap& tw, const uint8_t* sx,
                             const uint8_t* sw, const float* alpha, const void* bias, int64_t M,
                             int64_t N, int64_t K, void* out, int* err, cudaStream_t stream);
+// The same product for K <= 1536 (gemm_fp4_xres_kernel): clusters of four CTAs
+// keep their x tiles resident and share W tiles by multicast.  tx: x codes
+// (box 128 rows); tw32: w codes with a box of 32 rows; tout: out [M, N] bf16
+// (make_2d_map with 32-row boxes), written by TMA stores.
+cudaError_t launch_gemm_fp4_xres(const CUtensorMap& tx, const CUtensorMap& tw32,
+                                 const CUtensorMap& tout, const uint8_t* sx, const uint8_t* sw,
+                                 const float* alpha, const void* bias, int64_t M, int64_t N,
+                                 int64_t K, void* out, int* err, cudaStream_t stream);
+constexpr int64_t kGemmFp4XresMaxK = 1536;
 // Two BF16 problems D_i [M_i, N_i] = A_i B_i^T (contraction K_i) in one
 // persistent launch, problem 0's tiles first.  An operand that is K-major
 // (a_mn / b_mn == 0) is mapped as [rows, K] with a box of {64, 128} (A) or
