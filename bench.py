@@ -1,8 +1,9 @@
 """Benchmark of the NVFP4 Attn-QAT hot path on GB300.
 
 One step = one Attn-QAT forward + straight-through backward (all kernels of the
-path: Q/K/V quantization, two-pass forward, delta pre-pass, key-outer dK/dV
-kernel, query-outer dQ kernel) on the Wan2.1-T2V-1.3B self-attention shape
+path: the Q/K/V quantization pass, two-pass forward, delta pre-pass, key-outer
+dK/dV kernel, query-outer dQ kernel; the backward reads the quantized operands
+the forward saved, as api.AttnQAT does) on the Wan2.1-T2V-1.3B self-attention shape
 B=1, H=12, N=25088, D=128 (16x28x56 latent tokens), seeded synthetic bf16
 inputs resident in HBM.  Counted FLOPs: forward 4*B*H*N^2*D, backward 2.5x that.
 
@@ -55,7 +56,8 @@ def kernel_work(kind, b, n, h, d):
         "attn_fwd": (3 * gemm, "flop", "tensor"),   # S (pass 1), S (pass 2) on FP4 UMMAs, P~ V~
         "bwd_dkdv": (4 * gemm, "flop", "tensor"),   # S, dP, dV, dK
         "bwd_dq": (3 * gemm, "flop", "tensor"),     # S (FP4 UMMAs), dP, dQ
-        "quantize": (2 * rows, "byte", "hbm"),      # one of q, k, v: read + write
+        # q, k, v read once; written as codes + scale blocks + bf16 (q, k) and f16 + bf16 (v)
+        "quantize": (rows * (3 + 2 * (0.25 + 1 / 32 + 1) + 2), "byte", "hbm"),
         "bwd_delta": (2 * rows + b * h * n * 4.0, "byte", "hbm"),  # o, dO in, delta out
     }
     return table[kind]
@@ -521,8 +523,8 @@ def hp_bench(peaks, stream, steps, inp, q, k, v, do, wsf, wsb):
 
     def step():
         fwd()
-        api.attn_qat_bwd(q, k, v, o_hp, stats, do, inp.scale, False, dq=dq, dk=dk, dv=dv,
-                         workspace=wsb)
+        api.attn_qat_bwd_saved(wsf, o_hp, stats, do, inp.scale, False, dq=dq, dk=dk, dv=dv,
+                               workspace=wsb)
 
     step()
     torch.cuda.synchronize()
@@ -629,14 +631,17 @@ def run_ours(args):
     stats = torch.empty((b, h, 2, n), dtype=torch.float32, device=dev)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     wsf = torch.empty(api.attn_qat_fwd_workspace(b, n, n, h, d), dtype=torch.uint8, device=dev)
-    wsb = torch.empty(api.attn_qat_bwd_workspace(b, n, n, h, d), dtype=torch.uint8, device=dev)
+    wsb = torch.empty(int(api._lib.load().attn_qat_bwd_saved_workspace(b, n, n, h, d)),
+                      dtype=torch.uint8, device=dev)
 
     def fwd():
         api.attn_qat_fwd(q, k, v, inp.scale, False, o=o, stats=stats, workspace=wsf)
 
     def bwd():
-        api.attn_qat_bwd(q, k, v, o, stats, do, inp.scale, False, dq=dq, dk=dk, dv=dv,
-                         workspace=wsb)
+        # the backward reads the quantized operands the forward left in wsf (the
+        # path of api.AttnQAT): no quantizer launch in the backward
+        api.attn_qat_bwd_saved(wsf, o, stats, do, inp.scale, False, dq=dq, dk=dk, dv=dv,
+                               workspace=wsb)
 
     def step():
         fwd()
@@ -713,8 +718,8 @@ def run_ours(args):
                 stream.wait_event(out[j - 2])
             api.attn_qat_fwd(st["q"], st["k"], st["v"], inp.scale, False, o=st["o"],
                              stats=st["stats"], workspace=wsf)
-            api.attn_qat_bwd(st["q"], st["k"], st["v"], st["o"], st["stats"], st["do"], inp.scale,
-                             False, dq=st["dq"], dk=st["dk"], dv=st["dv"], workspace=wsb)
+            api.attn_qat_bwd_saved(wsf, st["o"], st["stats"], st["do"], inp.scale, False,
+                                   dq=st["dq"], dk=st["dk"], dv=st["dv"], workspace=wsb)
             done[j].record(stream)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(done[j])

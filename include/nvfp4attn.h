@@ -167,9 +167,9 @@ size_t attn_qat_fwd_workspace(int B, int Nq, int Nkv, int H, int D);
  *   q_bf16, k_bf16, v_bf16  Q~, K~, V~ as bf16 [B, N, H, D]
  *   delta              f32 [B, H, Nq]: rowsum(dO * o) (backward only)
  *   total              the workspace size (*_workspace())
- * A region the workspace does not have is SIZE_MAX.  After attn_qat_fwd the
- * forward workspace holds q_codes, k_codes, q_scales, k_scales and v_f16
- * (attn_qat_fwd_hp and attn_qat_fwd_sparse: q_bf16, k_bf16, v_f16); after
+ * A region the workspace does not have is SIZE_MAX.  After attn_qat_fwd or
+ * attn_qat_fwd_hp the forward workspace holds every region it has (all but
+ * delta); after attn_qat_fwd_sparse only q_bf16, k_bf16 and v_f16.  After
  * attn_qat_bwd the backward workspace holds every region it has.  Other bytes
  * are unspecified.  NVQ_ERR_INVALID for sizes the calls reject or a NULL out.
  */
@@ -217,6 +217,28 @@ nvq_status attn_qat_bwd(const void* q, const void* k, const void* v, const void*
                         const float* stats, const void* dout, void* dq, void* dk, void* dv,
                         int B, int Nq, int Nkv, int H, int D, float scale, int causal,
                         void* ws, size_t ws_bytes, nvq_stream_t stream);
+
+/*
+ * Straight-through backward from the quantized operands the forward saved.
+ * attn_qat_fwd and attn_qat_fwd_hp leave Q~, K~ and V~ in their workspace in
+ * every form the backward reads (attn_qat_fwd_layout: codes, scale blocks,
+ * bf16 copies); this call reads them there instead of quantizing q, k and v
+ * again, so it takes neither.  A training step that keeps the forward's
+ * workspace until the backward saves the backward's quantizer pass.
+ *   saved   the workspace of an attn_qat_fwd or attn_qat_fwd_hp call on the
+ *           same q, k, v and sizes, unmodified since (not checked: other bytes
+ *           give wrong gradients, never out-of-bounds accesses); 256-byte
+ *           aligned; saved_bytes >= attn_qat_fwd_workspace(B, Nq, Nkv, H, D)
+ *   o, stats, dout, dq, dk, dv, sizes, scale, causal: as in attn_qat_bwd
+ *   ws      attn_qat_bwd_saved_workspace(...) bytes (delta), 256-byte aligned
+ * The gradients equal attn_qat_bwd's on the same inputs bit for bit.  Not for
+ * the block-sparse forward, whose workspace lacks the codes.
+ */
+size_t attn_qat_bwd_saved_workspace(int B, int Nq, int Nkv, int H, int D);
+nvq_status attn_qat_bwd_saved(const void* saved, size_t saved_bytes, const void* o,
+                              const float* stats, const void* dout, void* dq, void* dk, void* dv,
+                              int B, int Nq, int Nkv, int H, int D, float scale, int causal,
+                              void* ws, size_t ws_bytes, nvq_stream_t stream);
 
 /*
  * attn_qat_bwd with no caller-provided workspace and no allocation.  The paper

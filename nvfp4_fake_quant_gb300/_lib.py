@@ -41,6 +41,10 @@ SIGNATURES = {
     "attn_qat_bwd": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                              c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_float, c_int,
                              c_void_p, c_size_t, c_void_p]),
+    "attn_qat_bwd_saved_workspace": (c_size_t, [c_int, c_int, c_int, c_int, c_int]),
+    "attn_qat_bwd_saved": (c_int, [c_void_p, c_size_t, c_void_p, c_void_p, c_void_p, c_void_p,
+                                   c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_int, c_float,
+                                   c_int, c_void_p, c_size_t, c_void_p]),
     "attn_qat_bwd_builtin_scratch": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                              c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int,
                                              c_int, c_int, c_int, c_float, c_int, c_void_p]),

@@ -204,6 +204,30 @@ def attn_qat_bwd(q, k, v, o, stats, do, scale=None, causal=False, dq=None, dk=No
     return dq, dk, dv
 
 
+def attn_qat_bwd_saved(saved, o, stats, do, scale=None, causal=False, nkv=None, dq=None,
+                       dk=None, dv=None, workspace=None):
+    """Straight-through backward from the quantized operands a forward left in its
+    workspace ``saved`` (the ``workspace`` tensor passed to attn_qat_fwd or
+    attn_qat_fwd_hp on the same q, k, v): returns (dq, dk, dv), equal to
+    attn_qat_bwd's bit for bit.  ``nkv`` is the key count (default Nq)."""
+    _check_bnhd(o, "o")
+    b, nq, h, d = o.shape
+    nkv = nq if nkv is None else int(nkv)
+    _check_bnhd(do, "do", o.shape)
+    _check(stats, "stats", torch.float32)
+    _check(saved, "saved", torch.uint8)
+    scale = _scale(scale, d)
+    dq = torch.empty_like(o) if dq is None else dq
+    dk = torch.empty((b, nkv, h, d), dtype=BF16, device=o.device) if dk is None else dk
+    dv = torch.empty((b, nkv, h, d), dtype=BF16, device=o.device) if dv is None else dv
+    need = int(_lib.load().attn_qat_bwd_saved_workspace(b, nq, nkv, h, d))
+    ws = _workspace(need, o.device, workspace)
+    _lib.call("attn_qat_bwd_saved", _ptr(saved), saved.numel(), _ptr(o), _ptr(stats), _ptr(do),
+              _ptr(dq), _ptr(dk), _ptr(dv), b, nq, nkv, h, d, scale, int(bool(causal)), _ptr(ws),
+              ws.numel() * ws.element_size(), _stream_ptr(o))
+    return dq, dk, dv
+
+
 # ------------------------------------------------------------------ NVFP4 linear
 def nvfp4_tiled_scale_bytes(rows: int, cols: int) -> int:
     return int(_lib.load().nvfp4_tiled_scale_bytes(rows, cols))
@@ -445,21 +469,27 @@ class AttnQATFunction(torch.autograd.Function):
 
     @staticmethod
     def forward(ctx, q, k, v, scale, causal, delta_mode="o"):
+        b, nq, h, d = q.shape
+        # the forward's workspace keeps Q~, K~, V~ in every form the backward
+        # reads: it is saved instead of q, k, v, and the backward quantizes nothing
+        saved = torch.empty(attn_qat_fwd_workspace(b, nq, k.shape[1], h, d), dtype=torch.uint8,
+                            device=q.device)
         if delta_mode == "hp":
-            o, o_d, stats = attn_qat_fwd_hp(q, k, v, scale, causal)
+            o, o_d, stats = attn_qat_fwd_hp(q, k, v, scale, causal, workspace=saved)
         elif delta_mode == "o":
-            o, stats = attn_qat_fwd(q, k, v, scale, causal)
+            o, stats = attn_qat_fwd(q, k, v, scale, causal, workspace=saved)
             o_d = o
         else:
             raise ValueError(f"delta_mode must be one of {DELTA_MODES}, got {delta_mode!r}")
-        ctx.save_for_backward(q, k, v, o_d, stats)
-        ctx.scale, ctx.causal = scale, causal
+        ctx.save_for_backward(saved, o_d, stats)
+        ctx.scale, ctx.causal, ctx.nkv = scale, causal, k.shape[1]
         return o
 
     @staticmethod
     def backward(ctx, do):
-        q, k, v, o_d, stats = ctx.saved_tensors
-        dq, dk, dv = attn_qat_bwd(q, k, v, o_d, stats, do.contiguous(), ctx.scale, ctx.causal)
+        saved, o_d, stats = ctx.saved_tensors
+        dq, dk, dv = attn_qat_bwd_saved(saved, o_d, stats, do.contiguous(), ctx.scale,
+                                        ctx.causal, nkv=ctx.nkv)
         return dq, dk, dv, None, None, None
 
 

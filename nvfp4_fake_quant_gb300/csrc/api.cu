@@ -254,12 +254,14 @@ size_t bytes_bnhd(int B, int N, int H, int D, size_t elem) {
   return static_cast<size_t>(B) * N * H * D * elem;
 }
 
-// Forward workspace: every region at its own offset (nvq_attn_layout).  The
-// dense form writes the packed codes of Q~ and K~ (qc, kc), their scale blocks
-// (qs, ks) and V~ as f16 (v16); the block-sparse and auxiliary-output forms,
-// whose S runs on BF16 UMMAs, write Q~ and K~ as bf16 (qb, kb) and V~ as f16.
+// Forward workspace: every region at its own offset (nvq_attn_layout).  Every
+// form writes the quantized operands once: the packed codes of Q~ and K~ (qc,
+// kc) with their scale blocks (qs, ks), V~ as f16 (v16), and Q~, K~, V~ as bf16
+// (qb, kb, vb).  The dense forward reads the codes and v16, the block-sparse
+// and auxiliary-output forms (BF16 S) qb, kb and v16; attn_qat_bwd_saved reads
+// the codes and the bf16 copies.  The block-sparse forward writes qb, kb, v16 only.
 struct FwdWs {
-  size_t qc, kc, qs, ks, v16, qb, kb, total;
+  size_t qc, kc, qs, ks, v16, qb, kb, vb, total;
 };
 FwdWs fwd_ws(int B, int Nq, int Nkv, int H, int D) {
   FwdWs w;
@@ -270,7 +272,8 @@ FwdWs fwd_ws(int B, int Nq, int Nkv, int H, int D) {
   w.v16 = round_up(w.ks + attn_fp4_scale_bytes(B, Nkv, H, D), 256);
   w.qb = round_up(w.v16 + bytes_bnhd(B, Nkv, H, D, 2), 256);
   w.kb = round_up(w.qb + bytes_bnhd(B, Nq, H, D, 2), 256);
-  w.total = round_up(w.kb + bytes_bnhd(B, Nkv, H, D, 2), 256);
+  w.vb = round_up(w.kb + bytes_bnhd(B, Nkv, H, D, 2), 256);
+  w.total = round_up(w.vb + bytes_bnhd(B, Nkv, H, D, 2), 256);
   return w;
 }
 
@@ -305,13 +308,9 @@ BwdWs bwd_ws(int B, int Nq, int Nkv, int H, int D, int topk = 0) {
   return w;
 }
 
-// Fake-quantizes `rows` contiguous rows of D elements (unit global scale) into
-// `out`, as one timed quantizer launch.
-cudaError_t quantize_rows(const void* x, int64_t rows, int D, int mode, void* out,
-                          cudaStream_t stream) {
-  return timed(NVQ_KERNEL_QUANTIZE, stream, [&] {
-    return launch_fake_quant(x, rows, D, D, nullptr, mode, out, D, nullptr, 0, nullptr, 0, stream);
-  });
+// Workspace of attn_qat_bwd_saved: delta only.
+size_t saved_bwd_ws_bytes(int B, int Nq, int H) {
+  return round_up(static_cast<size_t>(B) * H * Nq * 4, 256);
 }
 
 nvq_status check_quant(const void* x, int64_t rows, int64_t cols, int64_t ld_x) {
@@ -339,52 +338,93 @@ nvq_status fwd_impl(const void* q, const void* k, const void* v, int B, int Nq, 
   int* err = error_word();
   if (err == nullptr) return NVQ_ERR_CUDA;
   uint8_t* wb = static_cast<uint8_t*>(ws);
-  const int64_t rq = static_cast<int64_t>(B) * Nq * H, rk = static_cast<int64_t>(B) * Nkv * H;
   const AttnShape s{B, Nq, Nkv, H, D, scale, causal};
   CUtensorMap mq, mk, mv;
   int r;
   cudaError_t e;
-  if (kv_list == nullptr && o_hp == nullptr) {
+  uint8_t* qc = wb + w.qc;
+  uint8_t* kc = wb + w.kc;
+  uint8_t* qs = wb + w.qs;
+  uint8_t* ks = wb + w.ks;
+  void* v16 = wb + w.v16;
+  void* qb = wb + w.qb;
+  void* kb = wb + w.kb;
+  void* vb = wb + w.vb;
+  // Q~, K~, V~ in every form the forward and a later attn_qat_bwd_saved read
+  // (block-sparse: the bf16 Q~, K~ and f16 V~ its BF16-S kernels read)
+  const bool sparse = kv_list != nullptr;
+  const AttnOpSpec ops[3] = {
+      {q, Nq, sparse ? nullptr : qc, sparse ? nullptr : qs, qb, nullptr},
+      {k, Nkv, sparse ? nullptr : kc, sparse ? nullptr : ks, kb, nullptr},
+      {v, Nkv, nullptr, nullptr, sparse ? nullptr : vb, v16}};
+  if ((e = timed(NVQ_KERNEL_QUANTIZE, stream,
+                 [&] { return launch_quant_attn_ops(ops, 3, B, H, D, stream); })) != cudaSuccess)
+    return fail_cuda("quantize q, k, v", e);
+  if (!sparse && o_hp == nullptr) {
     // dense: S on FP4 UMMAs, Q~ and K~ as codes + scale blocks
-    uint8_t* qc = wb + w.qc;
-    uint8_t* kc = wb + w.kc;
-    uint8_t* qs = wb + w.qs;
-    uint8_t* ks = wb + w.ks;
-    void* vt = wb + w.v16;
     if ((r = make_bnhd_u8_map(&mq, qc, B, Nq, H, D)) != 0 ||
         (r = make_bnhd_u8_map(&mk, kc, B, Nkv, H, D)) != 0 ||
-        (r = make_bnhd_map(&mv, vt, B, Nkv, H, D, true)) != 0)
+        (r = make_bnhd_map(&mv, v16, B, Nkv, H, D, true)) != 0)
       return fail_driver("cuTensorMapEncodeTiled", r);
-    if ((e = timed(NVQ_KERNEL_QUANTIZE, stream, [&] {
-           return launch_quant_attn_fp4(q, B, Nq, H, D, qc, qs, stream);
-         })) != cudaSuccess)
-      return fail_cuda("quantize q (fp4)", e);
-    if ((e = timed(NVQ_KERNEL_QUANTIZE, stream, [&] {
-           return launch_quant_attn_fp4(k, B, Nkv, H, D, kc, ks, stream);
-         })) != cudaSuccess)
-      return fail_cuda("quantize k (fp4)", e);
-    if ((e = quantize_rows(v, rk, D, kUnitF16, vt, stream)) != cudaSuccess)
-      return fail_cuda("quantize v", e);
     return from_cuda("attn_fwd", timed(NVQ_KERNEL_ATTN_FWD, stream, [&] {
                        return launch_attn_fwd_fp4(s, mq, mk, mv, qs, ks, o, stats, err, stream);
                      }));
   }
-  void* qt = wb + w.qb;
-  void* kt = wb + w.kb;
-  void* vt = wb + w.v16;
-  if ((r = make_bnhd_map(&mq, qt, B, Nq, H, D, false)) != 0 ||
-      (r = make_bnhd_map(&mk, kt, B, Nkv, H, D, false)) != 0 ||
-      (r = make_bnhd_map(&mv, vt, B, Nkv, H, D, true)) != 0)
+  if ((r = make_bnhd_map(&mq, qb, B, Nq, H, D, false)) != 0 ||
+      (r = make_bnhd_map(&mk, kb, B, Nkv, H, D, false)) != 0 ||
+      (r = make_bnhd_map(&mv, v16, B, Nkv, H, D, true)) != 0)
     return fail_driver("cuTensorMapEncodeTiled", r);
-  if ((e = quantize_rows(q, rq, D, kUnitBf16, qt, stream)) != cudaSuccess)
-    return fail_cuda("quantize q", e);
-  if ((e = quantize_rows(k, rk, D, kUnitBf16, kt, stream)) != cudaSuccess)
-    return fail_cuda("quantize k", e);
-  if ((e = quantize_rows(v, rk, D, kUnitF16, vt, stream)) != cudaSuccess)
-    return fail_cuda("quantize v", e);
   return from_cuda("attn_fwd", timed(NVQ_KERNEL_ATTN_FWD, stream, [&] {
                      return launch_attn_fwd(s, mq, mk, mv, o, o_hp, stats, kv_list, topk, err,
                                             stream);
+                   }));
+}
+
+// The backward's kernels on quantized operands already in device memory: qb,
+// kb, vb (bf16 Q~, K~, V~) and, dense, the codes and scale blocks of Q~ and K~
+// (qc, kc, qs, ks); kv_list, q_off, q_list for the block-sparse form; delta:
+// f32 [B, H, Nq] scratch.
+nvq_status bwd_kernels(const AttnShape& s, const void* qb, const void* kb, const void* vb,
+                       const uint8_t* qc, const uint8_t* kc, const uint8_t* qs, const uint8_t* ks,
+                       const void* o, const float* stats, const void* dout, const int* kv_list,
+                       int topk, int* q_off, int* q_list, float* delta, void* dq, void* dk,
+                       void* dv, int* err, cudaStream_t stream) {
+  const int B = s.B, Nq = s.Nq, Nkv = s.Nkv, H = s.H, D = s.D;
+  const int n_qt = (Nq + kTile - 1) / kTile, n_kt = (Nkv + kTile - 1) / kTile;
+  CUtensorMap mq, mk, mv, mdo;
+  int r;
+  if ((r = make_bnhd_map(&mq, qb, B, Nq, H, D, false)) != 0 ||
+      (r = make_bnhd_map(&mk, kb, B, Nkv, H, D, false)) != 0 ||
+      (r = make_bnhd_map(&mv, vb, B, Nkv, H, D, false)) != 0 ||
+      (r = make_bnhd_map(&mdo, dout, B, Nq, H, D, false)) != 0)
+    return fail_driver("cuTensorMapEncodeTiled", r);
+  cudaError_t e;
+  if ((e = timed(NVQ_KERNEL_BWD_DELTA, stream,
+                 [&] { return launch_bwd_prep(s, o, dout, delta, stream); })) != cudaSuccess)
+    return fail_cuda("bwd_prep", e);
+  if (kv_list != nullptr &&
+      (e = launch_tile_transpose(kv_list, B, H, n_qt, n_kt, topk, q_off, q_list, stream)) !=
+          cudaSuccess)
+    return fail_cuda("tile_transpose", e);
+  if ((e = timed(NVQ_KERNEL_BWD_DKDV, stream, [&] {
+         return launch_attn_bwd(s, mq, mk, mv, mdo, stats, delta, dk, dv, q_off, q_list,
+                                n_qt * topk, err, stream);
+       })) != cudaSuccess)
+    return fail_cuda("attn_bwd (dK, dV)", e);
+  if (kv_list == nullptr) {
+    // dense: dQ with S on FP4 UMMAs over the codes and scale blocks of Q~, K~
+    CUtensorMap mq4, mk4;
+    if ((r = make_bnhd_u8_map(&mq4, qc, B, Nq, H, D)) != 0 ||
+        (r = make_bnhd_u8_map(&mk4, kc, B, Nkv, H, D)) != 0)
+      return fail_driver("cuTensorMapEncodeTiled", r);
+    return from_cuda("attn_bwd_dq", timed(NVQ_KERNEL_BWD_DQ, stream, [&] {
+                       return launch_attn_bwd_dq_fp4(s, mq4, mdo, mk4, mk, mv, qs, ks, stats,
+                                                     delta, dq, err, stream);
+                     }));
+  }
+  return from_cuda("attn_bwd_dq", timed(NVQ_KERNEL_BWD_DQ, stream, [&] {
+                     return launch_attn_bwd_dq(s, mq, mdo, mk, mv, stats, delta, dq, kv_list, topk,
+                                               err, stream);
                    }));
 }
 
@@ -400,7 +440,8 @@ nvq_status check_bwd_args(const void* q, const void* k, const void* v, const voi
   return NVQ_OK;
 }
 
-// Straight-through backward; kv_list as in fwd_impl.
+// Straight-through backward from q, k, v: quantizes them (one launch) into the
+// workspace, then runs the backward's kernels; kv_list as in fwd_impl.
 nvq_status bwd_impl(const void* q, const void* k, const void* v, const void* o,
                     const float* stats, const void* dout, const int* kv_list, int topk, void* dq,
                     void* dk, void* dv, int B, int Nq, int Nkv, int H, int D, float scale,
@@ -414,68 +455,50 @@ nvq_status bwd_impl(const void* q, const void* k, const void* v, const void* o,
   int* err = error_word();
   if (err == nullptr) return NVQ_ERR_CUDA;
   uint8_t* wb = static_cast<uint8_t*>(ws);
-  void* qt = wb + w.q;
-  void* kt = wb + w.k;
-  void* vt = wb + w.v;
-  float* delta = reinterpret_cast<float*>(wb + w.delta);
-  int* q_off = kv_list != nullptr ? reinterpret_cast<int*>(wb + w.q_off) : nullptr;
-  int* q_list = kv_list != nullptr ? reinterpret_cast<int*>(wb + w.q_list) : nullptr;
-  const int n_qt = (Nq + kTile - 1) / kTile, n_kt = (Nkv + kTile - 1) / kTile;
-  CUtensorMap mq, mk, mv, mdo;
-  int r;
-  if ((r = make_bnhd_map(&mq, qt, B, Nq, H, D, false)) != 0 ||
-      (r = make_bnhd_map(&mk, kt, B, Nkv, H, D, false)) != 0 ||
-      (r = make_bnhd_map(&mv, vt, B, Nkv, H, D, false)) != 0 ||
-      (r = make_bnhd_map(&mdo, dout, B, Nq, H, D, false)) != 0)
-    return fail_driver("cuTensorMapEncodeTiled", r);
-  const int64_t rq = static_cast<int64_t>(B) * Nq * H, rk = static_cast<int64_t>(B) * Nkv * H;
-  const AttnShape s{B, Nq, Nkv, H, D, scale, causal};
+  const bool sparse = kv_list != nullptr;
+  uint8_t* qc = sparse ? nullptr : wb + w.qc;
+  uint8_t* kc = sparse ? nullptr : wb + w.kc;
+  uint8_t* qs = sparse ? nullptr : wb + w.qs;
+  uint8_t* ks = sparse ? nullptr : wb + w.ks;
+  const AttnOpSpec ops[3] = {{q, Nq, qc, qs, wb + w.q, nullptr},
+                             {k, Nkv, kc, ks, wb + w.k, nullptr},
+                             {v, Nkv, nullptr, nullptr, wb + w.v, nullptr}};
   cudaError_t e;
-  if ((e = quantize_rows(q, rq, D, kUnitBf16, qt, stream)) != cudaSuccess)
-    return fail_cuda("quantize q", e);
-  if ((e = quantize_rows(k, rk, D, kUnitBf16, kt, stream)) != cudaSuccess)
-    return fail_cuda("quantize k", e);
-  if ((e = quantize_rows(v, rk, D, kUnitBf16, vt, stream)) != cudaSuccess)
-    return fail_cuda("quantize v", e);
-  if ((e = timed(NVQ_KERNEL_BWD_DELTA, stream,
-                 [&] { return launch_bwd_prep(s, o, dout, delta, stream); })) != cudaSuccess)
-    return fail_cuda("bwd_prep", e);
-  if (kv_list != nullptr &&
-      (e = launch_tile_transpose(kv_list, B, H, n_qt, n_kt, topk, q_off, q_list, stream)) !=
-          cudaSuccess)
-    return fail_cuda("tile_transpose", e);
-  if ((e = timed(NVQ_KERNEL_BWD_DKDV, stream, [&] {
-         return launch_attn_bwd(s, mq, mk, mv, mdo, stats, delta, dk, dv, q_off, q_list,
-                                n_qt * topk, err, stream);
-       })) != cudaSuccess)
-    return fail_cuda("attn_bwd (dK, dV)", e);
-  if (kv_list == nullptr) {
-    // dense: dQ with S on FP4 UMMAs over the codes and scale blocks of Q~, K~
-    uint8_t* qc = wb + w.qc;
-    uint8_t* kc = wb + w.kc;
-    uint8_t* qs = wb + w.qs;
-    uint8_t* ks = wb + w.ks;
-    CUtensorMap mq4, mk4;
-    if ((r = make_bnhd_u8_map(&mq4, qc, B, Nq, H, D)) != 0 ||
-        (r = make_bnhd_u8_map(&mk4, kc, B, Nkv, H, D)) != 0)
-      return fail_driver("cuTensorMapEncodeTiled", r);
-    if ((e = timed(NVQ_KERNEL_QUANTIZE, stream, [&] {
-           return launch_quant_attn_fp4(q, B, Nq, H, D, qc, qs, stream);
-         })) != cudaSuccess)
-      return fail_cuda("quantize q (fp4)", e);
-    if ((e = timed(NVQ_KERNEL_QUANTIZE, stream, [&] {
-           return launch_quant_attn_fp4(k, B, Nkv, H, D, kc, ks, stream);
-         })) != cudaSuccess)
-      return fail_cuda("quantize k (fp4)", e);
-    return from_cuda("attn_bwd_dq", timed(NVQ_KERNEL_BWD_DQ, stream, [&] {
-                       return launch_attn_bwd_dq_fp4(s, mq4, mdo, mk4, mk, mv, qs, ks, stats,
-                                                     delta, dq, err, stream);
-                     }));
-  }
-  return from_cuda("attn_bwd_dq", timed(NVQ_KERNEL_BWD_DQ, stream, [&] {
-                     return launch_attn_bwd_dq(s, mq, mdo, mk, mv, stats, delta, dq, kv_list, topk,
-                                               err, stream);
-                   }));
+  if ((e = timed(NVQ_KERNEL_QUANTIZE, stream,
+                 [&] { return launch_quant_attn_ops(ops, 3, B, H, D, stream); })) != cudaSuccess)
+    return fail_cuda("quantize q, k, v", e);
+  const AttnShape s{B, Nq, Nkv, H, D, scale, causal};
+  return bwd_kernels(s, wb + w.q, wb + w.k, wb + w.v, qc, kc, qs, ks, o, stats, dout, kv_list,
+                     topk, sparse ? reinterpret_cast<int*>(wb + w.q_off) : nullptr,
+                     sparse ? reinterpret_cast<int*>(wb + w.q_list) : nullptr,
+                     reinterpret_cast<float*>(wb + w.delta), dq, dk, dv, err, stream);
+}
+
+// Straight-through backward from the quantized operands a dense forward left
+// in its workspace (no quantizer launch).
+nvq_status bwd_saved_impl(const void* saved, size_t saved_bytes, const void* o,
+                          const float* stats, const void* dout, void* dq, void* dk, void* dv,
+                          int B, int Nq, int Nkv, int H, int D, float scale, int causal, void* ws,
+                          size_t ws_bytes, cudaStream_t stream) {
+  nvq_status st = check_attn(B, Nq, Nkv, H, D, scale, causal);
+  if (st != NVQ_OK) return st;
+  const void* ptrs[] = {o, stats, dout, dq, dk, dv};
+  for (const void* p : ptrs)
+    if (p == nullptr || !aligned16(p)) return NVQ_ERR_INVALID;
+  const FwdWs f = fwd_ws(B, Nq, Nkv, H, D);
+  if (saved == nullptr || saved_bytes < f.total ||
+      (reinterpret_cast<uintptr_t>(saved) & 255u) != 0)
+    return NVQ_ERR_WORKSPACE;
+  if (ws == nullptr || ws_bytes < saved_bwd_ws_bytes(B, Nq, H) ||
+      (reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
+    return NVQ_ERR_WORKSPACE;
+  int* err = error_word();
+  if (err == nullptr) return NVQ_ERR_CUDA;
+  const uint8_t* fb = static_cast<const uint8_t*>(saved);
+  const AttnShape s{B, Nq, Nkv, H, D, scale, causal};
+  return bwd_kernels(s, fb + f.qb, fb + f.kb, fb + f.vb, fb + f.qc, fb + f.kc, fb + f.qs,
+                     fb + f.ks, o, stats, dout, nullptr, 0, nullptr, nullptr,
+                     static_cast<float*>(ws), dq, dk, dv, err, stream);
 }
 
 }  // namespace nvq
@@ -575,7 +598,7 @@ nvq_status attn_qat_fwd_layout(int B, int Nq, int Nkv, int H, int D, nvq_attn_la
   if (out == nullptr || B < 1 || Nq < 1 || Nkv < 1 || H < 1 || (D != 64 && D != 128))
     return NVQ_ERR_INVALID;
   const FwdWs w = fwd_ws(B, Nq, Nkv, H, D);
-  *out = nvq_attn_layout{w.qc, w.kc, w.qs, w.ks, w.v16, w.qb, w.kb, SIZE_MAX, SIZE_MAX, w.total};
+  *out = nvq_attn_layout{w.qc, w.kc, w.qs, w.ks, w.v16, w.qb, w.kb, w.vb, SIZE_MAX, w.total};
   return NVQ_OK;
 }
 
@@ -608,6 +631,19 @@ nvq_status attn_qat_bwd(const void* q, const void* k, const void* v, const void*
                         size_t ws_bytes, nvq_stream_t stream) {
   return bwd_impl(q, k, v, o, stats, dout, nullptr, 0, dq, dk, dv, B, Nq, Nkv, H, D, scale, causal,
                   ws, ws_bytes, stream);
+}
+
+size_t attn_qat_bwd_saved_workspace(int B, int Nq, int Nkv, int H, int D) {
+  if (B < 1 || Nq < 1 || Nkv < 1 || H < 1 || D < 1) return 0;
+  return saved_bwd_ws_bytes(B, Nq, H);
+}
+
+nvq_status attn_qat_bwd_saved(const void* saved, size_t saved_bytes, const void* o,
+                              const float* stats, const void* dout, void* dq, void* dk, void* dv,
+                              int B, int Nq, int Nkv, int H, int D, float scale, int causal,
+                              void* ws, size_t ws_bytes, nvq_stream_t stream) {
+  return bwd_saved_impl(saved, saved_bytes, o, stats, dout, dq, dk, dv, B, Nq, Nkv, H, D, scale,
+                        causal, ws, ws_bytes, stream);
 }
 
 // Block-sparse: N % 128 == 0 (whole tiles), 1 <= topk <= N / 128, an int32

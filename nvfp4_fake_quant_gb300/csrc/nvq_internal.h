@@ -33,6 +33,34 @@ cudaError_t launch_quant_tiled(const void* x, int64_t rows, int64_t cols, int64_
 size_t attn_fp4_scale_bytes(int B, int N, int H, int D);
 cudaError_t launch_quant_attn_fp4(const void* x, int B, int N, int H, int D, uint8_t* codes,
                                   uint8_t* scales, cudaStream_t stream);
+// One attention operand x bf16 [B, N, H, D] (contiguous) and the forms to write
+// (each may be null): packed codes [B, N, H, D/2] and scale blocks (the layout
+// of launch_quant_attn_fp4), fake-quantized bf16 and f16 copies [B, N, H, D].
+struct AttnOpSpec {
+  const void* x;
+  int N;
+  uint8_t* codes;
+  uint8_t* scales;
+  void* bf16;
+  void* f16;
+};
+// Device form of AttnOpSpec (quant.cu).
+struct AttnOpJob {
+  const uint16_t* x;
+  uint8_t* codes;
+  uint8_t* scales;
+  uint16_t* bf16;
+  uint16_t* f16;
+  uint32_t nblocks, npad, N, n_tiles;
+};
+struct AttnOpJobs {
+  AttnOpJob j[3];
+  uint32_t H, lg_nbd;
+};
+// Quantizes `count` (1..3) operands with the same B, H, D (unit global scale)
+// in one launch; D in {64, 128}.
+cudaError_t launch_quant_attn_ops(const AttnOpSpec* specs, int count, int B, int H, int D,
+                                  cudaStream_t stream);
 cudaError_t launch_global_sf(const void* x, int64_t rows, int64_t cols, int64_t ld_x, float* gsf,
                              cudaStream_t stream);
 

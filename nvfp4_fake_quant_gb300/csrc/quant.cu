@@ -158,6 +158,86 @@ __global__ void __launch_bounds__(256) quant_attn_fp4_kernel(
   }
 }
 
+// Every quantized form of up to three attention operands in one launch.  Blocks
+// of all jobs form one flat index space (job after job, 16-element blocks in
+// memory order, two in flight per thread); each block's decision is taken once
+// (quant16_unit) and written in every form its job asks for.  The f16 value of
+// a code times an E4M3 scale is exact, and so is its bf16 rounding (at most 6
+// significant bits), so both copies hold the same numbers.  The indices after
+// the blocks zero the scales of the padding tokens of the last 128-token tile
+// of every job that writes scale blocks.
+__global__ void __launch_bounds__(256) quant_attn_ops_kernel(const AttnOpJobs jobs) {
+  const uint32_t nbd = 1u << jobs.lg_nbd;  // 16-element blocks per row (D / 16)
+  const uint32_t nkk = nbd >> 2;           // 64-element groups per row
+  const uint32_t step = gridDim.x * blockDim.x;
+  const uint32_t n0 = jobs.j[0].nblocks, n01 = n0 + jobs.j[1].nblocks;
+  const uint32_t total = n01 + jobs.j[2].nblocks;
+  auto scale_at = [&](const AttnOpJob& jb, uint32_t bh, uint32_t n, uint32_t cb) -> uint8_t* {
+    return jb.scales +
+           ((static_cast<int64_t>(bh) * jb.n_tiles + (n >> 7)) * nkk + (cb >> 2)) * 512 +
+           (n & 31u) * 16 + ((n >> 5) & 3u) * 4 + (cb & 3u);
+  };
+  constexpr uint32_t kUnroll = 2;
+  for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += kUnroll * step) {
+    Block16 v[kUnroll];
+    uint32_t jid[kUnroll], blk[kUnroll];
+#pragma unroll
+    for (uint32_t u = 0; u < kUnroll; ++u) {
+      const uint32_t g = i + u * step;
+      jid[u] = g < n0 ? 0u : (g < n01 ? 1u : 2u);
+      blk[u] = g - (jid[u] == 0 ? 0u : (jid[u] == 1 ? n0 : n01));
+      if (g < total) v[u] = load_block(jobs.j[jid[u]].x + static_cast<int64_t>(blk[u]) * 16);
+    }
+#pragma unroll
+    for (uint32_t u = 0; u < kUnroll; ++u) {
+      if (i + u * step >= total) continue;
+      const AttnOpJob& jb = jobs.j[jid[u]];
+      const uint32_t xv[8] = {v[u].lo.x, v[u].lo.y, v[u].lo.z, v[u].lo.w,
+                              v[u].hi.x, v[u].hi.y, v[u].hi.z, v[u].hi.w};
+      Q16 q = quant16_unit<true>(xv);  // f16 dequantized values
+      const int64_t e0 = static_cast<int64_t>(blk[u]) * 16;
+      if (jb.f16 != nullptr) {
+        uint4* dst = reinterpret_cast<uint4*>(jb.f16 + e0);
+        dst[0] = make_uint4(q.out[0], q.out[1], q.out[2], q.out[3]);
+        dst[1] = make_uint4(q.out[4], q.out[5], q.out[6], q.out[7]);
+      }
+      if (jb.bf16 != nullptr) {
+        uint32_t w[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          __nv_bfloat162 bv = __floats2bfloat162_rn(f16lo_to_f32(q.out[k]), f16lo_to_f32(q.out[k] >> 16));
+          w[k] = *reinterpret_cast<uint32_t*>(&bv) | (q.out[k] & 0x80008000u);  // keeps -0
+        }
+        uint4* dst = reinterpret_cast<uint4*>(jb.bf16 + e0);
+        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+      }
+      if (jb.codes != nullptr) {
+        code_signs(xv, q.codes);
+        *reinterpret_cast<uint2*>(jb.codes + static_cast<int64_t>(blk[u]) * 8) =
+            make_uint2(q.codes[0], q.codes[1]);
+      }
+      if (jb.scales != nullptr) {
+        const uint32_t row = blk[u] >> jobs.lg_nbd, cb = blk[u] & (nbd - 1u);
+        const uint32_t bn = row / jobs.H, h = row - bn * jobs.H;
+        const uint32_t b = bn / jb.N, n = bn - b * jb.N;
+        *scale_at(jb, b * jobs.H + h, n, cb) = static_cast<uint8_t>(q.sbyte);
+      }
+    }
+  }
+  // padding tokens of the last tile: scale 0
+  const uint32_t p0 = jobs.j[0].npad, p01 = p0 + jobs.j[1].npad, ptot = p01 + jobs.j[2].npad;
+  for (uint32_t t = blockIdx.x * blockDim.x + threadIdx.x; t < ptot; t += step) {
+    const uint32_t j = t < p0 ? 0u : (t < p01 ? 1u : 2u);
+    const AttnOpJob& jb = jobs.j[j];
+    const uint32_t idx = t - (j == 0 ? 0u : (j == 1 ? p0 : p01));
+    const uint32_t pad_rows = jb.n_tiles * 128u - jb.N;
+    const uint32_t cb = idx & (nbd - 1u), r = idx >> jobs.lg_nbd;
+    const uint32_t bh = r / pad_rows, n = jb.N + (r - bh * pad_rows);
+    *scale_at(jb, bh, n, cb) = 0;
+  }
+}
+
 // Byte offset of the scale of (row r, 16-element block cb) in the 128x4 tiled
 // layout of block-scaled FP4 GEMMs: 512-byte tiles of 128 rows x 4 blocks,
 // tiles ordered by row tile, then block tile (n_bt tiles per row tile); inside
@@ -406,6 +486,38 @@ cudaError_t launch_quant_attn_fp4(const void* x, int B, int N, int H, int D, uin
       static_cast<const uint16_t*>(x), static_cast<uint32_t>(nblocks), static_cast<uint32_t>(npad),
       static_cast<uint32_t>(N), static_cast<uint32_t>(H), D == 128 ? 3u : 2u,
       static_cast<uint32_t>(n_tiles), codes, scales);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_attn_ops(const AttnOpSpec* specs, int count, int B, int H, int D,
+                                  cudaStream_t stream) {
+  if ((D != 64 && D != 128) || count < 1 || count > 3) return cudaErrorInvalidValue;
+  AttnOpJobs jobs{};
+  jobs.H = static_cast<uint32_t>(H);
+  jobs.lg_nbd = D == 128 ? 3u : 2u;
+  int64_t total = 0, ptot = 0;
+  for (int i = 0; i < count; ++i) {
+    const AttnOpSpec& sp = specs[i];
+    AttnOpJob& jb = jobs.j[i];
+    const int64_t nb = static_cast<int64_t>(B) * sp.N * H * (D / 16);
+    const int64_t nt = (sp.N + 127) / 128;
+    jb.x = static_cast<const uint16_t*>(sp.x);
+    jb.codes = sp.codes;
+    jb.scales = sp.scales;
+    jb.bf16 = static_cast<uint16_t*>(sp.bf16);
+    jb.f16 = static_cast<uint16_t*>(sp.f16);
+    jb.nblocks = static_cast<uint32_t>(nb);
+    jb.N = static_cast<uint32_t>(sp.N);
+    jb.n_tiles = static_cast<uint32_t>(nt);
+    const int64_t np = sp.scales != nullptr ? static_cast<int64_t>(B) * H * (nt * 128 - sp.N) * (D / 16) : 0;
+    jb.npad = static_cast<uint32_t>(np);
+    total += nb;
+    ptot += np;
+  }
+  if (total >= (int64_t{1} << 31) || ptot >= (int64_t{1} << 31)) return cudaErrorInvalidValue;
+  const int threads = 256;
+  const int64_t work = std::max<int64_t>((total + 1) / 2, ptot);
+  quant_attn_ops_kernel<<<wave_grid<quant_attn_ops_kernel>(work, threads), threads, 0, stream>>>(jobs);
   return cudaGetLastError();
 }
 

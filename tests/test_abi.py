@@ -63,8 +63,9 @@ def test_workspace_sizes(lib):
     # 512-byte scale blocks (one per 128 rows and 64 elements of D) of Q~ and K~
     codes = b * n * h * d // 2
     scales = b * h * ((n + 127) // 128) * (d // 64) * 512
-    # forward: codes and scale blocks of Q~, K~, V~ in f16, Q~ and K~ in bf16
-    assert lib.attn_qat_fwd_workspace(b, n, n, h, d) == 2 * codes + 2 * scales + 3 * t
+    # forward: codes and scale blocks of Q~, K~, V~ in f16, Q~, K~ and V~ in bf16
+    assert lib.attn_qat_fwd_workspace(b, n, n, h, d) == 2 * codes + 2 * scales + 4 * t
+    assert lib.attn_qat_bwd_saved_workspace(b, n, n, h, d) == b * h * n * 4
     assert lib.attn_qat_bwd_workspace(b, n, n, h, d) == 3 * t + b * h * n * 4 + 2 * codes + 2 * scales
     assert lib.attn_qat_fwd_workspace(0, n, n, h, d) == 0
     assert lib.attn_qat_fwd_workspace(1, 3, 5, 1, 64) % 256 == 0
@@ -91,7 +92,8 @@ def test_workspace_layouts(lib):
             assert all(e0 <= s1 for (_, e0), (s1, _) in zip(spans, spans[1:]))
             assert spans[-1][1] <= lay["total"]
         assert set(api.attn_qat_layout(b, nq, nkv, h, d, "fwd")) == \
-            {"q_codes", "k_codes", "q_scales", "k_scales", "v_f16", "q_bf16", "k_bf16", "total"}
+            {"q_codes", "k_codes", "q_scales", "k_scales", "v_f16", "q_bf16", "k_bf16", "v_bf16",
+             "total"}
         assert set(api.attn_qat_layout(b, nq, nkv, h, d, "bwd")) == \
             {"q_codes", "k_codes", "q_scales", "k_scales", "q_bf16", "k_bf16", "v_bf16", "delta",
              "total"}
@@ -152,6 +154,27 @@ def test_bwd_rejects_bad_arguments(lib):
     assert bwd(dq=A + 2) == INVALID
     assert bwd(scale=float("nan")) == INVALID
     assert bwd(ws_bytes=0) == WORKSPACE
+
+
+def test_bwd_saved_rejects_bad_arguments(lib):
+    b, n, h, d = 1, 256, 2, 128
+    fws = lib.attn_qat_fwd_workspace(b, n, n, h, d)
+    bws = lib.attn_qat_bwd_saved_workspace(b, n, n, h, d)
+
+    def bwd(saved=A, saved_bytes=fws, o=A, D=d, causal=0, scale=0.1, ws=A + (1 << 30),
+            ws_bytes=bws, nkv=n):
+        return lib.attn_qat_bwd_saved(saved, saved_bytes, o, A, A, A, A, A, b, n, nkv, h, D, scale,
+                                      causal, ws, ws_bytes, None)
+    assert bwd(D=96) == UNSUPPORTED
+    assert bwd(causal=1, nkv=n + 1) == UNSUPPORTED
+    assert bwd(scale=float("nan")) == INVALID
+    assert bwd(o=None) == INVALID
+    assert bwd(o=A + 8) == INVALID
+    assert bwd(saved=None) == WORKSPACE
+    assert bwd(saved_bytes=fws - 1) == WORKSPACE
+    assert bwd(saved=A + 16) == WORKSPACE
+    assert bwd(ws_bytes=bws - 1) == WORKSPACE
+    assert bwd(ws=None) == WORKSPACE
 
 
 def test_quantizer_rejects_bad_arguments(lib):

@@ -159,9 +159,39 @@ def test_kernel_timing_hook_counts_every_launch():
         got = api.timing_read()
     finally:
         api.timing_enable(False)
+    # one fused quantizer launch per call (q, k, v in every form the call reads)
     assert {k: n for k, (n, _) in got.items()} == {
-        "quantize": 8, "attn_fwd": 1, "bwd_delta": 1, "bwd_dkdv": 1, "bwd_dq": 1, "global_sf": 0,
+        "quantize": 2, "attn_fwd": 1, "bwd_delta": 1, "bwd_dkdv": 1, "bwd_dq": 1, "global_sf": 0,
         "vsa": 0, "linear": 0}
     assert all(ms > 0 for n, ms in got.values() if n)
     assert sum(ms for _, ms in got.values()) <= wall_ms
     assert api.timing_read()["attn_fwd"] == (0, 0.0)  # disabled: records discarded
+
+
+SAVED_CASES = [c for c in CASES if c[0] in ("tiny_config", "ragged_d128", "cross_d128",
+                                            "causal_d64", "short", "thirteen_tiles")]
+
+
+@pytest.mark.parametrize("case", SAVED_CASES, ids=lambda c: c[0])
+def test_saved_operand_backward_matches(case):
+    """attn_qat_bwd_saved reads the quantized operands the forward left in its
+    workspace; its gradients equal attn_qat_bwd's (which quantizes q, k, v
+    itself) bit for bit, after attn_qat_fwd and after attn_qat_fwd_hp."""
+    name, b, nq, nkv, h, d, causal, seed, dist, scale = case
+    inp = workloads.attn_inputs(b, nq, nkv, h, d, seed, scale=scale, causal=causal, dist=dist)
+    q, k, v, do = (t.cuda() for t in (inp.q, inp.k, inp.v, inp.do))
+    saved = torch.full((api.attn_qat_fwd_workspace(b, nq, nkv, h, d),), 0x5A, dtype=torch.uint8,
+                       device="cuda")
+    o, stats = api.attn_qat_fwd(q, k, v, inp.scale, causal, workspace=saved)
+    ref = api.attn_qat_bwd(q, k, v, o, stats, do, inp.scale, causal)
+    got = api.attn_qat_bwd_saved(saved, o, stats, do, inp.scale, causal, nkv=nkv)
+    assert api.device_status() == 0
+    for n_, g, r in zip(("dq", "dk", "dv"), got, ref):
+        assert torch.equal(g, r), n_
+    saved.fill_(0xA5)
+    o2, o_hp, stats2 = api.attn_qat_fwd_hp(q, k, v, inp.scale, causal, workspace=saved)
+    ref = api.attn_qat_bwd(q, k, v, o_hp, stats2, do, inp.scale, causal)
+    got = api.attn_qat_bwd_saved(saved, o_hp, stats2, do, inp.scale, causal, nkv=nkv)
+    assert api.device_status() == 0
+    for n_, g, r in zip(("dq", "dk", "dv"), got, ref):
+        assert torch.equal(g, r), n_

@@ -5,8 +5,9 @@ byte for byte, and the agreement of the forward's and the backward's P~.
    workspaces hold the quantized Q, K, V at the offsets attn_qat_*_layout
    reports (include/nvfp4attn.h): the E2M1 codes and the 512-byte scale blocks
    of Q~ and K~ that feed the block-scaled FP4 MMA, V~ in f16, Q~/K~/V~ in
-   bf16.  Spec acceptance asks for bit-exact codes and E4M3 scales on
-   identical inputs, so every byte is compared with the oracle's quantizer
+   bf16 (the forward's copies are what attn_qat_bwd_saved reads).  North-star
+   acceptance asks for bit-exact codes and E4M3 scales on identical inputs,
+   so every byte is compared with the oracle's quantizer
    ("nvfp4_qad.py", module docstring: blocks of 16, E4M3 scale, E2M1 codes),
    re-laid into the documented block layout; the padding tokens of the last
    128-token tile must carry scale 0.  The workspaces are filled with a
@@ -110,19 +111,18 @@ def test_forward_workspace_operands_are_bit_exact(case):
     b, nq, nkv, h, d, causal, _ = case
     inp, (q, k, v, _do) = _inputs(case)
     lay = api.attn_qat_layout(b, nq, nkv, h, d, "fwd")
-    ws = torch.full((lay["total"],), FILL, dtype=torch.uint8, device="cuda")
-    api.attn_qat_fwd(q, k, v, inp.scale, causal, workspace=ws)
-    assert api.device_status() == 0
-    check_fp4(ws, lay, "q", inp.q)
-    check_fp4(ws, lay, "k", inp.k)
-    check_16bit(ws, lay["v_f16"], inp.v, torch.float16, "V~ (f16)")
-    # the auxiliary-output forward (BF16 S) keeps Q~, K~ in bf16 and V~ in f16
-    ws.fill_(FILL)
-    api.attn_qat_fwd_hp(q, k, v, inp.scale, causal, workspace=ws)
-    assert api.device_status() == 0
-    check_16bit(ws, lay["q_bf16"], inp.q, torch.bfloat16, "Q~ (bf16)")
-    check_16bit(ws, lay["k_bf16"], inp.k, torch.bfloat16, "K~ (bf16)")
-    check_16bit(ws, lay["v_f16"], inp.v, torch.float16, "V~ (f16)")
+    ws = torch.empty((lay["total"],), dtype=torch.uint8, device="cuda")
+    # both dense forwards leave every form of Q~, K~, V~ the backward reads
+    for fwd in (api.attn_qat_fwd, api.attn_qat_fwd_hp):
+        ws.fill_(FILL)
+        fwd(q, k, v, inp.scale, causal, workspace=ws)
+        assert api.device_status() == 0
+        check_fp4(ws, lay, "q", inp.q)
+        check_fp4(ws, lay, "k", inp.k)
+        check_16bit(ws, lay["v_f16"], inp.v, torch.float16, "V~ (f16)")
+        check_16bit(ws, lay["q_bf16"], inp.q, torch.bfloat16, "Q~ (bf16)")
+        check_16bit(ws, lay["k_bf16"], inp.k, torch.bfloat16, "K~ (bf16)")
+        check_16bit(ws, lay["v_bf16"], inp.v, torch.bfloat16, "V~ (bf16)")
 
 
 @pytest.mark.parametrize("case", CASES, ids=lambda c: "x".join(map(str, c[:5])))
