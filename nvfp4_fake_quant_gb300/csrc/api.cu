@@ -370,13 +370,18 @@ nvq_status fwd_impl(const void* q, const void* k, const void* v, int B, int Nq, 
                        return launch_attn_fwd_fp4(s, mq, mk, mv, qs, ks, o, stats, err, stream);
                      }));
   }
+  CUtensorMap mq4, mk4;  // auxiliary output: codes of Q~, K~ for the FP4 pass 1
   if ((r = make_bnhd_map(&mq, qb, B, Nq, H, D, false)) != 0 ||
       (r = make_bnhd_map(&mk, kb, B, Nkv, H, D, false)) != 0 ||
-      (r = make_bnhd_map(&mv, v16, B, Nkv, H, D, true)) != 0)
+      (r = make_bnhd_map(&mv, v16, B, Nkv, H, D, true)) != 0 ||
+      (!sparse && ((r = make_bnhd_u8_map(&mq4, qc, B, Nq, H, D)) != 0 ||
+                   (r = make_bnhd_u8_map(&mk4, kc, B, Nkv, H, D)) != 0)))
     return fail_driver("cuTensorMapEncodeTiled", r);
+  if (sparse) mq4 = mk4 = mq;  // unused by the block-sparse form
   return from_cuda("attn_fwd", timed(NVQ_KERNEL_ATTN_FWD, stream, [&] {
-                     return launch_attn_fwd(s, mq, mk, mv, o, o_hp, stats, kv_list, topk, err,
-                                            stream);
+                     return launch_attn_fwd(s, mq, mk, mv, mq4, mk4, sparse ? nullptr : qs,
+                                            sparse ? nullptr : ks, o, o_hp, stats, kv_list, topk,
+                                            err, stream);
                    }));
 }
 

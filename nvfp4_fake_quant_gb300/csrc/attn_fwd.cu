@@ -65,6 +65,8 @@ constexpr int kDense = 0, kSparse = 1, kAux = 2;  // forward modes
 template <int D>
 struct FwdLayout {
   static constexpr uint32_t kTileBytes = 128u * D * 2u;
+  static constexpr uint32_t kCodeBytes = 128u * D / 2;      // E2M1 codes of a 128-row tile
+  static constexpr uint32_t kScBytes = (D / 64) * 512u;     // their scale blocks
   static constexpr uint32_t kQ = 0;                          // [2] query tiles
   static constexpr uint32_t kRingOff = kQ + 2u * kTileBytes;
   static constexpr uint32_t kX = kRingOff + kRing * kTileBytes;  // [2 tiles][128] f32
@@ -90,7 +92,9 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
 template <int D, int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                    const __grid_constant__ CUtensorMap tv, __nv_bfloat16* __restrict__ o,
+                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tq4,
+                    const __grid_constant__ CUtensorMap tk4, const uint8_t* __restrict__ q_sc,
+                    const uint8_t* __restrict__ k_sc, __nv_bfloat16* __restrict__ o,
                     __nv_bfloat16* __restrict__ o_hp, float* __restrict__ stats, int Nq, int Nkv,
                     int H, float scale, int causal, const int* __restrict__ kv_list, int topk,
                     int* __restrict__ err) {
@@ -185,13 +189,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tq);
     tma_prefetch_desc(&tk);
     tma_prefetch_desc(&tv);
-    mbar_arrive_expect_tx_w(q_full, static_cast<uint32_t>(kQTiles) * L::kTileBytes);
+    mbar_arrive_expect_tx_w(q_full, static_cast<uint32_t>(kQTiles) * L::kTileBytes +
+                                        (aux ? L::kCodeBytes + L::kScBytes : 0u));
 #pragma unroll
     for (int i = 0; i < kQTiles; ++i)
 #pragma unroll
       for (int blk = 0; blk < D / 64; ++blk)
         tma_load_4d_w(smem + L::kQ + i * L::kTileBytes + blk * kAtomBlock, &tq, blk * 64,
                       q0 + i * kTile, h, b, q_full);
+    if constexpr (aux) {  // Q~ codes and scale blocks for the FP4 S of pass 1 (second Q slot)
+      tma_prefetch_desc(&tq4);
+      tma_prefetch_desc(&tk4);
+      uint8_t* q4 = smem + L::kQ + L::kTileBytes;
+      tma_load_4d_w(q4, &tq4, 0, q0, h, b, q_full);
+      bulk_load_w(q4 + L::kCodeBytes,
+                  q_sc + ((static_cast<int64_t>(b) * H + h) * n_qt + blockIdx.x) * L::kScBytes,
+                  L::kScBytes, q_full);
+    }
     int last[kRing];
     for (int s = 0; s < kRing; ++s) last[s] = -1;
     bool ok = true;
@@ -209,8 +223,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++li;
       return true;
     };
+    // auxiliary output, pass 1: K~ as codes + scale blocks (a key tile past the
+    // last one, the missing odd tile of the last step, gets zero codes and no
+    // scales: its scores are masked)
+    auto load4 = [&](int tile) -> bool {
+      const int slot = li % kRing;
+      const uint32_t use = static_cast<uint32_t>(li / kRing);
+      if (!mbar_wait_warp(&r_empty[slot], (use & 1u) ^ 1u, abort)) return false;
+      const bool have = tile < n_kv_all;
+      uint8_t* dst = smem + L::kRingOff + slot * L::kTileBytes;
+      mbar_arrive_expect_tx_w(&r_full[slot], L::kCodeBytes + (have ? L::kScBytes : 0u));
+      tma_load_4d_w(dst, &tk4, 0, tile * kTile, h, b, &r_full[slot]);
+      if (have)
+        bulk_load_w(dst + L::kCodeBytes,
+                    k_sc + ((static_cast<int64_t>(b) * H + h) * n_kv_all + tile) * L::kScBytes,
+                    L::kScBytes, &r_full[slot]);
+      last[slot] = static_cast<int>(use & 1u);
+      ++li;
+      return true;
+    };
     for (int j = 0; j < n_kv && ok; ++j)
-      for (int i = 0; i < nt && ok; ++i) ok = load(&tk, key_tile(i, j));
+      for (int i = 0; i < nt && ok; ++i) ok = aux ? load4(key_tile(i, j)) : load(&tk, key_tile(i, j));
     for (int i = 0; i < nt && ok; ++i) ok = load(&tk, key_tile(i, 0));
     for (int j = 0; j < n_kv && ok; ++j) {
       for (int i = 0; i < nt && ok; ++i) ok = load(&tv, key_tile(i, j));
@@ -271,14 +304,47 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto release = [&](int base, int i) {
       if (per_pair || i == 1) umma_commit_w(&r_empty[tile_load(base, i) % kRing]);
     };
+    // Auxiliary output, pass 1: S on block-scaled FP4 UMMAs from the codes of Q~
+    // and K~.  Pass 1 only needs the row maxima, and the O and O_hp columns
+    // [256, 256 + 2 D) are not live yet, so they hold the scale operands: Q~'s at
+    // [256 + 4 kk), those of pass-1 load c at [264 + 8 (c % 4) + 4 kk).  A copy
+    // for load c comes after the release of S_i two steps earlier, so the load
+    // that used its region last (c - 4) has completed.
+    constexpr uint32_t idesc_s4 = idesc_mxf4nvf4(128, 128);
+    constexpr uint32_t lay4 = D == 128 ? 4u : 6u;  // (D/2)-byte swizzle of code rows
+    constexpr uint32_t sbo4 = 8u * (D / 2);
+    const uint32_t q4_addr = q_addr + L::kTileBytes;
+    auto issue_s4 = [&](int i, int idx) {
+      const uint32_t kb = ring_addr + (idx % kRing) * L::kTileBytes;
+      const uint32_t sc = 264u + 8u * static_cast<uint32_t>(idx % 4);
+#pragma unroll
+      for (int kk = 0; kk < D / 64; ++kk)
+        tmem_cp_32x128_x4_w(tmem + sc + 4 * kk, kb + L::kCodeBytes + kk * 512);
+#pragma unroll
+      for (int kk = 0; kk < D / 64; ++kk)
+        umma_fp4_ss_w(tmem + i * 128, sdesc(q4_addr + 32 * kk, 16, sbo4, lay4),
+                      sdesc(kb + 32 * kk, 16, sbo4, lay4), idesc_s4, tmem + 256 + 4 * kk,
+                      tmem + sc + 4 * kk, kk > 0 ? 1u : 0u);
+      umma_commit_w(&s_full[i]);
+    };
     bool ok = mbar_wait_warp(q_full, 0, abort);
+    if (aux && ok) {  // the Q~ scales stay in TMEM for pass 1
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < D / 64; ++kk)
+        tmem_cp_32x128_x4_w(tmem + 256 + 4 * kk, q4_addr + L::kCodeBytes + kk * 512);
+    }
     // pass 1: S_0(j), S_1(j) for the row maxima
     for (int j = 0; j < n_kv && ok; ++j, li += nt) {
       for (int i = 0; i < 2 && ok; ++i) {
         if ((per_pair || i == 0) && !(ok = wait_slot(tile_load(li, i)))) break;
         if (j > 0 && !(ok = mbar_wait_warp(&s_free[i], static_cast<uint32_t>((j - 1) & 1), abort))) break;
         tc_fence_after();
-        issue_s(i, tile_load(li, i));
+        if constexpr (aux) {
+          issue_s4(i, tile_load(li, i));
+        } else {
+          issue_s(i, tile_load(li, i));
+        }
         release(li, i);
       }
     }
@@ -491,8 +557,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int D, int kMode>
 cudaError_t launch_fwd_t(const AttnShape& s, const CUtensorMap& tq, const CUtensorMap& tk,
-                         const CUtensorMap& tv, void* o, void* o_hp, float* stats,
-                         const int* kv_list, int topk, int* err, cudaStream_t stream) {
+                         const CUtensorMap& tv, const CUtensorMap& tq4, const CUtensorMap& tk4,
+                         const uint8_t* q_sc, const uint8_t* k_sc, void* o, void* o_hp,
+                         float* stats, const int* kv_list, int topk, int* err,
+                         cudaStream_t stream) {
   using L = FwdLayout<D>;
   const int q_per_cta = (kMode == kAux ? 1 : 2) * kTile;
   const dim3 grid((s.Nq + q_per_cta - 1) / q_per_cta, s.H, s.B);
@@ -500,28 +568,37 @@ cudaError_t launch_fwd_t(const AttnShape& s, const CUtensorMap& tq, const CUtens
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
   attn_fwd_kernel<D, kMode><<<grid, kThreads, L::kAlloc, stream>>>(
-      tq, tk, tv, static_cast<__nv_bfloat16*>(o), static_cast<__nv_bfloat16*>(o_hp), stats, s.Nq,
+      tq, tk, tv, tq4, tk4, q_sc, k_sc, static_cast<__nv_bfloat16*>(o), static_cast<__nv_bfloat16*>(o_hp), stats, s.Nq,
       s.Nkv, s.H, s.scale, s.causal, kv_list, topk, err);
   return cudaGetLastError();
 }
 
 template <int D>
 cudaError_t launch_fwd_d(const AttnShape& s, const CUtensorMap& tq, const CUtensorMap& tk,
-                         const CUtensorMap& tv, void* o, void* o_hp, float* stats,
-                         const int* kv_list, int topk, int* err, cudaStream_t stream) {
+                         const CUtensorMap& tv, const CUtensorMap& tq4, const CUtensorMap& tk4,
+                         const uint8_t* q_sc, const uint8_t* k_sc, void* o, void* o_hp,
+                         float* stats, const int* kv_list, int topk, int* err,
+                         cudaStream_t stream) {
   if (kv_list != nullptr)
-    return launch_fwd_t<D, kSparse>(s, tq, tk, tv, o, o_hp, stats, kv_list, topk, err, stream);
+    return launch_fwd_t<D, kSparse>(s, tq, tk, tv, tq4, tk4, q_sc, k_sc, o, o_hp, stats, kv_list,
+                                    topk, err, stream);
   if (o_hp != nullptr)
-    return launch_fwd_t<D, kAux>(s, tq, tk, tv, o, o_hp, stats, kv_list, topk, err, stream);
+    return launch_fwd_t<D, kAux>(s, tq, tk, tv, tq4, tk4, q_sc, k_sc, o, o_hp, stats, kv_list,
+                                 topk, err, stream);
   return cudaErrorInvalidValue;  // dense: attn_fwd_fp4_kernel
 }
 
 cudaError_t launch_attn_fwd(const AttnShape& s, const CUtensorMap& tq, const CUtensorMap& tk,
-                            const CUtensorMap& tv, void* o, void* o_hp, float* stats,
-                            const int* kv_list, int topk, int* err, cudaStream_t stream) {
+                            const CUtensorMap& tv, const CUtensorMap& tq4, const CUtensorMap& tk4,
+                            const uint8_t* q_sc, const uint8_t* k_sc, void* o, void* o_hp,
+                            float* stats, const int* kv_list, int topk, int* err,
+                            cudaStream_t stream) {
   if ((kv_list != nullptr) == (o_hp != nullptr)) return cudaErrorInvalidValue;
-  return s.D == 128 ? launch_fwd_d<128>(s, tq, tk, tv, o, o_hp, stats, kv_list, topk, err, stream)
-                    : launch_fwd_d<64>(s, tq, tk, tv, o, o_hp, stats, kv_list, topk, err, stream);
+  if (o_hp != nullptr && (q_sc == nullptr || k_sc == nullptr)) return cudaErrorInvalidValue;
+  return s.D == 128 ? launch_fwd_d<128>(s, tq, tk, tv, tq4, tk4, q_sc, k_sc, o, o_hp, stats,
+                                        kv_list, topk, err, stream)
+                    : launch_fwd_d<64>(s, tq, tk, tv, tq4, tk4, q_sc, k_sc, o, o_hp, stats,
+                                       kv_list, topk, err, stream);
 }
 
 }  // namespace nvq
