@@ -862,6 +862,8 @@ def main(argv=None):
                     help="skip the measurement of the step with the auxiliary output")
     ap.add_argument("--quantizer-only", action="store_true",
                     help="time only the standalone quantizer (profiling of that kernel)")
+    ap.add_argument("--linear-only", action="store_true",
+                    help="time only the NVFP4 linear (profiling of its GEMMs)")
     ap.add_argument("--n", type=int, default=None,
                     help="override N (profiling of smaller cases; not the headline workload)")
     ap.add_argument("--heads", type=int, default=None, help="override H (profiling only)")
@@ -881,6 +883,14 @@ def main(argv=None):
         peaks, _ = load_peaks()
         print(json.dumps({"quantizer": quantizer_bench(peaks, torch.cuda.current_stream(),
                                                        iters=args.steps)}), flush=True)
+        return 0
+    if args.linear_only:
+        import torch
+        from nvfp4_fake_quant_gb300 import _lib
+        _lib.load()
+        peaks, _ = load_peaks()
+        print(json.dumps({"nvfp4_linear": linear_bench(peaks, torch.cuda.current_stream(),
+                                                       max(3, args.steps))}), flush=True)
         return 0
     return run_ours(args)
 

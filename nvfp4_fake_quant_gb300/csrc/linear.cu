@@ -51,31 +51,59 @@ __global__ void alpha_kernel(const float* gx, const float* gw, float* ab) {
   ab[0] = 1.0f / a;
 }
 
-// grad_b[n] = sum over m of grad[m, n] (bf16 in, fp32 sums, bf16 out).  Threads
-// of a block take consecutive columns (coalesced rows); blockIdx.y splits the
-// rows into chunks whose partial sums meet in fp32 scratch; the last chunk to
-// finish a column group writes the bf16 result.
+// grad_b[n] = sum over m of grad[m, n] (bf16 in, fp32 sums, bf16 out).  A
+// thread owns 8 consecutive columns (one 16-byte load per row) of a chunk of
+// rows (blockIdx.y) and keeps four rows' loads in flight; a block's threads
+// take consecutive column groups, so every row's loads are coalesced.  The
+// chunks' partial sums meet in fp32 scratch by atomics, and the last chunk to
+// finish a column group writes the bf16 result.  N % 8 == 0.
 __global__ void __launch_bounds__(256) bias_grad_kernel(const __nv_bfloat16* __restrict__ g,
                                                         int64_t M, int64_t N,
                                                         float* __restrict__ acc,
                                                         unsigned int* __restrict__ done,
                                                         __nv_bfloat16* __restrict__ gb) {
-  const int64_t n = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t c8 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) * 8;
   const int64_t chunk = (M + gridDim.y - 1) / gridDim.y;
   const int64_t m0 = blockIdx.y * chunk, m1 = m0 + chunk < M ? m0 + chunk : M;
-  if (n < N) {
-    float s = 0.f;
-    for (int64_t m = m0; m < m1; ++m) s += __bfloat162float(g[m * N + n]);
-    atomicAdd(&acc[n], s);
+  if (c8 < N) {
+    float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    const __nv_bfloat16* col = g + c8;
+    int64_t m = m0;
+    for (; m + 4 <= m1; m += 4) {
+      uint4 v[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) v[u] = __ldg(reinterpret_cast<const uint4*>(col + (m + u) * N));
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          s[2 * k] += __uint_as_float(w[k] << 16);
+          s[2 * k + 1] += __uint_as_float(w[k] & 0xFFFF0000u);
+        }
+      }
+    }
+    for (; m < m1; ++m) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(col + m * N));
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        s[2 * k] += __uint_as_float(w[k] << 16);
+        s[2 * k + 1] += __uint_as_float(w[k] & 0xFFFF0000u);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) atomicAdd(&acc[c8 + k], s[k]);
   }
   __threadfence();
   __syncthreads();
   __shared__ unsigned int last;
   if (threadIdx.x == 0) last = (atomicAdd(&done[blockIdx.x], 1u) == gridDim.y - 1) ? 1u : 0u;
   __syncthreads();
-  if (last && n < N) {
+  if (last && c8 < N) {
     __threadfence();
-    gb[n] = __float2bfloat16_rn(atomicAdd(&acc[n], 0.0f));
+#pragma unroll
+    for (int k = 0; k < 8; ++k) gb[c8 + k] = __float2bfloat16_rn(atomicAdd(&acc[c8 + k], 0.0f));
   }
 }
 
@@ -97,7 +125,11 @@ nvq_status cuda_st(const char* where, cudaError_t e) {
   return e == cudaSuccess ? NVQ_OK : nvq::fail_cuda(where, e);
 }
 
-size_t bwd_scratch(int64_t N) { return nvq::rup(static_cast<size_t>(N) * 4, 256) + nvq::rup(static_cast<size_t>((N + 255) / 256) * 4, 256); }
+// bias gradient scratch: fp32 sums [N] and one counter per block of 2048 columns
+size_t bwd_scratch(int64_t N) {
+  return nvq::rup(static_cast<size_t>(N) * 4, 256) +
+         nvq::rup(static_cast<size_t>((N + 2047) / 2048) * 4, 256);
+}
 
 }  // namespace
 
@@ -206,7 +238,7 @@ nvq_status nvfp4_linear_bwd(const void* grad_out, const void* x, const void* w, 
   if (ws == nullptr || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
     return NVQ_ERR_WORKSPACE;
   uint8_t* wb = static_cast<uint8_t*>(ws);
-  const int col_blocks = static_cast<int>((N + 255) / 256);
+  const int col_blocks = static_cast<int>((N + 2047) / 2048);  // 256 threads x 8 columns
   float* acc = reinterpret_cast<float*>(wb);
   unsigned int* done = reinterpret_cast<unsigned int*>(wb + nvq::rup(static_cast<size_t>(N) * 4, 256));
   cudaError_t e = cudaSuccess;
@@ -236,8 +268,9 @@ nvq_status nvfp4_linear_bwd(const void* grad_out, const void* x, const void* w, 
     int dev = 0, sms = 152;
     if (cudaGetDevice(&dev) == cudaSuccess)
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    // enough row chunks for about four blocks per SM, at least 32 rows each
     const int64_t chunks = std::max<int64_t>(
-        1, std::min<int64_t>((M + 63) / 64, (4 * static_cast<int64_t>(sms) + col_blocks - 1) / col_blocks));
+        1, std::min<int64_t>((M + 31) / 32, (4 * static_cast<int64_t>(sms) + col_blocks - 1) / col_blocks));
     e = nvq::timed(NVQ_KERNEL_LINEAR, stream, [&] {
       nvq::bias_grad_kernel<<<dim3(col_blocks, static_cast<unsigned>(std::min<int64_t>(chunks, 65535))),
                               256, 0, stream>>>(static_cast<const __nv_bfloat16*>(grad_out), M, N,

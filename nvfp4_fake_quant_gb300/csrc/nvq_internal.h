@@ -192,8 +192,8 @@ int make_codes_map(CUtensorMap* map, const void* base, int64_t rows, int64_t row
 cudaError_t launch_gemm_fp4(const CUtensorMap& tx, const CUtensorMap& tw, const uint8_t* sx,
                             const uint8_t* sw, const float* alpha, const void* bias, int64_t M,
                             int64_t N, int64_t K, void* out, int* err, cudaStream_t stream);
-// The same product for K <= 1536 (gemm_fp4_xres_kernel): clusters of four CTAs
-// keep their x tiles resident and share W tiles by multicast.  tx: x codes
+// The same product for K <= 1536 (gemm_fp4_xres_kernel): clusters of CTAs keep
+// their x tiles resident and share W tiles by multicast.  tx: x codes
 // (box 128 rows); tw32: w codes with a box of 32 rows; tout: out [M, N] bf16
 // (make_2d_map with 32-row boxes), written by TMA stores.
 cudaError_t launch_gemm_fp4_xres(const CUtensorMap& tx, const CUtensorMap& tw32,
