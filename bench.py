@@ -68,12 +68,8 @@ def kernel_work(kind, b, n, h, d):
 # (profiles/traffic_attn_kernels_wan25088.md), with the SHA-256 of the kernel's
 # sources at the time: a changed source reports null.
 TRAFFIC = {
-    "bwd_dkdv": {"bytes": 439465472, "sources": ['nvfp4_fake_quant_gb300/csrc/attn_bwd.cu', 'nvfp4_fake_quant_gb300/csrc/nvq_ptx.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_quant.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_internal.h'],
-                "sha256": "06550a8286468dea84648e0c7c58a21bd1e2ff7f8e40811b2aea9ad0bdff9e69"},
-    "bwd_dq": {"bytes": 350589952, "sources": ['nvfp4_fake_quant_gb300/csrc/attn_bwd_dq_fp4.cu', 'nvfp4_fake_quant_gb300/csrc/nvq_ptx.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_quant.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_internal.h'],
-              "sha256": "becd6cbc983ebb8d4bcbcf51586a160b801c48db4ae6bd534f1b55c7ae8144c1"},
-    "attn_fwd": {"bytes": 173405440, "sources": ['nvfp4_fake_quant_gb300/csrc/attn_fwd_fp4.cu', 'nvfp4_fake_quant_gb300/csrc/nvq_ptx.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_quant.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_internal.h'],
-                "sha256": "80e409674a3707b9119daa067d7c2cf661bedd636bedd4fdc0bb5d9641552e1e"},
+    "bwd_dkdv": {"bytes": 439484160, "sources": ['nvfp4_fake_quant_gb300/csrc/attn_bwd.cu', 'nvfp4_fake_quant_gb300/csrc/nvq_ptx.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_quant.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_internal.h'],
+                "sha256": "6f4fea45f8102c39c1776200066afc212b3097aa0ac340bc8fa00bed66ae2937"},
 }
 
 
