@@ -277,9 +277,9 @@ FwdWs fwd_ws(int B, int Nq, int Nkv, int H, int D) {
   return w;
 }
 
-// Backward workspace: Q~, K~, V~ (bf16) and delta; block-sparse (topk > 0):
-// the transposed tile lists; dense: the packed codes and scale blocks of Q~
-// and K~ for the FP4 S of the dQ kernel.
+// Backward workspace: Q~, K~, V~ (bf16), delta, the packed codes and scale
+// blocks of Q~ and K~ for the FP4 S of the dQ kernel; block-sparse (topk > 0):
+// also the transposed tile lists.
 struct BwdWs {
   size_t q, k, v, delta, q_off, q_list, qc, kc, qs, ks, total;
 };
@@ -289,19 +289,15 @@ BwdWs bwd_ws(int B, int Nq, int Nkv, int H, int D, int topk = 0) {
   w.k = round_up(w.q + bytes_bnhd(B, Nq, H, D, 2), 256);
   w.v = round_up(w.k + bytes_bnhd(B, Nkv, H, D, 2), 256);
   w.delta = round_up(w.v + bytes_bnhd(B, Nkv, H, D, 2), 256);
-  w.q_off = round_up(w.delta + static_cast<size_t>(B) * H * Nq * 4, 256);
-  w.q_list = w.q_off;
-  w.qc = w.kc = w.qs = w.ks = w.q_off;
-  w.total = w.q_off;
-  if (topk <= 0) {
-    w.qc = w.q_off;
-    w.kc = round_up(w.qc + bytes_bnhd(B, Nq, H, D, 1) / 2, 256);
-    w.qs = round_up(w.kc + bytes_bnhd(B, Nkv, H, D, 1) / 2, 256);
-    w.ks = round_up(w.qs + attn_fp4_scale_bytes(B, Nq, H, D), 256);
-    w.total = round_up(w.ks + attn_fp4_scale_bytes(B, Nkv, H, D), 256);
-  }
+  w.qc = round_up(w.delta + static_cast<size_t>(B) * H * Nq * 4, 256);
+  w.kc = round_up(w.qc + bytes_bnhd(B, Nq, H, D, 1) / 2, 256);
+  w.qs = round_up(w.kc + bytes_bnhd(B, Nkv, H, D, 1) / 2, 256);
+  w.ks = round_up(w.qs + attn_fp4_scale_bytes(B, Nq, H, D), 256);
+  w.total = round_up(w.ks + attn_fp4_scale_bytes(B, Nkv, H, D), 256);
+  w.q_off = w.q_list = w.total;
   if (topk > 0) {
     const size_t n_qt = (Nq + kTile - 1) / kTile, n_kt = (Nkv + kTile - 1) / kTile;
+    w.q_off = w.total;
     w.q_list = round_up(w.q_off + static_cast<size_t>(B) * H * (n_kt + 1) * 4, 256);
     w.total = round_up(w.q_list + static_cast<size_t>(B) * H * n_qt * topk * 4, 256);
   }
@@ -351,12 +347,11 @@ nvq_status fwd_impl(const void* q, const void* k, const void* v, int B, int Nq, 
   void* kb = wb + w.kb;
   void* vb = wb + w.vb;
   // Q~, K~, V~ in every form the forward and a later attn_qat_bwd_saved read
-  // (block-sparse: the bf16 Q~, K~ and f16 V~ its BF16-S kernels read)
+  // (block-sparse: all but the bf16 V~)
   const bool sparse = kv_list != nullptr;
-  const AttnOpSpec ops[3] = {
-      {q, Nq, sparse ? nullptr : qc, sparse ? nullptr : qs, qb, nullptr},
-      {k, Nkv, sparse ? nullptr : kc, sparse ? nullptr : ks, kb, nullptr},
-      {v, Nkv, nullptr, nullptr, sparse ? nullptr : vb, v16}};
+  const AttnOpSpec ops[3] = {{q, Nq, qc, qs, qb, nullptr},
+                             {k, Nkv, kc, ks, kb, nullptr},
+                             {v, Nkv, nullptr, nullptr, sparse ? nullptr : vb, v16}};
   if ((e = timed(NVQ_KERNEL_QUANTIZE, stream,
                  [&] { return launch_quant_attn_ops(ops, 3, B, H, D, stream); })) != cudaSuccess)
     return fail_cuda("quantize q, k, v", e);
@@ -370,25 +365,23 @@ nvq_status fwd_impl(const void* q, const void* k, const void* v, int B, int Nq, 
                        return launch_attn_fwd_fp4(s, mq, mk, mv, qs, ks, o, stats, err, stream);
                      }));
   }
-  CUtensorMap mq4, mk4;  // auxiliary output: codes of Q~, K~ for the FP4 pass 1
+  CUtensorMap mq4, mk4;  // codes of Q~, K~ for the FP4 pass 1
   if ((r = make_bnhd_map(&mq, qb, B, Nq, H, D, false)) != 0 ||
       (r = make_bnhd_map(&mk, kb, B, Nkv, H, D, false)) != 0 ||
       (r = make_bnhd_map(&mv, v16, B, Nkv, H, D, true)) != 0 ||
-      (!sparse && ((r = make_bnhd_u8_map(&mq4, qc, B, Nq, H, D)) != 0 ||
-                   (r = make_bnhd_u8_map(&mk4, kc, B, Nkv, H, D)) != 0)))
+      (r = make_bnhd_u8_map(&mq4, qc, B, Nq, H, D)) != 0 ||
+      (r = make_bnhd_u8_map(&mk4, kc, B, Nkv, H, D)) != 0)
     return fail_driver("cuTensorMapEncodeTiled", r);
-  if (sparse) mq4 = mk4 = mq;  // unused by the block-sparse form
   return from_cuda("attn_fwd", timed(NVQ_KERNEL_ATTN_FWD, stream, [&] {
-                     return launch_attn_fwd(s, mq, mk, mv, mq4, mk4, sparse ? nullptr : qs,
-                                            sparse ? nullptr : ks, o, o_hp, stats, kv_list, topk,
-                                            err, stream);
+                     return launch_attn_fwd(s, mq, mk, mv, mq4, mk4, qs, ks, o, o_hp, stats,
+                                            kv_list, topk, err, stream);
                    }));
 }
 
 // The backward's kernels on quantized operands already in device memory: qb,
-// kb, vb (bf16 Q~, K~, V~) and, dense, the codes and scale blocks of Q~ and K~
-// (qc, kc, qs, ks); kv_list, q_off, q_list for the block-sparse form; delta:
-// f32 [B, H, Nq] scratch.
+// kb, vb (bf16 Q~, K~, V~) and the codes and scale blocks of Q~ and K~ (qc, kc,
+// qs, ks); kv_list, q_off, q_list for the block-sparse form; delta: f32
+// [B, H, Nq] scratch.
 nvq_status bwd_kernels(const AttnShape& s, const void* qb, const void* kb, const void* vb,
                        const uint8_t* qc, const uint8_t* kc, const uint8_t* qs, const uint8_t* ks,
                        const void* o, const float* stats, const void* dout, const int* kv_list,
@@ -416,20 +409,15 @@ nvq_status bwd_kernels(const AttnShape& s, const void* qb, const void* kb, const
                                 n_qt * topk, err, stream);
        })) != cudaSuccess)
     return fail_cuda("attn_bwd (dK, dV)", e);
-  if (kv_list == nullptr) {
-    // dense: dQ with S on FP4 UMMAs over the codes and scale blocks of Q~, K~
-    CUtensorMap mq4, mk4;
-    if ((r = make_bnhd_u8_map(&mq4, qc, B, Nq, H, D)) != 0 ||
-        (r = make_bnhd_u8_map(&mk4, kc, B, Nkv, H, D)) != 0)
-      return fail_driver("cuTensorMapEncodeTiled", r);
-    return from_cuda("attn_bwd_dq", timed(NVQ_KERNEL_BWD_DQ, stream, [&] {
-                       return launch_attn_bwd_dq_fp4(s, mq4, mdo, mk4, mk, mv, qs, ks, stats,
-                                                     delta, dq, err, stream);
-                     }));
-  }
+  // dQ with S on FP4 UMMAs over the codes and scale blocks of Q~, K~ (every key
+  // tile, or the listed ones)
+  CUtensorMap mq4, mk4;
+  if ((r = make_bnhd_u8_map(&mq4, qc, B, Nq, H, D)) != 0 ||
+      (r = make_bnhd_u8_map(&mk4, kc, B, Nkv, H, D)) != 0)
+    return fail_driver("cuTensorMapEncodeTiled", r);
   return from_cuda("attn_bwd_dq", timed(NVQ_KERNEL_BWD_DQ, stream, [&] {
-                     return launch_attn_bwd_dq(s, mq, mdo, mk, mv, stats, delta, dq, kv_list, topk,
-                                               err, stream);
+                     return launch_attn_bwd_dq_fp4(s, mq4, mdo, mk4, mk, mv, qs, ks, stats, delta,
+                                                   dq, kv_list, topk, err, stream);
                    }));
 }
 
@@ -461,10 +449,10 @@ nvq_status bwd_impl(const void* q, const void* k, const void* v, const void* o,
   if (err == nullptr) return NVQ_ERR_CUDA;
   uint8_t* wb = static_cast<uint8_t*>(ws);
   const bool sparse = kv_list != nullptr;
-  uint8_t* qc = sparse ? nullptr : wb + w.qc;
-  uint8_t* kc = sparse ? nullptr : wb + w.kc;
-  uint8_t* qs = sparse ? nullptr : wb + w.qs;
-  uint8_t* ks = sparse ? nullptr : wb + w.ks;
+  uint8_t* qc = wb + w.qc;
+  uint8_t* kc = wb + w.kc;
+  uint8_t* qs = wb + w.qs;
+  uint8_t* ks = wb + w.ks;
   const AttnOpSpec ops[3] = {{q, Nq, qc, qs, wb + w.q, nullptr},
                              {k, Nkv, kc, ks, wb + w.k, nullptr},
                              {v, Nkv, nullptr, nullptr, wb + w.v, nullptr}};

@@ -1,8 +1,7 @@
 // Attn-QAT straight-through backward on sm_103a, dK/dV part (key-outer), and
 // the delta pre-pass.
 //
-// Kernels, in launch order (the dQ kernel follows them: attn_bwd_dq_fp4.cu for
-// the dense form, attn_bwd_dq.cu for the block-sparse one):
+// Kernels, in launch order (the dQ kernel, attn_bwd_dq_fp4.cu, follows them):
 //   bwd_prep    delta_i = sum_d dO_id * O_id (fp32)
 //   attn_bwd    one CTA per (128-key tile, head, batch); K~ and V~ stay in shared
 //               memory, the dK and dV accumulators in TMEM; the CTA loops over the

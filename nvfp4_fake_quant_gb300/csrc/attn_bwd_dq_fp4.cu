@@ -86,7 +86,9 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 
 // Grid: (ceil(Nq / 128), H, B).  tq4, tk4: packed codes of Q~, K~ (box of D/2
 // bytes x 128 rows); q_sc, k_sc: their scale blocks; tdo, tk, tv: bf16 dO, K~, V~.
-template <int D>
+// kSparse: the query tile's steps run over its listed key tiles
+// kv_list[b][h][qt][0..topk) instead of all of them.
+template <int D, bool kSparse>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_bwd_dq_fp4_kernel(const __grid_constant__ CUtensorMap tq4,
                            const __grid_constant__ CUtensorMap tdo,
@@ -96,7 +98,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                            const uint8_t* __restrict__ q_sc, const uint8_t* __restrict__ k_sc,
                            const float* __restrict__ stats, const float* __restrict__ delta,
                            __nv_bfloat16* __restrict__ dq, int Nq, int Nkv, int H, float scale,
-                           int causal, int* __restrict__ err) {
+                           int causal, const int* __restrict__ kv_list, int topk,
+                           int* __restrict__ err) {
   using L = DqLayout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023u) &
@@ -123,9 +126,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kAbort);
 
   const int n_all = (Nkv + kStep - 1) / kStep;
-  // steps: every key tile (causal: Nq == Nkv, kStep == kTile, up to the diagonal)
-  const int n = causal ? min(n_all, q0 / kStep + 1) : n_all;
   const int64_t bh = static_cast<int64_t>(b) * H + h;
+  // steps: every key tile (causal: Nq == Nkv, kStep == kTile, up to the
+  // diagonal), or the listed ones (block-sparse)
+  const int* list = kSparse ? kv_list + (bh * ((Nq + kTile - 1) / kTile) + qt) * topk : nullptr;
+  const int n = kSparse ? topk : causal ? min(n_all, q0 / kStep + 1) : n_all;
+  auto ktile = [&](int j) -> int { return kSparse ? list[j] : j; };
 
   if (threadIdx.x == 0) {
     *abort = 0;
@@ -189,9 +195,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t k4u = static_cast<uint32_t>(j / kK4Slots), vu = static_cast<uint32_t>(j / kVSlots);
       if (!(ok = mbar_wait_warp(&k4_empty[k4s], (k4u & 1u) ^ 1u, abort))) break;
       uint8_t* k4dst = smem + L::kK4 + k4s * L::kC4;
+      const int kt = ktile(j);
       mbar_arrive_expect_tx_w(&k4_full[k4s], L::kCodeBytes + L::kScBytes);
-      tma_load_4d_w(k4dst, &tk4, 0, j * kStep, h, b, &k4_full[k4s]);
-      bulk_load_w(k4dst + L::kCodeBytes, k_sc + (bh * n_kt + j) * L::kScBytes, L::kScBytes,
+      tma_load_4d_w(k4dst, &tk4, 0, kt * kStep, h, b, &k4_full[k4s]);
+      bulk_load_w(k4dst + L::kCodeBytes, k_sc + (bh * n_kt + kt) * L::kScBytes, L::kScBytes,
                   &k4_full[k4s]);
       last_k4[k4s] = static_cast<int>(k4u & 1u);
       if (!(ok = mbar_wait_warp(&v_empty[vs], (vu & 1u) ^ 1u, abort))) break;
@@ -199,14 +206,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int blk = 0; blk < D / 64; ++blk)
         tma_load_4d_w(smem + L::kV + vs * L::kTileBytes + blk * L::kBlock, &tv, blk * 64,
-                      j * kStep, h, b, &v_full[vs]);
+                      kt * kStep, h, b, &v_full[vs]);
       last_v[vs] = static_cast<int>(vu & 1u);
       if (!(ok = mbar_wait_warp(&k_empty[ks], (ku & 1u) ^ 1u, abort))) break;
       mbar_arrive_expect_tx_w(&k_full[ks], L::kTileBytes);
 #pragma unroll
       for (int blk = 0; blk < D / 64; ++blk)
         tma_load_4d_w(smem + L::kK + ks * L::kTileBytes + blk * L::kBlock, &tk, blk * 64,
-                      j * kStep, h, b, &k_full[ks]);
+                      kt * kStep, h, b, &k_full[ks]);
       last_k[ks] = static_cast<int>(ku & 1u);
     }
     if (!ok) {  // let the loads already issued land before the block exits
@@ -320,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     uint32_t rs[32], rd[32];
     for (int j = 0; j < n && ok; ++j) {
-      const int kt = j;
+      const int kt = ktile(j);
       const int key0 = kt * kStep + static_cast<int>(kc);
       const bool edge = !row_ok || (kt * kStep + kStep > Nkv) ||
                         (causal && kt * kStep + kStep - 1 > q0);
@@ -389,20 +396,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D>
+template <int D, bool kSparse>
 cudaError_t launch_dq4_t(const AttnShape& s, const CUtensorMap& tq4, const CUtensorMap& tdo,
                          const CUtensorMap& tk4, const CUtensorMap& tk, const CUtensorMap& tv,
                          const uint8_t* q_sc, const uint8_t* k_sc, const float* stats,
-                         const float* delta, void* dq, int* err, cudaStream_t stream) {
+                         const float* delta, void* dq, const int* kv_list, int topk, int* err,
+                         cudaStream_t stream) {
   using L = DqLayout<D>;
   static_assert(L::kAlloc <= 227u * 1024u, "shared memory");
   const dim3 grid((s.Nq + kTile - 1) / kTile, s.H, s.B);
-  cudaError_t e = cudaFuncSetAttribute(attn_bwd_dq_fp4_kernel<D>,
+  cudaError_t e = cudaFuncSetAttribute(attn_bwd_dq_fp4_kernel<D, kSparse>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
-  attn_bwd_dq_fp4_kernel<D><<<grid, kThreads, L::kAlloc, stream>>>(
+  attn_bwd_dq_fp4_kernel<D, kSparse><<<grid, kThreads, L::kAlloc, stream>>>(
       tq4, tdo, tk4, tk, tv, q_sc, k_sc, stats, delta, static_cast<__nv_bfloat16*>(dq), s.Nq,
-      s.Nkv, s.H, s.scale, s.causal, err);
+      s.Nkv, s.H, s.scale, s.causal, kv_list, topk, err);
   return cudaGetLastError();
 }
 
@@ -412,9 +420,13 @@ cudaError_t launch_attn_bwd_dq_fp4(const AttnShape& s, const CUtensorMap& tq4,
                                    const CUtensorMap& tdo, const CUtensorMap& tk4,
                                    const CUtensorMap& tk, const CUtensorMap& tv,
                                    const uint8_t* q_sc, const uint8_t* k_sc, const float* stats,
-                                   const float* delta, void* dq, int* err, cudaStream_t stream) {
-  return s.D == 128 ? launch_dq4_t<128>(s, tq4, tdo, tk4, tk, tv, q_sc, k_sc, stats, delta, dq, err, stream)
-                    : launch_dq4_t<64>(s, tq4, tdo, tk4, tk, tv, q_sc, k_sc, stats, delta, dq, err, stream);
+                                   const float* delta, void* dq, const int* kv_list, int topk,
+                                   int* err, cudaStream_t stream) {
+  if (kv_list != nullptr)
+    return s.D == 128 ? launch_dq4_t<128, true>(s, tq4, tdo, tk4, tk, tv, q_sc, k_sc, stats, delta, dq, kv_list, topk, err, stream)
+                      : launch_dq4_t<64, true>(s, tq4, tdo, tk4, tk, tv, q_sc, k_sc, stats, delta, dq, kv_list, topk, err, stream);
+  return s.D == 128 ? launch_dq4_t<128, false>(s, tq4, tdo, tk4, tk, tv, q_sc, k_sc, stats, delta, dq, nullptr, 0, err, stream)
+                    : launch_dq4_t<64, false>(s, tq4, tdo, tk4, tk, tv, q_sc, k_sc, stats, delta, dq, nullptr, 0, err, stream);
 }
 
 }  // namespace nvq

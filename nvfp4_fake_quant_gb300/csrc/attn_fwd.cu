@@ -57,20 +57,26 @@ constexpr int kPairWarps = 8;
 constexpr int kTmaWarp = 16;
 constexpr int kMmaWarp = 17;
 constexpr int kThreads = 576;
-constexpr int kRing = 5;  // K/V tile ring (K and V tiles interleave in pass 2)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint32_t kAtomBlock = 128u * 128u;  // bytes of one 64-column block of a 128-row tile
 constexpr int kDense = 0, kSparse = 1, kAux = 2;  // forward modes
 
-template <int D>
+// K/V tile ring (K and V tiles interleave in pass 2): 5 slots, 4 in the
+// block-sparse mode, whose two query tiles' FP4 codes take the room of the fifth.
+template <int D, int kMode>
 struct FwdLayout {
+  static constexpr int kRing = kMode == kSparse ? 4 : 5;
   static constexpr uint32_t kTileBytes = 128u * D * 2u;
   static constexpr uint32_t kCodeBytes = 128u * D / 2;      // E2M1 codes of a 128-row tile
   static constexpr uint32_t kScBytes = (D / 64) * 512u;     // their scale blocks
+  static constexpr uint32_t kC4 = (kCodeBytes + kScBytes + 1023u) / 1024u * 1024u;
   static constexpr uint32_t kQ = 0;                          // [2] query tiles
   static constexpr uint32_t kRingOff = kQ + 2u * kTileBytes;
   static constexpr uint32_t kX = kRingOff + kRing * kTileBytes;  // [2 tiles][128] f32
-  static constexpr uint32_t kBars = kX + 2u * 128u * 4u;
+  // codes + scale blocks of Q~ for the FP4 pass 1: block-sparse, one per query
+  // tile here; auxiliary output, in the unused second query-tile slot
+  static constexpr uint32_t kQ4s = kX + 1024u;
+  static constexpr uint32_t kBars = kQ4s + (kMode == kSparse ? 2u * kC4 : 0u);
   static constexpr uint32_t kNumBars = 1 + 2 * kRing + 2 * 4 + 1;
   static constexpr uint32_t kTmemSlot = kBars + kNumBars * 8u;
   static constexpr uint32_t kAbort = kTmemSlot + 4u;
@@ -101,12 +107,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr bool sparse = kMode == kSparse;
   constexpr bool aux = kMode == kAux;
   constexpr int kQTiles = aux ? 1 : 2;  // query tiles per CTA
-  using L = FwdLayout<D>;
+  using L = FwdLayout<D, kMode>;
+  constexpr int kRing = L::kRing;
+  constexpr bool fp4_pass1 = kMode == kSparse || kMode == kAux;  // pass-1 S on FP4 UMMAs
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023u) &
                                              ~static_cast<uintptr_t>(1023u));
   const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
   const int h = blockIdx.y, b = blockIdx.z;
   const int q0 = blockIdx.x * kQTiles * kTile;
 
@@ -189,22 +196,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tq);
     tma_prefetch_desc(&tk);
     tma_prefetch_desc(&tv);
-    mbar_arrive_expect_tx_w(q_full, static_cast<uint32_t>(kQTiles) * L::kTileBytes +
-                                        (aux ? L::kCodeBytes + L::kScBytes : 0u));
+    // Q~ codes and scale blocks for the FP4 S of pass 1 (a query tile past the
+    // last one, the missing second tile of the block-sparse mode, gets zero
+    // codes and no scales: its rows are never written)
+    const int qt0 = static_cast<int>(blockIdx.x) * kQTiles;
+    uint32_t q4_bytes = 0;
+    if constexpr (fp4_pass1)
+      for (int i = 0; i < kQTiles; ++i)
+        q4_bytes += L::kCodeBytes + (qt0 + i < n_qt ? L::kScBytes : 0u);
+    mbar_arrive_expect_tx_w(q_full, static_cast<uint32_t>(kQTiles) * L::kTileBytes + q4_bytes);
 #pragma unroll
     for (int i = 0; i < kQTiles; ++i)
 #pragma unroll
       for (int blk = 0; blk < D / 64; ++blk)
         tma_load_4d_w(smem + L::kQ + i * L::kTileBytes + blk * kAtomBlock, &tq, blk * 64,
                       q0 + i * kTile, h, b, q_full);
-    if constexpr (aux) {  // Q~ codes and scale blocks for the FP4 S of pass 1 (second Q slot)
+    if constexpr (fp4_pass1) {
       tma_prefetch_desc(&tq4);
       tma_prefetch_desc(&tk4);
-      uint8_t* q4 = smem + L::kQ + L::kTileBytes;
-      tma_load_4d_w(q4, &tq4, 0, q0, h, b, q_full);
-      bulk_load_w(q4 + L::kCodeBytes,
-                  q_sc + ((static_cast<int64_t>(b) * H + h) * n_qt + blockIdx.x) * L::kScBytes,
-                  L::kScBytes, q_full);
+      for (int i = 0; i < kQTiles; ++i) {
+        uint8_t* q4 = smem + (aux ? L::kQ + L::kTileBytes : L::kQ4s + i * L::kC4);
+        tma_load_4d_w(q4, &tq4, 0, q0 + i * kTile, h, b, q_full);
+        if (qt0 + i < n_qt)
+          bulk_load_w(q4 + L::kCodeBytes,
+                      q_sc + ((static_cast<int64_t>(b) * H + h) * n_qt + qt0 + i) * L::kScBytes,
+                      L::kScBytes, q_full);
+      }
     }
     int last[kRing];
     for (int s = 0; s < kRing; ++s) last[s] = -1;
@@ -223,9 +240,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++li;
       return true;
     };
-    // auxiliary output, pass 1: K~ as codes + scale blocks (a key tile past the
-    // last one, the missing odd tile of the last step, gets zero codes and no
-    // scales: its scores are masked)
+    // FP4 pass 1: K~ as codes + scale blocks (a key tile past the last one, the
+    // missing odd tile of the last step of the auxiliary-output mode, gets zero
+    // codes and no scales: its scores are masked)
     auto load4 = [&](int tile) -> bool {
       const int slot = li % kRing;
       const uint32_t use = static_cast<uint32_t>(li / kRing);
@@ -243,7 +260,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       return true;
     };
     for (int j = 0; j < n_kv && ok; ++j)
-      for (int i = 0; i < nt && ok; ++i) ok = aux ? load4(key_tile(i, j)) : load(&tk, key_tile(i, j));
+      for (int i = 0; i < nt && ok; ++i)
+        ok = fp4_pass1 ? load4(key_tile(i, j)) : load(&tk, key_tile(i, j));
     for (int i = 0; i < nt && ok; ++i) ok = load(&tk, key_tile(i, 0));
     for (int j = 0; j < n_kv && ok; ++j) {
       for (int i = 0; i < nt && ok; ++i) ok = load(&tv, key_tile(i, j));
@@ -304,35 +322,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto release = [&](int base, int i) {
       if (per_pair || i == 1) umma_commit_w(&r_empty[tile_load(base, i) % kRing]);
     };
-    // Auxiliary output, pass 1: S on block-scaled FP4 UMMAs from the codes of Q~
-    // and K~.  Pass 1 only needs the row maxima, and the O and O_hp columns
-    // [256, 256 + 2 D) are not live yet, so they hold the scale operands: Q~'s at
-    // [256 + 4 kk), those of pass-1 load c at [264 + 8 (c % 4) + 4 kk).  A copy
-    // for load c comes after the release of S_i two steps earlier, so the load
-    // that used its region last (c - 4) has completed.
+    // Pass 1 of the auxiliary-output and block-sparse modes: S on block-scaled
+    // FP4 UMMAs from the codes of Q~ and K~.  Pass 1 only needs the row maxima,
+    // and the O columns [256, 512) are not live yet, so they hold the scale
+    // operands: query tile qi's at [256 + 8 qi + 4 kk), those of pass-1 load c
+    // at [272 + 8 (c % 4) + 4 kk).  A copy for load c comes after the release of
+    // S_i two steps earlier, so the load that used its region last (c - 4) has
+    // completed.
     constexpr uint32_t idesc_s4 = idesc_mxf4nvf4(128, 128);
     constexpr uint32_t lay4 = D == 128 ? 4u : 6u;  // (D/2)-byte swizzle of code rows
     constexpr uint32_t sbo4 = 8u * (D / 2);
-    const uint32_t q4_addr = q_addr + L::kTileBytes;
+    auto q4_addr = [&](int qi) {
+      return smem_u32(smem + (aux ? L::kQ + L::kTileBytes : L::kQ4s + qi * L::kC4));
+    };
     auto issue_s4 = [&](int i, int idx) {
+      const int qi = aux ? 0 : i;  // query tile of S_i
       const uint32_t kb = ring_addr + (idx % kRing) * L::kTileBytes;
-      const uint32_t sc = 264u + 8u * static_cast<uint32_t>(idx % 4);
+      const uint32_t sc = 272u + 8u * static_cast<uint32_t>(idx % 4);
+      const uint32_t qa = q4_addr(qi);
 #pragma unroll
       for (int kk = 0; kk < D / 64; ++kk)
         tmem_cp_32x128_x4_w(tmem + sc + 4 * kk, kb + L::kCodeBytes + kk * 512);
 #pragma unroll
       for (int kk = 0; kk < D / 64; ++kk)
-        umma_fp4_ss_w(tmem + i * 128, sdesc(q4_addr + 32 * kk, 16, sbo4, lay4),
-                      sdesc(kb + 32 * kk, 16, sbo4, lay4), idesc_s4, tmem + 256 + 4 * kk,
-                      tmem + sc + 4 * kk, kk > 0 ? 1u : 0u);
+        umma_fp4_ss_w(tmem + i * 128, sdesc(qa + 32 * kk, 16, sbo4, lay4),
+                      sdesc(kb + 32 * kk, 16, sbo4, lay4), idesc_s4,
+                      tmem + 256 + 8 * qi + 4 * kk, tmem + sc + 4 * kk, kk > 0 ? 1u : 0u);
       umma_commit_w(&s_full[i]);
     };
     bool ok = mbar_wait_warp(q_full, 0, abort);
-    if (aux && ok) {  // the Q~ scales stay in TMEM for pass 1
+    if (fp4_pass1 && ok) {  // the Q~ scales stay in TMEM for pass 1
       tc_fence_after();
+      for (int qi = 0; qi < kQTiles; ++qi)
 #pragma unroll
-      for (int kk = 0; kk < D / 64; ++kk)
-        tmem_cp_32x128_x4_w(tmem + 256 + 4 * kk, q4_addr + L::kCodeBytes + kk * 512);
+        for (int kk = 0; kk < D / 64; ++kk)
+          tmem_cp_32x128_x4_w(tmem + 256 + 8 * qi + 4 * kk, q4_addr(qi) + L::kCodeBytes + kk * 512);
     }
     // pass 1: S_0(j), S_1(j) for the row maxima
     for (int j = 0; j < n_kv && ok; ++j, li += nt) {
@@ -340,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if ((per_pair || i == 0) && !(ok = wait_slot(tile_load(li, i)))) break;
         if (j > 0 && !(ok = mbar_wait_warp(&s_free[i], static_cast<uint32_t>((j - 1) & 1), abort))) break;
         tc_fence_after();
-        if constexpr (aux) {
+        if constexpr (fp4_pass1) {
           issue_s4(i, tile_load(li, i));
         } else {
           issue_s(i, tile_load(li, i));
@@ -561,7 +585,7 @@ cudaError_t launch_fwd_t(const AttnShape& s, const CUtensorMap& tq, const CUtens
                          const uint8_t* q_sc, const uint8_t* k_sc, void* o, void* o_hp,
                          float* stats, const int* kv_list, int topk, int* err,
                          cudaStream_t stream) {
-  using L = FwdLayout<D>;
+  using L = FwdLayout<D, kMode>;
   const int q_per_cta = (kMode == kAux ? 1 : 2) * kTile;
   const dim3 grid((s.Nq + q_per_cta - 1) / q_per_cta, s.H, s.B);
   cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D, kMode>,
@@ -594,7 +618,7 @@ cudaError_t launch_attn_fwd(const AttnShape& s, const CUtensorMap& tq, const CUt
                             float* stats, const int* kv_list, int topk, int* err,
                             cudaStream_t stream) {
   if ((kv_list != nullptr) == (o_hp != nullptr)) return cudaErrorInvalidValue;
-  if (o_hp != nullptr && (q_sc == nullptr || k_sc == nullptr)) return cudaErrorInvalidValue;
+  if (q_sc == nullptr || k_sc == nullptr) return cudaErrorInvalidValue;
   return s.D == 128 ? launch_fwd_d<128>(s, tq, tk, tv, tq4, tk4, q_sc, k_sc, o, o_hp, stats,
                                         kv_list, topk, err, stream)
                     : launch_fwd_d<64>(s, tq, tk, tv, tq4, tk4, q_sc, k_sc, o, o_hp, stats,

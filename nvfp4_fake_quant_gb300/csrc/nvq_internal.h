@@ -146,21 +146,16 @@ cudaError_t launch_attn_bwd(const AttnShape& s, const CUtensorMap& tq, const CUt
 // q_off [n_kt + 1] and ascending query tiles q_list [n_qt * topk].
 cudaError_t launch_tile_transpose(const int* kv_list, int B, int H, int n_qt, int n_kt, int topk,
                                   int* q_off, int* q_list, cudaStream_t stream);
-// block-sparse dQ with BF16 S (query-outer; Q~, dO, K~, V~ maps with 128-row boxes;
-// kv_list required: the dense form is launch_attn_bwd_dq_fp4)
-cudaError_t launch_attn_bwd_dq(const AttnShape& s, const CUtensorMap& tq, const CUtensorMap& tdo,
-                               const CUtensorMap& tk, const CUtensorMap& tv, const float* stats,
-                               const float* delta, void* dq, const int* kv_list, int topk,
-                               int* err, cudaStream_t stream);
-
-// dQ with S on FP4 UMMAs (dense): tq4, tk4 map the packed codes of Q~ and K~
+// dQ with S on FP4 UMMAs: tq4, tk4 map the packed codes of Q~ and K~
 // (make_bnhd_u8_map), q_sc, k_sc their scale blocks; tdo, tk, tv the bf16 dO,
-// K~, V~ (128-row boxes).
+// K~, V~ (128-row boxes).  kv_list: NULL (dense) or the block-sparse key-tile
+// lists [B, H, ceil(Nq/128), topk].
 cudaError_t launch_attn_bwd_dq_fp4(const AttnShape& s, const CUtensorMap& tq4,
                                    const CUtensorMap& tdo, const CUtensorMap& tk4,
                                    const CUtensorMap& tk, const CUtensorMap& tv,
                                    const uint8_t* q_sc, const uint8_t* k_sc, const float* stats,
-                                   const float* delta, void* dq, int* err, cudaStream_t stream);
+                                   const float* delta, void* dq, const int* kv_list, int topk,
+                                   int* err, cudaStream_t stream);
 
 // Token rows [B, T*Hh*W, H, D] (bf16) between raster and cube order.
 cudaError_t launch_vsa_reorder(const void* x, int B, int T, int Hh, int W, int H, int D, int ct,

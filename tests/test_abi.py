@@ -209,8 +209,9 @@ def test_block_sparse_and_vsa_calls_reject_bad_arguments(lib):
     n, h, d = 25088, 12, 128
     assert lib.vsa_select_workspace(1, n, h, d) == 2 * 12 * 196 * 128 * 4
     assert lib.vsa_select_workspace(1, n - 8, h, d) == 0
-    # Q~, K~, V~ (bf16) and delta as in the dense backward (without its FP4 operands)
-    common = 3 * n * h * d * 2 + h * n * 4
+    # the dense backward's workspace (Q~, K~, V~ bf16, delta, the FP4 operands of the
+    # dQ kernel) followed by the transposed tile lists
+    common = lib.attn_qat_bwd_workspace(1, n, n, h, d)
     offsets = (12 * 197 * 4 + 255) // 256 * 256  # [B, H, n_tiles + 1] int32, 256-byte aligned
     assert lib.attn_qat_bwd_sparse_workspace(1, n, h, d, 20) == common + offsets + 12 * 196 * 20 * 4
     big = 1 << 40
