@@ -317,13 +317,6 @@ nvq_status check_quant(const void* x, int64_t rows, int64_t cols, int64_t ld_x) 
 }
 
 }  // namespace
-// Whether the dense forward quantizes its query tiles inside the forward
-// kernel (the K/V quantizer pass then skips q) instead of in the quantizer pass.
-#ifndef NVQ_FUSE_Q
-#define NVQ_FUSE_Q 0
-#endif
-constexpr bool kFuseQForward = NVQ_FUSE_Q != 0;
-
 // Forward; kv_list: NULL (dense) or the block-sparse key-tile lists (validated
 // by the caller); o_hp: NULL or the auxiliary high-precision output (not with
 // kv_list).
@@ -356,27 +349,20 @@ nvq_status fwd_impl(const void* q, const void* k, const void* v, int B, int Nq, 
   // Q~, K~, V~ in every form the forward and a later attn_qat_bwd_saved read
   // (block-sparse: all but the bf16 V~)
   const bool sparse = kv_list != nullptr;
-  const bool dense = !sparse && o_hp == nullptr;
-  // dense forward with kFuseQForward: the forward kernel quantizes Q itself
-  const bool fuse_q = dense && kFuseQForward;
-  const AttnOpSpec ops[3] = {{k, Nkv, kc, ks, kb, nullptr},
-                             {v, Nkv, nullptr, nullptr, sparse ? nullptr : vb, v16},
-                             {q, Nq, qc, qs, qb, nullptr}};
-  if ((e = timed(NVQ_KERNEL_QUANTIZE, stream, [&] {
-         return launch_quant_attn_ops(ops, fuse_q ? 2 : 3, B, H, D, stream);
-       })) != cudaSuccess)
+  const AttnOpSpec ops[3] = {{q, Nq, qc, qs, qb, nullptr},
+                             {k, Nkv, kc, ks, kb, nullptr},
+                             {v, Nkv, nullptr, nullptr, sparse ? nullptr : vb, v16}};
+  if ((e = timed(NVQ_KERNEL_QUANTIZE, stream,
+                 [&] { return launch_quant_attn_ops(ops, 3, B, H, D, stream); })) != cudaSuccess)
     return fail_cuda("quantize q, k, v", e);
-  if (dense) {
+  if (!sparse && o_hp == nullptr) {
     // dense: S on FP4 UMMAs, Q~ and K~ as codes + scale blocks
-    CUtensorMap mq16;
     if ((r = make_bnhd_u8_map(&mq, qc, B, Nq, H, D)) != 0 ||
         (r = make_bnhd_u8_map(&mk, kc, B, Nkv, H, D)) != 0 ||
-        (r = make_bnhd_map(&mv, v16, B, Nkv, H, D, true)) != 0 ||
-        (fuse_q && (r = make_bnhd_map(&mq16, q, B, Nq, H, D, false)) != 0))
+        (r = make_bnhd_map(&mv, v16, B, Nkv, H, D, true)) != 0)
       return fail_driver("cuTensorMapEncodeTiled", r);
     return from_cuda("attn_fwd", timed(NVQ_KERNEL_ATTN_FWD, stream, [&] {
-                       return launch_attn_fwd_fp4(s, mq, mk, mv, fuse_q ? &mq16 : nullptr, qs, ks,
-                                                  qc, qs, qb, o, stats, err, stream);
+                       return launch_attn_fwd_fp4(s, mq, mk, mv, qs, ks, o, stats, err, stream);
                      }));
   }
   CUtensorMap mq4, mk4;  // codes of Q~, K~ for the FP4 pass 1

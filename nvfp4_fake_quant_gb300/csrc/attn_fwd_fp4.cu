@@ -87,30 +87,22 @@ struct Fp4Layout {
   static constexpr uint32_t kX = kVRingOff + kVRing * kVSlot;  // [4 warpgroups][128] f32
   static constexpr uint32_t kBars = kX + 4u * 128u * 4u;
   // q_full, k_full/k_empty, v_full/v_empty, s1_full[12], s1_free[6], pass1_done,
-  // s_full[2], p_full[2], pv_done[2], o_full, drain x2, q_sc_ready, q_ready
-  static constexpr uint32_t kNumBars = 1 + 2 * kKRing + 2 * kVRing + 12 + 6 + 1 + 6 + 4 + 1;
+  // s_full[2], p_full[2], pv_done[2], o_full, drain x2, q_sc_ready
+  static constexpr uint32_t kNumBars = 1 + 2 * kKRing + 2 * kVRing + 12 + 6 + 1 + 6 + 4;
   static constexpr uint32_t kTmemSlot = kBars + kNumBars * 8u;
   static constexpr uint32_t kAbort = kTmemSlot + 4u;
   static constexpr uint32_t kAlloc = kAbort + 4u + 1024u;
 };
 
 // Grid: (ceil(Nq / 128), H, B).
-// kFuseQ: the CTA quantizes its own query tile.  tq16 maps q (bf16, 128-row
-// boxes); the tile is staged through V~ ring slot 0 (first filled after every
-// pass-1 K~ load, and only after the softmax warps have read the tile), and
-// the softmax warps write its codes and scale block into shared memory in the
-// layout the TMA load of the codes would have written (the (D/2)-byte swizzle),
-// and into the workspace (q_codes, q_scales, q_bf16) for the backward.
-template <int D, bool kFuseQ>
+template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_fp4_kernel(const __grid_constant__ CUtensorMap tq,
                         const __grid_constant__ CUtensorMap tk,
-                        const __grid_constant__ CUtensorMap tv,
-                        const __grid_constant__ CUtensorMap tq16, const uint8_t* __restrict__ q_sc,
-                        const uint8_t* __restrict__ k_sc, uint8_t* __restrict__ q_codes_out,
-                        uint8_t* __restrict__ q_sc_out, __nv_bfloat16* __restrict__ q_bf16_out,
-                        __nv_bfloat16* __restrict__ o, float* __restrict__ stats, int Nq, int Nkv,
-                        int H, float scale, int causal, int* __restrict__ err) {
+                        const __grid_constant__ CUtensorMap tv, const uint8_t* __restrict__ q_sc,
+                        const uint8_t* __restrict__ k_sc, __nv_bfloat16* __restrict__ o,
+                        float* __restrict__ stats, int Nq, int Nkv, int H, float scale,
+                        int causal, int* __restrict__ err) {
   using L = Fp4Layout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023u) &
@@ -136,7 +128,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* o_full = pv_done + 2;
   uint64_t* drain = o_full + 1;          // [2]: S warp, PV warp
   uint64_t* q_sc_ready = drain + 2;
-  uint64_t* q_ready = q_sc_ready + 1;  // kFuseQ: the quantized query tile is in shared memory
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kAbort);
 
@@ -167,7 +158,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(o_full, 1);
     mbar_init(q_sc_ready, 1);
-    mbar_init(q_ready, kSoftmaxWarps);
     fence_mbar_init();
   }
   if (warp == kSWarp) {
@@ -237,18 +227,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tq);
     tma_prefetch_desc(&tk);
     tma_prefetch_desc(&tv);
-    if constexpr (kFuseQ) {  // the bf16 query tile, staged in V~ slot 0
-      tma_prefetch_desc(&tq16);
-      mbar_arrive_expect_tx_w(q_full, L::kVSlot);
-#pragma unroll
-      for (int blk = 0; blk < D / 64; ++blk)
-        tma_load_4d_w(smem + L::kVRingOff + blk * (128u * 128u), &tq16, blk * 64, q0, h, b, q_full);
-    } else {
-      mbar_arrive_expect_tx_w(q_full, L::kCodeBytes + L::kScBytes);
-      tma_load_4d_w(smem + L::kQ, &tq, 0, q0, h, b, q_full);
-      bulk_load_w(smem + L::kQ + L::kCodeBytes, q_sc + (bh * n_qt + qt) * L::kScBytes,
-                  L::kScBytes, q_full);
-    }
+    mbar_arrive_expect_tx_w(q_full, L::kCodeBytes + L::kScBytes);
+    tma_load_4d_w(smem + L::kQ, &tq, 0, q0, h, b, q_full);
+    bulk_load_w(smem + L::kQ + L::kCodeBytes, q_sc + (bh * n_qt + qt) * L::kScBytes, L::kScBytes,
+                q_full);
     int k_last[kKRing], v_last[kVRing];
     for (int s = 0; s < kKRing; ++s) k_last[s] = -1;
     for (int s = 0; s < kVRing; ++s) v_last[s] = -1;
@@ -282,7 +264,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     for (int j = 0; j < nk && ok; ++j) ok = load_k(j);
     for (int j = 0; j < 2 && j < nk && ok; ++j) ok = load_k(j);
-    if (kFuseQ && ok) ok = mbar_wait_warp(q_ready, 0, abort);  // V~ slot 0 read by the softmax
     for (int j = 0; j < nk && ok; ++j) {
       ok = load_v(j);
       if (ok && j + 2 < nk) ok = load_k(j + 2);
@@ -298,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kSWarp) {
     // ------------------------------------------------------------ S issuer
-    bool ok = mbar_wait_warp(kFuseQ ? q_ready : q_full, 0, abort);
+    bool ok = mbar_wait_warp(q_full, 0, abort);
     if (ok) {  // the Q~ scales stay in TMEM for the whole kernel
       tc_fence_after();
 #pragma unroll
@@ -364,48 +345,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto key0 = [&](int j) { return j * kTile + 32 * wg; };
     auto is_edge = [&](int k0) { return k0 + 32 > Nkv || (causal && k0 + 31 > q0); };
     bool ok = true;
-    if constexpr (kFuseQ) {
-      // quantize the staged query tile: 16-element block bi of the tile (row bi /
-      // (D/16)) per thread and step; the block decision is quant16_unit's, the
-      // same as the quantizer pass's
-      if ((ok = mbar_wait_warp(q_full, 0, abort))) {
-        constexpr int kBpr = D / 16;
-        for (int bi = threadIdx.x; bi < 128 * kBpr; bi += 32 * kSoftmaxWarps) {
-          const int rr = bi / kBpr, cb = bi % kBpr, c0 = 16 * cb;
-          const uint8_t* tile = smem + L::kVRingOff;
-          const uint4 lo = *reinterpret_cast<const uint4*>(tile + sw128_offset(rr, c0, 128));
-          const uint4 hi = *reinterpret_cast<const uint4*>(tile + sw128_offset(rr, c0 + 8, 128));
-          const uint32_t xv[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-          Q16 qq = quant16_unit<false>(xv);
-          code_signs(xv, qq.codes);
-          // codes: byte c0 / 2 of row rr, 16-byte chunks swizzled as the TMA load of
-          // the codes writes them (64-byte rows: chunk ^ ((rr / 2) % 4); 32-byte rows:
-          // chunk ^ ((rr / 4) % 2))
-          const uint32_t off = static_cast<uint32_t>(c0 / 2);
-          const uint32_t chunk = off >> 4;
-          const uint32_t phys =
-              D == 128 ? static_cast<uint32_t>(rr) * 64u + ((chunk ^ ((rr >> 1) & 3u)) << 4) + (off & 15u)
-                       : static_cast<uint32_t>(rr) * 32u + ((chunk ^ ((rr >> 2) & 1u)) << 4) + (off & 15u);
-          *reinterpret_cast<uint2*>(smem + L::kQ + phys) = make_uint2(qq.codes[0], qq.codes[1]);
-          const uint32_t sc_off = static_cast<uint32_t>(c0 / 64) * 512u + (rr & 31) * 16u +
-                                  (rr >> 5) * 4u + (cb & 3);
-          smem[L::kQ + L::kCodeBytes + sc_off] = static_cast<uint8_t>(qq.sbyte);
-          // the workspace copies the backward reads (rows past Nq: only their zero scales)
-          q_sc_out[(bh * n_qt + qt) * L::kScBytes + sc_off] = static_cast<uint8_t>(qq.sbyte);
-          const int grow = q0 + rr;
-          if (grow < Nq) {
-            const int64_t e0 = (static_cast<int64_t>(b) * Nq + grow) * H + h;
-            *reinterpret_cast<uint2*>(q_codes_out + e0 * (D / 2) + c0 / 2) =
-                make_uint2(qq.codes[0], qq.codes[1]);
-            uint4* dst = reinterpret_cast<uint4*>(q_bf16_out + e0 * D + c0);
-            dst[0] = make_uint4(qq.out[0], qq.out[1], qq.out[2], qq.out[3]);
-            dst[1] = make_uint4(qq.out[4], qq.out[5], qq.out[6], qq.out[7]);
-          }
-        }
-        fence_proxy_async_smem();  // the codes and scales feed tcgen05.cp and the UMMAs
-      }
-      mbar_arrive_warp(q_ready);
-    }
     float mraw = -INFINITY;
     uint32_t r[32];
     {
@@ -546,36 +485,29 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, bool kFuseQ>
+template <int D>
 cudaError_t launch_fp4_d(const AttnShape& s, const CUtensorMap& tq, const CUtensorMap& tk,
-                         const CUtensorMap& tv, const CUtensorMap& tq16, const uint8_t* q_sc,
-                         const uint8_t* k_sc, uint8_t* q_codes_out, uint8_t* q_sc_out,
-                         void* q_bf16_out, void* o, float* stats, int* err, cudaStream_t stream) {
+                         const CUtensorMap& tv, const uint8_t* q_sc, const uint8_t* k_sc, void* o,
+                         float* stats, int* err, cudaStream_t stream) {
   using L = Fp4Layout<D>;
   static_assert(L::kAlloc <= 227u * 1024u, "shared memory");
   const dim3 grid((s.Nq + kTile - 1) / kTile, s.H, s.B);
-  cudaError_t e = cudaFuncSetAttribute(attn_fwd_fp4_kernel<D, kFuseQ>,
+  cudaError_t e = cudaFuncSetAttribute(attn_fwd_fp4_kernel<D>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
-  attn_fwd_fp4_kernel<D, kFuseQ><<<grid, kThreads, L::kAlloc, stream>>>(
-      tq, tk, tv, tq16, q_sc, k_sc, q_codes_out, q_sc_out,
-      static_cast<__nv_bfloat16*>(q_bf16_out), static_cast<__nv_bfloat16*>(o), stats, s.Nq,
-      s.Nkv, s.H, s.scale, s.causal, err);
+  attn_fwd_fp4_kernel<D><<<grid, kThreads, L::kAlloc, stream>>>(
+      tq, tk, tv, q_sc, k_sc, static_cast<__nv_bfloat16*>(o), stats, s.Nq, s.Nkv, s.H, s.scale,
+      s.causal, err);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_attn_fwd_fp4(const AttnShape& s, const CUtensorMap& tq, const CUtensorMap& tk,
-                                const CUtensorMap& tv, const CUtensorMap* tq16,
-                                const uint8_t* q_sc, const uint8_t* k_sc, uint8_t* q_codes_out,
-                                uint8_t* q_sc_out, void* q_bf16_out, void* o, float* stats,
-                                int* err, cudaStream_t stream) {
-  if (tq16 != nullptr)
-    return s.D == 128 ? launch_fp4_d<128, true>(s, tq, tk, tv, *tq16, q_sc, k_sc, q_codes_out, q_sc_out, q_bf16_out, o, stats, err, stream)
-                      : launch_fp4_d<64, true>(s, tq, tk, tv, *tq16, q_sc, k_sc, q_codes_out, q_sc_out, q_bf16_out, o, stats, err, stream);
-  return s.D == 128 ? launch_fp4_d<128, false>(s, tq, tk, tv, tq, q_sc, k_sc, nullptr, nullptr, nullptr, o, stats, err, stream)
-                    : launch_fp4_d<64, false>(s, tq, tk, tv, tq, q_sc, k_sc, nullptr, nullptr, nullptr, o, stats, err, stream);
+                                const CUtensorMap& tv, const uint8_t* q_sc, const uint8_t* k_sc,
+                                void* o, float* stats, int* err, cudaStream_t stream) {
+  return s.D == 128 ? launch_fp4_d<128>(s, tq, tk, tv, q_sc, k_sc, o, stats, err, stream)
+                    : launch_fp4_d<64>(s, tq, tk, tv, q_sc, k_sc, o, stats, err, stream);
 }
 
 }  // namespace nvq
