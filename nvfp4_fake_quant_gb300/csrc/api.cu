@@ -404,17 +404,17 @@ nvq_status bwd_kernels(const AttnShape& s, const void* qb, const void* kb, const
       (e = launch_tile_transpose(kv_list, B, H, n_qt, n_kt, topk, q_off, q_list, stream)) !=
           cudaSuccess)
     return fail_cuda("tile_transpose", e);
-  if ((e = timed(NVQ_KERNEL_BWD_DKDV, stream, [&] {
-         return launch_attn_bwd(s, mq, mk, mv, mdo, stats, delta, dk, dv, q_off, q_list,
-                                n_qt * topk, err, stream);
-       })) != cudaSuccess)
-    return fail_cuda("attn_bwd (dK, dV)", e);
-  // dQ with S on FP4 UMMAs over the codes and scale blocks of Q~, K~ (every key
-  // tile, or the listed ones)
+  // both kernels form S on FP4 UMMAs from the codes and scale blocks of Q~, K~
   CUtensorMap mq4, mk4;
   if ((r = make_bnhd_u8_map(&mq4, qc, B, Nq, H, D)) != 0 ||
       (r = make_bnhd_u8_map(&mk4, kc, B, Nkv, H, D)) != 0)
     return fail_driver("cuTensorMapEncodeTiled", r);
+  if ((e = timed(NVQ_KERNEL_BWD_DKDV, stream, [&] {
+         return launch_attn_bwd(s, mq4, mk4, mq, mv, mdo, qs, ks, stats, delta, dk, dv, q_off,
+                                q_list, n_qt * topk, err, stream);
+       })) != cudaSuccess)
+    return fail_cuda("attn_bwd (dK, dV)", e);
+  // dQ (every key tile, or the listed ones)
   return from_cuda("attn_bwd_dq", timed(NVQ_KERNEL_BWD_DQ, stream, [&] {
                      return launch_attn_bwd_dq_fp4(s, mq4, mdo, mk4, mk, mv, qs, ks, stats, delta,
                                                    dq, kv_list, topk, err, stream);

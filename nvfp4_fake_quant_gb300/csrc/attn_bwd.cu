@@ -3,18 +3,18 @@
 //
 // Kernels, in launch order (the dQ kernel, attn_bwd_dq_fp4.cu, follows them):
 //   bwd_prep    delta_i = sum_d dO_id * O_id (fp32)
-//   attn_bwd    one CTA per (128-key tile, head, batch); K~ and V~ stay in shared
-//               memory, the dK and dV accumulators in TMEM; the CTA loops over the
-//               128-query tiles:
-//                 S  = Q~ K~^T, dP = dO V~^T              (BF16 UMMA -> TMEM)
-//                 P  = exp(scale*S - m)                    (m from the forward)
-//                 P~ = fq16(P) per 16 keys                 (the forward's code; S here
-//                                                           from BF16 UMMAs, the forward's
-//                                                           from FP4 ones: equal up to the
-//                                                           fp32 summation order)
+//   attn_bwd    one CTA per (128-key tile, head, batch); V~ and the K~ codes stay
+//               in shared memory, the dK and dV accumulators in TMEM; the CTA
+//               loops over the 128-query tiles i:
+//                 S  = Q~ K~^T          (block-scaled FP4 UMMA on the codes -> TMEM;
+//                                        the same exact products as the forward's)
+//                 P  = exp(scale*S - m) (m from the forward)
+//                 P~ = fq16(P) per 16 keys (the forward's code, bit for bit)
+//                 dP = dO V~^T          (BF16 UMMA -> TMEM, into S's buffer once S
+//                                        has been loaded)
 //                 A  = P / l,   dS = scale * A * (dP - delta)
-//                 P~/l and dS -> shared memory (bf16, one buffer used in turn)
-//                 dV += (P~/l)^T dO, dK += dS^T Q~         (BF16 UMMA)
+//                 P~/l and dS -> shared memory (bf16, a buffer each)
+//                 dV += (P~/l)^T dO, dK += dS^T Q~  (BF16 UMMA)
 //               then writes dK and dV (bf16).
 // ("attn_qat_train" API page, attn_qat_train(): the backward uses the quantized
 // Q, K, V and the quantized P, with straight-through gradients.)
@@ -23,11 +23,19 @@
 // (N/128) x |dQ| bytes through L2 reductions, which cost more than the extra
 // S and dP UMMAs of the second kernel.
 //
-// Roles (576 threads, one CTA per SM): warps 0-15 elementwise in four
-// warpgroups, each owning 32 keys of the tile (thread t = query row t = TMEM
-// lane t for S/dP, key row t for dK/dV), warp 16 TMA, warp 17 TMEM allocation
-// and UMMA issue.
-// TMEM columns: [0,128) S, [128,256) dP, [256,256+D) dV, [384,384+D) dK.
+// The elementwise work (exp, the P~ quantization, dS) is the critical path:
+// per tile it takes longer than the tensor pipe's 1664 cycles of products.
+// Shared memory (V~, K~ codes, 2 slots of Q~ codes, one bf16 Q~ slot for dK,
+// 2 dO slots, the P~ and dS buffers) is what lets P~_i and dS_i go out as soon
+// as each 32-key chunk is computed, without waiting for the products that read
+// the previous tile's buffers; S on FP4 codes is what frees the room for it.
+//
+// Roles (352 threads, one CTA per SM): warps 0-7 elementwise in two
+// warpgroups, each owning 64 keys of the tile (thread t = query row t = TMEM
+// lane t for S/dP, key row t for dK/dV); warp 8 TMA; warp 9 TMEM allocation and
+// the S and dP UMMAs; warp 10 the dV and dK UMMAs.
+// TMEM columns: [0,128) S and dP in turn, [128,136) K~ scales, [136,152) Q~
+// scales (2 slots), [256,256+D) dV, [384,384+D) dK.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -39,12 +47,18 @@ namespace nvq {
 
 namespace {
 
-constexpr int kElemWarps = 16;  // four elementwise warpgroups
-constexpr int kTmaWarp = 16;
-constexpr int kMmaWarp = 17;
-constexpr int kThreads = 576;
+constexpr int kElemWarps = 8;  // two elementwise warpgroups
+constexpr int kTmaWarp = 8;
+constexpr int kMmaWarp = 9;    // S, dP (the shared S/dP TMEM buffer); allocates TMEM
+constexpr int kGradWarp = 10;  // dV, dK
+constexpr int kThreads = 352;
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr uint32_t kAtomBlock = 128u * 128u;
+constexpr uint32_t kAtomBlock = 128u * 128u;  // 64-column block of a 128-row bf16 tile
+// TMEM columns
+constexpr uint32_t kColSP = 0;     // S_i, then dP_i, then S_{i+1} ... (one 128-column buffer)
+constexpr uint32_t kColScK = 128;  // K~ scale operand, 4 columns per 64 elements of D
+constexpr uint32_t kColScQ = 136;  // Q~ scale operands, 8 columns per slot, 2 slots
+constexpr uint32_t kColDV = 256, kColDK = 384;
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -57,30 +71,97 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// *p (0 where !pred), loaded where the call stands: as a volatile asm the load
+// stays ahead of the barrier waits that follow it instead of sinking to its
+// first use a tile later, so its latency hides behind a tile of work.
+__device__ __forceinline__ float ld_ahead(const float* p, bool pred) {
+  float v;
+  asm volatile(
+      "{\n\t.reg .pred q;\n\t"
+      "setp.ne.b32 q, %2, 0;\n\t"
+      "mov.b32 %0, 0;\n\t"
+      "@q ld.global.nc.f32 %0, [%1];\n\t}"
+      : "=f"(v)
+      : "l"(p), "r"(static_cast<int>(pred))
+      : "memory");
+  return v;
+}
+
+// kSteps (4 or 8) kind::f16 UMMAs into one accumulator from a single asm block
+// and one elected lane: the first with the given accumulate flag, the rest
+// accumulating; the caller computes the (warp-uniform) descriptors.  The UMMA
+// warp shares its sub-partition's issue slots with elementwise warps, and one
+// block takes far fewer of them than kSteps separate elect-and-issue sequences.
+template <int kSteps>
+__device__ __forceinline__ void umma_f16_steps_w(uint32_t d, const uint64_t* ad, const uint64_t* bd,
+                                                 uint32_t idesc, uint32_t acc) {
+  static_assert(kSteps == 4 || kSteps == 8, "4 or 8 K steps");
+  if constexpr (kSteps == 8) {
+    asm volatile(
+        "{\n\t.reg .pred p, e, t;\n\t"
+        "setp.ne.b32 p, %2, 0;\n\t"
+        "setp.eq.u32 t, 0, 0;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %11, %1, p;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %12, %1, t;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %13, %1, t;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %6, %14, %1, t;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %7, %15, %1, t;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %8, %16, %1, t;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %9, %17, %1, t;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %10, %18, %1, t;\n\t}" ::"r"(d),
+        "r"(idesc), "r"(acc), "l"(ad[0]), "l"(ad[1]), "l"(ad[2]), "l"(ad[3]), "l"(ad[4]),
+        "l"(ad[5]), "l"(ad[6]), "l"(ad[7]), "l"(bd[0]), "l"(bd[1]), "l"(bd[2]), "l"(bd[3]),
+        "l"(bd[4]), "l"(bd[5]), "l"(bd[6]), "l"(bd[7])
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p, e, t;\n\t"
+        "setp.ne.b32 p, %2, 0;\n\t"
+        "setp.eq.u32 t, 0, 0;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %7, %1, p;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %8, %1, t;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %9, %1, t;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %6, %10, %1, t;\n\t}" ::"r"(d),
+        "r"(idesc), "r"(acc), "l"(ad[0]), "l"(ad[1]), "l"(ad[2]), "l"(ad[3]), "l"(bd[0]),
+        "l"(bd[1]), "l"(bd[2]), "l"(bd[3])
+        : "memory");
+  }
+}
+
 template <int D>
 struct BwdLayout {
-  static constexpr uint32_t kTileBytes = 128u * D * 2u;
-  static constexpr uint32_t kK = 0;
-  static constexpr uint32_t kV = kK + kTileBytes;
-  static constexpr uint32_t kQ = kV + kTileBytes;        // [2] stages
-  static constexpr uint32_t kDO = kQ + 2u * kTileBytes;  // [2] stages
-  static constexpr uint32_t kPD = kDO + 2u * kTileBytes; // P~/l, then dS: [128 q][128 keys] bf16
-  static constexpr uint32_t kBars = kPD + 128u * 128u * 2u;
-  static constexpr uint32_t kNumBars = 16;
-  static constexpr uint32_t kStats = kBars + kNumBars * 8u;  // unused padding slot
-  static constexpr uint32_t kTmemSlot = kStats + 8u;
+  static constexpr uint32_t kTileBytes = 128u * D * 2u;  // a bf16 128-row tile
+  static constexpr uint32_t kCodeBytes = 128u * D / 2;   // E2M1 codes of a 128-row tile
+  static constexpr uint32_t kScBytes = (D / 64) * 512u;  // its scale blocks
+  static constexpr uint32_t kC4 = (kCodeBytes + kScBytes + 1023u) / 1024u * 1024u;
+  static constexpr uint32_t kV = 0;                          // V~ (bf16)
+  static constexpr uint32_t kK4 = kV + kTileBytes;           // K~ codes + scales
+  static constexpr uint32_t kQ4 = kK4 + kC4;                 // [2] Q~ codes + scales
+  static constexpr uint32_t kQB = kQ4 + 2u * kC4;            // bf16 Q~ (for dK)
+  static constexpr uint32_t kDO = kQB + kTileBytes;          // [2] dO
+  static constexpr uint32_t kP = kDO + 2u * kTileBytes;      // P~/l [128 q][128 keys] bf16
+  static constexpr uint32_t kDS = kP + 128u * 128u * 2u;     // dS, the same layout
+  static constexpr uint32_t kBars = kDS + 128u * 128u * 2u;
+  static constexpr uint32_t kNumBars = 24;
+  static constexpr uint32_t kTmemSlot = kBars + kNumBars * 8u;
   static constexpr uint32_t kAbort = kTmemSlot + 4u;
   static constexpr uint32_t kUsed = kAbort + 4u;
-  static constexpr uint32_t kAlloc =
-      (kUsed + 1024u) > 150u * 1024u ? (kUsed + 1024u) : 150u * 1024u;
+  static constexpr uint32_t kAlloc = kUsed + 1024u;
+  static_assert(kAlloc <= 232448u, "shared memory of one CTA");
 };
 
+// One CTA per (128-key tile, head, batch).  tq4, tk4: packed codes of Q~, K~
+// (box of D/2 bytes x 128 rows); q_sc, k_sc: their scale blocks per 128-row
+// tile; tq, tv, tdo: bf16 Q~, V~, dO (128-row boxes).
 template <int D, bool kSparse>
 __global__ void __launch_bounds__(kThreads, 1)
-    attn_bwd_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                    const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
-                    const float* __restrict__ stats, const float* __restrict__ delta,
-                    __nv_bfloat16* __restrict__ dk,
+    attn_bwd_kernel(const __grid_constant__ CUtensorMap tq4, const __grid_constant__ CUtensorMap tk4,
+                    const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tv,
+                    const __grid_constant__ CUtensorMap tdo, const uint8_t* __restrict__ q_sc,
+                    const uint8_t* __restrict__ k_sc, const float* __restrict__ stats,
+                    const float* __restrict__ delta, __nv_bfloat16* __restrict__ dk,
                     __nv_bfloat16* __restrict__ dv, int Nq, int Nkv, int H, float scale,
                     int causal, const int* __restrict__ q_off, const int* __restrict__ q_list,
                     int q_stride, int* __restrict__ err) {
@@ -89,26 +170,33 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023u) &
                                              ~static_cast<uintptr_t>(1023u));
   const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
   const int kt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int k0 = kt * kTile;
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBars);
-  uint64_t* kv_full = bars + 0;
-  uint64_t* qdo_full = bars + 1;   // [2]
-  uint64_t* qdo_empty = bars + 3;  // [2]
-  uint64_t* s_full = bars + 5;
-  uint64_t* dp_full = bars + 6;
-  uint64_t* pt_full = bars + 7;
-  uint64_t* pt_free = bars + 8;
-  uint64_t* ds_full = bars + 9;
-  uint64_t* ds_free = bars + 10;
-  uint64_t* dkdv_done = bars + 11;
-  uint64_t* mma_drain = bars + 12;
+  uint64_t* kv_full = bars + 0;    // V~, K~ codes and scales
+  uint64_t* q4_full = bars + 1;    // [2]
+  uint64_t* q4_empty = bars + 3;   // [2]
+  uint64_t* do_full = bars + 5;    // [2]
+  uint64_t* do_empty = bars + 7;   // [2]
+  uint64_t* qb_full = bars + 9;
+  uint64_t* qb_empty = bars + 10;
+  uint64_t* s_full = bars + 11;    // S_i in TMEM
+  uint64_t* s_free = bars + 12;    // every elementwise warp has loaded S_i
+  uint64_t* dp_full = bars + 13;   // dP_i in TMEM
+  uint64_t* dp_free = bars + 14;   // every elementwise warp has loaded dP_i
+  uint64_t* pt_full = bars + 15;   // P~_i/l stored
+  uint64_t* pt_free = bars + 16;   // dV += ... of tile i done
+  uint64_t* ds_full = bars + 17;   // dS_i stored
+  uint64_t* ds_free = bars + 18;   // dK += ... of tile i done
+  uint64_t* dkdv_done = bars + 19;
+  uint64_t* mma_drain = bars + 20;  // [2]: S/dP warp, dV/dK warp
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + L::kAbort);
 
   const int n_q_all = (Nq + kTile - 1) / kTile;
+  const int n_kt = (Nkv + kTile - 1) / kTile;
+  const int64_t bh = static_cast<int64_t>(b) * H + h;
   // query tiles of this key tile: all (dense; causal from the diagonal on, which
   // needs Nq == Nkv) or those whose block-sparse list holds it (q_off/q_list,
   // per (b, h): offsets [n_kt + 1] and query tiles in ascending order)
@@ -116,30 +204,34 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int* qsel = nullptr;
   int n_iter = n_q_all - i_begin;
   if (kSparse) {
-    const int n_kt = (Nkv + kTile - 1) / kTile;
-    const int64_t head = static_cast<int64_t>(b) * H + h;
-    const int* off = q_off + head * (n_kt + 1);
-    qsel = q_list + head * q_stride + off[kt];
+    const int* off = q_off + bh * (n_kt + 1);
+    qsel = q_list + bh * q_stride + off[kt];
     n_iter = off[kt + 1] - off[kt];
   }
   auto qtile = [&](int it) -> int { return kSparse ? qsel[it] : i_begin + it; };
-
 
   if (threadIdx.x == 0) {
     *abort = 0;
     mbar_init(kv_full, 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&qdo_full[s], 1);
-      mbar_init(&qdo_empty[s], 1);
+      mbar_init(&q4_full[s], 1);
+      mbar_init(&q4_empty[s], 1);
+      mbar_init(&do_full[s], 1);
+      mbar_init(&do_empty[s], 2);  // dP and dV both read dO
     }
+    mbar_init(qb_full, 1);
+    mbar_init(qb_empty, 1);
     mbar_init(s_full, 1);
+    mbar_init(s_free, kElemWarps);
     mbar_init(dp_full, 1);
+    mbar_init(dp_free, kElemWarps);
     mbar_init(pt_full, kElemWarps);
     mbar_init(pt_free, 1);
     mbar_init(ds_full, kElemWarps);
     mbar_init(ds_free, 1);
     mbar_init(dkdv_done, 1);
-    mbar_init(mma_drain, 1);
+    mbar_init(&mma_drain[0], 1);
+    mbar_init(&mma_drain[1], 1);
     fence_mbar_init();
   }
   if (warp == kMmaWarp) {
@@ -153,134 +245,212 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kTmaWarp) {
     // ------------------------------------------------------------ producer
+    // V~ and the K~ codes once; Q~ codes and dO one tile ahead of the UMMAs
+    // (two slots each); bf16 Q~ (one slot, read only by dK) for the current tile.
+    tma_prefetch_desc(&tq4);
+    tma_prefetch_desc(&tk4);
     tma_prefetch_desc(&tq);
-    tma_prefetch_desc(&tk);
     tma_prefetch_desc(&tv);
     tma_prefetch_desc(&tdo);
-    mbar_arrive_expect_tx_w(kv_full, 2u * L::kTileBytes);
+    mbar_arrive_expect_tx_w(kv_full, L::kTileBytes + L::kCodeBytes + L::kScBytes);
 #pragma unroll
-    for (int blk = 0; blk < D / 64; ++blk) {
-      tma_load_4d_w(smem + L::kK + blk * kAtomBlock, &tk, blk * 64, k0, h, b, kv_full);
+    for (int blk = 0; blk < D / 64; ++blk)
       tma_load_4d_w(smem + L::kV + blk * kAtomBlock, &tv, blk * 64, k0, h, b, kv_full);
-    }
-    int last[2] = {-1, -1};
+    tma_load_4d_w(smem + L::kK4, &tk4, 0, k0, h, b, kv_full);
+    bulk_load_w(smem + L::kK4 + L::kCodeBytes, k_sc + (bh * n_kt + kt) * L::kScBytes,
+                L::kScBytes, kv_full);
+    int last_q4[2] = {-1, -1}, last_do[2] = {-1, -1}, last_qb = -1;
     bool ok = true;
-    for (int it = 0; it < n_iter; ++it) {
+    auto load_q4_do = [&](int it) -> bool {  // Q~ codes and dO of tile it into slot it & 1
       const int st = it & 1;
-      if (!(ok = mbar_wait_warp(&qdo_empty[st], ((it >> 1) & 1) ^ 1, abort))) break;
-      const int qrow0 = qtile(it) * kTile;
-      mbar_arrive_expect_tx_w(&qdo_full[st], 2u * L::kTileBytes);
+      const uint32_t u = static_cast<uint32_t>((it >> 1) & 1);
+      const int qt = qtile(it);
+      if (!mbar_wait_warp(&q4_empty[st], u ^ 1u, abort)) return false;
+      uint8_t* q4dst = smem + L::kQ4 + st * L::kC4;
+      mbar_arrive_expect_tx_w(&q4_full[st], L::kCodeBytes + L::kScBytes);
+      tma_load_4d_w(q4dst, &tq4, 0, qt * kTile, h, b, &q4_full[st]);
+      bulk_load_w(q4dst + L::kCodeBytes, q_sc + (bh * n_q_all + qt) * L::kScBytes, L::kScBytes,
+                  &q4_full[st]);
+      last_q4[st] = static_cast<int>(u);
+      if (!mbar_wait_warp(&do_empty[st], u ^ 1u, abort)) return false;
+      mbar_arrive_expect_tx_w(&do_full[st], L::kTileBytes);
 #pragma unroll
-      for (int blk = 0; blk < D / 64; ++blk) {
-        tma_load_4d_w(smem + L::kQ + st * L::kTileBytes + blk * kAtomBlock, &tq, blk * 64, qrow0,
-                      h, b, &qdo_full[st]);
+      for (int blk = 0; blk < D / 64; ++blk)
         tma_load_4d_w(smem + L::kDO + st * L::kTileBytes + blk * kAtomBlock, &tdo, blk * 64,
-                      qrow0, h, b, &qdo_full[st]);
-      }
-      last[st] = (it >> 1) & 1;
-    }
-    if (!ok) {
-      mbar_wait_warp(kv_full, 0, nullptr, 10000000ull);
-      for (int s2 = 0; s2 < 2; ++s2)
-        if (last[s2] >= 0)
-          mbar_wait_warp(&qdo_full[s2], static_cast<uint32_t>(last[s2]), nullptr, 10000000ull);
-    }
-  } else if (warp == kMmaWarp) {
-    // ---------------------------------------------------------------- MMA
-    // Issue order per query tile i: dV_i, S_{i+1}, dK_i, dP_{i+1}, so the
-    // elementwise work of one tile overlaps the UMMAs of its neighbours.
-    constexpr uint32_t idesc_s = idesc_f16(128, 128, 1, 0, 0);  // S, dP
-    constexpr uint32_t idesc_t = idesc_f16(128, D, 1, 1, 1);    // dV, dK (A, B MN-major)
-    const uint32_t k_addr = smem_u32(smem + L::kK);
-    const uint32_t v_addr = smem_u32(smem + L::kV);
-    const uint32_t q_addr = smem_u32(smem + L::kQ);
-    const uint32_t do_addr = smem_u32(smem + L::kDO);
-    const uint32_t pd_addr = smem_u32(smem + L::kPD);
-    auto issue_s = [&](int st) {  // S = Q~_st K~^T -> TMEM [0,128)
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = (kk >> 2) * kAtomBlock + (kk & 3) * 32;
-        umma_f16_ss_w(tmem + 0, sdesc_sw128(q_addr + st * L::kTileBytes + off, 16, 1024),
-                      sdesc_sw128(k_addr + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
-      }
-      umma_commit_w(s_full);
+                      qt * kTile, h, b, &do_full[st]);
+      last_do[st] = static_cast<int>(u);
+      return true;
     };
-    auto issue_dp = [&](int st) {  // dP = dO_st V~^T -> TMEM [128,256)
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = (kk >> 2) * kAtomBlock + (kk & 3) * 32;
-        umma_f16_ss_w(tmem + 128, sdesc_sw128(do_addr + st * L::kTileBytes + off, 16, 1024),
-                      sdesc_sw128(v_addr + off, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
-      }
-      umma_commit_w(dp_full);
-    };
-    bool ok = mbar_wait_warp(kv_full, 0, abort) && (n_iter > 0) && mbar_wait_warp(&qdo_full[0], 0, abort);
-    if (ok) {
-      tc_fence_after();
-      issue_s(0);
-      issue_dp(0);
-    }
+    if (n_iter > 0) ok = load_q4_do(0);
     for (int it = 0; it < n_iter && ok; ++it) {
-      const int st = it & 1;
-      const uint32_t ph = static_cast<uint32_t>(it & 1);
-      if (!(ok = mbar_wait_warp(pt_full, ph, abort))) break;
-      tc_fence_after();
+      if (it + 1 < n_iter && !(ok = load_q4_do(it + 1))) break;
+      const uint32_t u = static_cast<uint32_t>(it & 1);
+      if (!(ok = mbar_wait_warp(qb_empty, u ^ 1u, abort))) break;
+      mbar_arrive_expect_tx_w(qb_full, L::kTileBytes);
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk)  // dV += (P~/l)^T dO: contraction over 128 queries
-        umma_f16_ss_w(tmem + 256, sdesc_sw128(pd_addr + kk * 2048, kAtomBlock, 1024),
-                      sdesc_sw128(do_addr + st * L::kTileBytes + kk * 2048, kAtomBlock, 1024),
-                      idesc_t, (it > 0 || kk > 0) ? 1u : 0u);
-      umma_commit_w(pt_free);
-      if (it + 1 < n_iter) {
-        if (!(ok = mbar_wait_warp(&qdo_full[st ^ 1], static_cast<uint32_t>(((it + 1) >> 1) & 1), abort)))
+      for (int blk = 0; blk < D / 64; ++blk)
+        tma_load_4d_w(smem + L::kQB + blk * kAtomBlock, &tq, blk * 64, qtile(it) * kTile, h, b,
+                      qb_full);
+      last_qb = static_cast<int>(u);
+    }
+    if (!ok) {  // let the loads already issued land before the block exits
+      mbar_wait_warp(kv_full, 0, nullptr, 10000000ull);
+      for (int s = 0; s < 2; ++s) {
+        if (last_q4[s] >= 0)
+          mbar_wait_warp(&q4_full[s], static_cast<uint32_t>(last_q4[s]), nullptr, 10000000ull);
+        if (last_do[s] >= 0)
+          mbar_wait_warp(&do_full[s], static_cast<uint32_t>(last_do[s]), nullptr, 10000000ull);
+      }
+      if (last_qb >= 0) mbar_wait_warp(qb_full, static_cast<uint32_t>(last_qb), nullptr, 10000000ull);
+    }
+  } else if (warp == kMmaWarp || warp == kGradWarp) {
+    // ---------------------------------------------------------------- MMA
+    // Two issuing warps, as each tcgen05 instruction and mbarrier wait costs
+    // its warp tens of cycles and one warp issuing all four products per tile
+    // was the critical path.  kMmaWarp: dP_i once the elementwise warps have
+    // loaded S_i, S_{i+1} once they have loaded dP_i (S and dP share one TMEM
+    // buffer); so dP_i runs while they turn S_i into P~_i, S_{i+1} while they
+    // turn dP_i into dS_i.  kGradWarp: dK_{i-1} once dS_{i-1} is stored, dV_i
+    // once P~_i is.  The two touch disjoint TMEM; dO's slot is released by
+    // both (dP and dV read it).
+    constexpr uint32_t idesc_s4 = idesc_mxf4nvf4(128, 128);     // S (FP4, N = 128 keys)
+    constexpr uint32_t idesc_p = idesc_f16(128, 128, 1, 0, 0);  // dP (N = 128 keys)
+    constexpr uint32_t idesc_t = idesc_f16(128, D, 1, 1, 1);    // dV, dK (A, B MN-major)
+    constexpr uint32_t lay = D == 128 ? 4u : 6u;                // (D/2)-byte swizzle of code rows
+    constexpr uint32_t sbo = 8u * (D / 2);
+    const uint32_t v_addr = smem_u32(smem + L::kV);
+    const uint32_t k4_addr = smem_u32(smem + L::kK4);
+    const uint32_t q4_addr = smem_u32(smem + L::kQ4);
+    const uint32_t qb_addr = smem_u32(smem + L::kQB);
+    const uint32_t do_addr = smem_u32(smem + L::kDO);
+    const uint32_t p_addr = smem_u32(smem + L::kP);
+    const uint32_t ds_addr = smem_u32(smem + L::kDS);
+    // S_{it} from slot it & 1: its Q~ scales go to TMEM first (their columns were
+    // last read by S_{it-2}, complete since dP_{it-1} was issued after S_{it-1}
+    // had been loaded)
+    auto issue_s = [&](int it) -> bool {
+      const int st = it & 1;
+      if (!mbar_wait_warp(&q4_full[st], static_cast<uint32_t>((it >> 1) & 1), abort)) return false;
+      tc_fence_after();
+      const uint32_t qa = q4_addr + st * L::kC4;
+      const uint32_t sc = kColScQ + 8u * static_cast<uint32_t>(st);
+#pragma unroll
+      for (int kk = 0; kk < D / 64; ++kk)
+        tmem_cp_32x128_x4_w(tmem + sc + 4 * kk, qa + L::kCodeBytes + kk * 512);
+#pragma unroll
+      for (int kk = 0; kk < D / 64; ++kk)
+        umma_fp4_ss_w(tmem + kColSP, sdesc(qa + 32 * kk, 16, sbo, lay),
+                      sdesc(k4_addr + 32 * kk, 16, sbo, lay), idesc_s4, tmem + sc + 4 * kk,
+                      tmem + kColScK + 4 * kk, kk > 0 ? 1u : 0u);
+      umma_commit_w(s_full);
+      umma_commit_w(&q4_empty[st]);
+      return true;
+    };
+    auto issue_dp = [&](int it) -> bool {  // dP = dO V~^T, contraction over D
+      const int st = it & 1;
+      if (!mbar_wait_warp(&do_full[st], static_cast<uint32_t>((it >> 1) & 1), abort)) return false;
+      tc_fence_after();
+      const uint32_t da = do_addr + st * L::kTileBytes;
+      uint64_t ad[D / 16], bd[D / 16];
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * kAtomBlock + (kk & 3) * 32;
+        ad[kk] = sdesc_sw128(da + off, 16, 1024);
+        bd[kk] = sdesc_sw128(v_addr + off, 16, 1024);
+      }
+      umma_f16_steps_w<D / 16>(tmem + kColSP, ad, bd, idesc_p, 0u);
+      umma_commit_w(dp_full);
+      return true;
+    };
+    // contraction over the 128 queries of a tile (MN-major operands)
+    auto issue_t = [&](uint32_t dcol, uint32_t a0, uint32_t b0, uint32_t acc) {
+      uint64_t ad[8], bd[8];
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        ad[kk] = sdesc_sw128(a0 + kk * 2048, kAtomBlock, 1024);
+        bd[kk] = sdesc_sw128(b0 + kk * 2048, kAtomBlock, 1024);
+      }
+      umma_f16_steps_w<8>(tmem + dcol, ad, bd, idesc_t, acc);
+    };
+    auto issue_dk = [&](int it) -> bool {  // dK += dS^T Q~
+      if (!mbar_wait_warp(ds_full, static_cast<uint32_t>(it & 1), abort) ||
+          !mbar_wait_warp(qb_full, static_cast<uint32_t>(it & 1), abort))
+        return false;
+      tc_fence_after();
+      issue_t(kColDK, ds_addr, qb_addr, it > 0 ? 1u : 0u);
+      umma_commit_w(ds_free);
+      umma_commit_w(qb_empty);
+      return true;
+    };
+    const int w = warp == kMmaWarp ? 0 : 1;
+    bool ok = true;
+    if (w == 0) {
+      ok = mbar_wait_warp(kv_full, 0, abort) && n_iter > 0;
+      if (ok) {  // the K~ scales stay in TMEM for the whole kernel
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 64; ++kk)
+          tmem_cp_32x128_x4_w(tmem + kColScK + 4 * kk, k4_addr + L::kCodeBytes + kk * 512);
+        ok = issue_s(0);
+      }
+      for (int it = 0; it < n_iter && ok; ++it) {
+        const uint32_t ph = static_cast<uint32_t>(it & 1);
+        if (!(ok = mbar_wait_warp(s_free, ph, abort))) break;
+        tc_fence_after();
+        if (!(ok = issue_dp(it))) break;
+        umma_commit_w(&do_empty[it & 1]);
+        if (it + 1 < n_iter) {
+          if (!(ok = mbar_wait_warp(dp_free, ph, abort))) break;
+          tc_fence_after();
+          if (!(ok = issue_s(it + 1))) break;
+        }
+      }
+    } else {
+      for (int it = 0; it < n_iter && ok; ++it) {
+        if (it > 0 && !(ok = issue_dk(it - 1))) break;
+        const int st = it & 1;
+        if (!(ok = mbar_wait_warp(pt_full, static_cast<uint32_t>(it & 1), abort)) ||
+            !(ok = mbar_wait_warp(&do_full[st], static_cast<uint32_t>((it >> 1) & 1), abort)))
           break;
         tc_fence_after();
-        issue_s(st ^ 1);  // S was read before pt_full_i
+        issue_t(kColDV, p_addr, do_addr + st * L::kTileBytes, it > 0 ? 1u : 0u);
+        umma_commit_w(pt_free);
+        umma_commit_w(&do_empty[st]);
       }
-      if (!(ok = mbar_wait_warp(ds_full, ph, abort))) break;
-      tc_fence_after();
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk)  // dK += dS^T Q~: contraction over 128 queries
-        umma_f16_ss_w(tmem + 384, sdesc_sw128(pd_addr + kk * 2048, kAtomBlock, 1024),
-                      sdesc_sw128(q_addr + st * L::kTileBytes + kk * 2048, kAtomBlock, 1024),
-                      idesc_t, (it > 0 || kk > 0) ? 1u : 0u);
-      umma_commit_w(ds_free);
-      umma_commit_w(&qdo_empty[st]);
-      if (it + 1 < n_iter) issue_dp(st ^ 1);  // dP was read before ds_full_i
+      if (ok && n_iter > 0 && (ok = issue_dk(n_iter - 1))) umma_commit_w(dkdv_done);
     }
-    if (ok && n_iter > 0) umma_commit_w(dkdv_done);
-    umma_commit_w(mma_drain);
-    mbar_wait_warp(mma_drain, 0, nullptr, 10000000ull);
+    umma_commit_w(&mma_drain[w]);
+    mbar_wait_warp(&mma_drain[w], 0, nullptr, 10000000ull);
   } else {
     // --------------------------------------------------------- elementwise
-    // Warpgroup g (0..3) owns keys [32g, 32g+32) of every tile; thread t of the
-    // group owns query row t (TMEM lane t).  dS is stored pre-multiplied by
+    // Warpgroup hg (0, 1) owns keys [64hg, 64hg+64) of every tile as two
+    // 32-key chunks; thread t of the group owns query row t (TMEM lane t).
+    // Each chunk's P~/l and dS go to shared memory as soon as they are
+    // computed (P~ and dS have a buffer each).  dS is stored pre-multiplied by
     // `scale`, so dK comes out scaled.
-    const int g = warp >> 2;
+    const int hg = warp >> 2;
     const int t = threadIdx.x & 127;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const float c1 = scale * kLog2e;
-    uint8_t* pd_smem = smem + L::kPD;
-    const float* lse_g = stats + (static_cast<int64_t>(b) * H + h) * 2 * Nq;
+    uint8_t* p_smem = smem + L::kP;
+    uint8_t* ds_smem = smem + L::kDS;
+    const float* lse_g = stats + bh * 2 * Nq;
     const float* m_g = lse_g + Nq;
-    const float* delta_g = delta + (static_cast<int64_t>(b) * H + h) * Nq;
-    const uint32_t key_col = static_cast<uint32_t>(g * 32);
+    const float* delta_g = delta + bh * Nq;
+    const uint32_t key_col = static_cast<uint32_t>(hg * 64);
     bool ok = true;
-    uint32_t r[32];
+    uint32_t r[2][32];
     // statistics of this thread's row, prefetched one tile ahead
     auto load_row = [&](int it, float& m, float& lse, float& dl) {
       const int qrow = (it < n_iter ? qtile(it) : 0) * kTile + t;
       const bool in = it < n_iter && qrow < Nq;
-      m = in ? m_g[qrow] : 0.f;
-      lse = in ? lse_g[qrow] : 0.f;
-      dl = in ? delta_g[qrow] : 0.f;
+      const int qr = in ? qrow : 0;
+      m = ld_ahead(m_g + qr, in);
+      lse = ld_ahead(lse_g + qr, in);
+      dl = ld_ahead(delta_g + qr, in);
     };
     float nm, nlse, ndl;
     load_row(0, nm, nlse, ndl);
-    // The dS stores of tile i are fenced and announced (ds_full) early in tile
-    // i+1, after S_{i+1} has been loaded, so the stores drain while the warp
-    // works instead of stalling it in the fence.
-    bool ds_pending = false;
     for (int it = 0; it < n_iter && ok; ++it) {
       const int qi = qtile(it);
       const int qrow = qi * kTile + t;
@@ -295,102 +465,99 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---- P part: S -> P, P~/l
       if (!(ok = mbar_wait_warp(s_full, ph, abort))) break;
       tc_fence_after();
-      float pp0[16], pp1[16];  // P (fp32) of this thread's 32 keys, for dS
-      {
-        tmem_ld32(tmem + lane_base + key_col, r);
-        tmem_wait_ld();
+      tmem_ld32(tmem + lane_base + kColSP + key_col, r[0]);
+      tmem_ld32(tmem + lane_base + kColSP + key_col + 32, r[1]);
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive_warp(s_free);
+      // the P~ buffer is free once dV of the previous tile is done
+      if (it > 0 && !(ok = mbar_wait_warp(pt_free, ph ^ 1u, abort))) break;
+      float pp[4][16];  // P (fp32) of this thread's 64 keys, for dS
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
         float x[32];
 #pragma unroll
         for (int i = 0; i < 16; ++i)
-          up2(fma2(pk2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), c12, nmb2),
+          up2(fma2(pk2(__uint_as_float(r[c][2 * i]), __uint_as_float(r[c][2 * i + 1])), c12, nmb2),
               x[2 * i], x[2 * i + 1]);
         if (edge) {
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            const int key = k0 + key_col + i;
+            const int key = k0 + key_col + 32 * c + i;
             if (!(row_ok && key < Nkv && (!causal || key <= qrow))) x[i] = -INFINITY;
           }
         }
-        if (ds_pending) {  // dS of the previous tile -> dK
-          tc_fence_before();
-          fence_proxy_async_smem();
-          mbar_arrive_warp(ds_full);
-          ds_pending = false;
-        }
-        uint32_t ptw0[8], ptw1[8];  // P~ / l as bf16x2
-        pquant16_scaled_bf16(x, inv_l, pp0, ptw0);
-        pquant16_scaled_bf16(x + 16, inv_l, pp1, ptw1);
-        tc_fence_before();
-        // the P~/dS buffer is free once dK of the previous tile is done
-        if (it > 0 && !(ok = mbar_wait_warp(ds_free, ph ^ 1u, abort))) break;
+        uint32_t ptw[2][8];  // P~ / l as bf16x2
+        pquant16_scaled_bf16(x, inv_l, pp[2 * c], ptw[0]);
+        pquant16_scaled_bf16(x + 16, inv_l, pp[2 * c + 1], ptw[1]);
 #pragma unroll
         for (int ch = 0; ch < 4; ++ch) {
-          const uint32_t* w = ch < 2 ? ptw0 + 4 * ch : ptw1 + 4 * (ch - 2);
-          const uint32_t off = sw128_offset(t, key_col + ch * 8, 128);
-          *reinterpret_cast<uint4*>(pd_smem + off) = make_uint4(w[0], w[1], w[2], w[3]);
+          const uint32_t* w = ptw[ch >> 1] + 4 * (ch & 1);
+          const uint32_t off = sw128_offset(t, key_col + 32 * c + ch * 8, 128);
+          *reinterpret_cast<uint4*>(p_smem + off) = make_uint4(w[0], w[1], w[2], w[3]);
         }
       }
-      // ---- dS part: dP -> dS = scale * A * (dP - delta), A = P / l
-      // The first dP load is issued before the P~ stores are fenced, so its
-      // latency overlaps their drain.
-      if (!(ok = mbar_wait_warp(dp_full, ph, abort))) break;
-      tc_fence_after();
-      uint32_t dsw[16];
-      uint32_t (&r16)[16] = *reinterpret_cast<uint32_t(*)[16]>(r);
-      tmem_ld16(tmem + lane_base + 128 + key_col, r16);
       fence_proxy_async_smem();
       mbar_arrive_warp(pt_full);
+      // ---- dS part: dP -> dS = scale * A * (dP - delta), A = P / l
+      if (!(ok = mbar_wait_warp(dp_full, ph, abort))) break;
+      tc_fence_after();
+      // dP one 32-key chunk at a time: the second load waits until the first
+      // chunk's P values are consumed, which keeps the register peak (all 64 P
+      // values and 64 dP values at once) under what 320 threads may hold
+      tmem_ld32(tmem + lane_base + kColSP + key_col, r[0]);
+      tmem_wait_ld();
+      // the dS buffer is free once dK of the previous tile is done
+      if (it > 0 && !(ok = mbar_wait_warp(ds_free, ph ^ 1u, abort))) break;
       {
-        // dP in two halves of 16 keys (P stays in fp32 registers meanwhile);
         // dS = P * (sl * dP - sl * delta) with sl = scale / l
         const float sl = scale * inv_l;
         const uint64_t sl2 = pk2(sl, sl), nsd2 = pk2(-sl * dl, -sl * dl);
 #pragma unroll
-        for (int hv = 0; hv < 2; ++hv) {
-          const float* pp = hv ? pp1 : pp0;
-          if (hv) tmem_ld16(tmem + lane_base + 128 + key_col + 16, r16);
-          tmem_wait_ld();
+        for (int q = 0; q < 4; ++q) {
+          if (q == 2) {
+            tmem_ld32(tmem + lane_base + kColSP + key_col + 32, r[0]);
+            tmem_wait_ld();
+            tc_fence_before();
+            mbar_arrive_warp(dp_free);
+          }
+          uint32_t dsw[8];
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
-            const uint64_t t2 = fma2(pk2(__uint_as_float(r16[2 * u]), __uint_as_float(r16[2 * u + 1])), sl2, nsd2);
+            const uint32_t* rr = r[0] + 16 * (q & 1);
+            const uint64_t t2 =
+                fma2(pk2(__uint_as_float(rr[2 * u]), __uint_as_float(rr[2 * u + 1])), sl2, nsd2);
             float d0, d1;
-            up2(mul2(pk2(pp[2 * u], pp[2 * u + 1]), t2), d0, d1);
-            dsw[8 * hv + u] = pack_bf16(d0, d1);
+            up2(mul2(pk2(pp[q][2 * u], pp[q][2 * u + 1]), t2), d0, d1);
+            dsw[u] = pack_bf16(d0, d1);
+          }
+#pragma unroll
+          for (int ch = 0; ch < 2; ++ch) {
+            const uint32_t off = sw128_offset(t, key_col + 16 * q + ch * 8, 128);
+            *reinterpret_cast<uint4*>(ds_smem + off) =
+                make_uint4(dsw[4 * ch], dsw[4 * ch + 1], dsw[4 * ch + 2], dsw[4 * ch + 3]);
           }
         }
       }
-      tc_fence_before();
-      if (!(ok = mbar_wait_warp(pt_free, ph, abort))) break;
-#pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        const uint32_t off = sw128_offset(t, key_col + ch * 8, 128);
-        *reinterpret_cast<uint4*>(pd_smem + off) =
-            make_uint4(dsw[4 * ch], dsw[4 * ch + 1], dsw[4 * ch + 2], dsw[4 * ch + 3]);
-      }
-      ds_pending = true;
-    }
-    if (ok && ds_pending) {
-      tc_fence_before();
       fence_proxy_async_smem();
       mbar_arrive_warp(ds_full);
     }
     if (ok && n_iter > 0 && (ok = mbar_wait_warp(dkdv_done, 0, abort))) {
       tc_fence_after();
-      // groups 0, 1 write dV; groups 2, 3 write dK (already scaled); each group
-      // D/2 columns; thread t = key row t
+      // group 0 writes dV, group 1 dK (already scaled); thread t = key row t
       const int key = k0 + t;
       const int64_t base = ((static_cast<int64_t>(b) * Nkv + key) * H + h) * D;
-      __nv_bfloat16* dst = (g < 2 ? dv : dk) + base + (g & 1) * (D / 2);
-      const uint32_t col = (g < 2 ? 256u : 384u) + static_cast<uint32_t>((g & 1) * (D / 2));
+      __nv_bfloat16* dst = (hg == 0 ? dv : dk) + base;
+      const uint32_t col = hg == 0 ? kColDV : kColDK;
 #pragma unroll
-      for (int c = 0; c < D / 64; ++c) {
-        tmem_ld32(tmem + lane_base + col + c * 32, r);
+      for (int c = 0; c < D / 32; ++c) {
+        tmem_ld32(tmem + lane_base + col + c * 32, r[0]);
         tmem_wait_ld();
         if (key < Nkv) {
           uint32_t w[16];
 #pragma unroll
           for (int u = 0; u < 16; ++u)
-            w[u] = pack_bf16(__uint_as_float(r[2 * u]), __uint_as_float(r[2 * u + 1]));
+            w[u] = pack_bf16(__uint_as_float(r[0][2 * u]), __uint_as_float(r[0][2 * u + 1]));
           uint4* pw = reinterpret_cast<uint4*>(dst + c * 32);
 #pragma unroll
           for (int u = 0; u < 4; ++u)
@@ -402,8 +569,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int key = k0 + t;
       if (key < Nkv) {
         const int64_t base = ((static_cast<int64_t>(b) * Nkv + key) * H + h) * D;
-        __nv_bfloat16* dst = (g < 2 ? dv : dk) + base + (g & 1) * (D / 2);
-        for (int c = 0; c < D / 2; c += 8)
+        __nv_bfloat16* dst = (hg == 0 ? dv : dk) + base;
+        for (int c = 0; c < D; c += 8)
           *reinterpret_cast<uint4*>(dst + c) = make_uint4(0, 0, 0, 0);
       }
     }
@@ -527,8 +694,9 @@ cudaError_t launch_bwd_prep(const AttnShape& s, const void* o, const void* dout,
 }
 
 template <int D, bool kSparse>
-cudaError_t launch_bwd_t(const AttnShape& s, const CUtensorMap& tq, const CUtensorMap& tk,
-                         const CUtensorMap& tv, const CUtensorMap& tdo, const float* stats,
+cudaError_t launch_bwd_t(const AttnShape& s, const CUtensorMap& tq4, const CUtensorMap& tk4,
+                         const CUtensorMap& tq, const CUtensorMap& tv, const CUtensorMap& tdo,
+                         const uint8_t* q_sc, const uint8_t* k_sc, const float* stats,
                          const float* delta, void* dk, void* dv, const int* q_off,
                          const int* q_list, int q_stride, int* err, cudaStream_t stream) {
   using L = BwdLayout<D>;
@@ -537,26 +705,24 @@ cudaError_t launch_bwd_t(const AttnShape& s, const CUtensorMap& tq, const CUtens
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
   attn_bwd_kernel<D, kSparse><<<grid, kThreads, L::kAlloc, stream>>>(
-      tq, tk, tv, tdo, stats, delta, static_cast<__nv_bfloat16*>(dk),
+      tq4, tk4, tq, tv, tdo, q_sc, k_sc, stats, delta, static_cast<__nv_bfloat16*>(dk),
       static_cast<__nv_bfloat16*>(dv), s.Nq, s.Nkv, s.H, s.scale, s.causal, q_off, q_list,
       q_stride, err);
   return cudaGetLastError();
 }
 
-cudaError_t launch_attn_bwd(const AttnShape& s, const CUtensorMap& tq, const CUtensorMap& tk,
-                            const CUtensorMap& tv, const CUtensorMap& tdo, const float* stats,
+cudaError_t launch_attn_bwd(const AttnShape& s, const CUtensorMap& tq4, const CUtensorMap& tk4,
+                            const CUtensorMap& tq, const CUtensorMap& tv, const CUtensorMap& tdo,
+                            const uint8_t* q_sc, const uint8_t* k_sc, const float* stats,
                             const float* delta, void* dk, void* dv, const int* q_off,
                             const int* q_list, int q_stride, int* err, cudaStream_t stream) {
   const bool sp = q_off != nullptr;
-  if (s.D == 128)
-    return sp ? launch_bwd_t<128, true>(s, tq, tk, tv, tdo, stats, delta, dk, dv, q_off, q_list,
-                                        q_stride, err, stream)
-              : launch_bwd_t<128, false>(s, tq, tk, tv, tdo, stats, delta, dk, dv, q_off, q_list,
-                                         q_stride, err, stream);
-  return sp ? launch_bwd_t<64, true>(s, tq, tk, tv, tdo, stats, delta, dk, dv, q_off, q_list,
-                                     q_stride, err, stream)
-            : launch_bwd_t<64, false>(s, tq, tk, tv, tdo, stats, delta, dk, dv, q_off, q_list,
-                                      q_stride, err, stream);
+  auto go = [&](auto fn) {
+    return fn(s, tq4, tk4, tq, tv, tdo, q_sc, k_sc, stats, delta, dk, dv, q_off, q_list, q_stride,
+              err, stream);
+  };
+  if (s.D == 128) return sp ? go(launch_bwd_t<128, true>) : go(launch_bwd_t<128, false>);
+  return sp ? go(launch_bwd_t<64, true>) : go(launch_bwd_t<64, false>);
 }
 
 }  // namespace nvq

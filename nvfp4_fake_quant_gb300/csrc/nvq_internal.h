@@ -138,8 +138,9 @@ cudaError_t launch_bwd_prep(const AttnShape& s, const void* o, const void* dout,
                             cudaStream_t stream);
 // dK, dV (key-outer; Q~, K~, V~, dO maps with 128-row boxes).  Block-sparse:
 // q_off/q_list from launch_tile_transpose (q_stride = n_qt * topk), else NULL.
-cudaError_t launch_attn_bwd(const AttnShape& s, const CUtensorMap& tq, const CUtensorMap& tk,
-                            const CUtensorMap& tv, const CUtensorMap& tdo, const float* stats,
+cudaError_t launch_attn_bwd(const AttnShape& s, const CUtensorMap& tq4, const CUtensorMap& tk4,
+                            const CUtensorMap& tq, const CUtensorMap& tv, const CUtensorMap& tdo,
+                            const uint8_t* q_sc, const uint8_t* k_sc, const float* stats,
                             const float* delta, void* dk, void* dv, const int* q_off,
                             const int* q_list, int q_stride, int* err, cudaStream_t stream);
 // Block-sparse lists [B, H, n_qt, topk] transposed to, per (b, h), offsets
