@@ -436,7 +436,8 @@ def quantizer_bench(peaks, stream, iters=20):
 def sparse_bench(peaks, stream, steps, warmup):
     """The block-sparse workload (Wan latent 16x28x56, B=1, H=12, D=128, 196 cubes
     of 4x4x8 tokens, top-20 key cubes per query cube): one step = raster -> cube
-    order of q, k, v, dO, block selection, sparse forward and backward, cube ->
+    order of q, k, v, dO, block selection, sparse forward and backward (from the
+    operands the forward saved), cube ->
     raster order of o, dq, dk, dv.  Counted FLOPs: forward 4*H*N*(20*128)*D,
     backward 2.5x that."""
     import torch
@@ -452,16 +453,17 @@ def sparse_bench(peaks, stream, steps, warmup):
     o, dq, dk, dv = (torch.empty_like(q) for _ in range(4))
     stats = torch.empty((b, h, 2, n), dtype=torch.float32, device=q.device)
     wsf = torch.empty(api.attn_qat_fwd_workspace(b, n, n, h, d), dtype=torch.uint8, device=q.device)
-    wsb = torch.empty(api.attn_qat_bwd_sparse_workspace(b, n, h, d, topk), dtype=torch.uint8,
-                      device=q.device)
+    wsb = torch.empty(api.attn_qat_bwd_sparse_saved_workspace(b, n, h, d, topk),
+                      dtype=torch.uint8, device=q.device)
 
     def step():
         for src, dst in ((q, qc), (k, kc), (v, vc), (do, doc)):
             api.vsa_reorder(src, grid, out=dst)
         tiles = api.vsa_select_tiles(qc, kc, topk)
         api.attn_qat_fwd_sparse(qc, kc, vc, tiles, inp.scale, o=o_c, stats=stats, workspace=wsf)
-        api.attn_qat_bwd_sparse(qc, kc, vc, o_c, stats, doc, tiles, inp.scale, dq=dq_c, dk=dk_c,
-                                dv=dv_c, workspace=wsb)
+        # the backward reads the quantized operands the forward left in wsf
+        api.attn_qat_bwd_sparse_saved(wsf, o_c, stats, doc, tiles, inp.scale, dq=dq_c, dk=dk_c,
+                                      dv=dv_c, workspace=wsb)
         for src, dst in ((o_c, o), (dq_c, dq), (dk_c, dk), (dv_c, dv)):
             api.vsa_reorder(src, grid, to_cubes=False, out=dst)
 

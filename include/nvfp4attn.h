@@ -167,11 +167,10 @@ size_t attn_qat_fwd_workspace(int B, int Nq, int Nkv, int H, int D);
  *   q_bf16, k_bf16, v_bf16  Q~, K~, V~ as bf16 [B, N, H, D]
  *   delta              f32 [B, H, Nq]: rowsum(dO * o) (backward only)
  *   total              the workspace size (*_workspace())
- * A region the workspace does not have is SIZE_MAX.  After attn_qat_fwd or
- * attn_qat_fwd_hp the forward workspace holds every region it has (all but
- * delta); after attn_qat_fwd_sparse only q_bf16, k_bf16 and v_f16.  After
- * attn_qat_bwd the backward workspace holds every region it has.  Other bytes
- * are unspecified.  NVQ_ERR_INVALID for sizes the calls reject or a NULL out.
+ * A region the workspace does not have is SIZE_MAX.  After attn_qat_fwd,
+ * attn_qat_fwd_hp or attn_qat_fwd_sparse the forward workspace holds every
+ * region it has (all but delta).  After attn_qat_bwd the backward workspace
+ * holds every region it has.  Other bytes are unspecified.  NVQ_ERR_INVALID for sizes the calls reject or a NULL out.
  */
 typedef struct {
   size_t q_codes, k_codes, q_scales, k_scales, v_f16, q_bf16, k_bf16, v_bf16, delta, total;
@@ -231,8 +230,8 @@ nvq_status attn_qat_bwd(const void* q, const void* k, const void* v, const void*
  *           aligned; saved_bytes >= attn_qat_fwd_workspace(B, Nq, Nkv, H, D)
  *   o, stats, dout, dq, dk, dv, sizes, scale, causal: as in attn_qat_bwd
  *   ws      attn_qat_bwd_saved_workspace(...) bytes (delta), 256-byte aligned
- * The gradients equal attn_qat_bwd's on the same inputs bit for bit.  Not for
- * the block-sparse forward, whose workspace lacks the codes.
+ * The gradients equal attn_qat_bwd's on the same inputs bit for bit.  After
+ * the block-sparse forward use attn_qat_bwd_sparse_saved.
  */
 size_t attn_qat_bwd_saved_workspace(int B, int Nq, int Nkv, int H, int D);
 nvq_status attn_qat_bwd_saved(const void* saved, size_t saved_bytes, const void* o,
@@ -324,6 +323,28 @@ nvq_status attn_qat_bwd_sparse(const void* q, const void* k, const void* v, cons
                                int topk, void* dq, void* dk, void* dv, int B, int N, int H, int D,
                                float scale, void* ws, size_t ws_bytes, nvq_stream_t stream);
 
+/*
+ * Block-sparse backward from the quantized operands attn_qat_fwd_sparse left in
+ * its workspace (as attn_qat_bwd_saved for the dense forward): no quantizer pass.
+ *   saved, saved_bytes   the workspace of an attn_qat_fwd_sparse call on the same
+ *                        q, k, v, sizes and kv_tiles, unmodified since (not
+ *                        checked: other bytes give wrong gradients, never
+ *                        out-of-bounds accesses); 256-byte aligned;
+ *                        saved_bytes >= attn_qat_fwd_workspace(B, N, N, H, D)
+ *   o, stats, dout, kv_tiles, topk, dq, dk, dv, sizes, scale: as in
+ *                        attn_qat_bwd_sparse
+ *   ws                   attn_qat_bwd_sparse_saved_workspace(...) bytes (delta
+ *                        and the transposed lists), 256-byte aligned
+ * The gradients equal attn_qat_bwd_sparse's on the same inputs bit for bit.
+ * NVQ_ERR_INVALID / NVQ_ERR_WORKSPACE as the other backward calls.
+ */
+size_t attn_qat_bwd_sparse_saved_workspace(int B, int N, int H, int D, int topk);
+nvq_status attn_qat_bwd_sparse_saved(const void* saved, size_t saved_bytes, const void* o,
+                                     const float* stats, const void* dout,
+                                     const int32_t* kv_tiles, int topk, void* dq, void* dk,
+                                     void* dv, int B, int N, int H, int D, float scale, void* ws,
+                                     size_t ws_bytes, nvq_stream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* NVFP4 linear ("nvfp4_qad.py": nvfp4_gemm and _NVFP4STE)                   */
 /* ------------------------------------------------------------------------ */
@@ -394,7 +415,7 @@ enum {
   NVQ_KERNEL_BWD_DKDV = 3,   /* backward, key-outer dK and dV kernel */
   NVQ_KERNEL_BWD_DQ = 4,     /* backward, query-outer dQ kernel */
   NVQ_KERNEL_GLOBAL_SF = 5,  /* static global scale (amax reduction and finalize) */
-  NVQ_KERNEL_VSA = 6,        /* block-sparse support: token reorder, block selection */
+  NVQ_KERNEL_VSA = 6,        /* block-sparse support: token reorder, block selection, list transpose */
   NVQ_KERNEL_LINEAR = 7,     /* NVFP4 linear: the FP4 and BF16 GEMMs and the bias gradient */
   NVQ_KERNEL_KINDS = 8
 };

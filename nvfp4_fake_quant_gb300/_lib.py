@@ -69,6 +69,11 @@ SIGNATURES = {
     "attn_qat_bwd_sparse": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                     c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_int, c_int,
                                     c_int, c_int, c_float, c_void_p, c_size_t, c_void_p]),
+    "attn_qat_bwd_sparse_saved_workspace": (c_size_t, [c_int, c_int, c_int, c_int, c_int]),
+    "attn_qat_bwd_sparse_saved": (c_int, [c_void_p, c_size_t, c_void_p, c_void_p, c_void_p,
+                                          c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_int,
+                                          c_int, c_int, c_int, c_float, c_void_p, c_size_t,
+                                          c_void_p]),
     "nvq_timing_enable": (c_int, [c_int]),
     "nvq_timing_read": (c_int, [c_int, c_void_p, c_void_p]),
     "nvq_selftest_umma": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int,

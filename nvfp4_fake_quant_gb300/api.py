@@ -453,6 +453,33 @@ def attn_qat_bwd_sparse(q, k, v, o, stats, do, kv_tiles, scale=None, dq=None, dk
     return dq, dk, dv
 
 
+def attn_qat_bwd_sparse_saved_workspace(b, n, h, d, topk) -> int:
+    return int(_lib.load().attn_qat_bwd_sparse_saved_workspace(b, n, h, d, topk))
+
+
+def attn_qat_bwd_sparse_saved(saved, o, stats, do, kv_tiles, scale=None, dq=None, dk=None,
+                              dv=None, workspace=None):
+    """Block-sparse backward from the quantized operands attn_qat_fwd_sparse left in
+    its workspace ``saved`` (same q, k, v and kv_tiles): (dq, dk, dv), equal to
+    attn_qat_bwd_sparse's bit for bit, without its quantizer pass."""
+    _check_bnhd(o, "o")
+    b, n, h, d = o.shape
+    _check_bnhd(do, "do", o.shape)
+    _check(stats, "stats", torch.float32)
+    _check(saved, "saved", torch.uint8)
+    _check_tiles(kv_tiles, b, h, n)
+    topk = kv_tiles.shape[-1]
+    scale = _scale(scale, d)
+    dq = torch.empty_like(o) if dq is None else dq
+    dk = torch.empty_like(o) if dk is None else dk
+    dv = torch.empty_like(o) if dv is None else dv
+    ws = _workspace(attn_qat_bwd_sparse_saved_workspace(b, n, h, d, topk), o.device, workspace)
+    _lib.call("attn_qat_bwd_sparse_saved", _ptr(saved), saved.numel(), _ptr(o), _ptr(stats),
+              _ptr(do), _ptr(kv_tiles), topk, _ptr(dq), _ptr(dk), _ptr(dv), b, n, h, d, scale,
+              _ptr(ws), ws.numel() * ws.element_size(), _stream_ptr(o))
+    return dq, dk, dv
+
+
 def device_status(device=None) -> int:
     """Synchronize the current stream and return (and clear) the device error word."""
     s = torch.cuda.current_stream(device).cuda_stream

@@ -346,12 +346,12 @@ nvq_status fwd_impl(const void* q, const void* k, const void* v, int B, int Nq, 
   void* qb = wb + w.qb;
   void* kb = wb + w.kb;
   void* vb = wb + w.vb;
-  // Q~, K~, V~ in every form the forward and a later attn_qat_bwd_saved read
-  // (block-sparse: all but the bf16 V~)
+  // Q~, K~, V~ in every form the forward and a later backward from the saved
+  // operands read
   const bool sparse = kv_list != nullptr;
   const AttnOpSpec ops[3] = {{q, Nq, qc, qs, qb, nullptr},
                              {k, Nkv, kc, ks, kb, nullptr},
-                             {v, Nkv, nullptr, nullptr, sparse ? nullptr : vb, v16}};
+                             {v, Nkv, nullptr, nullptr, vb, v16}};
   if ((e = timed(NVQ_KERNEL_QUANTIZE, stream,
                  [&] { return launch_quant_attn_ops(ops, 3, B, H, D, stream); })) != cudaSuccess)
     return fail_cuda("quantize q, k, v", e);
@@ -401,8 +401,9 @@ nvq_status bwd_kernels(const AttnShape& s, const void* qb, const void* kb, const
                  [&] { return launch_bwd_prep(s, o, dout, delta, stream); })) != cudaSuccess)
     return fail_cuda("bwd_prep", e);
   if (kv_list != nullptr &&
-      (e = launch_tile_transpose(kv_list, B, H, n_qt, n_kt, topk, q_off, q_list, stream)) !=
-          cudaSuccess)
+      (e = timed(NVQ_KERNEL_VSA, stream, [&] {
+         return launch_tile_transpose(kv_list, B, H, n_qt, n_kt, topk, q_off, q_list, stream);
+       })) != cudaSuccess)
     return fail_cuda("tile_transpose", e);
   // both kernels form S on FP4 UMMAs from the codes and scale blocks of Q~, K~
   CUtensorMap mq4, mk4;
@@ -469,10 +470,20 @@ nvq_status bwd_impl(const void* q, const void* k, const void* v, const void* o,
 
 // Straight-through backward from the quantized operands a dense forward left
 // in its workspace (no quantizer launch).
+// Backward from a forward's saved operands; kv_list (NULL: dense) and topk as
+// in bwd_impl.  ws: delta, then (block-sparse) the transposed lists.
+size_t saved_sparse_ws_bytes(int B, int N, int H, int topk) {
+  const size_t n_t = static_cast<size_t>((N + kTile - 1) / kTile);
+  const size_t off = round_up(saved_bwd_ws_bytes(B, N, H), 256);
+  const size_t lst = round_up(off + static_cast<size_t>(B) * H * (n_t + 1) * 4, 256);
+  return round_up(lst + static_cast<size_t>(B) * H * n_t * topk * 4, 256);
+}
+
 nvq_status bwd_saved_impl(const void* saved, size_t saved_bytes, const void* o,
-                          const float* stats, const void* dout, void* dq, void* dk, void* dv,
-                          int B, int Nq, int Nkv, int H, int D, float scale, int causal, void* ws,
-                          size_t ws_bytes, cudaStream_t stream) {
+                          const float* stats, const void* dout, const int* kv_list, int topk,
+                          void* dq, void* dk, void* dv, int B, int Nq, int Nkv, int H, int D,
+                          float scale, int causal, void* ws, size_t ws_bytes,
+                          cudaStream_t stream) {
   nvq_status st = check_attn(B, Nq, Nkv, H, D, scale, causal);
   if (st != NVQ_OK) return st;
   const void* ptrs[] = {o, stats, dout, dq, dk, dv};
@@ -482,15 +493,22 @@ nvq_status bwd_saved_impl(const void* saved, size_t saved_bytes, const void* o,
   if (saved == nullptr || saved_bytes < f.total ||
       (reinterpret_cast<uintptr_t>(saved) & 255u) != 0)
     return NVQ_ERR_WORKSPACE;
-  if (ws == nullptr || ws_bytes < saved_bwd_ws_bytes(B, Nq, H) ||
-      (reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
+  const bool sparse = kv_list != nullptr;
+  const size_t need = sparse ? saved_sparse_ws_bytes(B, Nq, H, topk) : saved_bwd_ws_bytes(B, Nq, H);
+  if (ws == nullptr || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0)
     return NVQ_ERR_WORKSPACE;
   int* err = error_word();
   if (err == nullptr) return NVQ_ERR_CUDA;
   const uint8_t* fb = static_cast<const uint8_t*>(saved);
+  uint8_t* wb = static_cast<uint8_t*>(ws);
+  const size_t off = round_up(saved_bwd_ws_bytes(B, Nq, H), 256);
+  const size_t n_t = static_cast<size_t>((Nq + kTile - 1) / kTile);
+  const size_t lst = round_up(off + static_cast<size_t>(B) * H * (n_t + 1) * 4, 256);
   const AttnShape s{B, Nq, Nkv, H, D, scale, causal};
   return bwd_kernels(s, fb + f.qb, fb + f.kb, fb + f.vb, fb + f.qc, fb + f.kc, fb + f.qs,
-                     fb + f.ks, o, stats, dout, nullptr, 0, nullptr, nullptr,
+                     fb + f.ks, o, stats, dout, kv_list, topk,
+                     sparse ? reinterpret_cast<int*>(wb + off) : nullptr,
+                     sparse ? reinterpret_cast<int*>(wb + lst) : nullptr,
                      static_cast<float*>(ws), dq, dk, dv, err, stream);
 }
 
@@ -635,8 +653,8 @@ nvq_status attn_qat_bwd_saved(const void* saved, size_t saved_bytes, const void*
                               const float* stats, const void* dout, void* dq, void* dk, void* dv,
                               int B, int Nq, int Nkv, int H, int D, float scale, int causal,
                               void* ws, size_t ws_bytes, nvq_stream_t stream) {
-  return bwd_saved_impl(saved, saved_bytes, o, stats, dout, dq, dk, dv, B, Nq, Nkv, H, D, scale,
-                        causal, ws, ws_bytes, stream);
+  return bwd_saved_impl(saved, saved_bytes, o, stats, dout, nullptr, 0, dq, dk, dv, B, Nq, Nkv,
+                        H, D, scale, causal, ws, ws_bytes, stream);
 }
 
 // Block-sparse: N % 128 == 0 (whole tiles), 1 <= topk <= N / 128, an int32
@@ -670,6 +688,22 @@ nvq_status attn_qat_bwd_sparse(const void* q, const void* k, const void* v, cons
   if (st != NVQ_OK) return st;
   return bwd_impl(q, k, v, o, stats, dout, kv_tiles, topk, dq, dk, dv, B, N, N, H, D, scale, 0, ws,
                   ws_bytes, stream);
+}
+
+size_t attn_qat_bwd_sparse_saved_workspace(int B, int N, int H, int D, int topk) {
+  if (B < 1 || N < 1 || H < 1 || D < 1 || topk < 1) return 0;
+  return saved_sparse_ws_bytes(B, N, H, topk);
+}
+
+nvq_status attn_qat_bwd_sparse_saved(const void* saved, size_t saved_bytes, const void* o,
+                                     const float* stats, const void* dout,
+                                     const int32_t* kv_tiles, int topk, void* dq, void* dk,
+                                     void* dv, int B, int N, int H, int D, float scale, void* ws,
+                                     size_t ws_bytes, nvq_stream_t stream) {
+  const nvq_status st = check_sparse(N, topk, kv_tiles);
+  if (st != NVQ_OK) return st;
+  return bwd_saved_impl(saved, saved_bytes, o, stats, dout, kv_tiles, topk, dq, dk, dv, B, N, N,
+                        H, D, scale, 0, ws, ws_bytes, stream);
 }
 
 nvq_status vsa_reorder(const void* x, int B, int T, int Hh, int W, int H, int D, int ct, int ch,

@@ -629,8 +629,9 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(const __nv_bfloat16* __re
 // Block-sparse lists transposed, per (b, h) (grid (H, B)): for each key tile
 // the query tiles whose list holds it, in ascending order: offsets
 // q_off[n_kt + 1] and entries q_list[<= n_qt * topk].  A list that names a key
-// tile twice counts it once.
-__global__ void __launch_bounds__(256) tile_transpose_kernel(const int* __restrict__ kv_list,
+// tile twice counts it once.  This form rescans the lists per key tile; it
+// serves lists whose bitmap (below) would not fit in shared memory.
+__global__ void __launch_bounds__(256) tile_transpose_scan_kernel(const int* __restrict__ kv_list,
                                                              int H, int n_qt, int n_kt, int topk,
                                                              int* __restrict__ q_off,
                                                              int* __restrict__ q_list) {
@@ -668,14 +669,93 @@ __global__ void __launch_bounds__(256) tile_transpose_kernel(const int* __restri
   }
 }
 
+// The same transpose through a bitmap in shared memory: bit i of row kt says
+// that query tile i's list holds key tile kt (entries outside [0, n_kt) are
+// ignored, repeats set the same bit).  Then one warp per key tile counts its
+// row, one warp forms the offsets, and one warp per key tile writes its query
+// tiles in ascending order.  Grid (H, B), 512 threads.
+__global__ void __launch_bounds__(512) tile_transpose_kernel(const int* __restrict__ kv_list,
+                                                             int H, int n_qt, int n_kt, int topk,
+                                                             int* __restrict__ q_off,
+                                                             int* __restrict__ q_list) {
+  extern __shared__ uint32_t tt_smem[];
+  const int words = (n_qt + 31) / 32;
+  uint32_t* bits = tt_smem;                                    // [n_kt][words]
+  int* start = reinterpret_cast<int*>(tt_smem + n_kt * words);  // [n_kt + 1]
+  const int64_t head = static_cast<int64_t>(blockIdx.y) * H + blockIdx.x;
+  const int* lst = kv_list + head * n_qt * topk;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+  for (int i = tid; i < n_kt * words; i += blockDim.x) bits[i] = 0u;
+  __syncthreads();
+  for (int e = tid; e < n_qt * topk; e += blockDim.x) {
+    const int i = e / topk, kt = lst[e];
+    if (kt >= 0 && kt < n_kt) atomicOr(&bits[kt * words + (i >> 5)], 1u << (i & 31));
+  }
+  __syncthreads();
+  for (int kt = warp; kt < n_kt; kt += nwarps) {
+    int c = 0;
+    for (int w = lane; w < words; w += 32) c += __popc(bits[kt * words + w]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xFFFFFFFFu, c, o);
+    if (lane == 0) start[kt] = c;
+  }
+  __syncthreads();
+  if (warp == 0) {  // exclusive prefix sum, 32 key tiles at a time
+    int carry = 0;
+    for (int base = 0; base < n_kt; base += 32) {
+      const int v = base + lane < n_kt ? start[base + lane] : 0;
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      if (base + lane < n_kt) start[base + lane] = carry + incl - v;
+      carry += __shfl_sync(0xFFFFFFFFu, incl, 31);
+    }
+    if (lane == 0) start[n_kt] = carry;
+  }
+  __syncthreads();
+  int* off = q_off + head * (n_kt + 1);
+  for (int kt = tid; kt <= n_kt; kt += blockDim.x) off[kt] = start[kt];
+  int* out = q_list + head * n_qt * topk;
+  for (int kt = warp; kt < n_kt; kt += nwarps) {
+    int pos = start[kt];
+    for (int w0 = 0; w0 < words; w0 += 32) {
+      const int w = w0 + lane;
+      uint32_t m = w < words ? bits[kt * words + w] : 0u;
+      const int c = __popc(m);
+      int incl = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      int p = pos + incl - c;
+      while (m != 0u) {
+        out[p++] = w * 32 + __ffs(m) - 1;
+        m &= m - 1u;
+      }
+      pos += __shfl_sync(0xFFFFFFFFu, incl, 31);
+    }
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_tile_transpose(const int* kv_list, int B, int H, int n_qt, int n_kt, int topk,
                                   int* q_off, int* q_list, cudaStream_t stream) {
-  const size_t smem = static_cast<size_t>(n_kt + 1) * sizeof(int);
-  if (smem > 48 * 1024) return cudaErrorInvalidValue;
-  tile_transpose_kernel<<<dim3(H, B), 256, smem, stream>>>(kv_list, H, n_qt, n_kt, topk, q_off,
-                                                           q_list);
+  const size_t words = static_cast<size_t>(n_qt + 31) / 32;
+  const size_t smem = (static_cast<size_t>(n_kt) * words + n_kt + 1) * sizeof(uint32_t);
+  if (smem <= 48 * 1024) {
+    tile_transpose_kernel<<<dim3(H, B), 512, smem, stream>>>(kv_list, H, n_qt, n_kt, topk, q_off,
+                                                             q_list);
+    return cudaGetLastError();
+  }
+  const size_t smem_scan = static_cast<size_t>(n_kt + 1) * sizeof(int);
+  if (smem_scan > 48 * 1024) return cudaErrorInvalidValue;
+  tile_transpose_scan_kernel<<<dim3(H, B), 256, smem_scan, stream>>>(kv_list, H, n_qt, n_kt, topk,
+                                                                     q_off, q_list);
   return cudaGetLastError();
 }
 

@@ -177,6 +177,39 @@ def test_bwd_saved_rejects_bad_arguments(lib):
     assert bwd(ws=None) == WORKSPACE
 
 
+def test_sparse_saved_backward_workspace_and_rejections(lib):
+    """attn_qat_bwd_sparse_saved: its workspace is delta [B, H, N] f32 followed by the
+    transposed lists (offsets [B, H, n_tiles + 1], entries [B, H, n_tiles, topk] int32),
+    each region 256-byte aligned; bad sizes, lists and buffers are rejected before any
+    device work."""
+    def up(x):
+        return (x + 255) // 256 * 256
+    n, h, d = 25088, 12, 128
+    want = up(12 * n * 4) + up(12 * 197 * 4) + up(12 * 196 * 20 * 4)
+    assert lib.attn_qat_bwd_sparse_saved_workspace(1, n, h, d, 20) == want
+    assert lib.attn_qat_bwd_sparse_saved_workspace(1, n, h, d, 0) == 0
+    b, n, h, d, topk = 1, 512, 2, 128, 2
+    fws = lib.attn_qat_fwd_workspace(b, n, n, h, d)
+    bws = lib.attn_qat_bwd_sparse_saved_workspace(b, n, h, d, topk)
+
+    def bwd(saved=A, saved_bytes=fws, o=A, tiles=A, topk=topk, n=n, D=d, scale=0.1,
+            ws=A + (1 << 30), ws_bytes=bws):
+        return lib.attn_qat_bwd_sparse_saved(saved, saved_bytes, o, A, A, tiles, topk, A, A, A,
+                                             b, n, h, D, scale, ws, ws_bytes, None)
+    assert bwd(topk=0) == INVALID
+    assert bwd(topk=5) == INVALID           # more than n / 128 key tiles
+    assert bwd(n=500) == INVALID            # not whole tiles
+    assert bwd(tiles=None) == INVALID
+    assert bwd(tiles=A + 2) == INVALID
+    assert bwd(D=96) == UNSUPPORTED
+    assert bwd(scale=float("nan")) == INVALID
+    assert bwd(o=A + 8) == INVALID
+    assert bwd(saved=None) == WORKSPACE
+    assert bwd(saved_bytes=fws - 1) == WORKSPACE
+    assert bwd(ws_bytes=bws - 1) == WORKSPACE
+    assert bwd(ws=A + 16) == WORKSPACE
+
+
 def test_quantizer_rejects_bad_arguments(lib):
     def fq(x=A, rows=4, cols=32, ld=32, gsf=None, out=A + 4096, ld_out=32, sc=A, ld_s=2):
         return lib.nvfp4_fake_quant(x, rows, cols, ld, gsf, out, ld_out, sc, ld_s, None)

@@ -116,6 +116,24 @@ def test_hand_built_lists_and_unselected_key_tiles():
     assert bool((dk[:, 256:] == 0).all()) and bool((dv[:, 256:] == 0).all())
 
 
+@pytest.mark.parametrize("b,n_tiles,h,d,topk,seed", [(1, 6, 2, 128, 2, 47), (2, 5, 3, 64, 3, 48)])
+def test_sparse_saved_operand_backward_matches(b, n_tiles, h, d, topk, seed):
+    """attn_qat_bwd_sparse_saved reads the operands attn_qat_fwd_sparse left in its
+    workspace; its gradients equal attn_qat_bwd_sparse's bit for bit."""
+    n = n_tiles * 128
+    inp = workloads.attn_inputs(b, n, n, h, d, seed)
+    q, k, v, do = (t.cuda() for t in (inp.q, inp.k, inp.v, inp.do))
+    tiles = api.vsa_select_tiles(q, k, topk)
+    saved = torch.full((api.attn_qat_fwd_workspace(b, n, n, h, d),), 0x5A, dtype=torch.uint8,
+                       device="cuda")
+    o, stats = api.attn_qat_fwd_sparse(q, k, v, tiles, inp.scale, workspace=saved)
+    ref = api.attn_qat_bwd_sparse(q, k, v, o, stats, do, tiles, inp.scale)
+    got = api.attn_qat_bwd_sparse_saved(saved, o, stats, do, tiles, inp.scale)
+    assert api.device_status() == 0
+    for name, g, r in zip(("dq", "dk", "dv"), got, ref):
+        assert torch.equal(g, r), name
+
+
 def _sample(n, count, seed):
     g = torch.Generator().manual_seed(seed)
     fixed = [0, 1, 127, 128, 129, 255, 256, n // 2, n - 129, n - 128, n - 2, n - 1]
