@@ -68,8 +68,8 @@ def kernel_work(kind, b, n, h, d):
 # (profiles/traffic_attn_kernels_wan25088.md), with the SHA-256 of the kernel's
 # sources at the time: a changed source reports null.
 TRAFFIC = {
-    "bwd_dkdv": {"bytes": 418806272, "sources": ['nvfp4_fake_quant_gb300/csrc/attn_bwd.cu', 'nvfp4_fake_quant_gb300/csrc/nvq_ptx.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_quant.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_internal.h'],
-                "sha256": "7111e260080fcbdbfb906d123b15ade1f37bb79e542a1ae4cc36c91cbc0ee66c"},
+    "bwd_dkdv": {"bytes": 419349632, "sources": ['nvfp4_fake_quant_gb300/csrc/attn_bwd.cu', 'nvfp4_fake_quant_gb300/csrc/nvq_ptx.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_quant.cuh', 'nvfp4_fake_quant_gb300/csrc/nvq_internal.h'],
+                "sha256": "73eb7e7302dee69f94de0c49b266ecf1ca70e42fb8c366ea6b1ae782bc08cb33"},
 }
 
 
