@@ -471,6 +471,17 @@ nvq_status nvq_selftest_fp4(const void* a, const void* b, const uint32_t* sf_img
                             int sf_stride, int mode, nvq_stream_t stream);
 
 /*
+ * Checks on the device that the hardware 2^x the attention kernels use
+ * (ex2.approx.ftz.f32) is non-decreasing over every float in [-200, 2]: the P~
+ * quantization takes a block's maximum of P as 2^(maximum of the arguments),
+ * which equals the maximum of the 2^x only for a non-decreasing 2^x.
+ *   out   device u64 [2], 8-byte aligned (written): out[0] = the number of
+ *         consecutive float pairs x < y with 2^y < 2^x, out[1] = the first such
+ *         pair's index (all ones if none).  About 2.2e9 pairs, a second or so.
+ */
+nvq_status nvq_selftest_ex2_monotone(unsigned long long* out, nvq_stream_t stream);
+
+/*
  * Launches one block that waits on a barrier nothing arrives on, with a wait
  * limit of `limit_ns` nanoseconds (1..1e9).  The wait must run out and record
  * NVQ_ERR_TIMEOUT for nvq_device_status(); nothing hangs.

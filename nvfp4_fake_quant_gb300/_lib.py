@@ -79,6 +79,7 @@ SIGNATURES = {
     "nvq_selftest_umma": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_int,
                                   c_void_p]),
     "nvq_selftest_timeout": (c_int, [c_int64, c_void_p]),
+    "nvq_selftest_ex2_monotone": (c_int, [c_void_p, c_void_p]),
     "nvq_selftest_fp4": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                                  c_int, c_int, c_int, c_int, c_void_p]),
 }

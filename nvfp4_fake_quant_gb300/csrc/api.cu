@@ -781,6 +781,12 @@ nvq_status nvq_selftest_fp4(const void* a, const void* b, const uint32_t* sf_img
                                                        sf_stride, mode, err, stream));
 }
 
+nvq_status nvq_selftest_ex2_monotone(unsigned long long* out, nvq_stream_t stream) {
+  if (out == nullptr || (reinterpret_cast<uintptr_t>(out) & 7u) != 0) return NVQ_ERR_INVALID;
+  return from_cuda("selftest_ex2_monotone",
+                   launch_selftest_ex2_monotone(out, static_cast<cudaStream_t>(stream)));
+}
+
 nvq_status nvq_selftest_timeout(int64_t limit_ns, nvq_stream_t stream) {
   if (limit_ns < 1 || limit_ns > 1000000000) return NVQ_ERR_INVALID;
   int* err = error_word();

@@ -169,6 +169,7 @@ cudaError_t launch_selftest_umma(const CUtensorMap& ta, const CUtensorMap& tb, c
                                  float* c, int N, int K, int a_mn, int b_mn, int* err,
                                  cudaStream_t stream);
 cudaError_t launch_selftest_timeout(int64_t limit_ns, int* err, cudaStream_t stream);
+cudaError_t launch_selftest_ex2_monotone(unsigned long long* out, cudaStream_t stream);
 cudaError_t launch_selftest_fp4(const CUtensorMap& ta, const CUtensorMap& tb, const uint32_t* sf_img,
                                 const uint8_t* sf_src, float* c, uint32_t* dump, int N, int nmma,
                                 int sf_stride, int mode, int* err, cudaStream_t stream);

@@ -296,21 +296,30 @@ __device__ __forceinline__ uint32_t e2m1_pair_f16x2(float lo, float hi) {
   return r;
 }
 
+// amax of P over a 16-key block, max_i 2^x_i, as 2^(max_i x_i): equal bit for
+// bit because ex2.approx.ftz.f32 is non-decreasing (nvq_selftest_ex2_monotone
+// checks every float in [-200, 2] on the device; below -200 it returns 0, and
+// a NaN argument is skipped by the maximum either way).  Taking the maximum
+// of the arguments lets the block's scale be formed while its sixteen
+// exponentials are still in flight.
+__device__ __forceinline__ float block_amax_p(const float* x) {
+  float a = max3f(x[0], x[1], x[2]);
+  a = max3f(a, x[3], x[4]);
+  a = max3f(a, x[5], x[6]);
+  a = max3f(a, x[7], x[8]);
+  a = max3f(a, x[9], x[10]);
+  a = max3f(a, x[11], x[12]);
+  a = max3f(a, x[13], x[14]);
+  return ex2_f32(fmaxf(a, x[15]));
+}
+
 // One 16-key block.  x: exponent arguments log2(e)*(scale*S - m) (-inf for
 // masked keys).  Out: p = 2^x (fp32) and P~ = E2M1(p/s)*s as f16x2 pairs,
 // s = E4M3(amax/6).  Returns nothing else; the caller sums p.
 __device__ __forceinline__ void pquant16(const float* x, float (&p)[16], uint32_t (&pt)[8]) {
+  const uint32_t sb = e4m3_rn_sat(block_amax_p(x) * (1.0f / 6.0f));
 #pragma unroll
   for (int i = 0; i < 16; ++i) p[i] = ex2_f32(x[i]);
-  float a = max3f(p[0], p[1], p[2]);
-  a = max3f(a, p[3], p[4]);
-  a = max3f(a, p[5], p[6]);
-  a = max3f(a, p[7], p[8]);
-  a = max3f(a, p[9], p[10]);
-  a = max3f(a, p[11], p[12]);
-  a = max3f(a, p[13], p[14]);
-  a = fmaxf(a, p[15]);
-  const uint32_t sb = e4m3_rn_sat(a * (1.0f / 6.0f));
   const uint32_t s_h = e4m3_to_f16x2(sb);
   const uint32_t s_h2 = (s_h & 0xFFFFu) | (s_h << 16);
   const float s = f16lo_to_f32(s_h);
@@ -364,17 +373,9 @@ __device__ __forceinline__ void e2m1x8_bf16_mul(uint32_t codes, uint32_t f2, uin
 // to bf16 and multiplied by bf16(s * inv_l).  Also returns p (fp32).
 __device__ __forceinline__ void pquant16_scaled_bf16(const float* x, float inv_l, float (&p)[16],
                                                      uint32_t (&out)[8]) {
+  const uint32_t sb = e4m3_rn_sat(block_amax_p(x) * (1.0f / 6.0f));
 #pragma unroll
   for (int i = 0; i < 16; ++i) p[i] = ex2_f32(x[i]);
-  float a = max3f(p[0], p[1], p[2]);
-  a = max3f(a, p[3], p[4]);
-  a = max3f(a, p[5], p[6]);
-  a = max3f(a, p[7], p[8]);
-  a = max3f(a, p[9], p[10]);
-  a = max3f(a, p[11], p[12]);
-  a = max3f(a, p[13], p[14]);
-  a = fmaxf(a, p[15]);
-  const uint32_t sb = e4m3_rn_sat(a * (1.0f / 6.0f));
   const float s = f16lo_to_f32(e4m3_to_f16x2(sb));
   const float inv = s > 0.f ? rcp_approx(s) : 0.f;
   const uint64_t inv2 = pk2(inv, inv);

@@ -10,6 +10,7 @@
 
 #include "nvq_internal.h"
 #include "nvq_ptx.cuh"
+#include "nvq_quant.cuh"
 
 namespace nvq {
 
@@ -255,6 +256,34 @@ __global__ void selftest_timeout_kernel(int64_t limit_ns, int* __restrict__ err)
   report_abort(&abort, err);
 }
 
+// Is ex2.approx.ftz.f32 non-decreasing?  Every pair of consecutive floats in
+// [-200, 2] (in increasing order: bit patterns 0xC3480000 down to 0x80000000,
+// then 0 up to 0x40000000); out[0] counts pairs with 2^next < 2^this, out[1]
+// is the first such index (all ones if none).
+constexpr uint64_t kMonoNeg = 0xC3480000ull - 0x80000000ull + 1;  // -200 .. -0
+constexpr uint64_t kMonoN = kMonoNeg + 0x40000000ull + 1;          // .. 2.0
+
+__device__ __forceinline__ float mono_value(uint64_t i) {
+  return __uint_as_float(static_cast<uint32_t>(i < kMonoNeg ? 0xC3480000ull - i : i - kMonoNeg));
+}
+
+__global__ void __launch_bounds__(256) selftest_ex2_monotone_kernel(
+    unsigned long long* __restrict__ out) {
+  const uint64_t stride = static_cast<uint64_t>(gridDim.x) * blockDim.x;
+  unsigned long long bad = 0, first = ~0ull;
+  for (uint64_t i = static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i + 1 < kMonoN;
+       i += stride) {
+    if (ex2_f32(mono_value(i + 1)) < ex2_f32(mono_value(i))) {
+      ++bad;
+      first = first < i ? first : i;
+    }
+  }
+  if (bad != 0) {
+    atomicAdd(&out[0], bad);
+    atomicMin(&out[1], first);
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_selftest_umma(const CUtensorMap& ta, const CUtensorMap& tb, const void* a,
@@ -276,6 +305,17 @@ cudaError_t launch_selftest_fp4(const CUtensorMap& ta, const CUtensorMap& tb, co
   if (e != cudaSuccess) return e;
   selftest_fp4_kernel<<<1, 128, kFp4Smem, stream>>>(ta, tb, sf_img, sf_src, c, dump, N, nmma,
                                                      sf_stride, mode, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_selftest_ex2_monotone(unsigned long long* out, cudaStream_t stream) {
+  cudaError_t e = cudaMemsetAsync(out, 0, sizeof(unsigned long long), stream);
+  if (e == cudaSuccess) e = cudaMemsetAsync(out + 1, 0xFF, sizeof(unsigned long long), stream);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 152;
+  if (cudaGetDevice(&dev) == cudaSuccess)
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  selftest_ex2_monotone_kernel<<<sms * 8, 256, 0, stream>>>(out);
   return cudaGetLastError();
 }
 

@@ -229,6 +229,8 @@ def test_quantizer_rejects_bad_arguments(lib):
     assert lib.nvfp4_global_sf(A, 4, 32, 32, None, None) == INVALID
     assert lib.nvfp4_global_sf(A, 0, 32, 32, A, None) == INVALID
     assert lib.nvq_selftest_timeout(0, None) == INVALID
+    assert lib.nvq_selftest_ex2_monotone(None, None) == INVALID
+    assert lib.nvq_selftest_ex2_monotone(A + 4, None) == INVALID
     assert lib.nvq_selftest_umma(A, A, A, 96, 64, 0, 0, None) == INVALID
     assert lib.nvq_selftest_umma(A, A, A, 64, 64, 3, 0, None) == INVALID
     assert lib.nvq_selftest_fp4(A, A, A, None, A, A, 96, 1, 4, 0, None) == INVALID

@@ -123,3 +123,14 @@ def test_fp4_block_scaled_umma(n, nmma, mode):
         for m in range(2):
             assert torch.equal(dump[:, 32 * m:32 * m + 4 * nmma], want[m, :, :4 * nmma])
     assert torch.all((c - ref).abs() <= 1e-6 * mag + 1e-30), float((c - ref).abs().max())
+
+
+def test_hardware_exp2_is_non_decreasing():
+    """The P~ quantization forms a block's maximum of P = 2^x as 2^(max x); that is the
+    same value only if the hardware 2^x (ex2.approx.ftz.f32) never decreases.  Checked
+    for every pair of consecutive floats in [-200, 2] (about 2.2e9 pairs)."""
+    out = torch.zeros(2, dtype=torch.int64, device="cuda")
+    assert _lib.load().nvq_selftest_ex2_monotone(out.data_ptr(), None) == 0
+    torch.cuda.synchronize()
+    bad, first = out.cpu().tolist()
+    assert bad == 0, (bad, first)
