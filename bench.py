@@ -609,6 +609,44 @@ def linear_bench(peaks, stream, steps):
                             for name, (c, t) in kt_b.items() if c}}
 
 
+def gpu_local_cpus(dev):
+    """The CPUs sysfs lists as local to the GPU's PCI device (its NUMA node), or None."""
+    import torch
+    try:
+        pr = torch.cuda.get_device_properties(dev)
+        path = "/sys/bus/pci/devices/%04x:%02x:%02x.0/local_cpulist" % (
+            pr.pci_domain_id, pr.pci_bus_id, pr.pci_device_id)
+        cpus = set()
+        with open(path) as f:
+            for part in f.read().strip().split(","):
+                if "-" in part:
+                    a, b_ = part.split("-")
+                    cpus.update(range(int(a), int(b_) + 1))
+                elif part:
+                    cpus.add(int(part))
+        allowed = os.sched_getaffinity(0)
+        cpus &= allowed
+        return cpus if cpus and cpus != allowed else None
+    except Exception:
+        return None
+
+
+def pinned_near(dev, make):
+    """make() run with this process's threads on the CPUs local to the GPU (when
+    sysfs names a proper subset of the allowed CPUs), so that the pinned host
+    pages it touches first sit on the GPU's NUMA node; the affinity is restored
+    afterwards.  Returns (result, the CPUs used or None)."""
+    cpus = gpu_local_cpus(dev)
+    if cpus is None:
+        return make(), None
+    old = os.sched_getaffinity(0)
+    try:
+        os.sched_setaffinity(0, cpus)
+        return make(), sorted(cpus)
+    finally:
+        os.sched_setaffinity(0, old)
+
+
 def run_ours(args):
     import torch
 
@@ -683,8 +721,12 @@ def run_ours(args):
     # pinned host memory.  The copies run on two copy streams over two device
     # buffer sets: step j+1's inputs arrive and step j's gradients leave while the
     # GPU computes, the way a training loop overlaps its transfers.
-    hq, hk, hv, hdo = (t.pin_memory() for t in (inp.q, inp.k, inp.v, inp.do))
-    hdq, hdk, hdv = (torch.empty_like(t).pin_memory() for t in (inp.q, inp.k, inp.v))
+    def make_host():
+        ins = tuple(t.pin_memory() for t in (inp.q, inp.k, inp.v, inp.do))
+        outs = tuple(torch.zeros_like(t).pin_memory() for t in (inp.q, inp.k, inp.v))
+        return ins + outs
+
+    (hq, hk, hv, hdo, hdq, hdk, hdv), host_cpus = pinned_near(dev, make_host)
     e2e_sets = []
     if not args.skip_e2e:
         for _ in range(2):
@@ -787,7 +829,10 @@ def run_ours(args):
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "method": "per step: q, k, v, dO copied in from pinned host memory and dq, dk, "
                           "dv copied out to it, on two copy streams over two device buffer "
-                          "sets overlapping the neighbouring steps' compute"},
+                          "sets overlapping the neighbouring steps' compute",
+                "pinned_first_touch_cpus": (f"{host_cpus[0]}-{host_cpus[-1]} (local to the GPU)"
+                                            if host_cpus else "all allowed (sysfs named no "
+                                            "narrower GPU-local set)")},
         "gpu_launches": sum(k["launches"] for k in kernels.values()),
         "clocks": clocks,
     }

@@ -497,15 +497,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           *reinterpret_cast<uint4*>(p_smem + off) = make_uint4(w[0], w[1], w[2], w[3]);
         }
       }
-      fence_proxy_async_smem();
-      mbar_arrive_warp(pt_full);
       // ---- dS part: dP -> dS = scale * A * (dP - delta), A = P / l
+      // The first dP load is issued before the P~ stores are fenced, so the
+      // fence's wait for the stores overlaps the load (dP_i is issued when S_i
+      // has been loaded, long before this point).
       if (!(ok = mbar_wait_warp(dp_full, ph, abort))) break;
       tc_fence_after();
       // dP one 32-key chunk at a time: the second load waits until the first
       // chunk's P values are consumed, which keeps the register peak (all 64 P
       // values and 64 dP values at once) under what 320 threads may hold
       tmem_ld32(tmem + lane_base + kColSP + key_col, r[0]);
+      fence_proxy_async_smem();
+      mbar_arrive_warp(pt_full);
       tmem_wait_ld();
       // the dS buffer is free once dK of the previous tile is done
       if (it > 0 && !(ok = mbar_wait_warp(ds_free, ph ^ 1u, abort))) break;

@@ -493,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int hb = 0; hb < 2; ++hb) {
           float pp[16];
           uint32_t (&ph)[8] = *reinterpret_cast<uint32_t(*)[8]>(pt + 8 * hb);
-          pquant16(x + 16 * hb, pp, ph);
+          pquant16_pmax(x + 16 * hb, pp, ph);
 #pragma unroll
           for (int u = 0; u < 8; ++u) l2 = add2(l2, pk2(pp[2 * u], pp[2 * u + 1]));
           if constexpr (aux) {
