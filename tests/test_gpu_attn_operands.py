@@ -1,7 +1,7 @@
 """The quantized operands inside the attention calls, compared with the oracle
 byte for byte, and the agreement of the forward's and the backward's P~.
 
-1. After attn_qat_fwd / attn_qat_fwd_hp / attn_qat_bwd the caller-owned
+1. After attn_qat_fwd / attn_qat_fwd_hp / attn_qat_fwd_sparse / attn_qat_bwd the caller-owned
    workspaces hold the quantized Q, K, V at the offsets attn_qat_*_layout
    reports (include/nvfp4attn.h): the E2M1 codes and the 512-byte scale blocks
    of Q~ and K~ that feed the block-scaled FP4 MMA, V~ in f16, Q~/K~/V~ in
@@ -13,12 +13,13 @@ byte for byte, and the agreement of the forward's and the backward's P~.
    128-token tile must carry scale 0.  The workspaces are filled with a
    non-zero pattern first, so nothing passes by being left untouched.
 
-2. P~ = fq16(exp(S - m)) is computed twice: by the forward (S on block-scaled
-   FP4 MMAs) for O = P~ V~ / l, and by the dK/dV kernel (S on BF16 MMAs) for
-   dV = (P~ / l)^T dO.  The two S differ only in fp32 accumulation order, so
-   P~ may differ where P / s lies within rounding of an E2M1 decision
-   ("Attn-QAT Training" guide, "Architecture-specific Triton routing": the
-   exact-m statistics exist to keep dV consistent with the forward's P~).
+2. P~ = fq16(exp(S - m)) is computed twice: by the forward for O = P~ V~ / l
+   and by the dK/dV kernel for dV = (P~ / l)^T dO, both from S on the same
+   block-scaled FP4 MMAs (earlier forms of the dK/dV kernel formed S on BF16
+   MMAs, equal up to the fp32 accumulation order), so a difference would show
+   where P / s lies within rounding of an E2M1 decision ("Attn-QAT Training"
+   guide, "Architecture-specific Triton routing": the exact-m statistics exist
+   to keep dV consistent with the forward's P~).
    Both P~ are read out through the public calls, with no instrumentation:
    V = one-hot rows over one tile of keys makes O[i, c] = 1.03125 P~[i, j] / l_i
    (the fake-quantized one-hot block is 6 * E4M3(1/6) = 1.03125), and dO =
@@ -123,6 +124,26 @@ def test_forward_workspace_operands_are_bit_exact(case):
         check_16bit(ws, lay["q_bf16"], inp.q, torch.bfloat16, "Q~ (bf16)")
         check_16bit(ws, lay["k_bf16"], inp.k, torch.bfloat16, "K~ (bf16)")
         check_16bit(ws, lay["v_bf16"], inp.v, torch.bfloat16, "V~ (bf16)")
+
+
+@pytest.mark.parametrize("b,n_tiles,h,d,topk,seed", [(1, 3, 2, 128, 2, 30), (2, 2, 3, 64, 1, 31)])
+def test_sparse_forward_workspace_operands_are_bit_exact(b, n_tiles, h, d, topk, seed):
+    """The block-sparse forward leaves the same forms as the dense ones (what
+    attn_qat_bwd_sparse_saved reads), whatever tiles the lists select."""
+    n = n_tiles * 128
+    inp = workloads.attn_inputs(b, n, n, h, d, seed)
+    q, k, v = (t.cuda() for t in (inp.q, inp.k, inp.v))
+    tiles = api.vsa_select_tiles(q, k, topk)
+    lay = api.attn_qat_layout(b, n, n, h, d, "fwd")
+    ws = torch.full((lay["total"],), FILL, dtype=torch.uint8, device="cuda")
+    api.attn_qat_fwd_sparse(q, k, v, tiles, inp.scale, workspace=ws)
+    assert api.device_status() == 0
+    check_fp4(ws, lay, "q", inp.q)
+    check_fp4(ws, lay, "k", inp.k)
+    check_16bit(ws, lay["v_f16"], inp.v, torch.float16, "V~ (f16)")
+    check_16bit(ws, lay["q_bf16"], inp.q, torch.bfloat16, "Q~ (bf16)")
+    check_16bit(ws, lay["k_bf16"], inp.k, torch.bfloat16, "K~ (bf16)")
+    check_16bit(ws, lay["v_bf16"], inp.v, torch.bfloat16, "V~ (bf16)")
 
 
 @pytest.mark.parametrize("case", CASES, ids=lambda c: "x".join(map(str, c[:5])))
