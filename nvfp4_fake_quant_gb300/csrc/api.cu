@@ -355,14 +355,16 @@ nvq_status fwd_impl(const void* q, const void* k, const void* v, int B, int Nq, 
   if ((e = timed(NVQ_KERNEL_QUANTIZE, stream,
                  [&] { return launch_quant_attn_ops(ops, 3, B, H, D, stream); })) != cudaSuccess)
     return fail_cuda("quantize q, k, v", e);
-  if (!sparse && o_hp == nullptr) {
-    // dense: S on FP4 UMMAs, Q~ and K~ as codes + scale blocks
+  if (!sparse) {
+    // dense (with or without the auxiliary output): S on FP4 UMMAs, Q~ and K~
+    // as codes + scale blocks
     if ((r = make_bnhd_u8_map(&mq, qc, B, Nq, H, D)) != 0 ||
         (r = make_bnhd_u8_map(&mk, kc, B, Nkv, H, D)) != 0 ||
         (r = make_bnhd_map(&mv, v16, B, Nkv, H, D, true)) != 0)
       return fail_driver("cuTensorMapEncodeTiled", r);
     return from_cuda("attn_fwd", timed(NVQ_KERNEL_ATTN_FWD, stream, [&] {
-                       return launch_attn_fwd_fp4(s, mq, mk, mv, qs, ks, o, stats, err, stream);
+                       return launch_attn_fwd_fp4(s, mq, mk, mv, qs, ks, o, o_hp, stats, err,
+                                                  stream);
                      }));
   }
   CUtensorMap mq4, mk4;  // codes of Q~, K~ for the FP4 pass 1

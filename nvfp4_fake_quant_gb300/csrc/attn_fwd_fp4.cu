@@ -53,6 +53,19 @@
 // producer, warp 17 TMEM allocator and S issuer, warp 18 P~V~ issuer
 // (converged warps, one elected lane issuing).  Shared memory: Q~ codes and
 // scales, a ring of K~ tiles (codes + scales), a ring of V~ tiles (f16).
+//
+// Auxiliary-output form (kAux; the "auxiliary output" of the Attn-QAT
+// backward, "use_high_prec_o"): next to O it accumulates O_hp = P V~ / l from
+// the unquantized P (f16).  O_hp takes the TMEM columns [256 + D, 256 + 2 D),
+// so pass 2 runs on half tiles of 64 keys: half u (keys [64 (u % 2), +64) of
+// tile u / 2) is one N = 64 UMMA pair into buffer u % 3 of three 64-column
+// buffers [0, 192); warpgroup w owns keys [16 w, 16 w + 16) of every half and
+// writes, over the 16 columns it has loaded, P~ (f16 pairs) into the first 8
+// and P into the next 8.  The P~V~ warp adds both into O and O_hp.  The Q~
+// scale operand of pass 2 sits at [192, 192 + D/16) (pass 1's copy is under
+// O_hp), the K~ scale operand of pass-2 tile j at [200 + 8 (j % 4), +8); a
+// half reads the scale columns of its 64 keys, 2 (u % 2) columns in (key n of
+// a 128-key region is at column n / 32).  Pass 1 is unchanged.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -74,6 +87,9 @@ constexpr int kVRing = 4;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint32_t kScA = 384, kScB = 392;  // TMEM columns of the scale operands
 constexpr int kScRegions = 12;               // K~ scale copies at kScB + 8 r, up to 488
+// auxiliary-output pass 2: the Q~ scale operand and four K~ scale regions
+constexpr uint32_t kScA2 = 192, kScB2 = 200;
+constexpr int kScRegions2 = 4;
 
 template <int D>
 struct Fp4Layout {
@@ -87,22 +103,23 @@ struct Fp4Layout {
   static constexpr uint32_t kX = kVRingOff + kVRing * kVSlot;  // [4 warpgroups][128] f32
   static constexpr uint32_t kBars = kX + 4u * 128u * 4u;
   // q_full, k_full/k_empty, v_full/v_empty, s1_full[12], s1_free[6], pass1_done,
-  // s_full[2], p_full[2], pv_done[2], o_full, drain x2, q_sc_ready
-  static constexpr uint32_t kNumBars = 1 + 2 * kKRing + 2 * kVRing + 12 + 6 + 1 + 6 + 4;
+  // s_full[3], p_full[3], pv_done[3] (two of each without the auxiliary output),
+  // o_full, drain x2, q_sc_ready
+  static constexpr uint32_t kNumBars = 1 + 2 * kKRing + 2 * kVRing + 12 + 6 + 1 + 9 + 4;
   static constexpr uint32_t kTmemSlot = kBars + kNumBars * 8u;
   static constexpr uint32_t kAbort = kTmemSlot + 4u;
   static constexpr uint32_t kAlloc = kAbort + 4u + 1024u;
 };
 
 // Grid: (ceil(Nq / 128), H, B).
-template <int D>
+template <int D, bool kAux>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_fp4_kernel(const __grid_constant__ CUtensorMap tq,
                         const __grid_constant__ CUtensorMap tk,
                         const __grid_constant__ CUtensorMap tv, const uint8_t* __restrict__ q_sc,
                         const uint8_t* __restrict__ k_sc, __nv_bfloat16* __restrict__ o,
-                        float* __restrict__ stats, int Nq, int Nkv, int H, float scale,
-                        int causal, int* __restrict__ err) {
+                        __nv_bfloat16* __restrict__ o_hp, float* __restrict__ stats, int Nq,
+                        int Nkv, int H, float scale, int causal, int* __restrict__ err) {
   using L = Fp4Layout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023u) &
@@ -122,10 +139,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* s1_full = v_empty + kVRing;  // pass 1 [12]: tile j -> j % 12
   uint64_t* s1_free = s1_full + 12;      // pass 1 [6]: tile j -> j % 6
   uint64_t* pass1_done = s1_free + 6;
-  uint64_t* s_full = pass1_done + 1;     // pass 2 [2]
-  uint64_t* p_full = s_full + 2;         // pass 2 [2]
-  uint64_t* pv_done = p_full + 2;        // pass 2 [2]
-  uint64_t* o_full = pv_done + 2;
+  uint64_t* s_full = pass1_done + 1;     // pass 2 [3]
+  uint64_t* p_full = s_full + 3;         // pass 2 [3]
+  uint64_t* pv_done = p_full + 3;        // pass 2 [3]
+  uint64_t* o_full = pv_done + 3;
   uint64_t* drain = o_full + 1;          // [2]: S warp, PV warp
   uint64_t* q_sc_ready = drain + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kTmemSlot);
@@ -150,12 +167,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 12; ++i) mbar_init(&s1_full[i], 1);
     for (int i = 0; i < 6; ++i) mbar_init(&s1_free[i], kSoftmaxWarps / 4);
     mbar_init(pass1_done, kSoftmaxWarps);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < 3; ++i) {
       mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], kSoftmaxWarps);
       mbar_init(&pv_done[i], 1);
-      mbar_init(&drain[i], 1);
     }
+    mbar_init(&drain[0], 1);
+    mbar_init(&drain[1], 1);
     mbar_init(o_full, 1);
     mbar_init(q_sc_ready, 1);
     fence_mbar_init();
@@ -177,14 +195,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t sbo = 8u * (D / 2);
   const uint32_t q_addr = smem_u32(smem + L::kQ);
   const uint32_t k_ring = smem_u32(smem + L::kKRingOff);
-  // prep_s: wait for the K~ tile of load kl and copy its scales for tile counter g
-  auto prep_s = [&](int kl, int g) -> bool {
+  // the K~ scale region of tile counter g
+  auto sc_region = [&](int g) { return kScB + 8u * static_cast<uint32_t>(g % kScRegions); };
+  // prep_s: wait for the K~ tile of load kl and copy its scales into TMEM column sc
+  auto prep_s = [&](int kl, uint32_t sc) -> bool {
     const int slot = kl % kKRing;
     if (!mbar_wait_warp(&k_full[slot], static_cast<uint32_t>((kl / kKRing) & 1), abort))
       return false;
     tc_fence_after();
     const uint32_t kb = k_ring + slot * L::kKSlot;
-    const uint32_t sc = kScB + 8u * static_cast<uint32_t>(g % kScRegions);
 #pragma unroll
     for (int kk = 0; kk < D / 64; ++kk)
       tmem_cp_32x128_x4_w(tmem + sc + 4 * kk, kb + L::kCodeBytes + kk * 512);
@@ -195,7 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto fire_s = [&](uint32_t col, int kl, int g, uint64_t* bar) {
     const int slot = kl % kKRing;
     const uint32_t kb = k_ring + slot * L::kKSlot;
-    const uint32_t sc = kScB + 8u * static_cast<uint32_t>(g % kScRegions);
+    const uint32_t sc = sc_region(g);
 #pragma unroll
     for (int kk = 0; kk < D / 64; ++kk)
       umma_fp4_ss_w(tmem + col, sdesc(q_addr + 32 * kk, 16, sbo, lay),
@@ -204,13 +223,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     umma_commit_w(bar);
     if (g >= nk) umma_commit_w(&k_empty[slot]);
   };
+  // Auxiliary output, pass 2: half hh (keys [64 hh, 64 hh + 64)) of the K~ tile
+  // of load kl into the 64-column buffer at `col`; the tile's scales at column sc
+  constexpr uint32_t idesc_h = idesc_mxf4nvf4(128, 64);
+  auto fire_half = [&](uint32_t col, int kl, uint32_t sc, int hh, uint64_t* bar) {
+    const int slot = kl % kKRing;
+    const uint32_t kb = k_ring + slot * L::kKSlot + static_cast<uint32_t>(hh) * 64u * (D / 2);
+#pragma unroll
+    for (int kk = 0; kk < D / 64; ++kk)
+      umma_fp4_ss_w(tmem + col, sdesc(q_addr + 32 * kk, 16, sbo, lay),
+                    sdesc(kb + 32 * kk, 16, sbo, lay), idesc_h, tmem + kScA2 + 4 * kk,
+                    tmem + sc + 4 * kk + 2 * hh, kk > 0 ? 1u : 0u);
+    umma_commit_w(bar);
+    if (hh == 1) umma_commit_w(&k_empty[slot]);
+  };
   // Pass 1, tile j (load j) into buffer j % 3 once the softmax has loaded tile
   // j - 3 from there.  The S warp takes the even tiles, the P~V~ warp (idle
   // until pass 2) the odd ones.
   auto pass1 = [&](int first) -> bool {
     bool ok = true;
     for (int j = first; j < nk && ok; j += 2) {
-      if (!(ok = prep_s(j, j))) break;
+      if (!(ok = prep_s(j, sc_region(j)))) break;
       if (j >= 3 && !(ok = mbar_wait_warp(&s1_free[(j - 3) % 6],
                                           static_cast<uint32_t>(((j - 3) / 6) & 1), abort)))
         break;
@@ -291,18 +324,43 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) ok = pass1(0);
     // every pass-1 tile loaded by the softmax (pass 2 reuses the columns)
     if (ok) ok = mbar_wait_warp(pass1_done, 0, abort);
-    // Pass 2 (tile counter g = nk + j): tiles 0 and 1 at once, then tile j + 2
-    // into buffer j % 2 once the P~V~ of tile j, the last reader of its P~, is done.
-    for (int j = 0; j < 2 && j < nk && ok; ++j) {
-      if (!(ok = prep_s(nk + j, nk + j))) break;
-      fire_s(128u * j, nk + j, nk + j, &s_full[j]);
-    }
-    for (int j = 0; j + 2 < nk && ok; ++j) {
-      const int buf = j & 1;
-      if (!(ok = prep_s(nk + j + 2, nk + j + 2))) break;
-      if (!(ok = mbar_wait_warp(&pv_done[buf], static_cast<uint32_t>((j >> 1) & 1), abort))) break;
-      tc_fence_after();
-      fire_s(128u * buf, nk + j + 2, nk + j + 2, &s_full[buf]);
+    if constexpr (!kAux) {
+      // Pass 2 (tile counter g = nk + j): tiles 0 and 1 at once, then tile j + 2
+      // into buffer j % 2 once the P~V~ of tile j, the last reader of its P~, is done.
+      for (int j = 0; j < 2 && j < nk && ok; ++j) {
+        if (!(ok = prep_s(nk + j, sc_region(nk + j)))) break;
+        fire_s(128u * j, nk + j, nk + j, &s_full[j]);
+      }
+      for (int j = 0; j + 2 < nk && ok; ++j) {
+        const int buf = j & 1;
+        if (!(ok = prep_s(nk + j + 2, sc_region(nk + j + 2)))) break;
+        if (!(ok = mbar_wait_warp(&pv_done[buf], static_cast<uint32_t>((j >> 1) & 1), abort)))
+          break;
+        tc_fence_after();
+        fire_s(128u * buf, nk + j + 2, nk + j + 2, &s_full[buf]);
+      }
+    } else {
+      // Pass 2 on half tiles: the Q~ scales again (pass 1's copy lies under
+      // O_hp), then half u into buffer u % 3 once the P~V~ of half u - 3, the
+      // last reader of that buffer, is done.  A tile's K~ scales are copied at
+      // its first half into region j % 4: the copy for tile j follows the wait
+      // for the P~V~ of half 2 j - 4, so the S UMMAs of tile j - 2 and before,
+      // the last readers of the region, have completed.
+      if (ok) {
+#pragma unroll
+        for (int kk = 0; kk < D / 64; ++kk)
+          tmem_cp_32x128_x4_w(tmem + kScA2 + 4 * kk, q_addr + L::kCodeBytes + kk * 512);
+      }
+      for (int u = 0; u < 2 * nk && ok; ++u) {
+        const int j = u >> 1, hh = u & 1, c = u % 3;
+        const uint32_t sc = kScB2 + 8u * static_cast<uint32_t>(j % kScRegions2);
+        if (hh == 0 && !(ok = prep_s(nk + j, sc))) break;
+        if (u >= 3 &&
+            !(ok = mbar_wait_warp(&pv_done[c], static_cast<uint32_t>(((u - 3) / 3) & 1), abort)))
+          break;
+        tc_fence_after();
+        fire_half(64u * c, nk + j, sc, hh, &s_full[c]);
+      }
     }
     umma_commit_w(&drain[0]);
     mbar_wait_warp(&drain[0], 0, nullptr, 10000000ull);
@@ -316,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       ok = pass1(1);
     }
-    for (int j = 0; j < nk && ok; ++j) {
+    for (int j = 0; j < nk && ok && !kAux; ++j) {
       const int buf = j & 1, slot = j % kVRing;
       if (!(ok = mbar_wait_warp(&v_full[slot], static_cast<uint32_t>((j / kVRing) & 1), abort))) break;
       if (!(ok = mbar_wait_warp(&p_full[buf], static_cast<uint32_t>((j >> 1) & 1), abort))) break;
@@ -330,6 +388,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                       (j > 0 || kk > 0) ? 1u : 0u);
       umma_commit_w(&pv_done[buf]);
       umma_commit_w(&v_empty[slot]);
+    }
+    // auxiliary output: per half u, keys [64 hh + 16 w, +16) from warpgroup w's
+    // columns of buffer u % 3, P~ into O and P into O_hp
+    for (int u = 0; u < 2 * nk && ok && kAux; ++u) {
+      const int j = u >> 1, hh = u & 1, c = u % 3, slot = j % kVRing;
+      if (hh == 0 &&
+          !(ok = mbar_wait_warp(&v_full[slot], static_cast<uint32_t>((j / kVRing) & 1), abort)))
+        break;
+      if (!(ok = mbar_wait_warp(&p_full[c], static_cast<uint32_t>((u / 3) & 1), abort))) break;
+      tc_fence_after();
+      const uint32_t vb = v_ring + slot * L::kVSlot;
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const uint64_t bd = sdesc_sw128(vb + (4 * hh + w) * 2048, 128u * 128u, 1024);
+        const uint32_t acc = (u > 0 || w > 0) ? 1u : 0u;
+        umma_f16_ts_w(tmem + 256, tmem + 64 * c + 16 * w, bd, idesc_pv, acc);
+        umma_f16_ts_w(tmem + 256 + D, tmem + 64 * c + 16 * w + 8, bd, idesc_pv, acc);
+      }
+      umma_commit_w(&pv_done[c]);
+      if (hh == 1) umma_commit_w(&v_empty[slot]);
     }
     if (ok) umma_commit_w(o_full);
     umma_commit_w(&drain[1]);
@@ -399,7 +477,44 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float negmb = -m * kLog2e;
     const uint64_t c12 = pk2(c1, c1), nmb2 = pk2(negmb, negmb);
     uint64_t l2 = pk2(0.f, 0.f);
-    for (int j = 0; j < nk && ok; ++j) {
+    // auxiliary output: half u, keys [64 hh + 16 wg, +16) of tile j
+    for (int u = 0; u < 2 * nk && ok && kAux; ++u) {
+      const int j = u >> 1, hh = u & 1, c = u % 3;
+      if (!(ok = mbar_wait_warp(&s_full[c], static_cast<uint32_t>((u / 3) & 1), abort))) break;
+      tc_fence_after();
+      const uint32_t col = 64u * c + 16u * wg;
+      uint32_t r16[16];
+      tmem_ld16(tmem + lane_base + col, r16);
+      tmem_wait_ld();
+      float x[16];
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        up2(fma2(pk2(__uint_as_float(r16[2 * i]), __uint_as_float(r16[2 * i + 1])), c12, nmb2),
+            x[2 * i], x[2 * i + 1]);
+      const int k0 = j * kTile + 64 * hh + 16 * wg;
+      if (k0 + 16 > Nkv || (causal && k0 + 15 > q0)) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int key = k0 + i;
+          if (!(key < Nkv && (!causal || key <= qrow))) x[i] = -INFINITY;
+        }
+      }
+      // P~ (f16 pairs) into the first 8 of the 16 columns just loaded, P into the next 8
+      uint32_t pw[16];
+      float pp[16];
+      pquant16(x, pp, *reinterpret_cast<uint32_t(*)[8]>(pw));
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        l2 = add2(l2, pk2(pp[2 * i], pp[2 * i + 1]));
+        __half2 h2 = __floats2half2_rn(pp[2 * i], pp[2 * i + 1]);
+        pw[8 + i] = *reinterpret_cast<uint32_t*>(&h2);
+      }
+      tmem_st16(tmem + lane_base + col, pw);
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive_warp(&p_full[c]);
+    }
+    for (int j = 0; j < nk && ok && !kAux; ++j) {
       const int buf = j & 1;
       if (!(ok = mbar_wait_warp(&s_full[buf], static_cast<uint32_t>((j >> 1) & 1), abort))) break;
       tc_fence_after();
@@ -443,34 +558,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (have_o) {
       tc_fence_after();
       const float inv_l = 1.0f / l;
-      // warpgroup wg writes O columns [wg D/4, (wg + 1) D/4)
+      // warpgroup wg writes O columns [wg D/4, (wg + 1) D/4) (and the same of O_hp)
       constexpr int kCols = D / 4;
-      const uint32_t o_col = 256u + static_cast<uint32_t>(wg * kCols);
-      uint32_t w[kCols / 2];
-      if constexpr (kCols == 32) {
-        tmem_ld32(tmem + lane_base + o_col, r);
-      } else {
-        uint32_t (&r16)[16] = *reinterpret_cast<uint32_t(*)[16]>(r);
-        tmem_ld16(tmem + lane_base + o_col, r16);
+#pragma unroll
+      for (int oi = 0; oi < (kAux ? 2 : 1); ++oi) {
+        const uint32_t o_col = 256u + static_cast<uint32_t>(oi * D + wg * kCols);
+        uint32_t w[kCols / 2];
+        if constexpr (kCols == 32) {
+          tmem_ld32(tmem + lane_base + o_col, r);
+        } else {
+          uint32_t (&r16)[16] = *reinterpret_cast<uint32_t(*)[16]>(r);
+          tmem_ld16(tmem + lane_base + o_col, r16);
+        }
+        tmem_wait_ld();
+        if (qrow < Nq) {
+#pragma unroll
+          for (int i = 0; i < kCols / 2; ++i) {
+            __nv_bfloat162 v2 = __floats2bfloat162_rn(__uint_as_float(r[2 * i]) * inv_l,
+                                                      __uint_as_float(r[2 * i + 1]) * inv_l);
+            w[i] = *reinterpret_cast<uint32_t*>(&v2);
+          }
+          __nv_bfloat16* orow = (oi ? o_hp : o) +
+                                ((static_cast<int64_t>(b) * Nq + qrow) * H + h) * D + wg * kCols;
+          uint4* dst = reinterpret_cast<uint4*>(orow);
+#pragma unroll
+          for (int u = 0; u < kCols / 8; ++u)
+            dst[u] = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+        }
       }
-      tmem_wait_ld();
-      if (qrow < Nq) {
-#pragma unroll
-        for (int i = 0; i < kCols / 2; ++i) {
-          __nv_bfloat162 v2 = __floats2bfloat162_rn(__uint_as_float(r[2 * i]) * inv_l,
-                                                    __uint_as_float(r[2 * i + 1]) * inv_l);
-          w[i] = *reinterpret_cast<uint32_t*>(&v2);
-        }
-        __nv_bfloat16* orow = o + ((static_cast<int64_t>(b) * Nq + qrow) * H + h) * D + wg * kCols;
-        uint4* dst = reinterpret_cast<uint4*>(orow);
-#pragma unroll
-        for (int u = 0; u < kCols / 8; ++u)
-          dst[u] = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
-        if (wg == 0) {
-          float* st = stats + bh * 2 * Nq;
-          st[qrow] = m + logf(l);
-          st[Nq + qrow] = m;
-        }
+      if (qrow < Nq && wg == 0) {
+        float* st = stats + bh * 2 * Nq;
+        st[qrow] = m + logf(l);
+        st[Nq + qrow] = m;
       }
     }
   }
@@ -485,19 +604,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D>
+template <int D, bool kAux>
 cudaError_t launch_fp4_d(const AttnShape& s, const CUtensorMap& tq, const CUtensorMap& tk,
                          const CUtensorMap& tv, const uint8_t* q_sc, const uint8_t* k_sc, void* o,
-                         float* stats, int* err, cudaStream_t stream) {
+                         void* o_hp, float* stats, int* err, cudaStream_t stream) {
   using L = Fp4Layout<D>;
   static_assert(L::kAlloc <= 227u * 1024u, "shared memory");
   const dim3 grid((s.Nq + kTile - 1) / kTile, s.H, s.B);
-  cudaError_t e = cudaFuncSetAttribute(attn_fwd_fp4_kernel<D>,
+  cudaError_t e = cudaFuncSetAttribute(attn_fwd_fp4_kernel<D, kAux>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
-  attn_fwd_fp4_kernel<D><<<grid, kThreads, L::kAlloc, stream>>>(
-      tq, tk, tv, q_sc, k_sc, static_cast<__nv_bfloat16*>(o), stats, s.Nq, s.Nkv, s.H, s.scale,
-      s.causal, err);
+  attn_fwd_fp4_kernel<D, kAux><<<grid, kThreads, L::kAlloc, stream>>>(
+      tq, tk, tv, q_sc, k_sc, static_cast<__nv_bfloat16*>(o), static_cast<__nv_bfloat16*>(o_hp),
+      stats, s.Nq, s.Nkv, s.H, s.scale, s.causal, err);
   return cudaGetLastError();
 }
 
@@ -505,9 +624,14 @@ cudaError_t launch_fp4_d(const AttnShape& s, const CUtensorMap& tq, const CUtens
 
 cudaError_t launch_attn_fwd_fp4(const AttnShape& s, const CUtensorMap& tq, const CUtensorMap& tk,
                                 const CUtensorMap& tv, const uint8_t* q_sc, const uint8_t* k_sc,
-                                void* o, float* stats, int* err, cudaStream_t stream) {
-  return s.D == 128 ? launch_fp4_d<128>(s, tq, tk, tv, q_sc, k_sc, o, stats, err, stream)
-                    : launch_fp4_d<64>(s, tq, tk, tv, q_sc, k_sc, o, stats, err, stream);
+                                void* o, void* o_hp, float* stats, int* err, cudaStream_t stream) {
+  if (o_hp != nullptr)
+    return s.D == 128
+               ? launch_fp4_d<128, true>(s, tq, tk, tv, q_sc, k_sc, o, o_hp, stats, err, stream)
+               : launch_fp4_d<64, true>(s, tq, tk, tv, q_sc, k_sc, o, o_hp, stats, err, stream);
+  return s.D == 128
+             ? launch_fp4_d<128, false>(s, tq, tk, tv, q_sc, k_sc, o, nullptr, stats, err, stream)
+             : launch_fp4_d<64, false>(s, tq, tk, tv, q_sc, k_sc, o, nullptr, stats, err, stream);
 }
 
 }  // namespace nvq

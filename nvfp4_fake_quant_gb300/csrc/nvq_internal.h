@@ -130,10 +130,11 @@ cudaError_t launch_attn_fwd(const AttnShape& s, const CUtensorMap& tq, const CUt
                             cudaStream_t stream);
 // Dense forward with S on FP4 UMMAs: tq, tk map the packed codes of Q~ and K~
 // (make_bnhd_u8_map), q_sc, k_sc their scale blocks (launch_quant_attn_fp4),
-// tv the f16 V~ (make_bnhd_map).
+// tv the f16 V~ (make_bnhd_map); o_hp: NULL, or the auxiliary output P V~ / l
+// (bf16, layout of o).
 cudaError_t launch_attn_fwd_fp4(const AttnShape& s, const CUtensorMap& tq, const CUtensorMap& tk,
                                 const CUtensorMap& tv, const uint8_t* q_sc, const uint8_t* k_sc,
-                                void* o, float* stats, int* err, cudaStream_t stream);
+                                void* o, void* o_hp, float* stats, int* err, cudaStream_t stream);
 cudaError_t launch_bwd_prep(const AttnShape& s, const void* o, const void* dout, float* delta,
                             cudaStream_t stream);
 // dK, dV (key-outer; Q~, K~, V~, dO maps with 128-row boxes).  Block-sparse:
