@@ -375,8 +375,8 @@ nvq_status fwd_impl(const void* q, const void* k, const void* v, int B, int Nq, 
       (r = make_bnhd_u8_map(&mk4, kc, B, Nkv, H, D)) != 0)
     return fail_driver("cuTensorMapEncodeTiled", r);
   return from_cuda("attn_fwd", timed(NVQ_KERNEL_ATTN_FWD, stream, [&] {
-                     return launch_attn_fwd(s, mq, mk, mv, mq4, mk4, qs, ks, o, o_hp, stats,
-                                            kv_list, topk, err, stream);
+                     return launch_attn_fwd(s, mq, mk, mv, mq4, mk4, qs, ks, o, stats, kv_list,
+                                            topk, err, stream);
                    }));
 }
 

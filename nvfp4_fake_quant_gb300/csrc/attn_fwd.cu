@@ -26,21 +26,12 @@
 // into the first 32 of its own 64 S columns, which it has already loaded:
 // the 16-key slice kk of P~_i is at column 128 i + 64 (kk / 4) + 8 (kk % 4).
 //
-// Modes (template kMode; the dense form runs attn_fwd_fp4_kernel, so only the
-// block-sparse and auxiliary-output modes are instantiated):
+// Modes (template kMode; the dense form and the auxiliary output run
+// attn_fwd_fp4_kernel, so only the block-sparse mode is instantiated):
 //   kDense   every key tile, one K/V load per step shared by the two query tiles
-//            (the structure the other two modes specialise);
+//            (the structure the block-sparse mode specialises);
 //   kSparse  block-sparse: query tile i runs over its own listed key tiles, one
-//            load per query tile per step;
-//   kAux     the auxiliary high-precision output O_hp = P V~ / l next to O (the
-//            "auxiliary output" of the Attn-QAT backward, "use_high_prec_o"):
-//            one query tile per CTA, and the two softmax pairs take the even
-//            and the odd key tiles of it (key tile 2 j + i at step j for pair
-//            i).  Row maxima and sums are combined over all four warpgroups.
-//            TMEM: S_0, S_1 as above; O at [256, 256 + D), O_hp at
-//            [256 + D, 256 + 2 D).  Each warpgroup writes, per 32 keys c of its
-//            64, P~ into columns [32 c, 32 c + 16) and P (f16) into
-//            [32 c + 16, 32 c + 32) of its S columns (both already loaded).
+//            load per query tile per step; pass 1 on FP4 UMMAs.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -59,7 +50,7 @@ constexpr int kMmaWarp = 17;
 constexpr int kThreads = 576;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint32_t kAtomBlock = 128u * 128u;  // bytes of one 64-column block of a 128-row tile
-constexpr int kDense = 0, kSparse = 1, kAux = 2;  // forward modes
+constexpr int kDense = 0, kSparse = 1;  // forward modes
 
 // K/V tile ring (K and V tiles interleave in pass 2): 5 slots, 4 in the
 // block-sparse mode, whose two query tiles' FP4 codes take the room of the fifth.
@@ -73,8 +64,8 @@ struct FwdLayout {
   static constexpr uint32_t kQ = 0;                          // [2] query tiles
   static constexpr uint32_t kRingOff = kQ + 2u * kTileBytes;
   static constexpr uint32_t kX = kRingOff + kRing * kTileBytes;  // [2 tiles][128] f32
-  // codes + scale blocks of Q~ for the FP4 pass 1: block-sparse, one per query
-  // tile here; auxiliary output, in the unused second query-tile slot
+  // codes + scale blocks of Q~ for the FP4 pass 1 of the block-sparse mode, one
+  // per query tile
   static constexpr uint32_t kQ4s = kX + 1024u;
   static constexpr uint32_t kBars = kQ4s + (kMode == kSparse ? 2u * kC4 : 0u);
   static constexpr uint32_t kNumBars = 1 + 2 * kRing + 2 * 4 + 1;
@@ -101,15 +92,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tq4,
                     const __grid_constant__ CUtensorMap tk4, const uint8_t* __restrict__ q_sc,
                     const uint8_t* __restrict__ k_sc, __nv_bfloat16* __restrict__ o,
-                    __nv_bfloat16* __restrict__ o_hp, float* __restrict__ stats, int Nq, int Nkv,
+                    float* __restrict__ stats, int Nq, int Nkv,
                     int H, float scale, int causal, const int* __restrict__ kv_list, int topk,
                     int* __restrict__ err) {
   constexpr bool sparse = kMode == kSparse;
-  constexpr bool aux = kMode == kAux;
-  constexpr int kQTiles = aux ? 1 : 2;  // query tiles per CTA
+  constexpr int kQTiles = 2;  // query tiles per CTA
   using L = FwdLayout<D, kMode>;
   constexpr int kRing = L::kRing;
-  constexpr bool fp4_pass1 = kMode == kSparse || kMode == kAux;  // pass-1 S on FP4 UMMAs
+  constexpr bool fp4_pass1 = kMode == kSparse;  // pass-1 S on FP4 UMMAs
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023u) &
                                              ~static_cast<uintptr_t>(1023u));
@@ -132,14 +122,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_kv_all = (Nkv + kTile - 1) / kTile;
   // causal: the second query tile sees one more key tile than the first; both
   // run over it (the first tile's part of it is fully masked); block-sparse:
-  // topk listed key tiles per query tile; auxiliary output: two key tiles per
-  // step (a missing odd one is fully masked)
+  // topk listed key tiles per query tile
   int n_kv;
   if (sparse) {
     n_kv = topk;
-  } else if (aux) {
-    const int nk = causal ? min(n_kv_all, static_cast<int>(blockIdx.x) + 1) : n_kv_all;
-    n_kv = (nk + 1) / 2;
   } else {
     n_kv = causal ? min(n_kv_all, 2 * static_cast<int>(blockIdx.x) + 2) : n_kv_all;
   }
@@ -171,9 +157,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // Block-sparse: query tile i attends to the key tiles list_i[0..topk); a K or V
   // step then loads one tile per query tile.  Dense: key tile j at step j, one
-  // load shared by both query tiles.  Auxiliary output: key tile 2 j + i for
-  // pair i, one load per pair.
-  constexpr bool per_pair = sparse || aux;  // one K or V load per pair and step
+  // load shared by both query tiles.
+  constexpr bool per_pair = sparse;  // one K or V load per pair and step
   constexpr int nt = per_pair ? 2 : 1;      // loads per K or V step
   const int n_qt = (Nq + kTile - 1) / kTile;
   const int* list0 = nullptr;
@@ -185,7 +170,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     list1 = kv_list + (base + min(qt0 + 1, n_qt - 1)) * topk;  // a missing tile's rows are masked
   }
   auto key_tile = [&](int i, int j) -> int {
-    return sparse ? (i ? list1[j] : list0[j]) : aux ? 2 * j + i : j;
+    return sparse ? (i ? list1[j] : list0[j]) : j;
   };
 
   if (warp == kTmaWarp) {
@@ -215,7 +200,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tq4);
       tma_prefetch_desc(&tk4);
       for (int i = 0; i < kQTiles; ++i) {
-        uint8_t* q4 = smem + (aux ? L::kQ + L::kTileBytes : L::kQ4s + i * L::kC4);
+        uint8_t* q4 = smem + L::kQ4s + i * L::kC4;
         tma_load_4d_w(q4, &tq4, 0, q0 + i * kTile, h, b, q_full);
         if (qt0 + i < n_qt)
           bulk_load_w(q4 + L::kCodeBytes,
@@ -240,9 +225,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++li;
       return true;
     };
-    // FP4 pass 1: K~ as codes + scale blocks (a key tile past the last one, the
-    // missing odd tile of the last step of the auxiliary-output mode, gets zero
-    // codes and no scales: its scores are masked)
+    // FP4 pass 1: K~ as codes + scale blocks (a key tile past the last one gets
+    // zero codes and no scales: its scores are masked)
     auto load4 = [&](int tile) -> bool {
       const int slot = li % kRing;
       const uint32_t use = static_cast<uint32_t>(li / kRing);
@@ -285,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     auto issue_s = [&](int i, int idx) {  // S_i = Q~_i K~^T, K~ in ring slot of load idx
       const uint32_t kb = ring_addr + (idx % kRing) * L::kTileBytes;
-      const uint32_t qb = q_addr + (aux ? 0 : i) * L::kTileBytes;
+      const uint32_t qb = q_addr + i * L::kTileBytes;
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = (kk >> 2) * kAtomBlock + (kk & 3) * 32;
@@ -294,27 +278,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       umma_commit_w(&s_full[i]);
     };
-    // O_i += P~_i V~ with P~_i read from TMEM, V~ in the ring slot of load idx;
-    // auxiliary output: O += P~_i V~ and O_hp += P_i V~ (one O for both pairs)
+    // O_i += P~_i V~ with P~_i read from TMEM, V~ in the ring slot of load idx
     auto issue_pv = [&](int i, int idx, bool acc) {
       const uint32_t vb = ring_addr + (idx % kRing) * L::kTileBytes;
-      if constexpr (aux) {
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t col = i * 128 + 64 * (kk >> 2) + 32 * ((kk >> 1) & 1) + 8 * (kk & 1);
-          umma_f16_ts_w(tmem + 256, tmem + col, sdesc_sw128(vb + kk * 2048, kAtomBlock, 1024),
-                        idesc_pv, (acc || kk > 0) ? 1u : 0u);
-          umma_f16_ts_w(tmem + 256 + D, tmem + col + 16,
-                        sdesc_sw128(vb + kk * 2048, kAtomBlock, 1024), idesc_pv,
-                        (acc || kk > 0) ? 1u : 0u);
-        }
-      } else {
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_f16_ts_w(tmem + 256 + i * 128, tmem + i * 128 + 64 * (kk >> 2) + 8 * (kk & 3),
-                        sdesc_sw128(vb + kk * 2048, kAtomBlock, 1024), idesc_pv,
-                        (acc || kk > 0) ? 1u : 0u);
-      }
+      for (int kk = 0; kk < 8; ++kk)
+        umma_f16_ts_w(tmem + 256 + i * 128, tmem + i * 128 + 64 * (kk >> 2) + 8 * (kk & 3),
+                      sdesc_sw128(vb + kk * 2048, kAtomBlock, 1024), idesc_pv,
+                      (acc || kk > 0) ? 1u : 0u);
     };
     // Load idx of query tile i within a step whose loads start at `base`; a dense
     // load serves both tiles and is released after tile 1's UMMAs.
@@ -322,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto release = [&](int base, int i) {
       if (per_pair || i == 1) umma_commit_w(&r_empty[tile_load(base, i) % kRing]);
     };
-    // Pass 1 of the auxiliary-output and block-sparse modes: S on block-scaled
+    // Pass 1 of the block-sparse mode: S on block-scaled
     // FP4 UMMAs from the codes of Q~ and K~.  Pass 1 only needs the row maxima,
     // and the O columns [256, 512) are not live yet, so they hold the scale
     // operands: query tile qi's at [256 + 8 qi + 4 kk), those of pass-1 load c
@@ -332,11 +303,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t idesc_s4 = idesc_mxf4nvf4(128, 128);
     constexpr uint32_t lay4 = D == 128 ? 4u : 6u;  // (D/2)-byte swizzle of code rows
     constexpr uint32_t sbo4 = 8u * (D / 2);
-    auto q4_addr = [&](int qi) {
-      return smem_u32(smem + (aux ? L::kQ + L::kTileBytes : L::kQ4s + qi * L::kC4));
-    };
+    auto q4_addr = [&](int qi) { return smem_u32(smem + L::kQ4s + qi * L::kC4); };
     auto issue_s4 = [&](int i, int idx) {
-      const int qi = aux ? 0 : i;  // query tile of S_i
+      const int qi = i;  // query tile of S_i
       const uint32_t kb = ring_addr + (idx % kRing) * L::kTileBytes;
       const uint32_t sc = 272u + 8u * static_cast<uint32_t>(idx % 4);
       const uint32_t qa = q4_addr(qi);
@@ -390,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if ((per_pair || i == 0) && !(ok = wait_slot(tile_load(vbase, i)))) break;
         if (!(ok = mbar_wait_warp(&p_full[i], static_cast<uint32_t>(j & 1), abort))) break;
         tc_fence_after();
-        issue_pv(i, tile_load(vbase, i), j > 0 || (aux && i > 0));
+        issue_pv(i, tile_load(vbase, i), j > 0);
         release(vbase, i);
         if (kbase >= 0) {
           if ((per_pair || i == 0) && !(ok = wait_slot(tile_load(kbase, i)))) break;
@@ -416,7 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ti = wg >> 1;                // query tile
     const int hf = wg & 1;                 // half of the key columns
     const int t = threadIdx.x & 127;       // row in the tile == TMEM lane
-    const int tile_q0 = q0 + (aux ? 0 : ti * kTile);
+    const int tile_q0 = q0 + ti * kTile;
     const int qrow = tile_q0 + t;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t s_col = static_cast<uint32_t>(ti * 128 + hf * 64);
@@ -456,12 +425,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (hf == 0) xchg[t] = mraw = fmaxf(mraw, xchg[t]);
     named_bar_sync(pair_bar, kPairThreads);
     if (hf == 1) mraw = xchg[t];
-    if constexpr (aux) {  // both pairs hold the same rows: combine their maxima
-      const float* xall = reinterpret_cast<const float*>(smem + L::kX);
-      named_bar_sync(3, 2 * kPairThreads);
-      mraw = fmaxf(xall[t], xall[128 + t]);
-      named_bar_sync(3, 2 * kPairThreads);  // read before the sums reuse the area
-    }
     const float m = mraw * scale;
     const float negmb = -m * kLog2e;
     const uint64_t c12 = pk2(c1, c1), nmb2 = pk2(negmb, negmb);
@@ -496,25 +459,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           pquant16_pmax(x + 16 * hb, pp, ph);
 #pragma unroll
           for (int u = 0; u < 8; ++u) l2 = add2(l2, pk2(pp[2 * u], pp[2 * u + 1]));
-          if constexpr (aux) {
-            // P itself as f16 pairs: keys [64 hf + 32 c + 16 hb, +16) -> columns
-            // [64 hf + 32 c + 16 + 8 hb, +8), inside the 32 columns just loaded
-            uint32_t pr[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-              __half2 h2 = __floats2half2_rn(pp[2 * u], pp[2 * u + 1]);
-              pr[u] = *reinterpret_cast<uint32_t*>(&h2);
-            }
-            tmem_st8(tmem + lane_base + s_col + c * 32 + 16 + 8 * hb, pr);
-          }
         }
-        if constexpr (aux) {
-          // keys [64 hf + 32 c, +32): P~ -> columns [64 hf + 32 c, +16)
-          tmem_st16(tmem + lane_base + s_col + c * 32, pt);
-        } else {
-          // keys [64 hf + 32 c, +32) -> columns [64 hf + 16 c, +16) of S_i, already loaded
-          tmem_st16(tmem + lane_base + s_col + c * 16, pt);
-        }
+        // keys [64 hf + 32 c, +32) -> columns [64 hf + 16 c, +16) of S_i, already loaded
+        tmem_st16(tmem + lane_base + s_col + c * 16, pt);
       }
       tmem_wait_st();
       tc_fence_before();
@@ -529,18 +476,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (hf == 0) xchg[t] = l = l + xchg[t];
     named_bar_sync(pair_bar, kPairThreads);
     if (hf == 1) l = xchg[t];
-    if constexpr (aux) {
-      const float* xall = reinterpret_cast<const float*>(smem + L::kX);
-      named_bar_sync(3, 2 * kPairThreads);
-      l = xall[t] + xall[128 + t];
-    }
     if (have_o) {
       tc_fence_after();
       const float inv_l = 1.0f / l;
-      // auxiliary output: pair 0 writes O, pair 1 O_hp
-      __nv_bfloat16* obase = (aux && ti == 1) ? o_hp : o;
-      __nv_bfloat16* orow = obase + ((static_cast<int64_t>(b) * Nq + qrow) * H + h) * D + hf * (D / 2);
-      const uint32_t o_col = 256u + static_cast<uint32_t>(ti * (aux ? D : 128) + hf * (D / 2));
+      __nv_bfloat16* orow = o + ((static_cast<int64_t>(b) * Nq + qrow) * H + h) * D + hf * (D / 2);
+      const uint32_t o_col = 256u + static_cast<uint32_t>(ti * 128 + hf * (D / 2));
 #pragma unroll
       for (int c = 0; c < D / 64; ++c) {
         tmem_ld32(tmem + lane_base + o_col + c * 32, r);
@@ -559,7 +499,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             dst[u] = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
         }
       }
-      if (qrow < Nq && hf == 0 && (!aux || ti == 0)) {
+      if (qrow < Nq && hf == 0) {
         float* st = stats + (static_cast<int64_t>(b) * H + h) * 2 * Nq;
         st[qrow] = m + logf(l);
         st[Nq + qrow] = m;
@@ -579,50 +519,32 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-template <int D, int kMode>
-cudaError_t launch_fwd_t(const AttnShape& s, const CUtensorMap& tq, const CUtensorMap& tk,
-                         const CUtensorMap& tv, const CUtensorMap& tq4, const CUtensorMap& tk4,
-                         const uint8_t* q_sc, const uint8_t* k_sc, void* o, void* o_hp,
-                         float* stats, const int* kv_list, int topk, int* err,
-                         cudaStream_t stream) {
-  using L = FwdLayout<D, kMode>;
-  const int q_per_cta = (kMode == kAux ? 1 : 2) * kTile;
+template <int D>
+cudaError_t launch_sparse_d(const AttnShape& s, const CUtensorMap& tq, const CUtensorMap& tk,
+                            const CUtensorMap& tv, const CUtensorMap& tq4, const CUtensorMap& tk4,
+                            const uint8_t* q_sc, const uint8_t* k_sc, void* o, float* stats,
+                            const int* kv_list, int topk, int* err, cudaStream_t stream) {
+  using L = FwdLayout<D, kSparse>;
+  const int q_per_cta = 2 * kTile;
   const dim3 grid((s.Nq + q_per_cta - 1) / q_per_cta, s.H, s.B);
-  cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D, kMode>,
+  cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D, kSparse>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
-  attn_fwd_kernel<D, kMode><<<grid, kThreads, L::kAlloc, stream>>>(
-      tq, tk, tv, tq4, tk4, q_sc, k_sc, static_cast<__nv_bfloat16*>(o), static_cast<__nv_bfloat16*>(o_hp), stats, s.Nq,
-      s.Nkv, s.H, s.scale, s.causal, kv_list, topk, err);
+  attn_fwd_kernel<D, kSparse><<<grid, kThreads, L::kAlloc, stream>>>(
+      tq, tk, tv, tq4, tk4, q_sc, k_sc, static_cast<__nv_bfloat16*>(o), stats, s.Nq, s.Nkv, s.H,
+      s.scale, s.causal, kv_list, topk, err);
   return cudaGetLastError();
-}
-
-template <int D>
-cudaError_t launch_fwd_d(const AttnShape& s, const CUtensorMap& tq, const CUtensorMap& tk,
-                         const CUtensorMap& tv, const CUtensorMap& tq4, const CUtensorMap& tk4,
-                         const uint8_t* q_sc, const uint8_t* k_sc, void* o, void* o_hp,
-                         float* stats, const int* kv_list, int topk, int* err,
-                         cudaStream_t stream) {
-  if (kv_list != nullptr)
-    return launch_fwd_t<D, kSparse>(s, tq, tk, tv, tq4, tk4, q_sc, k_sc, o, o_hp, stats, kv_list,
-                                    topk, err, stream);
-  if (o_hp != nullptr)
-    return launch_fwd_t<D, kAux>(s, tq, tk, tv, tq4, tk4, q_sc, k_sc, o, o_hp, stats, kv_list,
-                                 topk, err, stream);
-  return cudaErrorInvalidValue;  // dense: attn_fwd_fp4_kernel
 }
 
 cudaError_t launch_attn_fwd(const AttnShape& s, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, const CUtensorMap& tq4, const CUtensorMap& tk4,
-                            const uint8_t* q_sc, const uint8_t* k_sc, void* o, void* o_hp,
-                            float* stats, const int* kv_list, int topk, int* err,
-                            cudaStream_t stream) {
-  if ((kv_list != nullptr) == (o_hp != nullptr)) return cudaErrorInvalidValue;
-  if (q_sc == nullptr || k_sc == nullptr) return cudaErrorInvalidValue;
-  return s.D == 128 ? launch_fwd_d<128>(s, tq, tk, tv, tq4, tk4, q_sc, k_sc, o, o_hp, stats,
-                                        kv_list, topk, err, stream)
-                    : launch_fwd_d<64>(s, tq, tk, tv, tq4, tk4, q_sc, k_sc, o, o_hp, stats,
-                                       kv_list, topk, err, stream);
+                            const uint8_t* q_sc, const uint8_t* k_sc, void* o, float* stats,
+                            const int* kv_list, int topk, int* err, cudaStream_t stream) {
+  if (kv_list == nullptr || q_sc == nullptr || k_sc == nullptr) return cudaErrorInvalidValue;
+  return s.D == 128 ? launch_sparse_d<128>(s, tq, tk, tv, tq4, tk4, q_sc, k_sc, o, stats,
+                                           kv_list, topk, err, stream)
+                    : launch_sparse_d<64>(s, tq, tk, tv, tq4, tk4, q_sc, k_sc, o, stats, kv_list,
+                                          topk, err, stream);
 }
 
 }  // namespace nvq
