@@ -87,14 +87,16 @@ __device__ __forceinline__ float ld_ahead(const float* p, bool pred) {
   return v;
 }
 
-// kSteps (4 or 8) kind::f16 UMMAs into one accumulator from a single asm block
-// and one elected lane: the first with the given accumulate flag, the rest
-// accumulating; the caller computes the (warp-uniform) descriptors.  The UMMA
-// warp shares its sub-partition's issue slots with elementwise warps, and one
-// block takes far fewer of them than kSteps separate elect-and-issue sequences.
+// kSteps (4 or 8) kind::f16 UMMAs into one accumulator, then tcgen05.commit
+// to c0 and c1, all from one asm block and one elected lane: the first UMMA with
+// the given accumulate flag, the rest accumulating.  The descriptors come
+// precomputed (outside the tile loop).  The issuing warps share their
+// sub-partitions with busy elementwise warps and get few issue slots, so
+// every instruction they need between a barrier and the UMMAs delays the UMMAs.
 template <int kSteps>
-__device__ __forceinline__ void umma_f16_steps_w(uint32_t d, const uint64_t* ad, const uint64_t* bd,
-                                                 uint32_t idesc, uint32_t acc) {
+__device__ __forceinline__ void umma_f16_group_w(uint32_t d, const uint64_t* ad, const uint64_t* bd,
+                                                 uint32_t idesc, uint32_t acc, uint64_t* c0,
+                                                 uint64_t* c1) {
   static_assert(kSteps == 4 || kSteps == 8, "4 or 8 K steps");
   if constexpr (kSteps == 8) {
     asm volatile(
@@ -109,10 +111,13 @@ __device__ __forceinline__ void umma_f16_steps_w(uint32_t d, const uint64_t* ad,
         "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %7, %15, %1, t;\n\t"
         "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %8, %16, %1, t;\n\t"
         "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %9, %17, %1, t;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %10, %18, %1, t;\n\t}" ::"r"(d),
-        "r"(idesc), "r"(acc), "l"(ad[0]), "l"(ad[1]), "l"(ad[2]), "l"(ad[3]), "l"(ad[4]),
-        "l"(ad[5]), "l"(ad[6]), "l"(ad[7]), "l"(bd[0]), "l"(bd[1]), "l"(bd[2]), "l"(bd[3]),
-        "l"(bd[4]), "l"(bd[5]), "l"(bd[6]), "l"(bd[7])
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %10, %18, %1, t;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%19];\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%20];\n\t}"
+        ::"r"(d), "r"(idesc), "r"(acc), "l"(ad[0]), "l"(ad[1]), "l"(ad[2]), "l"(ad[3]),
+        "l"(ad[4]), "l"(ad[5]), "l"(ad[6]), "l"(ad[7]), "l"(bd[0]), "l"(bd[1]), "l"(bd[2]),
+        "l"(bd[3]), "l"(bd[4]), "l"(bd[5]), "l"(bd[6]), "l"(bd[7]), "r"(smem_u32(c0)),
+        "r"(smem_u32(c1))
         : "memory");
   } else {
     asm volatile(
@@ -123,9 +128,51 @@ __device__ __forceinline__ void umma_f16_steps_w(uint32_t d, const uint64_t* ad,
         "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %7, %1, p;\n\t"
         "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %8, %1, t;\n\t"
         "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %9, %1, t;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %6, %10, %1, t;\n\t}" ::"r"(d),
-        "r"(idesc), "r"(acc), "l"(ad[0]), "l"(ad[1]), "l"(ad[2]), "l"(ad[3]), "l"(bd[0]),
-        "l"(bd[1]), "l"(bd[2]), "l"(bd[3])
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %6, %10, %1, t;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%11];\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%12];\n\t}"
+        ::"r"(d), "r"(idesc), "r"(acc), "l"(ad[0]), "l"(ad[1]), "l"(ad[2]), "l"(ad[3]),
+        "l"(bd[0]), "l"(bd[1]), "l"(bd[2]), "l"(bd[3]), "r"(smem_u32(c0)), "r"(smem_u32(c1))
+        : "memory");
+  }
+}
+
+// The S UMMAs (kind::mxf4nvf4, K = 64 each: D/64 of them) and commits to c0 and
+// c1 from one elected lane; sa/sb: TMEM addresses of the scale operands of the
+// first K step (each further step's are 4 columns on).
+template <int kSteps>
+__device__ __forceinline__ void umma_fp4_group_w(uint32_t d, const uint64_t* ad, const uint64_t* bd,
+                                                 uint32_t idesc, uint32_t sa, uint32_t sb,
+                                                 uint64_t* c0, uint64_t* c1) {
+  static_assert(kSteps == 1 || kSteps == 2, "D = 64 or 128");
+  if constexpr (kSteps == 2) {
+    asm volatile(
+        "{\n\t.reg .pred e, t, f;\n\t.reg .b32 sa1, sb1;\n\t"
+        "setp.eq.u32 t, 0, 0;\n\t"
+        "setp.ne.u32 f, 0, 0;\n\t"
+        "add.u32 sa1, %4, 4;\n\t"
+        "add.u32 sb1, %5, 4;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %2, %6, %1, "
+        "[%4], [%5], f;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %3, %7, %1, "
+        "[sa1], [sb1], t;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%8];\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%9];\n\t}"
+        ::"r"(d), "r"(idesc), "l"(ad[0]), "l"(ad[1]), "r"(sa), "r"(sb), "l"(bd[0]), "l"(bd[1]),
+        "r"(smem_u32(c0)), "r"(smem_u32(c1))
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred e, f;\n\t"
+        "setp.ne.u32 f, 0, 0;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %2, %3, %1, "
+        "[%4], [%5], f;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%6];\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%7];\n\t}"
+        ::"r"(d), "r"(idesc), "l"(ad[0]), "l"(bd[0]), "r"(sa), "r"(sb), "r"(smem_u32(c0)),
+        "r"(smem_u32(c1))
         : "memory");
   }
 }
@@ -325,10 +372,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t do_addr = smem_u32(smem + L::kDO);
     const uint32_t p_addr = smem_u32(smem + L::kP);
     const uint32_t ds_addr = smem_u32(smem + L::kDS);
-    // S_{it} from slot it & 1: its Q~ scales go to TMEM first (their columns were
-    // last read by S_{it-2}, complete since dP_{it-1} was issued after S_{it-1}
-    // had been loaded)
-    auto issue_s = [&](int it) -> bool {
+    // Descriptors of every operand the UMMAs read, computed once: a K step
+    // moves a descriptor's start address (bits 0-13, address / 16) by the
+    // step's byte offset / 16, with no carry out of the field (shared-memory
+    // addresses stay below 2^18).
+    auto koff = [](int kk) {  // K-major bf16 tile: K step kk (16 elements)
+      return static_cast<uint32_t>((kk >> 2) * kAtomBlock + (kk & 3) * 32);
+    };
+    // S_{it} from slot it & 1: the copy of its Q~ scales to TMEM (their columns
+    // were last read by S_{it-2}, complete since dP_{it-1} was issued after
+    // S_{it-1} had been loaded) is issued before the wait for the S/dP buffer,
+    // then the UMMAs and their commits as one group
+    auto prep_s = [&](int it) -> bool {
       const int st = it & 1;
       if (!mbar_wait_warp(&q4_full[st], static_cast<uint32_t>((it >> 1) & 1), abort)) return false;
       tc_fence_after();
@@ -337,85 +392,99 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int kk = 0; kk < D / 64; ++kk)
         tmem_cp_32x128_x4_w(tmem + sc + 4 * kk, qa + L::kCodeBytes + kk * 512);
-#pragma unroll
-      for (int kk = 0; kk < D / 64; ++kk)
-        umma_fp4_ss_w(tmem + kColSP, sdesc(qa + 32 * kk, 16, sbo, lay),
-                      sdesc(k4_addr + 32 * kk, 16, sbo, lay), idesc_s4, tmem + sc + 4 * kk,
-                      tmem + kColScK + 4 * kk, kk > 0 ? 1u : 0u);
-      umma_commit_w(s_full);
-      umma_commit_w(&q4_empty[st]);
       return true;
     };
-    auto issue_dp = [&](int it) -> bool {  // dP = dO V~^T, contraction over D
-      const int st = it & 1;
-      if (!mbar_wait_warp(&do_full[st], static_cast<uint32_t>((it >> 1) & 1), abort)) return false;
-      tc_fence_after();
-      const uint32_t da = do_addr + st * L::kTileBytes;
-      uint64_t ad[D / 16], bd[D / 16];
+    uint64_t s_ad[2][D / 64], s_bd[D / 64];
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = (kk >> 2) * kAtomBlock + (kk & 3) * 32;
-        ad[kk] = sdesc_sw128(da + off, 16, 1024);
-        bd[kk] = sdesc_sw128(v_addr + off, 16, 1024);
-      }
-      umma_f16_steps_w<D / 16>(tmem + kColSP, ad, bd, idesc_p, 0u);
-      umma_commit_w(dp_full);
-      return true;
-    };
-    // contraction over the 128 queries of a tile (MN-major operands)
-    auto issue_t = [&](uint32_t dcol, uint32_t a0, uint32_t b0, uint32_t acc) {
-      uint64_t ad[8], bd[8];
+    for (int kk = 0; kk < D / 64; ++kk) {
+      s_bd[kk] = sdesc(k4_addr + 32 * kk, 16, sbo, lay);
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        ad[kk] = sdesc_sw128(a0 + kk * 2048, kAtomBlock, 1024);
-        bd[kk] = sdesc_sw128(b0 + kk * 2048, kAtomBlock, 1024);
-      }
-      umma_f16_steps_w<8>(tmem + dcol, ad, bd, idesc_t, acc);
-    };
-    auto issue_dk = [&](int it) -> bool {  // dK += dS^T Q~
-      if (!mbar_wait_warp(ds_full, static_cast<uint32_t>(it & 1), abort) ||
-          !mbar_wait_warp(qb_full, static_cast<uint32_t>(it & 1), abort))
-        return false;
-      tc_fence_after();
-      issue_t(kColDK, ds_addr, qb_addr, it > 0 ? 1u : 0u);
-      umma_commit_w(ds_free);
-      umma_commit_w(qb_empty);
-      return true;
+      for (int st = 0; st < 2; ++st) s_ad[st][kk] = sdesc(q4_addr + st * L::kC4 + 32 * kk, 16, sbo, lay);
+    }
+    // (the slot is a branch, not an index, so the descriptors stay in registers)
+    auto fire_s = [&](int it) {
+      if (it & 1)
+        umma_fp4_group_w<D / 64>(tmem + kColSP, s_ad[1], s_bd, idesc_s4, tmem + kColScQ + 8u,
+                                 tmem + kColScK, s_full, &q4_empty[1]);
+      else
+        umma_fp4_group_w<D / 64>(tmem + kColSP, s_ad[0], s_bd, idesc_s4, tmem + kColScQ,
+                                 tmem + kColScK, s_full, &q4_empty[0]);
     };
     const int w = warp == kMmaWarp ? 0 : 1;
     bool ok = true;
     if (w == 0) {
+      // dP = dO V~^T, contraction over D
+      uint64_t dp_ad[2][D / 16], dp_bd[D / 16];
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk) {
+        dp_bd[kk] = sdesc_sw128(v_addr + koff(kk), 16, 1024);
+#pragma unroll
+        for (int st = 0; st < 2; ++st)
+          dp_ad[st][kk] = sdesc_sw128(do_addr + st * L::kTileBytes + koff(kk), 16, 1024);
+      }
       ok = mbar_wait_warp(kv_full, 0, abort) && n_iter > 0;
       if (ok) {  // the K~ scales stay in TMEM for the whole kernel
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 64; ++kk)
           tmem_cp_32x128_x4_w(tmem + kColScK + 4 * kk, k4_addr + L::kCodeBytes + kk * 512);
-        ok = issue_s(0);
+        if ((ok = prep_s(0))) fire_s(0);
       }
       for (int it = 0; it < n_iter && ok; ++it) {
         const uint32_t ph = static_cast<uint32_t>(it & 1);
+        const int st = it & 1;
+        // dO of this tile (loaded long before) first, then the buffer
+        if (!(ok = mbar_wait_warp(&do_full[st], static_cast<uint32_t>((it >> 1) & 1), abort)))
+          break;
         if (!(ok = mbar_wait_warp(s_free, ph, abort))) break;
         tc_fence_after();
-        if (!(ok = issue_dp(it))) break;
-        umma_commit_w(&do_empty[it & 1]);
+        if (st)
+          umma_f16_group_w<D / 16>(tmem + kColSP, dp_ad[1], dp_bd, idesc_p, 0u, dp_full,
+                                   &do_empty[1]);
+        else
+          umma_f16_group_w<D / 16>(tmem + kColSP, dp_ad[0], dp_bd, idesc_p, 0u, dp_full,
+                                   &do_empty[0]);
         if (it + 1 < n_iter) {
+          if (!(ok = prep_s(it + 1))) break;
           if (!(ok = mbar_wait_warp(dp_free, ph, abort))) break;
           tc_fence_after();
-          if (!(ok = issue_s(it + 1))) break;
+          fire_s(it + 1);
         }
       }
     } else {
+      // dV += (P~/l)^T dO and dK += dS^T Q~, contractions over the 128 queries
+      // of a tile (MN-major operands, K step kk at 2048 kk bytes)
+      uint64_t dv_ad[8], dv_bd[2][8], dk_ad[8], dk_bd[8];
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        dv_ad[kk] = sdesc_sw128(p_addr + kk * 2048, kAtomBlock, 1024);
+        dk_ad[kk] = sdesc_sw128(ds_addr + kk * 2048, kAtomBlock, 1024);
+        dk_bd[kk] = sdesc_sw128(qb_addr + kk * 2048, kAtomBlock, 1024);
+#pragma unroll
+        for (int st = 0; st < 2; ++st)
+          dv_bd[st][kk] = sdesc_sw128(do_addr + st * L::kTileBytes + kk * 2048, kAtomBlock, 1024);
+      }
+      auto issue_dk = [&](int it) -> bool {  // dK += dS^T Q~ (bf16 Q~ first: loaded earlier)
+        if (!mbar_wait_warp(qb_full, static_cast<uint32_t>(it & 1), abort) ||
+            !mbar_wait_warp(ds_full, static_cast<uint32_t>(it & 1), abort))
+          return false;
+        tc_fence_after();
+        umma_f16_group_w<8>(tmem + kColDK, dk_ad, dk_bd, idesc_t, it > 0 ? 1u : 0u, ds_free,
+                            qb_empty);
+        return true;
+      };
       for (int it = 0; it < n_iter && ok; ++it) {
         if (it > 0 && !(ok = issue_dk(it - 1))) break;
         const int st = it & 1;
-        if (!(ok = mbar_wait_warp(pt_full, static_cast<uint32_t>(it & 1), abort)) ||
-            !(ok = mbar_wait_warp(&do_full[st], static_cast<uint32_t>((it >> 1) & 1), abort)))
+        if (!(ok = mbar_wait_warp(&do_full[st], static_cast<uint32_t>((it >> 1) & 1), abort)) ||
+            !(ok = mbar_wait_warp(pt_full, static_cast<uint32_t>(it & 1), abort)))
           break;
         tc_fence_after();
-        issue_t(kColDV, p_addr, do_addr + st * L::kTileBytes, it > 0 ? 1u : 0u);
-        umma_commit_w(pt_free);
-        umma_commit_w(&do_empty[st]);
+        if (st)
+          umma_f16_group_w<8>(tmem + kColDV, dv_ad, dv_bd[1], idesc_t, 1u, pt_free, &do_empty[1]);
+        else
+          umma_f16_group_w<8>(tmem + kColDV, dv_ad, dv_bd[0], idesc_t, it > 0 ? 1u : 0u, pt_free,
+                              &do_empty[0]);
       }
       if (ok && n_iter > 0 && (ok = issue_dk(n_iter - 1))) umma_commit_w(dkdv_done);
     }
