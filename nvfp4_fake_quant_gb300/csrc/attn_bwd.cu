@@ -87,96 +87,6 @@ __device__ __forceinline__ float ld_ahead(const float* p, bool pred) {
   return v;
 }
 
-// kSteps (4 or 8) kind::f16 UMMAs into one accumulator, then tcgen05.commit
-// to c0 and c1, all from one asm block and one elected lane: the first UMMA with
-// the given accumulate flag, the rest accumulating.  The descriptors come
-// precomputed (outside the tile loop).  The issuing warps share their
-// sub-partitions with busy elementwise warps and get few issue slots, so
-// every instruction they need between a barrier and the UMMAs delays the UMMAs.
-template <int kSteps>
-__device__ __forceinline__ void umma_f16_group_w(uint32_t d, const uint64_t* ad, const uint64_t* bd,
-                                                 uint32_t idesc, uint32_t acc, uint64_t* c0,
-                                                 uint64_t* c1) {
-  static_assert(kSteps == 4 || kSteps == 8, "4 or 8 K steps");
-  if constexpr (kSteps == 8) {
-    asm volatile(
-        "{\n\t.reg .pred p, e, t;\n\t"
-        "setp.ne.b32 p, %2, 0;\n\t"
-        "setp.eq.u32 t, 0, 0;\n\t"
-        "elect.sync _|e, 0xffffffff;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %11, %1, p;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %12, %1, t;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %13, %1, t;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %6, %14, %1, t;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %7, %15, %1, t;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %8, %16, %1, t;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %9, %17, %1, t;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %10, %18, %1, t;\n\t"
-        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%19];\n\t"
-        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%20];\n\t}"
-        ::"r"(d), "r"(idesc), "r"(acc), "l"(ad[0]), "l"(ad[1]), "l"(ad[2]), "l"(ad[3]),
-        "l"(ad[4]), "l"(ad[5]), "l"(ad[6]), "l"(ad[7]), "l"(bd[0]), "l"(bd[1]), "l"(bd[2]),
-        "l"(bd[3]), "l"(bd[4]), "l"(bd[5]), "l"(bd[6]), "l"(bd[7]), "r"(smem_u32(c0)),
-        "r"(smem_u32(c1))
-        : "memory");
-  } else {
-    asm volatile(
-        "{\n\t.reg .pred p, e, t;\n\t"
-        "setp.ne.b32 p, %2, 0;\n\t"
-        "setp.eq.u32 t, 0, 0;\n\t"
-        "elect.sync _|e, 0xffffffff;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %7, %1, p;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %8, %1, t;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %9, %1, t;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %6, %10, %1, t;\n\t"
-        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%11];\n\t"
-        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%12];\n\t}"
-        ::"r"(d), "r"(idesc), "r"(acc), "l"(ad[0]), "l"(ad[1]), "l"(ad[2]), "l"(ad[3]),
-        "l"(bd[0]), "l"(bd[1]), "l"(bd[2]), "l"(bd[3]), "r"(smem_u32(c0)), "r"(smem_u32(c1))
-        : "memory");
-  }
-}
-
-// The S UMMAs (kind::mxf4nvf4, K = 64 each: D/64 of them) and commits to c0 and
-// c1 from one elected lane; sa/sb: TMEM addresses of the scale operands of the
-// first K step (each further step's are 4 columns on).
-template <int kSteps>
-__device__ __forceinline__ void umma_fp4_group_w(uint32_t d, const uint64_t* ad, const uint64_t* bd,
-                                                 uint32_t idesc, uint32_t sa, uint32_t sb,
-                                                 uint64_t* c0, uint64_t* c1) {
-  static_assert(kSteps == 1 || kSteps == 2, "D = 64 or 128");
-  if constexpr (kSteps == 2) {
-    asm volatile(
-        "{\n\t.reg .pred e, t, f;\n\t.reg .b32 sa1, sb1;\n\t"
-        "setp.eq.u32 t, 0, 0;\n\t"
-        "setp.ne.u32 f, 0, 0;\n\t"
-        "add.u32 sa1, %4, 4;\n\t"
-        "add.u32 sb1, %5, 4;\n\t"
-        "elect.sync _|e, 0xffffffff;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %2, %6, %1, "
-        "[%4], [%5], f;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %3, %7, %1, "
-        "[sa1], [sb1], t;\n\t"
-        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%8];\n\t"
-        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%9];\n\t}"
-        ::"r"(d), "r"(idesc), "l"(ad[0]), "l"(ad[1]), "r"(sa), "r"(sb), "l"(bd[0]), "l"(bd[1]),
-        "r"(smem_u32(c0)), "r"(smem_u32(c1))
-        : "memory");
-  } else {
-    asm volatile(
-        "{\n\t.reg .pred e, f;\n\t"
-        "setp.ne.u32 f, 0, 0;\n\t"
-        "elect.sync _|e, 0xffffffff;\n\t"
-        "@e tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %2, %3, %1, "
-        "[%4], [%5], f;\n\t"
-        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%6];\n\t"
-        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%7];\n\t}"
-        ::"r"(d), "r"(idesc), "l"(ad[0]), "l"(bd[0]), "r"(sa), "r"(sb), "r"(smem_u32(c0)),
-        "r"(smem_u32(c1))
-        : "memory");
-  }
-}
-
 template <int D>
 struct BwdLayout {
   static constexpr uint32_t kTileBytes = 128u * D * 2u;  // a bf16 128-row tile
@@ -405,10 +315,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto fire_s = [&](int it) {
       if (it & 1)
         umma_fp4_group_w<D / 64>(tmem + kColSP, s_ad[1], s_bd, idesc_s4, tmem + kColScQ + 8u,
-                                 tmem + kColScK, s_full, &q4_empty[1]);
+                                 tmem + kColScK, bar_u32(s_full), bar_u32(&q4_empty[1]));
       else
         umma_fp4_group_w<D / 64>(tmem + kColSP, s_ad[0], s_bd, idesc_s4, tmem + kColScQ,
-                                 tmem + kColScK, s_full, &q4_empty[0]);
+                                 tmem + kColScK, bar_u32(s_full), bar_u32(&q4_empty[0]));
     };
     const int w = warp == kMmaWarp ? 0 : 1;
     bool ok = true;
@@ -439,11 +349,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = mbar_wait_warp(s_free, ph, abort))) break;
         tc_fence_after();
         if (st)
-          umma_f16_group_w<D / 16>(tmem + kColSP, dp_ad[1], dp_bd, idesc_p, 0u, dp_full,
-                                   &do_empty[1]);
+          umma_f16_group_w<D / 16>(tmem + kColSP, dp_ad[1], dp_bd, idesc_p, 0u, bar_u32(dp_full),
+                                   bar_u32(&do_empty[1]));
         else
-          umma_f16_group_w<D / 16>(tmem + kColSP, dp_ad[0], dp_bd, idesc_p, 0u, dp_full,
-                                   &do_empty[0]);
+          umma_f16_group_w<D / 16>(tmem + kColSP, dp_ad[0], dp_bd, idesc_p, 0u, bar_u32(dp_full),
+                                   bar_u32(&do_empty[0]));
         if (it + 1 < n_iter) {
           if (!(ok = prep_s(it + 1))) break;
           if (!(ok = mbar_wait_warp(dp_free, ph, abort))) break;
@@ -469,8 +379,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             !mbar_wait_warp(ds_full, static_cast<uint32_t>(it & 1), abort))
           return false;
         tc_fence_after();
-        umma_f16_group_w<8>(tmem + kColDK, dk_ad, dk_bd, idesc_t, it > 0 ? 1u : 0u, ds_free,
-                            qb_empty);
+        umma_f16_group_w<8>(tmem + kColDK, dk_ad, dk_bd, idesc_t, it > 0 ? 1u : 0u,
+                            bar_u32(ds_free), bar_u32(qb_empty));
         return true;
       };
       for (int it = 0; it < n_iter && ok; ++it) {
@@ -481,10 +391,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         tc_fence_after();
         if (st)
-          umma_f16_group_w<8>(tmem + kColDV, dv_ad, dv_bd[1], idesc_t, 1u, pt_free, &do_empty[1]);
+          umma_f16_group_w<8>(tmem + kColDV, dv_ad, dv_bd[1], idesc_t, 1u, bar_u32(pt_free),
+                              bar_u32(&do_empty[1]));
         else
-          umma_f16_group_w<8>(tmem + kColDV, dv_ad, dv_bd[0], idesc_t, it > 0 ? 1u : 0u, pt_free,
-                              &do_empty[0]);
+          umma_f16_group_w<8>(tmem + kColDV, dv_ad, dv_bd[0], idesc_t, it > 0 ? 1u : 0u,
+                              bar_u32(pt_free), bar_u32(&do_empty[0]));
       }
       if (ok && n_iter > 0 && (ok = issue_dk(n_iter - 1))) umma_commit_w(dkdv_done);
     }

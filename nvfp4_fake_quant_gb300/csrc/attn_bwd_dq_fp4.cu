@@ -241,6 +241,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     // dP_{j-1}.  The K~ scales are copied before that last wait, off the path
     // from the release to the UMMAs (their columns were last read by S_{j-2},
     // complete since this warp saw S_{j-2} and dP_{j-2} released).
+    // Descriptors, computed once: the Q~ codes (a 64-element K step is 32 bytes,
+    // 2 in the start-address field), dO and the V~ slots (K step kk of a
+    // K-major bf16 tile at byte (kk / 4) 16384 + (kk % 4) 32)
+    uint64_t q_d[D / 64], dp_ad[D / 16], dp_bd[kVSlots][D / 16];
+#pragma unroll
+    for (int kk = 0; kk < D / 64; ++kk) q_d[kk] = sdesc(q_addr + 32 * kk, 16, sbo, lay);
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const uint32_t off = (kk >> 2) * L::kBlock + (kk & 3) * 32;
+      dp_ad[kk] = sdesc_sw128(do_addr + off, 16, 1024);
+#pragma unroll
+      for (int vs = 0; vs < kVSlots; ++vs)
+        dp_bd[vs][kk] = sdesc_sw128(v_addr + vs * L::kTileBytes + off, 16, 1024);
+    }
+    static_assert(kVSlots == 2, "the V~ slot is a branch below");
     auto issue_step = [&](int j) -> bool {
       const int k4s = j % kK4Slots, vs = j % kVSlots;
       if (!mbar_wait_warp(&k4_full[k4s], static_cast<uint32_t>((j / kK4Slots) & 1), abort))
@@ -255,21 +270,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         return false;
       if (j > 0 && !mbar_wait_warp(sdp_free, static_cast<uint32_t>((j - 1) & 1), abort)) return false;
       tc_fence_after();
-#pragma unroll
-      for (int kk = 0; kk < D / 64; ++kk)
-        umma_fp4_ss_w(tmem + kColS, sdesc(q_addr + 32 * kk, 16, sbo, lay),
-                      sdesc(kb + 32 * kk, 16, sbo, lay), idesc_s4, tmem + kScA + 4 * kk,
-                      tmem + sc + 4 * kk, kk > 0 ? 1u : 0u);
-      const uint32_t vb = v_addr + vs * L::kTileBytes;
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t off = (kk >> 2) * L::kBlock + (kk & 3) * 32;
-        umma_f16_ss_w(tmem + kColDP, sdesc_sw128(do_addr + off, 16, 1024),
-                      sdesc_sw128(vb + off, 16, 1024), idesc_p, kk > 0 ? 1u : 0u);
-      }
-      umma_commit_w(sdp_full);
-      umma_commit_w(&k4_empty[k4s]);  // the K~ codes of step j are no longer needed
-      umma_commit_w(&v_empty[vs]);    // V~_j is no longer needed
+      uint64_t kd[D / 64];
+      kd[0] = sdesc(kb, 16, sbo, lay);
+      if constexpr (D == 128) kd[1] = kd[0] + 2;
+      // S, then the K~ codes of step j are no longer needed
+      umma_fp4_group_w<D / 64>(tmem + kColS, q_d, kd, idesc_s4, tmem + kScA, tmem + sc,
+                               bar_u32(&k4_empty[k4s]), 0u);
+      // dP, then S_j and dP_j are in TMEM and V~_j is no longer needed
+      if (vs)
+        umma_f16_group_w<D / 16>(tmem + kColDP, dp_ad, dp_bd[1], idesc_p, 0u, bar_u32(sdp_full),
+                                 bar_u32(&v_empty[1]));
+      else
+        umma_f16_group_w<D / 16>(tmem + kColDP, dp_ad, dp_bd[0], idesc_p, 0u, bar_u32(sdp_full),
+                                 bar_u32(&v_empty[0]));
       return true;
     };
     bool ok = mbar_wait_warp(q_full, 0, abort);
@@ -286,6 +299,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------------------------------------------------------- dQ
     constexpr uint32_t idesc_q = idesc_f16(128, D, 1, 0, 1);  // dQ (A in TMEM, B MN-major)
     const uint32_t k_addr = smem_u32(smem + L::kK);
+    const uint64_t k_d0 = sdesc_sw128(k_addr, L::kBlock, 1024);  // bf16 K~ slot 0, keys 0-15
+    uint32_t a[8];  // dS_j, 16 keys (8 columns) per K step
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) a[kk] = tmem + kColDS + kk * 8;
     bool ok = true;
     for (int j = 0; j < n && ok; ++j) {
       const int ks = j % kKSlots;
@@ -293,14 +310,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           !(ok = mbar_wait_warp(&k_full[ks], static_cast<uint32_t>((j / kKSlots) & 1), abort)))
         break;
       tc_fence_after();
-      const uint32_t kb = k_addr + ks * L::kTileBytes;
-#pragma unroll
-      for (int kk = 0; kk < kStep / 16; ++kk)  // dQ += dS K~: contraction over 128 keys
-        umma_f16_ts_w(tmem + kColDQ, tmem + kColDS + kk * 8,
-                      sdesc_sw128(kb + kk * 2048, L::kBlock, 1024), idesc_q,
-                      (j > 0 || kk > 0) ? 1u : 0u);
-      umma_commit_w(ds_free);
-      umma_commit_w(&k_empty[ks]);  // bf16 K~_j is no longer needed
+      // dQ += dS K~: contraction over the 128 keys; then bf16 K~_j is no longer needed
+      static_assert(kStep == 128, "eight K steps of 16 keys");
+      umma_f16_ts8_w(tmem + kColDQ, a, k_d0 + static_cast<uint64_t>(ks) * (L::kTileBytes >> 4),
+                     idesc_q, j > 0 ? 1u : 0u, bar_u32(ds_free), bar_u32(&k_empty[ks]));
     }
     if (ok) umma_commit_w(dq_done);
     umma_commit_w(&mma_drain[1]);

@@ -209,33 +209,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_cp_32x128_x4_w(tmem + sc + 4 * kk, kb + L::kCodeBytes + kk * 512);
     return true;
   };
-  // fire_s: the UMMAs of a prepared tile (after its S buffer is free); the K~
-  // slot is released by a commit here in pass 2, by the softmax in pass 1
+  // Descriptors of the Q~ codes (fixed) and of a K~ slot's codes: a 64-element
+  // K step is 32 bytes on (2 in the descriptor's start-address field).
+  uint64_t q_d[D / 64];
+#pragma unroll
+  for (int kk = 0; kk < D / 64; ++kk) q_d[kk] = sdesc(q_addr + 32 * kk, 16, sbo, lay);
+  auto k_desc = [&](uint32_t kb, uint64_t (&kd)[D / 64]) {
+    kd[0] = sdesc(kb, 16, sbo, lay);
+    if constexpr (D == 128) kd[1] = kd[0] + 2;
+  };
+  // fire_s: the UMMAs of a prepared tile (after its S buffer is free) and their
+  // commits as one group; the K~ slot is released by a commit here in pass 2,
+  // by the softmax in pass 1
   auto fire_s = [&](uint32_t col, int kl, int g, uint64_t* bar) {
     const int slot = kl % kKRing;
-    const uint32_t kb = k_ring + slot * L::kKSlot;
-    const uint32_t sc = sc_region(g);
-#pragma unroll
-    for (int kk = 0; kk < D / 64; ++kk)
-      umma_fp4_ss_w(tmem + col, sdesc(q_addr + 32 * kk, 16, sbo, lay),
-                    sdesc(kb + 32 * kk, 16, sbo, lay), idesc_s, tmem + kScA + 4 * kk,
-                    tmem + sc + 4 * kk, kk > 0 ? 1u : 0u);
-    umma_commit_w(bar);
-    if (g >= nk) umma_commit_w(&k_empty[slot]);
+    uint64_t kd[D / 64];
+    k_desc(k_ring + slot * L::kKSlot, kd);
+    umma_fp4_group_w<D / 64>(tmem + col, q_d, kd, idesc_s, tmem + kScA, tmem + sc_region(g),
+                             bar_u32(bar), g >= nk ? bar_u32(&k_empty[slot]) : 0u);
   };
   // Auxiliary output, pass 2: half hh (keys [64 hh, 64 hh + 64)) of the K~ tile
   // of load kl into the 64-column buffer at `col`; the tile's scales at column sc
   constexpr uint32_t idesc_h = idesc_mxf4nvf4(128, 64);
   auto fire_half = [&](uint32_t col, int kl, uint32_t sc, int hh, uint64_t* bar) {
     const int slot = kl % kKRing;
-    const uint32_t kb = k_ring + slot * L::kKSlot + static_cast<uint32_t>(hh) * 64u * (D / 2);
-#pragma unroll
-    for (int kk = 0; kk < D / 64; ++kk)
-      umma_fp4_ss_w(tmem + col, sdesc(q_addr + 32 * kk, 16, sbo, lay),
-                    sdesc(kb + 32 * kk, 16, sbo, lay), idesc_h, tmem + kScA2 + 4 * kk,
-                    tmem + sc + 4 * kk + 2 * hh, kk > 0 ? 1u : 0u);
-    umma_commit_w(bar);
-    if (hh == 1) umma_commit_w(&k_empty[slot]);
+    uint64_t kd[D / 64];
+    k_desc(k_ring + slot * L::kKSlot + static_cast<uint32_t>(hh) * 64u * (D / 2), kd);
+    umma_fp4_group_w<D / 64>(tmem + col, q_d, kd, idesc_h, tmem + kScA2,
+                             tmem + sc + 2 * static_cast<uint32_t>(hh), bar_u32(bar),
+                             hh == 1 ? bar_u32(&k_empty[slot]) : 0u);
   };
   // Pass 1, tile j (load j) into buffer j % 3 once the softmax has loaded tile
   // j - 3 from there.  The S warp takes the even tiles, the P~V~ warp (idle
@@ -368,6 +370,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ P~V~ issuer
     constexpr uint32_t idesc_pv = idesc_f16(128, D, 0, 0, 1);
     const uint32_t v_ring = smem_u32(smem + L::kVRingOff);
+    // V~ slot s: descriptor of its first 16 keys, 2048 * s on from slot 0's
+    const uint64_t v_d0 = sdesc_sw128(v_ring, 128u * 128u, 1024);
+    auto v_desc = [&](int slot) { return v_d0 + static_cast<uint64_t>(slot) * (L::kVSlot >> 4); };
     // the Q~ scale copy (S warp) precedes the odd pass-1 tiles' UMMAs
     bool ok = mbar_wait_warp(q_sc_ready, 0, abort);
     if (ok) {
@@ -379,15 +384,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!(ok = mbar_wait_warp(&v_full[slot], static_cast<uint32_t>((j / kVRing) & 1), abort))) break;
       if (!(ok = mbar_wait_warp(&p_full[buf], static_cast<uint32_t>((j >> 1) & 1), abort))) break;
       tc_fence_after();
-      const uint32_t vb = v_ring + slot * L::kVSlot;
       // keys [16 kk, 16 kk + 16): warpgroup kk / 2, its P~ columns 8 (kk % 2)
+      uint32_t a[8];
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
-        umma_f16_ts_w(tmem + 256, tmem + 128 * buf + 32 * (kk >> 1) + 8 * (kk & 1),
-                      sdesc_sw128(vb + kk * 2048, 128u * 128u, 1024), idesc_pv,
-                      (j > 0 || kk > 0) ? 1u : 0u);
-      umma_commit_w(&pv_done[buf]);
-      umma_commit_w(&v_empty[slot]);
+        a[kk] = tmem + 128u * static_cast<uint32_t>(buf) + 32 * (kk >> 1) + 8 * (kk & 1);
+      umma_f16_ts8_w(tmem + 256, a, v_desc(slot), idesc_pv, j > 0 ? 1u : 0u,
+                     bar_u32(&pv_done[buf]), bar_u32(&v_empty[slot]));
     }
     // auxiliary output: per half u, keys [64 hh + 16 w, +16) from warpgroup w's
     // columns of buffer u % 3, P~ into O and P into O_hp
@@ -398,16 +401,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       if (!(ok = mbar_wait_warp(&p_full[c], static_cast<uint32_t>((u / 3) & 1), abort))) break;
       tc_fence_after();
-      const uint32_t vb = v_ring + slot * L::kVSlot;
+      uint32_t a[4];
 #pragma unroll
-      for (int w = 0; w < 4; ++w) {
-        const uint64_t bd = sdesc_sw128(vb + (4 * hh + w) * 2048, 128u * 128u, 1024);
-        const uint32_t acc = (u > 0 || w > 0) ? 1u : 0u;
-        umma_f16_ts_w(tmem + 256, tmem + 64 * c + 16 * w, bd, idesc_pv, acc);
-        umma_f16_ts_w(tmem + 256 + D, tmem + 64 * c + 16 * w + 8, bd, idesc_pv, acc);
-      }
-      umma_commit_w(&pv_done[c]);
-      if (hh == 1) umma_commit_w(&v_empty[slot]);
+      for (int w = 0; w < 4; ++w) a[w] = tmem + 64u * static_cast<uint32_t>(c) + 16 * w;
+      umma_f16_ts4x2_w(tmem + 256, tmem + 256 + D, a, v_desc(slot) + 512u * hh, idesc_pv,
+                       u > 0 ? 1u : 0u, bar_u32(&pv_done[c]),
+                       hh == 1 ? bar_u32(&v_empty[slot]) : 0u);
     }
     if (ok) umma_commit_w(o_full);
     umma_commit_w(&drain[1]);

@@ -318,6 +318,177 @@ __device__ __forceinline__ void umma_commit_mc_w(uint64_t* bar, uint16_t mask) {
       : "memory");
 }
 
+// ------------------------------------------- grouped issue with commits
+// A group of UMMAs and the tcgen05.commit(s) after them from one asm block and
+// one elected lane, operands precomputed by the caller.  The issuing warps share
+// their sub-partitions with busy elementwise warps and get few issue slots, so
+// every instruction between the barrier that releases a group and the UMMAs
+// delays the UMMAs.  Commits go to the mbarrier at shared address c0 and, unless
+// c1 is 0 (no barrier lives at shared address 0), to c1.
+//
+// kSteps (4 or 8) kind::f16 UMMAs into one accumulator, A and B from
+// shared-memory descriptors: the first with the given accumulate flag, the rest
+// accumulating.
+template <int kSteps>
+__device__ __forceinline__ void umma_f16_group_w(uint32_t d, const uint64_t* ad, const uint64_t* bd,
+                                                 uint32_t idesc, uint32_t acc, uint32_t c0,
+                                                 uint32_t c1) {
+  static_assert(kSteps == 4 || kSteps == 8, "4 or 8 K steps");
+  if constexpr (kSteps == 8) {
+    asm volatile(
+        "{\n\t.reg .pred p, e, t, q;\n\t"
+        "setp.ne.b32 p, %2, 0;\n\t"
+        "setp.eq.u32 t, 0, 0;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.and.u32 q, %20, 0, e;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %11, %1, p;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %12, %1, t;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %13, %1, t;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %6, %14, %1, t;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %7, %15, %1, t;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %8, %16, %1, t;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %9, %17, %1, t;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %10, %18, %1, t;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%19];\n\t"
+        "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%20];\n\t}"
+        ::"r"(d), "r"(idesc), "r"(acc), "l"(ad[0]), "l"(ad[1]), "l"(ad[2]), "l"(ad[3]),
+        "l"(ad[4]), "l"(ad[5]), "l"(ad[6]), "l"(ad[7]), "l"(bd[0]), "l"(bd[1]), "l"(bd[2]),
+        "l"(bd[3]), "l"(bd[4]), "l"(bd[5]), "l"(bd[6]), "l"(bd[7]), "r"(c0), "r"(c1)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p, e, t, q;\n\t"
+        "setp.ne.b32 p, %2, 0;\n\t"
+        "setp.eq.u32 t, 0, 0;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.and.u32 q, %12, 0, e;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %7, %1, p;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %8, %1, t;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %9, %1, t;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %6, %10, %1, t;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%11];\n\t"
+        "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%12];\n\t}"
+        ::"r"(d), "r"(idesc), "r"(acc), "l"(ad[0]), "l"(ad[1]), "l"(ad[2]), "l"(ad[3]),
+        "l"(bd[0]), "l"(bd[1]), "l"(bd[2]), "l"(bd[3]), "r"(c0), "r"(c1)
+        : "memory");
+  }
+}
+
+// kSteps (1 or 2) block-scaled kind::mxf4nvf4 UMMAs (K = 64 each) starting a
+// fresh accumulator; sa/sb: TMEM addresses of the scale operands of the first K
+// step (the next step's are 4 columns on).
+template <int kSteps>
+__device__ __forceinline__ void umma_fp4_group_w(uint32_t d, const uint64_t* ad, const uint64_t* bd,
+                                                 uint32_t idesc, uint32_t sa, uint32_t sb,
+                                                 uint32_t c0, uint32_t c1) {
+  static_assert(kSteps == 1 || kSteps == 2, "D = 64 or 128");
+  if constexpr (kSteps == 2) {
+    asm volatile(
+        "{\n\t.reg .pred e, t, f, q;\n\t.reg .b32 sa1, sb1;\n\t"
+        "setp.eq.u32 t, 0, 0;\n\t"
+        "setp.ne.u32 f, 0, 0;\n\t"
+        "add.u32 sa1, %4, 4;\n\t"
+        "add.u32 sb1, %5, 4;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.and.u32 q, %9, 0, e;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %2, %6, %1, "
+        "[%4], [%5], f;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %3, %7, %1, "
+        "[sa1], [sb1], t;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%8];\n\t"
+        "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%9];\n\t}"
+        ::"r"(d), "r"(idesc), "l"(ad[0]), "l"(ad[1]), "r"(sa), "r"(sb), "l"(bd[0]), "l"(bd[1]),
+        "r"(c0), "r"(c1)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred e, f, q;\n\t"
+        "setp.ne.u32 f, 0, 0;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.and.u32 q, %7, 0, e;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %2, %3, %1, "
+        "[%4], [%5], f;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%6];\n\t"
+        "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%7];\n\t}"
+        ::"r"(d), "r"(idesc), "l"(ad[0]), "l"(bd[0]), "r"(sa), "r"(sb), "r"(c0), "r"(c1)
+        : "memory");
+  }
+}
+
+// Eight kind::f16 UMMAs (K = 16 each) into the accumulator d with A read from
+// TMEM at a[k] and B through the descriptor b0 advanced by 2048 k bytes (128 k
+// in its start-address field, which does not carry below 2^18 bytes of shared
+// memory): an MN-major B whose K steps are 16 rows of 128 bytes.
+__device__ __forceinline__ void umma_f16_ts8_w(uint32_t d, const uint32_t (&a)[8], uint64_t b0,
+                                               uint32_t idesc, uint32_t acc, uint32_t c0,
+                                               uint32_t c1) {
+  asm volatile(
+      "{\n\t.reg .pred p, e, t, q;\n\t.reg .b32 lo, hi;\n\t"
+      ".reg .b64 b1, b2, b3, b4, b5, b6, b7;\n\t"
+      "setp.ne.b32 p, %2, 0;\n\t"
+      "setp.eq.u32 t, 0, 0;\n\t"
+      "mov.b64 {lo, hi}, %11;\n\t"
+      "add.u32 lo, lo, 128;\n\tmov.b64 b1, {lo, hi};\n\t"
+      "add.u32 lo, lo, 128;\n\tmov.b64 b2, {lo, hi};\n\t"
+      "add.u32 lo, lo, 128;\n\tmov.b64 b3, {lo, hi};\n\t"
+      "add.u32 lo, lo, 128;\n\tmov.b64 b4, {lo, hi};\n\t"
+      "add.u32 lo, lo, 128;\n\tmov.b64 b5, {lo, hi};\n\t"
+      "add.u32 lo, lo, 128;\n\tmov.b64 b6, {lo, hi};\n\t"
+      "add.u32 lo, lo, 128;\n\tmov.b64 b7, {lo, hi};\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.and.u32 q, %13, 0, e;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %11, %1, p;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%4], b1, %1, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%5], b2, %1, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%6], b3, %1, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%7], b4, %1, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%8], b5, %1, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%9], b6, %1, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%10], b7, %1, t;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%12];\n\t"
+      "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%13];\n\t}"
+      ::"r"(d), "r"(idesc), "r"(acc), "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(a[4]),
+      "r"(a[5]), "r"(a[6]), "r"(a[7]), "l"(b0), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+// Four pairs of kind::f16 UMMAs with A in TMEM: pair k adds A at a[k] into d0
+// and A at a[k] + 8 into d1, both with B through b0 advanced by 2048 k bytes;
+// the first pair with the given accumulate flag.
+__device__ __forceinline__ void umma_f16_ts4x2_w(uint32_t d0, uint32_t d1, const uint32_t (&a)[4],
+                                                 uint64_t b0, uint32_t idesc, uint32_t acc,
+                                                 uint32_t c0, uint32_t c1) {
+  asm volatile(
+      "{\n\t.reg .pred p, e, t, q;\n\t.reg .b32 lo, hi, a0, a1, a2, a3;\n\t"
+      ".reg .b64 b1, b2, b3;\n\t"
+      "setp.ne.b32 p, %3, 0;\n\t"
+      "setp.eq.u32 t, 0, 0;\n\t"
+      "mov.b64 {lo, hi}, %8;\n\t"
+      "add.u32 lo, lo, 128;\n\tmov.b64 b1, {lo, hi};\n\t"
+      "add.u32 lo, lo, 128;\n\tmov.b64 b2, {lo, hi};\n\t"
+      "add.u32 lo, lo, 128;\n\tmov.b64 b3, {lo, hi};\n\t"
+      "add.u32 a0, %4, 8;\n\tadd.u32 a1, %5, 8;\n\t"
+      "add.u32 a2, %6, 8;\n\tadd.u32 a3, %7, 8;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.and.u32 q, %10, 0, e;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%4], %8, %2, p;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%1], [a0], %8, %2, p;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%5], b1, %2, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%1], [a1], b1, %2, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%6], b2, %2, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%1], [a2], b2, %2, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%7], b3, %2, t;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%1], [a3], b3, %2, t;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%9];\n\t"
+      "@q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%10];\n\t}"
+      ::"r"(d0), "r"(d1), "r"(idesc), "r"(acc), "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]),
+      "l"(b0), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+// Shared-memory address of an mbarrier as a commit target (0: none).
+__device__ __forceinline__ uint32_t bar_u32(uint64_t* bar) { return smem_u32(bar); }
+
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
