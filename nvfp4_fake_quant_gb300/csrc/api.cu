@@ -257,9 +257,9 @@ size_t bytes_bnhd(int B, int N, int H, int D, size_t elem) {
 // Forward workspace: every region at its own offset (nvq_attn_layout).  Every
 // form writes the quantized operands once: the packed codes of Q~ and K~ (qc,
 // kc) with their scale blocks (qs, ks), V~ as f16 (v16), and Q~, K~, V~ as bf16
-// (qb, kb, vb).  The dense forward reads the codes and v16, the block-sparse
-// and auxiliary-output forms (BF16 S) qb, kb and v16; attn_qat_bwd_saved reads
-// the codes and the bf16 copies.  The block-sparse forward writes qb, kb, v16 only.
+// (qb, kb, vb).  The forward (dense, auxiliary-output or block-sparse) reads the
+// codes, their scale blocks and v16; attn_qat_bwd_saved and its block-sparse form
+// read the codes and the bf16 copies.
 struct FwdWs {
   size_t qc, kc, qs, ks, v16, qb, kb, vb, total;
 };
@@ -348,35 +348,21 @@ nvq_status fwd_impl(const void* q, const void* k, const void* v, int B, int Nq, 
   void* vb = wb + w.vb;
   // Q~, K~, V~ in every form the forward and a later backward from the saved
   // operands read
-  const bool sparse = kv_list != nullptr;
   const AttnOpSpec ops[3] = {{q, Nq, qc, qs, qb, nullptr},
                              {k, Nkv, kc, ks, kb, nullptr},
                              {v, Nkv, nullptr, nullptr, vb, v16}};
   if ((e = timed(NVQ_KERNEL_QUANTIZE, stream,
                  [&] { return launch_quant_attn_ops(ops, 3, B, H, D, stream); })) != cudaSuccess)
     return fail_cuda("quantize q, k, v", e);
-  if (!sparse) {
-    // dense (with or without the auxiliary output): S on FP4 UMMAs, Q~ and K~
-    // as codes + scale blocks
-    if ((r = make_bnhd_u8_map(&mq, qc, B, Nq, H, D)) != 0 ||
-        (r = make_bnhd_u8_map(&mk, kc, B, Nkv, H, D)) != 0 ||
-        (r = make_bnhd_map(&mv, v16, B, Nkv, H, D, true)) != 0)
-      return fail_driver("cuTensorMapEncodeTiled", r);
-    return from_cuda("attn_fwd", timed(NVQ_KERNEL_ATTN_FWD, stream, [&] {
-                       return launch_attn_fwd_fp4(s, mq, mk, mv, qs, ks, o, o_hp, stats, err,
-                                                  stream);
-                     }));
-  }
-  CUtensorMap mq4, mk4;  // codes of Q~, K~ for the FP4 pass 1
-  if ((r = make_bnhd_map(&mq, qb, B, Nq, H, D, false)) != 0 ||
-      (r = make_bnhd_map(&mk, kb, B, Nkv, H, D, false)) != 0 ||
-      (r = make_bnhd_map(&mv, v16, B, Nkv, H, D, true)) != 0 ||
-      (r = make_bnhd_u8_map(&mq4, qc, B, Nq, H, D)) != 0 ||
-      (r = make_bnhd_u8_map(&mk4, kc, B, Nkv, H, D)) != 0)
+  // S on FP4 UMMAs: Q~ and K~ as codes + scale blocks (dense, auxiliary output
+  // or block-sparse)
+  if ((r = make_bnhd_u8_map(&mq, qc, B, Nq, H, D)) != 0 ||
+      (r = make_bnhd_u8_map(&mk, kc, B, Nkv, H, D)) != 0 ||
+      (r = make_bnhd_map(&mv, v16, B, Nkv, H, D, true)) != 0)
     return fail_driver("cuTensorMapEncodeTiled", r);
   return from_cuda("attn_fwd", timed(NVQ_KERNEL_ATTN_FWD, stream, [&] {
-                     return launch_attn_fwd(s, mq, mk, mv, mq4, mk4, qs, ks, o, stats, kv_list,
-                                            topk, err, stream);
+                     return launch_attn_fwd_fp4(s, mq, mk, mv, qs, ks, o, o_hp, stats, kv_list,
+                                                topk, err, stream);
                    }));
 }
 

@@ -66,6 +66,12 @@
 // O_hp), the K~ scale operand of pass-2 tile j at [200 + 8 (j % 4), +8); a
 // half reads the scale columns of its 64 keys, 2 (u % 2) columns in (key n of
 // a 128-key region is at column n / 32).  Pass 1 is unchanged.
+//
+// Block-sparse form (kSparseFwd; the "VSA" fine branch, "vsqa-preview-1.3b
+// metadata.json", attention.selection): step j of both passes visits key tile
+// list[j] of the query tile's topk selected tiles instead of tile j; the TMA
+// warp loads the listed tiles, nothing else changes (the sparse calls take
+// N % 128 == 0 and no causal mask, so no listed key is masked).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -85,6 +91,7 @@ constexpr int kPvWarp = 18;
 constexpr int kKRing = 6;
 constexpr int kVRing = 4;
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kDenseFwd = 0, kAuxFwd = 1, kSparseFwd = 2;  // kernel modes
 constexpr uint32_t kScA = 384, kScB = 392;  // TMEM columns of the scale operands
 constexpr int kScRegions = 12;               // K~ scale copies at kScB + 8 r, up to 488
 // auxiliary-output pass 2: the Q~ scale operand and four K~ scale regions
@@ -111,15 +118,20 @@ struct Fp4Layout {
   static constexpr uint32_t kAlloc = kAbort + 4u + 1024u;
 };
 
-// Grid: (ceil(Nq / 128), H, B).
-template <int D, bool kAux>
+// Grid: (ceil(Nq / 128), H, B).  kMode: kDenseFwd, kAuxFwd (o_hp) or
+// kSparseFwd (kv_list: int32 [B, H, ceil(Nq/128), topk], the key tiles of each
+// query tile, in the order they are visited).
+template <int D, int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_fp4_kernel(const __grid_constant__ CUtensorMap tq,
                         const __grid_constant__ CUtensorMap tk,
                         const __grid_constant__ CUtensorMap tv, const uint8_t* __restrict__ q_sc,
                         const uint8_t* __restrict__ k_sc, __nv_bfloat16* __restrict__ o,
                         __nv_bfloat16* __restrict__ o_hp, float* __restrict__ stats, int Nq,
-                        int Nkv, int H, float scale, int causal, int* __restrict__ err) {
+                        int Nkv, int H, float scale, int causal,
+                        const int* __restrict__ kv_list, int topk, int* __restrict__ err) {
+  constexpr bool kAux = kMode == kAuxFwd;
+  constexpr bool kSparse = kMode == kSparseFwd;
   using L = Fp4Layout<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023u) &
@@ -150,8 +162,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int n_kt = (Nkv + kTile - 1) / kTile;
   const int n_qt = (Nq + kTile - 1) / kTile;
-  // key tiles this query tile sees (causal: up to its diagonal tile)
-  const int nk = causal ? min(n_kt, qt + 1) : n_kt;
+  // key tiles this query tile sees (causal: up to its diagonal tile;
+  // block-sparse: its topk listed tiles, step j visiting tile list[j])
+  const int nk = kSparse ? topk : causal ? min(n_kt, qt + 1) : n_kt;
+  const int* list = kSparse ? kv_list + (bh * n_qt + qt) * topk : nullptr;
 
   if (threadIdx.x == 0) {
     *abort = 0;
@@ -271,15 +285,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < kVRing; ++s) v_last[s] = -1;
     int kli = 0, vli = 0;
     bool ok = true;
+    // key tile of step j (a listed tile outside [0, n_kt), which the caller must
+    // not pass, reads zero codes and no scales instead of memory it does not own)
+    auto tile_of = [&](int j) { return kSparse ? __ldg(list + j) : j; };
     auto load_k = [&](int tile) -> bool {
       const int slot = kli % kKRing;
       const uint32_t use = static_cast<uint32_t>(kli / kKRing);
       if (!mbar_wait_warp(&k_empty[slot], (use & 1u) ^ 1u, abort)) return false;
       uint8_t* dst = smem + L::kKRingOff + slot * L::kKSlot;
-      mbar_arrive_expect_tx_w(&k_full[slot], L::kCodeBytes + L::kScBytes);
+      const bool have = !kSparse || (tile >= 0 && tile < n_kt);
+      mbar_arrive_expect_tx_w(&k_full[slot], L::kCodeBytes + (have ? L::kScBytes : 0u));
       tma_load_4d_w(dst, &tk, 0, tile * kTile, h, b, &k_full[slot]);
-      bulk_load_w(dst + L::kCodeBytes, k_sc + (bh * n_kt + tile) * L::kScBytes, L::kScBytes,
-                  &k_full[slot]);
+      if (have)
+        bulk_load_w(dst + L::kCodeBytes, k_sc + (bh * n_kt + tile) * L::kScBytes, L::kScBytes,
+                    &k_full[slot]);
       k_last[slot] = static_cast<int>(use & 1u);
       ++kli;
       return true;
@@ -297,11 +316,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++vli;
       return true;
     };
-    for (int j = 0; j < nk && ok; ++j) ok = load_k(j);
-    for (int j = 0; j < 2 && j < nk && ok; ++j) ok = load_k(j);
+    for (int j = 0; j < nk && ok; ++j) ok = load_k(tile_of(j));
+    for (int j = 0; j < 2 && j < nk && ok; ++j) ok = load_k(tile_of(j));
     for (int j = 0; j < nk && ok; ++j) {
-      ok = load_v(j);
-      if (ok && j + 2 < nk) ok = load_k(j + 2);
+      ok = load_v(tile_of(j));
+      if (ok && j + 2 < nk) ok = load_k(tile_of(j + 2));
     }
     if (!ok) {  // let the copies in flight land before the block exits
       mbar_wait_warp(q_full, 0, nullptr, 10000000ull);
@@ -433,8 +452,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         if ((warp & 3) == 0) mbar_arrive_warp(&k_empty[j % kKRing]);  // S_j read its K~ slot
         const uint32_t col = 128u * static_cast<uint32_t>(j % 3);
+        // (block-sparse: N % 128 == 0 and non-causal, so no listed tile has a
+        // masked key)
         const int k0 = j * kTile;
-        const bool edge = k0 + kTile > Nkv || (causal && k0 + kTile - 1 > q0);
+        const bool edge = !kSparse && (k0 + kTile > Nkv || (causal && k0 + kTile - 1 > q0));
         float mx[4] = {mraw, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
@@ -526,7 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         up2(fma2(pk2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])), c12, nmb2),
             x[2 * i], x[2 * i + 1]);
       const int k0 = key0(j);
-      if (is_edge(k0)) {
+      if (!kSparse && is_edge(k0)) {
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           const int key = k0 + i;
@@ -603,34 +624,49 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, bool kAux>
+template <int D, int kMode>
 cudaError_t launch_fp4_d(const AttnShape& s, const CUtensorMap& tq, const CUtensorMap& tk,
                          const CUtensorMap& tv, const uint8_t* q_sc, const uint8_t* k_sc, void* o,
-                         void* o_hp, float* stats, int* err, cudaStream_t stream) {
+                         void* o_hp, float* stats, const int* kv_list, int topk, int* err,
+                         cudaStream_t stream) {
   using L = Fp4Layout<D>;
   static_assert(L::kAlloc <= 227u * 1024u, "shared memory");
   const dim3 grid((s.Nq + kTile - 1) / kTile, s.H, s.B);
-  cudaError_t e = cudaFuncSetAttribute(attn_fwd_fp4_kernel<D, kAux>,
+  cudaError_t e = cudaFuncSetAttribute(attn_fwd_fp4_kernel<D, kMode>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, L::kAlloc);
   if (e != cudaSuccess) return e;
-  attn_fwd_fp4_kernel<D, kAux><<<grid, kThreads, L::kAlloc, stream>>>(
+  attn_fwd_fp4_kernel<D, kMode><<<grid, kThreads, L::kAlloc, stream>>>(
       tq, tk, tv, q_sc, k_sc, static_cast<__nv_bfloat16*>(o), static_cast<__nv_bfloat16*>(o_hp),
-      stats, s.Nq, s.Nkv, s.H, s.scale, s.causal, err);
+      stats, s.Nq, s.Nkv, s.H, s.scale, s.causal, kv_list, topk, err);
   return cudaGetLastError();
+}
+
+template <int kMode>
+cudaError_t launch_fp4_mode(const AttnShape& s, const CUtensorMap& tq, const CUtensorMap& tk,
+                            const CUtensorMap& tv, const uint8_t* q_sc, const uint8_t* k_sc,
+                            void* o, void* o_hp, float* stats, const int* kv_list, int topk,
+                            int* err, cudaStream_t stream) {
+  return s.D == 128 ? launch_fp4_d<128, kMode>(s, tq, tk, tv, q_sc, k_sc, o, o_hp, stats, kv_list,
+                                               topk, err, stream)
+                    : launch_fp4_d<64, kMode>(s, tq, tk, tv, q_sc, k_sc, o, o_hp, stats, kv_list,
+                                              topk, err, stream);
 }
 
 }  // namespace
 
 cudaError_t launch_attn_fwd_fp4(const AttnShape& s, const CUtensorMap& tq, const CUtensorMap& tk,
                                 const CUtensorMap& tv, const uint8_t* q_sc, const uint8_t* k_sc,
-                                void* o, void* o_hp, float* stats, int* err, cudaStream_t stream) {
+                                void* o, void* o_hp, float* stats, const int* kv_list, int topk,
+                                int* err, cudaStream_t stream) {
+  if (o_hp != nullptr && kv_list != nullptr) return cudaErrorInvalidValue;
+  if (kv_list != nullptr)
+    return launch_fp4_mode<kSparseFwd>(s, tq, tk, tv, q_sc, k_sc, o, nullptr, stats, kv_list, topk,
+                                       err, stream);
   if (o_hp != nullptr)
-    return s.D == 128
-               ? launch_fp4_d<128, true>(s, tq, tk, tv, q_sc, k_sc, o, o_hp, stats, err, stream)
-               : launch_fp4_d<64, true>(s, tq, tk, tv, q_sc, k_sc, o, o_hp, stats, err, stream);
-  return s.D == 128
-             ? launch_fp4_d<128, false>(s, tq, tk, tv, q_sc, k_sc, o, nullptr, stats, err, stream)
-             : launch_fp4_d<64, false>(s, tq, tk, tv, q_sc, k_sc, o, nullptr, stats, err, stream);
+    return launch_fp4_mode<kAuxFwd>(s, tq, tk, tv, q_sc, k_sc, o, o_hp, stats, nullptr, 0, err,
+                                    stream);
+  return launch_fp4_mode<kDenseFwd>(s, tq, tk, tv, q_sc, k_sc, o, nullptr, stats, nullptr, 0, err,
+                                    stream);
 }
 
 }  // namespace nvq

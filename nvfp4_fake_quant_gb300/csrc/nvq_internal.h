@@ -117,20 +117,16 @@ int make_bnhd_u8_map(CUtensorMap* map, const void* base, int B, int N, int H, in
 int make_bnhd_map(CUtensorMap* map, const void* base, int B, int N, int H, int D, bool f16,
                    int box_rows = kTile);
 
-// Block-sparse forward (BF16 S in pass 2): kv_list: int32 [B, H, ceil(Nq/128),
-// topk] key tiles per query tile.  Pass 1 runs on FP4 UMMAs: tq4, tk4 map the
-// codes of Q~, K~ (make_bnhd_u8_map) and q_sc, k_sc are their scale blocks.
-cudaError_t launch_attn_fwd(const AttnShape& s, const CUtensorMap& tq, const CUtensorMap& tk,
-                            const CUtensorMap& tv, const CUtensorMap& tq4, const CUtensorMap& tk4,
-                            const uint8_t* q_sc, const uint8_t* k_sc, void* o, float* stats,
-                            const int* kv_list, int topk, int* err, cudaStream_t stream);
-// Dense forward with S on FP4 UMMAs: tq, tk map the packed codes of Q~ and K~
+// Forward with S on FP4 UMMAs: tq, tk map the packed codes of Q~ and K~
 // (make_bnhd_u8_map), q_sc, k_sc their scale blocks (launch_quant_attn_fp4),
-// tv the f16 V~ (make_bnhd_map); o_hp: NULL, or the auxiliary output P V~ / l
-// (bf16, layout of o).
+// tv the f16 V~ (make_bnhd_map).  At most one of: o_hp, the auxiliary output
+// P V~ / l (bf16, layout of o); kv_list, the block-sparse key tiles, int32
+// [B, H, ceil(Nq/128), topk], entries in [0, ceil(Nkv/128)) (N % 128 == 0,
+// non-causal).
 cudaError_t launch_attn_fwd_fp4(const AttnShape& s, const CUtensorMap& tq, const CUtensorMap& tk,
                                 const CUtensorMap& tv, const uint8_t* q_sc, const uint8_t* k_sc,
-                                void* o, void* o_hp, float* stats, int* err, cudaStream_t stream);
+                                void* o, void* o_hp, float* stats, const int* kv_list, int topk,
+                                int* err, cudaStream_t stream);
 cudaError_t launch_bwd_prep(const AttnShape& s, const void* o, const void* dout, float* delta,
                             cudaStream_t stream);
 // dK, dV (key-outer; Q~, K~, V~, dO maps with 128-row boxes).  Block-sparse:

@@ -24,9 +24,8 @@
 //                   whose outputs leave the normal fp32 range to quant16_static.
 //  * pquant16       the softmax probabilities inside attention (fp32 inputs):
 //                   reciprocal and product without snapping.  The forward and
-//                   the backward run this same code on S values that agree up
-//                   to the summation order of their UMMAs (FP4 in the forward,
-//                   BF16 in the dK/dV kernel).
+//                   the dK/dV kernel run this same code on S from the same FP4
+//                   UMMA on the same codes and scales.
 #pragma once
 #include <cstdint>
 #include <cuda_bf16.h>
@@ -320,35 +319,6 @@ __device__ __forceinline__ void pquant16(const float* x, float (&p)[16], uint32_
   const uint32_t sb = e4m3_rn_sat(block_amax_p(x) * (1.0f / 6.0f));
 #pragma unroll
   for (int i = 0; i < 16; ++i) p[i] = ex2_f32(x[i]);
-  const uint32_t s_h = e4m3_to_f16x2(sb);
-  const uint32_t s_h2 = (s_h & 0xFFFFu) | (s_h << 16);
-  const float s = f16lo_to_f32(s_h);
-  const float inv = s > 0.f ? rcp_approx(s) : 0.f;
-  const uint64_t inv2 = pk2(inv, inv);
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    float q0, q1;
-    up2(mul2(pk2(p[2 * j], p[2 * j + 1]), inv2), q0, q1);
-    pt[j] = hmul2(e2m1_pair_f16x2(q0, q1), s_h2);
-  }
-}
-
-// pquant16 with the block maximum taken over the sixteen 2^x: the same bits
-// (block_amax_p) for one exponential less per block.  The BF16-S forward
-// (auxiliary-output and block-sparse modes) measured faster with this form, the
-// FP4 forward and the dK/dV kernel with block_amax_p.
-__device__ __forceinline__ void pquant16_pmax(const float* x, float (&p)[16], uint32_t (&pt)[8]) {
-#pragma unroll
-  for (int i = 0; i < 16; ++i) p[i] = ex2_f32(x[i]);
-  float a = max3f(p[0], p[1], p[2]);
-  a = max3f(a, p[3], p[4]);
-  a = max3f(a, p[5], p[6]);
-  a = max3f(a, p[7], p[8]);
-  a = max3f(a, p[9], p[10]);
-  a = max3f(a, p[11], p[12]);
-  a = max3f(a, p[13], p[14]);
-  a = fmaxf(a, p[15]);
-  const uint32_t sb = e4m3_rn_sat(a * (1.0f / 6.0f));
   const uint32_t s_h = e4m3_to_f16x2(sb);
   const uint32_t s_h2 = (s_h & 0xFFFFu) | (s_h << 16);
   const float s = f16lo_to_f32(s_h);
