@@ -61,9 +61,10 @@ __device__ __forceinline__ void quant_block(const Block16& v, const float g, con
 
 // Contiguous operands (row strides equal to the row lengths): block i of the
 // flattened matrix at element 16 i, scale byte i, code bytes 8 i.  Each thread
-// loads several blocks (a grid stride apart) before quantizing any, to keep
-// more loads in flight: four with a unit scale, two with a static one (whose
-// longer arithmetic needs the registers).
+// takes several blocks a pass (a grid stride apart): four with a unit scale, two
+// with a static one (whose longer arithmetic needs the registers), and issues
+// the next pass's loads before this pass's arithmetic, so that HBM reads stay in
+// flight while the threads quantize (the grid is one wave, a few passes each).
 template <int MODE>
 __global__ void __launch_bounds__(256) fake_quant_flat_kernel(
     const uint16_t* __restrict__ x, int64_t nblocks, const float* __restrict__ gsf,
@@ -72,12 +73,18 @@ __global__ void __launch_bounds__(256) fake_quant_flat_kernel(
   const float g = (MODE == kStaticBf16) ? *gsf : 1.0f;
   const float inv_g = (MODE == kStaticBf16) ? __frcp_rn(g) : 1.0f;
   const int64_t step = static_cast<int64_t>(gridDim.x) * blockDim.x;
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < nblocks;
-       i += kUnroll * step) {
-    Block16 v[kUnroll];
+  int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  Block16 v[kUnroll];
+#pragma unroll
+  for (int u = 0; u < kUnroll; ++u)
+    if (i + u * step < nblocks) v[u] = load_block(x + (i + u * step) * 16);
+  for (; i < nblocks; i += kUnroll * step) {
+    // the next pass's loads go out before this pass's arithmetic
+    const int64_t in = i + kUnroll * step;
+    Block16 nv[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u)
-      if (i + u * step < nblocks) v[u] = load_block(x + (i + u * step) * 16);
+      if (in + u * step < nblocks) nv[u] = load_block(x + (in + u * step) * 16);
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       const int64_t b = i + u * step;
@@ -86,6 +93,8 @@ __global__ void __launch_bounds__(256) fake_quant_flat_kernel(
                           scales != nullptr ? scales + b : nullptr,
                           codes != nullptr ? codes + b * 8 : nullptr);
     }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) v[u] = nv[u];
   }
 }
 
