@@ -276,3 +276,52 @@ def test_forward_and_backward_ptilde_agree(case):
         cb, okb = grid_index(pt_b[idx] / s)
         assert bool(okf.all()) and bool(okb.all()), (pt_f[idx], pt_b[idx], s)
         assert bool(((cf - cb).abs() == 1).all()), (cf, cb)
+
+
+@pytest.mark.parametrize("case", PT_CASES, ids=lambda c: "x".join(map(str, c[:4])))
+def test_auxiliary_output_forward_ptilde_agrees(case):
+    """The auxiliary-output forward ("use_high_prec_o") forms pass 2's S from 64-key FP4
+    UMMAs (its half tiles) and the dense forward from 128-key ones: the row maxima must
+    be the same bits, and the P~ that its o applies must be the dense forward's and the
+    oracle's up to the same bounded, one-E2M1-step differences (l may differ in the
+    last bits: its fp32 sums run in another order)."""
+    b, n, h, d, causal, seed, scale = case
+    inp = workloads.attn_inputs(b, n, n, h, d, seed, scale=scale, causal=causal)
+    q, k = inp.q.cuda(), inp.k.cuda()
+    pf, stats = forward_ptilde(q, k, inp.scale, causal)
+    ph = torch.zeros_like(pf)
+    stats_h = None
+    for t in range(-(-n // d)):
+        v, rows = _onehot(b, n, h, d, t)
+        o, _, st = api.attn_qat_fwd_hp(q, k, v, inp.scale, causal)
+        if stats_h is None:
+            stats_h = st
+        assert torch.equal(st, stats_h)  # the statistics do not depend on V
+        ph[:, :, :, rows] = o[:, :, :, :len(rows)].permute(0, 2, 1, 3).cpu().double() / C_ONEHOT
+    assert api.device_status() == 0
+    assert torch.equal(stats_h[:, :, 1], stats[:, :, 1])  # m
+    st_f, st_h = stats.cpu().double(), stats_h.cpu().double()
+    pt_f = pf * torch.exp(st_f[:, :, 0] - st_f[:, :, 1])[..., None]
+    pt_h = ph * torch.exp(st_h[:, :, 0] - st_h[:, :, 1])[..., None]
+
+    pt_o = torch.zeros_like(pf)
+    s_o = torch.zeros(b, h, n, -(-n // 16), dtype=torch.float64)
+    for bb in range(b):
+        for hh in range(h):
+            hp = oa.HeadProblem(inp.q, inp.k, inp.v, bb, hh, inp.scale, causal)
+            _, _, _, pt, sb = hp.probs_rows(torch.arange(n))
+            pt_o[bb, hh] = pt
+            s_o[bb, hh] = onv.E4M3_VALUES[sb.long()]
+    d_fh = differ(pt_f, pt_h)
+    d_ho = differ(pt_h, pt_o)
+    total = pf.numel()
+    print(f"P~ elements {total}: dense!=aux {int(d_fh.sum())}, aux!=oracle {int(d_ho.sum())}")
+    assert float(d_fh.sum()) <= MAX_DIFF_FRAC * total
+    assert float(d_ho.sum()) <= MAX_DIFF_FRAC * total
+    idx = d_fh.nonzero(as_tuple=True)
+    if idx[0].numel():
+        s = s_o[idx[0], idx[1], idx[2], idx[3] // 16]
+        cf, okf = grid_index(pt_f[idx] / s)
+        ch, okh = grid_index(pt_h[idx] / s)
+        assert bool(okf.all()) and bool(okh.all()), (pt_f[idx], pt_h[idx], s)
+        assert bool(((cf - ch).abs() == 1).all()), (cf, ch)
