@@ -175,3 +175,25 @@ def test_config5_fullsize_sampled_parity():
         dk_ref, dv_ref = hp.dkdv_cols(cols, o_hd, do_hd, block=1024)
         assert rel_l2(dk.cpu()[0, cols, hh], dk_ref) <= G_RTOL
         assert rel_l2(dv.cpu()[0, cols, hh], dv_ref) <= G_RTOL
+
+
+@pytest.mark.parametrize("b,n_tiles,h,d,seed", [(1, 5, 2, 128, 60), (2, 3, 3, 64, 61)])
+def test_full_lists_equal_the_dense_calls(b, n_tiles, h, d, seed):
+    """With every query tile listing all key tiles in order, the block-sparse calls
+    visit the same key tiles in the same order as the dense ones, through the same
+    kernels' block-sparse instances: o, stats, dq, dk and dv must be the same bits."""
+    n = 128 * n_tiles
+    inp = workloads.attn_inputs(b, n, n, h, d, seed)
+    q, k, v, do = (t.cuda() for t in (inp.q, inp.k, inp.v, inp.do))
+    tiles = torch.arange(n_tiles, dtype=torch.int32, device="cuda")
+    kv = tiles.expand(b, h, n_tiles, n_tiles).contiguous()
+    o_s, st_s = api.attn_qat_fwd_sparse(q, k, v, kv, inp.scale)
+    o_d, st_d = api.attn_qat_fwd(q, k, v, inp.scale, False)
+    assert api.device_status() == 0
+    assert torch.equal(o_s, o_d)
+    assert torch.equal(st_s, st_d)
+    g_s = api.attn_qat_bwd_sparse(q, k, v, o_s, st_s, do, kv, inp.scale)
+    g_d = api.attn_qat_bwd(q, k, v, o_d, st_d, do, inp.scale, False)
+    assert api.device_status() == 0
+    for name, x, y in zip(("dq", "dk", "dv"), g_s, g_d):
+        assert torch.equal(x, y), name
